@@ -1,0 +1,181 @@
+"""Python binding of libgdn: argument marshalling around the C ABI, nothing else.
+
+Every step of the computation runs in the CUDA kernels behind ``gdn_chunk_fwd``
+and ``gdn_decode``; this module checks tensors, allocates outputs and scratch
+with PyTorch (device memory only), and passes raw pointers plus torch's current
+CUDA stream.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional, Tuple
+
+import torch
+
+from . import _lib
+
+__all__ = ["chunk_gated_delta_rule", "gated_delta_decode", "chunk_workspace_size",
+           "chunk_fwd_path", "GdnError"]
+
+GdnError = _lib.GdnError
+
+_DT = {torch.float32: _lib.GDN_F32, torch.bfloat16: _lib.GDN_BF16}
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, device=None, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.device.type != "cuda":
+        raise ValueError("%s must be a CUDA tensor (got %s)" % (name, t.device))
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError("%s has dtype %s, expected %s" % (name, t.dtype, dtype))
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def _scale(scale) -> float:
+    return float("nan") if scale is None else float(scale)
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def chunk_fwd_path(K: int, V: int, dtype=torch.bfloat16, beta_dtype=None) -> int:
+    """1: fused tcgen05 kernel; 0: fp32 CUDA-core chunk kernels; -1: rejected."""
+    return _lib.load().gdn_chunk_fwd_path(K, V, _DT[dtype], _DT[beta_dtype or dtype])
+
+
+def chunk_workspace_size(B, T, Hqk, Hv, K, V, num_seqs, dtype=torch.bfloat16,
+                         beta_dtype=None) -> int:
+    n = _lib.load().gdn_chunk_fwd_workspace_size(B, T, Hqk, Hv, K, V, num_seqs, _DT[dtype],
+                                                 _DT[beta_dtype or dtype])
+    if n == (1 << 64) - 1:
+        raise ValueError("sizes rejected by gdn_chunk_fwd")
+    return int(n)
+
+
+def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, chunk_size=64, initial_state=None,
+                           output_final_state=False, use_qk_l2norm_in_kernel=False,
+                           cu_seqlens=None, *, state_indices=None, out=None, final_state=None,
+                           workspace=None, dev_status=None,
+                           **kwargs) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Chunkwise gated delta rule forward through ``gdn_chunk_fwd``.
+
+    Signature of torch_chunk_gated_delta_rule ("Megatron-Core API:
+    core.ssm.gated_delta_net.gdn"): q, k [B, T, Hqk, K]; v [B, T, Hv, V];
+    g [B, T, Hv] fp32; beta [B, T, Hv]; scale None -> 1/sqrt(K); chunk_size 64;
+    returns ``(o, final_state or None)``.  Extra keyword arguments are accepted and
+    ignored, as that function does.
+
+    ``state_indices`` ([N] int32): ``initial_state`` is then a slot cache
+    [num_slots, Hv, K, V]; sequence n starts from slot ``state_indices[n]`` and,
+    with ``output_final_state``, writes its final state back into that slot of
+    ``final_state`` (default: the same cache, updated in place).  Slot -1 marks a
+    padding sequence: zero output, no state access.
+    """
+    _need(q, "q", (torch.float32, torch.bfloat16))
+    dev, dt = q.device, q.dtype
+    if q.dim() != 4:
+        raise ValueError("q must be [B, T, Hqk, K]")
+    B, T, Hqk, K = q.shape
+    _need(k, "k", dt, dev, q.shape)
+    _need(v, "v", dt, dev)
+    if v.dim() != 4 or v.shape[:2] != q.shape[:2]:
+        raise ValueError("v must be [B, T, Hv, V]")
+    Hv, V = v.shape[2], v.shape[3]
+    _need(g, "g", torch.float32, dev, (B, T, Hv))
+    _need(beta, "beta", (dt, torch.float32), dev, (B, T, Hv))
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+        if B != 1:
+            raise ValueError("cu_seqlens requires B == 1")
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    num_slots = 0
+    if state_indices is not None:
+        _need(state_indices, "state_indices", torch.int32, dev, (N,))
+        cache = initial_state if initial_state is not None else final_state
+        if cache is None:
+            raise ValueError("state_indices needs initial_state or final_state (the slot cache)")
+        num_slots = cache.shape[0]
+        st_shape = (num_slots, Hv, K, V)
+        if output_final_state and final_state is None:
+            final_state = initial_state
+    else:
+        st_shape = (N, Hv, K, V)
+    if initial_state is not None:
+        _need(initial_state, "initial_state", torch.float32, dev, st_shape)
+    if output_final_state:
+        if final_state is None:
+            final_state = torch.empty(st_shape, dtype=torch.float32, device=dev)
+        _need(final_state, "final_state", torch.float32, dev, st_shape)
+    else:
+        final_state = None
+    if out is None:
+        out = torch.empty((B, T, Hv, V), dtype=dt, device=dev)
+    _need(out, "out", dt, dev, (B, T, Hv, V))
+    L = _lib.load()
+    bdt = _DT[beta.dtype]
+    need = chunk_workspace_size(B, T, Hqk, Hv, K, V, N, dt, beta.dtype)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32, dev, (1,))
+    st = L.gdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), B, T, Hqk, Hv, K, V,
+                         _DT[dt], bdt, _scale(scale), int(chunk_size), _ptr(initial_state),
+                         int(bool(output_final_state)), _ptr(final_state),
+                         int(bool(use_qk_l2norm_in_kernel)), _ptr(cu_seqlens), N,
+                         _ptr(state_indices), num_slots, _ptr(out), _ptr(workspace), ws_bytes,
+                         _ptr(dev_status), _stream(dev))
+    _lib.check("gdn_chunk_fwd", st)
+    return out, final_state
+
+
+def gated_delta_decode(q, k, v, g, beta, ssm_state, batch_indices=None, scale=None,
+                       use_qk_l2norm_in_kernel=True, *, out=None, dev_status=None) -> torch.Tensor:
+    """One decode token per request through ``gdn_decode``; ``ssm_state`` is updated in place.
+
+    q, k [n, Hqk, K]; v [n, Hv, V]; g [n, Hv] fp32; beta [n, Hv];
+    ssm_state [num_slots, Hv, K, V] fp32; batch_indices [n] int32 (-1 = padding) or
+    None (request i uses slot i).  Returns o [n, Hv, V].
+    """
+    _need(q, "q", (torch.float32, torch.bfloat16))
+    dev, dt = q.device, q.dtype
+    if q.dim() != 3:
+        raise ValueError("q must be [n, Hqk, K]")
+    n, Hqk, K = q.shape
+    _need(k, "k", dt, dev, q.shape)
+    _need(v, "v", dt, dev)
+    if v.dim() != 3 or v.shape[0] != n:
+        raise ValueError("v must be [n, Hv, V]")
+    Hv, V = v.shape[1], v.shape[2]
+    _need(g, "g", torch.float32, dev, (n, Hv))
+    _need(beta, "beta", (dt, torch.float32), dev, (n, Hv))
+    _need(ssm_state, "ssm_state", torch.float32, dev)
+    if ssm_state.dim() != 4 or tuple(ssm_state.shape[1:]) != (Hv, K, V):
+        raise ValueError("ssm_state must be [num_slots, Hv, K, V]")
+    if batch_indices is not None:
+        _need(batch_indices, "batch_indices", torch.int32, dev, (n,))
+    if out is None:
+        out = torch.empty((n, Hv, V), dtype=dt, device=dev)
+    _need(out, "out", dt, dev, (n, Hv, V))
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32, dev, (1,))
+    st = _lib.load().gdn_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(ssm_state),
+                                ssm_state.shape[0], _ptr(batch_indices), n, Hqk, Hv, K, V,
+                                _DT[dt], _DT[beta.dtype], _scale(scale),
+                                int(bool(use_qk_l2norm_in_kernel)), _ptr(out), _ptr(dev_status),
+                                _stream(dev))
+    _lib.check("gdn_decode", st)
+    return out

@@ -1,0 +1,155 @@
+// gdn_api.cu -- the extern "C" boundary of libgdn: argument validation and
+// dispatch to the kernels.  Declarations and the full contract are in gdn.h.
+#include <math.h>
+#include <stdint.h>
+
+#include "gdn.h"
+#include "gdn_internal.h"
+
+namespace {
+
+bool is_dtype(int d) { return d == GDN_F32 || d == GDN_BF16; }
+size_t elem_size(int d) { return d == GDN_BF16 ? 2 : 4; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+float resolve_scale(float scale, int K) {
+  return isnan(scale) ? 1.0f / sqrtf((float)K) : scale;
+}
+
+// Shape / dtype checks shared by the chunk entry point and its size queries.
+gdn_status_t check_chunk_shapes(int B, int T, int Hqk, int Hv, int K, int V, int io_dtype,
+                                int beta_dtype) {
+  if (!is_dtype(io_dtype) || !is_dtype(beta_dtype)) return GDN_ERR_DTYPE;
+  if (beta_dtype != GDN_F32 && beta_dtype != io_dtype) return GDN_ERR_DTYPE;
+  if (B < 0 || T < 0 || Hqk <= 0 || Hv <= 0 || Hv % Hqk != 0) return GDN_ERR_SHAPE;
+  if (K <= 0 || V <= 0 || K > GDN_MAX_HEAD_DIM || V > GDN_MAX_HEAD_DIM) return GDN_ERR_SHAPE;
+  if ((K * elem_size(io_dtype)) % 16 != 0 || (V * elem_size(io_dtype)) % 16 != 0)
+    return GDN_ERR_SHAPE;
+  if ((long long)B * T > 0x7fffffffLL) return GDN_ERR_SHAPE;
+  return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gdn_status_string(gdn_status_t s) {
+  switch (s) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_NULL: return "GDN_ERR_NULL";
+    case GDN_ERR_SHAPE: return "GDN_ERR_SHAPE";
+    case GDN_ERR_DTYPE: return "GDN_ERR_DTYPE";
+    case GDN_ERR_LAYOUT: return "GDN_ERR_LAYOUT";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+    case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE";
+  }
+  return "GDN_ERR_UNKNOWN";
+}
+
+int gdn_version(void) { return 100; }
+
+int gdn_chunk_fwd_path(int K, int V, gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype) {
+  if (check_chunk_shapes(1, 1, 1, 1, K, V, io_dtype, beta_dtype) != GDN_OK) return -1;
+  return gdn::chunk_tc_supported(K, V, io_dtype, beta_dtype) ? 1 : 0;
+}
+
+size_t gdn_chunk_fwd_workspace_size(int B, int T, int Hqk, int Hv, int K, int V, int num_seqs,
+                                    gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype) {
+  if (check_chunk_shapes(B, T, Hqk, Hv, K, V, io_dtype, beta_dtype) != GDN_OK || num_seqs < 0)
+    return (size_t)-1;
+  if (gdn::chunk_tc_supported(K, V, io_dtype, beta_dtype)) return 0;
+  const long long T_total = (long long)B * T;
+  return gdn::chunk_generic_workspace_bytes((int)T_total, num_seqs, Hv, K, V);
+}
+
+gdn_status_t gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                           const void* beta, int B, int T, int Hqk, int Hv, int K, int V,
+                           gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype, float scale,
+                           int chunk_size, const float* initial_state, int output_final_state,
+                           float* final_state, int use_qk_l2norm, const int32_t* cu_seqlens,
+                           int num_seqs, const int32_t* state_indices, int num_slots, void* o,
+                           void* workspace, size_t workspace_bytes, int* dev_status,
+                           void* stream) {
+  gdn_status_t st = check_chunk_shapes(B, T, Hqk, Hv, K, V, io_dtype, beta_dtype);
+  if (st != GDN_OK) return st;
+  if (chunk_size != 64) return GDN_ERR_UNSUPPORTED;
+  if (cu_seqlens) {
+    if (B != 1 || num_seqs < 0) return GDN_ERR_SHAPE;
+  } else {
+    num_seqs = B;
+  }
+  const long long T_total = (long long)B * T;
+  if (T_total > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_NULL;
+  if (output_final_state && !final_state) return GDN_ERR_NULL;
+  if (state_indices) {
+    if (num_slots <= 0) return GDN_ERR_SHAPE;
+  }
+  if (T_total > 0 && (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+                      ((uintptr_t)beta & (elem_size(beta_dtype) - 1)) || ((uintptr_t)g & 3u)))
+    return GDN_ERR_LAYOUT;
+  if ((initial_state && !aligned16(initial_state)) ||
+      (output_final_state && !aligned16(final_state)))
+    return GDN_ERR_LAYOUT;
+  if (num_seqs == 0) return GDN_OK;
+
+  gdn::ChunkArgs a;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
+  a.B = B; a.T = T; a.Hqk = Hqk; a.Hv = Hv; a.K = K; a.V = V;
+  a.io_dtype = io_dtype; a.beta_dtype = beta_dtype;
+  a.scale = resolve_scale(scale, K);
+  a.initial_state = initial_state;
+  a.final_state = output_final_state ? final_state : nullptr;
+  a.use_qk_l2norm = use_qk_l2norm ? 1 : 0;
+  a.cu_seqlens = cu_seqlens;
+  a.num_seqs = num_seqs;
+  a.state_indices = state_indices;
+  a.num_slots = num_slots;
+  a.o = o;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.dev_status = dev_status;
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+
+  cudaError_t err;
+  if (gdn::chunk_tc_supported(K, V, io_dtype, beta_dtype)) {
+    err = gdn::launch_chunk_tc(a);
+  } else {
+    const size_t need = gdn::chunk_generic_workspace_bytes((int)T_total, num_seqs, Hv, K, V);
+    if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return GDN_ERR_LAYOUT;
+    err = gdn::launch_chunk_generic(a);
+  }
+  return err == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status_t gdn_decode(const void* q, const void* k, const void* v, const float* g,
+                        const void* beta, float* ssm_state, int num_slots,
+                        const int32_t* batch_indices, int n, int Hqk, int Hv, int K, int V,
+                        gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype, float scale,
+                        int use_qk_l2norm, void* o, int* dev_status, void* stream) {
+  gdn_status_t st = check_chunk_shapes(1, 1, Hqk, Hv, K, V, io_dtype, beta_dtype);
+  if (st != GDN_OK) return st;
+  if (n < 0 || num_slots < 0) return GDN_ERR_SHAPE;
+  if (!batch_indices && n > num_slots) return GDN_ERR_SHAPE;
+  if (n == 0) return GDN_OK;
+  if (!q || !k || !v || !g || !beta || !o || !ssm_state) return GDN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(ssm_state) ||
+      ((uintptr_t)g & 3u) || ((uintptr_t)beta & (elem_size(beta_dtype) - 1)))
+    return GDN_ERR_LAYOUT;
+  gdn::DecodeArgs a;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
+  a.state = ssm_state;
+  a.num_slots = num_slots;
+  a.batch_indices = batch_indices;
+  a.n = n; a.Hqk = Hqk; a.Hv = Hv; a.K = K; a.V = V;
+  a.io_dtype = io_dtype; a.beta_dtype = beta_dtype;
+  a.scale = resolve_scale(scale, K);
+  a.use_qk_l2norm = use_qk_l2norm ? 1 : 0;
+  a.o = o;
+  a.dev_status = dev_status;
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  return gdn::launch_decode(a) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // extern "C"

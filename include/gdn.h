@@ -1,0 +1,184 @@
+/*
+ * gdn.h -- C ABI of libgdn, the GB300 (sm_103a) gated delta rule library.
+ *
+ * The gated delta rule, per (sequence, value head h) with a K x V fp32 state S:
+ *
+ *     S   <- exp(g_t) * S
+ *     S   <- S + k_t * (beta_t * (v_t - S^T k_t))^T
+ *     o_t  = scale * S^T q_t
+ *
+ * q_t, k_t optionally L2-normalised in-kernel (x / sqrt(sum x^2 + 1e-6)), value
+ * head h reading query/key head h / (Hv / Hqk).  Sources: the GDN mixer and its
+ * torch-native chunked rule on "Megatron-Core API: core.ssm.gated_delta_net.gdn"
+ * (GatedDeltaNet, GatedDeltaNet._compute_gates "per-head log-decay g and the
+ * write strength beta", torch_chunk_gated_delta_rule); the inference contract on
+ * "Megatron-Core API: core.ssm.gated_delta_product" (GatedDeltaProductMixer.
+ * ssm_decode, ssm_prefill, ssm_inference_chunk_size); and the -1 padding rule on
+ * "Add GDN dynamic inference" (Megatron-LM pull request 6499, review thread).
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument named as device memory must be device memory
+ *     allocated by the caller; the library allocates, frees and synchronises
+ *     nothing.  All work is enqueued on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and the call returns before it finishes, so the
+ *     calls can be captured in a CUDA graph (ssm_decode and ssm_prefill on the
+ *     gated_delta_product page require graph-safe steps: no host sync, no
+ *     data-dependent shapes, device-side indices).
+ *   - Argument errors are detected on the host before anything is launched and
+ *     returned as a gdn_status_t; nothing is enqueued then.  A failed launch
+ *     returns GDN_ERR_CUDA.
+ *   - Bad data that only the device can see (a slot outside [-1, num_slots), a
+ *     non-monotone cu_seqlens) is skipped by the kernels, never trapped on, and
+ *     reported by OR-ing GDN_DEV_* bits into *dev_status when dev_status is a
+ *     non-NULL device int.
+ *   - Dense tensors are contiguous, row-major, in the layouts given per
+ *     argument; q, k, v and o must start on 16-byte boundaries (g and beta on their element size).
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_ERR_NULL = 1,        /* a required pointer is NULL                         */
+  GDN_ERR_SHAPE = 2,       /* a size is out of range or sizes disagree           */
+  GDN_ERR_DTYPE = 3,       /* unknown dtype code                                 */
+  GDN_ERR_LAYOUT = 4,      /* a pointer is not aligned as required               */
+  GDN_ERR_UNSUPPORTED = 5, /* well-formed but not provided (e.g. chunk_size 32)  */
+  GDN_ERR_CUDA = 6,        /* a CUDA runtime call or kernel launch failed        */
+  GDN_ERR_WORKSPACE = 7    /* workspace missing or smaller than required         */
+} gdn_status_t;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype_t;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define GDN_DEV_BAD_SLOT 1        /* a slot index >= num_slots or < -1 was skipped */
+#define GDN_DEV_BAD_CU_SEQLENS 2  /* cu_seqlens not monotone / out of [0, T]       */
+#define GDN_DEV_TIMEOUT 4         /* a bounded in-kernel wait gave up (unit skipped) */
+
+/* Largest head dimensions the library accepts (K, V). */
+#define GDN_MAX_HEAD_DIM 128
+
+/*
+ * gdn_chunk_fwd -- chunkwise forward (training / prefill) of the gated delta rule.
+ *
+ * Arguments follow torch_chunk_gated_delta_rule (q, k, v, g, beta, scale,
+ * chunk_size, initial_state, output_final_state, use_qk_l2norm_in_kernel,
+ * cu_seqlens) on "Megatron-Core API: core.ssm.gated_delta_net.gdn"; the packed
+ * layout with cu_seqlens follows GatedDeltaProductMixer._run_gdp_kernel and
+ * ssm_prefill on "Megatron-Core API: core.ssm.gated_delta_product".
+ *
+ *   q, k        [B, T, Hqk, K] io_dtype, device.
+ *   v           [B, T, Hv, V] io_dtype, device.          Hv % Hqk == 0.
+ *   g           [B, T, Hv] fp32 log-decay, device; every value finite.
+ *   beta        [B, T, Hv] beta_dtype, device.
+ *   B, T        batch and tokens per batch row.  With cu_seqlens, B must be 1 and
+ *               T is the packed token count.
+ *   K, V        head dims, 1..GDN_MAX_HEAD_DIM (K * sizeof(io_dtype) and
+ *               V * sizeof(io_dtype) multiples of 16 bytes).
+ *   io_dtype    GDN_F32 or GDN_BF16 (q, k, v, o); beta_dtype GDN_F32 or io_dtype.
+ *   scale       read-out scale; NaN selects the default 1/sqrt(K) (the page's
+ *               "scale defaults to 1 / sqrt(K)").
+ *   chunk_size  must be 64 (the inference kernels "chunk at a fixed 64",
+ *               ssm_inference_chunk_size); anything else: GDN_ERR_UNSUPPORTED.
+ *   initial_state  fp32, device, or NULL (zero state).  Without state_indices:
+ *               [N, Hv, K, V], N = B or num_seqs.  With state_indices: a slot
+ *               cache [num_slots, Hv, K, V].
+ *   output_final_state, final_state  when the flag is set, final_state (fp32,
+ *               device, same shape rule as initial_state) receives the state
+ *               after the last token; it may be the same pointer as
+ *               initial_state (in-place slot update).
+ *   use_qk_l2norm  L2-normalise q and k inside the kernels.
+ *   cu_seqlens  [num_seqs + 1] int32, device, or NULL: sequence n is the packed
+ *               tokens [cu_seqlens[n], cu_seqlens[n+1]); chunks restart at every
+ *               sequence start; empty sequences are allowed and leave their
+ *               state unchanged.
+ *   state_indices  [N] int32, device, or NULL.  Sequence n reads its initial
+ *               state from slot state_indices[n] and writes its final state back
+ *               to that slot ("each request enters carrying whatever state its
+ *               cache slot holds and leaves having written the slot back",
+ *               ssm_prefill).  Slot -1 is padding: the sequence's output rows are
+ *               zero and no state is read or written.  Slots must be distinct.
+ *   num_slots   slots in the cache when state_indices is given.
+ *   o           [B, T, Hv, V] io_dtype, device, written completely.
+ *   workspace, workspace_bytes  device scratch of at least
+ *               gdn_chunk_fwd_workspace_size(...) bytes (may be NULL when that
+ *               size is 0).  Not read before it is written; may be reused once
+ *               the call's work on `stream` has finished.
+ *   dev_status  NULL or a device int receiving GDN_DEV_* bits.
+ *   stream      cudaStream_t.
+ */
+gdn_status_t gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                           const void* beta, int B, int T, int Hqk, int Hv, int K, int V,
+                           gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype, float scale,
+                           int chunk_size, const float* initial_state, int output_final_state,
+                           float* final_state, int use_qk_l2norm, const int32_t* cu_seqlens,
+                           int num_seqs, const int32_t* state_indices, int num_slots, void* o,
+                           void* workspace, size_t workspace_bytes, int* dev_status,
+                           void* stream);
+
+/*
+ * Device scratch (bytes) gdn_chunk_fwd needs for these sizes; 0 when the fused
+ * tensor-core kernel serves them.  num_seqs is N (B when cu_seqlens is NULL).
+ * Returns (size_t)-1 for sizes gdn_chunk_fwd would reject.
+ */
+size_t gdn_chunk_fwd_workspace_size(int B, int T, int Hqk, int Hv, int K, int V, int num_seqs,
+                                    gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype);
+
+/*
+ * Which kernel family gdn_chunk_fwd uses for these sizes: 1 = the fused
+ * tcgen05 / TMEM / TMA kernel (bf16, K = V = 128), 0 = the fp32 CUDA-core
+ * chunk kernels (every other accepted case), -1 = rejected.
+ */
+int gdn_chunk_fwd_path(int K, int V, gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype);
+
+/*
+ * gdn_decode -- one token per request on a slot-indexed state cache, in place.
+ *
+ * Follows GatedDeltaNet.ssm_decode ("one CUDA-graph-compatible GDN decode token
+ * per request", "Megatron-Core API: core.ssm.gated_delta_net.gdn") and
+ * GatedDeltaProductMixer.ssm_decode ("Megatron-Core API:
+ * core.ssm.gated_delta_product": states read and written in place at the slots
+ * named by batch_indices, -1 marks padding whose output is zeroed,
+ * batch_indices=None means the cache is already in request order).  Padding
+ * slots are skipped inside the kernel rather than clamped to slot 0 ("Add GDN
+ * dynamic inference" review thread: writes ignore -1; the Mamba2-style in-kernel
+ * skip writes zeros).
+ *
+ *   q, k        [n, Hqk, K] io_dtype, device.
+ *   v           [n, Hv, V] io_dtype, device.
+ *   g           [n, Hv] fp32, device.      beta [n, Hv] beta_dtype, device.
+ *   ssm_state   [num_slots, Hv, K, V] fp32, device, updated in place.
+ *   batch_indices  [n] int32, device, or NULL (request i uses slot i; then
+ *               n <= num_slots).  -1: output row zero, state untouched.  Slots
+ *               outside [-1, num_slots): skipped like -1 and reported through
+ *               GDN_DEV_BAD_SLOT.  Non-negative slots must be distinct.
+ *   scale       NaN selects 1/sqrt(K).    use_qk_l2norm: normalise q, k.
+ *   o           [n, Hv, V] io_dtype, device.
+ *   dev_status, stream  as above.
+ * Slot selection, padding and untouched slots are exact: a padding row is +0.0
+ * and a slot not named in batch_indices is never accessed.
+ */
+gdn_status_t gdn_decode(const void* q, const void* k, const void* v, const float* g,
+                        const void* beta, float* ssm_state, int num_slots,
+                        const int32_t* batch_indices, int n, int Hqk, int Hv, int K, int V,
+                        gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype, float scale,
+                        int use_qk_l2norm, void* o, int* dev_status, void* stream);
+
+/* Static, NUL-terminated name of a status code ("GDN_OK", ...). */
+const char* gdn_status_string(gdn_status_t status);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

@@ -1,0 +1,103 @@
+"""Helpers for the GPU parity tests: run the fp64 oracle on the same seeded inputs
+the CUDA path receives, optionally on a sample of (sequence, value head) pairs,
+and compare with relative L2 error."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+# Bars from the method's stated tolerances: relative L2 error of o and of the
+# final state against the fp64 oracle.
+TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}
+
+
+def rel_l2(x, ref) -> float:
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = np.linalg.norm(ref)
+    return float(np.linalg.norm(x - ref) / (den if den > 0 else 1.0))
+
+
+def f64(t):
+    return t.detach().cpu().double().numpy()
+
+
+def to_dev(inp, device="cuda"):
+    """Copy every tensor field of a ChunkInputs / DecodeInputs to the device."""
+    out = {}
+    for k, v in vars(inp).items():
+        out[k] = v.to(device) if isinstance(v, torch.Tensor) else v
+    return out
+
+
+def seq_bounds(inp):
+    B, T = inp.q.shape[:2]
+    if inp.cu_seqlens is None:
+        return [(b * T, (b + 1) * T) for b in range(B)]
+    cu = inp.cu_seqlens.tolist()
+    return [(cu[n], cu[n + 1]) for n in range(len(cu) - 1)]
+
+
+def oracle_chunk(inp, pairs=None, nthreads=0):
+    """Oracle (token-by-token recurrence) outputs for a ChunkInputs.
+
+    pairs: None (all) or a list of (sequence n, value head h).  Returns a dict
+    {(n, h): (o [L, V], final [K, V] or None)}; sequences whose slot is -1 are
+    reported as None (padding: zero output, no state).
+    """
+    B, T, Hqk, K = inp.q.shape
+    Hv, V = inp.v.shape[2], inp.v.shape[3]
+    grp = Hv // Hqk
+    flat = lambda x: x.reshape((B * T,) + tuple(x.shape[2:]))
+    q, k, v, g, beta = (flat(x) for x in (inp.q, inp.k, inp.v, inp.g, inp.beta))
+    bounds = seq_bounds(inp)
+    if pairs is None:
+        pairs = [(n, h) for n in range(len(bounds)) for h in range(Hv)]
+    res = {}
+    for n, h in pairs:
+        s, e = bounds[n]
+        slot = n
+        if inp.state_indices is not None:
+            slot = int(inp.state_indices[n])
+            if slot < 0:
+                res[(n, h)] = None
+                continue
+        init = None
+        if inp.initial_state is not None:
+            init = f64(inp.initial_state[slot, h])[None, None]
+        hq = h // grp
+        o, fin = oracle.recurrent(
+            f64(q[s:e, hq:hq + 1])[None], f64(k[s:e, hq:hq + 1])[None],
+            f64(v[s:e, h:h + 1])[None], f64(g[s:e, h:h + 1])[None], f64(beta[s:e, h:h + 1])[None],
+            scale=inp.scale, initial_state=init, use_qk_l2norm_in_kernel=inp.use_qk_l2norm,
+            nthreads=nthreads)
+        res[(n, h)] = (o[0, :, 0], fin[0, 0])
+    return res
+
+
+def compare_chunk(inp, o_gpu, fin_gpu, ref, tol, label=""):
+    """Compare sampled (sequence, head) pairs.  fin_gpu indexed by slot or by sequence.
+    Returns (max rel-L2 of o, max rel-L2 of final state)."""
+    B, T = inp.q.shape[:2]
+    Hv, V = inp.v.shape[2], inp.v.shape[3]
+    o_flat = o_gpu.reshape(B * T, Hv, V)
+    bounds = seq_bounds(inp)
+    worst_o, worst_f = 0.0, 0.0
+    for (n, h), r in ref.items():
+        s, e = bounds[n]
+        og = f64(o_flat[s:e, h])
+        if r is None:   # padding sequence: exact zeros
+            assert np.all(og == 0.0), "%s: padding sequence %d has nonzero output" % (label, n)
+            continue
+        o_ref, f_ref = r
+        if e > s:
+            worst_o = max(worst_o, rel_l2(og, o_ref))
+        if fin_gpu is not None:
+            slot = n if inp.state_indices is None else int(inp.state_indices[n])
+            worst_f = max(worst_f, rel_l2(f64(fin_gpu[slot, h]), f_ref))
+    print("%s: max rel-L2 o=%.3e final=%.3e (tol %.1e)" % (label, worst_o, worst_f, tol))
+    assert worst_o <= tol, "%s: o rel-L2 %.3e > %.1e" % (label, worst_o, tol)
+    assert worst_f <= tol, "%s: final-state rel-L2 %.3e > %.1e" % (label, worst_f, tol)
+    return worst_o, worst_f

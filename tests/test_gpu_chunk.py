@@ -1,0 +1,199 @@
+"""GPU parity of gdn_chunk_fwd against the fp64 oracle: the named workloads (full
+size where the oracle finishes in seconds, sampled (sequence, head) pairs
+otherwise), ragged tails, varlen with empty sequences, slot caches with -1
+padding, grouped heads, options, and run-to-run determinism."""
+import numpy as np
+import pytest
+import torch
+
+from chunked_gated_delta_gdn_gb300 import chunk_fwd_path, chunk_gated_delta_rule, synthetic
+from chunked_gated_delta_gdn_gb300._lib import GDN_DEV_BAD_CU_SEQLENS, GDN_DEV_BAD_SLOT
+from tests.parity import TOL, compare_chunk, f64, oracle_chunk, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu(inp, **extra):
+    d = to_dev(inp)
+    cache = d["initial_state"]
+    kw = dict(scale=inp.scale, initial_state=cache, output_final_state=True,
+              use_qk_l2norm_in_kernel=inp.use_qk_l2norm, cu_seqlens=d["cu_seqlens"],
+              state_indices=d["state_indices"])
+    kw.update(extra)
+    if inp.state_indices is not None:
+        cache = cache.clone()        # updated in place; keep the host copy for the oracle
+        kw["initial_state"] = cache
+    o, fin = chunk_gated_delta_rule(d["q"], d["k"], d["v"], d["g"], d["beta"], **kw)
+    torch.cuda.synchronize()
+    return o, fin
+
+
+def check(inp, label, pairs=None):
+    o, fin = run_gpu(inp)
+    ref = oracle_chunk(inp, pairs)
+    compare_chunk(inp, o, fin, ref, TOL[inp.q.dtype], label)
+    return o, fin
+
+
+# ------------------------------------------------------------------ named workloads
+
+def test_tiny_fp32_full():
+    inp = synthetic.workload("tiny_fp32")
+    check(inp, "tiny_fp32")
+
+
+def test_single_sequence_bf16_full():
+    inp = synthetic.workload("single_seq_bf16")
+    check(inp, "single_seq_bf16")
+
+
+def test_varlen_prefill_slots_full():
+    inp = synthetic.workload("varlen_prefill_bf16")
+    cache_before = inp.initial_state.clone()
+    o, cache = check(inp, "varlen_prefill_bf16")
+    # slots not named by state_indices are byte-identical after the in-place update
+    named = set(inp.state_indices.tolist())
+    rest = [s for s in range(cache.shape[0]) if s not in named]
+    assert torch.equal(cache[rest].cpu(), cache_before[rest])
+
+
+def test_long_context_bf16_sampled():
+    """The full training shape (4 x 32768 tokens, 32 value heads), as launched by the
+    benchmark; the oracle checks 6 sampled (sequence, head) pairs end to end."""
+    inp = synthetic.workload("long_context_bf16")
+    pairs = [(0, 0), (1, 13), (2, 31), (3, 7), (0, 30), (3, 16)]
+    check(inp, "long_context_bf16", pairs)
+
+
+# ------------------------------------------------------------------ edge cases
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 200])
+def test_ragged_lengths(dtype, T):
+    inp = synthetic.chunk_inputs(B=2, T=T, Hqk=2, Hv=4, K=128, V=128, dtype=dtype, init="randn",
+                                 seed=T)
+    check(inp, "ragged %s T=%d" % (dtype, T))
+
+
+@pytest.mark.parametrize("KV", [(64, 64), (128, 64), (64, 128), (32, 32)])
+def test_other_head_dims(KV):
+    K, V = KV
+    for dtype in (torch.float32, torch.bfloat16):
+        inp = synthetic.chunk_inputs(B=1, T=150, Hqk=1, Hv=2, K=K, V=V, dtype=dtype,
+                                     init="randn", seed=K * V)
+        check(inp, "dims %s K=%d V=%d" % (dtype, K, V))
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_varlen_with_empty_and_boundary_lengths(dtype):
+    lengths = [0, 1, 63, 64, 65, 0, 127, 128, 129, 300]
+    inp = synthetic.chunk_inputs(lengths=lengths, Hqk=2, Hv=4, K=128, V=128, dtype=dtype,
+                                 init="randn", seed=11)
+    o, fin = check(inp, "varlen edges %s" % dtype)
+    # empty sequences keep their initial state exactly
+    for n in (0, 5):
+        assert torch.equal(fin[n].cpu(), inp.initial_state[n])
+
+
+def test_slot_padding_sequences():
+    """Slot -1: zero output, no state read or written (zero-length and non-empty)."""
+    lengths = [70, 0, 130, 33]
+    inp = synthetic.chunk_inputs(lengths=lengths, Hqk=1, Hv=2, K=128, V=128,
+                                 dtype=torch.bfloat16, init="slots", num_slots=6, seed=12)
+    inp.state_indices[1] = -1
+    inp.state_indices[3] = -1
+    before = inp.initial_state.clone()
+    o, cache = check(inp, "slot padding")
+    named = set(int(x) for x in inp.state_indices.tolist() if x >= 0)
+    for s in range(6):
+        if s not in named:
+            assert torch.equal(cache[s].cpu(), before[s])
+    cu = inp.cu_seqlens.tolist()
+    assert torch.count_nonzero(o[0, cu[3]:cu[4]].float()).item() == 0
+
+
+def test_bad_slot_and_bad_cu_seqlens_reported():
+    inp = synthetic.chunk_inputs(lengths=[40, 40], Hqk=1, Hv=1, K=128, V=128,
+                                 dtype=torch.bfloat16, init="slots", num_slots=4, seed=13)
+    inp.state_indices[0] = 9
+    d = to_dev(inp)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    chunk_gated_delta_rule(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                           initial_state=d["initial_state"], output_final_state=True,
+                           cu_seqlens=d["cu_seqlens"], state_indices=d["state_indices"],
+                           dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & GDN_DEV_BAD_SLOT
+    bad_cu = torch.tensor([0, 50, 30], dtype=torch.int32, device="cuda")
+    st.zero_()
+    chunk_gated_delta_rule(d["q"], d["k"], d["v"], d["g"], d["beta"], cu_seqlens=bad_cu,
+                           dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & GDN_DEV_BAD_CU_SEQLENS
+
+
+def test_options_no_l2norm_scale_fp32_beta_no_initial_state():
+    inp = synthetic.chunk_inputs(B=1, T=190, Hqk=2, Hv=2, K=128, V=128, dtype=torch.bfloat16,
+                                 init="none", seed=14, use_qk_l2norm=False, scale=0.05,
+                                 beta_dtype=torch.float32)
+    check(inp, "options")
+
+
+def test_grouped_heads_equal_repeated_heads():
+    inp = synthetic.chunk_inputs(B=1, T=130, Hqk=2, Hv=8, K=128, V=128, dtype=torch.bfloat16,
+                                 init="randn", seed=15)
+    o1, f1 = run_gpu(inp)
+    rep = synthetic.ChunkInputs(**{**vars(inp), "q": inp.q.repeat_interleave(4, dim=2),
+                                   "k": inp.k.repeat_interleave(4, dim=2)})
+    o2, f2 = run_gpu(rep)
+    assert torch.equal(o1, o2) and torch.equal(f1, f2)
+
+
+def test_strong_decay_gates():
+    inp = synthetic.chunk_inputs(B=2, T=300, Hqk=2, Hv=4, K=128, V=128, dtype=torch.bfloat16,
+                                 init="randn", gates="mixer", seed=16)
+    assert float(inp.g.min()) < -20
+    check(inp, "mixer gates")
+
+
+def test_deterministic_run_to_run():
+    inp = synthetic.chunk_inputs(lengths=[500, 77, 1000], Hqk=2, Hv=4, K=128, V=128,
+                                 dtype=torch.bfloat16, init="randn", seed=17)
+    o1, f1 = run_gpu(inp)
+    o2, f2 = run_gpu(inp)
+    assert torch.equal(o1, o2) and torch.equal(f1, f2)
+
+
+def test_prefill_then_decode_continuity():
+    """Chunked prefill of a prefix, then gdn_decode of the rest, matches a prefill of
+    the whole sequence (both through the CUDA path)."""
+    from chunked_gated_delta_gdn_gb300 import gated_delta_decode
+    inp = synthetic.chunk_inputs(B=1, T=100, Hqk=2, Hv=4, K=128, V=128, dtype=torch.bfloat16,
+                                 init="randn", seed=18)
+    d = to_dev(inp)
+    o_all, f_all = chunk_gated_delta_rule(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                          initial_state=d["initial_state"],
+                                          output_final_state=True, use_qk_l2norm_in_kernel=True)
+    t = 70
+    o_pre, f_pre = chunk_gated_delta_rule(d["q"][:, :t].contiguous(), d["k"][:, :t].contiguous(),
+                                          d["v"][:, :t].contiguous(), d["g"][:, :t].contiguous(),
+                                          d["beta"][:, :t].contiguous(),
+                                          initial_state=d["initial_state"],
+                                          output_final_state=True, use_qk_l2norm_in_kernel=True)
+    outs = [o_pre[0]]
+    for s in range(t, 100):
+        outs.append(gated_delta_decode(d["q"][0, s:s + 1].contiguous(),
+                                       d["k"][0, s:s + 1].contiguous(),
+                                       d["v"][0, s:s + 1].contiguous(),
+                                       d["g"][0, s:s + 1].contiguous(),
+                                       d["beta"][0, s:s + 1].contiguous(), f_pre, None))
+    o_cat = torch.cat(outs, 0)
+    torch.cuda.synchronize()
+    from tests.parity import rel_l2
+    assert rel_l2(f64(o_cat), f64(o_all[0])) <= 2e-2
+    assert rel_l2(f64(f_pre), f64(f_all)) <= 2e-2
+
+
+def test_path_for_bf16_128_is_tensor_core_when_available():
+    # documents which kernel family served the bf16 K=V=128 cases above
+    print("chunk path for bf16 K=V=128:", chunk_fwd_path(128, 128, torch.bfloat16))

@@ -1,0 +1,116 @@
+"""GPU parity of gdn_decode against the fp64 oracle, plus the exact properties:
+padding rows are +0.0, slots not named are byte-identical, each request's state
+lands in its own slot."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from chunked_gated_delta_gdn_gb300 import gated_delta_decode, synthetic
+from chunked_gated_delta_gdn_gb300._lib import GDN_DEV_BAD_SLOT
+from tests.parity import TOL, f64, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+def run_case(inp, label):
+    dev = "cuda"
+    state_gpu = inp.ssm_state.to(dev)
+    before = state_gpu.clone()
+    idx = None if inp.batch_indices is None else inp.batch_indices.to(dev)
+    o = gated_delta_decode(inp.q.to(dev), inp.k.to(dev), inp.v.to(dev), inp.g.to(dev),
+                           inp.beta.to(dev), state_gpu, idx, scale=inp.scale,
+                           use_qk_l2norm_in_kernel=inp.use_qk_l2norm)
+    torch.cuda.synchronize()
+    cache = f64(inp.ssm_state).copy()
+    o_ref = oracle.decode(inp.q, inp.k, inp.v, inp.g, inp.beta, cache, inp.batch_indices,
+                          scale=inp.scale, use_qk_l2norm_in_kernel=inp.use_qk_l2norm)
+    tol = TOL[inp.q.dtype]
+    n = inp.q.shape[0]
+    slots = list(range(n)) if inp.batch_indices is None else inp.batch_indices.tolist()
+    real = [i for i in range(n) if slots[i] >= 0]
+    pad = [i for i in range(n) if slots[i] < 0]
+    # o on real requests, and the written slots
+    e_o = rel_l2(f64(o[real]), o_ref[real])
+    used = sorted(slots[i] for i in real)
+    e_s = rel_l2(f64(state_gpu[used]), cache[used])
+    print("%s: rel-L2 o=%.3e state=%.3e (tol %.1e)" % (label, e_o, e_s, tol))
+    assert e_o <= tol and e_s <= tol
+    # each request's new state is in its own slot: compare per request
+    for i in real[:: max(1, len(real) // 16)]:
+        assert rel_l2(f64(state_gpu[slots[i]]), cache[slots[i]]) <= tol
+    # padding rows are exactly +0.0 (bit pattern zero)
+    if pad:
+        bits = o[pad].contiguous().view(torch.int16 if o.dtype == torch.bfloat16 else torch.int32)
+        assert torch.count_nonzero(bits).item() == 0
+    # slots not named by any request are byte-identical
+    untouched = sorted(set(range(state_gpu.shape[0])) - set(used))
+    if untouched:
+        assert torch.equal(state_gpu[untouched].view(torch.int32),
+                           before[untouched].view(torch.int32))
+    return o, state_gpu
+
+
+def test_decode_workload_full_size():
+    """256 requests (26 padding) on the 512-slot, 1 GiB fp32 cache, bf16 I/O."""
+    inp = synthetic.workload("decode_bf16")
+    assert int((inp.batch_indices < 0).sum()) == 26
+    run_case(inp, "decode_bf16 full")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("KV", [(128, 128), (64, 64), (64, 128), (32, 16)])
+def test_decode_shapes(dtype, KV):
+    K, V = KV
+    inp = synthetic.decode_inputs(n=37, Hqk=2, Hv=4, K=K, V=V, dtype=dtype, num_slots=50,
+                                  pad_frac=0.2, seed=7 + K + V)
+    run_case(inp, "decode %s K=%d V=%d" % (dtype, K, V))
+
+
+def test_decode_identity_indices_and_options():
+    inp = synthetic.decode_inputs(n=16, Hqk=4, Hv=4, K=128, V=128, dtype=torch.bfloat16,
+                                  num_slots=20, identity=True, seed=3, use_qk_l2norm=False,
+                                  scale=0.37, beta_dtype=torch.float32)
+    run_case(inp, "decode identity/no-l2/fp32-beta")
+
+
+def test_decode_bad_slot_is_skipped_and_reported():
+    inp = synthetic.decode_inputs(n=8, Hqk=1, Hv=2, K=128, V=128, dtype=torch.bfloat16,
+                                  num_slots=10, pad_frac=0.0, seed=5)
+    inp.batch_indices[3] = 10       # == num_slots: out of range
+    inp.batch_indices[5] = -7       # below -1
+    dev = "cuda"
+    state = inp.ssm_state.to(dev)
+    before = state.clone()
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    o = gated_delta_decode(inp.q.to(dev), inp.k.to(dev), inp.v.to(dev), inp.g.to(dev),
+                           inp.beta.to(dev), state, inp.batch_indices.to(dev),
+                           dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & GDN_DEV_BAD_SLOT
+    assert torch.count_nonzero(o[[3, 5]].float()).item() == 0
+    named = set(int(x) for x in inp.batch_indices.tolist() if 0 <= x < 10)
+    for s in range(10):
+        if s not in named:
+            assert torch.equal(state[s], before[s])
+
+
+def test_decode_continues_a_prefill_state():
+    """Decode steps fed from a cached state reproduce the oracle's token-by-token run."""
+    torch.manual_seed(0)
+    n_steps, Hqk, Hv, K, V = 5, 2, 4, 128, 128
+    cache = 0.1 * torch.randn(3, Hv, K, V)
+    dev = "cuda"
+    c_gpu = cache.to(dev)
+    c_ref = f64(cache).copy()
+    idx = torch.tensor([2], dtype=torch.int32)
+    for t in range(n_steps):
+        q = torch.randn(1, Hqk, K).bfloat16(); k = torch.randn(1, Hqk, K).bfloat16()
+        v = torch.randn(1, Hv, V).bfloat16()
+        g = -torch.nn.functional.softplus(torch.randn(1, Hv))
+        b = torch.sigmoid(torch.randn(1, Hv)).bfloat16()
+        o = gated_delta_decode(q.to(dev), k.to(dev), v.to(dev), g.to(dev), b.to(dev), c_gpu,
+                               idx.to(dev))
+        o_ref = oracle.decode(q, k, v, g, b, c_ref, idx)
+        assert rel_l2(f64(o), o_ref) <= TOL[torch.bfloat16]
+    assert rel_l2(f64(c_gpu), c_ref) <= TOL[torch.bfloat16]
