@@ -1,0 +1,342 @@
+#!/usr/bin/env python3
+"""Benchmark of the gated delta rule hot path on one GB300 (or N replicas).
+
+One step = one chunked forward over the long-context training batch
+(B=4, T=32768, Hqk=16, Hv=32, K=V=128, bf16 I/O, fp32 state, chunk 64, q/k L2
+norm, mixer-style gates) followed by one decode step over 256 requests (26 of
+them padding) on a 512-slot fp32 state cache -- every kernel of the path.
+
+Prints one JSON line.  ``value`` is chunked-forward tokens/s (B*T per step over
+the chunked-forward time); the decode half is reported under ``decode``.
+``--impl reference`` times the fp64 CPU oracle instead (the reference arm).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+CHUNK_WL = "long_context_bf16"
+DECODE_WL = "decode_bf16"
+# Algorithmic work per token of the chunked forward (triangles counted once,
+# K K^T / Q K^T per query/key head, the O(C^2) solve and elementwise work left
+# out): Hqk * 2 C K + Hv * (C K + 2 C V + 6 K V).
+C_, K_, V_, HQK_, HV_ = 64, 128, 128, 16, 32
+FLOP_PER_TOKEN = HQK_ * 2 * C_ * K_ + HV_ * (C_ * K_ + 2 * C_ * V_ + 6 * K_ * V_)
+# Minimum HBM bytes per token of a fully fused pass: q, k, v, o in bf16, g fp32, beta bf16.
+BYTES_PER_TOKEN = HQK_ * K_ * 2 * 2 + HV_ * V_ * 2 * 2 + HV_ * 4 + HV_ * 2
+STATE_BYTES = K_ * V_ * 4
+METRIC = "chunked GDN fwd tokens/s + % tensor peak; decode tokens/s + state HBM GB/s"
+WORKLOAD = ("long-context chunked fwd B=4 T=32768 Hqk=16 Hv=32 K=V=128 chunk 64 + decode 256 "
+            "requests (26 padding) on 512 slots")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def traffic_record():
+    """DRAM bytes per launch of the fused chunk kernel from the committed ncu
+    summary, if it was taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "chunk_tc_traffic.json")
+    src = os.path.join(ROOT, "chunked_gated_delta_gdn_gb300", "csrc", "gdn_chunk_tc.cu")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p))
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if rec.get("kernel_source_sha256_16") != h:
+        return None
+    return rec.get("dram_bytes_per_full_launch")
+
+
+def cpu_oracle_sample(inp, tokens, nthreads=0):
+    """Run the fp64 oracle on the first `tokens` tokens of sequence 0 (all heads).
+    Returns (seconds, threads used)."""
+    import oracle
+    sl = slice(0, tokens)
+    args = [x[0:1, sl] for x in (inp.q, inp.k, inp.v, inp.g, inp.beta)]
+    t = time.perf_counter()
+    oracle.recurrent(*args, use_qk_l2norm_in_kernel=True, nthreads=nthreads)
+    dt = time.perf_counter() - t
+    return dt, (nthreads or oracle.max_threads())
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the fp64 CPU oracle on the host cores, as it stands."""
+    if rank != 0:
+        return 0
+    from chunked_gated_delta_gdn_gb300 import synthetic
+    tokens = 1024
+    inp = synthetic.chunk_inputs(B=1, T=tokens, Hqk=16, Hv=32, K=128, V=128, dtype=torch.bfloat16,
+                                 init="none", gates="mixer", seed=1005)
+    for _ in range(args.warmup):
+        cpu_oracle_sample(inp, tokens)
+    times, cores = [], 1
+    for _ in range(args.steps):
+        dt, cores = cpu_oracle_sample(inp, tokens)
+        times.append(dt)
+    tot = sum(times)
+    val = tokens * len(times) / tot
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val,
+        "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000 * tot / len(times), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": 4, "seq_len": 32768,
+                   "reference_sample": "%d tokens x 32 value heads per step (chunked-forward "
+                                       "half only; bf16 inputs read as f64)" % tokens},
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": "first %d tokens of sequence 0, all 32 heads, per step" % tokens},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    if args.warmup < 3:
+        args.warmup = 3
+
+    from chunked_gated_delta_gdn_gb300 import (chunk_gated_delta_rule, chunk_fwd_path,
+                                               gated_delta_decode, synthetic)
+    from chunked_gated_delta_gdn_gb300 import _lib
+    _lib.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    hbm_peak, bf16_peak, peak_src = load_peaks()
+
+    # Inputs: each rank its own independent batch (weak scaling, no collective).
+    cin = synthetic.workload(CHUNK_WL, seed=1005 + 1000 * rank)
+    din = synthetic.workload(DECODE_WL, seed=1004 + 1000 * rank)
+    B, T = cin.q.shape[:2]
+    tokens = B * T
+    host = {k: getattr(cin, k).pin_memory() for k in ("q", "k", "v", "g", "beta")}
+    d = {k: v.to(dev) for k, v in host.items()}
+    dd = {k: getattr(din, k).to(dev) for k in ("q", "k", "v", "g", "beta", "ssm_state",
+                                               "batch_indices")}
+    o = torch.empty_like(d["v"])
+    fin = torch.empty(B, HV_, K_, V_, dtype=torch.float32, device=dev)
+    od = torch.empty_like(dd["v"])
+    n_real = int((din.batch_indices >= 0).sum())
+    stream = torch.cuda.current_stream(dev)
+    path = chunk_fwd_path(K_, V_, torch.bfloat16)
+    launches_per_step = (1 if path == 1 else 4) + 1
+
+    def chunk():
+        chunk_gated_delta_rule(d["q"], d["k"], d["v"], d["g"], d["beta"], output_final_state=True,
+                               use_qk_l2norm_in_kernel=True, out=o, final_state=fin)
+
+    def decode():
+        gated_delta_decode(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dd["ssm_state"],
+                           dd["batch_indices"], out=od)
+
+    for _ in range(args.warmup):
+        chunk()
+        decode()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for e0, e1, e2 in ev:
+            e0.record(stream)
+            chunk()
+            e1.record(stream)
+            decode()
+            e2.record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    total_ms = t_start.elapsed_time(t_end)
+    chunk_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    dec_ms = [b.elapsed_time(c) for _, b, c in ev]
+    total_ms = max_over_ranks(total_ms, world, dev)
+    chunk_sum = max_over_ranks(sum(chunk_ms), world, dev)
+    dec_sum = max_over_ranks(sum(dec_ms), world, dev)
+    K = args.steps
+    value = world * tokens * K / (chunk_sum / 1000.0)
+    chunk_avg_s = chunk_sum / K / 1000.0
+    dec_avg_s = dec_sum / K / 1000.0
+
+    # end to end through the public API: pinned host inputs in, o and the final state out
+    o_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    f_host = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = o_host.numel() * o_host.element_size() + f_host.numel() * f_host.element_size()
+    e2e_steps = max(1, min(K, 5))
+    torch.cuda.synchronize()
+    barrier(world)
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ea.record(stream)
+    for _ in range(e2e_steps):
+        g = {k: v.to(dev, non_blocking=True) for k, v in host.items()}
+        oo, ff = chunk_gated_delta_rule(g["q"], g["k"], g["v"], g["g"], g["beta"],
+                                        output_final_state=True, use_qk_l2norm_in_kernel=True)
+        o_host.copy_(oo, non_blocking=True)
+        f_host.copy_(ff, non_blocking=True)
+    eb.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(ea.elapsed_time(eb), world, dev) / e2e_steps
+    e2e_val = world * tokens / (e2e_ms / 1000.0)
+
+    flops = FLOP_PER_TOKEN * tokens
+    alg_bytes = BYTES_PER_TOKEN * tokens + B * HV_ * STATE_BYTES   # + the final state written
+    achieved_gbs = alg_bytes / chunk_avg_s / 1e9
+    achieved_tf = flops / chunk_avg_s / 1e12
+    traffic = traffic_record()
+    dec_bytes = n_real * HV_ * STATE_BYTES * 2
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": world * B, "seq_len": T, "parallelism": "dp%d" % world,
+                   "l2": "inputs larger than L2 (1.6 GB chunk inputs, 1 GiB state cache); no flush",
+                   "chunk_path": "tcgen05 fused" if path == 1 else "fp32 CUDA-core"},
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved_gbs / hbm_peak, "traffic": traffic,
+                     "peak_source": peak_src, "kernel": "chunk_tc_kernel" if path == 1 else
+                     "chunk kernels"},
+        "tensor": {"achieved": achieved_tf, "peak": bf16_peak, "unit": "TFLOP/s",
+                   "frac": achieved_tf / bf16_peak, "flop_per_token": FLOP_PER_TOKEN,
+                   "peak_source": peak_src},
+        "chunk_ms": chunk_avg_s * 1000.0,
+        "decode": {"ms": dec_avg_s * 1000.0, "requests_per_s": world * n_real / dec_avg_s,
+                   "tokens_per_s_incl_padding": world * din.q.shape[0] / dec_avg_s,
+                   "state_gbs": dec_bytes / dec_avg_s / 1e9,
+                   "hbm_frac": dec_bytes / dec_avg_s / 1e9 / hbm_peak},
+        "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample = 8192
+        dt, cores = cpu_oracle_sample(cin, sample)
+        line["cpu_baseline"] = {"value": sample / dt, "unit": "tokens/s", "cores": cores,
+                                "kind": "oracle",
+                                "sample": "first %d tokens of sequence 0 of the same batch, all "
+                                          "32 value heads (fp64 recurrence)" % sample}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -40,12 +40,13 @@ def seq_bounds(inp):
     return [(cu[n], cu[n + 1]) for n in range(len(cu) - 1)]
 
 
-def oracle_chunk(inp, pairs=None, nthreads=0):
+def oracle_chunk(inp, pairs=None, nthreads=0, batch=256):
     """Oracle (token-by-token recurrence) outputs for a ChunkInputs.
 
     pairs: None (all) or a list of (sequence n, value head h).  Returns a dict
-    {(n, h): (o [L, V], final [K, V] or None)}; sequences whose slot is -1 are
-    reported as None (padding: zero output, no state).
+    {(n, h): (o [L, V], final [K, V])}; sequences whose slot is -1 map to None
+    (padding: zero output, no state).  The requested pairs are packed as
+    independent one-head sequences so one oracle call runs them in parallel.
     """
     B, T, Hqk, K = inp.q.shape
     Hv, V = inp.v.shape[2], inp.v.shape[3]
@@ -56,24 +57,33 @@ def oracle_chunk(inp, pairs=None, nthreads=0):
     if pairs is None:
         pairs = [(n, h) for n in range(len(bounds)) for h in range(Hv)]
     res = {}
+    todo = []
     for n, h in pairs:
-        s, e = bounds[n]
         slot = n
         if inp.state_indices is not None:
             slot = int(inp.state_indices[n])
             if slot < 0:
                 res[(n, h)] = None
                 continue
-        init = None
-        if inp.initial_state is not None:
-            init = f64(inp.initial_state[slot, h])[None, None]
-        hq = h // grp
-        o, fin = oracle.recurrent(
-            f64(q[s:e, hq:hq + 1])[None], f64(k[s:e, hq:hq + 1])[None],
-            f64(v[s:e, h:h + 1])[None], f64(g[s:e, h:h + 1])[None], f64(beta[s:e, h:h + 1])[None],
-            scale=inp.scale, initial_state=init, use_qk_l2norm_in_kernel=inp.use_qk_l2norm,
-            nthreads=nthreads)
-        res[(n, h)] = (o[0, :, 0], fin[0, 0])
+        todo.append((n, h, slot))
+    for i0 in range(0, len(todo), batch):
+        part = todo[i0:i0 + batch]
+        qs, ks, vs, gs, bs, inits, cu = [], [], [], [], [], [], [0]
+        for n, h, slot in part:
+            s, e = bounds[n]
+            hq = h // grp
+            qs.append(q[s:e, hq:hq + 1]); ks.append(k[s:e, hq:hq + 1])
+            vs.append(v[s:e, h:h + 1]); gs.append(g[s:e, h:h + 1]); bs.append(beta[s:e, h:h + 1])
+            if inp.initial_state is not None:
+                inits.append(f64(inp.initial_state[slot, h])[None])
+            cu.append(cu[-1] + (e - s))
+        cat = lambda xs: f64(torch.cat(xs, 0))[None]
+        init = np.stack(inits, 0) if inits else None
+        o, fin = oracle.recurrent(cat(qs), cat(ks), cat(vs), cat(gs), cat(bs), scale=inp.scale,
+                                  initial_state=init, use_qk_l2norm_in_kernel=inp.use_qk_l2norm,
+                                  cu_seqlens=np.array(cu), nthreads=nthreads)
+        for j, (n, h, slot) in enumerate(part):
+            res[(n, h)] = (o[0, cu[j]:cu[j + 1], 0], fin[j, 0])
     return res
 
 
