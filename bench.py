@@ -197,6 +197,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override B of the chunked workload (profiling runs on a smaller case)")
+    ap.add_argument("--only", choices=["chunk", "decode"], default=None,
+                    help="time one half of the step (profiling); the JSON line stays the same")
     args = ap.parse_args()
     world, rank, local = dist_env()
     if world > 1:
@@ -216,7 +220,8 @@ def main():
     hbm_peak, bf16_peak, peak_src = load_peaks()
 
     # Inputs: each rank its own independent batch (weak scaling, no collective).
-    cin = synthetic.workload(CHUNK_WL, seed=1005 + 1000 * rank)
+    over = {} if args.batch is None else {"B": args.batch}
+    cin = synthetic.workload(CHUNK_WL, seed=1005 + 1000 * rank, **over)
     din = synthetic.workload(DECODE_WL, seed=1004 + 1000 * rank)
     B, T = cin.q.shape[:2]
     tokens = B * T
@@ -233,10 +238,14 @@ def main():
     launches_per_step = (1 if path == 1 else 4) + 1
 
     def chunk():
+        if args.only == "decode":
+            return
         chunk_gated_delta_rule(d["q"], d["k"], d["v"], d["g"], d["beta"], output_final_state=True,
                                use_qk_l2norm_in_kernel=True, out=o, final_state=fin)
 
     def decode():
+        if args.only == "chunk":
+            return
         gated_delta_decode(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dd["ssm_state"],
                            dd["batch_indices"], out=od)
 
@@ -268,30 +277,32 @@ def main():
     chunk_sum = max_over_ranks(sum(chunk_ms), world, dev)
     dec_sum = max_over_ranks(sum(dec_ms), world, dev)
     K = args.steps
-    value = world * tokens * K / (chunk_sum / 1000.0)
-    chunk_avg_s = chunk_sum / K / 1000.0
-    dec_avg_s = dec_sum / K / 1000.0
+    chunk_avg_s = max(chunk_sum, 1e-6) / K / 1000.0
+    dec_avg_s = max(dec_sum, 1e-6) / K / 1000.0
+    value = world * tokens / chunk_avg_s
 
     # end to end through the public API: pinned host inputs in, o and the final state out
     o_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
     f_host = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = o_host.numel() * o_host.element_size() + f_host.numel() * f_host.element_size()
-    e2e_steps = max(1, min(K, 5))
-    torch.cuda.synchronize()
-    barrier(world)
-    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ea.record(stream)
-    for _ in range(e2e_steps):
-        g = {k: v.to(dev, non_blocking=True) for k, v in host.items()}
-        oo, ff = chunk_gated_delta_rule(g["q"], g["k"], g["v"], g["g"], g["beta"],
-                                        output_final_state=True, use_qk_l2norm_in_kernel=True)
-        o_host.copy_(oo, non_blocking=True)
-        f_host.copy_(ff, non_blocking=True)
-    eb.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(ea.elapsed_time(eb), world, dev) / e2e_steps
-    e2e_val = world * tokens / (e2e_ms / 1000.0)
+    e2e_val = None
+    if args.only is None:
+        e2e_steps = max(1, min(K, 5))
+        torch.cuda.synchronize()
+        barrier(world)
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record(stream)
+        for _ in range(e2e_steps):
+            g = {k: v.to(dev, non_blocking=True) for k, v in host.items()}
+            oo, ff = chunk_gated_delta_rule(g["q"], g["k"], g["v"], g["g"], g["beta"],
+                                            output_final_state=True, use_qk_l2norm_in_kernel=True)
+            o_host.copy_(oo, non_blocking=True)
+            f_host.copy_(ff, non_blocking=True)
+        eb.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(ea.elapsed_time(eb), world, dev) / e2e_steps
+        e2e_val = world * tokens / (e2e_ms / 1000.0)
 
     flops = FLOP_PER_TOKEN * tokens
     alg_bytes = BYTES_PER_TOKEN * tokens + B * HV_ * STATE_BYTES   # + the final state written

@@ -55,24 +55,29 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def load_library(path: str) -> ctypes.CDLL:
+    """Open an oracle shared library built from gdn_oracle.c and declare its entry points."""
+    lib = ctypes.CDLL(path)
+    dp = ctypes.POINTER(ctypes.c_double)
+    lp = ctypes.POINTER(ctypes.c_int64)
+    i, d = ctypes.c_int, ctypes.c_double
+    lib.gdn_oracle_recurrent.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, lp, i, d, i,
+                                         dp, dp, dp, i]
+    lib.gdn_oracle_chunked.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, lp, i, d, i, i,
+                                       dp, dp, dp, i]
+    lib.gdn_oracle_decode.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, dp, i, lp, d, i,
+                                      dp, i]
+    for f in (lib.gdn_oracle_recurrent, lib.gdn_oracle_chunked, lib.gdn_oracle_decode):
+        f.restype = ctypes.c_int
+    lib.gdn_oracle_max_threads.restype = ctypes.c_int
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            dp = ctypes.POINTER(ctypes.c_double)
-            lp = ctypes.POINTER(ctypes.c_int64)
-            i, d = ctypes.c_int, ctypes.c_double
-            lib.gdn_oracle_recurrent.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, lp, i, d, i,
-                                                 dp, dp, dp, i]
-            lib.gdn_oracle_chunked.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, lp, i, d, i, i,
-                                               dp, dp, dp, i]
-            lib.gdn_oracle_decode.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, dp, i, lp, d, i,
-                                              dp, i]
-            for f in (lib.gdn_oracle_recurrent, lib.gdn_oracle_chunked, lib.gdn_oracle_decode):
-                f.restype = ctypes.c_int
-            lib.gdn_oracle_max_threads.restype = ctypes.c_int
-            _lib = lib
+            _lib = load_library(build())
     return _lib
 
 
@@ -132,13 +137,13 @@ def _scale(scale, K):
 
 
 def recurrent(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=True,
-              use_qk_l2norm_in_kernel=False, cu_seqlens=None, nthreads=0):
+              use_qk_l2norm_in_kernel=False, cu_seqlens=None, nthreads=0, lib=None):
     """Token-by-token gated delta rule.  Returns ``(o, final_state | None)`` as float64 numpy."""
     q, k, v, g, beta, cu, init, (B, T, Hqk, Hv, K, V, N) = _prep_seq(
         q, k, v, g, beta, cu_seqlens, initial_state)
-    o = np.zeros((B, T, Hv, V), dtype=np.float64)
+    o = np.full((B, T, Hv, V), np.nan)   # every row a sequence covers is written
     fin = np.zeros((N, Hv, K, V), dtype=np.float64) if output_final_state else None
-    rc = _load().gdn_oracle_recurrent(
+    rc = (lib or _load()).gdn_oracle_recurrent(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), B * T, Hqk, Hv, K, V,
         _ptr(cu, ctypes.c_int64), N, _scale(scale, K), int(bool(use_qk_l2norm_in_kernel)),
         _ptr(init), _ptr(o), _ptr(fin), int(nthreads))
@@ -148,13 +153,14 @@ def recurrent(q, k, v, g, beta, scale=None, initial_state=None, output_final_sta
 
 
 def chunked(q, k, v, g, beta, scale=None, chunk_size=64, initial_state=None,
-            output_final_state=True, use_qk_l2norm_in_kernel=False, cu_seqlens=None, nthreads=0):
+            output_final_state=True, use_qk_l2norm_in_kernel=False, cu_seqlens=None, nthreads=0,
+            lib=None):
     """Chunkwise (WY / UT-transform) evaluation for any ``chunk_size >= 1``."""
     q, k, v, g, beta, cu, init, (B, T, Hqk, Hv, K, V, N) = _prep_seq(
         q, k, v, g, beta, cu_seqlens, initial_state)
-    o = np.zeros((B, T, Hv, V), dtype=np.float64)
+    o = np.full((B, T, Hv, V), np.nan)   # every row a sequence covers is written
     fin = np.zeros((N, Hv, K, V), dtype=np.float64) if output_final_state else None
-    rc = _load().gdn_oracle_chunked(
+    rc = (lib or _load()).gdn_oracle_chunked(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), B * T, Hqk, Hv, K, V,
         _ptr(cu, ctypes.c_int64), N, _scale(scale, K), int(bool(use_qk_l2norm_in_kernel)),
         int(chunk_size), _ptr(init), _ptr(o), _ptr(fin), int(nthreads))
@@ -164,7 +170,7 @@ def chunked(q, k, v, g, beta, scale=None, chunk_size=64, initial_state=None,
 
 
 def decode(q, k, v, g, beta, ssm_state, batch_indices=None, scale=None,
-           use_qk_l2norm_in_kernel=True, nthreads=0, allow_bad_slots=False):
+           use_qk_l2norm_in_kernel=True, nthreads=0, allow_bad_slots=False, lib=None):
     """One token per request.  ``ssm_state`` ([num_slots, Hv, K, V] float64 numpy) is
     updated in place; returns ``o`` [n, Hv, V].  ``-1`` slots give zero rows."""
     q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
@@ -176,8 +182,8 @@ def decode(q, k, v, g, beta, ssm_state, batch_indices=None, scale=None,
     if ssm_state.ndim != 4 or ssm_state.shape[1:] != (Hv, K, V):
         raise ValueError("ssm_state must be [num_slots, Hv, K, V]")
     idx = _i64(batch_indices)
-    o = np.zeros((n, Hv, V), dtype=np.float64)
-    rc = _load().gdn_oracle_decode(
+    o = np.full((n, Hv, V), np.nan)      # every row is written (zeros for padding)
+    rc = (lib or _load()).gdn_oracle_decode(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), n, Hqk, Hv, K, V, _ptr(ssm_state),
         ssm_state.shape[0], _ptr(idx, ctypes.c_int64), _scale(scale, K),
         int(bool(use_qk_l2norm_in_kernel)), _ptr(o), int(nthreads))
