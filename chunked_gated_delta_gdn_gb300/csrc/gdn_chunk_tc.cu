@@ -4,21 +4,21 @@
 // whole chunk pipeline runs on chip: TMA brings each chunk's Q, K, V tiles into
 // 128-byte-swizzled shared memory (double-buffered), every contraction is a
 // tcgen05.mma with its fp32 accumulator in TMEM, the 64 x 64 unit-lower-
-// triangular solve runs in fp32 shared memory, and the K x V fp32 state lives in
-// registers for the whole sequence (each thread owns 64 entries of S^T).  Per
-// chunk (G = in-chunk cumulative log-decay, r_q / r_k = inverse L2 norms):
+// triangular solve runs in fp32 registers, and the K x V fp32 state lives in
+// TMEM for the whole sequence.  Per chunk (G = in-chunk cumulative log-decay,
+// r_q / r_k = inverse L2 norms, S = state entering the chunk):
 //
 //   D1  = [Q; K] K^T                       M=128 N=64  K=128   (Q K^T and K K^T)
 //   O1  = S^T Q^T                          M=128 N=64  K=128
 //   P   = r_q r_k^T * Q K^T * exp(G_i - G_j) * [j <= i]          (bf16, smem)
 //   A   = beta r_k r_k^T * K K^T * exp(G_i - G_j) * [j < i]      (fp32, smem)
-//   T   = (I + A)^{-1}                     blocked forward substitution, fp32
+//   T   = (I + A)^{-1}                     16 x 16 diagonal blocks, then block rows
 //   W^T = K^T (T diag(beta exp(G) r_k))^T  M=128 N=64  K=64
 //   U^T = V^T (T diag(beta))^T             M=128 N=64  K=64
 //   U'^T = U^T - S^T W^T                   M=128 N=64  K=128   (accumulates on U^T)
 //   O2  = U'^T P^T                         M=128 N=64  K=64
-//   dS  = (U' * exp(G_last - G) r_k)^T K   M=128 N=128 K=64
-//   o   = scale (exp(G) r_q * O1 + O2),    S <- exp(G_last) S + dS
+//   S^T <- exp(G_last) S^T + (U' * exp(G_last - G) r_k)^T K     M=128 N=128 K=64
+//   o   = scale (exp(G) r_q * O1 + O2)
 //
 // Every product is oriented so M = 128 (value or key features on the TMEM
 // lanes, tokens on the columns).  These are the chunkwise (WY / UT transform)
@@ -50,28 +50,35 @@ constexpr uint32_t OFF_V = 65536;       // 2 stages x 16 KB: [dv half][64 tokens
 constexpr uint32_t V_STAGE = 16384;
 constexpr uint32_t OFF_S = 98304;       // S^T bf16, A operand: [dk half][128 dv rows][128 B]
 constexpr uint32_t OFF_W = 131072;      // -W^T bf16, MN-major B: [128 dk rows][64 tokens]
-constexpr uint32_t OFF_TW = 147456;     // T diag(beta exp(G) r_k), K-major B [64 i][64 j]
-constexpr uint32_t OFF_TU = 155648;     // T diag(beta)
+constexpr uint32_t OFF_TW = 147456;     // (T diag(beta exp(G) r_k))^T, MN-major B: [64 j][64 i]
+constexpr uint32_t OFF_TU = 155648;     // (T diag(beta))^T, MN-major B
 constexpr uint32_t OFF_P = 163840;      // P, K-major B [64 i][64 j]
 constexpr uint32_t OFF_U = 172032;      // U'^T bf16, K-major A [128 dv][64 tokens]
 constexpr uint32_t OFF_UT = 188416;     // (U' exp(G_last - G) r_k)^T bf16
-constexpr uint32_t OFF_A = OFF_U;       // fp32 A [64][64]  (aliases U'^T: used earlier in the chunk)
-constexpr uint32_t OFF_T = OFF_UT;      // fp32 T [64][64]  (aliases the scaled U'^T)
-constexpr uint32_t OFF_VEC = 204800;    // per-token fp32 vectors, solve scratch, barriers
+constexpr uint32_t OFF_A = OFF_U;       // fp32 A [64][64], 16-byte-group swizzled (aliases U'^T,
+                                        // which is written later in the chunk)
+constexpr uint32_t OFF_VEC = 204800;    // per-token fp32 vectors, T diagonal blocks, barriers
 constexpr uint32_t VEC_G = 0, VEC_BETA = 64, VEC_RQ = 128, VEC_RK = 192, VEC_SW = 256,
-                   VEC_DL = 320, VEC_QS = 384, VEC_R = 448;   // floats; R is [16][48]
-constexpr uint32_t OFF_BAR = OFF_VEC + 4 * (448 + 16 * 48);  // 8-byte aligned
+                   VEC_DL = 320, VEC_QS = 384, VEC_TD = 448;   // floats; TD is [4][16][16]
+constexpr uint32_t OFF_BAR = OFF_VEC + 4 * (448 + 4 * 256);    // 8-byte aligned
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base
 
-constexpr uint32_t STAGE_TX = 2 * QK_STAGE / 2 + V_STAGE;  // Q + K + V bytes per stage = 48 KB
+constexpr uint32_t STAGE_TX = QK_STAGE + V_STAGE;  // Q + K + V bytes per stage = 48 KB
 
-// TMEM columns (fp32, 128 lanes).
+// TMEM columns (fp32, 128 lanes).  COL_S holds S^T for the whole sequence.
 constexpr uint32_t COL_D1 = 0, COL_W = 64, COL_U = 128, COL_O1 = 192, COL_O2 = 256,
                    COL_S = 320, TMEM_COLS = 512;
 
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(STAGE_TX == 49152, "stage bytes");
+
+// fp32 A tile: element (i, j) at i * 64 + 4 * ((j / 4) ^ (i % 16)) + j % 4, so that
+// 16-byte groups stay contiguous and the row-parallel accesses of the solve hit
+// distinct banks.
+__device__ __forceinline__ int a_idx(int i, int j) {
+  return i * 64 + ((((j >> 2) ^ (i & 15)) << 2) | (j & 3));
+}
 
 __device__ __forceinline__ void store_bf16x8(uint8_t* p, const float* v) {
   __nv_bfloat162 b0 = __floats2bfloat162_rn(v[0], v[1]);
@@ -97,7 +104,7 @@ __device__ __forceinline__ float sumsq_bf16x8(uint4 u) {
   return s;
 }
 
-// Issue the TMA loads of chunk starting at token t into stage s.
+// Issue the TMA loads of the chunk starting at token t into stage s.
 __device__ __forceinline__ void issue_chunk_loads(uint8_t* sm, uint64_t* bar, const CUtensorMap* tq,
                                                   const CUtensorMap* tk, const CUtensorMap* tv,
                                                   int s, int t, int hq, int h) {
@@ -109,6 +116,20 @@ __device__ __forceinline__ void issue_chunk_loads(uint8_t* sm, uint64_t* bar, co
     tma_load_3d(qk + hh * 16384, tq, bar, 64 * hh, hq, t);
     tma_load_3d(qk + hh * 16384 + 8192, tk, bar, 64 * hh, hq, t);
     tma_load_3d(vv + hh * 8192, tv, bar, 64 * hh, h, t);
+  }
+}
+
+// g and beta of tokens t0 + lane and t0 + lane + 32 (zero past the chunk end).
+__device__ __forceinline__ void load_gates(const ChunkArgs& a, int t0, int L, int h, int lane,
+                                           float* g, float* b) {
+  g[0] = g[1] = b[0] = b[1] = 0.f;
+  if (lane < L) {
+    g[0] = a.g[(size_t)(t0 + lane) * a.Hv + h];
+    b[0] = load_elem(a.beta, (size_t)(t0 + lane) * a.Hv + h, a.beta_dtype);
+  }
+  if (lane + 32 < L) {
+    g[1] = a.g[(size_t)(t0 + lane + 32) * a.Hv + h];
+    b[1] = load_elem(a.beta, (size_t)(t0 + lane + 32) * a.Hv + h, a.beta_dtype);
   }
 }
 
@@ -126,9 +147,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   float* sSw = vec + VEC_SW;
   float* sDl = vec + VEC_DL;
   float* sQs = vec + VEC_QS;
-  float* sR = vec + VEC_R;
+  float* sTd = vec + VEC_TD;   // diagonal 16 x 16 blocks of T: [block][row][col]
   float* sA = reinterpret_cast<float*>(sm + OFF_A);
-  float* sT = reinterpret_cast<float*>(sm + OFF_T);
   uint64_t* bar_full = reinterpret_cast<uint64_t*>(sm + OFF_BAR);  // [2]
   uint64_t* bar_mma = bar_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_full + 3);
@@ -157,26 +177,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       return;
     }
   }
-  // This thread's TMEM lane (a value / key feature index) and column half.
+  // This thread's TMEM lane (a value or key feature index) and column half.
   const int quad = warp & 3, chalf = warp >> 2;
   const int row = 32 * quad + lane;
   const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
-
-  // State S^T[row][64 chalf + j] = S[64 chalf + j][row], fp32, in registers.
-  float S[64];
   const size_t st_off = ((size_t)slot * a.Hv + h) * (size_t)(DK * DV);
-  if (a.initial_state) {
-#pragma unroll
-    for (int j = 0; j < 64; ++j) S[j] = a.initial_state[st_off + (size_t)(64 * chalf + j) * DV + row];
-  } else {
-#pragma unroll
-    for (int j = 0; j < 64; ++j) S[j] = 0.f;
-  }
   const int nchunks = (eos - bos + kChunk - 1) / kChunk;
-  if (nchunks == 0) {
+  if (nchunks == 0) {   // empty sequence: the state passes through unchanged
     if (a.final_state) {
-#pragma unroll
-      for (int j = 0; j < 64; ++j) a.final_state[st_off + (size_t)(64 * chalf + j) * DV + row] = S[j];
+      for (int j = 0; j < 64; ++j) {
+        const size_t e = st_off + (size_t)(64 * chalf + j) * DV + row;
+        a.final_state[e] = a.initial_state ? a.initial_state[e] : 0.f;
+      }
     }
     return;
   }
@@ -202,6 +214,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     issue_chunk_loads(sm, &bar_full[0], &tmQ, &tmK, &tmV, 0, bos, hq, h);
     if (nchunks > 1) issue_chunk_loads(sm, &bar_full[1], &tmQ, &tmK, &tmV, 1, bos + kChunk, hq, h);
   }
+  // Initial state -> TMEM (S^T: lane = value index, columns = key index).
+  {
+    float x[32];
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      const int k0 = 64 * chalf + 32 * part;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        x[j] = a.initial_state ? a.initial_state[st_off + (size_t)(k0 + j) * DV + row] : 0.f;
+      tmem_st32(tbase + lane_off + COL_S + k0, x);
+    }
+  }
+  // gates of chunk 0 (warp 0), later prefetched one chunk ahead
+  float gq[2], bq[2];
+  if (warp == 0) load_gates(a, bos, min(kChunk, eos - bos), h, lane, gq, bq);
+
   const uint32_t sbase = smem_u32(sm);
   uint32_t mma_parity = 0;
   int issued = nchunks > 1 ? 2 : 1;  // chunks whose loads have been issued
@@ -223,17 +251,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t qk_a = sbase + OFF_QK + s * QK_STAGE;
     const uint32_t v_a = sbase + OFF_V + s * V_STAGE;
 
-    // ---- gates: in-chunk cumulative log-decay and beta (zero past the chunk end)
+    // ---- gates: in-chunk cumulative log-decay and beta; prefetch the next chunk's
     if (warp == 0) {
-      float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
-      if (lane < L) {
-        g0 = a.g[(size_t)(t0 + lane) * a.Hv + h];
-        b0 = load_elem(a.beta, (size_t)(t0 + lane) * a.Hv + h, a.beta_dtype);
-      }
-      if (lane + 32 < L) {
-        g1 = a.g[(size_t)(t0 + lane + 32) * a.Hv + h];
-        b1 = load_elem(a.beta, (size_t)(t0 + lane + 32) * a.Hv + h, a.beta_dtype);
-      }
+      float g0 = gq[0], g1 = gq[1];
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const float x0 = __shfl_up_sync(0xffffffffu, g0, o);
@@ -242,18 +262,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       g1 += __shfl_sync(0xffffffffu, g0, 31);
       sG[lane] = g0; sG[lane + 32] = g1;
-      sBeta[lane] = b0; sBeta[lane + 32] = b1;
-    }
-    // ---- S (entry state of this chunk) -> bf16 A operand S^T [dv rows][dk]
-    {
-      uint8_t* dst = sm + OFF_S + chalf * 16384;
-#pragma unroll
-      for (int m = 0; m < 8; ++m) store_bf16x8(dst + sw128_offset(row, 8 * m), &S[8 * m]);
+      sBeta[lane] = bq[0]; sBeta[lane + 32] = bq[1];
+      if (c + 1 < nchunks) load_gates(a, t0 + kChunk, min(kChunk, eos - t0 - kChunk), h, lane, gq, bq);
     }
     // ---- this chunk's Q, K, V tiles
     {
       const bool ok = mbar_wait(&bar_full[s], (uint32_t)(c >> 1) & 1u, kWaitLimitNs);
       if (__syncthreads_or(!ok)) { failed = true; break; }
+    }
+    // ---- S (entry state) -> bf16 A operand S^T [dv rows][dk]; S <- exp(G_last) S in TMEM
+    {
+      const float dl = __expf(sG[L - 1]);
+      uint8_t* dst = sm + OFF_S + chalf * 16384;
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        float x[32];
+        const uint32_t col = COL_S + 64 * chalf + 32 * part;
+        tmem_ld32(tbase + lane_off + col, x);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) store_bf16x8(dst + sw128_offset(row, 32 * part + 8 * m), &x[8 * m]);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] *= dl;
+        tmem_st32(tbase + lane_off + col, x);
+      }
     }
     // ---- inverse L2 norms of the chunk's q and k rows (4 threads per row)
     {
@@ -275,6 +306,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
     fence_proxy_async_smem();
+    tc_fence_before();
     __syncthreads();
 
     // ---- MMA: D1 = [Q;K] K^T, O1 = S^T Q^T
@@ -299,9 +331,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (tid < kChunk) {
       const float gl = sG[L - 1];
       const float gt = sG[tid];
-      const float et = expf(gt);
+      const float et = __expf(gt);
       sSw[tid] = sBeta[tid] * et * sRk[tid];
-      sDl[tid] = expf(gl - gt) * sRk[tid];
+      sDl[tid] = __expf(gl - gt) * sRk[tid];
       sQs[tid] = a.scale * et * sRq[tid];
     }
     if (!wait_mma()) { failed = true; break; }
@@ -314,11 +346,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int j0 = 32 * chalf;
       if (quad < 2) {
         const int i = row;
-        const float gi = sG[i], ri = sRq[i];
+        const float gi = sG[i], ri = (i < L) ? sRq[i] : 0.f;
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
           const int j = j0 + jj;
-          x[jj] = (j <= i && i < L) ? ri * sRk[j] * x[jj] * expf(gi - sG[j]) : 0.f;
+          x[jj] = (j <= i) ? ri * sRk[j] * x[jj] * __expf(gi - sG[j]) : 0.f;
         }
         uint8_t* dst = sm + OFF_P;
 #pragma unroll
@@ -329,84 +361,110 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
           const int j = j0 + jj;
-          sA[i * 64 + j] = (j < i) ? bi * sRk[j] * x[jj] * expf(gi - sG[j]) : 0.f;
+          x[jj] = (j < i) ? bi * sRk[j] * x[jj] * __expf(gi - sG[j]) : 0.f;
         }
+#pragma unroll
+        for (int m = 0; m < 8; ++m)
+          *reinterpret_cast<float4*>(&sA[a_idx(i, j0 + 4 * m)]) =
+              make_float4(x[4 * m], x[4 * m + 1], x[4 * m + 2], x[4 * m + 3]);
       }
     }
     tc_fence_before();
     __syncthreads();
 
-    // ---- T = (I + A)^{-1}: 16 x 16 diagonal blocks by forward substitution ...
+    // ---- T = (I + A)^{-1}, step 1: the four 16 x 16 diagonal blocks (one column per thread)
     if (tid < 64) {
       const int b = tid >> 4, jj = tid & 15;
       float x[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) x[i] = (i == jj) ? 1.f : 0.f;
-      const float* Ab = sA + (16 * b) * 64 + 16 * b;
 #pragma unroll
       for (int i = 1; i < 16; ++i) {
-        if (i > jj) {
-          float acc = 0.f;
+        float acc = 0.f;
 #pragma unroll
-          for (int k = 0; k < i; ++k) acc += Ab[i * 64 + k] * x[k];
-          x[i] = -acc;
-        }
+        for (int k = 0; k < i; ++k) acc += sA[a_idx(16 * b + i, 16 * b + k)] * x[k];
+        if (i > jj) x[i] = -acc;
       }
-      float* Tb = sT + (16 * b) * 64 + 16 * b + jj;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) Tb[i * 64] = x[i];
+      for (int i = 0; i < 16; ++i) sTd[(b * 16 + i) * 16 + jj] = x[i];
     }
     __syncthreads();
-    // ... then row block b from the blocks above it: T[b, :16b] = -T_bb A[b, :16b] T[:16b, :16b]
-    for (int b = 1; b < 4; ++b) {
-      const int nb = 16 * b;
-      for (int o = tid; o < 16 * nb; o += kTcThreads) {
-        const int r = o & 15, cc = o >> 4;
-        float acc = 0.f;
-        for (int k = cc; k < nb; ++k) acc += sA[(nb + r) * 64 + k] * sT[k * 64 + cc];
-        sR[r * 48 + cc] = acc;
-      }
-      __syncthreads();
-      for (int o = tid; o < 16 * nb; o += kTcThreads) {
-        const int r = o & 15, cc = o >> 4;
-        float acc = 0.f;
-        for (int m = 0; m <= r; ++m) acc += sT[(nb + r) * 64 + nb + m] * sR[m * 48 + cc];
-        sT[(nb + r) * 64 + cc] = -acc;
-      }
-      __syncthreads();
-    }
-    // ---- T diag(beta exp(G) r_k) and T diag(beta) as bf16 B operands
+    // ---- step 2: each column of T in registers (4 threads per column, replicated);
+    //      block row b from the rows above it: T[b, c] = -T_bb A[b, :16b] T[:16b, c]
     {
-      const int i = tid >> 2, j0 = 16 * (tid & 3);
-      float w[16], u[16];
+      const int col = tid >> 2, q4 = tid & 3;
+      const int bc = col >> 4;                 // warp-uniform (a warp holds 8 columns)
+      float x[64];
 #pragma unroll
-      for (int jj = 0; jj < 16; ++jj) {
-        const int j = j0 + jj;
-        const float tv = (j <= i) ? sT[i * 64 + j] : 0.f;
-        w[jj] = tv * sSw[j];
-        u[jj] = tv * sBeta[j];
+      for (int i = 0; i < 64; ++i) x[i] = 0.f;
+#pragma unroll
+      for (int bb = 0; bb < 4; ++bb) {
+        if (bb == bc) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) x[16 * bb + i] = sTd[(bb * 16 + i) * 16 + (col & 15)];
+        }
       }
-      store_bf16x8(sm + OFF_TW + sw128_offset(i, j0), w);
-      store_bf16x8(sm + OFF_TW + sw128_offset(i, j0 + 8), w + 8);
-      store_bf16x8(sm + OFF_TU + sw128_offset(i, j0), u);
-      store_bf16x8(sm + OFF_TU + sw128_offset(i, j0 + 8), u + 8);
+#pragma unroll
+      for (int b = 1; b < 4; ++b) {
+        if (b > bc) {
+          // y[rr] = sum_k A[16b + r][k] x[k] for this thread's rows r = 4 rr + q4
+          float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int g = 0; g < 4 * b; ++g) {
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+              const int r = 16 * b + 4 * rr + q4;
+              const float4 a4 = *reinterpret_cast<const float4*>(&sA[a_idx(r, 4 * g)]);
+              y[rr] += a4.x * x[4 * g] + a4.y * x[4 * g + 1] + a4.z * x[4 * g + 2] +
+                       a4.w * x[4 * g + 3];
+            }
+          }
+          float ys[16];
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+            for (int src = 0; src < 4; ++src)
+              ys[4 * rr + src] = __shfl_sync(0xffffffffu, y[rr], (lane & ~3) | src);
+#pragma unroll
+          for (int r = 0; r < 16; ++r) {
+            float acc = 0.f;
+#pragma unroll
+            for (int m = 0; m <= r; ++m) acc += sTd[(b * 16 + r) * 16 + m] * ys[m];
+            x[16 * b + r] = -acc;
+          }
+        }
+      }
+      // (T diag(beta exp(G) r_k))^T and (T diag(beta))^T: row `col`, this thread's 16 entries
+      const float sw = sSw[col], sb = sBeta[col];
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) {
+        if (qq == q4) {
+          float w[16], u[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) { w[i] = x[16 * qq + i] * sw; u[i] = x[16 * qq + i] * sb; }
+          store_bf16x8(sm + OFF_TW + sw128_offset(col, 16 * qq), w);
+          store_bf16x8(sm + OFF_TW + sw128_offset(col, 16 * qq + 8), w + 8);
+          store_bf16x8(sm + OFF_TU + sw128_offset(col, 16 * qq), u);
+          store_bf16x8(sm + OFF_TU + sw128_offset(col, 16 * qq + 8), u + 8);
+        }
+      }
     }
     fence_proxy_async_smem();
     __syncthreads();
 
-    // ---- MMA: W^T = K^T Tw^T, U^T = V^T Tu^T   (A operands MN-major from the TMA tiles)
+    // ---- MMA: W^T = K^T Tw^T, U^T = V^T Tu^T   (all operands MN-major)
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t id = idesc_bf16(128, 64, true, false);
+      const uint32_t id = idesc_bf16(128, 64, true, true);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         mma_bf16(tbase + COL_W, sdesc_sw128(qk_a + 8192 + ks * 2048, 16384, 1024),
-                 sdesc_sw128(sbase + OFF_TW + ks * 32, 16, 1024), id, ks > 0);
+                 sdesc_sw128(sbase + OFF_TW + ks * 2048, 8192, 1024), id, ks > 0);
       }
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         mma_bf16(tbase + COL_U, sdesc_sw128(v_a + ks * 2048, 8192, 1024),
-                 sdesc_sw128(sbase + OFF_TU + ks * 32, 16, 1024), id, ks > 0);
+                 sdesc_sw128(sbase + OFF_TU + ks * 2048, 8192, 1024), id, ks > 0);
       }
       mma_commit(bar_mma);
     }
@@ -458,7 +516,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_before();
     __syncthreads();
 
-    // ---- MMA: O2 = U'^T P^T, dS = Ut^T K
+    // ---- MMA: O2 = U'^T P^T, S^T += Ut^T K
     if (tid == 0) {
       tc_fence_after();
       const uint32_t id6 = idesc_bf16(128, 64, false, false);
@@ -471,7 +529,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         mma_bf16(tbase + COL_S, sdesc_sw128(sbase + OFF_UT + ks * 32, 16, 1024),
-                 sdesc_sw128(qk_a + 8192 + ks * 2048, 16384, 1024), id7, ks > 0);
+                 sdesc_sw128(qk_a + 8192 + ks * 2048, 16384, 1024), id7, 1);
       }
       mma_commit(bar_mma);
     }
@@ -485,17 +543,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ++issued;
     }
 
-    // ---- S <- exp(G_last) S + dS ; o = exp(G) r_q scale O1 + scale O2
+    // ---- o = scale (exp(G) r_q O1 + O2)
     {
-      const float dl = expf(sG[L - 1]);
-      float x[32];
-      tmem_ld32(tbase + lane_off + COL_S + 64 * chalf, x);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) S[j] = dl * S[j] + x[j];
-      tmem_ld32(tbase + lane_off + COL_S + 64 * chalf + 32, x);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) S[32 + j] = dl * S[32 + j] + x[j];
-      float y[32];
+      float x[32], y[32];
       tmem_ld32(tbase + lane_off + COL_O1 + 32 * chalf, x);
       tmem_ld32(tbase + lane_off + COL_O2 + 32 * chalf, y);
       __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.o);
@@ -519,9 +569,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_wait(bar_mma, mma_parity ^ 1u, kWaitLimitNs);
     __syncthreads();
   } else if (a.final_state) {
+    tc_fence_after();
 #pragma unroll
-    for (int j = 0; j < 64; ++j) a.final_state[st_off + (size_t)(64 * chalf + j) * DV + row] = S[j];
+    for (int part = 0; part < 2; ++part) {
+      float x[32];
+      const int k0 = 64 * chalf + 32 * part;
+      tmem_ld32(tbase + lane_off + COL_S + k0, x);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) a.final_state[st_off + (size_t)(k0 + j) * DV + row] = x[j];
+    }
   }
+  tc_fence_before();
+  __syncthreads();
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tbase, TMEM_COLS);
 }
