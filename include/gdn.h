@@ -171,6 +171,43 @@ gdn_status_t gdn_decode(const void* q, const void* k, const void* v, const float
                         gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype, float scale,
                         int use_qk_l2norm, void* o, int* dev_status, void* stream);
 
+/*
+ * gdn_chunk_fwd_noalloc -- gdn_chunk_fwd without caller-provided scratch.
+ *
+ * The sources have no counterpart for this entry point; it exists for callers
+ * that cannot allocate device memory: plugins running inside another runtime
+ * whose device memory that runtime has already reserved, C callers without an
+ * allocator of their own, and code that must not call cudaMalloc mid-step
+ * because cudaMalloc can synchronise the device.
+ *
+ * Arguments, layouts and results are those of gdn_chunk_fwd without
+ * `workspace` / `workspace_bytes`: the scratch the CUDA-core chunk kernels need
+ * comes from one static device array of GDN_NOALLOC_SCRATCH_BYTES (64 MiB) that
+ * every GPU loading the library holds until the process exits.  Nothing is
+ * allocated or freed per call.
+ *   - Sizes whose scratch need (gdn_chunk_fwd_workspace_size) exceeds
+ *     GDN_NOALLOC_SCRATCH_BYTES are rejected with GDN_ERR_WORKSPACE before
+ *     anything is launched; other argument errors as in gdn_chunk_fwd.
+ *   - Cases the tensor-core kernel serves (bf16, K = V = 128) need no scratch
+ *     and run exactly as through gdn_chunk_fwd.
+ *   - The first call on a device looks up the array's device address on the
+ *     current device (cudaGetSymbolAddress, once per device); make that first
+ *     call before any stream capture.  `stream` must belong to the current device.
+ *   - Every call on a device shares the one array.  No scratch contents need to
+ *     start at zero (each launch writes everything it later reads), but calls
+ *     whose work overlaps on the GPU (different streams, or concurrent host
+ *     threads) race on it: serialise them.
+ */
+#define GDN_NOALLOC_SCRATCH_BYTES (64u << 20)
+gdn_status_t gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const float* g,
+                                   const void* beta, int B, int T, int Hqk, int Hv, int K, int V,
+                                   gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype, float scale,
+                                   int chunk_size, const float* initial_state,
+                                   int output_final_state, float* final_state, int use_qk_l2norm,
+                                   const int32_t* cu_seqlens, int num_seqs,
+                                   const int32_t* state_indices, int num_slots, void* o,
+                                   int* dev_status, void* stream);
+
 /* Static, NUL-terminated name of a status code ("GDN_OK", ...). */
 const char* gdn_status_string(gdn_status_t status);
 
