@@ -14,8 +14,8 @@ import torch
 
 from . import _lib
 
-__all__ = ["chunk_gated_delta_rule", "gated_delta_decode", "chunk_workspace_size",
-           "chunk_fwd_path", "GdnError"]
+__all__ = ["chunk_gated_delta_rule", "gated_delta_decode", "chunk_gated_delta_rule_fused_gates",
+           "gated_delta_decode_fused_gates", "chunk_workspace_size", "chunk_fwd_path", "GdnError"]
 
 GdnError = _lib.GdnError
 
@@ -178,4 +178,92 @@ def gated_delta_decode(q, k, v, g, beta, ssm_state, batch_indices=None, scale=No
                                 int(bool(use_qk_l2norm_in_kernel)), _ptr(out), _ptr(dev_status),
                                 _stream(dev))
     _lib.check("gdn_decode", st)
+    return out
+
+
+def _gate_args(a, b, A_log, dt_bias, dev, dt, lead_shape, Hv):
+    _need(a, "a", (dt, torch.float32), dev, tuple(lead_shape) + (Hv,))
+    _need(b, "b", a.dtype, dev, tuple(lead_shape) + (Hv,))
+    _need(A_log, "A_log", torch.float32, dev, (Hv,))
+    _need(dt_bias, "dt_bias", torch.float32, dev, (Hv,))
+    return _DT[a.dtype]
+
+
+def chunk_gated_delta_rule_fused_gates(q, k, v, a, b, A_log, dt_bias, scale=None, chunk_size=64,
+                                       initial_state=None, output_final_state=False,
+                                       use_qk_l2norm_in_kernel=False, cu_seqlens=None, *,
+                                       state_indices=None, out=None, final_state=None,
+                                       workspace=None, dev_status=None, **kwargs):
+    """Chunked forward with the gates computed in the kernels (``gdn_chunk_fwd_gated``):
+    g = -exp(A_log) * softplus(a + dt_bias), beta = sigmoid(b), with a, b [B, T, Hv]
+    and A_log, dt_bias [Hv] fp32.  Everything else as :func:`chunk_gated_delta_rule`."""
+    _need(q, "q", (torch.float32, torch.bfloat16))
+    dev, dt = q.device, q.dtype
+    if q.dim() != 4 or v.dim() != 4:
+        raise ValueError("q must be [B, T, Hqk, K] and v [B, T, Hv, V]")
+    B, T, Hqk, K = q.shape
+    Hv, V = v.shape[2], v.shape[3]
+    _need(k, "k", dt, dev, q.shape)
+    _need(v, "v", dt, dev)
+    ab_dt = _gate_args(a, b, A_log, dt_bias, dev, dt, (B, T), Hv)
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    num_slots = 0
+    if state_indices is not None:
+        _need(state_indices, "state_indices", torch.int32, dev, (N,))
+        cache = initial_state if initial_state is not None else final_state
+        num_slots = cache.shape[0]
+        st_shape = (num_slots, Hv, K, V)
+        if output_final_state and final_state is None:
+            final_state = initial_state
+    else:
+        st_shape = (N, Hv, K, V)
+    if initial_state is not None:
+        _need(initial_state, "initial_state", torch.float32, dev, st_shape)
+    if output_final_state:
+        if final_state is None:
+            final_state = torch.empty(st_shape, dtype=torch.float32, device=dev)
+        _need(final_state, "final_state", torch.float32, dev, st_shape)
+    else:
+        final_state = None
+    if out is None:
+        out = torch.empty((B, T, Hv, V), dtype=dt, device=dev)
+    _need(out, "out", dt, dev, (B, T, Hv, V))
+    need = chunk_workspace_size(B, T, Hqk, Hv, K, V, N, dt, dt)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _lib.load().gdn_chunk_fwd_gated(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), ab_dt, _ptr(A_log), _ptr(dt_bias), B, T,
+        Hqk, Hv, K, V, _DT[dt], _scale(scale), int(chunk_size), _ptr(initial_state),
+        int(bool(output_final_state)), _ptr(final_state), int(bool(use_qk_l2norm_in_kernel)),
+        _ptr(cu_seqlens), N, _ptr(state_indices), num_slots, _ptr(out), _ptr(workspace), ws_bytes,
+        _ptr(dev_status), _stream(dev))
+    _lib.check("gdn_chunk_fwd_gated", st)
+    return out, final_state
+
+
+def gated_delta_decode_fused_gates(q, k, v, a, b, A_log, dt_bias, ssm_state, batch_indices=None,
+                                   scale=None, use_qk_l2norm_in_kernel=True, *, out=None,
+                                   dev_status=None):
+    """Decode step with the gates computed in the kernel (``gdn_decode_gated``); a, b [n, Hv]."""
+    _need(q, "q", (torch.float32, torch.bfloat16))
+    dev, dt = q.device, q.dtype
+    n, Hqk, K = q.shape
+    Hv, V = v.shape[1], v.shape[2]
+    _need(k, "k", dt, dev, q.shape)
+    _need(v, "v", dt, dev)
+    ab_dt = _gate_args(a, b, A_log, dt_bias, dev, dt, (n,), Hv)
+    _need(ssm_state, "ssm_state", torch.float32, dev)
+    if batch_indices is not None:
+        _need(batch_indices, "batch_indices", torch.int32, dev, (n,))
+    if out is None:
+        out = torch.empty((n, Hv, V), dtype=dt, device=dev)
+    st = _lib.load().gdn_decode_gated(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), ab_dt, _ptr(A_log), _ptr(dt_bias),
+        _ptr(ssm_state), ssm_state.shape[0], _ptr(batch_indices), n, Hqk, Hv, K, V, _DT[dt],
+        _scale(scale), int(bool(use_qk_l2norm_in_kernel)), _ptr(out), _ptr(dev_status),
+        _stream(dev))
+    _lib.check("gdn_decode_gated", st)
     return out

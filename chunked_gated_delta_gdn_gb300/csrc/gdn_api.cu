@@ -29,6 +29,17 @@ gdn_status_t check_chunk_shapes(int B, int T, int Hqk, int Hv, int K, int V, int
   return GDN_OK;
 }
 
+// Arguments of the fused-gate entry points (checked before anything else).
+gdn_status_t check_gate_args(const void* a, const void* b, int ab_dtype, const float* A_log,
+                             const float* dt_bias, int io_dtype, long long count) {
+  if (!is_dtype(ab_dtype) || (ab_dtype != GDN_F32 && ab_dtype != io_dtype)) return GDN_ERR_DTYPE;
+  if (count > 0 && (!a || !b || !A_log || !dt_bias)) return GDN_ERR_NULL;
+  if (((uintptr_t)a & (elem_size(ab_dtype) - 1)) || ((uintptr_t)b & (elem_size(ab_dtype) - 1)) ||
+      ((uintptr_t)A_log & 3u) || ((uintptr_t)dt_bias & 3u))
+    return GDN_ERR_LAYOUT;
+  return GDN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -63,14 +74,14 @@ size_t gdn_chunk_fwd_workspace_size(int B, int T, int Hqk, int Hv, int K, int V,
   return gdn::chunk_generic_workspace_bytes((int)T_total, num_seqs, Hv, K, V);
 }
 
-gdn_status_t gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
-                           const void* beta, int B, int T, int Hqk, int Hv, int K, int V,
-                           gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype, float scale,
-                           int chunk_size, const float* initial_state, int output_final_state,
-                           float* final_state, int use_qk_l2norm, const int32_t* cu_seqlens,
-                           int num_seqs, const int32_t* state_indices, int num_slots, void* o,
-                           void* workspace, size_t workspace_bytes, int* dev_status,
-                           void* stream) {
+static gdn_status_t chunk_impl(const void* q, const void* k, const void* v, const float* g,
+                               const void* beta, int B, int T, int Hqk, int Hv, int K, int V,
+                               gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype, float scale,
+                               int chunk_size, const float* initial_state, int output_final_state,
+                               float* final_state, int use_qk_l2norm, const int32_t* cu_seqlens,
+                               int num_seqs, const int32_t* state_indices, int num_slots, void* o,
+                               void* workspace, size_t workspace_bytes, int* dev_status,
+                               void* stream, const gdn::GateArgs& gates) {
   gdn_status_t st = check_chunk_shapes(B, T, Hqk, Hv, K, V, io_dtype, beta_dtype);
   if (st != GDN_OK) return st;
   if (chunk_size != 64) return GDN_ERR_UNSUPPORTED;
@@ -80,7 +91,8 @@ gdn_status_t gdn_chunk_fwd(const void* q, const void* k, const void* v, const fl
     num_seqs = B;
   }
   const long long T_total = (long long)B * T;
-  if (T_total > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_NULL;
+  if (T_total > 0 && (!q || !k || !v || !o)) return GDN_ERR_NULL;
+  if (T_total > 0 && gates.mode == gdn::kGatesGiven && (!g || !beta)) return GDN_ERR_NULL;
   if (output_final_state && !final_state) return GDN_ERR_NULL;
   if (state_indices) {
     if (num_slots <= 0) return GDN_ERR_SHAPE;
@@ -110,6 +122,7 @@ gdn_status_t gdn_chunk_fwd(const void* q, const void* k, const void* v, const fl
   a.workspace_bytes = workspace_bytes;
   a.dev_status = dev_status;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
+  a.gates = gates;
 
   cudaError_t err;
   if (gdn::chunk_tc_supported(K, V, io_dtype, beta_dtype)) {
@@ -123,19 +136,65 @@ gdn_status_t gdn_chunk_fwd(const void* q, const void* k, const void* v, const fl
   return err == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
-gdn_status_t gdn_decode(const void* q, const void* k, const void* v, const float* g,
-                        const void* beta, float* ssm_state, int num_slots,
-                        const int32_t* batch_indices, int n, int Hqk, int Hv, int K, int V,
-                        gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype, float scale,
-                        int use_qk_l2norm, void* o, int* dev_status, void* stream) {
+gdn_status_t gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                           const void* beta, int B, int T, int Hqk, int Hv, int K, int V,
+                           gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype, float scale,
+                           int chunk_size, const float* initial_state, int output_final_state,
+                           float* final_state, int use_qk_l2norm, const int32_t* cu_seqlens,
+                           int num_seqs, const int32_t* state_indices, int num_slots, void* o,
+                           void* workspace, size_t workspace_bytes, int* dev_status,
+                           void* stream) {
+  gdn::GateArgs gates{};
+  gates.mode = gdn::kGatesGiven;
+  return chunk_impl(q, k, v, g, beta, B, T, Hqk, Hv, K, V, io_dtype, beta_dtype, scale,
+                    chunk_size, initial_state, output_final_state, final_state, use_qk_l2norm,
+                    cu_seqlens, num_seqs, state_indices, num_slots, o, workspace,
+                    workspace_bytes, dev_status, stream, gates);
+}
+
+gdn_status_t gdn_chunk_fwd_gated(const void* q, const void* k, const void* v, const void* a,
+                                 const void* b, gdn_dtype_t ab_dtype, const float* A_log,
+                                 const float* dt_bias, int B, int T, int Hqk, int Hv, int K, int V,
+                                 gdn_dtype_t io_dtype, float scale, int chunk_size,
+                                 const float* initial_state, int output_final_state,
+                                 float* final_state, int use_qk_l2norm,
+                                 const int32_t* cu_seqlens, int num_seqs,
+                                 const int32_t* state_indices, int num_slots, void* o,
+                                 void* workspace, size_t workspace_bytes, int* dev_status,
+                                 void* stream) {
+  gdn_status_t st = check_gate_args(a, b, ab_dtype, A_log, dt_bias, io_dtype, (long long)B * T);
+  if (st != GDN_OK) return st;
+  gdn::GateArgs gates{};
+  gates.mode = gdn::kGatesFused;
+  gates.a = a;
+  gates.b = b;
+  gates.ab_dtype = ab_dtype;
+  gates.A_log = A_log;
+  gates.dt_bias = dt_bias;
+  // beta_dtype only selects the kernel family here; the fused gates replace g / beta.
+  return chunk_impl(q, k, v, nullptr, nullptr, B, T, Hqk, Hv, K, V, io_dtype, io_dtype, scale,
+                    chunk_size, initial_state, output_final_state, final_state, use_qk_l2norm,
+                    cu_seqlens, num_seqs, state_indices, num_slots, o, workspace,
+                    workspace_bytes, dev_status, stream, gates);
+}
+
+static gdn_status_t decode_impl(const void* q, const void* k, const void* v, const float* g,
+                                const void* beta, float* ssm_state, int num_slots,
+                                const int32_t* batch_indices, int n, int Hqk, int Hv, int K, int V,
+                                gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype, float scale,
+                                int use_qk_l2norm, void* o, int* dev_status, void* stream,
+                                const gdn::GateArgs& gates) {
   gdn_status_t st = check_chunk_shapes(1, 1, Hqk, Hv, K, V, io_dtype, beta_dtype);
   if (st != GDN_OK) return st;
   if (n < 0 || num_slots < 0) return GDN_ERR_SHAPE;
   if (!batch_indices && n > num_slots) return GDN_ERR_SHAPE;
   if (n == 0) return GDN_OK;
-  if (!q || !k || !v || !g || !beta || !o || !ssm_state) return GDN_ERR_NULL;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(ssm_state) ||
-      ((uintptr_t)g & 3u) || ((uintptr_t)beta & (elem_size(beta_dtype) - 1)))
+  if (!q || !k || !v || !o || !ssm_state) return GDN_ERR_NULL;
+  if (gates.mode == gdn::kGatesGiven && (!g || !beta)) return GDN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(ssm_state))
+    return GDN_ERR_LAYOUT;
+  if (gates.mode == gdn::kGatesGiven &&
+      (((uintptr_t)g & 3u) || ((uintptr_t)beta & (elem_size(beta_dtype) - 1))))
     return GDN_ERR_LAYOUT;
   gdn::DecodeArgs a;
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
@@ -149,7 +208,38 @@ gdn_status_t gdn_decode(const void* q, const void* k, const void* v, const float
   a.o = o;
   a.dev_status = dev_status;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
+  a.gates = gates;
   return gdn::launch_decode(a) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status_t gdn_decode(const void* q, const void* k, const void* v, const float* g,
+                        const void* beta, float* ssm_state, int num_slots,
+                        const int32_t* batch_indices, int n, int Hqk, int Hv, int K, int V,
+                        gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype, float scale,
+                        int use_qk_l2norm, void* o, int* dev_status, void* stream) {
+  gdn::GateArgs gates{};
+  gates.mode = gdn::kGatesGiven;
+  return decode_impl(q, k, v, g, beta, ssm_state, num_slots, batch_indices, n, Hqk, Hv, K, V,
+                     io_dtype, beta_dtype, scale, use_qk_l2norm, o, dev_status, stream, gates);
+}
+
+gdn_status_t gdn_decode_gated(const void* q, const void* k, const void* v, const void* a,
+                              const void* b, gdn_dtype_t ab_dtype, const float* A_log,
+                              const float* dt_bias, float* ssm_state, int num_slots,
+                              const int32_t* batch_indices, int n, int Hqk, int Hv, int K, int V,
+                              gdn_dtype_t io_dtype, float scale, int use_qk_l2norm, void* o,
+                              int* dev_status, void* stream) {
+  gdn_status_t st = check_gate_args(a, b, ab_dtype, A_log, dt_bias, io_dtype, n);
+  if (st != GDN_OK) return st;
+  gdn::GateArgs gates{};
+  gates.mode = gdn::kGatesFused;
+  gates.a = a;
+  gates.b = b;
+  gates.ab_dtype = ab_dtype;
+  gates.A_log = A_log;
+  gates.dt_bias = dt_bias;
+  return decode_impl(q, k, v, nullptr, nullptr, ssm_state, num_slots, batch_indices, n, Hqk, Hv,
+                     K, V, io_dtype, io_dtype, scale, use_qk_l2norm, o, dev_status, stream, gates);
 }
 
 }  // extern "C"

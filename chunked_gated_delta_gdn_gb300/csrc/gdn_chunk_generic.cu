@@ -177,14 +177,26 @@ __device__ void load_rows(const void* src, int dtype, int t0, int L, int H, int 
   }
 }
 
+// g and beta of element i = token * Hv + h: given, or computed from the raw gate
+// features (fused gates).
+__device__ __forceinline__ void gate_values(const ChunkArgs& a, size_t i, int h, float* g,
+                                            float* beta) {
+  if (a.gates.mode == kGatesFused) {
+    fused_gates(a.gates, i, h, g, beta);
+  } else {
+    *g = a.g[i];
+    *beta = load_elem(a.beta, i, a.beta_dtype);
+  }
+}
+
 // In-chunk inclusive cumsum of g (rows >= L get the last valid value) and beta
 // (zero for rows >= L).  Done by warp 0.
 __device__ void load_gates(const ChunkArgs& a, int t0, int L, int h, float* G, float* bt) {
   if (threadIdx.x >= 32) return;
   const int lane = threadIdx.x;
   float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
-  if (lane < L) { g0 = a.g[(size_t)(t0 + lane) * a.Hv + h]; b0 = load_elem(a.beta, (size_t)(t0 + lane) * a.Hv + h, a.beta_dtype); }
-  if (lane + 32 < L) { g1 = a.g[(size_t)(t0 + lane + 32) * a.Hv + h]; b1 = load_elem(a.beta, (size_t)(t0 + lane + 32) * a.Hv + h, a.beta_dtype); }
+  if (lane < L) gate_values(a, (size_t)(t0 + lane) * a.Hv + h, h, &g0, &b0);
+  if (lane + 32 < L) gate_values(a, (size_t)(t0 + lane + 32) * a.Hv + h, h, &g1, &b1);
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const float x0 = __shfl_up_sync(0xffffffffu, g0, o);

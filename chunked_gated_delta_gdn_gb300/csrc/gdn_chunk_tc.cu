@@ -146,14 +146,47 @@ __device__ __forceinline__ void issue_chunk_loads(uint8_t* sm, uint64_t* bar, co
 // g and beta of tokens t0 + lane and t0 + lane + 32, clamped to a valid token:
 // loaded one chunk ahead and masked (zero past the chunk end) where used, so the
 // loads never stall the issuing warp.
+__device__ __forceinline__ float ld_f32_early(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float ld_bf16_early(const void* p) {
+  unsigned short v;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return __bfloat162float(__ushort_as_bfloat16(v));
+}
+// (volatile loads stay where they are issued: the compiler cannot sink them to
+// their use one chunk later and expose the memory latency there)
+__device__ __forceinline__ float ld_early(const void* base, size_t i, int dtype) {
+  return dtype == GDN_BF16 ? ld_bf16_early(reinterpret_cast<const __nv_bfloat16*>(base) + i)
+                           : ld_f32_early(reinterpret_cast<const float*>(base) + i);
+}
+// Raw gate inputs of tokens t0 + lane and t0 + lane + 32: g and beta, or, with
+// fused gates, the features a and b (turned into g and beta where used).
 __device__ __forceinline__ void load_gates(const ChunkArgs& a, int t0, int h, int lane,
                                            int T_total, float* g, float* b) {
   const size_t ta = (size_t)min(t0 + lane, T_total - 1), tb = (size_t)min(t0 + lane + 32, T_total - 1);
-  g[0] = a.g[ta * a.Hv + h];
-  g[1] = a.g[tb * a.Hv + h];
-  b[0] = load_elem(a.beta, ta * a.Hv + h, a.beta_dtype);
-  b[1] = load_elem(a.beta, tb * a.Hv + h, a.beta_dtype);
+  if (a.gates.mode == kGatesFused) {
+    g[0] = ld_early(a.gates.a, ta * a.Hv + h, a.gates.ab_dtype);
+    g[1] = ld_early(a.gates.a, tb * a.Hv + h, a.gates.ab_dtype);
+    b[0] = ld_early(a.gates.b, ta * a.Hv + h, a.gates.ab_dtype);
+    b[1] = ld_early(a.gates.b, tb * a.Hv + h, a.gates.ab_dtype);
+  } else {
+    g[0] = ld_f32_early(a.g + ta * a.Hv + h);
+    g[1] = ld_f32_early(a.g + tb * a.Hv + h);
+    b[0] = ld_early(a.beta, ta * a.Hv + h, a.beta_dtype);
+    b[1] = ld_early(a.beta, tb * a.Hv + h, a.beta_dtype);
+  }
 }
+
+// 2^x on the special-function unit (inputs here are <= 0 or moderate).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ bool flag_set(const int* f) {
   return *reinterpret_cast<const volatile int*>(f) != 0;
@@ -180,6 +213,9 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
   const int T_total = a.cu_seqlens ? a.T : a.B * a.T;
   float gq[2], bq[2];
   if (warp == 0) load_gates(a, bos, h, lane, T_total, gq, bq);
+  const bool fused = a.gates.mode == kGatesFused;
+  const float expA = fused ? expf(a.gates.A_log[h]) : 0.f;
+  const float dtb = fused ? a.gates.dt_bias[h] : 0.f;
 
   for (int c = 0; c < nchunks; ++c) {
     const int s = c & 1;
@@ -201,6 +237,12 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
 
     // ---- gates: in-chunk cumulative log-decay and beta; prefetch the next chunk's
     if (warp == 0) {
+      if (fused) {   // g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b)
+        gq[0] = -expA * softplus_f(gq[0] + dtb);
+        gq[1] = -expA * softplus_f(gq[1] + dtb);
+        bq[0] = sigmoid_f(bq[0]);
+        bq[1] = sigmoid_f(bq[1]);
+      }
       float g0 = lane < L ? gq[0] : 0.f, g1 = lane + 32 < L ? gq[1] : 0.f;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -209,7 +251,7 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
         if (lane >= o) { g0 += x0; g1 += x1; }
       }
       g1 += __shfl_sync(0xffffffffu, g0, 31);
-      vec[VEC_G + lane] = g0; vec[VEC_G + lane + 32] = g1;
+      vec[VEC_G + lane] = g0 * kLog2e; vec[VEC_G + lane + 32] = g1 * kLog2e;   // base-2 log-decay
       vec[VEC_BETA + lane] = lane < L ? bq[0] : 0.f;
       vec[VEC_BETA + lane + 32] = lane + 32 < L ? bq[1] : 0.f;
       if (c + 1 < nchunks) load_gates(a, t0 + kChunk, h, lane, T_total, gq, bq);
@@ -252,9 +294,9 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
     }
     if (tid < kChunk) {   // per-token scalars while the tensor core works
       const float gl = vec[VEC_G + L - 1], gt = vec[VEC_G + tid];
-      const float et = __expf(gt), rk = vec[VEC_RK + tid];
+      const float et = ex2(gt), rk = vec[VEC_RK + tid];
       vec[VEC_SW + tid] = vec[VEC_BETA + tid] * et * rk;
-      vec[VEC_DL + tid] = __expf(gl - gt) * rk;
+      vec[VEC_DL + tid] = ex2(gl - gt) * rk;
       vec[VEC_QS + tid] = a.scale * et * vec[VEC_RQ + tid];
     }
     if (leader) {
@@ -279,13 +321,19 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
         gj[4 * m] = g4.x; gj[4 * m + 1] = g4.y; gj[4 * m + 2] = g4.z; gj[4 * m + 3] = g4.w;
         rkj[4 * m] = r4.x; rkj[4 * m + 1] = r4.y; rkj[4 * m + 2] = r4.z; rkj[4 * m + 3] = r4.w;
       }
+      const bool zero_tile = ((quad & 1) == 0) && chalf == 1;   // rows 0-31 x cols 32-63
       if (quad < 2) {
         const int i = row;
         const float gi = G[i], ri = (i < L) ? vec[VEC_RQ + i] : 0.f;
+        if (zero_tile) {
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int j = j0 + jj;
-          x[jj] = (j <= i) ? ri * rkj[jj] * x[jj] * __expf(gi - gj[jj]) : 0.f;
+          for (int jj = 0; jj < 32; ++jj) x[jj] = 0.f;
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            const int j = j0 + jj;
+            x[jj] = (j <= i) ? ri * rkj[jj] * x[jj] * ex2(gi - gj[jj]) : 0.f;
+          }
         }
         uint8_t* dst = sm + OFF_P + s * 8192;
 #pragma unroll
@@ -293,10 +341,15 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
       } else {
         const int i = row - 64;
         const float gi = G[i], bi = vec[VEC_BETA + i] * vec[VEC_RK + i];
+        if (zero_tile) {
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int j = j0 + jj;
-          x[jj] = (j < i) ? bi * rkj[jj] * x[jj] * __expf(gi - gj[jj]) : 0.f;
+          for (int jj = 0; jj < 32; ++jj) x[jj] = 0.f;
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            const int j = j0 + jj;
+            x[jj] = (j < i) ? bi * rkj[jj] * x[jj] * ex2(gi - gj[jj]) : 0.f;
+          }
         }
 #pragma unroll
         for (int m = 0; m < 8; ++m)
@@ -400,7 +453,7 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
     // ---- (T diag(beta exp(G) r_k))^T and (T diag(beta))^T as bf16 MN-major tiles:
     //      thread -> row j of the tiles (column j of T), entries i in [16 q4, 16 q4 + 16)
     {
-      const int j = tid >> 2, q4 = tid & 3;
+      const int j = tid & 63, q4 = tid >> 6;   // q4 warp-uniform: a warp reads 32 columns of a row
       const int bj = j >> 4;
       float tv[16];
 #pragma unroll
@@ -501,7 +554,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
 
     // ---- S (entry state) -> bf16 A operand S^T [dv rows][dk]; S <- exp(G_last) S in TMEM
     {
-      const float dl = __expf(vec[VEC_G + L - 1]);
+      const float dl = ex2(vec[VEC_G + L - 1]);
 #pragma unroll
       for (int part = 0; part < 4; ++part) {
         float x[32];

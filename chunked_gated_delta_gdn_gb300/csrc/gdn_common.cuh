@@ -34,6 +34,22 @@ __device__ __forceinline__ void report(int* dev_status, int bits) {
   if (dev_status) atomicOr(dev_status, bits);
 }
 
+// softplus(x) = log(1 + e^x), written as max(x, 0) + log1p(e^{-|x|}) so that it
+// neither overflows nor loses the tail.
+__device__ __forceinline__ float softplus_f(float x) {
+  return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)));
+}
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+// Gate values of element i (= token * Hv + h) from the raw gate features (the
+// fused-gate mode): g = -exp(A_log[h]) softplus(a + dt_bias[h]), beta = sigmoid(b).
+template <class GA>
+__device__ __forceinline__ void fused_gates(const GA& ga, size_t i, int h, float* g, float* beta) {
+  const float av = load_elem(ga.a, i, ga.ab_dtype), bv = load_elem(ga.b, i, ga.ab_dtype);
+  *g = -expf(ga.A_log[h]) * softplus_f(av + ga.dt_bias[h]);
+  *beta = sigmoid_f(bv);
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);

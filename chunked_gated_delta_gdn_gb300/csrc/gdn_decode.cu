@@ -22,6 +22,18 @@ namespace {
 
 constexpr int kDecodeThreads = 256;
 
+// g and beta of element i = request * Hv + h: given, or computed from the raw gate
+// features (fused gates).
+__device__ __forceinline__ void gate_values(const DecodeArgs& a, size_t i, int h, float* g,
+                                            float* beta) {
+  if (a.gates.mode == kGatesFused) {
+    fused_gates(a.gates, i, h, g, beta);
+  } else {
+    *g = a.g[i];
+    *beta = load_elem(a.beta, i, a.beta_dtype);
+  }
+}
+
 // Zero the V-vector o[i, h, :] (padding or skipped slot).
 __device__ __forceinline__ void zero_output(const DecodeArgs& a, int i, int h) {
   for (int c = threadIdx.x; c < a.V; c += blockDim.x)
@@ -110,8 +122,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode128_kernel(const Deco
   __syncthreads();
 
   const size_t hv_off = (size_t)i * a.Hv + h;
-  const float dec = expf(a.g[hv_off]);
-  const float bt = load_elem(a.beta, hv_off, a.beta_dtype);
+  float gv, bt;
+  gate_values(a, hv_off, h, &gv, &bt);
+  const float dec = expf(gv);
   const float kq = wdot[0] + wdot[1] + wdot[2] + wdot[3];
   float u[4], o[4];
 #pragma unroll
@@ -180,8 +193,9 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_generic_kernel(const De
   __syncthreads();
   float* Sp = a.state + ((size_t)s * a.Hv + h) * (size_t)K * V;
   const size_t hv_off = (size_t)i * a.Hv + h;
-  const float dec = expf(a.g[hv_off]);
-  const float bt = load_elem(a.beta, hv_off, a.beta_dtype);
+  float gv, bt;
+  gate_values(a, hv_off, h, &gv, &bt);
+  const float dec = expf(gv);
   if (tid < V) {
     float r = 0.f, p = 0.f;
     for (int row = 0; row < K; ++row) {

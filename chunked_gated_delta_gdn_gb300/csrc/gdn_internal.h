@@ -9,6 +9,21 @@
 
 namespace gdn {
 
+// Where the log-decay g and the write strength beta come from.  kGatesGiven: the
+// g / beta tensors.  kGatesFused: computed in the kernels from the raw gate
+// features a, b and the per-head parameters A_log, dt_bias:
+//   g = -exp(A_log[h]) * softplus(a + dt_bias[h]),   beta = sigmoid(b).
+enum { kGatesGiven = 0, kGatesFused = 1 };
+
+struct GateArgs {
+  int mode;
+  const void* a;           // [.., Hv], ab_dtype
+  const void* b;           // [.., Hv], ab_dtype
+  int ab_dtype;
+  const float* A_log;      // [Hv]
+  const float* dt_bias;    // [Hv]
+};
+
 struct ChunkArgs {
   const void* q;
   const void* k;
@@ -30,6 +45,7 @@ struct ChunkArgs {
   size_t workspace_bytes;
   int* dev_status;
   cudaStream_t stream;
+  GateArgs gates;
 };
 
 struct DecodeArgs {
@@ -48,6 +64,7 @@ struct DecodeArgs {
   void* o;
   int* dev_status;
   cudaStream_t stream;
+  GateArgs gates;
 };
 
 // Upper bound on the number of 64-token chunks over all sequences.

@@ -172,6 +172,40 @@ gdn_status_t gdn_decode(const void* q, const void* k, const void* v, const float
                         int use_qk_l2norm, void* o, int* dev_status, void* stream);
 
 /*
+ * Fused gates.  The GDN mixer computes "the per-head log-decay g and the write
+ * strength beta" from its gate features and the per-head parameters A_log and
+ * dt_bias ("Megatron-Core API: core.ssm.gated_delta_net.gdn",
+ * GatedDeltaNet._compute_gates; "_prepare_inference_inputs ... leaving
+ * normalization and gates fused in-kernel").  These two entry points take the
+ * raw features instead of g and beta and evaluate, inside the kernels,
+ *
+ *     g = -exp(A_log[h]) * softplus(a + dt_bias[h]),     beta = sigmoid(b),
+ *
+ * so g and beta never exist in device memory.
+ *   a, b        [B, T, Hv] (chunk) or [n, Hv] (decode), ab_dtype = GDN_F32 or io_dtype.
+ *   A_log, dt_bias  [Hv] fp32, device.
+ * Every other argument, layout and error behaviour is that of gdn_chunk_fwd /
+ * gdn_decode (beta_dtype is implied).
+ */
+gdn_status_t gdn_chunk_fwd_gated(const void* q, const void* k, const void* v, const void* a,
+                                 const void* b, gdn_dtype_t ab_dtype, const float* A_log,
+                                 const float* dt_bias, int B, int T, int Hqk, int Hv, int K, int V,
+                                 gdn_dtype_t io_dtype, float scale, int chunk_size,
+                                 const float* initial_state, int output_final_state,
+                                 float* final_state, int use_qk_l2norm,
+                                 const int32_t* cu_seqlens, int num_seqs,
+                                 const int32_t* state_indices, int num_slots, void* o,
+                                 void* workspace, size_t workspace_bytes, int* dev_status,
+                                 void* stream);
+
+gdn_status_t gdn_decode_gated(const void* q, const void* k, const void* v, const void* a,
+                              const void* b, gdn_dtype_t ab_dtype, const float* A_log,
+                              const float* dt_bias, float* ssm_state, int num_slots,
+                              const int32_t* batch_indices, int n, int Hqk, int Hv, int K, int V,
+                              gdn_dtype_t io_dtype, float scale, int use_qk_l2norm, void* o,
+                              int* dev_status, void* stream);
+
+/*
  * gdn_chunk_fwd_noalloc -- gdn_chunk_fwd without caller-provided scratch.
  *
  * The sources have no counterpart for this entry point; it exists for callers

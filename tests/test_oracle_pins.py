@@ -449,3 +449,43 @@ def test_decode_bad_slot_is_reported_and_skipped():
         oracle.decode(*args, cache, np.array([5, 1]))
     o = oracle.decode(*args, before.copy(), np.array([5, 1]), allow_bad_slots=True)
     assert np.all(o[0] == 0)
+
+
+# --------------------------------------------------------------------------- gate computation
+
+def test_gate_functions_against_textbook_values():
+    from oracle import gates
+    # softplus: log 2 at 0, identity asymptote, e^x asymptote, symmetry softplus(x) - softplus(-x) = x
+    assert gates.softplus(0.0) == pytest.approx(math.log(2.0), rel=1e-15)
+    assert gates.softplus(40.0) == pytest.approx(40.0, rel=1e-15)
+    assert gates.softplus(-40.0) == pytest.approx(math.exp(-40.0), rel=1e-12)
+    xs = np.linspace(-30, 30, 121)
+    np.testing.assert_allclose(gates.softplus(xs) - gates.softplus(-xs), xs, atol=1e-12)
+    np.testing.assert_allclose(gates.softplus(xs), np.log1p(np.exp(xs)), rtol=1e-13)
+    # sigmoid: 1/2 at 0, sigmoid(x) + sigmoid(-x) = 1, derivative identity s' = s (1 - s)
+    assert gates.sigmoid(0.0) == 0.5
+    np.testing.assert_allclose(gates.sigmoid(xs) + gates.sigmoid(-xs), 1.0, atol=1e-15)
+    h = 1e-6
+    num = (gates.sigmoid(xs + h) - gates.sigmoid(xs - h)) / (2 * h)
+    s = gates.sigmoid(xs)
+    np.testing.assert_allclose(num, s * (1 - s), atol=1e-9)
+    assert gates.sigmoid(800.0) == 1.0 and gates.sigmoid(-800.0) == 0.0
+
+
+def test_gates_formula_and_ranges():
+    from oracle import gates
+    rng = np.random.default_rng(14)
+    Hv = 6
+    A_log = np.log(rng.uniform(1, 16, Hv))
+    dt_bias = 0.5 * rng.standard_normal(Hv)
+    a = rng.standard_normal((3, 5, Hv))
+    b = rng.standard_normal((3, 5, Hv))
+    g, beta = gates.compute_gates(a, b, A_log, dt_bias)
+    assert np.all(g < 0) and np.all((beta > 0) & (beta < 1))
+    # a = -dt_bias gives softplus(0) = log 2: g = -exp(A_log) log 2 exactly
+    g0, _ = gates.compute_gates(np.broadcast_to(-dt_bias, (1, Hv)), np.zeros((1, Hv)), A_log,
+                                dt_bias)
+    np.testing.assert_allclose(g0[0], -np.exp(A_log) * math.log(2.0), rtol=1e-15)
+    # decay of one step = exp(g) = (1 + e^{a + dt})^{-exp(A_log)}
+    np.testing.assert_allclose(np.exp(g), (1 + np.exp(a + dt_bias)) ** (-np.exp(A_log)),
+                               rtol=1e-12)
