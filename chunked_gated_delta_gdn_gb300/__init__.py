@@ -10,8 +10,9 @@ its thin PyTorch binding:
 """
 from .api import (GdnError, chunk_fwd_path, chunk_gated_delta_rule,
                   chunk_gated_delta_rule_fused_gates, chunk_workspace_size, gated_delta_decode,
-                  gated_delta_decode_fused_gates)
+                  gated_delta_decode_fused_gates, gated_delta_decode_multi)
 
-__all__ = ["chunk_gated_delta_rule", "gated_delta_decode", "chunk_gated_delta_rule_fused_gates",
+__all__ = ["chunk_gated_delta_rule", "gated_delta_decode", "gated_delta_decode_multi",
+           "chunk_gated_delta_rule_fused_gates",
            "gated_delta_decode_fused_gates", "chunk_workspace_size", "chunk_fwd_path", "GdnError"]
 __version__ = "0.1.0"

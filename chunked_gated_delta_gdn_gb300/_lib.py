@@ -21,7 +21,8 @@ GDN_F32, GDN_BF16 = 0, 1
 GDN_DEV_BAD_SLOT, GDN_DEV_BAD_CU_SEQLENS = 1, 2
 
 EXPORTS = ("gdn_chunk_fwd", "gdn_chunk_fwd_workspace_size", "gdn_chunk_fwd_path", "gdn_decode",
-           "gdn_chunk_fwd_gated", "gdn_decode_gated", "gdn_status_string", "gdn_version")
+           "gdn_chunk_fwd_gated", "gdn_decode_gated", "gdn_decode_multi", "gdn_status_string",
+           "gdn_version")
 
 
 class GdnError(RuntimeError):
@@ -65,6 +66,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.gdn_decode_gated.argtypes = [vp, vp, vp, vp, vp, i, vp, vp, vp, i, vp, i, i, i, i, i,
                                          i, f, i, vp, vp, vp]
         lib.gdn_decode_gated.restype = i
+        lib.gdn_decode_multi.argtypes = [vp, vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, i, i, i,
+                                         f, i, vp, vp, vp, vp]
+        lib.gdn_decode_multi.restype = i
         lib.gdn_status_string.argtypes = [i]
         lib.gdn_status_string.restype = ctypes.c_char_p
         lib.gdn_version.argtypes = []

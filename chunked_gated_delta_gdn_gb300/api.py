@@ -14,7 +14,8 @@ import torch
 
 from . import _lib
 
-__all__ = ["chunk_gated_delta_rule", "gated_delta_decode", "chunk_gated_delta_rule_fused_gates",
+__all__ = ["chunk_gated_delta_rule", "gated_delta_decode", "gated_delta_decode_multi",
+           "chunk_gated_delta_rule_fused_gates",
            "gated_delta_decode_fused_gates", "chunk_workspace_size", "chunk_fwd_path", "GdnError"]
 
 GdnError = _lib.GdnError
@@ -267,3 +268,40 @@ def gated_delta_decode_fused_gates(q, k, v, a, b, A_log, dt_bias, ssm_state, bat
         _stream(dev))
     _lib.check("gdn_decode_gated", st)
     return out
+
+
+def gated_delta_decode_multi(q, k, v, g, beta, ssm_state, batch_indices=None, scale=None,
+                             use_qk_l2norm_in_kernel=True, output_intermediate_states=False, *,
+                             out=None, intermediate_states=None, dev_status=None):
+    """L decode tokens per request through ``gdn_decode_multi``.
+
+    q, k [n, L, Hqk, K]; v [n, L, Hv, V]; g [n, L, Hv] fp32; beta [n, L, Hv];
+    ssm_state [num_slots, Hv, K, V] fp32 (updated in place to the state after the last
+    token).  Returns ``(o [n, L, Hv, V], intermediate_states [n, L, Hv, K, V] or None)``.
+    """
+    _need(q, "q", (torch.float32, torch.bfloat16))
+    dev, dt = q.device, q.dtype
+    if q.dim() != 4 or v.dim() != 4:
+        raise ValueError("q must be [n, L, Hqk, K] and v [n, L, Hv, V]")
+    n, L, Hqk, K = q.shape
+    Hv, V = v.shape[2], v.shape[3]
+    _need(k, "k", dt, dev, q.shape)
+    _need(v, "v", dt, dev, (n, L, Hv, V))
+    _need(g, "g", torch.float32, dev, (n, L, Hv))
+    _need(beta, "beta", (dt, torch.float32), dev, (n, L, Hv))
+    _need(ssm_state, "ssm_state", torch.float32, dev)
+    if batch_indices is not None:
+        _need(batch_indices, "batch_indices", torch.int32, dev, (n,))
+    if out is None:
+        out = torch.empty((n, L, Hv, V), dtype=dt, device=dev)
+    if output_intermediate_states and intermediate_states is None:
+        intermediate_states = torch.empty((n, L, Hv, K, V), dtype=torch.float32, device=dev)
+    if intermediate_states is not None:
+        _need(intermediate_states, "intermediate_states", torch.float32, dev, (n, L, Hv, K, V))
+    st = _lib.load().gdn_decode_multi(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(ssm_state), ssm_state.shape[0],
+        _ptr(batch_indices), n, L, Hqk, Hv, K, V, _DT[dt], _DT[beta.dtype], _scale(scale),
+        int(bool(use_qk_l2norm_in_kernel)), _ptr(out), _ptr(intermediate_states),
+        _ptr(dev_status), _stream(dev))
+    _lib.check("gdn_decode_multi", st)
+    return out, intermediate_states

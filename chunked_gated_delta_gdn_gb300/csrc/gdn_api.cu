@@ -183,13 +183,16 @@ static gdn_status_t decode_impl(const void* q, const void* k, const void* v, con
                                 const int32_t* batch_indices, int n, int Hqk, int Hv, int K, int V,
                                 gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype, float scale,
                                 int use_qk_l2norm, void* o, int* dev_status, void* stream,
-                                const gdn::GateArgs& gates) {
+                                const gdn::GateArgs& gates, int L = 1,
+                                float* intermediate = nullptr) {
   gdn_status_t st = check_chunk_shapes(1, 1, Hqk, Hv, K, V, io_dtype, beta_dtype);
   if (st != GDN_OK) return st;
-  if (n < 0 || num_slots < 0) return GDN_ERR_SHAPE;
+  if (n < 0 || num_slots < 0 || L < 0) return GDN_ERR_SHAPE;
+  if ((long long)n * L > 0x7fffffffLL) return GDN_ERR_SHAPE;
   if (!batch_indices && n > num_slots) return GDN_ERR_SHAPE;
-  if (n == 0) return GDN_OK;
+  if (n == 0 || L == 0) return GDN_OK;
   if (!q || !k || !v || !o || !ssm_state) return GDN_ERR_NULL;
+  if (intermediate && !aligned16(intermediate)) return GDN_ERR_LAYOUT;
   if (gates.mode == gdn::kGatesGiven && (!g || !beta)) return GDN_ERR_NULL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(ssm_state))
     return GDN_ERR_LAYOUT;
@@ -209,6 +212,8 @@ static gdn_status_t decode_impl(const void* q, const void* k, const void* v, con
   a.dev_status = dev_status;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   a.gates = gates;
+  a.L = L;
+  a.intermediate = intermediate;
   return gdn::launch_decode(a) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -221,6 +226,19 @@ gdn_status_t gdn_decode(const void* q, const void* k, const void* v, const float
   gates.mode = gdn::kGatesGiven;
   return decode_impl(q, k, v, g, beta, ssm_state, num_slots, batch_indices, n, Hqk, Hv, K, V,
                      io_dtype, beta_dtype, scale, use_qk_l2norm, o, dev_status, stream, gates);
+}
+
+gdn_status_t gdn_decode_multi(const void* q, const void* k, const void* v, const float* g,
+                              const void* beta, float* ssm_state, int num_slots,
+                              const int32_t* batch_indices, int n, int L, int Hqk, int Hv, int K,
+                              int V, gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype, float scale,
+                              int use_qk_l2norm, void* o, float* intermediate_states,
+                              int* dev_status, void* stream) {
+  gdn::GateArgs gates{};
+  gates.mode = gdn::kGatesGiven;
+  return decode_impl(q, k, v, g, beta, ssm_state, num_slots, batch_indices, n, Hqk, Hv, K, V,
+                     io_dtype, beta_dtype, scale, use_qk_l2norm, o, dev_status, stream, gates, L,
+                     intermediate_states);
 }
 
 gdn_status_t gdn_decode_gated(const void* q, const void* k, const void* v, const void* a,

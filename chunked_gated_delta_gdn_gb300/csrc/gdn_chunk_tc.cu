@@ -54,15 +54,16 @@ constexpr uint32_t OFF_QK = 0;          // 2 stages x 32 KB: [dk half][Q rows 0-
 constexpr uint32_t QK_STAGE = 32768;
 constexpr uint32_t OFF_V = 65536;       // 2 stages x 16 KB: [dv half][64 tokens][128 B]
 constexpr uint32_t V_STAGE = 16384;
-constexpr uint32_t OFF_S = 98304;       // S^T bf16, A operand: [dk half][128 dv rows][128 B]
+constexpr uint32_t OFF_S = 98304;       // S^T bf16, A operand: [dk half][128 dv rows][128 B]; after
+                                        // the MMAs that read it, the bf16 output tile staged for a
+                                        // TMA store
 constexpr uint32_t OFF_W = 131072;      // -W^T bf16, MN-major B: [128 dk rows][64 tokens]
-constexpr uint32_t OFF_A = 147456;      // fp32 A [64][64], 16-byte-group swizzled; afterwards
-constexpr uint32_t OFF_TW = 147456;     //   (T diag(beta exp(G) r_k))^T, MN-major B [64 j][64 i]
-constexpr uint32_t OFF_TU = 155648;     //   (T diag(beta))^T, MN-major B
+constexpr uint32_t OFF_A = 147456;      // fp32 A [64][64], 16-byte-group swizzled; the solve
+                                        // overwrites its strictly-lower blocks with those of T
 constexpr uint32_t OFF_P = 163840;      // 2 x P, K-major B [64 i][64 j]
 constexpr uint32_t OFF_U = 180224;      // U'^T bf16, K-major A [128 dv][64 tokens]
-constexpr uint32_t OFF_UT = 196608;     // (U' exp(G_last - G) r_k)^T bf16; after the MMA that
-                                        // reads it, the bf16 output tile staged for a TMA store
+constexpr uint32_t OFF_TW = 196608;     // (T diag(beta exp(G) r_k))^T, MN-major B [64 j][64 i]
+constexpr uint32_t OFF_TU = 204800;     // (T diag(beta))^T, MN-major B
 constexpr uint32_t OFF_VEC = 212992;    // 2 x per-token fp32 vectors [7][64]
 constexpr uint32_t VEC_G = 0, VEC_BETA = 64, VEC_RQ = 128, VEC_RK = 192, VEC_SW = 256,
                    VEC_DL = 320, VEC_QS = 384, VEC_FLOATS = 448;
@@ -235,6 +236,19 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
     }
     if (group_sync_or(kBarPrep, kPrepThreads, !ok || flag_set(flag))) { if (leader) set_flag(flag); return; }
 
+    // ---- MMA: D1 = [Q;K] K^T, issued as soon as the tiles are in (overlaps gates and norms)
+    if (leader) {
+      tc_fence_after();
+      const uint32_t id1 = idesc_bf16(128, 64, false, false);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+        mma_bf16(tbase + COL_D1, sdesc_sw128(qk_a + off, 16, 1024),
+                 sdesc_sw128(qk_a + off + 8192, 16, 1024), id1, ks > 0);
+      }
+      mma_commit(&bars[B_MMA_P]);
+    }
+
     // ---- gates: in-chunk cumulative log-decay and beta; prefetch the next chunk's
     if (warp == 0) {
       if (fused) {   // g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b)
@@ -277,21 +291,7 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
         vec[VEC_RK + r] = a.use_qk_l2norm ? 1.0f / sqrtf(sk + kL2Eps) : 1.0f;
       }
     }
-    tc_fence_before();
     group_sync(kBarPrep, kPrepThreads);
-
-    // ---- MMA: D1 = [Q;K] K^T
-    if (leader) {
-      tc_fence_after();
-      const uint32_t id1 = idesc_bf16(128, 64, false, false);
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-        mma_bf16(tbase + COL_D1, sdesc_sw128(qk_a + off, 16, 1024),
-                 sdesc_sw128(qk_a + off + 8192, 16, 1024), id1, ks > 0);
-      }
-      mma_commit(&bars[B_MMA_P]);
-    }
     if (tid < kChunk) {   // per-token scalars while the tensor core works
       const float gl = vec[VEC_G + L - 1], gt = vec[VEC_G + tid];
       const float et = ex2(gt), rk = vec[VEC_RK + tid];
@@ -385,6 +385,22 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
       }
 #pragma unroll
       for (int i = 0; i < 16; ++i) sTd[(b * 16 + i) * 16 + jj] = x[i];
+      // row j = 16 b + jj of (T diag(beta exp(G) r_k))^T and (T diag(beta))^T: the zeros
+      // before the diagonal block and the diagonal block itself
+      const int j = 16 * b + jj;
+      const float sw = vec[VEC_SW + j], sb = vec[VEC_BETA + j];
+      float w[16], u[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) { w[i] = x[i] * sw; u[i] = x[i] * sb; }
+      store_bf16x8(sm + OFF_TW + sw128_offset(j, 16 * b), w);
+      store_bf16x8(sm + OFF_TW + sw128_offset(j, 16 * b + 8), w + 8);
+      store_bf16x8(sm + OFF_TU + sw128_offset(j, 16 * b), u);
+      store_bf16x8(sm + OFF_TU + sw128_offset(j, 16 * b + 8), u + 8);
+      const float zeros[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int i8 = 0; i8 < 2 * b; ++i8) {
+        store_bf16x8(sm + OFF_TW + sw128_offset(j, 8 * i8), zeros);
+        store_bf16x8(sm + OFF_TU + sw128_offset(j, 8 * i8), zeros);
+      }
     }
     group_sync(kBarPrep, kPrepThreads);
     // ---- step 2: block row b from the rows above it, T[b, :16b] = -T_bb (A[b, :16b] T[:16b, :16b]),
@@ -439,40 +455,34 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
           }
           __syncwarp();
         }
-        group_sync(kBarPrep, kPrepThreads);   // all reads of A's block row b are done
         if (active) {
+          // T block row b, columns c0, c0 + 1 of this tile -> Tw / Tu entries (row = column of T)
           const int r0 = 16 * b + g8, c0 = 8 * nt + 2 * t4;
-          sA[a_idx(r0, c0)] = -z[0];
-          sA[a_idx(r0, c0 + 1)] = -z[1];
-          sA[a_idx(r0 + 8, c0)] = -z[2];
-          sA[a_idx(r0 + 8, c0 + 1)] = -z[3];
+          const float sw0 = vec[VEC_SW + c0], sw1 = vec[VEC_SW + c0 + 1];
+          const float sb0 = vec[VEC_BETA + c0], sb1 = vec[VEC_BETA + c0 + 1];
+          __nv_bfloat16* tw = reinterpret_cast<__nv_bfloat16*>(sm + OFF_TW);
+          __nv_bfloat16* tu = reinterpret_cast<__nv_bfloat16*>(sm + OFF_TU);
+          tw[sw128_offset(c0, r0) >> 1] = __float2bfloat16_rn(-z[0] * sw0);
+          tw[sw128_offset(c0 + 1, r0) >> 1] = __float2bfloat16_rn(-z[1] * sw1);
+          tw[sw128_offset(c0, r0 + 8) >> 1] = __float2bfloat16_rn(-z[2] * sw0);
+          tw[sw128_offset(c0 + 1, r0 + 8) >> 1] = __float2bfloat16_rn(-z[3] * sw1);
+          tu[sw128_offset(c0, r0) >> 1] = __float2bfloat16_rn(-z[0] * sb0);
+          tu[sw128_offset(c0 + 1, r0) >> 1] = __float2bfloat16_rn(-z[1] * sb1);
+          tu[sw128_offset(c0, r0 + 8) >> 1] = __float2bfloat16_rn(-z[2] * sb0);
+          tu[sw128_offset(c0 + 1, r0 + 8) >> 1] = __float2bfloat16_rn(-z[3] * sb1);
         }
-        group_sync(kBarPrep, kPrepThreads);
+        if (b < 3) {
+          group_sync(kBarPrep, kPrepThreads);   // all reads of A's block row b are done
+          if (active) {   // fp32 T block for the later rounds, over A in place
+            const int r0 = 16 * b + g8, c0 = 8 * nt + 2 * t4;
+            sA[a_idx(r0, c0)] = -z[0];
+            sA[a_idx(r0, c0 + 1)] = -z[1];
+            sA[a_idx(r0 + 8, c0)] = -z[2];
+            sA[a_idx(r0 + 8, c0 + 1)] = -z[3];
+          }
+          group_sync(kBarPrep, kPrepThreads);
+        }
       }
-    }
-    // ---- (T diag(beta exp(G) r_k))^T and (T diag(beta))^T as bf16 MN-major tiles:
-    //      thread -> row j of the tiles (column j of T), entries i in [16 q4, 16 q4 + 16)
-    {
-      const int j = tid & 63, q4 = tid >> 6;   // q4 warp-uniform: a warp reads 32 columns of a row
-      const int bj = j >> 4;
-      float tv[16];
-#pragma unroll
-      for (int ii = 0; ii < 16; ++ii) {
-        const int i = 16 * q4 + ii;
-        float v = 0.f;
-        if (q4 == bj) v = sTd[(bj * 16 + ii) * 16 + (j & 15)];
-        else if (q4 > bj) v = sA[a_idx(i, j)];
-        tv[ii] = v;
-      }
-      group_sync(kBarPrep, kPrepThreads);   // every read of the A region is done: tiles overwrite it
-      const float sw = vec[VEC_SW + j], sb = vec[VEC_BETA + j];
-      float w[16], u[16];
-#pragma unroll
-      for (int ii = 0; ii < 16; ++ii) { w[ii] = tv[ii] * sw; u[ii] = tv[ii] * sb; }
-      store_bf16x8(sm + OFF_TW + sw128_offset(j, 16 * q4), w);
-      store_bf16x8(sm + OFF_TW + sw128_offset(j, 16 * q4 + 8), w + 8);
-      store_bf16x8(sm + OFF_TU + sw128_offset(j, 16 * q4), u);
-      store_bf16x8(sm + OFF_TU + sw128_offset(j, 16 * q4 + 8), u + 8);
     }
     fence_proxy_async_smem();
     group_sync(kBarPrep, kPrepThreads);
@@ -548,7 +558,10 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     const uint32_t qk_a = sbase + OFF_QK + s * QK_STAGE;
 
     bool ok = true;
-    if (leader) ok = mbar_wait(&bars[B_READY + s], (uint32_t)(c >> 1) & 1u, kWaitLimitNs);
+    if (leader) {
+      ok = mbar_wait(&bars[B_READY + s], (uint32_t)(c >> 1) & 1u, kWaitLimitNs);
+      tma_store_wait_read();   // the previous output tile (staged where S^T goes) has been read
+    }
     if (group_sync_or(kBarState, kStateThreads, !ok || flag_set(flag))) { failed = true; break; }
     tc_fence_after();
 
@@ -592,24 +605,37 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
                  sdesc_sw128(qk_a + off, 16, 1024), id5, ks > 0);
       }
       mma_commit(&bars[B_MMA_S]);
-      tma_store_wait_read();   // the previous output tile (staged where Ut goes) has been read
     }
     if (leader) ok = mbar_wait(&bars[B_MMA_S], ps, kWaitLimitNs);
     ps ^= 1u;
     if (group_sync_or(kBarState, kStateThreads, !ok || flag_set(flag))) { failed = true; break; }
     tc_fence_after();
 
-    // ---- U'^T and (U' exp(G_last - G) r_k)^T -> bf16 K-major A operands [dv rows][tokens]
+    // ---- U'^T -> bf16 K-major A operand [dv rows][tokens]; K tile rows scaled by
+    //      exp(G_last - G_t) r_k[t] in place (the state update's B operand; the prep
+    //      group is done with this K tile)
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-      float x[32], y[32];
+      float x[32];
       tmem_ld32(tbase + lane_off + COL_U + 64 * s + 32 * half, x);
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj) y[jj] = x[jj] * vec[VEC_DL + 32 * half + jj];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
+      for (int m = 0; m < 4; ++m)
         store_bf16x8(sm + OFF_U + sw128_offset(row, 32 * half + 8 * m), &x[8 * m]);
-        store_bf16x8(sm + OFF_UT + sw128_offset(row, 32 * half + 8 * m), &y[8 * m]);
+    }
+    {
+      const int t = tid >> 1, kh = tid & 1;
+      const float dl = vec[VEC_DL + t];
+      uint8_t* krow = sm + OFF_QK + s * QK_STAGE + kh * 16384 + 8192 + t * 128;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        uint4 u = *reinterpret_cast<uint4*>(krow + 16 * m);
+        __nv_bfloat162* b2 = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(b2[e]);
+          b2[e] = __floats2bfloat162_rn(f.x * dl, f.y * dl);
+        }
+        *reinterpret_cast<uint4*>(krow + 16 * m) = u;
       }
     }
     fence_proxy_async_smem();
@@ -629,7 +655,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
       const uint32_t id7 = idesc_bf16(128, 128, false, true);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
-        mma_bf16(tbase + COL_S, sdesc_sw128(sbase + OFF_UT + ks * 32, 16, 1024),
+        mma_bf16(tbase + COL_S, sdesc_sw128(sbase + OFF_U + ks * 32, 16, 1024),
                  sdesc_sw128(qk_a + 8192 + ks * 2048, 16384, 1024), id7, 1);
       }
       mma_commit(&bars[B_P_FREE + s]);
@@ -649,7 +675,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     //      128-byte-swizzled [64 tokens][64 dv] halves) and written by one TMA store;
     //      the last, partial chunk of a sequence is stored row by row
     if (L == kChunk) {
-      uint8_t* stage = sm + OFF_UT + (row >> 6) * 8192;
+      uint8_t* stage = sm + OFF_S + (row >> 6) * 8192;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         float x[32], y[32];
@@ -665,8 +691,8 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
       fence_proxy_async_smem();
       group_sync(kBarState, kStateThreads);
       if (leader) {
-        tma_store_3d(to, sm + OFF_UT, 0, h, t0);
-        tma_store_3d(to, sm + OFF_UT + 8192, 64, h, t0);
+        tma_store_3d(to, sm + OFF_S, 0, h, t0);
+        tma_store_3d(to, sm + OFF_S + 8192, 64, h, t0);
         tma_store_commit();
       }
     } else {

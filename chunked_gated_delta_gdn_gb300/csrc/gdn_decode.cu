@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode128_kernel(const Deco
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int s = resolve_slot(a, i);
   if (s < 0) {
-    zero_output(a, i, h);
+    for (int t = 0; t < a.L; ++t) zero_output(a, i * a.L + t, h);
     return;
   }
   const int hq = h / (a.Hv / a.Hqk);
@@ -79,85 +79,92 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode128_kernel(const Deco
   __shared__ float wsum[8], wdot[4];
   __shared__ float red[2][2][V];
 
-  // q and k: threads 0..127 take q, 128..255 take k; per-vector sums of squares.
-  const size_t qk_off = ((size_t)i * a.Hqk + hq) * K;
-  const float x = tid < K ? load_elem(a.q, qk_off + tid, a.io_dtype)
-                          : load_elem(a.k, qk_off + tid - K, a.io_dtype);
-  const float ss = warp_sum(x * x);
-  if (lane == 0) wsum[warp] = ss;
-  __syncthreads();
-  float rn = 1.0f;
-  if (a.use_qk_l2norm) {
-    const float tot = tid < K ? wsum[0] + wsum[1] + wsum[2] + wsum[3]
-                              : wsum[4] + wsum[5] + wsum[6] + wsum[7];
-    rn = 1.0f / sqrtf(tot + kL2Eps);
-  }
-  if (tid < K) sq[tid] = x * rn; else sk[tid - K] = x * rn;
-  __syncthreads();
-  if (tid < K) {
-    const float d = warp_sum(sq[tid] * sk[tid]);
-    if (lane == 0) wdot[warp] = d;
-  }
+  for (int t = 0; t < a.L; ++t) {
+    const int it = i * a.L + t;   // row of this token in the [n * L, ...] inputs
+    if (t > 0) __syncthreads();   // sq / sk / red of the previous token fully consumed
+    // q and k: threads 0..127 take q, 128..255 take k; per-vector sums of squares.
+    const size_t qk_off = ((size_t)it * a.Hqk + hq) * K;
+    const float x = tid < K ? load_elem(a.q, qk_off + tid, a.io_dtype)
+                            : load_elem(a.k, qk_off + tid - K, a.io_dtype);
+    const float ss = warp_sum(x * x);
+    if (lane == 0) wsum[warp] = ss;
+    __syncthreads();
+    float rn = 1.0f;
+    if (a.use_qk_l2norm) {
+      const float tot = tid < K ? wsum[0] + wsum[1] + wsum[2] + wsum[3]
+                                : wsum[4] + wsum[5] + wsum[6] + wsum[7];
+      rn = 1.0f / sqrtf(tot + kL2Eps);
+    }
+    if (tid < K) sq[tid] = x * rn; else sk[tid - K] = x * rn;
+    __syncthreads();
+    if (tid < K) {
+      const float d = warp_sum(sq[tid] * sk[tid]);
+      if (lane == 0) wdot[warp] = d;
+    }
 
-  // Partial r = S^T k and p = S^T q over this thread's 16 rows.
-  float4 pr = make_float4(0.f, 0.f, 0.f, 0.f), pq = pr;
+    // Partial r = S^T k and p = S^T q over this thread's 16 rows.
+    float4 pr = make_float4(0.f, 0.f, 0.f, 0.f), pq = pr;
 #pragma unroll
-  for (int m = 0; m < 16; ++m) {
-    const float kr = sk[row0 + 4 * m], qr = sq[row0 + 4 * m];
-    pr.x += S[m].x * kr; pr.y += S[m].y * kr; pr.z += S[m].z * kr; pr.w += S[m].w * kr;
-    pq.x += S[m].x * qr; pq.y += S[m].y * qr; pq.z += S[m].z * qr; pq.w += S[m].w * qr;
-  }
-  // Reduce over the four row lanes of the warp (lane bits 3 and 4).
+    for (int m = 0; m < 16; ++m) {
+      const float kr = sk[row0 + 4 * m], qr = sq[row0 + 4 * m];
+      pr.x += S[m].x * kr; pr.y += S[m].y * kr; pr.z += S[m].z * kr; pr.w += S[m].w * kr;
+      pq.x += S[m].x * qr; pq.y += S[m].y * qr; pq.z += S[m].z * qr; pq.w += S[m].w * qr;
+    }
+    // Reduce over the four row lanes of the warp (lane bits 3 and 4).
 #pragma unroll
-  for (int o = 8; o <= 16; o <<= 1) {
-    pr.x += __shfl_xor_sync(0xffffffffu, pr.x, o); pr.y += __shfl_xor_sync(0xffffffffu, pr.y, o);
-    pr.z += __shfl_xor_sync(0xffffffffu, pr.z, o); pr.w += __shfl_xor_sync(0xffffffffu, pr.w, o);
-    pq.x += __shfl_xor_sync(0xffffffffu, pq.x, o); pq.y += __shfl_xor_sync(0xffffffffu, pq.y, o);
-    pq.z += __shfl_xor_sync(0xffffffffu, pq.z, o); pq.w += __shfl_xor_sync(0xffffffffu, pq.w, o);
-  }
-  if (lane < 8) {
-    *reinterpret_cast<float4*>(&red[warp >> 2][0][col]) = pr;
-    *reinterpret_cast<float4*>(&red[warp >> 2][1][col]) = pq;
-  }
-  __syncthreads();
+    for (int o = 8; o <= 16; o <<= 1) {
+      pr.x += __shfl_xor_sync(0xffffffffu, pr.x, o); pr.y += __shfl_xor_sync(0xffffffffu, pr.y, o);
+      pr.z += __shfl_xor_sync(0xffffffffu, pr.z, o); pr.w += __shfl_xor_sync(0xffffffffu, pr.w, o);
+      pq.x += __shfl_xor_sync(0xffffffffu, pq.x, o); pq.y += __shfl_xor_sync(0xffffffffu, pq.y, o);
+      pq.z += __shfl_xor_sync(0xffffffffu, pq.z, o); pq.w += __shfl_xor_sync(0xffffffffu, pq.w, o);
+    }
+    if (lane < 8) {
+      *reinterpret_cast<float4*>(&red[warp >> 2][0][col]) = pr;
+      *reinterpret_cast<float4*>(&red[warp >> 2][1][col]) = pq;
+    }
+    __syncthreads();
 
-  const size_t hv_off = (size_t)i * a.Hv + h;
-  float gv, bt;
-  gate_values(a, hv_off, h, &gv, &bt);
-  const float dec = expf(gv);
-  const float kq = wdot[0] + wdot[1] + wdot[2] + wdot[3];
-  float u[4], o[4];
+    const size_t hv_off = (size_t)it * a.Hv + h;
+    float gv, bt;
+    gate_values(a, hv_off, h, &gv, &bt);
+    const float dec = expf(gv);
+    const float kq = wdot[0] + wdot[1] + wdot[2] + wdot[3];
+    float u[4], o[4];
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const float r = red[0][0][col + c] + red[1][0][col + c];
-    const float p = red[0][1][col + c] + red[1][1][col + c];
-    const float vv = load_elem(a.v, hv_off * V + col + c, a.io_dtype);
-    u[c] = bt * (vv - dec * r);
-    o[c] = a.scale * (dec * p + kq * u[c]);
-  }
-  if (warp < 4 && lane < 8) {
-    if (a.io_dtype == GDN_BF16) {
-      __nv_bfloat162 lo = __floats2bfloat162_rn(o[0], o[1]);
-      __nv_bfloat162 hi = __floats2bfloat162_rn(o[2], o[3]);
-      uint2 pk;
-      pk.x = *reinterpret_cast<uint32_t*>(&lo);
-      pk.y = *reinterpret_cast<uint32_t*>(&hi);
-      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.o) + hv_off * V + col) = pk;
-    } else {
-      *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.o) + hv_off * V + col) =
-          make_float4(o[0], o[1], o[2], o[3]);
+    for (int c = 0; c < 4; ++c) {
+      const float r = red[0][0][col + c] + red[1][0][col + c];
+      const float p = red[0][1][col + c] + red[1][1][col + c];
+      const float vv = load_elem(a.v, hv_off * V + col + c, a.io_dtype);
+      u[c] = bt * (vv - dec * r);
+      o[c] = a.scale * (dec * p + kq * u[c]);
+    }
+    if (warp < 4 && lane < 8) {
+      if (a.io_dtype == GDN_BF16) {
+        __nv_bfloat162 lo = __floats2bfloat162_rn(o[0], o[1]);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(o[2], o[3]);
+        uint2 pk;
+        pk.x = *reinterpret_cast<uint32_t*>(&lo);
+        pk.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.o) + hv_off * V + col) = pk;
+      } else {
+        *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.o) + hv_off * V + col) =
+            make_float4(o[0], o[1], o[2], o[3]);
+      }
+    }
+    float* inter = a.intermediate ? a.intermediate + hv_off * (size_t)(K * V) : nullptr;
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      const float kr = sk[row0 + 4 * m];
+      S[m].x = dec * S[m].x + kr * u[0];
+      S[m].y = dec * S[m].y + kr * u[1];
+      S[m].z = dec * S[m].z + kr * u[2];
+      S[m].w = dec * S[m].w + kr * u[3];
+      if (inter) __stcs(reinterpret_cast<float4*>(inter + (size_t)(row0 + 4 * m) * V + col), S[m]);
     }
   }
 #pragma unroll
-  for (int m = 0; m < 16; ++m) {
-    const float kr = sk[row0 + 4 * m];
-    float4 w;
-    w.x = dec * S[m].x + kr * u[0];
-    w.y = dec * S[m].y + kr * u[1];
-    w.z = dec * S[m].z + kr * u[2];
-    w.w = dec * S[m].w + kr * u[3];
-    __stcs(reinterpret_cast<float4*>(Sp + (size_t)(row0 + 4 * m) * V + col), w);
-  }
+  for (int m = 0; m < 16; ++m)
+    __stcs(reinterpret_cast<float4*>(Sp + (size_t)(row0 + 4 * m) * V + col), S[m]);
 }
 
 // Any accepted K, V (<= 128): reductions by column threads, then an elementwise
@@ -169,55 +176,62 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_generic_kernel(const De
   const int tid = threadIdx.x;
   const int s = resolve_slot(a, i);
   if (s < 0) {
-    zero_output(a, i, h);
+    for (int t = 0; t < a.L; ++t) zero_output(a, i * a.L + t, h);
     return;
   }
   const int hq = h / (a.Hv / a.Hqk);
   __shared__ float sq[GDN_MAX_HEAD_DIM], sk[GDN_MAX_HEAD_DIM], su[GDN_MAX_HEAD_DIM];
   __shared__ float part[3][kDecodeThreads / 32];
-  const size_t qk_off = ((size_t)i * a.Hqk + hq) * K;
-  float xq = 0.f, xk = 0.f;
-  if (tid < K) {
-    xq = load_elem(a.q, qk_off + tid, a.io_dtype);
-    xk = load_elem(a.k, qk_off + tid, a.io_dtype);
-  }
-  float s1 = warp_sum(xq * xq), s2 = warp_sum(xk * xk), s3 = warp_sum(xq * xk);
-  if ((tid & 31) == 0) { part[0][tid >> 5] = s1; part[1][tid >> 5] = s2; part[2][tid >> 5] = s3; }
-  __syncthreads();
-  float nq = 0.f, nk = 0.f, dqk = 0.f;
-  for (int w = 0; w < kDecodeThreads / 32; ++w) { nq += part[0][w]; nk += part[1][w]; dqk += part[2][w]; }
-  float rq = 1.f, rk = 1.f;
-  if (a.use_qk_l2norm) { rq = 1.0f / sqrtf(nq + kL2Eps); rk = 1.0f / sqrtf(nk + kL2Eps); }
-  if (tid < K) { sq[tid] = xq * rq; sk[tid] = xk * rk; }
-  const float kq = dqk * rq * rk;
-  __syncthreads();
   float* Sp = a.state + ((size_t)s * a.Hv + h) * (size_t)K * V;
-  const size_t hv_off = (size_t)i * a.Hv + h;
-  float gv, bt;
-  gate_values(a, hv_off, h, &gv, &bt);
-  const float dec = expf(gv);
-  if (tid < V) {
-    float r = 0.f, p = 0.f;
-    for (int row = 0; row < K; ++row) {
-      const float x = Sp[(size_t)row * V + tid];
-      r += x * sk[row];
-      p += x * sq[row];
+  for (int t = 0; t < a.L; ++t) {
+    const int it = i * a.L + t;
+    if (t > 0) __syncthreads();
+    const size_t qk_off = ((size_t)it * a.Hqk + hq) * K;
+    float xq = 0.f, xk = 0.f;
+    if (tid < K) {
+      xq = load_elem(a.q, qk_off + tid, a.io_dtype);
+      xk = load_elem(a.k, qk_off + tid, a.io_dtype);
     }
-    const float u = bt * (load_elem(a.v, hv_off * V + tid, a.io_dtype) - dec * r);
-    su[tid] = u;
-    store_elem(a.o, hv_off * V + tid, a.scale * (dec * p + kq * u), a.io_dtype);
-  }
-  __syncthreads();
-  for (int e = tid; e < K * V; e += blockDim.x) {
-    const int row = e / V, c = e - row * V;
-    Sp[e] = dec * Sp[e] + sk[row] * su[c];
+    float s1 = warp_sum(xq * xq), s2 = warp_sum(xk * xk), s3 = warp_sum(xq * xk);
+    if ((tid & 31) == 0) { part[0][tid >> 5] = s1; part[1][tid >> 5] = s2; part[2][tid >> 5] = s3; }
+    __syncthreads();
+    float nq = 0.f, nk = 0.f, dqk = 0.f;
+    for (int w = 0; w < kDecodeThreads / 32; ++w) { nq += part[0][w]; nk += part[1][w]; dqk += part[2][w]; }
+    float rq = 1.f, rk = 1.f;
+    if (a.use_qk_l2norm) { rq = 1.0f / sqrtf(nq + kL2Eps); rk = 1.0f / sqrtf(nk + kL2Eps); }
+    if (tid < K) { sq[tid] = xq * rq; sk[tid] = xk * rk; }
+    const float kq = dqk * rq * rk;
+    __syncthreads();
+    const size_t hv_off = (size_t)it * a.Hv + h;
+    float gv, bt;
+    gate_values(a, hv_off, h, &gv, &bt);
+    const float dec = expf(gv);
+    if (tid < V) {
+      float r = 0.f, p = 0.f;
+      for (int row = 0; row < K; ++row) {
+        const float x = Sp[(size_t)row * V + tid];
+        r += x * sk[row];
+        p += x * sq[row];
+      }
+      const float u = bt * (load_elem(a.v, hv_off * V + tid, a.io_dtype) - dec * r);
+      su[tid] = u;
+      store_elem(a.o, hv_off * V + tid, a.scale * (dec * p + kq * u), a.io_dtype);
+    }
+    __syncthreads();
+    float* inter = a.intermediate ? a.intermediate + hv_off * (size_t)K * V : nullptr;
+    for (int e = tid; e < K * V; e += blockDim.x) {
+      const int row = e / V, c = e - row * V;
+      const float nv = dec * Sp[e] + sk[row] * su[c];
+      Sp[e] = nv;
+      if (inter) inter[e] = nv;
+    }
   }
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs& a) {
-  if (a.n == 0) return cudaSuccess;
+  if (a.n == 0 || a.L == 0) return cudaSuccess;
   const long long blocks = (long long)a.n * a.Hv;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   if (a.K == 128 && a.V == 128)

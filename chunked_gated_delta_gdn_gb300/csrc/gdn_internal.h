@@ -65,6 +65,8 @@ struct DecodeArgs {
   int* dev_status;
   cudaStream_t stream;
   GateArgs gates;
+  int L;                // tokens per request (1 for the single-token step)
+  float* intermediate;  // [n, L, Hv, K, V] state after every token, or NULL
 };
 
 // Upper bound on the number of 64-token chunks over all sequences.

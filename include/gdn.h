@@ -172,6 +172,29 @@ gdn_status_t gdn_decode(const void* q, const void* k, const void* v, const float
                         int use_qk_l2norm, void* o, int* dev_status, void* stream);
 
 /*
+ * gdn_decode_multi -- L tokens per request on the slot-indexed cache (multi-token
+ * decode, e.g. verifying speculative tokens), with optional per-token states.
+ *
+ * GatedDeltaProductMixer.ssm_decode ("Megatron-Core API:
+ * core.ssm.gated_delta_product") takes [n, seq_len, ...] inputs per request and
+ * optional intermediate_ssm_state / intermediate_conv_state outputs; the GDN mixer's
+ * ssm_decode has the same arguments ("Megatron-Core API: core.ssm.gated_delta_net.gdn").
+ * Request i applies its tokens t = 0..L-1 in order to slot batch_indices[i]:
+ *   q, k        [n, L, Hqk, K];  v, o [n, L, Hv, V];  g, beta [n, L, Hv]  (token-major per request)
+ *   intermediate_states  NULL, or [n, L, Hv, K, V] fp32 receiving the state after
+ *               every token (the last one equals the slot's new state).
+ * The slot receives the state after token L - 1.  Padding (-1) and invalid slots:
+ * all L output rows zero, no state read or written, intermediate rows untouched.
+ * Every other rule as gdn_decode (which is this call with L = 1 and no intermediates).
+ */
+gdn_status_t gdn_decode_multi(const void* q, const void* k, const void* v, const float* g,
+                              const void* beta, float* ssm_state, int num_slots,
+                              const int32_t* batch_indices, int n, int L, int Hqk, int Hv, int K,
+                              int V, gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype, float scale,
+                              int use_qk_l2norm, void* o, float* intermediate_states,
+                              int* dev_status, void* stream);
+
+/*
  * Fused gates.  The GDN mixer computes "the per-head log-decay g and the write
  * strength beta" from its gate features and the per-head parameters A_log and
  * dt_bias ("Megatron-Core API: core.ssm.gated_delta_net.gdn",

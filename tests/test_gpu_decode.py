@@ -114,3 +114,55 @@ def test_decode_continues_a_prefill_state():
         o_ref = oracle.decode(q, k, v, g, b, c_ref, idx)
         assert rel_l2(f64(o), o_ref) <= TOL[torch.bfloat16]
     assert rel_l2(f64(c_gpu), c_ref) <= TOL[torch.bfloat16]
+
+
+@pytest.mark.parametrize("dtype,KV", [(torch.bfloat16, 128), (torch.float32, 64)])
+def test_multi_token_decode_with_intermediate_states(dtype, KV):
+    """L tokens per request on the slot cache: outputs, the final slot state and the
+    state after every token match the oracle applied token by token."""
+    from chunked_gated_delta_gdn_gb300 import gated_delta_decode_multi
+    n, L, Hqk, Hv, slots = 12, 5, 2, 4, 20
+    gen = torch.Generator().manual_seed(71)
+    q = torch.randn(n, L, Hqk, KV, generator=gen).to(dtype)
+    k = torch.randn(n, L, Hqk, KV, generator=gen).to(dtype)
+    v = torch.randn(n, L, Hv, KV, generator=gen).to(dtype)
+    g = -torch.nn.functional.softplus(torch.randn(n, L, Hv, generator=gen))
+    beta = torch.sigmoid(torch.randn(n, L, Hv, generator=gen)).to(dtype)
+    cache = 0.1 * torch.randn(slots, Hv, KV, KV, generator=gen)
+    idx = torch.randperm(slots, generator=gen)[:n].to(torch.int32)
+    idx[4] = -1
+    dev = "cuda"
+    state = cache.to(dev)
+    before = state.clone()
+    o, inter = gated_delta_decode_multi(q.to(dev), k.to(dev), v.to(dev), g.to(dev), beta.to(dev),
+                                        state, idx.to(dev), output_intermediate_states=True)
+    torch.cuda.synchronize()
+    ref_cache = f64(cache).copy()
+    o_ref = np.zeros((n, L, Hv, KV))
+    inter_ref = np.zeros((n, L, Hv, KV, KV))
+    for t in range(L):
+        o_ref[:, t] = oracle.decode(q[:, t], k[:, t], v[:, t], g[:, t], beta[:, t], ref_cache, idx)
+        for i in range(n):
+            if idx[i] >= 0:
+                inter_ref[i, t] = ref_cache[idx[i]]
+    real = [i for i in range(n) if idx[i] >= 0]
+    tol = TOL[dtype]
+    e_o = rel_l2(f64(o[real]), o_ref[real])
+    e_s = rel_l2(f64(state), ref_cache)
+    e_i = rel_l2(f64(inter[real]), inter_ref[real])
+    print("multi-token decode %s: o %.3e state %.3e intermediates %.3e" % (dtype, e_o, e_s, e_i))
+    assert e_o <= tol and e_s <= tol and e_i <= tol
+    assert torch.count_nonzero(o[4].float()).item() == 0
+    assert torch.equal(inter[real, L - 1], state[idx[real].long()])
+    untouched = sorted(set(range(slots)) - set(int(x) for x in idx if x >= 0))
+    assert torch.equal(state[untouched], before[untouched])
+    # L = 1 is exactly the single-token entry point
+    s1, s2 = before.clone(), before.clone()
+    o1, _ = gated_delta_decode_multi(q[:, :1].contiguous().to(dev), k[:, :1].contiguous().to(dev),
+                                     v[:, :1].contiguous().to(dev), g[:, :1].contiguous().to(dev),
+                                     beta[:, :1].contiguous().to(dev), s1, idx.to(dev))
+    o2 = gated_delta_decode(q[:, 0].contiguous().to(dev), k[:, 0].contiguous().to(dev),
+                            v[:, 0].contiguous().to(dev), g[:, 0].contiguous().to(dev),
+                            beta[:, 0].contiguous().to(dev), s2, idx.to(dev))
+    torch.cuda.synchronize()
+    assert torch.equal(o1[:, 0], o2) and torch.equal(s1, s2)
