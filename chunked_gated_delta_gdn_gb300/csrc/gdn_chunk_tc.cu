@@ -6,17 +6,18 @@
 // fp32 state lives in TMEM for the whole sequence.  Per chunk (G = in-chunk
 // cumulative log-decay, r_q / r_k = inverse L2 norms, S = state entering the chunk):
 //
-//   D1  = [Q; K] K^T                       M=128 N=64  K=128   (Q K^T and K K^T)
-//   P   = r_q r_k^T * Q K^T * exp(G_i - G_j) * [j <= i]          (bf16, smem)
+//   D1  = [Q; K] [Q; K]^T                  M=128 N=128 K=128   (Q K^T, K K^T; the
+//                                                               diagonal gives |q|^2, |k|^2)
+//   P   = scale r_q r_k^T * Q K^T * exp(G_i - G_j) * [j <= i]    (bf16, smem)
 //   A   = beta r_k r_k^T * K K^T * exp(G_i - G_j) * [j < i]      (fp32, smem)
-//   T   = (I + A)^{-1}                     16 x 16 diagonal blocks, then block rows
+//   T   = (I + A)^{-1}                     16 x 16 diagonal blocks, then block rows (fp32)
 //   W^T = K^T (T diag(beta exp(G) r_k))^T  M=128 N=64  K=64
 //   U^T = V^T (T diag(beta))^T             M=128 N=64  K=64
 //   U'^T = U^T - S^T W^T                   M=128 N=64  K=128   (accumulates on U^T)
 //   O1  = S^T Q^T                          M=128 N=64  K=128
 //   O2  = U'^T P^T                         M=128 N=64  K=64
 //   S^T <- exp(G_last) S^T + (U' * exp(G_last - G) r_k)^T K     M=128 N=128 K=64
-//   o   = scale (exp(G) r_q * O1 + O2)
+//   o   = scale exp(G) r_q * O1 + O2
 //
 // Every product is oriented so M = 128 (value or key features on the TMEM
 // lanes, tokens on the columns).  The CTA is warp-specialised: a prep group
@@ -64,32 +65,34 @@ constexpr uint32_t OFF_P = 163840;      // 2 x P, K-major B [64 i][64 j]
 constexpr uint32_t OFF_U = 180224;      // U'^T bf16, K-major A [128 dv][64 tokens]
 constexpr uint32_t OFF_TW = 196608;     // (T diag(beta exp(G) r_k))^T, MN-major B [64 j][64 i]
 constexpr uint32_t OFF_TU = 204800;     // (T diag(beta))^T, MN-major B
-constexpr uint32_t OFF_VEC = 212992;    // 2 x per-token fp32 vectors [7][64]
+constexpr uint32_t OFF_VEC = 212992;    // 2 x per-token fp32 vectors [8][64]
 constexpr uint32_t VEC_G = 0, VEC_BETA = 64, VEC_RQ = 128, VEC_RK = 192, VEC_SW = 256,
-                   VEC_DL = 320, VEC_QS = 384, VEC_FLOATS = 448;
-constexpr uint32_t OFF_TD = OFF_VEC + 2 * 4 * VEC_FLOATS;  // diagonal blocks of T [4][16][16]
-constexpr uint32_t OFF_YS = OFF_TD + 4 * 1024;             // per-warp 16 x 8 fp32 scratch
-constexpr uint32_t OFF_BAR = OFF_YS + 8 * 512;
+                   VEC_DL = 320, VEC_QS = 384, VEC_H = 448, VEC_FLOATS = 512;
+constexpr uint32_t OFF_TD = OFF_VEC + 2 * 4 * VEC_FLOATS;  // diagonal blocks of T, column-major,
+constexpr int TD_LD = 20;                                  // [4 blocks][16 columns][20 (16 rows + pad)]
+constexpr uint32_t OFF_BAR = OFF_TD + 4 * 16 * TD_LD * 4;
 constexpr uint32_t SMEM_USED = OFF_BAR + 256;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base
 
 constexpr uint32_t STAGE_TX = QK_STAGE + V_STAGE;  // Q + K + V bytes per stage = 48 KB
 
-// TMEM columns (fp32, 128 lanes).  COL_S holds S^T for the whole sequence.
-constexpr uint32_t COL_D1 = 0, COL_W = 64, COL_U = 128 /* 2 x 64 */, COL_O1 = 256,
+// TMEM columns (fp32, 128 lanes).  COL_S holds S^T for the whole sequence.  W^T of chunk
+// c lands in the O1 columns once the output of chunk c - 1 has been read, and the state
+// group moves it to shared memory before O1 of chunk c is computed there.
+constexpr uint32_t COL_D1 = 0 /* 128 */, COL_U = 128 /* 2 x 64 */, COL_O1 = 256, COL_W = COL_O1,
                    COL_O2 = 320, COL_S = 384, TMEM_COLS = 512;
 
 // mbarriers (8 bytes each) at OFF_BAR.
 enum {
   B_FULL = 0,       // [2] TMA stage landed
-  B_MMA_P = 2,      // prep group's MMA commits
+  B_MMA_P = 2,      // prep group's D1 commits
   B_MMA_S = 3,      // state group's MMA commits
-  B_READY = 4,      // [2] prep -> state: chunk ready (vectors, P, U, -W^T)
-  B_W_FREE = 6,     // state -> prep: MMA on -W^T done
-  B_U_FREE = 7,     // [2] state -> prep: U accumulator read
-  B_P_FREE = 9,     // [2] state -> prep: MMA on P done
-  B_VEC_FREE = 11,  // [2] state -> prep: per-token vectors no longer needed
-  B_COUNT = 13
+  B_READY = 4,      // [2] prep -> state: chunk ready; two arrivals: the prep leader (vectors,
+                    //     P, T in shared memory) and the commit of the W / U MMAs
+  B_U_FREE = 6,     // [2] state -> prep: U accumulator read
+  B_P_FREE = 8,     // [2] state -> prep: MMA on P done
+  B_VEC_FREE = 10,  // [2] state -> prep: chunk finished (vectors and the O1 columns free)
+  B_COUNT = 12
 };
 constexpr uint32_t OFF_FLAG = OFF_BAR + 8 * B_COUNT;      // int: a group timed out
 constexpr uint32_t OFF_TSLOT = OFF_FLAG + 8;              // TMEM base address
@@ -116,17 +119,6 @@ __device__ __forceinline__ void store_bf16x8(uint8_t* p, const float* v) {
   u.z = *reinterpret_cast<uint32_t*>(&b2);
   u.w = *reinterpret_cast<uint32_t*>(&b3);
   *reinterpret_cast<uint4*>(p) = u;
-}
-
-__device__ __forceinline__ float sumsq_bf16x8(uint4 u) {
-  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
-  float s = 0.f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 f = __bfloat1622float2(b[i]);
-    s += f.x * f.x + f.y * f.y;
-  }
-  return s;
 }
 
 // Issue the TMA loads of the chunk starting at token t into stage s.
@@ -194,10 +186,29 @@ __device__ __forceinline__ bool flag_set(const int* f) {
 }
 __device__ __forceinline__ void set_flag(int* f) { *reinterpret_cast<volatile int*>(f) = 1; }
 
+// D1 = [Q;K][Q;K]^T of the stage at shared address qk_a: the stage holds Q rows 0-63 and
+// K rows 64-127, so one descriptor serves as A and as the N = 128 B.  Issued by one thread.
+__device__ __forceinline__ void issue_d1(uint32_t d_tmem, uint32_t qk_a, uint64_t* bar) {
+  const uint32_t id1 = idesc_bf16(128, 128, false, false);
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint64_t d = sdesc_sw128(qk_a + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
+    mma_bf16(d_tmem, d, d, id1, ks > 0);
+  }
+  mma_commit(bar);
+}
+
+// log2(x) on the special-function unit
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // =================================================================== prep group
-// Warps 0-7.  For each chunk: gates, norms, D1 = [Q;K]K^T, P, A, T = (I+A)^{-1},
-// W^T and U^T on the tensor core, -W^T to shared memory; then hands the chunk to
-// the state group.
+// Warps 0-7.  For each chunk: D1 = [Q;K][Q;K]^T, gates, norms (from the diagonal of
+// D1), P, A, T = (I+A)^{-1}, then the W^T and U^T MMAs, whose completion (with the
+// leader's arrival) hands the chunk to the state group; the group moves on at once.
 __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int bos, int eos,
                            int nchunks, int h) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -210,10 +221,11 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
   float* sA = reinterpret_cast<float*>(sm + OFF_A);
   float* sTd = reinterpret_cast<float*>(sm + OFF_TD);
   const bool leader = (tid == 0);
-  uint32_t pp = 0;   // parity of B_MMA_P
+  bool d1_ahead = false;   // leader: D1 of this chunk was issued during the previous one
   const int T_total = a.cu_seqlens ? a.T : a.B * a.T;
+  constexpr int kGateWarp = 1;   // not the leader's warp: gates overlap the MMA issue
   float gq[2], bq[2];
-  if (warp == 0) load_gates(a, bos, h, lane, T_total, gq, bq);
+  if (warp == kGateWarp) load_gates(a, bos, h, lane, T_total, gq, bq);
   const bool fused = a.gates.mode == kGatesFused;
   const float expA = fused ? expf(a.gates.A_log[h]) : 0.f;
   const float dtb = fused ? a.gates.dt_bias[h] : 0.f;
@@ -223,7 +235,6 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
     const int t0 = bos + c * kChunk;
     const int L = min(kChunk, eos - t0);
     float* vec = reinterpret_cast<float*>(sm + OFF_VEC) + s * VEC_FLOATS;
-    uint8_t* qk = sm + OFF_QK + s * QK_STAGE;
     const uint32_t qk_a = sbase + OFF_QK + s * QK_STAGE;
     const uint32_t v_a = sbase + OFF_V + s * V_STAGE;
 
@@ -236,21 +247,14 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
     }
     if (group_sync_or(kBarPrep, kPrepThreads, !ok || flag_set(flag))) { if (leader) set_flag(flag); return; }
 
-    // ---- MMA: D1 = [Q;K] K^T, issued as soon as the tiles are in (overlaps gates and norms)
-    if (leader) {
+    // ---- MMA: D1 = [Q;K][Q;K]^T, unless it was issued ahead during the previous chunk
+    if (leader && !d1_ahead) {
       tc_fence_after();
-      const uint32_t id1 = idesc_bf16(128, 64, false, false);
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-        mma_bf16(tbase + COL_D1, sdesc_sw128(qk_a + off, 16, 1024),
-                 sdesc_sw128(qk_a + off + 8192, 16, 1024), id1, ks > 0);
-      }
-      mma_commit(&bars[B_MMA_P]);
+      issue_d1(tbase + COL_D1, qk_a, &bars[B_MMA_P]);
     }
 
     // ---- gates: in-chunk cumulative log-decay and beta; prefetch the next chunk's
-    if (warp == 0) {
+    if (warp == kGateWarp) {
       if (fused) {   // g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b)
         gq[0] = -expA * softplus_f(gq[0] + dtb);
         gq[1] = -expA * softplus_f(gq[1] + dtb);
@@ -270,69 +274,61 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
       vec[VEC_BETA + lane + 32] = lane + 32 < L ? bq[1] : 0.f;
       if (c + 1 < nchunks) load_gates(a, t0 + kChunk, h, lane, T_total, gq, bq);
     }
-    // ---- inverse L2 norms of q and k rows: 4 threads per row, each reading four
-    //      16-byte chunks chosen so a warp's loads fall in distinct banks
-    {
-      const int r = tid >> 2, part = tid & 3;
-      const uint8_t* qrow = qk + (part >> 1) * 16384 + r * 128;
-      float sq = 0.f, sk = 0.f;
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int ch = ((part & 1) * 4 + m) ^ (r & 7);
-        sq += sumsq_bf16x8(*reinterpret_cast<const uint4*>(qrow + 16 * ch));
-        sk += sumsq_bf16x8(*reinterpret_cast<const uint4*>(qrow + 8192 + 16 * ch));
-      }
-      sq += __shfl_xor_sync(0xffffffffu, sq, 1);
-      sq += __shfl_xor_sync(0xffffffffu, sq, 2);
-      sk += __shfl_xor_sync(0xffffffffu, sk, 1);
-      sk += __shfl_xor_sync(0xffffffffu, sk, 2);
-      if (part == 0) {
-        vec[VEC_RQ + r] = a.use_qk_l2norm ? 1.0f / sqrtf(sq + kL2Eps) : 1.0f;
-        vec[VEC_RK + r] = a.use_qk_l2norm ? 1.0f / sqrtf(sk + kL2Eps) : 1.0f;
-      }
-    }
-    group_sync(kBarPrep, kPrepThreads);
-    if (tid < kChunk) {   // per-token scalars while the tensor core works
-      const float gl = vec[VEC_G + L - 1], gt = vec[VEC_G + tid];
-      const float et = ex2(gt), rk = vec[VEC_RK + tid];
-      vec[VEC_SW + tid] = vec[VEC_BETA + tid] * et * rk;
-      vec[VEC_DL + tid] = ex2(gl - gt) * rk;
-      vec[VEC_QS + tid] = a.scale * et * vec[VEC_RQ + tid];
-    }
     if (leader) {
-      ok = mbar_wait(&bars[B_MMA_P], pp, kWaitLimitNs);
+      ok = mbar_wait(&bars[B_MMA_P], (uint32_t)c & 1u, kWaitLimitNs);   // one D1 commit per chunk
       if (c >= 2) ok = ok && mbar_wait(&bars[B_P_FREE + s], (uint32_t)((c - 2) >> 1) & 1u, kWaitLimitNs);
     }
-    pp ^= 1u;
     if (group_sync_or(kBarPrep, kPrepThreads, !ok || flag_set(flag))) { if (leader) set_flag(flag); return; }
     tc_fence_after();
 
-    // ---- P (bf16, rows 0-63 of D1) and A (fp32, rows 64-127 of D1)
+    // ---- inverse L2 norms from the diagonal of D1 (lane i, column i: |q_i|^2 for i < 64,
+    //      |k_{i-64}|^2 above) and the per-token scalars built from them
+    float x[32];
+    tmem_ld32(tbase + lane_off + COL_D1 + 64 + 32 * chalf, x);   // Q K^T | K K^T, for P and A
+    if (chalf == 0) {
+      float dg[32];
+      tmem_ld32(tbase + lane_off + COL_D1 + 32 * quad, dg);
+      float d2 = dg[0];
+#pragma unroll
+      for (int jj = 1; jj < 32; ++jj) d2 = (lane == jj) ? dg[jj] : d2;
+      const float r = a.use_qk_l2norm ? rsqrtf(d2 + kL2Eps) : 1.0f;
+      const int i = row & 63;
+      const float gi = vec[VEC_G + i];
+      if (quad < 2) {
+        vec[VEC_RQ + i] = r;
+        vec[VEC_QS + i] = a.scale * ex2(gi) * r;
+      } else {
+        vec[VEC_RK + i] = r;
+        vec[VEC_SW + i] = vec[VEC_BETA + i] * ex2(gi) * r;
+        vec[VEC_DL + i] = ex2(vec[VEC_G + L - 1] - gi) * r;
+        vec[VEC_H + i] = gi - lg2(r);   // column factor r_k[j] 2^-G_j as an exponent
+      }
+    }
+    group_sync(kBarPrep, kPrepThreads);
+
+    // ---- P (bf16, rows 0-63 of D1, scale folded in) and A (fp32, rows 64-127 of D1); the
+    //      row and column factors enter as exponents: x * 2^(G_i + log2 f_i - H_j)
     {
-      float x[32];
-      tmem_ld32(tbase + lane_off + COL_D1 + 32 * chalf, x);
       const int j0 = 32 * chalf;
-      const float* G = vec + VEC_G;
-      float gj[32], rkj[32];
+      float hj[32];
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
-        const float4 g4 = *reinterpret_cast<const float4*>(G + j0 + 4 * m);
-        const float4 r4 = *reinterpret_cast<const float4*>(vec + VEC_RK + j0 + 4 * m);
-        gj[4 * m] = g4.x; gj[4 * m + 1] = g4.y; gj[4 * m + 2] = g4.z; gj[4 * m + 3] = g4.w;
-        rkj[4 * m] = r4.x; rkj[4 * m + 1] = r4.y; rkj[4 * m + 2] = r4.z; rkj[4 * m + 3] = r4.w;
+        const float4 h4 = *reinterpret_cast<const float4*>(vec + VEC_H + j0 + 4 * m);
+        hj[4 * m] = h4.x; hj[4 * m + 1] = h4.y; hj[4 * m + 2] = h4.z; hj[4 * m + 3] = h4.w;
       }
       const bool zero_tile = ((quad & 1) == 0) && chalf == 1;   // rows 0-31 x cols 32-63
       if (quad < 2) {
         const int i = row;
-        const float gi = G[i], ri = (i < L) ? vec[VEC_RQ + i] : 0.f;
+        // row factor scale r_q[i] (zero past the chunk end: lg2(0) = -inf gives exact zeros)
+        const float ui = vec[VEC_G + i] + lg2((i < L) ? a.scale * vec[VEC_RQ + i] : 0.f);
         if (zero_tile) {
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) x[jj] = 0.f;
         } else {
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) {
-            const int j = j0 + jj;
-            x[jj] = (j <= i) ? ri * rkj[jj] * x[jj] * ex2(gi - gj[jj]) : 0.f;
+            const float e = x[jj] * ex2(ui - hj[jj]);
+            x[jj] = (j0 + jj <= i) ? e : 0.f;
           }
         }
         uint8_t* dst = sm + OFF_P + s * 8192;
@@ -340,15 +336,15 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
         for (int m = 0; m < 4; ++m) store_bf16x8(dst + sw128_offset(i, j0 + 8 * m), &x[8 * m]);
       } else {
         const int i = row - 64;
-        const float gi = G[i], bi = vec[VEC_BETA + i] * vec[VEC_RK + i];
+        const float vi = vec[VEC_G + i] + lg2(vec[VEC_BETA + i] * vec[VEC_RK + i]);   // beta r_k[i]
         if (zero_tile) {
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) x[jj] = 0.f;
         } else {
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) {
-            const int j = j0 + jj;
-            x[jj] = (j < i) ? bi * rkj[jj] * x[jj] * ex2(gi - gj[jj]) : 0.f;
+            const float e = x[jj] * ex2(vi - hj[jj]);
+            x[jj] = (j0 + jj < i) ? e : 0.f;
           }
         }
 #pragma unroll
@@ -359,6 +355,14 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
     }
     tc_fence_before();
     group_sync(kBarPrep, kPrepThreads);
+    // D1 has been read: issue the next chunk's now if its tiles are in already
+    d1_ahead = false;
+    if (leader && c + 1 < nchunks &&
+        mbar_try_wait(&bars[B_FULL + (s ^ 1)], (uint32_t)((c + 1) >> 1) & 1u)) {
+      tc_fence_after();
+      issue_d1(tbase + COL_D1, sbase + OFF_QK + (s ^ 1) * QK_STAGE, &bars[B_MMA_P]);
+      d1_ahead = true;
+    }
 
     // ---- T = (I + A)^{-1}, step 1: the four 16 x 16 diagonal blocks, one column per
     //      thread; each row is a dot product with four partial sums (short dependency chain)
@@ -384,7 +388,9 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
         if (i > jj) x[i] = v;
       }
 #pragma unroll
-      for (int i = 0; i < 16; ++i) sTd[(b * 16 + i) * 16 + jj] = x[i];
+      for (int i4 = 0; i4 < 4; ++i4)
+        *reinterpret_cast<float4*>(&sTd[(b * 16 + jj) * TD_LD + 4 * i4]) =
+            make_float4(x[4 * i4], x[4 * i4 + 1], x[4 * i4 + 2], x[4 * i4 + 3]);
       // row j = 16 b + jj of (T diag(beta exp(G) r_k))^T and (T diag(beta))^T: the zeros
       // before the diagonal block and the diagonal block itself
       const int j = 16 * b + jj;
@@ -403,137 +409,105 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
       }
     }
     group_sync(kBarPrep, kPrepThreads);
-    // ---- step 2: block row b from the rows above it, T[b, :16b] = -T_bb (A[b, :16b] T[:16b, :16b]),
-    //      on the warp-level tf32 MMA: warp w owns columns 8w..8w+7; results overwrite A in place
+    // ---- step 2: block rows b = 1, 2, 3 in turn, T[b, :16b] = -T_bb (A[b, :16b] T[:16b, :16b]),
+    //      in fp32 on the CUDA cores.  Warp w owns columns 2w and 2w + 1 of every 16-column
+    //      block (half-warps), lane r = lane % 16 is the row within block row b.  The A row
+    //      and the diagonal blocks come from shared memory; the off-diagonal T blocks of
+    //      earlier rounds stay in the registers of the lanes that computed them and are read
+    //      with shuffles, so the rounds need no block-wide barrier.
     {
-      const int g8 = lane >> 2, t4 = lane & 3;
-      float* ys = reinterpret_cast<float*>(sm + OFF_YS) + warp * 128;
+      const int r = lane & 15, cl = 2 * warp + (lane >> 4), hb = lane & 16;
+      const float* tdc = sTd + cl * TD_LD;   // column cl of diagonal block q: tdc[16 TD_LD q + row]
+      __nv_bfloat16* tw = reinterpret_cast<__nv_bfloat16*>(sm + OFF_TW);
+      __nv_bfloat16* tu = reinterpret_cast<__nv_bfloat16*>(sm + OFF_TU);
+      float tz10 = 0.f, tz20 = 0.f, tz21 = 0.f;   // T[16 b' + r][16 q + cl] for (b', q) = (1,0), (2,0), (2,1)
 #pragma unroll
       for (int b = 1; b < 4; ++b) {
-        const int nt = warp;
-        const bool active = nt < 2 * b;       // warp-uniform
-        float z[4] = {0.f, 0.f, 0.f, 0.f};
-        if (active) {
-          const int cb = nt >> 1;
-          const int cc = 8 * nt + g8;
-          float y[4] = {0.f, 0.f, 0.f, 0.f};
-          for (int ks = nt; ks < 2 * b; ++ks) {
-            uint32_t af[4], bf[2];
-            af[0] = to_tf32(sA[a_idx(16 * b + g8, 8 * ks + t4)]);
-            af[1] = to_tf32(sA[a_idx(16 * b + g8 + 8, 8 * ks + t4)]);
-            af[2] = to_tf32(sA[a_idx(16 * b + g8, 8 * ks + t4 + 4)]);
-            af[3] = to_tf32(sA[a_idx(16 * b + g8 + 8, 8 * ks + t4 + 4)]);
-            const int k0 = 8 * ks + t4, k1 = k0 + 4;
-            float b0, b1;
-            if ((ks >> 1) == cb) {            // diagonal block of T
-              b0 = sTd[(cb * 16 + (k0 & 15)) * 16 + (cc & 15)];
-              b1 = sTd[(cb * 16 + (k1 & 15)) * 16 + (cc & 15)];
-            } else {                          // T rows of an earlier round, stored over A
-              b0 = sA[a_idx(k0, cc)];
-              b1 = sA[a_idx(k1, cc)];
-            }
-            bf[0] = to_tf32(b0);
-            bf[1] = to_tf32(b1);
-            mma_tf32_16x8x8(y, af, bf);
-          }
-          ys[g8 * 8 + 2 * t4] = y[0];
-          ys[g8 * 8 + 2 * t4 + 1] = y[1];
-          ys[(g8 + 8) * 8 + 2 * t4] = y[2];
-          ys[(g8 + 8) * 8 + 2 * t4 + 1] = y[3];
-          __syncwarp();
+        const int i = 16 * b + r;
+        float ya[3] = {0.f, 0.f, 0.f}, yb[3] = {0.f, 0.f, 0.f};   // two partial sums per output
 #pragma unroll
-          for (int k2 = 0; k2 < 2; ++k2) {
-            uint32_t af[4], bf[2];
-            const float* tb = sTd + (b * 16) * 16 + 8 * k2;
-            af[0] = to_tf32(tb[g8 * 16 + t4]);
-            af[1] = to_tf32(tb[(g8 + 8) * 16 + t4]);
-            af[2] = to_tf32(tb[g8 * 16 + t4 + 4]);
-            af[3] = to_tf32(tb[(g8 + 8) * 16 + t4 + 4]);
-            bf[0] = to_tf32(ys[(8 * k2 + t4) * 8 + g8]);
-            bf[1] = to_tf32(ys[(8 * k2 + t4 + 4) * 8 + g8]);
-            mma_tf32_16x8x8(z, af, bf);
+        for (int g = 0; g < 4 * b; ++g) {
+          const float4 a4 = *reinterpret_cast<const float4*>(&sA[i * 64 + ((g ^ r) << 2)]);
+          const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int m = 4 * g + e, mb = m >> 4, mr = m & 15;
+#pragma unroll
+            for (int q = 0; q <= mb; ++q) {
+              float t;
+              if (q == mb) t = tdc[16 * TD_LD * q + mr];                      // diagonal block
+              else if (mb == 1) t = __shfl_sync(0xffffffffu, tz10, mr + hb);  // block (1, 0)
+              else t = __shfl_sync(0xffffffffu, q == 0 ? tz20 : tz21, mr + hb);
+              if (e & 1) yb[q] = fmaf(av[e], t, yb[q]);
+              else ya[q] = fmaf(av[e], t, ya[q]);
+            }
           }
-          __syncwarp();
         }
-        if (active) {
-          // T block row b, columns c0, c0 + 1 of this tile -> Tw / Tu entries (row = column of T)
-          const int r0 = 16 * b + g8, c0 = 8 * nt + 2 * t4;
-          const float sw0 = vec[VEC_SW + c0], sw1 = vec[VEC_SW + c0 + 1];
-          const float sb0 = vec[VEC_BETA + c0], sb1 = vec[VEC_BETA + c0 + 1];
-          __nv_bfloat16* tw = reinterpret_cast<__nv_bfloat16*>(sm + OFF_TW);
-          __nv_bfloat16* tu = reinterpret_cast<__nv_bfloat16*>(sm + OFF_TU);
-          tw[sw128_offset(c0, r0) >> 1] = __float2bfloat16_rn(-z[0] * sw0);
-          tw[sw128_offset(c0 + 1, r0) >> 1] = __float2bfloat16_rn(-z[1] * sw1);
-          tw[sw128_offset(c0, r0 + 8) >> 1] = __float2bfloat16_rn(-z[2] * sw0);
-          tw[sw128_offset(c0 + 1, r0 + 8) >> 1] = __float2bfloat16_rn(-z[3] * sw1);
-          tu[sw128_offset(c0, r0) >> 1] = __float2bfloat16_rn(-z[0] * sb0);
-          tu[sw128_offset(c0 + 1, r0) >> 1] = __float2bfloat16_rn(-z[1] * sb1);
-          tu[sw128_offset(c0, r0 + 8) >> 1] = __float2bfloat16_rn(-z[2] * sb0);
-          tu[sw128_offset(c0 + 1, r0 + 8) >> 1] = __float2bfloat16_rn(-z[3] * sb1);
-        }
-        if (b < 3) {
-          group_sync(kBarPrep, kPrepThreads);   // all reads of A's block row b are done
-          if (active) {   // fp32 T block for the later rounds, over A in place
-            const int r0 = 16 * b + g8, c0 = 8 * nt + 2 * t4;
-            sA[a_idx(r0, c0)] = -z[0];
-            sA[a_idx(r0, c0 + 1)] = -z[1];
-            sA[a_idx(r0 + 8, c0)] = -z[2];
-            sA[a_idx(r0 + 8, c0 + 1)] = -z[3];
+        float y[3];   // y[q] = (A[b, :16b] T[:16b, :16b])[r][16 q + cl]
+#pragma unroll
+        for (int q = 0; q < 3; ++q) y[q] = ya[q] + yb[q];
+        float za[3] = {0.f, 0.f, 0.f}, zb[3] = {0.f, 0.f, 0.f};   // z = T_bb y
+        const float* tbr = sTd + 16 * TD_LD * b + r;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float tk = tbr[TD_LD * k];
+#pragma unroll
+          for (int q = 0; q < b; ++q) {
+            const float yk = __shfl_sync(0xffffffffu, y[q], k + hb);
+            if (k & 1) zb[q] = fmaf(tk, yk, zb[q]);
+            else za[q] = fmaf(tk, yk, za[q]);
           }
-          group_sync(kBarPrep, kPrepThreads);
+        }
+        float z[3];
+#pragma unroll
+        for (int q = 0; q < 3; ++q) z[q] = za[q] + zb[q];
+        if (b == 1) tz10 = -z[0];
+        if (b == 2) { tz20 = -z[0]; tz21 = -z[1]; }
+        // T[i][j] -> Tw^T / Tu^T at row j = 16 q + cl, column i
+#pragma unroll
+        for (int q = 0; q < b; ++q) {
+          const int j = 16 * q + cl;
+          const uint32_t o = sw128_offset(j, i) >> 1;
+          tw[o] = __float2bfloat16_rn(-z[q] * vec[VEC_SW + j]);
+          tu[o] = __float2bfloat16_rn(-z[q] * vec[VEC_BETA + j]);
         }
       }
     }
     fence_proxy_async_smem();
     group_sync(kBarPrep, kPrepThreads);
 
-    // ---- MMA: W^T = K^T Tw^T, U^T = V^T Tu^T (all operands MN-major); U into its buffer
-    //      once the state group has read the one two chunks back
+    // ---- MMA: W^T = K^T Tw^T into the O1 columns (free once the output of chunk c - 1 has
+    //      been read), U^T = V^T Tu^T into U buffer s (free once the state group has read
+    //      the one of chunk c - 2); all operands MN-major.  The commit and the leader's
+    //      arrival complete READY[s]; the group goes straight on to the next chunk.
     if (leader) {
       bool okl = true;
-      if (c >= 2) okl = mbar_wait(&bars[B_U_FREE + s], (uint32_t)((c - 2) >> 1) & 1u, kWaitLimitNs);
-      if (!okl) set_flag(flag);
-      tc_fence_after();
-      const uint32_t id = idesc_bf16(128, 64, true, true);
+      if (c >= 1) okl = mbar_wait(&bars[B_VEC_FREE + (s ^ 1)], (uint32_t)((c - 1) >> 1) & 1u, kWaitLimitNs);
+      if (okl && c >= 2) okl = mbar_wait(&bars[B_U_FREE + s], (uint32_t)((c - 2) >> 1) & 1u, kWaitLimitNs);
+      if (okl) {
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(128, 64, true, true);
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        mma_bf16(tbase + COL_W, sdesc_sw128(qk_a + 8192 + ks * 2048, 16384, 1024),
-                 sdesc_sw128(sbase + OFF_TW + ks * 2048, 8192, 1024), id, ks > 0);
+        for (int ks = 0; ks < 4; ++ks) {
+          mma_bf16(tbase + COL_W, sdesc_sw128(qk_a + 8192 + ks * 2048, 16384, 1024),
+                   sdesc_sw128(sbase + OFF_TW + ks * 2048, 8192, 1024), id, ks > 0);
+        }
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          mma_bf16(tbase + COL_U + 64 * s, sdesc_sw128(v_a + ks * 2048, 8192, 1024),
+                   sdesc_sw128(sbase + OFF_TU + ks * 2048, 8192, 1024), id, ks > 0);
+        }
+        mma_commit(&bars[B_READY + s]);
+        mbar_arrive(&bars[B_READY + s]);
+      } else {
+        set_flag(flag);
       }
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        mma_bf16(tbase + COL_U + 64 * s, sdesc_sw128(v_a + ks * 2048, 8192, 1024),
-                 sdesc_sw128(sbase + OFF_TU + ks * 2048, 8192, 1024), id, ks > 0);
-      }
-      mma_commit(&bars[B_MMA_P]);
     }
-    if (leader) {
-      ok = mbar_wait(&bars[B_MMA_P], pp, kWaitLimitNs);
-      if (c >= 1) ok = ok && mbar_wait(&bars[B_W_FREE], (uint32_t)(c - 1) & 1u, kWaitLimitNs);
-    }
-    pp ^= 1u;
-    if (group_sync_or(kBarPrep, kPrepThreads, !ok || flag_set(flag))) { if (leader) set_flag(flag); return; }
-    tc_fence_after();
-
-    // ---- -W^T -> bf16 MN-major B operand [dk rows][tokens]
-    {
-      float x[32];
-      tmem_ld32(tbase + lane_off + COL_W + 32 * chalf, x);
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) x[jj] = -x[jj];
-#pragma unroll
-      for (int m = 0; m < 4; ++m)
-        store_bf16x8(sm + OFF_W + sw128_offset(row, 32 * chalf + 8 * m), &x[8 * m]);
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    group_sync(kBarPrep, kPrepThreads);
-    if (leader) mbar_arrive(&bars[B_READY + s]);
   }
 }
 
 // =================================================================== state group
-// Warps 8-11.  For each chunk: S -> bf16 operand and decay of the TMEM state,
+// Warps 8-11.  For each chunk: -W^T and S -> bf16 operands, decay of the TMEM state,
 // U' = U - S W, O1 = S Q^T, O2 = U' P^T, S += (decayed U')^T K, output.
 __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int bos, int eos,
                             int nchunks, int h, int hq, size_t st_off,
@@ -565,6 +539,17 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     if (group_sync_or(kBarState, kStateThreads, !ok || flag_set(flag))) { failed = true; break; }
     tc_fence_after();
 
+    // ---- -W^T (TMEM, O1 columns) -> bf16 MN-major B operand [dk rows][tokens]
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float x[32];
+      tmem_ld32(tbase + lane_off + COL_W + 32 * half, x);
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) x[jj] = -x[jj];
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        store_bf16x8(sm + OFF_W + sw128_offset(row, 32 * half + 8 * m), &x[8 * m]);
+    }
     // ---- S (entry state) -> bf16 A operand S^T [dv rows][dk]; S <- exp(G_last) S in TMEM
     {
       const float dl = ex2(vec[VEC_G + L - 1]);
@@ -596,7 +581,6 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
                  sdesc_sw128(sbase + OFF_S + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
                  sdesc_sw128(sbase + OFF_W + ks * 2048, 8192, 1024), id4, 1);
       }
-      mma_commit(&bars[B_W_FREE]);
       const uint32_t id5 = idesc_bf16(128, 64, false, false);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
@@ -627,7 +611,8 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
       const float dl = vec[VEC_DL + t];
       uint8_t* krow = sm + OFF_QK + s * QK_STAGE + kh * 16384 + 8192 + t * 128;
 #pragma unroll
-      for (int m = 0; m < 8; ++m) {
+      for (int m0 = 0; m0 < 8; ++m0) {
+        const int m = (m0 + t) & 7;   // rows rotate through the 16-byte chunks: no bank conflicts
         uint4 u = *reinterpret_cast<uint4*>(krow + 16 * m);
         __nv_bfloat162* b2 = reinterpret_cast<__nv_bfloat162*>(&u);
 #pragma unroll
@@ -671,21 +656,44 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
       issue_chunk_loads(sm, &bars[B_FULL + s], tq, tk, tv, s, t0 + 2 * kChunk, hq, h);
     }
 
-    // ---- o = scale (exp(G) r_q O1 + O2): a full chunk is staged as a bf16 tile (two
-    //      128-byte-swizzled [64 tokens][64 dv] halves) and written by one TMA store;
-    //      the last, partial chunk of a sequence is stored row by row
+    // ---- o = scale exp(G) r_q O1 + O2 (P carries the scale): a full chunk is staged as a
+    //      bf16 tile (two 128-byte-swizzled [64 tokens][64 dv] halves) and written by one
+    //      TMA store; the last, partial chunk of a sequence is stored row by row
     if (L == kChunk) {
-      uint8_t* stage = sm + OFF_S + (row >> 6) * 8192;
+      // 16x256b loads hand each thread dv (t/4, t/4 + 8 of a 16-lane half) x tokens
+      // (2 (t%4), +1 of each 8-token group): the fragment of stmatrix .trans, which writes
+      // 8 x 8 (token, dv) blocks as 16-byte rows of the swizzled staging tile.  Lane l gives
+      // the row address of block l / 8 (dv 8 (l / 8) of this warp's 32) at token l % 8.
+      const int mblk = lane >> 3, rr = lane & 7;
+      const int d0 = 32 * wq + 8 * mblk;
+      const uint32_t st_base = sbase + OFF_S + (d0 >> 6) * 8192 + rr * 128 +
+                               ((((d0 & 63) >> 3) ^ rr) << 4);
+      const float* qs = vec + VEC_QS + 2 * (lane & 3);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float x[32], y[32];
-        tmem_ld32(tbase + lane_off + COL_O1 + 32 * half, x);
-        tmem_ld32(tbase + lane_off + COL_O2 + 32 * half, y);
+      for (int pass = 0; pass < 2; ++pass) {   // tokens 32 pass .. 32 pass + 31
+        uint32_t a0[16], a1[16], b0[16], b1[16];
+        tmem_ld16x256b_x4(tbase + lane_off + COL_O1 + 32 * pass, a0);                  // dv 0-15
+        tmem_ld16x256b_x4(tbase + lane_off + (16u << 16) + COL_O1 + 32 * pass, a1);    // dv 16-31
+        tmem_ld16x256b_x4(tbase + lane_off + COL_O2 + 32 * pass, b0);
+        tmem_ld16x256b_x4(tbase + lane_off + (16u << 16) + COL_O2 + 32 * pass, b1);
+        tmem_wait_ld();
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int t = 32 * half + jj;
-          *reinterpret_cast<__nv_bfloat16*>(stage + sw128_offset(t, row & 63)) =
-              __float2bfloat16_rn(vec[VEC_QS + t] * x[jj] + a.scale * y[jj]);
+        for (int j = 0; j < 4; ++j) {   // token group 4 pass + j
+          const float2 q2 = *reinterpret_cast<const float2*>(qs + 8 * (4 * pass + j));
+          uint32_t f[4];
+          const uint32_t* src[2] = {a0, a1};
+          const uint32_t* srb[2] = {b0, b1};
+#pragma unroll
+          for (int mm = 0; mm < 4; ++mm) {   // block mm: dv 8 mm .. 8 mm + 7 of the warp
+            const uint32_t* x = src[mm >> 1];
+            const uint32_t* y = srb[mm >> 1];
+            const int k = 4 * j + 2 * (mm & 1);
+            __nv_bfloat162 p = __floats2bfloat162_rn(
+                fmaf(q2.x, __uint_as_float(x[k]), __uint_as_float(y[k])),
+                fmaf(q2.y, __uint_as_float(x[k + 1]), __uint_as_float(y[k + 1])));
+            f[mm] = *reinterpret_cast<uint32_t*>(&p);
+          }
+          stmatrix_x4_trans(st_base + (4 * pass + j) * 1024, f);
         }
       }
       fence_proxy_async_smem();
@@ -706,7 +714,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
           const int t = 32 * half + jj;
           if (t < L)
             out[((size_t)(t0 + t) * a.Hv + h) * DV + row] =
-                __float2bfloat16_rn(vec[VEC_QS + t] * x[jj] + a.scale * y[jj]);
+                __float2bfloat16_rn(fmaf(vec[VEC_QS + t], x[jj], y[jj]));
         }
       }
     }
@@ -737,9 +745,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                     const ChunkArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);   // 1024-byte aligned
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   int* flag = reinterpret_cast<int*>(sm + OFF_FLAG);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_TSLOT);
@@ -779,7 +786,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 
   if (tid == 0) {
-    for (int i = 0; i < B_COUNT; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < B_COUNT; ++i)
+      mbar_init(&bars[i], (i == B_READY || i == B_READY + 1) ? 2u : 1u);
     *flag = 0;
     fence_mbar_init();
   }

@@ -203,6 +203,34 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 16 lanes x 256 bits, 4 repetitions along the columns (16 registers, no wait).  Thread t
+// receives, for repetition j (columns col + 8 j .. col + 8 j + 7):
+//   r[4j + 0] = (lane_base + t/4,     col + 8j + 2 (t%4))   r[4j + 1] = same lane, next column
+//   r[4j + 2] = (lane_base + t/4 + 8, col + 8j + 2 (t%4))   r[4j + 3] = same lane, next column
+// -- the register fragment that stmatrix consumes.  taddr = base | (lane_base << 16) + col.
+__device__ __forceinline__ void tmem_ld16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Four 8 x 8 b16 matrices stored transposed: register i of thread t holds row t/4, columns
+// 2 (t%4) and 2 (t%4) + 1 of matrix i (low half first); lane 8 i + r gives the shared
+// address of memory row r of matrix i, which receives column r of the source (16 bytes).
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t saddr, const uint32_t (&f)[4]) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(
+                   saddr),
+               "r"(f[0]), "r"(f[1]), "r"(f[2]), "r"(f[3])
+               : "memory");
+}
+
 // ------------------------------------------------------------------ MMA
 // D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 inputs, fp32 accumulate),
 // one CTA.  Issued by a single thread.
