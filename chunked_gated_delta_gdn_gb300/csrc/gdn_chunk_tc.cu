@@ -10,7 +10,9 @@
 //                                                               diagonal gives |q|^2, |k|^2)
 //   P   = scale r_q r_k^T * Q K^T * exp(G_i - G_j) * [j <= i]    (bf16, smem)
 //   A   = beta r_k r_k^T * K K^T * exp(G_i - G_j) * [j < i]      (fp32, smem)
-//   T   = (I + A)^{-1}                     16 x 16 diagonal blocks, then block rows (fp32)
+//   T   = (I + A)^{-1}                     16 x 16 diagonal blocks D_b (fp32 substitution),
+//                                           then with L = D A_off (block strictly lower):
+//                                           T = (I - L + L^2 - L^3) D (tf32 warp MMAs)
 //   W^T = K^T (T diag(beta exp(G) r_k))^T  M=128 N=64  K=64
 //   U^T = V^T (T diag(beta))^T             M=128 N=64  K=64
 //   U'^T = U^T - S^T W^T                   M=128 N=64  K=128   (accumulates on U^T)
@@ -22,9 +24,9 @@
 // Every product is oriented so M = 128 (value or key features on the TMEM
 // lanes, tokens on the columns).  The CTA is warp-specialised: a prep group
 // (warps 0-7) builds everything that does not depend on the state -- norms,
-// D1, P, A, T, W, U -- for chunk c + 1 while a state group (warps 8-11) runs
-// the state-dependent part of chunk c (U', O, the state update, the output);
-// they hand chunks over through mbarriers, double-buffering P, U, the per-token
+// D1, P, A, T -- for chunk c + 1 while a state group (warps 8-11) runs the
+// rest of chunk c (the W and U products, U', O, the state update, the output);
+// they hand chunks over through mbarriers, double-buffering P, the per-token
 // vectors and the TMA stages.  These are the chunkwise (WY / UT transform)
 // equations of the gated delta rule with the chunking of the inference kernels
 // ("Megatron-Core API: core.ssm.gated_delta_product", ssm_inference_chunk_size:
@@ -76,10 +78,8 @@ constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the bas
 
 constexpr uint32_t STAGE_TX = QK_STAGE + V_STAGE;  // Q + K + V bytes per stage = 48 KB
 
-// TMEM columns (fp32, 128 lanes).  COL_S holds S^T for the whole sequence.  W^T of chunk
-// c lands in the O1 columns once the output of chunk c - 1 has been read, and the state
-// group moves it to shared memory before O1 of chunk c is computed there.
-constexpr uint32_t COL_D1 = 0 /* 128 */, COL_U = 128 /* 2 x 64 */, COL_O1 = 256, COL_W = COL_O1,
+// TMEM columns (fp32, 128 lanes).  COL_S holds S^T for the whole sequence.
+constexpr uint32_t COL_D1 = 0 /* 128 */, COL_W = 128, COL_U = 192, COL_O1 = 256,
                    COL_O2 = 320, COL_S = 384, TMEM_COLS = 512;
 
 // mbarriers (8 bytes each) at OFF_BAR.
@@ -87,12 +87,11 @@ enum {
   B_FULL = 0,       // [2] TMA stage landed
   B_MMA_P = 2,      // prep group's D1 commits
   B_MMA_S = 3,      // state group's MMA commits
-  B_READY = 4,      // [2] prep -> state: chunk ready; two arrivals: the prep leader (vectors,
-                    //     P, T in shared memory) and the commit of the W / U MMAs
-  B_U_FREE = 6,     // [2] state -> prep: U accumulator read
-  B_P_FREE = 8,     // [2] state -> prep: MMA on P done
-  B_VEC_FREE = 10,  // [2] state -> prep: chunk finished (vectors and the O1 columns free)
-  B_COUNT = 12
+  B_READY = 4,      // [2] prep -> state: chunk ready (vectors, P, Tw / Tu in shared memory)
+  B_WU = 6,         // state: W / U MMAs done (W^T, U^T in TMEM; Tw / Tu free for the prep group)
+  B_P_FREE = 7,     // [2] state -> prep: MMA on P done
+  B_VEC_FREE = 9,   // [2] state -> prep: chunk finished (per-token vectors free)
+  B_COUNT = 11
 };
 constexpr uint32_t OFF_FLAG = OFF_BAR + 8 * B_COUNT;      // int: a group timed out
 constexpr uint32_t OFF_TSLOT = OFF_FLAG + 8;              // TMEM base address
@@ -205,10 +204,47 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 
+// ---- warp-level tf32 MMA operands for the block solve (g = lane / 4, t = lane % 4).
+// Blocks of the 64 x 64 fp32 tile sA (a_idx layout) and of the diagonal blocks of T, stored
+// column-major in sTd ([block][column][row], row stride 1, column stride TD_LD).
+__device__ __forceinline__ float tf32r(float x) { return __uint_as_float(to_tf32(x)); }
+
+// A operand (16 x 8): rows r0 + {g, g + 8}, columns c0 + {t, t + 4} of sA (values already tf32)
+__device__ __forceinline__ void frag_a(const float* sA, int r0, int c0, int g, int t, uint32_t (&a)[4]) {
+  a[0] = __float_as_uint(sA[a_idx(r0 + g, c0 + t)]);
+  a[1] = __float_as_uint(sA[a_idx(r0 + g + 8, c0 + t)]);
+  a[2] = __float_as_uint(sA[a_idx(r0 + g, c0 + t + 4)]);
+  a[3] = __float_as_uint(sA[a_idx(r0 + g + 8, c0 + t + 4)]);
+}
+// B operand (8 x 8): rows k0 + {t, t + 4}, column n0 + g of sA (values already tf32)
+__device__ __forceinline__ void frag_b(const float* sA, int k0, int n0, int g, int t, uint32_t (&b)[2]) {
+  b[0] = __float_as_uint(sA[a_idx(k0 + t, n0 + g)]);
+  b[1] = __float_as_uint(sA[a_idx(k0 + t + 4, n0 + g)]);
+}
+// A operand from diagonal block D: rows g, g + 8, columns c0 + {t, t + 4}
+__device__ __forceinline__ void frag_a_d(const float* D, int c0, int g, int t, uint32_t (&a)[4]) {
+  a[0] = __float_as_uint(D[(c0 + t) * TD_LD + g]);
+  a[1] = __float_as_uint(D[(c0 + t) * TD_LD + g + 8]);
+  a[2] = __float_as_uint(D[(c0 + t + 4) * TD_LD + g]);
+  a[3] = __float_as_uint(D[(c0 + t + 4) * TD_LD + g + 8]);
+}
+// B operand from diagonal block D: rows k0 + {t, t + 4}, column n0 + g
+__device__ __forceinline__ void frag_b_d(const float* D, int k0, int n0, int g, int t, uint32_t (&b)[2]) {
+  b[0] = __float_as_uint(D[(n0 + g) * TD_LD + k0 + t]);
+  b[1] = __float_as_uint(D[(n0 + g) * TD_LD + k0 + t + 4]);
+}
+// Store a 16 x 8 accumulator (rows r0 + {g, g + 8}, columns c0 + 2t, + 1) into sA, tf32-rounded
+__device__ __forceinline__ void store_c(float* sA, int r0, int c0, int g, int t, const float (&c)[4]) {
+  sA[a_idx(r0 + g, c0 + 2 * t)] = tf32r(c[0]);
+  sA[a_idx(r0 + g, c0 + 2 * t + 1)] = tf32r(c[1]);
+  sA[a_idx(r0 + g + 8, c0 + 2 * t)] = tf32r(c[2]);
+  sA[a_idx(r0 + g + 8, c0 + 2 * t + 1)] = tf32r(c[3]);
+}
+
 // =================================================================== prep group
 // Warps 0-7.  For each chunk: D1 = [Q;K][Q;K]^T, gates, norms (from the diagonal of
-// D1), P, A, T = (I+A)^{-1}, then the W^T and U^T MMAs, whose completion (with the
-// leader's arrival) hands the chunk to the state group; the group moves on at once.
+// D1), P, A, and T = (I+A)^{-1} as bf16 Tw / Tu operands; then hands the chunk to the
+// state group and moves on.
 __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int bos, int eos,
                            int nchunks, int h) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -236,7 +272,6 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
     const int L = min(kChunk, eos - t0);
     float* vec = reinterpret_cast<float*>(sm + OFF_VEC) + s * VEC_FLOATS;
     const uint32_t qk_a = sbase + OFF_QK + s * QK_STAGE;
-    const uint32_t v_a = sbase + OFF_V + s * V_STAGE;
 
     // ---- per-token vectors of chunk c - 2 released; this chunk's tiles landed
     // (one thread polls each mbarrier; the rest of the group sleeps in the named barrier)
@@ -354,7 +389,8 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
       }
     }
     tc_fence_before();
-    group_sync(kBarPrep, kPrepThreads);
+    if (leader && c >= 1) ok = mbar_wait(&bars[B_WU], (uint32_t)(c - 1) & 1u, kWaitLimitNs);   // Tw, Tu free
+    if (group_sync_or(kBarPrep, kPrepThreads, !ok || flag_set(flag))) { if (leader) set_flag(flag); return; }
     // D1 has been read: issue the next chunk's now if its tiles are in already
     d1_ahead = false;
     if (leader && c + 1 < nchunks &&
@@ -365,32 +401,27 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
     }
 
     // ---- T = (I + A)^{-1}, step 1: the four 16 x 16 diagonal blocks, one column per
-    //      thread; each row is a dot product with four partial sums (short dependency chain)
+    //      thread, by right-looking substitution: once x[m] is final its multiples of
+    //      column m of A leave the rows below (a one-FMA dependency chain per step)
     if (tid < 64) {
       const int b = tid >> 4, jj = tid & 15;
+      // A[16 b + i][16 b + m] = sA[1024 b + 64 i + 4 ((4 b ^ (i & 12)) | ((m / 4) ^ (i & 3))) + m % 4]
+      const float* ab[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) ab[k] = sA + 1024 * b + (((4 * b) ^ (4 * k)) << 2);
       float x[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) x[i] = (i == jj) ? 1.f : 0.f;
 #pragma unroll
-      for (int i = 1; i < 16; ++i) {
-        float p[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int m = 0; m < 15; ++m) {
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          if (4 * g < i) {
-            const float4 a4 = *reinterpret_cast<const float4*>(&sA[a_idx(16 * b + i, 16 * b + 4 * g)]);
-            if (4 * g + 0 < i) p[0] += a4.x * x[4 * g + 0];
-            if (4 * g + 1 < i) p[1] += a4.y * x[4 * g + 1];
-            if (4 * g + 2 < i) p[2] += a4.z * x[4 * g + 2];
-            if (4 * g + 3 < i) p[3] += a4.w * x[4 * g + 3];
-          }
-        }
-        const float v = -((p[0] + p[1]) + (p[2] + p[3]));
-        if (i > jj) x[i] = v;
+        for (int i = m + 1; i < 16; ++i)
+          x[i] = fmaf(-ab[i >> 2][64 * i + ((((m >> 2) ^ (i & 3))) << 2) + (m & 3)], x[m], x[i]);
       }
 #pragma unroll
       for (int i4 = 0; i4 < 4; ++i4)
-        *reinterpret_cast<float4*>(&sTd[(b * 16 + jj) * TD_LD + 4 * i4]) =
-            make_float4(x[4 * i4], x[4 * i4 + 1], x[4 * i4 + 2], x[4 * i4 + 3]);
+        *reinterpret_cast<float4*>(&sTd[(b * 16 + jj) * TD_LD + 4 * i4]) =   // tf32 MMA operand
+            make_float4(tf32r(x[4 * i4]), tf32r(x[4 * i4 + 1]), tf32r(x[4 * i4 + 2]), tf32r(x[4 * i4 + 3]));
       // row j = 16 b + jj of (T diag(beta exp(G) r_k))^T and (T diag(beta))^T: the zeros
       // before the diagonal block and the diagonal block itself
       const int j = 16 * b + jj;
@@ -409,106 +440,125 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
       }
     }
     group_sync(kBarPrep, kPrepThreads);
-    // ---- step 2: block rows b = 1, 2, 3 in turn, T[b, :16b] = -T_bb (A[b, :16b] T[:16b, :16b]),
-    //      in fp32 on the CUDA cores.  Warp w owns columns 2w and 2w + 1 of every 16-column
-    //      block (half-warps), lane r = lane % 16 is the row within block row b.  The A row
-    //      and the diagonal blocks come from shared memory; the off-diagonal T blocks of
-    //      earlier rounds stay in the registers of the lanes that computed them and are read
-    //      with shuffles, so the rounds need no block-wide barrier.
+    // ---- step 2: the off-diagonal blocks.  With D = diag(D_0..D_3) and L = D A_off (block
+    //      strictly lower, so L^4 = 0), (I + A)^{-1} = (I + L)^{-1} D = (I - L + L^2 - L^3) D.
+    //      Three levels of independent 16 x 16 products on the warp-level tf32 MMA, one
+    //      16 x 8 column half per task; intermediate blocks live in the free parts of sA:
+    //      L_bq over A_bq, (L^2)_bq in the upper-triangle block (q, b).
     {
-      const int r = lane & 15, cl = 2 * warp + (lane >> 4), hb = lane & 16;
-      const float* tdc = sTd + cl * TD_LD;   // column cl of diagonal block q: tdc[16 TD_LD q + row]
-      __nv_bfloat16* tw = reinterpret_cast<__nv_bfloat16*>(sm + OFF_TW);
-      __nv_bfloat16* tu = reinterpret_cast<__nv_bfloat16*>(sm + OFF_TU);
-      float tz10 = 0.f, tz20 = 0.f, tz21 = 0.f;   // T[16 b' + r][16 q + cl] for (b', q) = (1,0), (2,0), (2,1)
+      const int g = lane >> 2, t = lane & 3;
+      // level 1: L_bq = D_b A_bq for the six blocks (b, q), both column halves: 12 tasks
+      for (int task = warp; task < 12; task += 8) {
+        const int pr = task >> 1, nt = task & 1;
+        const int b = pr < 1 ? 1 : (pr < 3 ? 2 : 3);
+        const int q = pr < 1 ? pr : (pr < 3 ? pr - 1 : pr - 3);
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int b = 1; b < 4; ++b) {
-        const int i = 16 * b + r;
-        float ya[3] = {0.f, 0.f, 0.f}, yb[3] = {0.f, 0.f, 0.f};   // two partial sums per output
+        for (int ks = 0; ks < 2; ++ks) {
+          uint32_t af[4], bf[2];
+          frag_a_d(sTd + b * 16 * TD_LD, 8 * ks, g, t, af);
+          bf[0] = to_tf32(sA[a_idx(16 * b + 8 * ks + t, 16 * q + 8 * nt + g)]);
+          bf[1] = to_tf32(sA[a_idx(16 * b + 8 * ks + t + 4, 16 * q + 8 * nt + g)]);
+          mma_tf32_16x8x8(c, af, bf);
+        }
+        __syncwarp();   // this column half of A_bq has been read (only by this warp)
+        store_c(sA, 16 * b, 16 * q + 8 * nt, g, t, c);
+      }
+      group_sync(kBarPrep, kPrepThreads);
+      // level 2: (L^2)_20 = L_21 L_10, (L^2)_31 = L_32 L_21, (L^2)_30 = L_31 L_10 + L_32 L_20
+      if (warp < 6) {
+        const int pr = warp >> 1, nt = warp & 1;   // pr 0: (3,0) (two products), 1: (2,0), 2: (3,1)
+        const int b = pr == 1 ? 2 : 3, q = pr == 2 ? 1 : 0;
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int g = 0; g < 4 * b; ++g) {
-          const float4 a4 = *reinterpret_cast<const float4*>(&sA[i * 64 + ((g ^ r) << 2)]);
-          const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+        for (int term = 0; term < 2; ++term) {
+          if (term == 1 && pr != 0) break;
+          const int m = (pr == 0) ? (term == 0 ? 1 : 2) : b - 1;   // inner block: L_bm L_mq
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks) {
+            uint32_t af[4], bf[2];
+            frag_a(sA, 16 * b, 16 * m + 8 * ks, g, t, af);
+            frag_b(sA, 16 * m + 8 * ks, 16 * q + 8 * nt, g, t, bf);
+            mma_tf32_16x8x8(c, af, bf);
+          }
+        }
+        store_c(sA, 16 * q, 16 * b + 8 * nt, g, t, c);   // upper-triangle block (q, b)
+      }
+      group_sync(kBarPrep, kPrepThreads);
+      // level 3: T_bq = X_bq D_q with X = -L + L^2 - L^3 (L^3 only in block (3, 0):
+      // (L^3)_30 = L_32 (L^2)_20, computed whole by each of the two warps of that block into
+      // its own scratch, the diagonal block (1, 1) or (2, 2) of sA, free since step 1),
+      // written as Tw^T / Tu^T entries (row j = column of T).  Task pairs pr (two column
+      // halves each) in the order (1,0) (2,1) (3,0) (3,1) (3,2) (2,0): warps 4-7 take one
+      // task each and get the heavier blocks, warps 0-3 two light ones.
+      for (int task = warp; task < 12; task += 8) {
+        const int pr = task >> 1, nt = task & 1;
+        const int b = (3065 >> (2 * pr)) & 3, q = (580 >> (2 * pr)) & 3;
+        const bool l3 = (b == 3 && q == 0);
+        const int sc = 16 * (1 + nt);   // scratch: diagonal block (1 + nt, 1 + nt)
+        if (l3) {
+          // (L^3)_30 = L_32 (L^2)_20; (L^2)_20 is stored at block (0, 2)
+#pragma unroll
+          for (int n2 = 0; n2 < 2; ++n2) {
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+              uint32_t af[4], bf[2];
+              frag_a(sA, 48, 32 + 8 * ks, g, t, af);                  // L_32
+              bf[0] = __float_as_uint(sA[a_idx(8 * ks + t, 32 + 8 * n2 + g)]);       // (L^2)_20[k][n]
+              bf[1] = __float_as_uint(sA[a_idx(8 * ks + t + 4, 32 + 8 * n2 + g)]);
+              mma_tf32_16x8x8(c, af, bf);
+            }
+            store_c(sA, sc, sc + 8 * n2, g, t, c);
+          }
+          __syncwarp();
+        }
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+          // A operand: X_bq[rows][columns 8 ks + {t, t + 4}]
+          float xa[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int m = 4 * g + e, mb = m >> 4, mr = m & 15;
-#pragma unroll
-            for (int q = 0; q <= mb; ++q) {
-              float t;
-              if (q == mb) t = tdc[16 * TD_LD * q + mr];                      // diagonal block
-              else if (mb == 1) t = __shfl_sync(0xffffffffu, tz10, mr + hb);  // block (1, 0)
-              else t = __shfl_sync(0xffffffffu, q == 0 ? tz20 : tz21, mr + hb);
-              if (e & 1) yb[q] = fmaf(av[e], t, yb[q]);
-              else ya[q] = fmaf(av[e], t, ya[q]);
-            }
+            const int rr = g + 8 * (e & 1), cc = 8 * ks + t + 4 * (e >> 1);
+            float v = -sA[a_idx(16 * b + rr, 16 * q + cc)];                      // -L_bq
+            if (b - q >= 2) v += sA[a_idx(16 * q + rr, 16 * b + cc)];           // + (L^2)_bq
+            if (l3) v -= sA[a_idx(sc + rr, sc + cc)];                           // - (L^3)_30
+            xa[e] = v;
           }
+          uint32_t af[4] = {to_tf32(xa[0]), to_tf32(xa[1]), to_tf32(xa[2]), to_tf32(xa[3])};
+          uint32_t bf[2];
+          frag_b_d(sTd + q * 16 * TD_LD, 8 * ks, 8 * nt, g, t, bf);
+          mma_tf32_16x8x8(c, af, bf);
         }
-        float y[3];   // y[q] = (A[b, :16b] T[:16b, :16b])[r][16 q + cl]
-#pragma unroll
-        for (int q = 0; q < 3; ++q) y[q] = ya[q] + yb[q];
-        float za[3] = {0.f, 0.f, 0.f}, zb[3] = {0.f, 0.f, 0.f};   // z = T_bb y
-        const float* tbr = sTd + 16 * TD_LD * b + r;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float tk = tbr[TD_LD * k];
-#pragma unroll
-          for (int q = 0; q < b; ++q) {
-            const float yk = __shfl_sync(0xffffffffu, y[q], k + hb);
-            if (k & 1) zb[q] = fmaf(tk, yk, zb[q]);
-            else za[q] = fmaf(tk, yk, za[q]);
-          }
-        }
-        float z[3];
-#pragma unroll
-        for (int q = 0; q < 3; ++q) z[q] = za[q] + zb[q];
-        if (b == 1) tz10 = -z[0];
-        if (b == 2) { tz20 = -z[0]; tz21 = -z[1]; }
-        // T[i][j] -> Tw^T / Tu^T at row j = 16 q + cl, column i
-#pragma unroll
-        for (int q = 0; q < b; ++q) {
-          const int j = 16 * q + cl;
-          const uint32_t o = sw128_offset(j, i) >> 1;
-          tw[o] = __float2bfloat16_rn(-z[q] * vec[VEC_SW + j]);
-          tu[o] = __float2bfloat16_rn(-z[q] * vec[VEC_BETA + j]);
-        }
+        // T[i][j] -> Tw^T / Tu^T at row j = 16 q + 8 nt + 2 t (+1), column i = 16 b + g (+8)
+        __nv_bfloat16* tw = reinterpret_cast<__nv_bfloat16*>(sm + OFF_TW);
+        __nv_bfloat16* tu = reinterpret_cast<__nv_bfloat16*>(sm + OFF_TU);
+        const int i0 = 16 * b + g, j0 = 16 * q + 8 * nt + 2 * t;
+        const float sw0 = vec[VEC_SW + j0], sw1 = vec[VEC_SW + j0 + 1];
+        const float sb0 = vec[VEC_BETA + j0], sb1 = vec[VEC_BETA + j0 + 1];
+        tw[sw128_offset(j0, i0) >> 1] = __float2bfloat16_rn(c[0] * sw0);
+        tw[sw128_offset(j0 + 1, i0) >> 1] = __float2bfloat16_rn(c[1] * sw1);
+        tw[sw128_offset(j0, i0 + 8) >> 1] = __float2bfloat16_rn(c[2] * sw0);
+        tw[sw128_offset(j0 + 1, i0 + 8) >> 1] = __float2bfloat16_rn(c[3] * sw1);
+        tu[sw128_offset(j0, i0) >> 1] = __float2bfloat16_rn(c[0] * sb0);
+        tu[sw128_offset(j0 + 1, i0) >> 1] = __float2bfloat16_rn(c[1] * sb1);
+        tu[sw128_offset(j0, i0 + 8) >> 1] = __float2bfloat16_rn(c[2] * sb0);
+        tu[sw128_offset(j0 + 1, i0 + 8) >> 1] = __float2bfloat16_rn(c[3] * sb1);
       }
     }
     fence_proxy_async_smem();
     group_sync(kBarPrep, kPrepThreads);
 
-    // ---- MMA: W^T = K^T Tw^T into the O1 columns (free once the output of chunk c - 1 has
-    //      been read), U^T = V^T Tu^T into U buffer s (free once the state group has read
-    //      the one of chunk c - 2); all operands MN-major.  The commit and the leader's
-    //      arrival complete READY[s]; the group goes straight on to the next chunk.
-    if (leader) {
-      bool okl = true;
-      if (c >= 1) okl = mbar_wait(&bars[B_VEC_FREE + (s ^ 1)], (uint32_t)((c - 1) >> 1) & 1u, kWaitLimitNs);
-      if (okl && c >= 2) okl = mbar_wait(&bars[B_U_FREE + s], (uint32_t)((c - 2) >> 1) & 1u, kWaitLimitNs);
-      if (okl) {
-        tc_fence_after();
-        const uint32_t id = idesc_bf16(128, 64, true, true);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          mma_bf16(tbase + COL_W, sdesc_sw128(qk_a + 8192 + ks * 2048, 16384, 1024),
-                   sdesc_sw128(sbase + OFF_TW + ks * 2048, 8192, 1024), id, ks > 0);
-        }
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          mma_bf16(tbase + COL_U + 64 * s, sdesc_sw128(v_a + ks * 2048, 8192, 1024),
-                   sdesc_sw128(sbase + OFF_TU + ks * 2048, 8192, 1024), id, ks > 0);
-        }
-        mma_commit(&bars[B_READY + s]);
-        mbar_arrive(&bars[B_READY + s]);
-      } else {
-        set_flag(flag);
-      }
-    }
+    // ---- hand chunk c to the state group (which runs the W / U products) and move on
+    if (leader) mbar_arrive(&bars[B_READY + s]);
   }
 }
 
 // =================================================================== state group
-// Warps 8-11.  For each chunk: -W^T and S -> bf16 operands, decay of the TMEM state,
-// U' = U - S W, O1 = S Q^T, O2 = U' P^T, S += (decayed U')^T K, output.
+// Warps 8-11.  For each chunk: W^T = K^T Tw^T and U^T = V^T Tu^T, -W^T and S -> bf16
+// operands, decay of the TMEM state, U' = U - S W, O1 = S Q^T, O2 = U' P^T,
+// S += (decayed U')^T K, output.
 __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int bos, int eos,
                             int nchunks, int h, int hq, size_t st_off,
                             const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
@@ -528,8 +578,9 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     const int s = c & 1;
     const int t0 = bos + c * kChunk;
     const int L = min(kChunk, eos - t0);
-    const float* vec = reinterpret_cast<const float*>(sm + OFF_VEC) + s * VEC_FLOATS;
+    float* vec = reinterpret_cast<float*>(sm + OFF_VEC) + s * VEC_FLOATS;
     const uint32_t qk_a = sbase + OFF_QK + s * QK_STAGE;
+    const uint32_t v_a = sbase + OFF_V + s * V_STAGE;
 
     bool ok = true;
     if (leader) {
@@ -539,16 +590,21 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     if (group_sync_or(kBarState, kStateThreads, !ok || flag_set(flag))) { failed = true; break; }
     tc_fence_after();
 
-    // ---- -W^T (TMEM, O1 columns) -> bf16 MN-major B operand [dk rows][tokens]
+    // ---- MMA: W^T = K^T Tw^T, U^T = V^T Tu^T (all operands MN-major); they run while the
+    //      state is converted below
+    if (leader) {
+      const uint32_t id = idesc_bf16(128, 64, true, true);
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float x[32];
-      tmem_ld32(tbase + lane_off + COL_W + 32 * half, x);
+      for (int ks = 0; ks < 4; ++ks) {
+        mma_bf16(tbase + COL_W, sdesc_sw128(qk_a + 8192 + ks * 2048, 16384, 1024),
+                 sdesc_sw128(sbase + OFF_TW + ks * 2048, 8192, 1024), id, ks > 0);
+      }
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj) x[jj] = -x[jj];
-#pragma unroll
-      for (int m = 0; m < 4; ++m)
-        store_bf16x8(sm + OFF_W + sw128_offset(row, 32 * half + 8 * m), &x[8 * m]);
+      for (int ks = 0; ks < 4; ++ks) {
+        mma_bf16(tbase + COL_U, sdesc_sw128(v_a + ks * 2048, 8192, 1024),
+                 sdesc_sw128(sbase + OFF_TU + ks * 2048, 8192, 1024), id, ks > 0);
+      }
+      mma_commit(&bars[B_WU]);
     }
     // ---- S (entry state) -> bf16 A operand S^T [dv rows][dk]; S <- exp(G_last) S in TMEM
     {
@@ -567,6 +623,20 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
         tmem_st32(tbase + lane_off + col, x);
       }
     }
+    if (leader) ok = mbar_wait(&bars[B_WU], (uint32_t)c & 1u, kWaitLimitNs);
+    if (group_sync_or(kBarState, kStateThreads, !ok || flag_set(flag))) { failed = true; break; }
+    tc_fence_after();
+    // ---- -W^T (TMEM) -> bf16 MN-major B operand [dk rows][tokens]
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float x[32];
+      tmem_ld32(tbase + lane_off + COL_W + 32 * half, x);
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) x[jj] = -x[jj];
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        store_bf16x8(sm + OFF_W + sw128_offset(row, 32 * half + 8 * m), &x[8 * m]);
+    }
     fence_proxy_async_smem();
     tc_fence_before();
     group_sync(kBarState, kStateThreads);
@@ -577,7 +647,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
       const uint32_t id4 = idesc_bf16(128, 64, false, true);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
-        mma_bf16(tbase + COL_U + 64 * s,
+        mma_bf16(tbase + COL_U,
                  sdesc_sw128(sbase + OFF_S + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
                  sdesc_sw128(sbase + OFF_W + ks * 2048, 8192, 1024), id4, 1);
       }
@@ -601,7 +671,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       float x[32];
-      tmem_ld32(tbase + lane_off + COL_U + 64 * s + 32 * half, x);
+      tmem_ld32(tbase + lane_off + COL_U + 32 * half, x);
 #pragma unroll
       for (int m = 0; m < 4; ++m)
         store_bf16x8(sm + OFF_U + sw128_offset(row, 32 * half + 8 * m), &x[8 * m]);
@@ -629,7 +699,6 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
 
     // ---- MMA: O2 = U'^T P^T, S^T += Ut^T K
     if (leader) {
-      mbar_arrive(&bars[B_U_FREE + s]);
       tc_fence_after();
       const uint32_t id6 = idesc_bf16(128, 64, false, false);
 #pragma unroll
@@ -656,7 +725,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
       issue_chunk_loads(sm, &bars[B_FULL + s], tq, tk, tv, s, t0 + 2 * kChunk, hq, h);
     }
 
-    // ---- o = scale exp(G) r_q O1 + O2 (P carries the scale): a full chunk is staged as a
+    // ---- o = scale exp(G) r_q O1 + O2 (P carries scale r_q): a full chunk is staged as a
     //      bf16 tile (two 128-byte-swizzled [64 tokens][64 dv] halves) and written by one
     //      TMA store; the last, partial chunk of a sequence is stored row by row
     if (L == kChunk) {
@@ -668,7 +737,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
       const int d0 = 32 * wq + 8 * mblk;
       const uint32_t st_base = sbase + OFF_S + (d0 >> 6) * 8192 + rr * 128 +
                                ((((d0 & 63) >> 3) ^ rr) << 4);
-      const float* qs = vec + VEC_QS + 2 * (lane & 3);
+      const float* qs = vec + VEC_QS + 2 * (lane & 3);   // scale r_q exp(G): factor of O1
 #pragma unroll
       for (int pass = 0; pass < 2; ++pass) {   // tokens 32 pass .. 32 pass + 31
         uint32_t a0[16], a1[16], b0[16], b1[16];
@@ -786,8 +855,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 
   if (tid == 0) {
-    for (int i = 0; i < B_COUNT; ++i)
-      mbar_init(&bars[i], (i == B_READY || i == B_READY + 1) ? 2u : 1u);
+    for (int i = 0; i < B_COUNT; ++i) mbar_init(&bars[i], 1);
     *flag = 0;
     fence_mbar_init();
   }
