@@ -10,9 +10,9 @@
 //                                                               diagonal gives |q|^2, |k|^2)
 //   P   = scale r_q r_k^T * Q K^T * exp(G_i - G_j) * [j <= i]    (bf16, smem)
 //   A   = beta r_k r_k^T * K K^T * exp(G_i - G_j) * [j < i]      (fp32, smem)
-//   T   = (I + A)^{-1}                     16 x 16 diagonal blocks D_b (fp32 substitution),
-//                                           then with L = D A_off (block strictly lower):
-//                                           T = (I - L + L^2 - L^3) D (tf32 warp MMAs)
+//   T   = (I + A)^{-1}                     with 16 x 16 diagonal blocks D_b = (I + A_bb)^-1 and
+//                                           L = D A_off (block strictly lower):
+//                                           T = (I - L + L^2 - L^3) D      (fp32, CUDA cores)
 //   W^T = K^T (T diag(beta exp(G) r_k))^T  M=128 N=64  K=64
 //   U^T = V^T (T diag(beta))^T             M=128 N=64  K=64
 //   U'^T = U^T - S^T W^T                   M=128 N=64  K=128   (accumulates on U^T)
@@ -204,43 +204,6 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 
-// ---- warp-level tf32 MMA operands for the block solve (g = lane / 4, t = lane % 4).
-// Blocks of the 64 x 64 fp32 tile sA (a_idx layout) and of the diagonal blocks of T, stored
-// column-major in sTd ([block][column][row], row stride 1, column stride TD_LD).
-__device__ __forceinline__ float tf32r(float x) { return __uint_as_float(to_tf32(x)); }
-
-// A operand (16 x 8): rows r0 + {g, g + 8}, columns c0 + {t, t + 4} of sA (values already tf32)
-__device__ __forceinline__ void frag_a(const float* sA, int r0, int c0, int g, int t, uint32_t (&a)[4]) {
-  a[0] = __float_as_uint(sA[a_idx(r0 + g, c0 + t)]);
-  a[1] = __float_as_uint(sA[a_idx(r0 + g + 8, c0 + t)]);
-  a[2] = __float_as_uint(sA[a_idx(r0 + g, c0 + t + 4)]);
-  a[3] = __float_as_uint(sA[a_idx(r0 + g + 8, c0 + t + 4)]);
-}
-// B operand (8 x 8): rows k0 + {t, t + 4}, column n0 + g of sA (values already tf32)
-__device__ __forceinline__ void frag_b(const float* sA, int k0, int n0, int g, int t, uint32_t (&b)[2]) {
-  b[0] = __float_as_uint(sA[a_idx(k0 + t, n0 + g)]);
-  b[1] = __float_as_uint(sA[a_idx(k0 + t + 4, n0 + g)]);
-}
-// A operand from diagonal block D: rows g, g + 8, columns c0 + {t, t + 4}
-__device__ __forceinline__ void frag_a_d(const float* D, int c0, int g, int t, uint32_t (&a)[4]) {
-  a[0] = __float_as_uint(D[(c0 + t) * TD_LD + g]);
-  a[1] = __float_as_uint(D[(c0 + t) * TD_LD + g + 8]);
-  a[2] = __float_as_uint(D[(c0 + t + 4) * TD_LD + g]);
-  a[3] = __float_as_uint(D[(c0 + t + 4) * TD_LD + g + 8]);
-}
-// B operand from diagonal block D: rows k0 + {t, t + 4}, column n0 + g
-__device__ __forceinline__ void frag_b_d(const float* D, int k0, int n0, int g, int t, uint32_t (&b)[2]) {
-  b[0] = __float_as_uint(D[(n0 + g) * TD_LD + k0 + t]);
-  b[1] = __float_as_uint(D[(n0 + g) * TD_LD + k0 + t + 4]);
-}
-// Store a 16 x 8 accumulator (rows r0 + {g, g + 8}, columns c0 + 2t, + 1) into sA, tf32-rounded
-__device__ __forceinline__ void store_c(float* sA, int r0, int c0, int g, int t, const float (&c)[4]) {
-  sA[a_idx(r0 + g, c0 + 2 * t)] = tf32r(c[0]);
-  sA[a_idx(r0 + g, c0 + 2 * t + 1)] = tf32r(c[1]);
-  sA[a_idx(r0 + g + 8, c0 + 2 * t)] = tf32r(c[2]);
-  sA[a_idx(r0 + g + 8, c0 + 2 * t + 1)] = tf32r(c[3]);
-}
-
 // =================================================================== prep group
 // Warps 0-7.  For each chunk: D1 = [Q;K][Q;K]^T, gates, norms (from the diagonal of
 // D1), P, A, and T = (I+A)^{-1} as bf16 Tw / Tu operands; then hands the chunk to the
@@ -400,151 +363,130 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
       d1_ahead = true;
     }
 
-    // ---- T = (I + A)^{-1}, step 1: the four 16 x 16 diagonal blocks, one column per
-    //      thread, by right-looking substitution: once x[m] is final its multiples of
-    //      column m of A leave the rows below (a one-FMA dependency chain per step)
-    if (tid < 64) {
-      const int b = tid >> 4, jj = tid & 15;
-      // A[16 b + i][16 b + m] = sA[1024 b + 64 i + 4 ((4 b ^ (i & 12)) | ((m / 4) ^ (i & 3))) + m % 4]
+    // ---- T = (I + A)^{-1} in fp32 on the CUDA cores.  With D_b = (I + A_bb)^{-1} and
+    //      L = D A_off (block strictly lower, so L^4 = 0): T = (I - L + L^2 - L^3) D.
+    // step 1: per block row b, one right-looking substitution (I + A_bb) X = R for the
+    //      right-hand sides R = [I | A_b0 | .. | A_b,b-1], one column per thread (16 (b + 1)
+    //      columns in block row b, 160 in all): X = [D_b | L_b0 | ..].  D_b goes to sTd and
+    //      to the diagonal blocks of Tw / Tu; L_bq replaces A_bq column by column.
+    if (tid < 160) {
+      const int b = tid < 16 ? 0 : (tid < 48 ? 1 : (tid < 96 ? 2 : 3));
+      const int j = tid - 8 * b * (b + 1);            // column of R
+      const bool ident = j < 16;
+      const int cq = j - 16;                          // column of A: block q = cq / 16, c = cq % 16
+      // A[16 b + i][16 b + m] = ab[i / 4][64 i + 4 ((m / 4) ^ (i % 4)) + m % 4]
       const float* ab[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) ab[k] = sA + 1024 * b + (((4 * b) ^ (4 * k)) << 2);
       float x[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) x[i] = (i == jj) ? 1.f : 0.f;
+      for (int i = 0; i < 16; ++i) x[i] = ident ? ((i == j) ? 1.f : 0.f) : sA[a_idx(16 * b + i, cq)];
 #pragma unroll
       for (int m = 0; m < 15; ++m) {
 #pragma unroll
         for (int i = m + 1; i < 16; ++i)
           x[i] = fmaf(-ab[i >> 2][64 * i + ((((m >> 2) ^ (i & 3))) << 2) + (m & 3)], x[m], x[i]);
       }
+      if (!ident) {
 #pragma unroll
-      for (int i4 = 0; i4 < 4; ++i4)
-        *reinterpret_cast<float4*>(&sTd[(b * 16 + jj) * TD_LD + 4 * i4]) =   // tf32 MMA operand
-            make_float4(tf32r(x[4 * i4]), tf32r(x[4 * i4 + 1]), tf32r(x[4 * i4 + 2]), tf32r(x[4 * i4 + 3]));
-      // row j = 16 b + jj of (T diag(beta exp(G) r_k))^T and (T diag(beta))^T: the zeros
-      // before the diagonal block and the diagonal block itself
-      const int j = 16 * b + jj;
-      const float sw = vec[VEC_SW + j], sb = vec[VEC_BETA + j];
-      float w[16], u[16];
+        for (int i = 0; i < 16; ++i) sA[a_idx(16 * b + i, cq)] = x[i];
+      } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) { w[i] = x[i] * sw; u[i] = x[i] * sb; }
-      store_bf16x8(sm + OFF_TW + sw128_offset(j, 16 * b), w);
-      store_bf16x8(sm + OFF_TW + sw128_offset(j, 16 * b + 8), w + 8);
-      store_bf16x8(sm + OFF_TU + sw128_offset(j, 16 * b), u);
-      store_bf16x8(sm + OFF_TU + sw128_offset(j, 16 * b + 8), u + 8);
-      const float zeros[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int i8 = 0; i8 < 2 * b; ++i8) {
-        store_bf16x8(sm + OFF_TW + sw128_offset(j, 8 * i8), zeros);
-        store_bf16x8(sm + OFF_TU + sw128_offset(j, 8 * i8), zeros);
+        for (int i4 = 0; i4 < 4; ++i4)
+          *reinterpret_cast<float4*>(&sTd[(b * 16 + j) * TD_LD + 4 * i4]) =
+              make_float4(x[4 * i4], x[4 * i4 + 1], x[4 * i4 + 2], x[4 * i4 + 3]);
+        // row jr = 16 b + j of (T diag(beta exp(G) r_k))^T and (T diag(beta))^T: the zeros
+        // before the diagonal block and the diagonal block itself
+        const int jr = 16 * b + j;
+        const float sw = vec[VEC_SW + jr], sb = vec[VEC_BETA + jr];
+        float w[16], u[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) { w[i] = x[i] * sw; u[i] = x[i] * sb; }
+        store_bf16x8(sm + OFF_TW + sw128_offset(jr, 16 * b), w);
+        store_bf16x8(sm + OFF_TW + sw128_offset(jr, 16 * b + 8), w + 8);
+        store_bf16x8(sm + OFF_TU + sw128_offset(jr, 16 * b), u);
+        store_bf16x8(sm + OFF_TU + sw128_offset(jr, 16 * b + 8), u + 8);
+        const float zeros[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int i8 = 0; i8 < 2 * b; ++i8) {
+          store_bf16x8(sm + OFF_TW + sw128_offset(jr, 8 * i8), zeros);
+          store_bf16x8(sm + OFF_TU + sw128_offset(jr, 8 * i8), zeros);
+        }
       }
     }
     group_sync(kBarPrep, kPrepThreads);
-    // ---- step 2: the off-diagonal blocks.  With D = diag(D_0..D_3) and L = D A_off (block
-    //      strictly lower, so L^4 = 0), (I + A)^{-1} = (I + L)^{-1} D = (I - L + L^2 - L^3) D.
-    //      Three levels of independent 16 x 16 products on the warp-level tf32 MMA, one
-    //      16 x 8 column half per task; intermediate blocks live in the free parts of sA:
-    //      L_bq over A_bq, (L^2)_bq in the upper-triangle block (q, b).
+    // step 2: (L^2)_20 = L_21 L_10, (L^2)_31 = L_32 L_21, (L^2)_30 - (L^3)_30 with
+    //      (L^3)_30 = (L^2)_31 L_10; thread (r, c) = (tid / 16, tid % 16), so a half-warp holds
+    //      a whole row of (L^2)_31 and passes it round by shuffles.  Results go to the
+    //      upper-triangle blocks (0, 2), (1, 3), (0, 3), which nothing else uses.
     {
-      const int g = lane >> 2, t = lane & 3;
-      // level 1: L_bq = D_b A_bq for the six blocks (b, q), both column halves: 12 tasks
-      for (int task = warp; task < 12; task += 8) {
-        const int pr = task >> 1, nt = task & 1;
-        const int b = pr < 1 ? 1 : (pr < 3 ? 2 : 3);
-        const int q = pr < 1 ? pr : (pr < 3 ? pr - 1 : pr - 3);
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
+      const int r = tid >> 4, c = tid & 15, hb = lane & 16;
+      float l21r[16], l32r[16], l31r[16];   // rows r of L_21, L_32, L_31
 #pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-          uint32_t af[4], bf[2];
-          frag_a_d(sTd + b * 16 * TD_LD, 8 * ks, g, t, af);
-          bf[0] = to_tf32(sA[a_idx(16 * b + 8 * ks + t, 16 * q + 8 * nt + g)]);
-          bf[1] = to_tf32(sA[a_idx(16 * b + 8 * ks + t + 4, 16 * q + 8 * nt + g)]);
-          mma_tf32_16x8x8(c, af, bf);
-        }
-        __syncwarp();   // this column half of A_bq has been read (only by this warp)
-        store_c(sA, 16 * b, 16 * q + 8 * nt, g, t, c);
+      for (int u = 0; u < 4; ++u) {
+        const float4 p = *reinterpret_cast<const float4*>(&sA[(32 + r) * 64 + (((4 + u) ^ r) << 2)]);
+        const float4 q = *reinterpret_cast<const float4*>(&sA[(48 + r) * 64 + (((8 + u) ^ r) << 2)]);
+        const float4 w = *reinterpret_cast<const float4*>(&sA[(48 + r) * 64 + (((4 + u) ^ r) << 2)]);
+        l21r[4 * u] = p.x; l21r[4 * u + 1] = p.y; l21r[4 * u + 2] = p.z; l21r[4 * u + 3] = p.w;
+        l32r[4 * u] = q.x; l32r[4 * u + 1] = q.y; l32r[4 * u + 2] = q.z; l32r[4 * u + 3] = q.w;
+        l31r[4 * u] = w.x; l31r[4 * u + 1] = w.y; l31r[4 * u + 2] = w.z; l31r[4 * u + 3] = w.w;
       }
-      group_sync(kBarPrep, kPrepThreads);
-      // level 2: (L^2)_20 = L_21 L_10, (L^2)_31 = L_32 L_21, (L^2)_30 = L_31 L_10 + L_32 L_20
-      if (warp < 6) {
-        const int pr = warp >> 1, nt = warp & 1;   // pr 0: (3,0) (two products), 1: (2,0), 2: (3,1)
-        const int b = pr == 1 ? 2 : 3, q = pr == 2 ? 1 : 0;
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
+      float l10c[16];
+      float m20 = 0.f, m31 = 0.f, m30 = 0.f;
 #pragma unroll
-        for (int term = 0; term < 2; ++term) {
-          if (term == 1 && pr != 0) break;
-          const int m = (pr == 0) ? (term == 0 ? 1 : 2) : b - 1;   // inner block: L_bm L_mq
-#pragma unroll
-          for (int ks = 0; ks < 2; ++ks) {
-            uint32_t af[4], bf[2];
-            frag_a(sA, 16 * b, 16 * m + 8 * ks, g, t, af);
-            frag_b(sA, 16 * m + 8 * ks, 16 * q + 8 * nt, g, t, bf);
-            mma_tf32_16x8x8(c, af, bf);
-          }
-        }
-        store_c(sA, 16 * q, 16 * b + 8 * nt, g, t, c);   // upper-triangle block (q, b)
+      for (int k = 0; k < 16; ++k) {
+        l10c[k] = sA[a_idx(16 + k, c)];
+        m20 = fmaf(l21r[k], l10c[k], m20);
+        m31 = fmaf(l32r[k], sA[a_idx(32 + k, 16 + c)], m31);
+        m30 = fmaf(l31r[k], l10c[k], fmaf(l32r[k], sA[a_idx(32 + k, c)], m30));
       }
-      group_sync(kBarPrep, kPrepThreads);
-      // level 3: T_bq = X_bq D_q with X = -L + L^2 - L^3 (L^3 only in block (3, 0):
-      // (L^3)_30 = L_32 (L^2)_20, computed whole by each of the two warps of that block into
-      // its own scratch, the diagonal block (1, 1) or (2, 2) of sA, free since step 1),
-      // written as Tw^T / Tu^T entries (row j = column of T).  Task pairs pr (two column
-      // halves each) in the order (1,0) (2,1) (3,0) (3,1) (3,2) (2,0): warps 4-7 take one
-      // task each and get the heavier blocks, warps 0-3 two light ones.
-      for (int task = warp; task < 12; task += 8) {
-        const int pr = task >> 1, nt = task & 1;
-        const int b = (3065 >> (2 * pr)) & 3, q = (580 >> (2 * pr)) & 3;
-        const bool l3 = (b == 3 && q == 0);
-        const int sc = 16 * (1 + nt);   // scratch: diagonal block (1 + nt, 1 + nt)
-        if (l3) {
-          // (L^3)_30 = L_32 (L^2)_20; (L^2)_20 is stored at block (0, 2)
+      float n30 = 0.f;
 #pragma unroll
-          for (int n2 = 0; n2 < 2; ++n2) {
-            float c[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int k = 0; k < 16; ++k) n30 = fmaf(__shfl_sync(0xffffffffu, m31, k + hb), l10c[k], n30);
+      sA[a_idx(r, 32 + c)] = m20;
+      sA[a_idx(16 + r, 48 + c)] = m31;
+      sA[a_idx(r, 48 + c)] = m30 - n30;
+    }
+    group_sync(kBarPrep, kPrepThreads);
+    // step 3: T_bq = X_bq D_q, X = -L + L^2 - L^3, for the six blocks below the diagonal;
+    //      thread (r, c) computes T_bq[r][c] for all of them, written as the Tw^T / Tu^T
+    //      entries at row j = 16 q + c, column i = 16 b + r
+    {
+      const int r = tid >> 4, c = tid & 15;
+      float dq[3][16];   // column c of D_0, D_1, D_2
 #pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-              uint32_t af[4], bf[2];
-              frag_a(sA, 48, 32 + 8 * ks, g, t, af);                  // L_32
-              bf[0] = __float_as_uint(sA[a_idx(8 * ks + t, 32 + 8 * n2 + g)]);       // (L^2)_20[k][n]
-              bf[1] = __float_as_uint(sA[a_idx(8 * ks + t + 4, 32 + 8 * n2 + g)]);
-              mma_tf32_16x8x8(c, af, bf);
-            }
-            store_c(sA, sc, sc + 8 * n2, g, t, c);
-          }
-          __syncwarp();
+      for (int q = 0; q < 3; ++q)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float4 d4 = *reinterpret_cast<const float4*>(&sTd[(q * 16 + c) * TD_LD + 4 * u]);
+          dq[q][4 * u] = d4.x; dq[q][4 * u + 1] = d4.y; dq[q][4 * u + 2] = d4.z; dq[q][4 * u + 3] = d4.w;
         }
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
+      __nv_bfloat16* tw = reinterpret_cast<__nv_bfloat16*>(sm + OFF_TW);
+      __nv_bfloat16* tu = reinterpret_cast<__nv_bfloat16*>(sm + OFF_TU);
 #pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-          // A operand: X_bq[rows][columns 8 ks + {t, t + 4}]
-          float xa[4];
+      for (int pr = 0; pr < 6; ++pr) {   // (1,0) (2,0) (3,0) (2,1) (3,1) (3,2)
+        const int b = pr < 3 ? pr + 1 : (pr < 5 ? pr - 1 : 3);
+        const int q = pr < 3 ? 0 : (pr < 5 ? 1 : 2);
+        float xr[16];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int rr = g + 8 * (e & 1), cc = 8 * ks + t + 4 * (e >> 1);
-            float v = -sA[a_idx(16 * b + rr, 16 * q + cc)];                      // -L_bq
-            if (b - q >= 2) v += sA[a_idx(16 * q + rr, 16 * b + cc)];           // + (L^2)_bq
-            if (l3) v -= sA[a_idx(sc + rr, sc + cc)];                           // - (L^3)_30
-            xa[e] = v;
+        for (int u = 0; u < 4; ++u) {
+          const float4 l4 = *reinterpret_cast<const float4*>(&sA[(16 * b + r) * 64 + (((4 * q + u) ^ r) << 2)]);
+          xr[4 * u] = -l4.x; xr[4 * u + 1] = -l4.y; xr[4 * u + 2] = -l4.z; xr[4 * u + 3] = -l4.w;
+          if (b - q >= 2) {   // + (L^2 - L^3)_bq, stored at block (q, b)
+            const float4 m4 = *reinterpret_cast<const float4*>(&sA[(16 * q + r) * 64 + (((4 * b + u) ^ r) << 2)]);
+            xr[4 * u] += m4.x; xr[4 * u + 1] += m4.y; xr[4 * u + 2] += m4.z; xr[4 * u + 3] += m4.w;
           }
-          uint32_t af[4] = {to_tf32(xa[0]), to_tf32(xa[1]), to_tf32(xa[2]), to_tf32(xa[3])};
-          uint32_t bf[2];
-          frag_b_d(sTd + q * 16 * TD_LD, 8 * ks, 8 * nt, g, t, bf);
-          mma_tf32_16x8x8(c, af, bf);
         }
-        // T[i][j] -> Tw^T / Tu^T at row j = 16 q + 8 nt + 2 t (+1), column i = 16 b + g (+8)
-        __nv_bfloat16* tw = reinterpret_cast<__nv_bfloat16*>(sm + OFF_TW);
-        __nv_bfloat16* tu = reinterpret_cast<__nv_bfloat16*>(sm + OFF_TU);
-        const int i0 = 16 * b + g, j0 = 16 * q + 8 * nt + 2 * t;
-        const float sw0 = vec[VEC_SW + j0], sw1 = vec[VEC_SW + j0 + 1];
-        const float sb0 = vec[VEC_BETA + j0], sb1 = vec[VEC_BETA + j0 + 1];
-        tw[sw128_offset(j0, i0) >> 1] = __float2bfloat16_rn(c[0] * sw0);
-        tw[sw128_offset(j0 + 1, i0) >> 1] = __float2bfloat16_rn(c[1] * sw1);
-        tw[sw128_offset(j0, i0 + 8) >> 1] = __float2bfloat16_rn(c[2] * sw0);
-        tw[sw128_offset(j0 + 1, i0 + 8) >> 1] = __float2bfloat16_rn(c[3] * sw1);
-        tu[sw128_offset(j0, i0) >> 1] = __float2bfloat16_rn(c[0] * sb0);
-        tu[sw128_offset(j0 + 1, i0) >> 1] = __float2bfloat16_rn(c[1] * sb1);
-        tu[sw128_offset(j0, i0 + 8) >> 1] = __float2bfloat16_rn(c[2] * sb0);
-        tu[sw128_offset(j0 + 1, i0 + 8) >> 1] = __float2bfloat16_rn(c[3] * sb1);
+        float ta = 0.f, tb = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; k += 2) {
+          ta = fmaf(xr[k], dq[q][k], ta);
+          tb = fmaf(xr[k + 1], dq[q][k + 1], tb);
+        }
+        const float tv = ta + tb;
+        const int jr = 16 * q + c, i = 16 * b + r;
+        const uint32_t o = sw128_offset(jr, i) >> 1;
+        tw[o] = __float2bfloat16_rn(tv * vec[VEC_SW + jr]);
+        tu[o] = __float2bfloat16_rn(tv * vec[VEC_BETA + jr]);
       }
     }
     fence_proxy_async_smem();
