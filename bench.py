@@ -68,7 +68,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -193,7 +193,7 @@ def run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -334,6 +334,10 @@ def main():
         "gpu_launches": launches_per_step * K,
         "clocks": clk.summary(),
     }
+    if args.only == "chunk":      # profiling runs: the half that was not timed is not reported
+        line["decode"] = None
+    elif args.only == "decode":
+        line.update(value=None, chunk_ms=None, roofline=None, tensor=None)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sample = 8192
         dt, cores = cpu_oracle_sample(cin, sample)
