@@ -13,10 +13,11 @@
 //   T   = (I + A)^{-1}                     with 16 x 16 diagonal blocks D_b = (I + A_bb)^-1 and
 //                                           L = D A_off (block strictly lower):
 //                                           T = (I - L + L^2 - L^3) D      (fp32, CUDA cores)
-//   W^T = K^T (T diag(beta exp(G) r_k))^T  M=128 N=64  K=64
-//   U^T = V^T (T diag(beta))^T             M=128 N=64  K=64
-//   U'^T = U^T - S^T W^T                   M=128 N=64  K=128   (accumulates on U^T)
-//   O1  = S^T Q^T                          M=128 N=64  K=128
+//   U^T = V^T Tu^T, Tu = T diag(beta)      M=128 N=64  K=64
+//   [O1 | Y] = S^T [Q; K]^T                M=128 N=128 K=128   (O1 = S^T Q^T, Y = S^T K^T)
+//   U'^T = U^T - Y Tw^T, Tw = T diag(beta exp(G) r_k)
+//                                          M=128 N=64  K=64    (accumulates on U^T; this is
+//                                                               U - W S with W = Tw K)
 //   O2  = U'^T P^T                         M=128 N=64  K=64
 //   S^T <- exp(G_last) S^T + (U' * exp(G_last - G) r_k)^T K     M=128 N=128 K=64
 //   o   = scale exp(G) r_q * O1 + O2
@@ -25,7 +26,7 @@
 // lanes, tokens on the columns).  The CTA is warp-specialised: a prep group
 // (warps 0-7) builds everything that does not depend on the state -- norms,
 // D1, P, A, T -- for chunk c + 1 while a state group (warps 8-11) runs the
-// rest of chunk c (the W and U products, U', O, the state update, the output);
+// rest of chunk c (the U product, O1 and S K^T, U', the state update, the output);
 // they hand chunks over through mbarriers, double-buffering P, the per-token
 // vectors and the TMA stages.  These are the chunkwise (WY / UT transform)
 // equations of the gated delta rule with the chunking of the inference kernels
@@ -60,7 +61,7 @@ constexpr uint32_t V_STAGE = 16384;
 constexpr uint32_t OFF_S = 98304;       // S^T bf16, A operand: [dk half][128 dv rows][128 B]; after
                                         // the MMAs that read it, the bf16 output tile staged for a
                                         // TMA store
-constexpr uint32_t OFF_W = 131072;      // -W^T bf16, MN-major B: [128 dk rows][64 tokens]
+constexpr uint32_t OFF_Y = 131072;      // -Y = -S^T K^T bf16, K-major A: [128 dv rows][64 tokens]
 constexpr uint32_t OFF_A = 147456;      // fp32 A [64][64], 16-byte-group swizzled; the solve
                                         // overwrites its strictly-lower blocks with those of T
 constexpr uint32_t OFF_P = 163840;      // 2 x P, K-major B [64 i][64 j]
@@ -79,7 +80,7 @@ constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the bas
 constexpr uint32_t STAGE_TX = QK_STAGE + V_STAGE;  // Q + K + V bytes per stage = 48 KB
 
 // TMEM columns (fp32, 128 lanes).  COL_S holds S^T for the whole sequence.
-constexpr uint32_t COL_D1 = 0 /* 128 */, COL_W = 128, COL_U = 192, COL_O1 = 256,
+constexpr uint32_t COL_D1 = 0 /* 128 */, COL_U = 128, COL_O1 = 192, COL_Y = 256 /* O1 | Y adjacent */,
                    COL_O2 = 320, COL_S = 384, TMEM_COLS = 512;
 
 // mbarriers (8 bytes each) at OFF_BAR.
@@ -88,7 +89,7 @@ enum {
   B_MMA_P = 2,      // prep group's D1 commits
   B_MMA_S = 3,      // state group's MMA commits
   B_READY = 4,      // [2] prep -> state: chunk ready (vectors, P, Tw / Tu in shared memory)
-  B_WU = 6,         // state: W / U MMAs done (W^T, U^T in TMEM; Tw / Tu free for the prep group)
+  B_WU = 6,         // state -> prep: the MMAs reading Tw / Tu are done (both free again)
   B_P_FREE = 7,     // [2] state -> prep: MMA on P done
   B_VEC_FREE = 9,   // [2] state -> prep: chunk finished (per-token vectors free)
   B_COUNT = 11
@@ -498,9 +499,8 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
 }
 
 // =================================================================== state group
-// Warps 8-11.  For each chunk: W^T = K^T Tw^T and U^T = V^T Tu^T, -W^T and S -> bf16
-// operands, decay of the TMEM state, U' = U - S W, O1 = S Q^T, O2 = U' P^T,
-// S += (decayed U')^T K, output.
+// Warps 8-11.  For each chunk: U^T = V^T Tu^T, S -> bf16 operand and decay of the TMEM
+// state, [O1 | Y] = S^T [Q; K]^T, U' = U - Y Tw^T, O2 = U' P^T, S += (decayed U')^T K, output.
 __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int bos, int eos,
                             int nchunks, int h, int hq, size_t st_off,
                             const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
@@ -532,21 +532,14 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     if (group_sync_or(kBarState, kStateThreads, !ok || flag_set(flag))) { failed = true; break; }
     tc_fence_after();
 
-    // ---- MMA: W^T = K^T Tw^T, U^T = V^T Tu^T (all operands MN-major); they run while the
-    //      state is converted below
+    // ---- MMA: U^T = V^T Tu^T (operands MN-major), running while the state is converted
     if (leader) {
       const uint32_t id = idesc_bf16(128, 64, true, true);
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        mma_bf16(tbase + COL_W, sdesc_sw128(qk_a + 8192 + ks * 2048, 16384, 1024),
-                 sdesc_sw128(sbase + OFF_TW + ks * 2048, 8192, 1024), id, ks > 0);
-      }
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         mma_bf16(tbase + COL_U, sdesc_sw128(v_a + ks * 2048, 8192, 1024),
                  sdesc_sw128(sbase + OFF_TU + ks * 2048, 8192, 1024), id, ks > 0);
       }
-      mma_commit(&bars[B_WU]);
     }
     // ---- S (entry state) -> bf16 A operand S^T [dv rows][dk]; S <- exp(G_last) S in TMEM
     {
@@ -565,41 +558,52 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
         tmem_st32(tbase + lane_off + col, x);
       }
     }
-    if (leader) ok = mbar_wait(&bars[B_WU], (uint32_t)c & 1u, kWaitLimitNs);
-    if (group_sync_or(kBarState, kStateThreads, !ok || flag_set(flag))) { failed = true; break; }
-    tc_fence_after();
-    // ---- -W^T (TMEM) -> bf16 MN-major B operand [dk rows][tokens]
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float x[32];
-      tmem_ld32(tbase + lane_off + COL_W + 32 * half, x);
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) x[jj] = -x[jj];
-#pragma unroll
-      for (int m = 0; m < 4; ++m)
-        store_bf16x8(sm + OFF_W + sw128_offset(row, 32 * half + 8 * m), &x[8 * m]);
-    }
     fence_proxy_async_smem();
     tc_fence_before();
     group_sync(kBarState, kStateThreads);
 
-    // ---- MMA: U'^T = U^T + S^T (-W^T);  O1 = S^T Q^T
+    // ---- MMA: [O1 | Y] = S^T [Q; K]^T, one N = 128 product over the stage as loaded
     if (leader) {
       tc_fence_after();
-      const uint32_t id4 = idesc_bf16(128, 64, false, true);
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        mma_bf16(tbase + COL_U,
-                 sdesc_sw128(sbase + OFF_S + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                 sdesc_sw128(sbase + OFF_W + ks * 2048, 8192, 1024), id4, 1);
-      }
-      const uint32_t id5 = idesc_bf16(128, 64, false, false);
+      const uint32_t id5 = idesc_bf16(128, 128, false, false);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
         mma_bf16(tbase + COL_O1, sdesc_sw128(sbase + OFF_S + off, 16, 1024),
                  sdesc_sw128(qk_a + off, 16, 1024), id5, ks > 0);
       }
+      mma_commit(&bars[B_MMA_S]);
+    }
+    if (leader) ok = mbar_wait(&bars[B_MMA_S], ps, kWaitLimitNs);
+    ps ^= 1u;
+    if (group_sync_or(kBarState, kStateThreads, !ok || flag_set(flag))) { failed = true; break; }
+    tc_fence_after();
+
+    // ---- -Y -> bf16 K-major A operand [dv rows][tokens]
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float x[32];
+      tmem_ld32(tbase + lane_off + COL_Y + 32 * half, x);
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) x[jj] = -x[jj];
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        store_bf16x8(sm + OFF_Y + sw128_offset(row, 32 * half + 8 * m), &x[8 * m]);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    group_sync(kBarState, kStateThreads);
+
+    // ---- MMA: U'^T = U^T + (-Y) Tw^T (Tw MN-major); then Tw / Tu are free for the prep group
+    if (leader) {
+      tc_fence_after();
+      const uint32_t id4 = idesc_bf16(128, 64, false, true);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        mma_bf16(tbase + COL_U, sdesc_sw128(sbase + OFF_Y + ks * 32, 16, 1024),
+                 sdesc_sw128(sbase + OFF_TW + ks * 2048, 8192, 1024), id4, 1);
+      }
+      mma_commit(&bars[B_WU]);
       mma_commit(&bars[B_MMA_S]);
     }
     if (leader) ok = mbar_wait(&bars[B_MMA_S], ps, kWaitLimitNs);
