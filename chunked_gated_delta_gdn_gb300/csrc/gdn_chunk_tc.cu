@@ -17,7 +17,8 @@
 //   [O1 | Y] = S^T [Q; K]^T                M=128 N=128 K=128   (O1 = S^T Q^T, Y = S^T K^T)
 //   U'^T = U^T - Y Tw^T, Tw = T diag(beta exp(G) r_k)
 //                                          M=128 N=64  K=64    (accumulates on U^T; this is
-//                                                               U - W S with W = Tw K)
+//                                                               U - W S with W = Tw K; -Y is
+//                                                               read from TMEM as bf16)
 //   O2  = U'^T P^T                         M=128 N=64  K=64
 //   S^T <- exp(G_last) S^T + (U' * exp(G_last - G) r_k)^T K     M=128 N=128 K=64
 //   o   = scale exp(G) r_q * O1 + O2
@@ -61,7 +62,8 @@ constexpr uint32_t V_STAGE = 16384;
 constexpr uint32_t OFF_S = 98304;       // S^T bf16, A operand: [dk half][128 dv rows][128 B]; after
                                         // the MMAs that read it, the bf16 output tile staged for a
                                         // TMA store
-constexpr uint32_t OFF_Y = 131072;      // -Y = -S^T K^T bf16, K-major A: [128 dv rows][64 tokens]
+constexpr uint32_t OFF_KT = 131072;     // K rows scaled by exp(G_last - G_t) r_k[t], bf16: the
+                                        // state update's MN-major B, [dk half][64 tokens][128 B]
 constexpr uint32_t OFF_A = 147456;      // fp32 A [64][64], 16-byte-group swizzled; the solve
                                         // overwrites its strictly-lower blocks with those of T
 constexpr uint32_t OFF_P = 163840;      // 2 x P, K-major B [64 i][64 j]
@@ -221,7 +223,6 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
   float* sA = reinterpret_cast<float*>(sm + OFF_A);
   float* sTd = reinterpret_cast<float*>(sm + OFF_TD);
   const bool leader = (tid == 0);
-  bool d1_ahead = false;   // leader: D1 of this chunk was issued during the previous one
   const int T_total = a.cu_seqlens ? a.T : a.B * a.T;
   constexpr int kGateWarp = 1;   // not the leader's warp: gates overlap the MMA issue
   float gq[2], bq[2];
@@ -246,8 +247,9 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
     }
     if (group_sync_or(kBarPrep, kPrepThreads, !ok || flag_set(flag))) { if (leader) set_flag(flag); return; }
 
-    // ---- MMA: D1 = [Q;K][Q;K]^T, unless it was issued ahead during the previous chunk
-    if (leader && !d1_ahead) {
+    // ---- MMA: D1 = [Q;K][Q;K]^T.  (Issuing it earlier, during the previous chunk, measured
+    //      slower: an MMA issue into the busy tensor pipe stalls the issuing thread.)
+    if (leader) {
       tc_fence_after();
       issue_d1(tbase + COL_D1, qk_a, &bars[B_MMA_P]);
     }
@@ -355,14 +357,6 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
     tc_fence_before();
     if (leader && c >= 1) ok = mbar_wait(&bars[B_WU], (uint32_t)(c - 1) & 1u, kWaitLimitNs);   // Tw, Tu free
     if (group_sync_or(kBarPrep, kPrepThreads, !ok || flag_set(flag))) { if (leader) set_flag(flag); return; }
-    // D1 has been read: issue the next chunk's now if its tiles are in already
-    d1_ahead = false;
-    if (leader && c + 1 < nchunks &&
-        mbar_try_wait(&bars[B_FULL + (s ^ 1)], (uint32_t)((c + 1) >> 1) & 1u)) {
-      tc_fence_after();
-      issue_d1(tbase + COL_D1, sbase + OFF_QK + (s ^ 1) * QK_STAGE, &bars[B_MMA_P]);
-      d1_ahead = true;
-    }
 
     // ---- T = (I + A)^{-1} in fp32 on the CUDA cores.  With D_b = (I + A_bb)^{-1} and
     //      L = D A_off (block strictly lower, so L^4 = 0): T = (I - L + L^2 - L^3) D.
@@ -383,10 +377,20 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
 #pragma unroll
       for (int i = 0; i < 16; ++i) x[i] = ident ? ((i == j) ? 1.f : 0.f) : sA[a_idx(16 * b + i, cq)];
 #pragma unroll
-      for (int m = 0; m < 15; ++m) {
+      for (int g = 0; g < 4; ++g) {   // columns m = 4 g .. 4 g + 3 of A_bb, one float4 per row
+        float4 ag[16];
 #pragma unroll
-        for (int i = m + 1; i < 16; ++i)
-          x[i] = fmaf(-ab[i >> 2][64 * i + ((((m >> 2) ^ (i & 3))) << 2) + (m & 3)], x[m], x[i]);
+        for (int i = 4 * g + 1; i < 16; ++i)
+          ag[i] = *reinterpret_cast<const float4*>(ab[i >> 2] + 64 * i + ((g ^ (i & 3)) << 2));
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int m = 4 * g + e;
+#pragma unroll
+          for (int i = m + 1; i < 16; ++i) {
+            const float am = e == 0 ? ag[i].x : (e == 1 ? ag[i].y : (e == 2 ? ag[i].z : ag[i].w));
+            x[i] = fmaf(-am, x[m], x[i]);
+          }
+        }
       }
       if (!ident) {
 #pragma unroll
@@ -574,23 +578,49 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
       }
       mma_commit(&bars[B_MMA_S]);
     }
+    // ---- K rows scaled by exp(G_last - G_t) r_k[t] into their own tile (the state update's
+    //      B operand), done while [O1 | Y] runs; then the stage is free
+    {
+      const int t = tid >> 1, kh = tid & 1;
+      const float dl = vec[VEC_DL + t];
+      const uint8_t* krow = sm + OFF_QK + s * QK_STAGE + kh * 16384 + 8192 + t * 128;
+      uint8_t* kdst = sm + OFF_KT + kh * 8192 + t * 128;   // same offsets: same swizzle
+#pragma unroll
+      for (int m0 = 0; m0 < 8; ++m0) {
+        const int m = (m0 + t) & 7;   // rows rotate through the 16-byte chunks: no bank conflicts
+        uint4 u = *reinterpret_cast<const uint4*>(krow + 16 * m);
+        __nv_bfloat162* b2 = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(b2[e]);
+          b2[e] = __floats2bfloat162_rn(f.x * dl, f.y * dl);
+        }
+        *reinterpret_cast<uint4*>(kdst + 16 * m) = u;
+      }
+    }
+    fence_proxy_async_smem();
     if (leader) ok = mbar_wait(&bars[B_MMA_S], ps, kWaitLimitNs);
     ps ^= 1u;
     if (group_sync_or(kBarState, kStateThreads, !ok || flag_set(flag))) { failed = true; break; }
+    // every read of stage s is done (U, D1, [O1 | Y], the K copy): load chunk c + 2 into it
+    if (leader && c + 2 < nchunks)
+      issue_chunk_loads(sm, &bars[B_FULL + s], tq, tk, tv, s, t0 + 2 * kChunk, hq, h);
     tc_fence_after();
 
-    // ---- -Y -> bf16 K-major A operand [dv rows][tokens]
+    // ---- -Y -> bf16, packed into the first 32 of its own TMEM columns (A operand from TMEM)
+    {
+      float x[32], y[32], pk[32];
+      tmem_ld32(tbase + lane_off + COL_Y, x);
+      tmem_ld32(tbase + lane_off + COL_Y + 32, y);
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float x[32];
-      tmem_ld32(tbase + lane_off + COL_Y + 32 * half, x);
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) x[jj] = -x[jj];
-#pragma unroll
-      for (int m = 0; m < 4; ++m)
-        store_bf16x8(sm + OFF_Y + sw128_offset(row, 32 * half + 8 * m), &x[8 * m]);
+      for (int jj = 0; jj < 16; ++jj) {
+        __nv_bfloat162 p0 = __floats2bfloat162_rn(-x[2 * jj], -x[2 * jj + 1]);
+        __nv_bfloat162 p1 = __floats2bfloat162_rn(-y[2 * jj], -y[2 * jj + 1]);
+        pk[jj] = __uint_as_float(*reinterpret_cast<uint32_t*>(&p0));
+        pk[16 + jj] = __uint_as_float(*reinterpret_cast<uint32_t*>(&p1));
+      }
+      tmem_st32(tbase + lane_off + COL_Y, pk);
     }
-    fence_proxy_async_smem();
     tc_fence_before();
     group_sync(kBarState, kStateThreads);
 
@@ -600,8 +630,8 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
       const uint32_t id4 = idesc_bf16(128, 64, false, true);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
-        mma_bf16(tbase + COL_U, sdesc_sw128(sbase + OFF_Y + ks * 32, 16, 1024),
-                 sdesc_sw128(sbase + OFF_TW + ks * 2048, 8192, 1024), id4, 1);
+        mma_bf16_ta(tbase + COL_U, tbase + COL_Y + 8 * ks,
+                    sdesc_sw128(sbase + OFF_TW + ks * 2048, 8192, 1024), id4, 1);
       }
       mma_commit(&bars[B_WU]);
       mma_commit(&bars[B_MMA_S]);
@@ -611,9 +641,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     if (group_sync_or(kBarState, kStateThreads, !ok || flag_set(flag))) { failed = true; break; }
     tc_fence_after();
 
-    // ---- U'^T -> bf16 K-major A operand [dv rows][tokens]; K tile rows scaled by
-    //      exp(G_last - G_t) r_k[t] in place (the state update's B operand; the prep
-    //      group is done with this K tile)
+    // ---- U'^T -> bf16 K-major A operand [dv rows][tokens]
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       float x[32];
@@ -622,28 +650,11 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
       for (int m = 0; m < 4; ++m)
         store_bf16x8(sm + OFF_U + sw128_offset(row, 32 * half + 8 * m), &x[8 * m]);
     }
-    {
-      const int t = tid >> 1, kh = tid & 1;
-      const float dl = vec[VEC_DL + t];
-      uint8_t* krow = sm + OFF_QK + s * QK_STAGE + kh * 16384 + 8192 + t * 128;
-#pragma unroll
-      for (int m0 = 0; m0 < 8; ++m0) {
-        const int m = (m0 + t) & 7;   // rows rotate through the 16-byte chunks: no bank conflicts
-        uint4 u = *reinterpret_cast<uint4*>(krow + 16 * m);
-        __nv_bfloat162* b2 = reinterpret_cast<__nv_bfloat162*>(&u);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(b2[e]);
-          b2[e] = __floats2bfloat162_rn(f.x * dl, f.y * dl);
-        }
-        *reinterpret_cast<uint4*>(krow + 16 * m) = u;
-      }
-    }
     fence_proxy_async_smem();
     tc_fence_before();
     group_sync(kBarState, kStateThreads);
 
-    // ---- MMA: O2 = U'^T P^T, S^T += Ut^T K
+    // ---- MMA: O2 = U'^T P^T, S^T += U'^T K~ (K~ = the scaled K rows)
     if (leader) {
       tc_fence_after();
       const uint32_t id6 = idesc_bf16(128, 64, false, false);
@@ -656,7 +667,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         mma_bf16(tbase + COL_S, sdesc_sw128(sbase + OFF_U + ks * 32, 16, 1024),
-                 sdesc_sw128(qk_a + 8192 + ks * 2048, 16384, 1024), id7, 1);
+                 sdesc_sw128(sbase + OFF_KT + ks * 2048, 8192, 1024), id7, 1);
       }
       mma_commit(&bars[B_P_FREE + s]);
       mma_commit(&bars[B_MMA_S]);
@@ -665,11 +676,6 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     ps ^= 1u;
     if (group_sync_or(kBarState, kStateThreads, !ok || flag_set(flag))) { failed = true; break; }
     tc_fence_after();
-    // Stage s is free again: load chunk c + 2 into it.
-    if (leader && c + 2 < nchunks) {
-      fence_proxy_async_smem();
-      issue_chunk_loads(sm, &bars[B_FULL + s], tq, tk, tv, s, t0 + 2 * kChunk, hq, h);
-    }
 
     // ---- o = scale exp(G) r_q O1 + O2 (P carries scale r_q): a full chunk is staged as a
     //      bf16 tile (two 128-byte-swizzled [64 tokens][64 dv] halves) and written by one
