@@ -16,6 +16,10 @@ Three functions wrap the C library built from ``gdn_oracle.c``:
   padding ("Megatron-Core API: core.ssm.gated_delta_product",
   GatedDeltaProductMixer.ssm_decode).
 
+:func:`product` and :func:`product_decode` evaluate the Gated Delta Product (several
+delta-rule writes per token, "Megatron-Core API: core.ssm.gated_delta_product",
+GatedDeltaProductMixer) by its recurrence.
+
 :mod:`oracle.closed_form` adds the unrolled product form for tiny inputs.
 
 Every function pinned by ``tests/test_oracle_pins.py``; see the header of
@@ -67,7 +71,12 @@ def load_library(path: str) -> ctypes.CDLL:
                                        dp, dp, dp, i]
     lib.gdn_oracle_decode.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, dp, i, lp, d, i,
                                       dp, i]
-    for f in (lib.gdn_oracle_recurrent, lib.gdn_oracle_chunked, lib.gdn_oracle_decode):
+    lib.gdn_oracle_product.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, i, lp, i, d, i,
+                                       dp, dp, dp, i]
+    lib.gdn_oracle_product_decode.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, i, dp, i, lp,
+                                              d, i, dp, i]
+    for f in (lib.gdn_oracle_recurrent, lib.gdn_oracle_chunked, lib.gdn_oracle_decode,
+              lib.gdn_oracle_product, lib.gdn_oracle_product_decode):
         f.restype = ctypes.c_int
     lib.gdn_oracle_max_threads.restype = ctypes.c_int
     return lib
@@ -191,4 +200,65 @@ def decode(q, k, v, g, beta, ssm_state, batch_indices=None, scale=None,
         return o
     if rc != ORACLE_OK:
         raise RuntimeError("gdn_oracle_decode failed with code %d" % rc)
+    return o
+
+
+def product(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=True,
+            use_qk_l2norm_in_kernel=False, cu_seqlens=None, nthreads=0, lib=None):
+    """Gated Delta Product by its recurrence: q [B, T, Hqk, K], k [B, T, n_h, Hqk, K],
+    v [B, T, n_h, Hv, V], g [B, T, Hv], beta [B, T, n_h, Hv].  Returns ``(o, final_state)``."""
+    q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
+    if q.ndim != 4 or k.ndim != 5 or v.ndim != 5:
+        raise ValueError("q must be [B, T, Hqk, K], k [B, T, n_h, Hqk, K], v [B, T, n_h, Hv, V]")
+    B, T, Hqk, K = q.shape
+    n_h = k.shape[2]
+    Hv, V = v.shape[3], v.shape[4]
+    if (k.shape != (B, T, n_h, Hqk, K) or v.shape[:3] != (B, T, n_h) or g.shape != (B, T, Hv)
+            or beta.shape != (B, T, n_h, Hv)):
+        raise ValueError("inconsistent shapes")
+    if cu_seqlens is None:
+        cu = np.arange(B + 1, dtype=np.int64) * T
+    else:
+        if B != 1:
+            raise ValueError("cu_seqlens requires B == 1")
+        cu = _i64(cu_seqlens)
+    N = cu.shape[0] - 1
+    init = _f64(initial_state)
+    if init is not None and init.shape != (N, Hv, K, V):
+        raise ValueError("initial_state must be [N, Hv, K, V]")
+    o = np.full((B, T, Hv, V), np.nan)
+    fin = np.zeros((N, Hv, K, V), dtype=np.float64) if output_final_state else None
+    rc = (lib or _load()).gdn_oracle_product(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), B * T, n_h, Hqk, Hv, K, V,
+        _ptr(cu, ctypes.c_int64), N, _scale(scale, K), int(bool(use_qk_l2norm_in_kernel)),
+        _ptr(init), _ptr(o), _ptr(fin), int(nthreads))
+    if rc != ORACLE_OK:
+        raise RuntimeError("gdn_oracle_product failed with code %d" % rc)
+    return o, fin
+
+
+def product_decode(q, k, v, g, beta, ssm_state, batch_indices=None, scale=None,
+                   use_qk_l2norm_in_kernel=True, nthreads=0, allow_bad_slots=False, lib=None):
+    """One Gated Delta Product token per request: q [n, Hqk, K], k [n, n_h, Hqk, K],
+    v [n, n_h, Hv, V], g [n, Hv], beta [n, n_h, Hv].  ``ssm_state`` (float64 numpy) is updated
+    in place; returns ``o`` [n, Hv, V]; ``-1`` slots give zero rows."""
+    q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
+    if not (isinstance(ssm_state, np.ndarray) and ssm_state.dtype == np.float64
+            and ssm_state.flags.c_contiguous):
+        raise TypeError("ssm_state must be a C-contiguous float64 numpy array (updated in place)")
+    n, Hqk, K = q.shape
+    n_h = k.shape[1]
+    Hv, V = v.shape[2], v.shape[3]
+    if ssm_state.ndim != 4 or ssm_state.shape[1:] != (Hv, K, V):
+        raise ValueError("ssm_state must be [num_slots, Hv, K, V]")
+    idx = _i64(batch_indices)
+    o = np.full((n, Hv, V), np.nan)
+    rc = (lib or _load()).gdn_oracle_product_decode(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), n, n_h, Hqk, Hv, K, V, _ptr(ssm_state),
+        ssm_state.shape[0], _ptr(idx, ctypes.c_int64), _scale(scale, K),
+        int(bool(use_qk_l2norm_in_kernel)), _ptr(o), int(nthreads))
+    if rc == ORACLE_ERR_SLOT and allow_bad_slots:
+        return o
+    if rc != ORACLE_OK:
+        raise RuntimeError("gdn_oracle_product_decode failed with code %d" % rc)
     return o

@@ -24,7 +24,7 @@
  * eps = 1e-6), scale defaulting to 1/sqrt(K) (torch_chunk_gated_delta_rule,
  * same page), and value head h reading query/key head h / (Hv / Hqk).
  *
- * Three entry points:
+ * Entry points:
  *   gdn_oracle_recurrent  -- the definition above, token by token.
  *   gdn_oracle_chunked    -- the chunkwise (WY / UT-transform) evaluation for
  *                            any chunk size C >= 1, chunks restarting at every
@@ -35,6 +35,8 @@
  *                            cache; slot -1 is padding: no state read or write,
  *                            output exactly zero (GatedDeltaProductMixer.ssm_decode;
  *                            "Add GDN dynamic inference" PR review thread).
+ *   gdn_oracle_product, gdn_oracle_product_decode -- the Gated Delta Product
+ *                            (several writes per token), at the end of this file.
  *
  * Layouts (all row-major, fp64):
  *   q, k   [T_total, Hqk, K]     v, o [T_total, Hv, V]     g, beta [T_total, Hv]
@@ -372,4 +374,146 @@ int gdn_oracle_max_threads(void) {
 #else
   return 1;
 #endif
+}
+
+/*
+ * Gated Delta Product: several delta-rule (Householder-type) writes per token.
+ * "Megatron-Core API: core.ssm.gated_delta_product", GatedDeltaProductMixer: each token is
+ * projected into the V, K, Q, beta and decay terms of a sequence of Householder updates, as
+ * many as num_householder (n_h) sets.  The pages print no formula; the plain reading taken:
+ * per token t the decay is applied once, before the first write; write j = 0..n_h-1 uses its
+ * own key, value and beta; the single query of the token reads the state after the last
+ * write:
+ *
+ *     S   <- exp(g_t) * S
+ *     for j = 0 .. n_h - 1:   r = S^T k_tj;  u = beta_tj (v_tj - r);  S <- S + k_tj u^T
+ *     o_t  = scale * S^T q_t
+ *
+ * Layouts (row-major, fp64):
+ *   q [T_total, Hqk, K]   k [T_total, n_h, Hqk, K]   v [T_total, n_h, Hv, V]
+ *   g [T_total, Hv]       beta [T_total, n_h, Hv]    o [T_total, Hv, V]
+ * states, cu_seqlens, the L2 norm, scale and the head map as for gdn_oracle_recurrent; with
+ * n_h = 1 this is gdn_oracle_recurrent.
+ */
+
+/* The writes of one token on S (decay already applied).  kb, vb, bb point at the token's
+ * first key / value / beta of this head; consecutive writes are ks, vs, bs apart. */
+static void oracle_product_writes(double* S, const double* kb, size_t ks, const double* vb,
+                                  size_t vs, const double* bb, size_t bs, int n_h, int K, int V,
+                                  int use_qk_l2norm, double* kn, double* r) {
+  for (int j = 0; j < n_h; ++j) {
+    oracle_l2norm(kb + (size_t)j * ks, K, use_qk_l2norm, kn);
+    const double* vj = vb + (size_t)j * vs;
+    const double bj = bb[(size_t)j * bs];
+    for (int c = 0; c < V; ++c) r[c] = 0.0;
+    for (int i = 0; i < K; ++i)
+      for (int c = 0; c < V; ++c) r[c] += S[i * V + c] * kn[i];
+    for (int c = 0; c < V; ++c) r[c] = bj * (vj[c] - r[c]);   /* r becomes u */
+    for (int i = 0; i < K; ++i)
+      for (int c = 0; c < V; ++c) S[i * V + c] += kn[i] * r[c];
+  }
+}
+
+/* o = scale * S^T qn */
+static void oracle_readout(const double* S, const double* qn, double scale, int K, int V,
+                           double* o) {
+  for (int c = 0; c < V; ++c) o[c] = 0.0;
+  for (int i = 0; i < K; ++i)
+    for (int c = 0; c < V; ++c) o[c] += S[i * V + c] * qn[i];
+  for (int c = 0; c < V; ++c) o[c] *= scale;
+}
+
+int gdn_oracle_product(const double* q, const double* k, const double* v, const double* g,
+                       const double* beta, int T_total, int n_h, int Hqk, int Hv, int K, int V,
+                       const int64_t* cu_seqlens, int N, double scale, int use_qk_l2norm,
+                       const double* initial_state, double* o, double* final_state,
+                       int nthreads) {
+  int err = check_common(Hqk, Hv, K, V, cu_seqlens, N);
+  if (err) return err;
+  if (n_h < 1 || cu_seqlens[N] > T_total || !q || !k || !v || !g || !beta || !o)
+    return ORACLE_ERR_ARG;
+  const int group = Hv / Hqk;
+  int failed = 0;
+  set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) collapse(2)
+  for (int n = 0; n < N; ++n) {
+    for (int h = 0; h < Hv; ++h) {
+      double* S = (double*)malloc(sizeof(double) * ((size_t)K * V + 2 * K + V));
+      if (!S) {
+#pragma omp atomic write
+        failed = 1;
+        continue;
+      }
+      double* qn = S + (size_t)K * V;
+      double* kn = qn + K;
+      double* r = kn + K;
+      const size_t soff = ((size_t)n * Hv + h) * K * V;
+      if (initial_state)
+        memcpy(S, initial_state + soff, sizeof(double) * K * V);
+      else
+        memset(S, 0, sizeof(double) * K * V);
+      const int hq = h / group;
+      for (int64_t t = cu_seqlens[n]; t < cu_seqlens[n + 1]; ++t) {
+        const double a = exp(g[(size_t)t * Hv + h]);
+        for (size_t x = 0; x < (size_t)K * V; ++x) S[x] *= a;
+        oracle_product_writes(S, k + (((size_t)t * n_h) * Hqk + hq) * K, (size_t)Hqk * K,
+                              v + (((size_t)t * n_h) * Hv + h) * V, (size_t)Hv * V,
+                              beta + ((size_t)t * n_h) * Hv + h, (size_t)Hv, n_h, K, V,
+                              use_qk_l2norm, kn, r);
+        oracle_l2norm(q + ((size_t)t * Hqk + hq) * K, K, use_qk_l2norm, qn);
+        oracle_readout(S, qn, scale, K, V, o + ((size_t)t * Hv + h) * V);
+      }
+      if (final_state) memcpy(final_state + soff, S, sizeof(double) * K * V);
+      free(S);
+    }
+  }
+  return failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
+
+/*
+ * One token per request of the Gated Delta Product on a slot-indexed cache (the decode step
+ * of GatedDeltaProductMixer.ssm_decode): q [n, Hqk, K], k [n, n_h, Hqk, K],
+ * v [n, n_h, Hv, V], g [n, Hv], beta [n, n_h, Hv], state [num_slots, Hv, K, V] updated in
+ * place, batch_indices [n] (NULL: request i uses slot i; -1: padding, zero output, no state
+ * access), o [n, Hv, V].
+ */
+int gdn_oracle_product_decode(const double* q, const double* k, const double* v,
+                              const double* g, const double* beta, int n, int n_h, int Hqk,
+                              int Hv, int K, int V, double* state, int num_slots,
+                              const int64_t* batch_indices, double scale, int use_qk_l2norm,
+                              double* o, int nthreads) {
+  if (n < 0 || n_h < 1 || Hqk <= 0 || Hv <= 0 || K <= 0 || V <= 0 || Hv % Hqk) return ORACLE_ERR_ARG;
+  if (K > 1024 || V > 1024) return ORACLE_ERR_ARG;
+  if (n > 0 && (!q || !k || !v || !g || !beta || !o || !state)) return ORACLE_ERR_ARG;
+  const int group = Hv / Hqk;
+  int bad = 0;
+  set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) collapse(2)
+  for (int i = 0; i < n; ++i) {
+    for (int h = 0; h < Hv; ++h) {
+      double* oi = o + ((size_t)i * Hv + h) * V;
+      const int64_t s = batch_indices ? batch_indices[i] : i;
+      if (s < 0 || s >= num_slots) {
+        for (int c = 0; c < V; ++c) oi[c] = 0.0;
+        if (s != -1) {
+#pragma omp atomic write
+          bad = 1;
+        }
+        continue;
+      }
+      double buf[3 * 1024];
+      double *qn = buf, *kn = buf + K, *r = buf + 2 * K;
+      double* S = state + ((size_t)s * Hv + h) * K * V;
+      const int hq = h / group;
+      const double a = exp(g[(size_t)i * Hv + h]);
+      for (size_t x = 0; x < (size_t)K * V; ++x) S[x] *= a;
+      oracle_product_writes(S, k + (((size_t)i * n_h) * Hqk + hq) * K, (size_t)Hqk * K,
+                            v + (((size_t)i * n_h) * Hv + h) * V, (size_t)Hv * V,
+                            beta + ((size_t)i * n_h) * Hv + h, (size_t)Hv, n_h, K, V,
+                            use_qk_l2norm, kn, r);
+      oracle_l2norm(q + ((size_t)i * Hqk + hq) * K, K, use_qk_l2norm, qn);
+      oracle_readout(S, qn, scale, K, V, oi);
+    }
+  }
+  return bad ? ORACLE_ERR_SLOT : ORACLE_OK;
 }

@@ -48,3 +48,41 @@ def run(q, k, v, a, beta, cu_seqlens, Hqk, Hv, scale, initial_state=None):
             per_head.append(S)
         final.append(per_head)
     return o, final
+
+
+def run_product(q, k, v, a, beta, cu_seqlens, Hqk, Hv, scale, initial_state=None):
+    """Gated Delta Product in exact arithmetic: per token the decay a_t once, then the writes
+    j = 0..n_h-1 with k[t][j], v[t][j], beta[t][j], then o_t = scale S^T q_t.
+    q: [T][Hqk][K]; k: [T][n_h][Hqk][K]; v: [T][n_h][Hv][V]; a: [T][Hv]; beta: [T][n_h][Hv]."""
+    T = len(q)
+    K = len(q[0][0])
+    V = len(v[0][0][0])
+    n_h = len(k[0])
+    N = len(cu_seqlens) - 1
+    grp = Hv // Hqk
+    o = [[[Fraction(0)] * V for _ in range(Hv)] for _ in range(T)]
+    final = []
+    for n in range(N):
+        per_head = []
+        for h in range(Hv):
+            if initial_state is None:
+                S = [[Fraction(0)] * V for _ in range(K)]
+            else:
+                S = [[Fraction(x) for x in row] for row in initial_state[n][h]]
+            hq = h // grp
+            for t in range(cu_seqlens[n], cu_seqlens[n + 1]):
+                at = Fraction(a[t][h])
+                S = [[at * S[i][j] for j in range(V)] for i in range(K)]
+                for w in range(n_h):
+                    kt = [Fraction(x) for x in k[t][w][hq]]
+                    vt = [Fraction(x) for x in v[t][w][h]]
+                    bt = Fraction(beta[t][w][h])
+                    r = _matT_vec(S, kt, K, V)
+                    u = [bt * (vt[j] - r[j]) for j in range(V)]
+                    S = [[S[i][j] + kt[i] * u[j] for j in range(V)] for i in range(K)]
+                qt = [Fraction(x) for x in q[t][hq]]
+                ot = _matT_vec(S, qt, K, V)
+                o[t][h] = [Fraction(scale) * x for x in ot]
+            per_head.append(S)
+        final.append(per_head)
+    return o, final
