@@ -6,13 +6,19 @@ its thin PyTorch binding:
 * :func:`chunk_gated_delta_rule` -- chunkwise forward (training / prefill,
   packed varlen via ``cu_seqlens``, optional slot-cache state I/O).
 * :func:`gated_delta_decode` -- one token per request on a slot-indexed
-  recurrent-state cache, ``-1`` = padding.
+  recurrent-state cache, ``-1`` = padding; :func:`gated_delta_decode_multi` for
+  several tokens per request.
+* ``*_fused_gates`` -- the same with g and beta computed in the kernels.
+* :func:`chunk_gated_delta_product`, :func:`gated_delta_product_decode` -- the Gated
+  Delta Product (several delta-rule writes per token).
 """
-from .api import (GdnError, chunk_fwd_path, chunk_gated_delta_rule,
+from .api import (GdnError, chunk_fwd_path, chunk_gated_delta_product, chunk_gated_delta_rule,
                   chunk_gated_delta_rule_fused_gates, chunk_workspace_size, gated_delta_decode,
-                  gated_delta_decode_fused_gates, gated_delta_decode_multi)
+                  gated_delta_decode_fused_gates, gated_delta_decode_multi,
+                  gated_delta_product_decode)
 
 __all__ = ["chunk_gated_delta_rule", "gated_delta_decode", "gated_delta_decode_multi",
-           "chunk_gated_delta_rule_fused_gates",
-           "gated_delta_decode_fused_gates", "chunk_workspace_size", "chunk_fwd_path", "GdnError"]
+           "chunk_gated_delta_rule_fused_gates", "gated_delta_decode_fused_gates",
+           "chunk_gated_delta_product", "gated_delta_product_decode",
+           "chunk_workspace_size", "chunk_fwd_path", "GdnError"]
 __version__ = "0.1.0"

@@ -21,8 +21,9 @@ GDN_F32, GDN_BF16 = 0, 1
 GDN_DEV_BAD_SLOT, GDN_DEV_BAD_CU_SEQLENS = 1, 2
 
 EXPORTS = ("gdn_chunk_fwd", "gdn_chunk_fwd_workspace_size", "gdn_chunk_fwd_path", "gdn_decode",
-           "gdn_chunk_fwd_gated", "gdn_decode_gated", "gdn_decode_multi", "gdn_status_string",
-           "gdn_version")
+           "gdn_chunk_fwd_gated", "gdn_decode_gated", "gdn_decode_multi", "gdn_chunk_fwd_noalloc",
+           "gdn_product_chunk_fwd", "gdn_product_chunk_fwd_workspace_size", "gdn_product_decode",
+           "gdn_status_string", "gdn_version")
 
 
 class GdnError(RuntimeError):
@@ -69,6 +70,14 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.gdn_decode_multi.argtypes = [vp, vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, i, i, i,
                                          f, i, vp, vp, vp, vp]
         lib.gdn_decode_multi.restype = i
+        lib.gdn_product_chunk_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, i,
+                                              vp, i, vp, i, vp, i, vp, i, vp, vp, sz, vp, vp]
+        lib.gdn_product_chunk_fwd.restype = i
+        lib.gdn_product_chunk_fwd_workspace_size.argtypes = [i, i, i, i, i, i, i, i, i, i]
+        lib.gdn_product_chunk_fwd_workspace_size.restype = sz
+        lib.gdn_product_decode.argtypes = [vp, vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, i, i, i,
+                                           f, i, vp, vp, vp, vp]
+        lib.gdn_product_decode.restype = i
         lib.gdn_status_string.argtypes = [i]
         lib.gdn_status_string.restype = ctypes.c_char_p
         lib.gdn_version.argtypes = []

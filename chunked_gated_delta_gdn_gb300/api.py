@@ -15,7 +15,8 @@ import torch
 from . import _lib
 
 __all__ = ["chunk_gated_delta_rule", "gated_delta_decode", "gated_delta_decode_multi",
-           "chunk_gated_delta_rule_fused_gates",
+           "chunk_gated_delta_rule_fused_gates", "chunk_gated_delta_product",
+           "gated_delta_product_decode",
            "gated_delta_decode_fused_gates", "chunk_workspace_size", "chunk_fwd_path", "GdnError"]
 
 GdnError = _lib.GdnError
@@ -304,4 +305,117 @@ def gated_delta_decode_multi(q, k, v, g, beta, ssm_state, batch_indices=None, sc
         int(bool(use_qk_l2norm_in_kernel)), _ptr(out), _ptr(intermediate_states),
         _ptr(dev_status), _stream(dev))
     _lib.check("gdn_decode_multi", st)
+    return out, intermediate_states
+
+
+def chunk_gated_delta_product(q, k, v, g, beta, scale=None, chunk_size=64, initial_state=None,
+                              output_final_state=False, use_qk_l2norm_in_kernel=False,
+                              cu_seqlens=None, *, state_indices=None, out=None, final_state=None,
+                              workspace=None, dev_status=None,
+                              **kwargs) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Gated Delta Product forward through ``gdn_product_chunk_fwd``: n_h delta-rule writes
+    per token ("Megatron-Core API: core.ssm.gated_delta_product", GatedDeltaProductMixer).
+
+    q [B, T, Hqk, K]; k [B, T, n_h, Hqk, K]; v [B, T, n_h, Hv, V]; g [B, T, Hv] fp32;
+    beta [B, T, n_h, Hv].  Every other argument as :func:`chunk_gated_delta_rule`.
+    Returns ``(o [B, T, Hv, V], final_state or None)``.
+    """
+    _need(q, "q", (torch.float32, torch.bfloat16))
+    dev, dt = q.device, q.dtype
+    if q.dim() != 4 or k.dim() != 5 or v.dim() != 5:
+        raise ValueError("q must be [B, T, Hqk, K], k [B, T, n_h, Hqk, K], v [B, T, n_h, Hv, V]")
+    B, T, Hqk, K = q.shape
+    n_h = k.shape[2]
+    Hv, V = v.shape[3], v.shape[4]
+    _need(k, "k", dt, dev, (B, T, n_h, Hqk, K))
+    _need(v, "v", dt, dev, (B, T, n_h, Hv, V))
+    _need(g, "g", torch.float32, dev, (B, T, Hv))
+    _need(beta, "beta", (dt, torch.float32), dev, (B, T, n_h, Hv))
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+        if B != 1:
+            raise ValueError("cu_seqlens requires B == 1")
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    num_slots = 0
+    if state_indices is not None:
+        _need(state_indices, "state_indices", torch.int32, dev, (N,))
+        cache = initial_state if initial_state is not None else final_state
+        if cache is None:
+            raise ValueError("state_indices needs initial_state or final_state (the slot cache)")
+        num_slots = cache.shape[0]
+        st_shape = (num_slots, Hv, K, V)
+        if output_final_state and final_state is None:
+            final_state = initial_state
+    else:
+        st_shape = (N, Hv, K, V)
+    if initial_state is not None:
+        _need(initial_state, "initial_state", torch.float32, dev, st_shape)
+    if output_final_state:
+        if final_state is None:
+            final_state = torch.empty(st_shape, dtype=torch.float32, device=dev)
+        _need(final_state, "final_state", torch.float32, dev, st_shape)
+    else:
+        final_state = None
+    if out is None:
+        out = torch.empty((B, T, Hv, V), dtype=dt, device=dev)
+    _need(out, "out", dt, dev, (B, T, Hv, V))
+    L = _lib.load()
+    need = L.gdn_product_chunk_fwd_workspace_size(B, T, n_h, Hqk, Hv, K, V, N, _DT[dt],
+                                                  _DT[beta.dtype])
+    if need == (1 << 64) - 1:
+        raise ValueError("sizes rejected by gdn_product_chunk_fwd")
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32, dev, (1,))
+    st = L.gdn_product_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), B, T, n_h, Hqk,
+                                 Hv, K, V, _DT[dt], _DT[beta.dtype], _scale(scale),
+                                 int(chunk_size), _ptr(initial_state),
+                                 int(bool(output_final_state)), _ptr(final_state),
+                                 int(bool(use_qk_l2norm_in_kernel)), _ptr(cu_seqlens), N,
+                                 _ptr(state_indices), num_slots, _ptr(out), _ptr(workspace),
+                                 ws_bytes, _ptr(dev_status), _stream(dev))
+    _lib.check("gdn_product_chunk_fwd", st)
+    return out, final_state
+
+
+def gated_delta_product_decode(q, k, v, g, beta, ssm_state, batch_indices=None, scale=None,
+                               use_qk_l2norm_in_kernel=True, output_intermediate_states=False, *,
+                               out=None, intermediate_states=None, dev_status=None):
+    """One Gated Delta Product token per request through ``gdn_product_decode``.
+
+    q [n, Hqk, K]; k [n, n_h, Hqk, K]; v [n, n_h, Hv, V]; g [n, Hv] fp32; beta [n, n_h, Hv];
+    ssm_state [num_slots, Hv, K, V] fp32, updated in place.  Returns ``(o [n, Hv, V],
+    intermediate_states [n, n_h, Hv, K, V] or None)``.
+    """
+    _need(q, "q", (torch.float32, torch.bfloat16))
+    dev, dt = q.device, q.dtype
+    if q.dim() != 3 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q must be [n, Hqk, K], k [n, n_h, Hqk, K], v [n, n_h, Hv, V]")
+    n, Hqk, K = q.shape
+    n_h = k.shape[1]
+    Hv, V = v.shape[2], v.shape[3]
+    _need(k, "k", dt, dev, (n, n_h, Hqk, K))
+    _need(v, "v", dt, dev, (n, n_h, Hv, V))
+    _need(g, "g", torch.float32, dev, (n, Hv))
+    _need(beta, "beta", (dt, torch.float32), dev, (n, n_h, Hv))
+    _need(ssm_state, "ssm_state", torch.float32, dev)
+    if batch_indices is not None:
+        _need(batch_indices, "batch_indices", torch.int32, dev, (n,))
+    if out is None:
+        out = torch.empty((n, Hv, V), dtype=dt, device=dev)
+    _need(out, "out", dt, dev, (n, Hv, V))
+    if output_intermediate_states and intermediate_states is None:
+        intermediate_states = torch.empty((n, n_h, Hv, K, V), dtype=torch.float32, device=dev)
+    if intermediate_states is not None:
+        _need(intermediate_states, "intermediate_states", torch.float32, dev, (n, n_h, Hv, K, V))
+    st = _lib.load().gdn_product_decode(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(ssm_state), ssm_state.shape[0],
+        _ptr(batch_indices), n, n_h, Hqk, Hv, K, V, _DT[dt], _DT[beta.dtype], _scale(scale),
+        int(bool(use_qk_l2norm_in_kernel)), _ptr(out), _ptr(intermediate_states),
+        _ptr(dev_status), _stream(dev))
+    _lib.check("gdn_product_decode", st)
     return out, intermediate_states

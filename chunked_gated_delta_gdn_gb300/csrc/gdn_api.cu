@@ -184,7 +184,7 @@ static gdn_status_t decode_impl(const void* q, const void* k, const void* v, con
                                 gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype, float scale,
                                 int use_qk_l2norm, void* o, int* dev_status, void* stream,
                                 const gdn::GateArgs& gates, int L = 1,
-                                float* intermediate = nullptr) {
+                                float* intermediate = nullptr, int product = 0) {
   gdn_status_t st = check_chunk_shapes(1, 1, Hqk, Hv, K, V, io_dtype, beta_dtype);
   if (st != GDN_OK) return st;
   if (n < 0 || num_slots < 0 || L < 0) return GDN_ERR_SHAPE;
@@ -214,6 +214,7 @@ static gdn_status_t decode_impl(const void* q, const void* k, const void* v, con
   a.gates = gates;
   a.L = L;
   a.intermediate = intermediate;
+  a.product = product;
   return gdn::launch_decode(a) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -258,6 +259,104 @@ gdn_status_t gdn_decode_gated(const void* q, const void* k, const void* v, const
   gates.dt_bias = dt_bias;
   return decode_impl(q, k, v, nullptr, nullptr, ssm_state, num_slots, batch_indices, n, Hqk, Hv,
                      K, V, io_dtype, io_dtype, scale, use_qk_l2norm, o, dev_status, stream, gates);
+}
+
+// ---- Gated Delta Product ("Megatron-Core API: core.ssm.gated_delta_product")
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Workspace of the product's chunk forward: q', g', o' over the T * n_h writes, the scaled
+// cu_seqlens, then the chunk kernels' own workspace for the write sequence.
+static size_t product_ws_parts(int B, int T, int n_h, int Hqk, int Hv, int K, int V, int num_seqs,
+                               int io_dtype, int beta_dtype, size_t* inner_off) {
+  const size_t te = (size_t)B * T * n_h, es = elem_size(io_dtype);
+  size_t off = align256(te * Hqk * K * es) + align256(te * Hv * 4) + align256(te * Hv * V * es) +
+               align256(((size_t)num_seqs + 1) * 4);
+  *inner_off = off;
+  return off + gdn_chunk_fwd_workspace_size(B, T * n_h, Hqk, Hv, K, V, num_seqs,
+                                            (gdn_dtype_t)io_dtype, (gdn_dtype_t)beta_dtype);
+}
+
+size_t gdn_product_chunk_fwd_workspace_size(int B, int T, int n_h, int Hqk, int Hv, int K, int V,
+                                            int num_seqs, gdn_dtype_t io_dtype,
+                                            gdn_dtype_t beta_dtype) {
+  if (n_h < 1 || B < 0 || T < 0 || num_seqs < 0 || (long long)B * T * n_h > 0x7fffffffLL)
+    return (size_t)-1;
+  if (check_chunk_shapes(B, T * n_h, Hqk, Hv, K, V, io_dtype, beta_dtype) != GDN_OK)
+    return (size_t)-1;
+  if (n_h == 1) return gdn_chunk_fwd_workspace_size(B, T, Hqk, Hv, K, V, num_seqs, io_dtype, beta_dtype);
+  size_t inner;
+  return product_ws_parts(B, T, n_h, Hqk, Hv, K, V, num_seqs, io_dtype, beta_dtype, &inner);
+}
+
+gdn_status_t gdn_product_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                                   const void* beta, int B, int T, int n_h, int Hqk, int Hv, int K,
+                                   int V, gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype,
+                                   float scale, int chunk_size, const float* initial_state,
+                                   int output_final_state, float* final_state, int use_qk_l2norm,
+                                   const int32_t* cu_seqlens, int num_seqs,
+                                   const int32_t* state_indices, int num_slots, void* o,
+                                   void* workspace, size_t workspace_bytes, int* dev_status,
+                                   void* stream) {
+  if (n_h < 1 || B < 0 || T < 0 || (long long)B * T * n_h > 0x7fffffffLL) return GDN_ERR_SHAPE;
+  gdn::GateArgs gates{};
+  gates.mode = gdn::kGatesGiven;
+  if (n_h == 1)   // one write per token: the gated delta rule itself
+    return chunk_impl(q, k, v, g, beta, B, T, Hqk, Hv, K, V, io_dtype, beta_dtype, scale,
+                      chunk_size, initial_state, output_final_state, final_state, use_qk_l2norm,
+                      cu_seqlens, num_seqs, state_indices, num_slots, o, workspace,
+                      workspace_bytes, dev_status, stream, gates);
+  gdn_status_t st = check_chunk_shapes(B, T * n_h, Hqk, Hv, K, V, io_dtype, beta_dtype);
+  if (st != GDN_OK) return st;
+  if (chunk_size != 64) return GDN_ERR_UNSUPPORTED;
+  if (cu_seqlens) {
+    if (B != 1 || num_seqs < 0) return GDN_ERR_SHAPE;
+  } else {
+    num_seqs = B;
+  }
+  const long long T_total = (long long)B * T;
+  if (T_total > 0 && (!q || !k || !v || !o || !g || !beta)) return GDN_ERR_NULL;
+  if (T_total > 0 && (!aligned16(q) || !aligned16(o) || ((uintptr_t)g & 3u)))
+    return GDN_ERR_LAYOUT;
+  size_t inner_off;
+  const size_t need = product_ws_parts(B, T, n_h, Hqk, Hv, K, V, num_seqs, io_dtype, beta_dtype,
+                                       &inner_off);
+  if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE;
+  if (((uintptr_t)workspace & 255u) != 0) return GDN_ERR_LAYOUT;
+  const size_t te = (size_t)T_total * n_h, es = elem_size(io_dtype);
+  uint8_t* w = reinterpret_cast<uint8_t*>(workspace);
+  void* q_exp = w;
+  float* g_exp = reinterpret_cast<float*>(w + align256(te * Hqk * K * es));
+  void* o_exp = w + align256(te * Hqk * K * es) + align256(te * Hv * 4);
+  int32_t* cu_exp = reinterpret_cast<int32_t*>(w + align256(te * Hqk * K * es) +
+                                               align256(te * Hv * 4) + align256(te * Hv * V * es));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (gdn::launch_product_expand(q, g, q_exp, g_exp, cu_seqlens, cu_exp, T_total, n_h, Hqk, Hv,
+                                 K, io_dtype, num_seqs, s) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  st = chunk_impl(q_exp, k, v, g_exp, beta, B, T * n_h, Hqk, Hv, K, V, io_dtype, beta_dtype,
+                  scale, chunk_size, initial_state, output_final_state, final_state,
+                  use_qk_l2norm, cu_seqlens ? cu_exp : nullptr, num_seqs, state_indices,
+                  num_slots, o_exp, w + inner_off, workspace_bytes - inner_off, dev_status,
+                  stream, gates);
+  if (st != GDN_OK) return st;
+  return gdn::launch_product_gather(o_exp, o, T_total, n_h, Hv, V, io_dtype, s) == cudaSuccess
+             ? GDN_OK
+             : GDN_ERR_CUDA;
+}
+
+gdn_status_t gdn_product_decode(const void* q, const void* k, const void* v, const float* g,
+                                const void* beta, float* ssm_state, int num_slots,
+                                const int32_t* batch_indices, int n, int n_h, int Hqk, int Hv,
+                                int K, int V, gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype,
+                                float scale, int use_qk_l2norm, void* o,
+                                float* intermediate_states, int* dev_status, void* stream) {
+  if (n_h < 1) return GDN_ERR_SHAPE;
+  gdn::GateArgs gates{};
+  gates.mode = gdn::kGatesGiven;
+  return decode_impl(q, k, v, g, beta, ssm_state, num_slots, batch_indices, n, Hqk, Hv, K, V,
+                     io_dtype, beta_dtype, scale, use_qk_l2norm, o, dev_status, stream, gates,
+                     n_h, intermediate_states, 1);
 }
 
 }  // extern "C"

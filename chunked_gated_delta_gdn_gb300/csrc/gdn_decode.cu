@@ -14,6 +14,11 @@
 // GatedDeltaProductMixer.ssm_decode; the in-kernel skip discussed on "Add GDN
 // dynamic inference", review thread).  The kernel is HBM-bound: 2 * K * V * 4
 // bytes of state traffic per real (request, head), under 1 FLOP per byte.
+//
+// With L > 1 the L tokens of a request are applied in order with the state held in
+// registers.  In product mode (the Gated Delta Product's decode step, same page) the L
+// entries are the n_h writes of one token: the decay goes with the first write, the
+// request's single query reads the state after the last, and only that output is written.
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 
@@ -62,7 +67,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode128_kernel(const Deco
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int s = resolve_slot(a, i);
   if (s < 0) {
-    for (int t = 0; t < a.L; ++t) zero_output(a, i * a.L + t, h);
+    if (a.product) zero_output(a, i, h);
+    else for (int t = 0; t < a.L; ++t) zero_output(a, i * a.L + t, h);
     return;
   }
   const int hq = h / (a.Hv / a.Hqk);
@@ -84,7 +90,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode128_kernel(const Deco
     if (t > 0) __syncthreads();   // sq / sk / red of the previous token fully consumed
     // q and k: threads 0..127 take q, 128..255 take k; per-vector sums of squares.
     const size_t qk_off = ((size_t)it * a.Hqk + hq) * K;
-    const float x = tid < K ? load_elem(a.q, qk_off + tid, a.io_dtype)
+    const size_t q_off = a.product ? ((size_t)i * a.Hqk + hq) * K : qk_off;
+    const float x = tid < K ? load_elem(a.q, q_off + tid, a.io_dtype)
                             : load_elem(a.k, qk_off + tid - K, a.io_dtype);
     const float ss = warp_sum(x * x);
     if (lane == 0) wsum[warp] = ss;
@@ -126,8 +133,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode128_kernel(const Deco
 
     const size_t hv_off = (size_t)it * a.Hv + h;
     float gv, bt;
-    gate_values(a, hv_off, h, &gv, &bt);
+    if (a.product) {   // the token's decay on its first write only
+      gv = (t == 0) ? a.g[(size_t)i * a.Hv + h] : 0.f;
+      bt = load_elem(a.beta, hv_off, a.beta_dtype);
+    } else {
+      gate_values(a, hv_off, h, &gv, &bt);
+    }
     const float dec = expf(gv);
+    const bool write_o = !a.product || t == a.L - 1;
+    const size_t o_row = a.product ? (size_t)i * a.Hv + h : hv_off;
     const float kq = wdot[0] + wdot[1] + wdot[2] + wdot[3];
     float u[4], o[4];
 #pragma unroll
@@ -138,16 +152,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode128_kernel(const Deco
       u[c] = bt * (vv - dec * r);
       o[c] = a.scale * (dec * p + kq * u[c]);
     }
-    if (warp < 4 && lane < 8) {
+    if (write_o && warp < 4 && lane < 8) {
       if (a.io_dtype == GDN_BF16) {
         __nv_bfloat162 lo = __floats2bfloat162_rn(o[0], o[1]);
         __nv_bfloat162 hi = __floats2bfloat162_rn(o[2], o[3]);
         uint2 pk;
         pk.x = *reinterpret_cast<uint32_t*>(&lo);
         pk.y = *reinterpret_cast<uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.o) + hv_off * V + col) = pk;
+        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.o) + o_row * V + col) = pk;
       } else {
-        *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.o) + hv_off * V + col) =
+        *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.o) + o_row * V + col) =
             make_float4(o[0], o[1], o[2], o[3]);
       }
     }
@@ -176,7 +190,8 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_generic_kernel(const De
   const int tid = threadIdx.x;
   const int s = resolve_slot(a, i);
   if (s < 0) {
-    for (int t = 0; t < a.L; ++t) zero_output(a, i * a.L + t, h);
+    if (a.product) zero_output(a, i, h);
+    else for (int t = 0; t < a.L; ++t) zero_output(a, i * a.L + t, h);
     return;
   }
   const int hq = h / (a.Hv / a.Hqk);
@@ -187,9 +202,10 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_generic_kernel(const De
     const int it = i * a.L + t;
     if (t > 0) __syncthreads();
     const size_t qk_off = ((size_t)it * a.Hqk + hq) * K;
+    const size_t q_off = a.product ? ((size_t)i * a.Hqk + hq) * K : qk_off;
     float xq = 0.f, xk = 0.f;
     if (tid < K) {
-      xq = load_elem(a.q, qk_off + tid, a.io_dtype);
+      xq = load_elem(a.q, q_off + tid, a.io_dtype);
       xk = load_elem(a.k, qk_off + tid, a.io_dtype);
     }
     float s1 = warp_sum(xq * xq), s2 = warp_sum(xk * xk), s3 = warp_sum(xq * xk);
@@ -204,8 +220,15 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_generic_kernel(const De
     __syncthreads();
     const size_t hv_off = (size_t)it * a.Hv + h;
     float gv, bt;
-    gate_values(a, hv_off, h, &gv, &bt);
+    if (a.product) {   // the token's decay on its first write only
+      gv = (t == 0) ? a.g[(size_t)i * a.Hv + h] : 0.f;
+      bt = load_elem(a.beta, hv_off, a.beta_dtype);
+    } else {
+      gate_values(a, hv_off, h, &gv, &bt);
+    }
     const float dec = expf(gv);
+    const bool write_o = !a.product || t == a.L - 1;
+    const size_t o_row = a.product ? (size_t)i * a.Hv + h : hv_off;
     if (tid < V) {
       float r = 0.f, p = 0.f;
       for (int row = 0; row < K; ++row) {
@@ -215,7 +238,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_generic_kernel(const De
       }
       const float u = bt * (load_elem(a.v, hv_off * V + tid, a.io_dtype) - dec * r);
       su[tid] = u;
-      store_elem(a.o, hv_off * V + tid, a.scale * (dec * p + kq * u), a.io_dtype);
+      if (write_o) store_elem(a.o, o_row * V + tid, a.scale * (dec * p + kq * u), a.io_dtype);
     }
     __syncthreads();
     float* inter = a.intermediate ? a.intermediate + hv_off * (size_t)K * V : nullptr;

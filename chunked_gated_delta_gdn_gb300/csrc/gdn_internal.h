@@ -67,6 +67,9 @@ struct DecodeArgs {
   GateArgs gates;
   int L;                // tokens per request (1 for the single-token step)
   float* intermediate;  // [n, L, Hv, K, V] state after every token, or NULL
+  int product;          // 1: Gated Delta Product -- the L entries of a request are the
+                        // writes of one token: q [n, Hqk, K] and g [n, Hv] per request,
+                        // decay on the first write, output [n, Hv, V] after the last
 };
 
 // Upper bound on the number of 64-token chunks over all sequences.
@@ -83,5 +86,15 @@ bool chunk_tc_supported(int K, int V, int io_dtype, int beta_dtype);
 cudaError_t launch_chunk_tc(const ChunkArgs& a);
 
 cudaError_t launch_decode(const DecodeArgs& a);
+
+// Gated Delta Product as the gated delta rule over the sequence of writes: q' (the query on
+// the last write of each token), g' (the decay on the first), n_h * cu_seqlens, and the
+// output rows of the last writes gathered back.
+cudaError_t launch_product_expand(const void* q, const float* g, void* q_exp, float* g_exp,
+                                  const int32_t* cu, int32_t* cu_exp, long long T_total, int n_h,
+                                  int Hqk, int Hv, int K, int io_dtype, int num_seqs,
+                                  cudaStream_t stream);
+cudaError_t launch_product_gather(const void* o_exp, void* o, long long T_total, int n_h, int Hv,
+                                  int V, int io_dtype, cudaStream_t stream);
 
 }  // namespace gdn

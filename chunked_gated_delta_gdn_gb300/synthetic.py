@@ -25,8 +25,8 @@ from typing import Optional
 
 import torch
 
-__all__ = ["ChunkInputs", "DecodeInputs", "chunk_inputs", "decode_inputs", "WORKLOADS",
-           "varlen_lengths"]
+__all__ = ["ChunkInputs", "DecodeInputs", "ProductInputs", "chunk_inputs", "decode_inputs",
+           "product_inputs", "product_decode_inputs", "WORKLOADS", "varlen_lengths"]
 
 
 @dataclasses.dataclass
@@ -180,3 +180,63 @@ def workload(name: str, **overrides):
     if spec.get("kind") == "decode":
         return decode_inputs(**spec)
     return chunk_inputs(**spec)
+
+
+@dataclasses.dataclass
+class ProductInputs:
+    q: torch.Tensor            # [B, T, Hqk, K]          (decode: [n, Hqk, K])
+    k: torch.Tensor            # [B, T, n_h, Hqk, K]     (decode: [n, n_h, Hqk, K])
+    v: torch.Tensor            # [B, T, n_h, Hv, V]      (decode: [n, n_h, Hv, V])
+    g: torch.Tensor            # [B, T, Hv] fp32         (decode: [n, Hv])
+    beta: torch.Tensor         # [B, T, n_h, Hv]         (decode: [n, n_h, Hv])
+    state: Optional[torch.Tensor]           # initial states [N, ...], or the slot cache
+    cu_seqlens: Optional[torch.Tensor]
+    slots: Optional[torch.Tensor]           # state_indices (chunk) / batch_indices (decode)
+
+
+def product_inputs(n_h=2, B=1, T=None, Hqk=2, Hv=4, K=128, V=128, dtype=torch.bfloat16,
+                   lengths=None, init="randn", num_slots=None, seed=0) -> ProductInputs:
+    """Inputs for the Gated Delta Product chunked forward: n_h writes per token, each with its
+    own key, value and beta (same distributions as :func:`chunk_inputs`).  ``lengths`` gives
+    packed varlen sequences; ``init``: "none", "randn" or "slots" (a ``num_slots`` cache)."""
+    gen = torch.Generator().manual_seed(seed)
+    cu = None
+    if lengths is not None:
+        cu = torch.zeros(len(lengths) + 1, dtype=torch.int32)
+        cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
+        B, T = 1, int(cu[-1])
+        N = len(lengths)
+    else:
+        N = B
+    q = _randn(gen, (B, T, Hqk, K)).to(dtype)
+    k = _randn(gen, (B, T, n_h, Hqk, K)).to(dtype)
+    v = _randn(gen, (B, T, n_h, Hv, V)).to(dtype)
+    g = (-torch.nn.functional.softplus(_randn(gen, (B, T, Hv)))).to(torch.float32).contiguous()
+    beta = torch.sigmoid(_randn(gen, (B, T, n_h, Hv))).to(dtype)
+    state, slots = None, None
+    if init == "randn":
+        state = 0.1 * _randn(gen, (N, Hv, K, V))
+    elif init == "slots":
+        state = 0.1 * _randn(gen, (num_slots, Hv, K, V))
+        slots = torch.randperm(num_slots, generator=gen)[:N].to(torch.int32)
+    elif init != "none":
+        raise ValueError("unknown init %r" % init)
+    return ProductInputs(q=q, k=k, v=v, g=g, beta=beta, state=state, cu_seqlens=cu, slots=slots)
+
+
+def product_decode_inputs(n_h=2, n=32, Hqk=2, Hv=4, K=128, V=128, dtype=torch.bfloat16,
+                          num_slots=48, pad_frac=0.125, seed=0) -> ProductInputs:
+    """One Gated Delta Product token per request on a ``num_slots`` cache; batch_indices as
+    in :func:`decode_inputs` (a seeded permutation prefix with padding entries set to -1)."""
+    gen = torch.Generator().manual_seed(seed)
+    q = _randn(gen, (n, Hqk, K)).to(dtype)
+    k = _randn(gen, (n, n_h, Hqk, K)).to(dtype)
+    v = _randn(gen, (n, n_h, Hv, V)).to(dtype)
+    g = (-torch.nn.functional.softplus(_randn(gen, (n, Hv)))).to(torch.float32).contiguous()
+    beta = torch.sigmoid(_randn(gen, (n, n_h, Hv))).to(dtype)
+    cache = 0.1 * _randn(gen, (num_slots, Hv, K, V))
+    idx = torch.randperm(num_slots, generator=gen)[:n].to(torch.int32)
+    npad = int(round(pad_frac * n))
+    if npad:
+        idx[torch.randperm(n, generator=gen)[:npad]] = -1
+    return ProductInputs(q=q, k=k, v=v, g=g, beta=beta, state=cache, cu_seqlens=None, slots=idx)

@@ -229,6 +229,57 @@ gdn_status_t gdn_decode_gated(const void* q, const void* k, const void* v, const
                               int* dev_status, void* stream);
 
 /*
+ * Gated Delta Product ("Megatron-Core API: core.ssm.gated_delta_product",
+ * GatedDeltaProductMixer: each token is projected into the V, K, Q, beta and decay terms
+ * of a sequence of Householder updates, num_householder = n_h of them; the forked
+ * inference kernels chunk at a fixed 64, ssm_inference_chunk_size).  Per token t, with
+ * the decay applied once before the first write and the token's single query reading the
+ * state after the last write:
+ *
+ *     S <- exp(g_t) S;   for j = 0..n_h-1:  S <- S + k_tj (beta_tj (v_tj - S^T k_tj))^T;
+ *     o_t = scale * S^T q_t
+ *
+ * (q_t and every k_tj L2-normalised in-kernel when use_qk_l2norm).  n_h = 1 is the gated
+ * delta rule.  Layouts, writes of a token consecutive:
+ *   q [B, T, Hqk, K];  k [B, T, n_h, Hqk, K];  v [B, T, n_h, Hv, V];  g [B, T, Hv] fp32;
+ *   beta [B, T, n_h, Hv] (fp32 or io_dtype);  o [B, T, Hv, V].
+ * Every other argument -- scale, chunk_size (64), initial / final states, cu_seqlens (in
+ * tokens), state_indices slot caching, dev_status, stream -- and every error rule as in
+ * gdn_chunk_fwd.  The workspace (gdn_product_chunk_fwd_workspace_size bytes, 256-byte
+ * aligned, caller-owned) holds the query and decay of every write, the outputs of all
+ * writes and the chunk kernels' own scratch; n_h = 1 needs only the latter.
+ */
+size_t gdn_product_chunk_fwd_workspace_size(int B, int T, int n_h, int Hqk, int Hv, int K, int V,
+                                            int num_seqs, gdn_dtype_t io_dtype,
+                                            gdn_dtype_t beta_dtype);
+
+gdn_status_t gdn_product_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                                   const void* beta, int B, int T, int n_h, int Hqk, int Hv, int K,
+                                   int V, gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype,
+                                   float scale, int chunk_size, const float* initial_state,
+                                   int output_final_state, float* final_state, int use_qk_l2norm,
+                                   const int32_t* cu_seqlens, int num_seqs,
+                                   const int32_t* state_indices, int num_slots, void* o,
+                                   void* workspace, size_t workspace_bytes, int* dev_status,
+                                   void* stream);
+
+/*
+ * One Gated Delta Product token per request on the slot cache (the decode step of
+ * GatedDeltaProductMixer.ssm_decode, same page):
+ *   q [n, Hqk, K];  k [n, n_h, Hqk, K];  v [n, n_h, Hv, V];  g [n, Hv] fp32;
+ *   beta [n, n_h, Hv];  o [n, Hv, V];
+ *   intermediate_states  NULL, or [n, n_h, Hv, K, V] fp32: the state after every write.
+ * Slots, padding (-1: zero output row, no state access), defaults and errors as in
+ * gdn_decode.
+ */
+gdn_status_t gdn_product_decode(const void* q, const void* k, const void* v, const float* g,
+                                const void* beta, float* ssm_state, int num_slots,
+                                const int32_t* batch_indices, int n, int n_h, int Hqk, int Hv,
+                                int K, int V, gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype,
+                                float scale, int use_qk_l2norm, void* o,
+                                float* intermediate_states, int* dev_status, void* stream);
+
+/*
  * gdn_chunk_fwd_noalloc -- gdn_chunk_fwd without caller-provided scratch.
  *
  * The sources have no counterpart for this entry point; it exists for callers

@@ -448,11 +448,11 @@ int gdn_oracle_product(const double* q, const double* k, const double* v, const 
       double* kn = qn + K;
       double* r = kn + K;
       const size_t soff = ((size_t)n * Hv + h) * K * V;
+      const int hq = h / group;   /* query / key head of value head h */
       if (initial_state)
         memcpy(S, initial_state + soff, sizeof(double) * K * V);
       else
         memset(S, 0, sizeof(double) * K * V);
-      const int hq = h / group;
       for (int64_t t = cu_seqlens[n]; t < cu_seqlens[n + 1]; ++t) {
         const double a = exp(g[(size_t)t * Hv + h]);
         for (size_t x = 0; x < (size_t)K * V; ++x) S[x] *= a;

@@ -114,3 +114,39 @@ def test_python_binding_validates_on_cpu_tensors():
     with pytest.raises(ValueError, match="CUDA"):
         gated_delta_decode(x[0], x[0], x[0], torch.zeros(4, 1), torch.zeros(4, 1),
                            torch.zeros(2, 1, 8, 8))
+
+
+def product_call(**kw):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, B=1, T=64, n_h=2, Hqk=1, Hv=1, K=64,
+                V=64, io=_lib.GDN_F32, bdt=_lib.GDN_F32, scale=float("nan"), chunk=64, init=None,
+                ofs=0, fin=None, l2=1, cu=None, N=1, si=None, slots=0, o=FAKE, ws=None, wsb=0,
+                status=None, stream=None)
+    args.update(kw)
+    return _lib.load().gdn_product_chunk_fwd(*args.values())
+
+
+def test_product_entry_points_reject_bad_arguments():
+    lib = _lib.load()
+    assert product_call(n_h=0) == _lib.GDN_ERR_SHAPE
+    assert product_call(chunk=32) == _lib.GDN_ERR_UNSUPPORTED
+    assert product_call(q=None) == _lib.GDN_ERR_NULL
+    assert product_call(Hv=3, Hqk=2) == _lib.GDN_ERR_SHAPE
+    assert product_call(q=FAKE + 4) == _lib.GDN_ERR_LAYOUT
+    assert product_call(ws=None, wsb=0) == _lib.GDN_ERR_WORKSPACE
+    need = lib.gdn_product_chunk_fwd_workspace_size(1, 64, 2, 1, 1, 64, 64, 1, 0, 0)
+    assert need != (1 << 64) - 1
+    assert product_call(ws=FAKE, wsb=need - 1) == _lib.GDN_ERR_WORKSPACE
+    assert product_call(ws=FAKE + 16, wsb=need) == _lib.GDN_ERR_LAYOUT   # needs 256-byte alignment
+    # the workspace holds q', g', o' of the 128 writes plus the chunk kernels' own scratch
+    assert need >= 128 * 64 * 4 + 128 * 4 + 128 * 64 * 4 + \
+        lib.gdn_chunk_fwd_workspace_size(1, 128, 1, 1, 64, 64, 1, 0, 0)
+    assert lib.gdn_product_chunk_fwd_workspace_size(1, 64, 0, 1, 1, 64, 64, 1, 0, 0) == (1 << 64) - 1
+    # one write per token is the gated delta rule: same scratch
+    assert lib.gdn_product_chunk_fwd_workspace_size(1, 64, 1, 1, 1, 64, 64, 1, 0, 0) == \
+        lib.gdn_chunk_fwd_workspace_size(1, 64, 1, 1, 64, 64, 1, 0, 0)
+    dec = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 8, None, 4, 2, 1, 1, 128, 128, _lib.GDN_BF16,
+           _lib.GDN_BF16, float("nan"), 1, FAKE, None, None, None]
+    bad = list(dec); bad[9] = 0
+    assert lib.gdn_product_decode(*bad) == _lib.GDN_ERR_SHAPE
+    bad = list(dec); bad[5] = None
+    assert lib.gdn_product_decode(*bad) == _lib.GDN_ERR_NULL
