@@ -135,6 +135,62 @@ def cpu_oracle_sample(inp, tokens, nthreads=0):
     return dt, (nthreads or oracle.max_threads())
 
 
+def measure_product(dev, seed, steps=10, warmup=3):
+    """The Gated Delta Product next to the headline: chunked forward on one 8192-token
+    sequence with n_h = 2 writes per token and a decode step of 256 requests (26 padding) on
+    a 512-slot cache, same head shapes.  CUDA events on the current stream, after warm-up."""
+    from chunked_gated_delta_gdn_gb300 import (chunk_gated_delta_product,
+                                               gated_delta_product_decode, synthetic)
+    n_h, T = 2, 8192
+    cin = synthetic.product_inputs(n_h=n_h, B=1, T=T, Hqk=HQK_, Hv=HV_, K=K_, V=V_,
+                                   dtype=torch.bfloat16, init="randn", seed=seed)
+    d = {k: getattr(cin, k).to(dev) for k in ("q", "k", "v", "g", "beta", "state")}
+    o = torch.empty(1, T, HV_, V_, dtype=torch.bfloat16, device=dev)
+    fin = torch.empty_like(d["state"])
+    ws = torch.empty(_product_ws(T, n_h), dtype=torch.uint8, device=dev)
+    din = synthetic.product_decode_inputs(n_h=n_h, n=256, Hqk=HQK_, Hv=HV_, K=K_, V=V_,
+                                          dtype=torch.bfloat16, num_slots=512, pad_frac=0.1,
+                                          seed=seed + 1)
+    dd = {k: getattr(din, k).to(dev) for k in ("q", "k", "v", "g", "beta", "state", "slots")}
+    od = torch.empty(256, HV_, V_, dtype=torch.bfloat16, device=dev)
+    n_real = int((din.slots >= 0).sum())
+
+    def chunk():
+        chunk_gated_delta_product(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                  initial_state=d["state"], output_final_state=True,
+                                  use_qk_l2norm_in_kernel=True, out=o, final_state=fin,
+                                  workspace=ws)
+
+    def decode():
+        gated_delta_product_decode(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dd["state"],
+                                   dd["slots"], out=od)
+
+    res = {}
+    for name, fn in (("chunk", chunk), ("decode", decode)):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        res[name] = e0.elapsed_time(e1) / steps / 1000.0
+    return {"workload": "Gated Delta Product, n_h=2 writes per token, Hqk=16 Hv=32 K=V=128 bf16",
+            "chunk": {"tokens": T, "ms": res["chunk"] * 1e3, "tokens_per_s": T / res["chunk"],
+                      "writes_per_s": T * n_h / res["chunk"]},
+            "decode": {"requests": 256, "padding": 256 - n_real, "ms": res["decode"] * 1e3,
+                       "requests_per_s": n_real / res["decode"],
+                       "state_gbs": n_real * HV_ * STATE_BYTES * 2 / res["decode"] / 1e9}}
+
+
+def _product_ws(T, n_h):
+    from chunked_gated_delta_gdn_gb300 import _lib
+    return int(_lib.load().gdn_product_chunk_fwd_workspace_size(1, T, n_h, HQK_, HV_, K_, V_, 1,
+                                                                _lib.GDN_BF16, _lib.GDN_BF16))
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -199,6 +255,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override B of the chunked workload (profiling runs on a smaller case)")
+    ap.add_argument("--no-product", action="store_true",
+                    help="skip the Gated Delta Product measurement reported beside the headline")
     ap.add_argument("--only", choices=["chunk", "decode"], default=None,
                     help="time one half of the step (profiling); the JSON line stays the same")
     args = ap.parse_args()
@@ -334,6 +392,8 @@ def main():
         "gpu_launches": launches_per_step * K,
         "clocks": clk.summary(),
     }
+    if args.only is None and not args.no_product:
+        line["product"] = measure_product(dev, 1006 + 1000 * rank)
     if args.only == "chunk":      # profiling runs: the half that was not timed is not reported
         line["decode"] = None
     elif args.only == "decode":
