@@ -59,15 +59,12 @@ constexpr uint32_t OFF_QK = 0;          // 2 stages x 32 KB: [dk half][Q rows 0-
 constexpr uint32_t QK_STAGE = 32768;
 constexpr uint32_t OFF_V = 65536;       // 2 stages x 16 KB: [dv half][64 tokens][128 B]
 constexpr uint32_t V_STAGE = 16384;
-constexpr uint32_t OFF_S = 98304;       // S^T bf16, A operand: [dk half][128 dv rows][128 B]; after
-                                        // the MMAs that read it, the bf16 output tile staged for a
-                                        // TMA store
+constexpr uint32_t OFF_S = 98304;       // the bf16 output tile staged for its TMA store (16 KB)
 constexpr uint32_t OFF_KT = 131072;     // K rows scaled by exp(G_last - G_t) r_k[t], bf16: the
                                         // state update's MN-major B, [dk half][64 tokens][128 B]
 constexpr uint32_t OFF_A = 147456;      // fp32 A [64][64], 16-byte-group swizzled; the solve
                                         // overwrites its strictly-lower blocks with those of T
 constexpr uint32_t OFF_P = 163840;      // 2 x P, K-major B [64 i][64 j]
-constexpr uint32_t OFF_U = 180224;      // U'^T bf16, K-major A [128 dv][64 tokens]
 constexpr uint32_t OFF_TW = 196608;     // (T diag(beta exp(G) r_k))^T, MN-major B [64 j][64 i]
 constexpr uint32_t OFF_TU = 204800;     // (T diag(beta))^T, MN-major B
 constexpr uint32_t OFF_VEC = 212992;    // 2 x per-token fp32 vectors [8][64]
@@ -81,7 +78,9 @@ constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the bas
 
 constexpr uint32_t STAGE_TX = QK_STAGE + V_STAGE;  // Q + K + V bytes per stage = 48 KB
 
-// TMEM columns (fp32, 128 lanes).  COL_S holds S^T for the whole sequence.
+// TMEM columns (fp32, 128 lanes).  COL_S holds S^T for the whole sequence.  Three products
+// read their A operand from TMEM as bf16 (two per 32-bit column): S^T (in the O2 columns,
+// until O2 is written), -Y (in its own first 32 columns) and U' (in the first 32 of U's).
 constexpr uint32_t COL_D1 = 0 /* 128 */, COL_U = 128, COL_O1 = 192, COL_Y = 256 /* O1 | Y adjacent */,
                    COL_O2 = 320, COL_S = 384, TMEM_COLS = 512;
 
@@ -545,36 +544,43 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
                  sdesc_sw128(sbase + OFF_TU + ks * 2048, 8192, 1024), id, ks > 0);
       }
     }
-    // ---- S (entry state) -> bf16 A operand S^T [dv rows][dk]; S <- exp(G_last) S in TMEM
+    // ---- S (entry state) -> bf16 S^T in the O2 columns (the next product's A operand);
+    //      S <- exp(G_last) S in TMEM
     {
       const float dl = ex2(vec[VEC_G + L - 1]);
 #pragma unroll
-      for (int part = 0; part < 4; ++part) {
-        float x[32];
-        const uint32_t col = COL_S + 32 * part;
-        tmem_ld32(tbase + lane_off + col, x);
-        uint8_t* dst = sm + OFF_S + (part >> 1) * 16384;
+      for (int pair = 0; pair < 2; ++pair) {
+        float pk[32];
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
-          store_bf16x8(dst + sw128_offset(row, 32 * (part & 1) + 8 * m), &x[8 * m]);
+        for (int sub = 0; sub < 2; ++sub) {
+          float x[32];
+          const uint32_t col = COL_S + 32 * (2 * pair + sub);
+          tmem_ld32(tbase + lane_off + col, x);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] *= dl;
-        tmem_st32(tbase + lane_off + col, x);
+          for (int jj = 0; jj < 16; ++jj) {
+            __nv_bfloat162 p2 = __floats2bfloat162_rn(x[2 * jj], x[2 * jj + 1]);
+            pk[16 * sub + jj] = __uint_as_float(*reinterpret_cast<uint32_t*>(&p2));
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) x[j] *= dl;
+          tmem_st32(tbase + lane_off + col, x);
+        }
+        tmem_st32(tbase + lane_off + COL_O2 + 32 * pair, pk);
       }
     }
-    fence_proxy_async_smem();
     tc_fence_before();
     group_sync(kBarState, kStateThreads);
 
-    // ---- MMA: [O1 | Y] = S^T [Q; K]^T, one N = 128 product over the stage as loaded
+    // ---- MMA: [O1 | Y] = S^T [Q; K]^T, one N = 128 product over the stage as loaded (A, the
+    //      bf16 S^T, from TMEM)
     if (leader) {
       tc_fence_after();
       const uint32_t id5 = idesc_bf16(128, 128, false, false);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-        mma_bf16(tbase + COL_O1, sdesc_sw128(sbase + OFF_S + off, 16, 1024),
-                 sdesc_sw128(qk_a + off, 16, 1024), id5, ks > 0);
+        mma_bf16_ta(tbase + COL_O1, tbase + COL_O2 + 8 * ks, sdesc_sw128(qk_a + off, 16, 1024),
+                    id5, ks > 0);
       }
       mma_commit(&bars[B_MMA_S]);
     }
@@ -641,16 +647,20 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     if (group_sync_or(kBarState, kStateThreads, !ok || flag_set(flag))) { failed = true; break; }
     tc_fence_after();
 
-    // ---- U'^T -> bf16 K-major A operand [dv rows][tokens]
+    // ---- U'^T -> bf16, packed into the first 32 of its own TMEM columns (A operand)
+    {
+      float x[32], y[32], pk[32];
+      tmem_ld32(tbase + lane_off + COL_U, x);
+      tmem_ld32(tbase + lane_off + COL_U + 32, y);
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float x[32];
-      tmem_ld32(tbase + lane_off + COL_U + 32 * half, x);
-#pragma unroll
-      for (int m = 0; m < 4; ++m)
-        store_bf16x8(sm + OFF_U + sw128_offset(row, 32 * half + 8 * m), &x[8 * m]);
+      for (int jj = 0; jj < 16; ++jj) {
+        __nv_bfloat162 p0 = __floats2bfloat162_rn(x[2 * jj], x[2 * jj + 1]);
+        __nv_bfloat162 p1 = __floats2bfloat162_rn(y[2 * jj], y[2 * jj + 1]);
+        pk[jj] = __uint_as_float(*reinterpret_cast<uint32_t*>(&p0));
+        pk[16 + jj] = __uint_as_float(*reinterpret_cast<uint32_t*>(&p1));
+      }
+      tmem_st32(tbase + lane_off + COL_U, pk);
     }
-    fence_proxy_async_smem();
     tc_fence_before();
     group_sync(kBarState, kStateThreads);
 
@@ -660,14 +670,14 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
       const uint32_t id6 = idesc_bf16(128, 64, false, false);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
-        mma_bf16(tbase + COL_O2, sdesc_sw128(sbase + OFF_U + ks * 32, 16, 1024),
-                 sdesc_sw128(sbase + OFF_P + s * 8192 + ks * 32, 16, 1024), id6, ks > 0);
+        mma_bf16_ta(tbase + COL_O2, tbase + COL_U + 8 * ks,
+                    sdesc_sw128(sbase + OFF_P + s * 8192 + ks * 32, 16, 1024), id6, ks > 0);
       }
       const uint32_t id7 = idesc_bf16(128, 128, false, true);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
-        mma_bf16(tbase + COL_S, sdesc_sw128(sbase + OFF_U + ks * 32, 16, 1024),
-                 sdesc_sw128(sbase + OFF_KT + ks * 2048, 8192, 1024), id7, 1);
+        mma_bf16_ta(tbase + COL_S, tbase + COL_U + 8 * ks,
+                    sdesc_sw128(sbase + OFF_KT + ks * 2048, 8192, 1024), id7, 1);
       }
       mma_commit(&bars[B_P_FREE + s]);
       mma_commit(&bars[B_MMA_S]);
