@@ -19,8 +19,9 @@
 //                                          M=128 N=64  K=64    (accumulates on U^T; this is
 //                                                               U - W S with W = Tw K; -Y is
 //                                                               read from TMEM as bf16)
-//   O2  = U'^T P^T                         M=128 N=64  K=64
-//   S^T <- exp(G_last) S^T + (U' * exp(G_last - G) r_k)^T K     M=128 N=128 K=64
+//   [O2 | S^T] += U'^T [P; K~^T]^T        M=128 N=192 K=64    (O2 columns zeroed first;
+//                                                               K~ = diag(exp(G_last - G) r_k) K,
+//                                                               S^T decayed by exp(G_last) before)
 //   o   = scale exp(G) r_q * O1 + O2
 //
 // Every product is oriented so M = 128 (value or key features on the TMEM
@@ -60,8 +61,10 @@ constexpr uint32_t QK_STAGE = 32768;
 constexpr uint32_t OFF_V = 65536;       // 2 stages x 16 KB: [dv half][64 tokens][128 B]
 constexpr uint32_t V_STAGE = 16384;
 constexpr uint32_t OFF_S = 98304;       // the bf16 output tile staged for its TMA store (16 KB)
-constexpr uint32_t OFF_KT = 131072;     // K rows scaled by exp(G_last - G_t) r_k[t], bf16: the
-                                        // state update's MN-major B, [dk half][64 tokens][128 B]
+constexpr uint32_t OFF_PF = 122880;     // copy of this chunk's P (8 KB), directly followed by
+constexpr uint32_t OFF_KT = 131072;     // K~^T: the K rows scaled by exp(G_last - G_t) r_k[t],
+                                        // transposed, K-major [128 dk rows][64 tokens]: together
+                                        // [P; K~^T] is the N = 192 B operand of the last product
 constexpr uint32_t OFF_A = 147456;      // fp32 A [64][64], 16-byte-group swizzled; the solve
                                         // overwrites its strictly-lower blocks with those of T
 constexpr uint32_t OFF_P = 163840;      // 2 x P, K-major B [64 i][64 j]
@@ -91,7 +94,7 @@ enum {
   B_MMA_S = 3,      // state group's MMA commits
   B_READY = 4,      // [2] prep -> state: chunk ready (vectors, P, Tw / Tu in shared memory)
   B_WU = 6,         // state -> prep: the MMAs reading Tw / Tu are done (both free again)
-  B_P_FREE = 7,     // [2] state -> prep: MMA on P done
+  B_P_FREE = 7,     // [2] state -> prep: P copied out (its buffer free)
   B_VEC_FREE = 9,   // [2] state -> prep: chunk finished (per-token vectors free)
   B_COUNT = 11
 };
@@ -503,7 +506,7 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
 
 // =================================================================== state group
 // Warps 8-11.  For each chunk: U^T = V^T Tu^T, S -> bf16 operand and decay of the TMEM
-// state, [O1 | Y] = S^T [Q; K]^T, U' = U - Y Tw^T, O2 = U' P^T, S += (decayed U')^T K, output.
+// state, [O1 | Y] = S^T [Q; K]^T, U' = U - Y Tw^T, [O2 | S^T] += U'^T [P; K~^T]^T, output.
 __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int bos, int eos,
                             int nchunks, int h, int hq, size_t st_off,
                             const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
@@ -584,33 +587,49 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
       }
       mma_commit(&bars[B_MMA_S]);
     }
-    // ---- K rows scaled by exp(G_last - G_t) r_k[t] into their own tile (the state update's
-    //      B operand), done while [O1 | Y] runs; then the stage is free
+    // ---- while [O1 | Y] runs: P copied next to K~^T, and K~^T built from the stage's K rows,
+    //      scaled by exp(G_last - G_t) r_k[t] and transposed in 8 x 8 blocks (ldmatrix,
+    //      stmatrix .trans); warp wq takes tokens 16 wq .. 16 wq + 15.  Then the stage is free.
     {
-      const int t = tid >> 1, kh = tid & 1;
-      const float dl = vec[VEC_DL + t];
-      const uint8_t* krow = sm + OFF_QK + s * QK_STAGE + kh * 16384 + 8192 + t * 128;
-      uint8_t* kdst = sm + OFF_KT + kh * 8192 + t * 128;   // same offsets: same swizzle
+      const uint4* psrc = reinterpret_cast<const uint4*>(sm + OFF_P + s * 8192);
+      uint4* pdst = reinterpret_cast<uint4*>(sm + OFF_PF);
 #pragma unroll
-      for (int m0 = 0; m0 < 8; ++m0) {
-        const int m = (m0 + t) & 7;   // rows rotate through the 16-byte chunks: no bank conflicts
-        uint4 u = *reinterpret_cast<const uint4*>(krow + 16 * m);
-        __nv_bfloat162* b2 = reinterpret_cast<__nv_bfloat162*>(&u);
+      for (int e = 0; e < 4; ++e) pdst[tid + 128 * e] = psrc[tid + 128 * e];
+      const int mi = lane >> 3, rr = lane & 7;   // matrix this lane addresses, row within it
+      const int tg = 2 * wq + (mi & 1);          // its token group (8 tokens)
+      const uint32_t kst = sbase + OFF_QK + s * QK_STAGE + 8192;
+      // fragment register m holds token 8 (2 wq + (m & 1)) + lane / 4
+      const float dl0 = vec[VEC_DL + 16 * wq + (lane >> 2)];
+      const float dl1 = vec[VEC_DL + 16 * wq + 8 + (lane >> 2)];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(b2[e]);
-          b2[e] = __floats2bfloat162_rn(f.x * dl, f.y * dl);
+      for (int it = 0; it < 8; ++it) {
+        const int dg = 2 * it + (mi >> 1);       // dk group of the matrix this lane addresses
+        const int tok = 8 * tg + rr, dk = 8 * dg;
+        uint32_t f[4];
+        ldmatrix_x4(kst + (dk >> 6) * 16384 + tok * 128 + ((((dk & 63) >> 3) ^ (tok & 7)) << 4), f);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          __nv_bfloat162 b2 = *reinterpret_cast<__nv_bfloat162*>(&f[m]);
+          const float2 x2 = __bfloat1622float2(b2);
+          const float d = (m & 1) ? dl1 : dl0;
+          b2 = __floats2bfloat162_rn(x2.x * d, x2.y * d);
+          f[m] = *reinterpret_cast<uint32_t*>(&b2);
         }
-        *reinterpret_cast<uint4*>(kdst + 16 * m) = u;
+        const int dkr = 8 * dg + rr;             // K~^T row this lane addresses
+        stmatrix_x4_trans(sbase + OFF_KT + dkr * 128 + ((tg ^ (dkr & 7)) << 4), f);
       }
     }
     fence_proxy_async_smem();
     if (leader) ok = mbar_wait(&bars[B_MMA_S], ps, kWaitLimitNs);
     ps ^= 1u;
     if (group_sync_or(kBarState, kStateThreads, !ok || flag_set(flag))) { failed = true; break; }
-    // every read of stage s is done (U, D1, [O1 | Y], the K copy): load chunk c + 2 into it
-    if (leader && c + 2 < nchunks)
-      issue_chunk_loads(sm, &bars[B_FULL + s], tq, tk, tv, s, t0 + 2 * kChunk, hq, h);
+    // every read of stage s is done (U, D1, [O1 | Y], the K copy): load chunk c + 2 into it;
+    // P of chunk c has been copied: the prep group may overwrite it
+    if (leader) {
+      if (c + 2 < nchunks)
+        issue_chunk_loads(sm, &bars[B_FULL + s], tq, tk, tv, s, t0 + 2 * kChunk, hq, h);
+      mbar_arrive(&bars[B_P_FREE + s]);
+    }
     tc_fence_after();
 
     // ---- -Y -> bf16, packed into the first 32 of its own TMEM columns (A operand from TMEM)
@@ -626,6 +645,13 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
         pk[16 + jj] = __uint_as_float(*reinterpret_cast<uint32_t*>(&p1));
       }
       tmem_st32(tbase + lane_off + COL_Y, pk);
+      // the O2 columns (the bf16 S^T, read by now) start from zero: the last product
+      // accumulates O2 and S^T in one go
+      float z[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) z[j] = 0.f;
+      tmem_st32(tbase + lane_off + COL_O2, z);
+      tmem_st32(tbase + lane_off + COL_O2 + 32, z);
     }
     tc_fence_before();
     group_sync(kBarState, kStateThreads);
@@ -664,22 +690,15 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     tc_fence_before();
     group_sync(kBarState, kStateThreads);
 
-    // ---- MMA: O2 = U'^T P^T, S^T += U'^T K~ (K~ = the scaled K rows)
+    // ---- MMA: [O2 | S^T] += U'^T [P; K~^T]^T, one N = 192 product (A, the bf16 U', from TMEM)
     if (leader) {
       tc_fence_after();
-      const uint32_t id6 = idesc_bf16(128, 64, false, false);
+      const uint32_t id67 = idesc_bf16(128, 192, false, false);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         mma_bf16_ta(tbase + COL_O2, tbase + COL_U + 8 * ks,
-                    sdesc_sw128(sbase + OFF_P + s * 8192 + ks * 32, 16, 1024), id6, ks > 0);
+                    sdesc_sw128(sbase + OFF_PF + ks * 32, 16, 1024), id67, 1);
       }
-      const uint32_t id7 = idesc_bf16(128, 128, false, true);
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        mma_bf16_ta(tbase + COL_S, tbase + COL_U + 8 * ks,
-                    sdesc_sw128(sbase + OFF_KT + ks * 2048, 8192, 1024), id7, 1);
-      }
-      mma_commit(&bars[B_P_FREE + s]);
       mma_commit(&bars[B_MMA_S]);
     }
     if (leader) ok = mbar_wait(&bars[B_MMA_S], ps, kWaitLimitNs);

@@ -221,6 +221,16 @@ __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Four 8 x 8 b16 matrices loaded from shared memory: lane 8 i + r gives the address of row r
+// (16 bytes) of matrix i; register i of thread t receives row t/4, columns 2 (t%4) and
+// 2 (t%4) + 1 of matrix i (low half first) -- the fragment stmatrix takes.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t saddr, uint32_t (&f)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(f[0]), "=r"(f[1]), "=r"(f[2]), "=r"(f[3])
+               : "r"(saddr)
+               : "memory");
+}
+
 // Four 8 x 8 b16 matrices stored transposed: register i of thread t holds row t/4, columns
 // 2 (t%4) and 2 (t%4) + 1 of matrix i (low half first); lane 8 i + r gives the shared
 // address of memory row r of matrix i, which receives column r of the source (16 bytes).
