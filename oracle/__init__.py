@@ -20,9 +20,14 @@ Three functions wrap the C library built from ``gdn_oracle.c``:
 delta-rule writes per token, "Megatron-Core API: core.ssm.gated_delta_product",
 GatedDeltaProductMixer) by its recurrence.
 
+:func:`backward` returns the gradients of every input of :func:`recurrent` for given
+output / final-state gradients (the reverse-mode adjoint of the recurrence).
+
 :mod:`oracle.closed_form` adds the unrolled product form for tiny inputs.
 
-Every function pinned by ``tests/test_oracle_pins.py``; see the header of
+Pinned by ``tests/test_oracle_pins.py`` (the gated delta rule),
+``tests/test_oracle_product_pins.py`` (the product) and
+``tests/test_oracle_backward_pins.py`` (the adjoint); see the header of
 ``gdn_oracle.c`` for the exact update rule and the readings it takes.
 """
 from __future__ import annotations
@@ -75,8 +80,10 @@ def load_library(path: str) -> ctypes.CDLL:
                                        dp, dp, dp, i]
     lib.gdn_oracle_product_decode.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, i, dp, i, lp,
                                               d, i, dp, i]
+    lib.gdn_oracle_backward.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, lp, i, d, i, dp, dp, dp,
+                                        dp, dp, dp, dp, dp, dp, i]
     for f in (lib.gdn_oracle_recurrent, lib.gdn_oracle_chunked, lib.gdn_oracle_decode,
-              lib.gdn_oracle_product, lib.gdn_oracle_product_decode):
+              lib.gdn_oracle_product, lib.gdn_oracle_product_decode, lib.gdn_oracle_backward):
         f.restype = ctypes.c_int
     lib.gdn_oracle_max_threads.restype = ctypes.c_int
     return lib
@@ -262,3 +269,32 @@ def product_decode(q, k, v, g, beta, ssm_state, batch_indices=None, scale=None,
     if rc != ORACLE_OK:
         raise RuntimeError("gdn_oracle_product_decode failed with code %d" % rc)
     return o
+
+
+def backward(q, k, v, g, beta, d_o, d_final_state=None, scale=None, initial_state=None,
+             use_qk_l2norm_in_kernel=False, cu_seqlens=None, nthreads=0, lib=None):
+    """Gradients of the gated delta rule (layouts of :func:`recurrent`) for the output
+    gradient ``d_o`` [B, T, Hv, V] and optional final-state gradient [N, Hv, K, V].
+    Returns ``(dq, dk, dv, dg, dbeta, d_initial_state)`` as float64 numpy."""
+    q, k, v, g, beta, cu, init, (B, T, Hqk, Hv, K, V, N) = _prep_seq(
+        q, k, v, g, beta, cu_seqlens, initial_state)
+    do = _f64(d_o)
+    dfin = _f64(d_final_state)
+    if do.shape != (B, T, Hv, V):
+        raise ValueError("d_o must be [B, T, Hv, V]")
+    if dfin is not None and dfin.shape != (N, Hv, K, V):
+        raise ValueError("d_final_state must be [N, Hv, K, V]")
+    dq = np.zeros((B, T, Hqk, K))
+    dk = np.zeros((B, T, Hqk, K))
+    dv = np.full((B, T, Hv, V), np.nan)
+    dg = np.full((B, T, Hv), np.nan)
+    db = np.full((B, T, Hv), np.nan)
+    dinit = np.zeros((N, Hv, K, V))
+    rc = (lib or _load()).gdn_oracle_backward(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), B * T, Hqk, Hv, K, V,
+        _ptr(cu, ctypes.c_int64), N, _scale(scale, K), int(bool(use_qk_l2norm_in_kernel)),
+        _ptr(init), _ptr(do), _ptr(dfin), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(db),
+        _ptr(dinit), int(nthreads))
+    if rc != ORACLE_OK:
+        raise RuntimeError("gdn_oracle_backward failed with code %d" % rc)
+    return dq, dk, dv, dg, db, dinit

@@ -36,7 +36,15 @@
  *                            output exactly zero (GatedDeltaProductMixer.ssm_decode;
  *                            "Add GDN dynamic inference" PR review thread).
  *   gdn_oracle_product, gdn_oracle_product_decode -- the Gated Delta Product
- *                            (several writes per token), at the end of this file.
+ *                            (several writes per token), near the end of this file.
+ *   gdn_oracle_backward   -- the gradients of every input of gdn_oracle_recurrent
+ *                            (its reverse-mode adjoint), for training: the chunked
+ *                            rule is the training path of the GDN layer
+ *                            (GatedDeltaNet, torch_chunk_gated_delta_rule's
+ *                            deterministic mode; GatedDeltaProductMixer._gdp_chunk_forward
+ *                            serves training too).  Pinned by central finite
+ *                            differences and by autograd of an independent
+ *                            recurrence in the tests.
  *
  * Layouts (all row-major, fp64):
  *   q, k   [T_total, Hqk, K]     v, o [T_total, Hv, V]     g, beta [T_total, Hv]
@@ -516,4 +524,166 @@ int gdn_oracle_product_decode(const double* q, const double* k, const double* v,
     }
   }
   return bad ? ORACLE_ERR_SLOT : ORACLE_OK;
+}
+
+/*
+ * Backward of the gated delta rule (the reverse-mode adjoint of gdn_oracle_recurrent).  For a
+ * loss with gradients d_o [T_total, Hv, V] on the outputs and d_final [N, Hv, K, V] on the
+ * final states (NULL: zero), returns the gradients of every input:
+ *   dq, dk [T_total, Hqk, K] (summed over the value heads sharing a query/key head),
+ *   dv [T_total, Hv, V], dg, dbeta [T_total, Hv], d_initial [N, Hv, K, V] (may be NULL).
+ *
+ * With S_{t-1} the state before token t, a = exp(g_t), hat-q / hat-k the (optionally)
+ * normalised vectors, r = a S_{t-1}^T k, u = beta (v - r), S_t = a S_{t-1} + k u^T and
+ * o_t = scale S_t^T q, walking t backwards with dS the gradient of S_t:
+ *   dS   += scale q do^T                    dq   = scale (a S_{t-1} do + (u . do) k)
+ *   du    = dS^T k                          dk   = dS u
+ *   dbeta = du . (v - r)                    dv   = beta du          dr = -beta du
+ *   dk   += a S_{t-1} dr                    da   = <dS, S_{t-1}> + (S_{t-1}^T k) . dr
+ *   dg    = a da                            dS  <- a (dS + k dr^T)     (the gradient of S_{t-1})
+ * then the L2 norm's Jacobian x -> x / sqrt(|x|^2 + eps) maps d(hat-x) to dx.  The states are
+ * recomputed forward first (stored per token).
+ */
+static void oracle_norm_backward(const double* x, const double* dxh, int n, int use, double* dx) {
+  if (!use) {
+    memcpy(dx, dxh, (size_t)n * sizeof(double));
+    return;
+  }
+  double ss = 0.0, xd = 0.0;
+  for (int i = 0; i < n; ++i) { ss += x[i] * x[i]; xd += x[i] * dxh[i]; }
+  const double rho = 1.0 / sqrt(ss + GDN_ORACLE_L2_EPS);
+  for (int i = 0; i < n; ++i) dx[i] = rho * dxh[i] - rho * rho * rho * xd * x[i];
+}
+
+int gdn_oracle_backward(const double* q, const double* k, const double* v, const double* g,
+                        const double* beta, int T_total, int Hqk, int Hv, int K, int V,
+                        const int64_t* cu_seqlens, int N, double scale, int use_qk_l2norm,
+                        const double* initial_state, const double* d_o, const double* d_final,
+                        double* dq, double* dk, double* dv, double* dg, double* dbeta,
+                        double* d_initial, int nthreads) {
+  int err = check_common(Hqk, Hv, K, V, cu_seqlens, N);
+  if (err) return err;
+  if (cu_seqlens[N] > T_total || !q || !k || !v || !g || !beta || !d_o || !dq || !dk || !dv ||
+      !dg || !dbeta)
+    return ORACLE_ERR_ARG;
+  const int group = Hv / Hqk;
+  int failed = 0;
+  memset(dq, 0, sizeof(double) * (size_t)T_total * Hqk * K);
+  memset(dk, 0, sizeof(double) * (size_t)T_total * Hqk * K);
+  set_threads(nthreads);
+  /* one task per (sequence, query/key head): its value heads add into the same dq / dk rows */
+#pragma omp parallel for schedule(dynamic, 1) collapse(2)
+  for (int n = 0; n < N; ++n) {
+    for (int hq = 0; hq < Hqk; ++hq) {
+      const int64_t t0 = cu_seqlens[n], L = cu_seqlens[n + 1] - cu_seqlens[n];
+      const size_t KV = (size_t)K * V;
+      double* states = (double*)malloc(sizeof(double) * (KV * ((size_t)L + 2) + 6 * (size_t)K + 4 * (size_t)V));
+      if (!states) {
+#pragma omp atomic write
+        failed = 1;
+        continue;
+      }
+      double* dS = states + KV * (size_t)(L + 1);   /* states[t] = S before token t0 + t */
+      double* qn = dS + KV;
+      double* kn = qn + K;
+      double* dqh = kn + K;
+      double* dkh = dqh + K;
+      double* tmpk = dkh + K;
+      double* tmpk2 = tmpk + K;
+      double* r = tmpk2 + K;
+      double* u = r + V;
+      double* du = u + V;
+      double* dr = du + V;
+      for (int h = hq * group; h < (hq + 1) * group; ++h) {
+        const size_t soff = ((size_t)n * Hv + h) * KV;
+        if (initial_state)
+          memcpy(states, initial_state + soff, sizeof(double) * KV);
+        else
+          memset(states, 0, sizeof(double) * KV);
+        /* forward: states[t + 1] = S after token t */
+        for (int64_t t = 0; t < L; ++t) {
+          const int64_t tt = t0 + t;
+          const double* Sp = states + KV * (size_t)t;
+          double* Sn = states + KV * (size_t)(t + 1);
+          oracle_l2norm(k + ((size_t)tt * Hqk + hq) * K, K, use_qk_l2norm, kn);
+          const double a = exp(g[(size_t)tt * Hv + h]);
+          const double bt = beta[(size_t)tt * Hv + h];
+          const double* vt = v + ((size_t)tt * Hv + h) * V;
+          for (int c = 0; c < V; ++c) r[c] = 0.0;
+          for (int i = 0; i < K; ++i)
+            for (int c = 0; c < V; ++c) r[c] += a * Sp[i * V + c] * kn[i];
+          for (int c = 0; c < V; ++c) u[c] = bt * (vt[c] - r[c]);
+          for (int i = 0; i < K; ++i)
+            for (int c = 0; c < V; ++c) Sn[i * V + c] = a * Sp[i * V + c] + kn[i] * u[c];
+        }
+        if (d_final)
+          memcpy(dS, d_final + soff, sizeof(double) * KV);
+        else
+          memset(dS, 0, sizeof(double) * KV);
+        for (int64_t t = L - 1; t >= 0; --t) {
+          const int64_t tt = t0 + t;
+          const double* Sp = states + KV * (size_t)t;
+          const double* qraw = q + ((size_t)tt * Hqk + hq) * K;
+          const double* kraw = k + ((size_t)tt * Hqk + hq) * K;
+          oracle_l2norm(qraw, K, use_qk_l2norm, qn);
+          oracle_l2norm(kraw, K, use_qk_l2norm, kn);
+          const double a = exp(g[(size_t)tt * Hv + h]);
+          const double bt = beta[(size_t)tt * Hv + h];
+          const double* vt = v + ((size_t)tt * Hv + h) * V;
+          const double* dot = d_o + ((size_t)tt * Hv + h) * V;
+          /* recompute S_{t-1}^T k (kept apart from the decay: r = a S_{t-1}^T k) and u */
+          for (int c = 0; c < V; ++c) r[c] = 0.0;
+          for (int i = 0; i < K; ++i)
+            for (int c = 0; c < V; ++c) r[c] += Sp[i * V + c] * kn[i];
+          for (int c = 0; c < V; ++c) u[c] = bt * (vt[c] - a * r[c]);
+          /* read-out */
+          for (int i = 0; i < K; ++i)
+            for (int c = 0; c < V; ++c) dS[i * V + c] += scale * qn[i] * dot[c];
+          double udo = 0.0;
+          for (int c = 0; c < V; ++c) udo += u[c] * dot[c];
+          for (int i = 0; i < K; ++i) {
+            double s = 0.0;
+            for (int c = 0; c < V; ++c) s += Sp[i * V + c] * dot[c];
+            dqh[i] = scale * (a * s + udo * kn[i]);
+          }
+          /* rank-1 write and the delta-rule read */
+          for (int c = 0; c < V; ++c) {
+            double s = 0.0;
+            for (int i = 0; i < K; ++i) s += dS[i * V + c] * kn[i];
+            du[c] = s;
+          }
+          double db = 0.0;
+          for (int c = 0; c < V; ++c) {
+            db += du[c] * (vt[c] - a * r[c]);
+            dv[((size_t)tt * Hv + h) * V + c] = bt * du[c];
+            dr[c] = -bt * du[c];
+          }
+          dbeta[(size_t)tt * Hv + h] = db;
+          double da = 0.0;
+          for (int i = 0; i < K; ++i) {
+            double s1 = 0.0, s2 = 0.0;
+            for (int c = 0; c < V; ++c) {
+              s1 += dS[i * V + c] * u[c];
+              s2 += Sp[i * V + c] * dr[c];
+              da += dS[i * V + c] * Sp[i * V + c];
+            }
+            dkh[i] = s1 + a * s2;
+          }
+          for (int c = 0; c < V; ++c) da += r[c] * dr[c];
+          dg[(size_t)tt * Hv + h] = a * da;
+          for (int i = 0; i < K; ++i)
+            for (int c = 0; c < V; ++c) dS[i * V + c] = a * (dS[i * V + c] + kn[i] * dr[c]);
+          oracle_norm_backward(qraw, dqh, K, use_qk_l2norm, tmpk);
+          oracle_norm_backward(kraw, dkh, K, use_qk_l2norm, tmpk2);
+          for (int i = 0; i < K; ++i) {
+            dq[((size_t)tt * Hqk + hq) * K + i] += tmpk[i];
+            dk[((size_t)tt * Hqk + hq) * K + i] += tmpk2[i];
+          }
+        }
+        if (d_initial) memcpy(d_initial + soff, dS, sizeof(double) * KV);
+      }
+      free(states);
+    }
+  }
+  return failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
 }
