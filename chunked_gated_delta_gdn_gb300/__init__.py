@@ -11,14 +11,18 @@ its thin PyTorch binding:
 * ``*_fused_gates`` -- the same with g and beta computed in the kernels.
 * :func:`chunk_gated_delta_product`, :func:`gated_delta_product_decode` -- the Gated
   Delta Product (several delta-rule writes per token).
+* :func:`chunk_gated_delta_rule_bwd` -- the backward (dq, dk, dv, dg, dbeta, d_initial_state);
+  :func:`chunk_gated_delta_rule_trainable` -- forward + backward as a torch autograd op.
 """
 from .api import (GdnError, chunk_fwd_path, chunk_gated_delta_product, chunk_gated_delta_rule,
-                  chunk_gated_delta_rule_fused_gates, chunk_workspace_size, gated_delta_decode,
+                  chunk_gated_delta_rule_bwd, chunk_gated_delta_rule_fused_gates,
+                  chunk_gated_delta_rule_trainable, chunk_workspace_size, gated_delta_decode,
                   gated_delta_decode_fused_gates, gated_delta_decode_multi,
                   gated_delta_product_decode)
 
 __all__ = ["chunk_gated_delta_rule", "gated_delta_decode", "gated_delta_decode_multi",
            "chunk_gated_delta_rule_fused_gates", "gated_delta_decode_fused_gates",
            "chunk_gated_delta_product", "gated_delta_product_decode",
+           "chunk_gated_delta_rule_bwd", "chunk_gated_delta_rule_trainable",
            "chunk_workspace_size", "chunk_fwd_path", "GdnError"]
 __version__ = "0.1.0"

@@ -23,7 +23,7 @@ GDN_DEV_BAD_SLOT, GDN_DEV_BAD_CU_SEQLENS = 1, 2
 EXPORTS = ("gdn_chunk_fwd", "gdn_chunk_fwd_workspace_size", "gdn_chunk_fwd_path", "gdn_decode",
            "gdn_chunk_fwd_gated", "gdn_decode_gated", "gdn_decode_multi", "gdn_chunk_fwd_noalloc",
            "gdn_product_chunk_fwd", "gdn_product_chunk_fwd_workspace_size", "gdn_product_decode",
-           "gdn_status_string", "gdn_version")
+           "gdn_chunk_bwd", "gdn_chunk_bwd_workspace_size", "gdn_status_string", "gdn_version")
 
 
 class GdnError(RuntimeError):
@@ -78,6 +78,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.gdn_product_decode.argtypes = [vp, vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, i, i, i,
                                            f, i, vp, vp, vp, vp]
         lib.gdn_product_decode.restype = i
+        lib.gdn_chunk_bwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp, i, vp,
+                                      i, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
+        lib.gdn_chunk_bwd.restype = i
+        lib.gdn_chunk_bwd_workspace_size.argtypes = [i, i, i, i, i, i, i, i, i]
+        lib.gdn_chunk_bwd_workspace_size.restype = sz
         lib.gdn_status_string.argtypes = [i]
         lib.gdn_status_string.restype = ctypes.c_char_p
         lib.gdn_version.argtypes = []

@@ -16,7 +16,8 @@ from . import _lib
 
 __all__ = ["chunk_gated_delta_rule", "gated_delta_decode", "gated_delta_decode_multi",
            "chunk_gated_delta_rule_fused_gates", "chunk_gated_delta_product",
-           "gated_delta_product_decode",
+           "gated_delta_product_decode", "chunk_gated_delta_rule_bwd",
+           "chunk_gated_delta_rule_trainable",
            "gated_delta_decode_fused_gates", "chunk_workspace_size", "chunk_fwd_path", "GdnError"]
 
 GdnError = _lib.GdnError
@@ -142,6 +143,105 @@ def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, chunk_size=64, initial_
                          _ptr(dev_status), _stream(dev))
     _lib.check("gdn_chunk_fwd", st)
     return out, final_state
+
+
+def chunk_gated_delta_rule_bwd(q, k, v, g, beta, d_o, d_final_state=None, scale=None,
+                               chunk_size=64, initial_state=None, use_qk_l2norm_in_kernel=False,
+                               cu_seqlens=None, *, need_d_initial_state=True, workspace=None,
+                               dev_status=None):
+    """Gradients of :func:`chunk_gated_delta_rule` through ``gdn_chunk_bwd``.
+
+    Takes the forward's inputs (no slot cache) plus ``d_o`` [B, T, Hv, V] (the
+    output gradient, q's dtype) and ``d_final_state`` [N, Hv, K, V] fp32 or None.
+    Returns ``(dq, dk, dv, dg, dbeta, d_initial_state)``: dq, dk, dv in q's dtype,
+    dg and dbeta fp32, d_initial_state fp32 [N, Hv, K, V] (None when
+    ``need_d_initial_state`` is False).
+    """
+    _need(q, "q", (torch.float32, torch.bfloat16))
+    dev, dt = q.device, q.dtype
+    if q.dim() != 4:
+        raise ValueError("q must be [B, T, Hqk, K]")
+    B, T, Hqk, K = q.shape
+    _need(k, "k", dt, dev, q.shape)
+    _need(v, "v", dt, dev)
+    if v.dim() != 4 or v.shape[:2] != q.shape[:2]:
+        raise ValueError("v must be [B, T, Hv, V]")
+    Hv, V = v.shape[2], v.shape[3]
+    _need(g, "g", torch.float32, dev, (B, T, Hv))
+    _need(beta, "beta", (dt, torch.float32), dev, (B, T, Hv))
+    _need(d_o, "d_o", dt, dev, (B, T, Hv, V))
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+        if B != 1:
+            raise ValueError("cu_seqlens requires B == 1")
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    st_shape = (N, Hv, K, V)
+    if initial_state is not None:
+        _need(initial_state, "initial_state", torch.float32, dev, st_shape)
+    if d_final_state is not None:
+        _need(d_final_state, "d_final_state", torch.float32, dev, st_shape)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    dg = torch.empty((B, T, Hv), dtype=torch.float32, device=dev)
+    dbeta = torch.empty((B, T, Hv), dtype=torch.float32, device=dev)
+    dh0 = torch.empty(st_shape, dtype=torch.float32, device=dev) if need_d_initial_state else None
+    L = _lib.load()
+    bdt = _DT[beta.dtype]
+    need = L.gdn_chunk_bwd_workspace_size(B, T, Hqk, Hv, K, V, N, _DT[dt], bdt)
+    if need == (1 << 64) - 1:
+        raise ValueError("sizes rejected by gdn_chunk_bwd")
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(int(need), 1), dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32, dev, (1,))
+    st = L.gdn_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), B, T, Hqk, Hv, K, V,
+                         _DT[dt], bdt, _scale(scale), int(chunk_size), _ptr(initial_state),
+                         int(bool(use_qk_l2norm_in_kernel)), _ptr(cu_seqlens), N, _ptr(d_o),
+                         _ptr(d_final_state), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg),
+                         _ptr(dbeta), _ptr(dh0), _ptr(workspace), ws_bytes, _ptr(dev_status),
+                         _stream(dev))
+    _lib.check("gdn_chunk_bwd", st)
+    return dq, dk, dv, dg, dbeta, dh0
+
+
+class _ChunkGatedDeltaRule(torch.autograd.Function):
+    """gdn_chunk_fwd forward, gdn_chunk_bwd backward."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, g, beta, initial_state, scale, output_final_state, use_l2,
+                cu_seqlens):
+        o, fin = chunk_gated_delta_rule(q, k, v, g, beta, scale=scale,
+                                        initial_state=initial_state,
+                                        output_final_state=output_final_state,
+                                        use_qk_l2norm_in_kernel=use_l2, cu_seqlens=cu_seqlens)
+        ctx.save_for_backward(q, k, v, g, beta, initial_state, cu_seqlens)
+        ctx.scale, ctx.use_l2 = scale, use_l2
+        return o, fin
+
+    @staticmethod
+    def backward(ctx, d_o, d_fin):
+        q, k, v, g, beta, init, cu = ctx.saved_tensors
+        dq, dk, dv, dg, db, dh0 = chunk_gated_delta_rule_bwd(
+            q, k, v, g, beta, d_o.contiguous(),
+            None if d_fin is None else d_fin.contiguous(), scale=ctx.scale,
+            initial_state=init, use_qk_l2norm_in_kernel=ctx.use_l2, cu_seqlens=cu,
+            need_d_initial_state=init is not None and ctx.needs_input_grad[5])
+        return dq, dk, dv, dg, db.to(beta.dtype), dh0, None, None, None, None
+
+
+def chunk_gated_delta_rule_trainable(q, k, v, g, beta, scale=None, initial_state=None,
+                                     output_final_state=False, use_qk_l2norm_in_kernel=False,
+                                     cu_seqlens=None):
+    """:func:`chunk_gated_delta_rule` as a differentiable op (torch autograd): the
+    forward runs ``gdn_chunk_fwd`` and the backward ``gdn_chunk_bwd``.  Returns
+    ``(o, final_state or None)``."""
+    return _ChunkGatedDeltaRule.apply(q, k, v, g, beta, initial_state, scale,
+                                      bool(output_final_state), bool(use_qk_l2norm_in_kernel),
+                                      cu_seqlens)
 
 
 def gated_delta_decode(q, k, v, g, beta, ssm_state, batch_indices=None, scale=None,

@@ -178,6 +178,71 @@ gdn_status_t gdn_chunk_fwd_gated(const void* q, const void* k, const void* v, co
                     workspace_bytes, dev_status, stream, gates);
 }
 
+size_t gdn_chunk_bwd_workspace_size(int B, int T, int Hqk, int Hv, int K, int V, int num_seqs,
+                                    gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype) {
+  if (check_chunk_shapes(B, T, Hqk, Hv, K, V, io_dtype, beta_dtype) != GDN_OK || num_seqs < 0)
+    return (size_t)-1;
+  return gdn::chunk_bwd_workspace_bytes((int)((long long)B * T), num_seqs, Hv, K, V);
+}
+
+gdn_status_t gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
+                           const void* beta, int B, int T, int Hqk, int Hv, int K, int V,
+                           gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype, float scale,
+                           int chunk_size, const float* initial_state, int use_qk_l2norm,
+                           const int32_t* cu_seqlens, int num_seqs, const void* d_o,
+                           const float* d_final_state, void* dq, void* dk, void* dv, float* dg,
+                           float* dbeta, float* d_initial_state, void* workspace,
+                           size_t workspace_bytes, int* dev_status, void* stream) {
+  gdn_status_t st = check_chunk_shapes(B, T, Hqk, Hv, K, V, io_dtype, beta_dtype);
+  if (st != GDN_OK) return st;
+  if (chunk_size != 64) return GDN_ERR_UNSUPPORTED;
+  if (cu_seqlens) {
+    if (B != 1 || num_seqs < 0) return GDN_ERR_SHAPE;
+  } else {
+    num_seqs = B;
+  }
+  const long long T_total = (long long)B * T;
+  if (T_total > 0 && (!q || !k || !v || !g || !beta || !d_o || !dq || !dk || !dv || !dg || !dbeta))
+    return GDN_ERR_NULL;
+  if (T_total > 0 && (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(d_o) ||
+                      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+                      ((uintptr_t)beta & (elem_size(beta_dtype) - 1)) || ((uintptr_t)g & 3u) ||
+                      ((uintptr_t)dg & 3u) || ((uintptr_t)dbeta & 3u)))
+    return GDN_ERR_LAYOUT;
+  if ((initial_state && !aligned16(initial_state)) || (d_final_state && !aligned16(d_final_state)) ||
+      (d_initial_state && !aligned16(d_initial_state)))
+    return GDN_ERR_LAYOUT;
+  if (num_seqs == 0 && T_total == 0) return GDN_OK;
+  const size_t need = gdn::chunk_bwd_workspace_bytes((int)T_total, num_seqs, Hv, K, V);
+  if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return GDN_ERR_LAYOUT;
+
+  gdn::ChunkArgs a{};
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
+  a.B = B; a.T = T; a.Hqk = Hqk; a.Hv = Hv; a.K = K; a.V = V;
+  a.io_dtype = io_dtype; a.beta_dtype = beta_dtype;
+  a.scale = resolve_scale(scale, K);
+  a.initial_state = initial_state;
+  a.final_state = nullptr;
+  a.use_qk_l2norm = use_qk_l2norm ? 1 : 0;
+  a.cu_seqlens = cu_seqlens;
+  a.num_seqs = num_seqs;
+  a.state_indices = nullptr;
+  a.num_slots = 0;
+  a.o = nullptr;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.dev_status = dev_status;
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  a.gates.mode = gdn::kGatesGiven;
+  gdn::BwdArgs b;
+  b.d_o = d_o;
+  b.d_final = d_final_state;
+  b.dq = dq; b.dk = dk; b.dv = dv; b.dg = dg; b.dbeta = dbeta;
+  b.d_initial = d_initial_state;
+  return gdn::launch_chunk_bwd(a, b) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 static gdn_status_t decode_impl(const void* q, const void* k, const void* v, const float* g,
                                 const void* beta, float* ssm_state, int num_slots,
                                 const int32_t* batch_indices, int n, int Hqk, int Hv, int K, int V,

@@ -21,8 +21,7 @@
 // ("Megatron-Core API: core.ssm.gated_delta_product", ssm_inference_chunk_size);
 // the argument set is torch_chunk_gated_delta_rule's ("Megatron-Core API:
 // core.ssm.gated_delta_net.gdn").  Intermediates live in the caller's workspace.
-#include "gdn_common.cuh"
-#include "gdn_internal.h"
+#include "gdn_chunk_util.cuh"
 
 namespace gdn {
 namespace {
@@ -60,156 +59,6 @@ __host__ __device__ inline WsLayout ws_layout(void* base, long long NC, int N, i
   return w;
 }
 
-// Token range of sequence n (cu_seqlens on the device, or uniform rows of T).
-__device__ __forceinline__ void seq_bounds(const ChunkArgs& a, int n, int* bos, int* eos) {
-  if (a.cu_seqlens) {
-    *bos = a.cu_seqlens[n];
-    *eos = a.cu_seqlens[n + 1];
-  } else {
-    *bos = n * a.T;
-    *eos = (n + 1) * a.T;
-  }
-}
-
-// Slot of sequence n when a slot cache is used: -1 padding / invalid, else slot.
-__device__ __forceinline__ int seq_slot(const ChunkArgs& a, int n) {
-  if (!a.state_indices) return n;
-  const int s = a.state_indices[n];
-  return (s >= 0 && s < a.num_slots) ? s : -1;
-}
-
-// ---------------------------------------------------------------- 1. chunk table
-// cu_seqlens must start at 0, never decrease and end at or before the token
-// count; otherwise every sequence is treated as empty (nothing is computed or
-// written), GDN_DEV_BAD_CU_SEQLENS is reported, and chunk_off[N + 1] = 0 tells
-// the later kernels to skip.  This bounds the chunk count by T/64 + N, the size
-// the workspace was laid out for.
-__global__ void chunk_table_kernel(const ChunkArgs a, int32_t* chunk_off) {
-  __shared__ int32_t carry;
-  __shared__ int bad;
-  __shared__ int32_t scan[1024];
-  const int N = a.num_seqs;
-  const int T_total = a.cu_seqlens ? a.T : a.B * a.T;
-  if (threadIdx.x == 0) { carry = 0; bad = 0; }
-  __syncthreads();
-  if (a.cu_seqlens) {
-    for (int n = threadIdx.x; n <= N; n += blockDim.x) {
-      const int x = a.cu_seqlens[n];
-      const bool ok = (n == 0) ? (x == 0) : (x >= a.cu_seqlens[n - 1] && x <= T_total);
-      if (!ok) bad = 1;
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0 && bad) report(a.dev_status, GDN_DEV_BAD_CU_SEQLENS);
-  for (int base = 0; base < N; base += blockDim.x) {
-    const int n = base + threadIdx.x;
-    int cnt = 0;
-    if (n < N) {
-      int bos, eos;
-      seq_bounds(a, n, &bos, &eos);
-      if (!bad) cnt = (eos - bos + C - 1) / C;
-      if (a.state_indices) {
-        const int s = a.state_indices[n];
-        if (s < -1 || s >= a.num_slots) report(a.dev_status, GDN_DEV_BAD_SLOT);
-      }
-    }
-    scan[threadIdx.x] = cnt;
-    __syncthreads();
-    for (int d = 1; d < (int)blockDim.x; d <<= 1) {  // inclusive Hillis-Steele scan
-      const int x = threadIdx.x >= d ? scan[threadIdx.x - d] : 0;
-      __syncthreads();
-      scan[threadIdx.x] += x;
-      __syncthreads();
-    }
-    if (n < N) chunk_off[n + 1] = carry + scan[threadIdx.x];
-    __syncthreads();
-    if (threadIdx.x == blockDim.x - 1) carry += scan[threadIdx.x];
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) {
-    chunk_off[0] = 0;
-    chunk_off[N + 1] = bad ? 0 : 1;
-  }
-}
-
-// Chunk c -> (sequence n, first token, length); false when c is past the end.
-__device__ __forceinline__ bool locate_chunk(const ChunkArgs& a, const int32_t* chunk_off, int c,
-                                             int* n_out, int* t0, int* L) {
-  const int N = a.num_seqs;
-  if (c >= chunk_off[N]) return false;
-  int lo = 0, hi = N - 1;  // largest n with chunk_off[n] <= c
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (chunk_off[mid] <= c) lo = mid; else hi = mid - 1;
-  }
-  int bos, eos;
-  seq_bounds(a, lo, &bos, &eos);
-  *n_out = lo;
-  *t0 = bos + (c - chunk_off[lo]) * C;
-  *L = min(C, eos - *t0);
-  return true;
-}
-
-// Load rows [t0, t0 + L) of a [T, H, D] tensor (head hd) into dst[C][D] fp32,
-// L2-normalised per row when asked; rows >= L are zero.  Needs a __syncthreads
-// after return before the tile is read.
-__device__ void load_rows(const void* src, int dtype, int t0, int L, int H, int hd, int D,
-                          bool l2, float* dst) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int r = warp; r < C; r += kThreads / 32) {
-    float* d = dst + r * D;
-    if (r >= L) {
-      for (int e = lane; e < D; e += 32) d[e] = 0.f;
-      continue;
-    }
-    const size_t base = ((size_t)(t0 + r) * H + hd) * D;
-    float ss = 0.f;
-    for (int e = lane; e < D; e += 32) {
-      const float x = load_elem(src, base + e, dtype);
-      d[e] = x;
-      ss += x * x;
-    }
-    if (l2) {
-      ss = warp_sum(ss);
-      const float rn = 1.0f / sqrtf(ss + kL2Eps);
-      for (int e = lane; e < D; e += 32) d[e] *= rn;
-    }
-  }
-}
-
-// g and beta of element i = token * Hv + h: given, or computed from the raw gate
-// features (fused gates).
-__device__ __forceinline__ void gate_values(const ChunkArgs& a, size_t i, int h, float* g,
-                                            float* beta) {
-  if (a.gates.mode == kGatesFused) {
-    fused_gates(a.gates, i, h, g, beta);
-  } else {
-    *g = a.g[i];
-    *beta = load_elem(a.beta, i, a.beta_dtype);
-  }
-}
-
-// In-chunk inclusive cumsum of g (rows >= L get the last valid value) and beta
-// (zero for rows >= L).  Done by warp 0.
-__device__ void load_gates(const ChunkArgs& a, int t0, int L, int h, float* G, float* bt) {
-  if (threadIdx.x >= 32) return;
-  const int lane = threadIdx.x;
-  float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
-  if (lane < L) gate_values(a, (size_t)(t0 + lane) * a.Hv + h, h, &g0, &b0);
-  if (lane + 32 < L) gate_values(a, (size_t)(t0 + lane + 32) * a.Hv + h, h, &g1, &b1);
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float x0 = __shfl_up_sync(0xffffffffu, g0, o);
-    const float x1 = __shfl_up_sync(0xffffffffu, g1, o);
-    if (lane >= o) { g0 += x0; g1 += x1; }
-  }
-  g1 += __shfl_sync(0xffffffffu, g0, 31);
-  G[lane] = g0;
-  G[lane + 32] = g1;
-  bt[lane] = b0;
-  bt[lane + 32] = b1;
-}
-
 // ---------------------------------------------------------------- 2. prep
 // smem: Kn[C][K], X[C][K + V], A[C][C], G[C], bt[C]
 __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(const ChunkArgs a, WsLayout ws) {
@@ -225,7 +74,7 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(const ChunkArgs a,
   if (!locate_chunk(a, ws.chunk_off, c, &n, &t0, &L)) return;
   if (a.state_indices && seq_slot(a, n) < 0) return;
   const int hq = h / (a.Hv / a.Hqk);
-  load_rows(a.k, a.io_dtype, t0, L, a.Hqk, hq, K, a.use_qk_l2norm != 0, Kn);
+  load_rows(a.k, a.io_dtype, t0, L, a.Hqk, hq, K, a.use_qk_l2norm != 0, Kn, K);
   load_gates(a, t0, L, h, G, bt);
   __syncthreads();
   // A (strictly lower) and the right-hand side [diag(beta exp G) Kn | diag(beta) V].
@@ -310,7 +159,7 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(const ChunkArgs a
       U[e] = cc < vt ? Ug[(size_t)i * V + c0 + cc] : 0.f;
     }
     if (threadIdx.x < C) G[threadIdx.x] = ws.G[ch * C + threadIdx.x];
-    load_rows(a.k, a.io_dtype, t0, L, a.Hqk, hq, K, a.use_qk_l2norm != 0, Kn);
+    load_rows(a.k, a.io_dtype, t0, L, a.Hqk, hq, K, a.use_qk_l2norm != 0, Kn, K);
     __syncthreads();
     // U' = U - W S   (rows >= L of W and U are zero, so U' is zero there)
     for (int e = threadIdx.x; e < C * kVT; e += kThreads) {
@@ -367,8 +216,8 @@ __global__ void __launch_bounds__(kThreads) chunk_output_kernel(const ChunkArgs 
   }
   const int hq = h / (a.Hv / a.Hqk);
   const size_t ch = (size_t)c * a.Hv + h;
-  load_rows(a.q, a.io_dtype, t0, L, a.Hqk, hq, K, a.use_qk_l2norm != 0, Qn);
-  load_rows(a.k, a.io_dtype, t0, L, a.Hqk, hq, K, a.use_qk_l2norm != 0, Kn);
+  load_rows(a.q, a.io_dtype, t0, L, a.Hqk, hq, K, a.use_qk_l2norm != 0, Qn, K);
+  load_rows(a.k, a.io_dtype, t0, L, a.Hqk, hq, K, a.use_qk_l2norm != 0, Kn, K);
   const float* Sg = ws.S + ch * K * V;
   for (int e = threadIdx.x; e < K * kVT; e += kThreads) {
     const int d = e / kVT, cc = e - d * kVT;
@@ -413,6 +262,23 @@ size_t chunk_generic_workspace_bytes(int T_total, int num_seqs, int Hv, int K, i
   size_t total = 0;
   ws_layout(nullptr, max_chunks(T_total, num_seqs), num_seqs, Hv, K, V, &total);
   return total;
+}
+
+cudaError_t launch_chunk_states(const ChunkArgs& a, int32_t* chunk_off, float* W, float* U,
+                                float* G, float* S) {
+  WsLayout ws;
+  ws.chunk_off = chunk_off;
+  ws.W = W;
+  ws.U = U;
+  ws.G = G;
+  ws.S = S;
+  const size_t ss = state_smem(a.K);
+  cudaError_t err;
+  if ((err = cudaFuncSetAttribute(chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss))) return err;
+  if (a.num_seqs <= 0) return cudaSuccess;
+  const unsigned vtiles = (unsigned)((a.V + kVT - 1) / kVT);
+  chunk_state_kernel<<<dim3(a.num_seqs, a.Hv, vtiles), kThreads, ss, a.stream>>>(a, ws);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_chunk_generic(const ChunkArgs& a) {

@@ -81,6 +81,30 @@ inline long long max_chunks(int T_total, int num_seqs) {
 size_t chunk_generic_workspace_bytes(int T_total, int num_seqs, int Hv, int K, int V);
 cudaError_t launch_chunk_generic(const ChunkArgs& a);
 
+// The serial state pass of the fp32 chunk path on caller-provided buffers: from the
+// per-chunk W = T diag(beta exp G) K, U = T diag(beta) V and in-chunk cumulative G
+// ([NC][Hv][C][K], [NC][Hv][C][V], [NC][Hv][C]), records the state at every chunk
+// entry in S [NC][Hv][K][V] and overwrites U with U' = U - W S.  chunk_off is the
+// device chunk table (launch_chunk_table).
+cudaError_t launch_chunk_states(const ChunkArgs& a, int32_t* chunk_off, float* W, float* U,
+                                float* G, float* S);
+
+// Gradients for the backward of the chunkwise rule (all device pointers).
+struct BwdArgs {
+  const void* d_o;        // [T_total, Hv, V] io dtype
+  const float* d_final;   // [N, Hv, K, V] or NULL (zero)
+  void* dq;               // [T_total, Hqk, K] io dtype
+  void* dk;               // [T_total, Hqk, K] io dtype
+  void* dv;               // [T_total, Hv, V] io dtype
+  float* dg;              // [T_total, Hv]
+  float* dbeta;           // [T_total, Hv]
+  float* d_initial;       // [N, Hv, K, V] or NULL
+};
+
+// Backward of the chunkwise rule on the fp32 CUDA cores (given gates, no slot cache).
+size_t chunk_bwd_workspace_bytes(int T_total, int num_seqs, int Hv, int K, int V);
+cudaError_t launch_chunk_bwd(const ChunkArgs& a, const BwdArgs& b);
+
 // Fused tcgen05 / TMEM / TMA path (bf16, K = V = 128).
 bool chunk_tc_supported(int K, int V, int io_dtype, int beta_dtype);
 cudaError_t launch_chunk_tc(const ChunkArgs& a);

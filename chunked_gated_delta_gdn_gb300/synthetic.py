@@ -26,7 +26,8 @@ from typing import Optional
 import torch
 
 __all__ = ["ChunkInputs", "DecodeInputs", "ProductInputs", "chunk_inputs", "decode_inputs",
-           "product_inputs", "product_decode_inputs", "WORKLOADS", "varlen_lengths"]
+           "product_inputs", "product_decode_inputs", "output_grads", "WORKLOADS",
+           "varlen_lengths"]
 
 
 @dataclasses.dataclass
@@ -240,3 +241,17 @@ def product_decode_inputs(n_h=2, n=32, Hqk=2, Hv=4, K=128, V=128, dtype=torch.bf
     if npad:
         idx[torch.randperm(n, generator=gen)[:npad]] = -1
     return ProductInputs(q=q, k=k, v=v, g=g, beta=beta, state=cache, cu_seqlens=None, slots=idx)
+
+
+def output_grads(inp: ChunkInputs, seed=0, d_final=True):
+    """Upstream gradients for the backward of a ChunkInputs batch: d_o ~ N(0, 1) in the
+    inputs' dtype, shaped like the output, and d_final_state ~ N(0, 1) fp32 [N, Hv, K, V]
+    (None when ``d_final`` is False)."""
+    gen = torch.Generator().manual_seed(seed)
+    B, T = inp.q.shape[:2]
+    Hv, V = inp.v.shape[2:]
+    K = inp.q.shape[3]
+    N = B if inp.cu_seqlens is None else inp.cu_seqlens.numel() - 1
+    d_o = _randn(gen, (B, T, Hv, V)).to(inp.q.dtype)
+    dfin = _randn(gen, (N, Hv, K, V)) if d_final else None
+    return d_o, dfin

@@ -316,6 +316,51 @@ gdn_status_t gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, 
                                    const int32_t* state_indices, int num_slots, void* o,
                                    int* dev_status, void* stream);
 
+/*
+ * gdn_chunk_bwd -- backward (training) of the chunkwise gated delta rule.
+ *
+ * Training runs the chunked rule ("Megatron-Core API: core.ssm.gated_delta_net.gdn",
+ * torch_chunk_gated_delta_rule, whose deterministic mode is the reason it exists;
+ * "Megatron-Core API: core.ssm.gated_delta_product", _gdp_chunk_forward, shared by
+ * training and prefill).  The sources print no backward: this returns the exact
+ * gradients of gdn_chunk_fwd's outputs, computed chunkwise in fp32 on the CUDA
+ * cores, with no atomics (bitwise identical from run to run).
+ *
+ * Forward arguments (q, k, v, g, beta, B, T, Hqk, Hv, K, V, io_dtype, beta_dtype,
+ * scale, chunk_size = 64, initial_state [N, Hv, K, V] or NULL, use_qk_l2norm,
+ * cu_seqlens, num_seqs) are those of the forward call being differentiated, with
+ * the same layouts and rules as gdn_chunk_fwd; there is no slot cache here
+ * (state_indices) and g / beta are given (not the fused gates).
+ *   d_o          [B, T, Hv, V] io_dtype, device: gradient of the loss w.r.t. o.
+ *   d_final_state  [N, Hv, K, V] fp32, device, or NULL (zero): gradient w.r.t.
+ *                the final states.
+ *   dq, dk       [B, T, Hqk, K] io_dtype, device, written completely (the value
+ *                heads sharing a query/key head are summed).
+ *   dv           [B, T, Hv, V] io_dtype, device, written completely.
+ *   dg, dbeta    [B, T, Hv] fp32, device, written completely.
+ *   d_initial_state  [N, Hv, K, V] fp32, device, or NULL (not computed).
+ * Tokens past the last sequence (cu_seqlens[N] < T) get zero gradients.  A
+ * non-monotone cu_seqlens is reported as GDN_DEV_BAD_CU_SEQLENS and every
+ * gradient is written as zero.
+ *   workspace, workspace_bytes  device scratch of at least
+ *                gdn_chunk_bwd_workspace_size(...) bytes, 16-byte aligned, owned
+ *                by the caller (about 4 (2 K V + 3 C V + C K + C C + C) bytes per
+ *                chunk of C = 64 tokens and value head, plus 8 Hv K bytes per token).
+ * Errors as gdn_chunk_fwd: host-side checks return a status before any launch.
+ */
+gdn_status_t gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
+                           const void* beta, int B, int T, int Hqk, int Hv, int K, int V,
+                           gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype, float scale,
+                           int chunk_size, const float* initial_state, int use_qk_l2norm,
+                           const int32_t* cu_seqlens, int num_seqs, const void* d_o,
+                           const float* d_final_state, void* dq, void* dk, void* dv, float* dg,
+                           float* dbeta, float* d_initial_state, void* workspace,
+                           size_t workspace_bytes, int* dev_status, void* stream);
+
+/* Device scratch (bytes) gdn_chunk_bwd needs; (size_t)-1 for rejected sizes. */
+size_t gdn_chunk_bwd_workspace_size(int B, int T, int Hqk, int Hv, int K, int V, int num_seqs,
+                                    gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype);
+
 /* Static, NUL-terminated name of a status code ("GDN_OK", ...). */
 const char* gdn_status_string(gdn_status_t status);
 

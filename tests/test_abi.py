@@ -150,3 +150,36 @@ def test_product_entry_points_reject_bad_arguments():
     assert lib.gdn_product_decode(*bad) == _lib.GDN_ERR_SHAPE
     bad = list(dec); bad[5] = None
     assert lib.gdn_product_decode(*bad) == _lib.GDN_ERR_NULL
+
+
+def bwd_call(**kw):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, B=1, T=64, Hqk=1, Hv=1, K=64, V=64,
+                io=_lib.GDN_F32, bdt=_lib.GDN_F32, scale=float("nan"), chunk=64, init=None, l2=1,
+                cu=None, N=1, do=FAKE, dfin=None, dq=FAKE, dk=FAKE, dv=FAKE, dg=FAKE, db=FAKE,
+                dinit=None, ws=None, wsb=0, status=None, stream=None)
+    args.update(kw)
+    return _lib.load().gdn_chunk_bwd(*args.values())
+
+
+def test_backward_entry_point_rejects_bad_arguments():
+    lib = _lib.load()
+    need = lib.gdn_chunk_bwd_workspace_size(1, 64, 1, 1, 64, 64, 1, 0, 0)
+    # per chunk and value head: W, U, dUp, dX (C x 64), S, dS (64 x 64), T (C x C), G (C);
+    # per token: dQ, dK of every value head; each piece rounded up to 256 bytes
+    per_chunk = 4 * (4 * 64 * 64 + 2 * 64 * 64 + 64 * 64 + 64)
+    assert per_chunk * 2 + 64 * 2 * 64 * 4 <= need <= per_chunk * 2 + 64 * 2 * 64 * 4 + 12 * 256
+    assert lib.gdn_chunk_bwd_workspace_size(1, 64, 2, 3, 64, 64, 1, 0, 0) == (1 << 64) - 1
+    assert bwd_call(chunk=32) == _lib.GDN_ERR_UNSUPPORTED
+    assert bwd_call(do=None) == _lib.GDN_ERR_NULL
+    assert bwd_call(db=None) == _lib.GDN_ERR_NULL
+    assert bwd_call(Hv=3, Hqk=2) == _lib.GDN_ERR_SHAPE
+    assert bwd_call(K=256) == _lib.GDN_ERR_SHAPE
+    assert bwd_call(io=5) == _lib.GDN_ERR_DTYPE
+    assert bwd_call(dq=FAKE + 4) == _lib.GDN_ERR_LAYOUT
+    assert bwd_call(dg=FAKE + 2) == _lib.GDN_ERR_LAYOUT
+    assert bwd_call(dinit=FAKE + 8) == _lib.GDN_ERR_LAYOUT
+    assert bwd_call(B=2, cu=FAKE) == _lib.GDN_ERR_SHAPE
+    assert bwd_call() == _lib.GDN_ERR_WORKSPACE
+    assert bwd_call(ws=FAKE, wsb=need - 1) == _lib.GDN_ERR_WORKSPACE
+    assert bwd_call(ws=FAKE + 8, wsb=need) == _lib.GDN_ERR_LAYOUT
+    assert bwd_call(T=0, N=0, B=1, cu=FAKE) == _lib.GDN_OK
