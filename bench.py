@@ -7,7 +7,9 @@ norm, mixer-style gates) followed by one decode step over 256 requests (26 of
 them padding) on a 512-slot fp32 state cache -- every kernel of the path.
 
 Prints one JSON line.  ``value`` is chunked-forward tokens/s (B*T per step over
-the chunked-forward time); the decode half is reported under ``decode``.
+the chunked-forward time); the decode half is reported under ``decode``.  Beside
+the step, and outside its timed region: the Gated Delta Product (``product``) and
+the chunked backward of the same batch (``backward``).
 ``--impl reference`` times the fp64 CPU oracle instead (the reference arm).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
@@ -40,6 +42,14 @@ FLOP_PER_TOKEN = HQK_ * 2 * C_ * K_ + HV_ * (C_ * K_ + 2 * C_ * V_ + 6 * K_ * V_
 # Minimum HBM bytes per token of a fully fused pass: q, k, v, o in bf16, g fp32, beta bf16.
 BYTES_PER_TOKEN = HQK_ * K_ * 2 * 2 + HV_ * V_ * 2 * 2 + HV_ * 4 + HV_ * 2
 STATE_BYTES = K_ * V_ * 4
+# Algorithmic work per token of the backward on top of the forward recompute (per value
+# head: K dS, Q^T dO', K^T dX', dO S0^T, dX S0^T, U' dS^T (6 K V), T^T dU', P^T dO and the
+# two [C][C] products over V (2 C V), the four triangular [C][C] x K products (2 C K); per
+# query/key head: Q K^T and K K^T (C K)), in multiply-adds, times 2 for FLOPs.
+BWD_FLOP_PER_TOKEN = FLOP_PER_TOKEN + 2 * (HV_ * (6 * K_ * V_ + 2 * C_ * V_ + 2 * C_ * K_) +
+                                           HQK_ * C_ * K_)
+# fp32 FMA peak of the CUDA cores: 152 SMs x 128 FP32 lanes x 2 FLOP x 2070 MHz (max SM clock).
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
 METRIC = "chunked GDN fwd tokens/s + % tensor peak; decode tokens/s + state HBM GB/s"
 WORKLOAD = ("long-context chunked fwd B=4 T=32768 Hqk=16 Hv=32 K=V=128 chunk 64 + decode 256 "
             "requests (26 padding) on 512 slots")
@@ -185,6 +195,46 @@ def measure_product(dev, seed, steps=10, warmup=3):
                        "state_gbs": n_real * HV_ * STATE_BYTES * 2 / res["decode"] / 1e9}}
 
 
+def measure_backward(dev, cin, d, seed, steps=5, warmup=3):
+    """The chunked backward (gdn_chunk_bwd: dq, dk, dv, dg, dbeta, d_initial_state) on the
+    headline batch with seeded upstream gradients d_o ~ N(0, 1) (bf16) and d_final ~ N(0, 1).
+    CUDA events on the current stream, after warm-up; the whole call (six launches)."""
+    from chunked_gated_delta_gdn_gb300 import _lib, chunk_gated_delta_rule_bwd, synthetic
+    B, T = cin.q.shape[:2]
+    d_o, dfin = synthetic.output_grads(cin, seed=seed)
+    d_o, dfin = d_o.to(dev), dfin.to(dev)
+    init = torch.zeros(B, HV_, K_, V_, dtype=torch.float32, device=dev)
+    need = int(_lib.load().gdn_chunk_bwd_workspace_size(B, T, HQK_, HV_, K_, V_, B,
+                                                        _lib.GDN_BF16, _lib.GDN_BF16))
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+
+    def bwd():
+        return chunk_gated_delta_rule_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d_o, dfin,
+                                          initial_state=init, use_qk_l2norm_in_kernel=True,
+                                          workspace=ws)
+
+    for _ in range(warmup):
+        bwd()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        bwd()
+    e1.record()
+    torch.cuda.synchronize()
+    sec = e0.elapsed_time(e1) / steps / 1000.0
+    tokens = B * T
+    tf = BWD_FLOP_PER_TOKEN * tokens / sec / 1e12
+    return {"workload": "backward of the headline batch (B=%d T=%d Hqk=16 Hv=32 K=V=128 bf16 "
+                        "I/O, fp32 compute), d_o and d_final_state given" % (B, T),
+            "ms": sec * 1e3, "tokens_per_s": tokens / sec, "launches": 6, "steps": steps,
+            "workspace_bytes": need,
+            "alu": {"bound": "alu", "achieved": tf, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
+                    "frac": tf / FP32_PEAK_TFLOPS, "flop_per_token": BWD_FLOP_PER_TOKEN,
+                    "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 x 2070 MHz",
+                    "scope": "whole backward call (all six launches)"}}
+
+
 def _product_ws(T, n_h):
     from chunked_gated_delta_gdn_gb300 import _lib
     return int(_lib.load().gdn_product_chunk_fwd_workspace_size(1, T, n_h, HQK_, HV_, K_, V_, 1,
@@ -257,8 +307,12 @@ def main():
                     help="override B of the chunked workload (profiling runs on a smaller case)")
     ap.add_argument("--no-product", action="store_true",
                     help="skip the Gated Delta Product measurement reported beside the headline")
-    ap.add_argument("--only", choices=["chunk", "decode"], default=None,
-                    help="time one half of the step (profiling); the JSON line stays the same")
+    ap.add_argument("--only", choices=["chunk", "decode", "backward"], default=None,
+                    help="time one half of the step, or only the backward (profiling); the "
+                         "JSON line keeps its keys, the parts not timed are null")
+    ap.add_argument("--no-backward", action="store_true",
+                    help="skip the chunked-backward measurement reported beside the headline")
+    ap.add_argument("--backward-steps", type=int, default=5)
     args = ap.parse_args()
     world, rank, local = dist_env()
     if world > 1:
@@ -296,13 +350,13 @@ def main():
     launches_per_step = (1 if path == 1 else 4) + 1
 
     def chunk():
-        if args.only == "decode":
+        if args.only in ("decode", "backward"):
             return
         chunk_gated_delta_rule(d["q"], d["k"], d["v"], d["g"], d["beta"], output_final_state=True,
                                use_qk_l2norm_in_kernel=True, out=o, final_state=fin)
 
     def decode():
-        if args.only == "chunk":
+        if args.only in ("chunk", "backward"):
             return
         gated_delta_decode(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dd["ssm_state"],
                            dd["batch_indices"], out=od)
@@ -394,10 +448,15 @@ def main():
     }
     if args.only is None and not args.no_product:
         line["product"] = measure_product(dev, 1006 + 1000 * rank)
+    if args.only in (None, "backward") and not args.no_backward:
+        line["backward"] = measure_backward(dev, cin, d, 1007 + 1000 * rank,
+                                            steps=args.backward_steps)
     if args.only == "chunk":      # profiling runs: the half that was not timed is not reported
         line["decode"] = None
-    elif args.only == "decode":
+    elif args.only in ("decode", "backward"):
         line.update(value=None, chunk_ms=None, roofline=None, tensor=None)
+        if args.only == "backward":
+            line["decode"] = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sample = 8192
         dt, cores = cpu_oracle_sample(cin, sample)

@@ -30,10 +30,12 @@
 // Six launches on the caller's stream, no host sync and no atomics (the result is
 // bitwise reproducible run to run):
 //   1. chunk table  from cu_seqlens, on the device
-//   2. prep         per (chunk, value head): T, W = T diag(beta gamma) K,
-//                   U = T diag(beta) V, dUp = scale P^T dO, G
-//   3. states       per (sequence, value head, 32 columns): the forward state pass of
-//                   the fp32 chunk path (entry state S0 of every chunk, U')
+//   2. states       the forward recompute of the entry state S0 of every chunk and of U':
+//                   bf16 with K = V = 128, the tensor-core forward kernel in record mode;
+//                   otherwise (after 3) the fp32 state pass per (sequence, value head,
+//                   32 columns) on W, U from the prep kernel
+//   3. prep         per (chunk, value head): T, dUp = scale P^T dO, G, and for the fp32
+//                   state pass W = T diag(beta gamma) K, U = T diag(beta) V
 //   4. reverse      per (sequence, value head, 32 columns), chunks last to first:
 //                   records dS (the gradient of each chunk's exit state) and dX
 //   5. grad         per (chunk, value head): dv, dbeta, dg, and dQ, dK per value head
@@ -164,7 +166,7 @@ constexpr int kPrepThreads = 256;
 constexpr size_t kPrepSmem = sizeof(float) * (3 * C * LD + 3 * C * LDC + 3 * C);
 
 __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const ChunkArgs a, const BwdArgs b,
-                                                                BwdWs ws) {
+                                                                BwdWs ws, int need_wu) {
   extern __shared__ float smem[];
   float* Kn = smem;           // [C][LD] normalised k, then diag(beta gamma) k
   float* X1 = Kn + C * LD;    // [C][LD] normalised q, then diag(beta) v
@@ -227,12 +229,14 @@ __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const ChunkArgs 
   const size_t ch = (size_t)c * a.Hv + h;
   {
     float acc[8][4];
-    zero(acc);  // W = T diag(beta gamma) K  (T lower triangular: columns m <= i)
-    fma_tile<8, 4, LDC, 1, LD, 32>(acc, Tm + i0 * LDC, Kn + lane, 0, i0 + 8);
-    store_rows(ws.W + ch * C * K, K, acc, i0, lane, 1.f);
-    zero(acc);  // U = T diag(beta) V
-    fma_tile<8, 4, LDC, 1, LD, 32>(acc, Tm + i0 * LDC, X1 + lane, 0, i0 + 8);
-    store_rows(ws.U + ch * C * V, V, acc, i0, lane, 1.f);
+    if (need_wu) {  // the inputs of the fp32 forward state pass
+      zero(acc);    // W = T diag(beta gamma) K  (T lower triangular: columns m <= i)
+      fma_tile<8, 4, LDC, 1, LD, 32>(acc, Tm + i0 * LDC, Kn + lane, 0, i0 + 8);
+      store_rows(ws.W + ch * C * K, K, acc, i0, lane, 1.f);
+      zero(acc);    // U = T diag(beta) V
+      fma_tile<8, 4, LDC, 1, LD, 32>(acc, Tm + i0 * LDC, X1 + lane, 0, i0 + 8);
+      store_rows(ws.U + ch * C * V, V, acc, i0, lane, 1.f);
+    }
     zero(acc);  // dUp = scale P^T dO  (P lower triangular: rows m >= i)
     fma_tile<8, 4, 1, LDC, LD, 32>(acc, P + i0, dO + lane, i0, C);
     store_rows(ws.dUp + ch * C * V, V, acc, i0, lane, a.scale);
@@ -674,11 +678,25 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
   if ((err = cudaFuncSetAttribute(bwd_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGradSmem))) return err;
   chunk_table_kernel<<<1, 1024, 0, a.stream>>>(a, ws.chunk_off);
   if ((err = cudaGetLastError())) return err;
+  // Forward recompute of the state entering every chunk and of U'.  bf16 with K = V = 128:
+  // the tensor-core kernel in record mode (its output goes to scratch that the dQ buffer
+  // reuses later); otherwise the fp32 state pass on W, U from the prep kernel.
+  const bool tc = chunk_tc_supported(a.K, a.V, a.io_dtype, a.beta_dtype) &&
+                  a.gates.mode == kGatesGiven;
+  if (tc && T_total > 0) {
+    ChunkArgs f = a;
+    f.o = ws.dQ;   // [T_total][Hv][V] bf16 fits in [T_total][Hv][K] fp32
+    f.rec_states = ws.S;
+    f.rec_u = ws.U;
+    f.rec_chunk_off = ws.chunk_off;
+    if ((err = launch_chunk_tc(f))) return err;
+  }
   if (NC > 0) {
-    bwd_prep_kernel<<<dim3((unsigned)NC, a.Hv), kPrepThreads, kPrepSmem, a.stream>>>(a, b, ws);
+    bwd_prep_kernel<<<dim3((unsigned)NC, a.Hv), kPrepThreads, kPrepSmem, a.stream>>>(a, b, ws,
+                                                                                      tc ? 0 : 1);
     if ((err = cudaGetLastError())) return err;
   }
-  if ((err = launch_chunk_states(a, ws.chunk_off, ws.W, ws.U, ws.G, ws.S))) return err;
+  if (!tc && (err = launch_chunk_states(a, ws.chunk_off, ws.W, ws.U, ws.G, ws.S))) return err;
   const unsigned vtiles = (unsigned)((a.V + VT - 1) / VT);
   if (a.num_seqs > 0) {
     bwd_reverse_kernel<<<dim3(a.num_seqs, a.Hv, vtiles), kRevThreads, kRevSmem, a.stream>>>(a, b, ws);

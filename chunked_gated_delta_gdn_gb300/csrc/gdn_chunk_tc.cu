@@ -507,8 +507,9 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
 // =================================================================== state group
 // Warps 8-11.  For each chunk: U^T = V^T Tu^T, S -> bf16 operand and decay of the TMEM
 // state, [O1 | Y] = S^T [Q; K]^T, U' = U - Y Tw^T, [O2 | S^T] += U'^T [P; K~^T]^T, output.
+template <bool kRecord>
 __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int bos, int eos,
-                            int nchunks, int h, int hq, size_t st_off,
+                            int nchunks, int h, int hq, size_t st_off, long long rec0,
                             const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                             const CUtensorMap* to) {
   const int tid = threadIdx.x - kPrepThreads, wq = tid >> 5, lane = tid & 31;
@@ -548,9 +549,11 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
       }
     }
     // ---- S (entry state) -> bf16 S^T in the O2 columns (the next product's A operand);
-    //      S <- exp(G_last) S in TMEM
+    //      S <- exp(G_last) S in TMEM.  Record mode also stores the fp32 entry state.
     {
       const float dl = ex2(vec[VEC_G + L - 1]);
+      float* rec_s = kRecord ? a.rec_states + ((size_t)(rec0 + c) * a.Hv + h) * (size_t)(DK * DV) + row
+                             : nullptr;
 #pragma unroll
       for (int pair = 0; pair < 2; ++pair) {
         float pk[32];
@@ -559,6 +562,10 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
           float x[32];
           const uint32_t col = COL_S + 32 * (2 * pair + sub);
           tmem_ld32(tbase + lane_off + col, x);
+          if (kRecord) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) rec_s[(size_t)(32 * (2 * pair + sub) + j) * DV] = x[j];
+          }
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
             __nv_bfloat162 p2 = __floats2bfloat162_rn(x[2 * jj], x[2 * jj + 1]);
@@ -673,11 +680,20 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     if (group_sync_or(kBarState, kStateThreads, !ok || flag_set(flag))) { failed = true; break; }
     tc_fence_after();
 
-    // ---- U'^T -> bf16, packed into the first 32 of its own TMEM columns (A operand)
+    // ---- U'^T -> bf16, packed into the first 32 of its own TMEM columns (A operand);
+    //      record mode stores the fp32 U' rows of the chunk's tokens
     {
       float x[32], y[32], pk[32];
       tmem_ld32(tbase + lane_off + COL_U, x);
       tmem_ld32(tbase + lane_off + COL_U + 32, y);
+      if (kRecord) {
+        float* ru = a.rec_u + ((size_t)(rec0 + c) * a.Hv + h) * (size_t)(kChunk * DV) + row;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (j < L) ru[(size_t)j * DV] = x[j];
+          if (j + 32 < L) ru[(size_t)(j + 32) * DV] = y[j];
+        }
+      }
 #pragma unroll
       for (int jj = 0; jj < 16; ++jj) {
         __nv_bfloat162 p0 = __floats2bfloat162_rn(x[2 * jj], x[2 * jj + 1]);
@@ -791,6 +807,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
   }
 }
 
+template <bool kRecord>
 __global__ void __launch_bounds__(kTcThreads, 1)
     chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -871,7 +888,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         x[j] = a.initial_state ? a.initial_state[st_off + (size_t)(32 * part + j) * DV + row] : 0.f;
       tmem_st32(tbase + lane_off + COL_S + 32 * part, x);
     }
-    state_group(a, sm, tbase, bos, eos, nchunks, h, hq, st_off, &tmQ, &tmK, &tmV, &tmO);
+    const long long rec0 = kRecord ? a.rec_chunk_off[n] : 0;
+    state_group<kRecord>(a, sm, tbase, bos, eos, nchunks, h, hq, st_off, rec0, &tmQ, &tmK, &tmV,
+                         &tmO);
   }
 
   __syncthreads();
@@ -931,13 +950,21 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a) {
         !encode_map(&mv, a.v, a.Hv, T_total) || !encode_map(&mo, a.o, a.Hv, T_total))
       return cudaErrorInvalidValue;
   }
-  cudaError_t err = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
+  const bool rec = a.rec_states && a.rec_u && a.rec_chunk_off;
+  cudaError_t err = rec ? cudaFuncSetAttribute(chunk_tc_kernel<true>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)SMEM_BYTES)
+                        : cudaFuncSetAttribute(chunk_tc_kernel<false>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)SMEM_BYTES);
   if (err != cudaSuccess) return err;
   const long long blocks = (long long)a.num_seqs * a.Hv;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  chunk_tc_kernel<<<(unsigned)blocks, kTcThreads, SMEM_BYTES, a.stream>>>(mq, mk, mv, mo, a);
+  if (rec)
+    chunk_tc_kernel<true><<<(unsigned)blocks, kTcThreads, SMEM_BYTES, a.stream>>>(mq, mk, mv, mo, a);
+  else
+    chunk_tc_kernel<false><<<(unsigned)blocks, kTcThreads, SMEM_BYTES, a.stream>>>(mq, mk, mv, mo, a);
   return cudaGetLastError();
 }
 

@@ -46,6 +46,12 @@ struct ChunkArgs {
   int* dev_status;
   cudaStream_t stream;
   GateArgs gates;
+  // Record mode of the tensor-core kernel (the backward's forward recompute): when set, the
+  // state entering every chunk goes to rec_states [NC][Hv][K][V] and U' (rows < L) to
+  // rec_u [NC][Hv][64][V], chunk numbering from the device chunk table rec_chunk_off.
+  float* rec_states = nullptr;
+  float* rec_u = nullptr;
+  const int32_t* rec_chunk_off = nullptr;
 };
 
 struct DecodeArgs {
