@@ -63,6 +63,7 @@ struct BwdWs {
   float* dUp;          // [NC][Hv][C][V]  scale P^T dO
   float* dS;           // [NC][Hv][K][V]  gradient of the chunk's exit state
   float* dX;           // [NC][Hv][C][V]
+  float* Z;            // [NC][Hv][K][V]  scale Q^T diag(gamma) dO
   float* dQ;           // [T_total][Hv][K] per value head, before the norm
   float* dK;           // [T_total][Hv][K]
 };
@@ -89,6 +90,7 @@ __host__ __device__ inline BwdWs bwd_layout(void* base, long long NC, int N, int
   w.dUp = reinterpret_cast<float*>(take(f * ch * C * V));
   w.dS = reinterpret_cast<float*>(take(f * ch * K * V));
   w.dX = reinterpret_cast<float*>(take(f * ch * C * V));
+  w.Z = reinterpret_cast<float*>(take(f * ch * K * V));
   w.dQ = reinterpret_cast<float*>(take(f * (size_t)T_total * Hv * K));
   w.dK = reinterpret_cast<float*>(take(f * (size_t)T_total * Hv * K));
   if (total) *total = off;
@@ -161,213 +163,350 @@ __device__ __forceinline__ void store_rows(float* dst, int D, const float (&acc)
     }
 }
 
-// ---------------------------------------------------------------- 2. prep
-constexpr int kPrepThreads = 256;
-constexpr size_t kPrepSmem = sizeof(float) * (3 * C * LD + 3 * C * LDC + 3 * C);
+// ---------------------------------------------------------------- 3. prep
+// Per (chunk, value head), 16 warps: A and P, T = (I + A)^{-1}, dUp = scale P^T dO and
+// Z = scale Q^T diag(gamma) dO (the part of the state-gradient step that does not depend on
+// the state gradient, taken out of the serial reverse pass), and for the fp32 state pass
+// W = T diag(beta gamma) K, U = T diag(beta) V.
+constexpr int kPrepThreads = 512;
+constexpr int DLD = KP + 4;  // row stride of [C][KP] tiles read as float4 (16-byte aligned rows)
+constexpr size_t kPrepSmem = sizeof(float) * (2 * C * LD + C * DLD + 3 * C * LDC + 3 * C);
+
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 
 __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const ChunkArgs a, const BwdArgs b,
                                                                 BwdWs ws, int need_wu) {
   extern __shared__ float smem[];
-  float* Kn = smem;           // [C][LD] normalised k, then diag(beta gamma) k
-  float* X1 = Kn + C * LD;    // [C][LD] normalised q, then diag(beta) v
-  float* dO = X1 + C * LD;    // [C][LD]
-  float* A = dO + C * LD;     // [C][LDC]
+  float* Kn = smem;           // [C][LD] normalised k (then diag(beta gamma) k)
+  float* Qn = Kn + C * LD;    // [C][LD] normalised q
+  float* dO = Qn + C * LD;    // [C][DLD] dO (then diag(beta) v)
+  float* A = dO + C * DLD;    // [C][LDC]
   float* P = A + C * LDC;     // [C][LDC]
   float* Tm = P + C * LDC;    // [C][LDC]
   float* G = Tm + C * LDC;    // [C]
   float* bt = G + C;          // [C]
-  float* bg = bt + C;         // [C] beta * gamma
+  float* gm = bt + C;         // [C] gamma
   const int c = blockIdx.x, h = blockIdx.y;
   int n, t0, L;
   if (!locate_chunk(a, ws.chunk_off, c, &n, &t0, &L)) return;
   const int K = a.K, V = a.V, hq = h / (a.Hv / a.Hqk);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool l2 = a.use_qk_l2norm != 0;
   load_rows(a.k, a.io_dtype, t0, L, a.Hqk, hq, K, l2, Kn, LD);
-  load_rows(a.q, a.io_dtype, t0, L, a.Hqk, hq, K, l2, X1, LD);
+  load_rows(a.q, a.io_dtype, t0, L, a.Hqk, hq, K, l2, Qn, LD);
   zero_cols(Kn, K);
-  zero_cols(X1, K);
+  zero_cols(Qn, K);
+  load_tile(b.d_o, a.io_dtype, t0, L, a.Hv, h, V, 0, KP, nullptr, dO, DLD, 0, kPrepThreads / 32);
   load_gates(a, t0, L, h, G, bt);
   __syncthreads();
-  const int i0 = 8 * warp;  // 8 warps x 8 rows
-  {
-    float kk[8][2], qk[8][2];
+  if (tid < C) gm[tid] = expf(G[tid]);
+  {  // A = strict_lower(diag(beta) K K^T * Gamma), P = (Q K^T * Gamma) on and below the diagonal
+    const int i0 = 4 * warp;
+    float kk[4][2], qk[4][2];
     zero(kk);
     zero(qk);
-    fma_tile<8, 2, LD, 1, 1, 32 * LD>(kk, Kn + i0 * LD, Kn + lane * LD, 0, K);
-    fma_tile<8, 2, LD, 1, 1, 32 * LD>(qk, X1 + i0 * LD, Kn + lane * LD, 0, K);
+    fma_tile<4, 2, LD, 1, 1, 32 * LD>(kk, Kn + i0 * LD, Kn + lane * LD, 0, K);
+    fma_tile<4, 2, LD, 1, 1, 32 * LD>(qk, Qn + i0 * LD, Kn + lane * LD, 0, K);
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
+    for (int r = 0; r < 4; ++r)
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
         const int i = i0 + r, j = lane + 32 * m;
-        const float gm = j <= i ? expf(G[i] - G[j]) : 0.f;
-        A[i * LDC + j] = j < i ? bt[i] * kk[r][m] * gm : 0.f;
-        P[i * LDC + j] = qk[r][m] * gm;
+        const float gij = j <= i ? expf(G[i] - G[j]) : 0.f;
+        A[i * LDC + j] = j < i ? bt[i] * kk[r][m] * gij : 0.f;
+        P[i * LDC + j] = qk[r][m] * gij;
       }
-  }
-  if (threadIdx.x < C) bg[threadIdx.x] = bt[threadIdx.x] * expf(G[threadIdx.x]);
-  __syncthreads();
-  if (threadIdx.x < C) {
-    // T = (I + A)^{-1}, one column per thread by forward substitution
-    const int j = threadIdx.x;
-    for (int i = 0; i < C; ++i) {
-      float t = i == j ? 1.f : 0.f;
-      for (int m = j; m < i; ++m) t -= A[i * LDC + m] * Tm[m * LDC + j];
-      Tm[i * LDC + j] = t;
-    }
-  } else {
-    // meanwhile: diag(beta gamma) K in place, diag(beta) V, dO
-    for (int e = threadIdx.x - C; e < C * KP; e += kPrepThreads - C) {
-      const int r = e / KP, d = e - r * KP;
-      Kn[r * LD + d] *= bg[r];
-    }
-    load_tile(a.v, a.io_dtype, t0, L, a.Hv, h, V, 0, KP, bt, X1, LD, 2, 6);
-    load_tile(b.d_o, a.io_dtype, t0, L, a.Hv, h, V, 0, KP, nullptr, dO, LD, 2, 6);
   }
   __syncthreads();
   const size_t ch = (size_t)c * a.Hv + h;
-  {
-    float acc[8][4];
-    if (need_wu) {  // the inputs of the fp32 forward state pass
-      zero(acc);    // W = T diag(beta gamma) K  (T lower triangular: columns m <= i)
-      fma_tile<8, 4, LDC, 1, LD, 32>(acc, Tm + i0 * LDC, Kn + lane, 0, i0 + 8);
-      store_rows(ws.W + ch * C * K, K, acc, i0, lane, 1.f);
-      zero(acc);    // U = T diag(beta) V
-      fma_tile<8, 4, LDC, 1, LD, 32>(acc, Tm + i0 * LDC, X1 + lane, 0, i0 + 8);
-      store_rows(ws.U + ch * C * V, V, acc, i0, lane, 1.f);
+  const int ty = tid >> 4, tx = tid & 15;  // 32 row groups x 16 groups of 8 columns
+  {  // Z = scale Q^T diag(gamma) dO: rows d = ty + 32 r, columns 8 tx .. 8 tx + 7
+    float z[4][8];
+    zero(z);
+    for (int i = 0; i < L; ++i) {
+      const float g = gm[i];
+      float x[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) x[r] = g * Qn[i * LD + ty + 32 * r];
+      const float4 y0 = ld4(dO + i * DLD + 8 * tx), y1 = ld4(dO + i * DLD + 8 * tx + 4);
+      const float y[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) z[r][q] = fmaf(x[r], y[q], z[r][q]);
     }
-    zero(acc);  // dUp = scale P^T dO  (P lower triangular: rows m >= i)
-    fma_tile<8, 4, 1, LDC, LD, 32>(acc, P + i0, dO + lane, i0, C);
-    store_rows(ws.dUp + ch * C * V, V, acc, i0, lane, a.scale);
+    float* Zg = ws.Z + ch * K * V;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int d = ty + 32 * r;
+      if (d >= K) continue;
+#pragma unroll
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        const int col = 8 * tx + 4 * hlf;
+        if (col < V)
+          st4(Zg + (size_t)d * V + col,
+              make_float4(a.scale * z[r][4 * hlf], a.scale * z[r][4 * hlf + 1],
+                          a.scale * z[r][4 * hlf + 2], a.scale * z[r][4 * hlf + 3]));
+      }
+    }
   }
-  for (int e = threadIdx.x; e < C * C; e += kPrepThreads) {
+  if (tid < C) {
+    // T = (I + A)^{-1}, one column per thread by forward substitution (four partial sums)
+    const int j = tid;
+    for (int i = 0; i < C; ++i) {
+      float t = i == j ? 1.f : 0.f;
+      if (i > j) {
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+        int m = j;
+        for (; m + 3 < i; m += 4) {
+          s0 = fmaf(A[i * LDC + m], Tm[m * LDC + j], s0);
+          s1 = fmaf(A[i * LDC + m + 1], Tm[(m + 1) * LDC + j], s1);
+          s2 = fmaf(A[i * LDC + m + 2], Tm[(m + 2) * LDC + j], s2);
+          s3 = fmaf(A[i * LDC + m + 3], Tm[(m + 3) * LDC + j], s3);
+        }
+        for (; m < i; ++m) s0 = fmaf(A[i * LDC + m], Tm[m * LDC + j], s0);
+        t = -((s0 + s1) + (s2 + s3));
+      }
+      Tm[i * LDC + j] = t;
+    }
+  }
+  __syncthreads();
+  {  // dUp = scale P^T dO: rows i = ty, ty + 32, columns 8 tx .. 8 tx + 7 (P[m][i] = 0 for m < i)
+    float u[2][8];
+    zero(u);
+    for (int m = ty; m < C; ++m) {
+      const float x0 = P[m * LDC + ty], x1 = P[m * LDC + ty + 32];
+      const float4 y0 = ld4(dO + m * DLD + 8 * tx), y1 = ld4(dO + m * DLD + 8 * tx + 4);
+      const float y[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        u[0][q] = fmaf(x0, y[q], u[0][q]);
+        u[1][q] = fmaf(x1, y[q], u[1][q]);
+      }
+    }
+    float* Ug = ws.dUp + ch * C * V;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int i = ty + 32 * r;
+#pragma unroll
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        const int col = 8 * tx + 4 * hlf;
+        if (col < V)
+          st4(Ug + (size_t)i * V + col,
+              make_float4(a.scale * u[r][4 * hlf], a.scale * u[r][4 * hlf + 1],
+                          a.scale * u[r][4 * hlf + 2], a.scale * u[r][4 * hlf + 3]));
+      }
+    }
+  }
+  for (int e = tid; e < C * C; e += kPrepThreads) {
     const int i = e / C, j = e - i * C;
     ws.T[ch * C * C + e] = Tm[i * LDC + j];
   }
-  if (threadIdx.x < C) ws.G[ch * C + threadIdx.x] = G[threadIdx.x];
+  if (tid < C) ws.G[ch * C + tid] = G[tid];
+  if (need_wu) {  // the inputs of the fp32 forward state pass
+    __syncthreads();
+    for (int e = tid; e < C * KP; e += kPrepThreads) {
+      const int r = e / KP, d = e - r * KP;
+      Kn[r * LD + d] *= bt[r] * gm[r];
+    }
+    load_tile(a.v, a.io_dtype, t0, L, a.Hv, h, V, 0, KP, bt, dO, DLD, 0, kPrepThreads / 32);
+    __syncthreads();
+    const int i0 = 4 * warp;
+    float acc[4][4];
+    zero(acc);  // W = T diag(beta gamma) K  (T lower triangular: columns m <= i)
+    fma_tile<4, 4, LDC, 1, LD, 32>(acc, Tm + i0 * LDC, Kn + lane, 0, i0 + 4);
+    store_rows(ws.W + ch * C * K, K, acc, i0, lane, 1.f);
+    zero(acc);  // U = T diag(beta) V
+    fma_tile<4, 4, LDC, 1, DLD, 32>(acc, Tm + i0 * LDC, dO + lane, 0, i0 + 4);
+    store_rows(ws.U + ch * C * V, V, acc, i0, lane, 1.f);
+  }
 }
 
 // ---------------------------------------------------------------- 4. reverse
+// Per (32 columns of V, value head, sequence), chunks last to first, 8 warps, two CTAs per SM.
+// The state gradient dS of the 32 columns lives in registers (a 4 x 4 block per thread) and,
+// for the next chunk's K dS, in shared memory.  Per chunk:
+//   Y = K dS,  dU' = dUp + diag(lambda) Y,  dX = T^T dU',
+//   dS <- gamma_L dS + Z - K^T diag(gamma beta) dX     (Z from the prep kernel)
 constexpr int kRevThreads = 256;
-constexpr size_t kRevSmem = sizeof(float) * (2 * C * LD + C * LDC + KP * VT + 3 * C * LDT + 4 * C);
+constexpr int KLD = KP + 4;   // [C][KLD]: k rows, float4 reads
+constexpr int TLD = C + 2;    // [KP][TLD]: k transposed, float2 reads
+constexpr size_t kRevSmem = sizeof(float) * (C * KLD + KP * TLD + KP * VT + 2 * C * VT + 2 * C);
 
-__global__ void __launch_bounds__(kRevThreads) bwd_reverse_kernel(const ChunkArgs a,
-                                                                  const BwdArgs b, BwdWs ws) {
+__global__ void __launch_bounds__(kRevThreads, 2) bwd_reverse_kernel(const ChunkArgs a,
+                                                                     const BwdArgs b, BwdWs ws) {
   extern __shared__ float smem[];
-  float* Kn = smem;           // [C][LD]
-  float* Qn = Kn + C * LD;    // [C][LD]
-  float* Tm = Qn + C * LD;    // [C][LDC]
-  float* dS = Tm + C * LDC;   // [KP][VT]
-  float* dU = dS + KP * VT;   // [C][LDT] dUp, then dU'
-  float* dX = dU + C * LDT;   // [C][LDT] -diag(gamma beta) dX
-  float* dO = dX + C * LDT;   // [C][LDT] scale diag(gamma) dO
-  float* G = dO + C * LDT;    // [C]
-  float* bt = G + C;          // [C]
-  float* gm = bt + C;         // [C] gamma
-  float* gb = gm + C;         // [C] gamma * beta
-  const int n = blockIdx.x, h = blockIdx.y, c0 = blockIdx.z * VT;
+  float* Kn = smem;             // [C][KLD]
+  float* Kt = Kn + C * KLD;     // [KP][TLD]
+  float* dSs = Kt + KP * TLD;   // [KP][VT]
+  float* X1 = dSs + KP * VT;    // [C][VT] dUp, then dU'
+  float* X2 = X1 + C * VT;      // [C][VT] -diag(gamma beta) dX
+  float* G = X2 + C * VT;       // [C]
+  float* bt = G + C;            // [C]
+  // blocks: (32-column slice, value head, sequence), the slice fastest so that the slices of
+  // one head run side by side and share its k, T, dUp and Z reads in L2
+  const int nvt = (a.V + VT - 1) / VT;
+  const int c0 = (int)(blockIdx.x % nvt) * VT, h = (int)((blockIdx.x / nvt) % a.Hv);
+  const int n = (int)(blockIdx.x / nvt / a.Hv);
   const int K = a.K, V = a.V, hq = h / (a.Hv / a.Hqk);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tx = tid & 7, ty = tid >> 3;   // columns 4 tx .. 4 tx + 3; rows 4 ty.. or 2 ty..
+  const int col = c0 + 4 * tx;             // V % 4 == 0: a column group is all in or all out
+  const bool colok = col < V;
   const size_t st_off = ((size_t)n * a.Hv + h) * K * V;
   if (!ws.chunk_off[a.num_seqs + 1]) {  // invalid cu_seqlens: zero gradient
-    if (b.d_initial) {
-      for (int e = threadIdx.x; e < K * VT; e += kRevThreads) {
-        const int d = e / VT, cc = e - d * VT;
-        if (c0 + cc < V) b.d_initial[st_off + (size_t)d * V + c0 + cc] = 0.f;
-      }
+    if (b.d_initial && colok) {
+      for (int r = 0; r < 4; ++r)
+        if (4 * ty + r < K) st4(b.d_initial + st_off + (size_t)(4 * ty + r) * V + col, make_float4(0.f, 0.f, 0.f, 0.f));
     }
     return;
   }
   int bos, eos;
   seq_bounds(a, n, &bos, &eos);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool l2 = a.use_qk_l2norm != 0;
-  for (int e = threadIdx.x; e < KP * VT; e += kRevThreads) {
-    const int d = e / VT, cc = e - d * VT;
-    dS[e] = (b.d_final && d < K && c0 + cc < V) ? b.d_final[st_off + (size_t)d * V + c0 + cc] : 0.f;
+  float s[4][4];   // dS rows 4 ty + r, columns col .. col + 3
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int d = 4 * ty + r;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (b.d_final && colok && d < K) x = ld4(b.d_final + st_off + (size_t)d * V + col);
+    s[r][0] = x.x; s[r][1] = x.y; s[r][2] = x.z; s[r][3] = x.w;
+    st4(dSs + d * VT + 4 * tx, x);
   }
   const int first = ws.chunk_off[n];
   const int nch = (eos - bos + C - 1) / C;
-  const int i0 = 8 * warp;   // rows of the [C][VT] products
-  const int d0 = 16 * warp;  // rows of the [KP][VT] state product
   for (int qc = nch - 1; qc >= 0; --qc) {
     const int t0 = bos + qc * C, L = min(C, eos - t0);
     const size_t ch = (size_t)(first + qc) * a.Hv + h;
-    __syncthreads();  // the previous chunk's dS is written back
-    float* dSg = ws.dS + ch * K * V;
-    for (int e = threadIdx.x; e < KP * VT; e += kRevThreads) {
-      const int d = e / VT, cc = e - d * VT;
-      if (d < K && c0 + cc < V) dSg[(size_t)d * V + c0 + cc] = dS[e];
-    }
-    load_rows(a.k, a.io_dtype, t0, L, a.Hqk, hq, K, l2, Kn, LD);
-    load_rows(a.q, a.io_dtype, t0, L, a.Hqk, hq, K, l2, Qn, LD);
-    zero_cols(Kn, K);
-    zero_cols(Qn, K);
-    load_gates(a, t0, L, h, G, bt);
-    const float* Tg = ws.T + ch * C * C;
-    for (int e = threadIdx.x; e < C * C; e += kRevThreads) {
-      const int i = e / C, j = e - i * C;
-      Tm[i * LDC + j] = Tg[e];
-    }
-    const float* dUg = ws.dUp + ch * C * V;
-    for (int e = threadIdx.x; e < C * VT; e += kRevThreads) {
-      const int i = e / VT, cc = e - i * VT;
-      dU[i * LDT + cc] = c0 + cc < V ? dUg[(size_t)i * V + c0 + cc] : 0.f;
-    }
-    __syncthreads();
-    if (threadIdx.x < C) {
-      const float x = expf(G[threadIdx.x]);
-      gm[threadIdx.x] = x;
-      gb[threadIdx.x] = x * bt[threadIdx.x];
-    }
-    for (int e = threadIdx.x; e < C * VT; e += kRevThreads) {
-      const int i = e / VT, cc = e - i * VT;
-      const float x = (i < L && c0 + cc < V)
-                          ? load_elem(b.d_o, ((size_t)(t0 + i) * a.Hv + h) * V + c0 + cc, a.io_dtype)
-                          : 0.f;
-      dO[i * LDT + cc] = a.scale * expf(G[i]) * x;
-    }
-    {  // dU' = dUp + diag(lambda) K dS
-      float y[8][1];
-      zero(y);
-      fma_tile<8, 1, LD, 1, VT, 0>(y, Kn + i0 * LD, dS + lane, 0, K);
+    __syncthreads();  // the previous chunk is done with every tile
+    if (colok) {      // record dS, the gradient of this chunk's exit state
+      float* dSg = ws.dS + ch * K * V;
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const int i = i0 + r;
-        dU[i * LDT + lane] += expf(G[L - 1] - G[i]) * y[r][0];
+      for (int r = 0; r < 4; ++r)
+        if (4 * ty + r < K)
+          st4(dSg + (size_t)(4 * ty + r) * V + col, make_float4(s[r][0], s[r][1], s[r][2], s[r][3]));
+    }
+    // normalised k rows into Kn and Kt (warp w: rows w, w + 8, ...)
+    for (int r = warp; r < C; r += kRevThreads / 32) {
+      float x[4];
+      float ss = 0.f;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int d = lane + 32 * m;
+        x[m] = (r < L && d < K) ? load_elem(a.k, ((size_t)(t0 + r) * a.Hqk + hq) * K + d, a.io_dtype) : 0.f;
+        ss = fmaf(x[m], x[m], ss);
+      }
+      if (l2) {
+        ss = warp_sum(ss);
+        const float rn = 1.0f / sqrtf(ss + kL2Eps);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) x[m] *= rn;
+      }
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        Kn[r * KLD + lane + 32 * m] = x[m];
+        Kt[(lane + 32 * m) * TLD + r] = x[m];
+      }
+    }
+    load_gates(a, t0, L, h, G, bt);
+    const float* dUg = ws.dUp + ch * C * V;
+    for (int e = tid; e < C * (VT / 4); e += kRevThreads) {
+      const int i = e / (VT / 4), q = e - i * (VT / 4);
+      const int cc = c0 + 4 * q;
+      st4(X1 + i * VT + 4 * q, cc < V ? ld4(dUg + (size_t)i * V + cc) : make_float4(0.f, 0.f, 0.f, 0.f));
+    }
+    float z[4][4];   // Z rows 4 ty + r, columns col ..
+    {
+      const float* Zg = ws.Z + ch * K * V;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int d = 4 * ty + r;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (colok && d < K) x = ld4(Zg + (size_t)d * V + col);
+        z[r][0] = x.x; z[r][1] = x.y; z[r][2] = x.z; z[r][3] = x.w;
       }
     }
     __syncthreads();
-    {  // dX = T^T dU'  (T lower triangular: rows j >= i)
-      float x[8][1];
+    const float gL = G[L - 1];
+    {  // Y = K dS for rows 2 ty, 2 ty + 1; dU' = dUp + lambda Y
+      float y[2][4];
+      zero(y);
+#pragma unroll 4
+      for (int d = 0; d < K; ++d) {
+        const float2 xa = *reinterpret_cast<const float2*>(Kt + d * TLD + 2 * ty);
+        const float4 xb = ld4(dSs + d * VT + 4 * tx);
+        const float bb[4] = {xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          y[0][q] = fmaf(xa.x, bb[q], y[0][q]);
+          y[1][q] = fmaf(xa.y, bb[q], y[1][q]);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int i = 2 * ty + r;
+        const float lam = expf(gL - G[i]);
+        float4 u = ld4(X1 + i * VT + 4 * tx);
+        u.x = fmaf(lam, y[r][0], u.x);
+        u.y = fmaf(lam, y[r][1], u.y);
+        u.z = fmaf(lam, y[r][2], u.z);
+        u.w = fmaf(lam, y[r][3], u.w);
+        st4(X1 + i * VT + 4 * tx, u);
+      }
+    }
+    __syncthreads();
+    {  // dX = T^T dU' for rows 2 ty, 2 ty + 1 (T[j][i] = 0 for j < i)
+      float x[2][4];
       zero(x);
-      fma_tile<8, 1, 1, LDC, LDT, 0>(x, Tm + i0, dU + lane, i0, C);
+      const float* Tg = ws.T + ch * C * C;
+      for (int j = 2 * ty; j < C; ++j) {
+        const float2 ta = __ldg(reinterpret_cast<const float2*>(Tg + j * C + 2 * ty));
+        const float4 xb = ld4(X1 + j * VT + 4 * tx);
+        const float bb[4] = {xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          x[0][q] = fmaf(ta.x, bb[q], x[0][q]);
+          x[1][q] = fmaf(ta.y, bb[q], x[1][q]);
+        }
+      }
       float* dXg = ws.dX + ch * C * V;
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const int i = i0 + r;
-        if (c0 + lane < V) dXg[(size_t)i * V + c0 + lane] = x[r][0];
-        dX[i * LDT + lane] = -gb[i] * x[r][0];
+      for (int r = 0; r < 2; ++r) {
+        const int i = 2 * ty + r;
+        if (colok) st4(dXg + (size_t)i * V + col, make_float4(x[r][0], x[r][1], x[r][2], x[r][3]));
+        const float w = -expf(G[i]) * bt[i];
+        st4(X2 + i * VT + 4 * tx, make_float4(w * x[r][0], w * x[r][1], w * x[r][2], w * x[r][3]));
       }
     }
     __syncthreads();
-    {  // dS <- gamma_L dS + Q^T (scale diag(gamma) dO) - K^T (diag(gamma beta) dX)
-      float s[16][1];
-      const float gL = gm[L - 1];
+    {  // dS <- gamma_L dS + Z - K^T diag(gamma beta) dX
+      const float dl = expf(gL);
 #pragma unroll
-      for (int r = 0; r < 16; ++r) s[r][0] = gL * dS[(d0 + r) * VT + lane];
-      fma_tile<16, 1, 1, LD, LDT, 0>(s, Qn + d0, dO + lane, 0, L);
-      fma_tile<16, 1, 1, LD, LDT, 0>(s, Kn + d0, dX + lane, 0, L);
+      for (int r = 0; r < 4; ++r)
 #pragma unroll
-      for (int r = 0; r < 16; ++r) dS[(d0 + r) * VT + lane] = s[r][0];
+        for (int q = 0; q < 4; ++q) s[r][q] = fmaf(dl, s[r][q], z[r][q]);
+#pragma unroll 4
+      for (int i = 0; i < L; ++i) {
+        const float4 xa = ld4(Kn + i * KLD + 4 * ty);
+        const float4 xb = ld4(X2 + i * VT + 4 * tx);
+        const float aa[4] = {xa.x, xa.y, xa.z, xa.w}, bb[4] = {xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) s[r][q] = fmaf(aa[r], bb[q], s[r][q]);
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+        st4(dSs + (4 * ty + r) * VT + 4 * tx, make_float4(s[r][0], s[r][1], s[r][2], s[r][3]));
     }
   }
-  __syncthreads();
-  if (b.d_initial) {
-    for (int e = threadIdx.x; e < KP * VT; e += kRevThreads) {
-      const int d = e / VT, cc = e - d * VT;
-      if (d < K && c0 + cc < V) b.d_initial[st_off + (size_t)d * V + c0 + cc] = dS[e];
-    }
+  if (b.d_initial && colok) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+      if (4 * ty + r < K)
+        st4(b.d_initial + st_off + (size_t)(4 * ty + r) * V + col,
+            make_float4(s[r][0], s[r][1], s[r][2], s[r][3]));
   }
 }
 
@@ -699,7 +838,9 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
   if (!tc && (err = launch_chunk_states(a, ws.chunk_off, ws.W, ws.U, ws.G, ws.S))) return err;
   const unsigned vtiles = (unsigned)((a.V + VT - 1) / VT);
   if (a.num_seqs > 0) {
-    bwd_reverse_kernel<<<dim3(a.num_seqs, a.Hv, vtiles), kRevThreads, kRevSmem, a.stream>>>(a, b, ws);
+    const long long blocks = (long long)vtiles * a.Hv * a.num_seqs;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    bwd_reverse_kernel<<<(unsigned)blocks, kRevThreads, kRevSmem, a.stream>>>(a, b, ws);
     if ((err = cudaGetLastError())) return err;
   }
   if (NC > 0) {

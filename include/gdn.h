@@ -344,7 +344,7 @@ gdn_status_t gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, 
  * gradient is written as zero.
  *   workspace, workspace_bytes  device scratch of at least
  *                gdn_chunk_bwd_workspace_size(...) bytes, 16-byte aligned, owned
- *                by the caller (about 4 (2 K V + 3 C V + C K + C C + C) bytes per
+ *                by the caller (about 4 (3 K V + 3 C V + C K + C C + C) bytes per
  *                chunk of C = 64 tokens and value head, plus 8 Hv K bytes per token).
  * Errors as gdn_chunk_fwd: host-side checks return a status before any launch.
  */

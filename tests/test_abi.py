@@ -164,10 +164,10 @@ def bwd_call(**kw):
 def test_backward_entry_point_rejects_bad_arguments():
     lib = _lib.load()
     need = lib.gdn_chunk_bwd_workspace_size(1, 64, 1, 1, 64, 64, 1, 0, 0)
-    # per chunk and value head: W, U, dUp, dX (C x 64), S, dS (64 x 64), T (C x C), G (C);
+    # per chunk and value head: W, U, dUp, dX (C x 64), S, dS, Z (64 x 64), T (C x C), G (C);
     # per token: dQ, dK of every value head; each piece rounded up to 256 bytes
-    per_chunk = 4 * (4 * 64 * 64 + 2 * 64 * 64 + 64 * 64 + 64)
-    assert per_chunk * 2 + 64 * 2 * 64 * 4 <= need <= per_chunk * 2 + 64 * 2 * 64 * 4 + 12 * 256
+    per_chunk = 4 * (4 * 64 * 64 + 3 * 64 * 64 + 64 * 64 + 64)
+    assert per_chunk * 2 + 64 * 2 * 64 * 4 <= need <= per_chunk * 2 + 64 * 2 * 64 * 4 + 13 * 256
     assert lib.gdn_chunk_bwd_workspace_size(1, 64, 2, 3, 64, 64, 1, 0, 0) == (1 << 64) - 1
     assert bwd_call(chunk=32) == _lib.GDN_ERR_UNSUPPORTED
     assert bwd_call(do=None) == _lib.GDN_ERR_NULL
