@@ -305,6 +305,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override B of the chunked workload (profiling runs on a smaller case)")
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="override T of the chunked workload (profiling runs on a smaller case)")
     ap.add_argument("--no-product", action="store_true",
                     help="skip the Gated Delta Product measurement reported beside the headline")
     ap.add_argument("--only", choices=["chunk", "decode", "backward"], default=None,
@@ -333,6 +335,8 @@ def main():
 
     # Inputs: each rank its own independent batch (weak scaling, no collective).
     over = {} if args.batch is None else {"B": args.batch}
+    if args.seq_len is not None:
+        over["T"] = args.seq_len
     cin = synthetic.workload(CHUNK_WL, seed=1005 + 1000 * rank, **over)
     din = synthetic.workload(DECODE_WL, seed=1004 + 1000 * rank)
     B, T = cin.q.shape[:2]

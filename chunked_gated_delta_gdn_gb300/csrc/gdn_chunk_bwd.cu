@@ -27,15 +27,13 @@
 // the L2 norm's Jacobian then maps dQ, dK (summed over the value heads of a query/key
 // head, in a fixed order) to dq, dk.
 //
-// Six launches on the caller's stream, no host sync and no atomics (the result is
+// Launches on the caller's stream, no host sync and no atomics (the result is
 // bitwise reproducible run to run):
 //   1. chunk table  from cu_seqlens, on the device
 //   2. states       the forward recompute of the entry state S0 of every chunk and of U':
 //                   bf16 with K = V = 128, the tensor-core forward kernel in record mode;
-//                   otherwise (after 3) the fp32 state pass per (sequence, value head,
-//                   32 columns) on W, U from the prep kernel
-//   3. prep         per (chunk, value head): T, dUp = scale P^T dO, G, and for the fp32
-//                   state pass W = T diag(beta gamma) K, U = T diag(beta) V
+//                   otherwise the prep and state passes of the fp32 chunk path
+//   3. prep         per (chunk, value head): T, dUp = scale P^T dO, Z = scale Q^T diag(gamma) dO
 //   4. reverse      per (sequence, value head, 32 columns), chunks last to first:
 //                   records dS (the gradient of each chunk's exit state) and dX
 //   5. grad         per (chunk, value head): dv, dbeta, dg, and dQ, dK per value head
@@ -51,7 +49,6 @@ constexpr int KP = GDN_MAX_HEAD_DIM;  // tiles are padded to the largest head di
 constexpr int LD = KP + 1;            // row stride of [C][KP] tiles (odd: column reads hit distinct banks)
 constexpr int LDC = C + 1;            // row stride of [C][C] tiles
 constexpr int VT = 32;                // V columns per V tile
-constexpr int LDT = VT + 1;           // row stride of [C][VT] tiles
 
 struct BwdWs {
   int32_t* chunk_off;  // [N + 2]
@@ -164,27 +161,28 @@ __device__ __forceinline__ void store_rows(float* dst, int D, const float (&acc)
 }
 
 // ---------------------------------------------------------------- 3. prep
-// Per (chunk, value head), 16 warps: A and P, T = (I + A)^{-1}, dUp = scale P^T dO and
-// Z = scale Q^T diag(gamma) dO (the part of the state-gradient step that does not depend on
-// the state gradient, taken out of the serial reverse pass), and for the fp32 state pass
-// W = T diag(beta gamma) K, U = T diag(beta) V.
+// Per (chunk, value head), 16 warps, two CTAs per SM: A and P, T = (I + A)^{-1} (in place of
+// A), dUp = scale P^T dO and Z = scale Q^T diag(gamma) dO -- the part of the state-gradient
+// step that does not depend on the state gradient, taken out of the serial reverse pass.
+// dO is taken in two halves of 64 columns.
 constexpr int kPrepThreads = 512;
-constexpr int DLD = KP + 4;  // row stride of [C][KP] tiles read as float4 (16-byte aligned rows)
-constexpr size_t kPrepSmem = sizeof(float) * (2 * C * LD + C * DLD + 3 * C * LDC + 3 * C);
+constexpr int HW = KP / 2;        // dO columns per half
+constexpr int HLD = HW + 4;       // row stride of the dO half (float4 reads)
+constexpr size_t kPrepSmem = sizeof(float) * (2 * C * LD + C * HLD + C * LDC + 3 * C);
+constexpr int kBarT = 1;          // named barrier of the two warps that build T
 
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 
-__global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const ChunkArgs a, const BwdArgs b,
-                                                                BwdWs ws, int need_wu) {
+__global__ void __launch_bounds__(kPrepThreads, 2) bwd_prep_kernel(const ChunkArgs a,
+                                                                   const BwdArgs b, BwdWs ws) {
   extern __shared__ float smem[];
-  float* Kn = smem;           // [C][LD] normalised k (then diag(beta gamma) k)
+  float* Kn = smem;           // [C][LD] normalised k
+  float* P = smem;            // [C][LDC] P, over Kn once A and P are formed
   float* Qn = Kn + C * LD;    // [C][LD] normalised q
-  float* dO = Qn + C * LD;    // [C][DLD] dO (then diag(beta) v)
-  float* A = dO + C * DLD;    // [C][LDC]
-  float* P = A + C * LDC;     // [C][LDC]
-  float* Tm = P + C * LDC;    // [C][LDC]
-  float* G = Tm + C * LDC;    // [C]
+  float* Dh = Qn + C * LD;    // [C][HLD] one half of dO's columns
+  float* At = Dh + C * HLD;   // [C][LDC] A, then T in place
+  float* G = At + C * LDC;    // [C]
   float* bt = G + C;          // [C]
   float* gm = bt + C;         // [C] gamma
   const int c = blockIdx.x, h = blockIdx.y;
@@ -197,62 +195,43 @@ __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const ChunkArgs 
   load_rows(a.q, a.io_dtype, t0, L, a.Hqk, hq, K, l2, Qn, LD);
   zero_cols(Kn, K);
   zero_cols(Qn, K);
-  load_tile(b.d_o, a.io_dtype, t0, L, a.Hv, h, V, 0, KP, nullptr, dO, DLD, 0, kPrepThreads / 32);
+  load_tile(b.d_o, a.io_dtype, t0, L, a.Hv, h, V, 0, HW, nullptr, Dh, HLD, 0, kPrepThreads / 32);
   load_gates(a, t0, L, h, G, bt);
   __syncthreads();
   if (tid < C) gm[tid] = expf(G[tid]);
-  {  // A = strict_lower(diag(beta) K K^T * Gamma), P = (Q K^T * Gamma) on and below the diagonal
+  {  // A = strict_lower(diag(beta) K K^T * Gamma), P = (Q K^T * Gamma) on and below the
+     // diagonal; warps whose rows all lie below 32 skip the upper column half
     const int i0 = 4 * warp;
     float kk[4][2], qk[4][2];
     zero(kk);
     zero(qk);
-    fma_tile<4, 2, LD, 1, 1, 32 * LD>(kk, Kn + i0 * LD, Kn + lane * LD, 0, K);
-    fma_tile<4, 2, LD, 1, 1, 32 * LD>(qk, Qn + i0 * LD, Kn + lane * LD, 0, K);
+    if (i0 + 3 < 32) {
+      float k1[4][1], q1[4][1];
+      zero(k1);
+      zero(q1);
+      fma_tile<4, 1, LD, 1, 1, 0>(k1, Kn + i0 * LD, Kn + lane * LD, 0, K);
+      fma_tile<4, 1, LD, 1, 1, 0>(q1, Qn + i0 * LD, Kn + lane * LD, 0, K);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) { kk[r][0] = k1[r][0]; qk[r][0] = q1[r][0]; }
+    } else {
+      fma_tile<4, 2, LD, 1, 1, 32 * LD>(kk, Kn + i0 * LD, Kn + lane * LD, 0, K);
+      fma_tile<4, 2, LD, 1, 1, 32 * LD>(qk, Qn + i0 * LD, Kn + lane * LD, 0, K);
+    }
+    __syncthreads();  // every read of Kn is done: P may overwrite it
 #pragma unroll
     for (int r = 0; r < 4; ++r)
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
         const int i = i0 + r, j = lane + 32 * m;
         const float gij = j <= i ? expf(G[i] - G[j]) : 0.f;
-        A[i * LDC + j] = j < i ? bt[i] * kk[r][m] * gij : 0.f;
+        At[i * LDC + j] = j < i ? bt[i] * kk[r][m] * gij : 0.f;
         P[i * LDC + j] = qk[r][m] * gij;
       }
   }
   __syncthreads();
-  const size_t ch = (size_t)c * a.Hv + h;
-  const int ty = tid >> 4, tx = tid & 15;  // 32 row groups x 16 groups of 8 columns
-  {  // Z = scale Q^T diag(gamma) dO: rows d = ty + 32 r, columns 8 tx .. 8 tx + 7
-    float z[4][8];
-    zero(z);
-    for (int i = 0; i < L; ++i) {
-      const float g = gm[i];
-      float x[4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r) x[r] = g * Qn[i * LD + ty + 32 * r];
-      const float4 y0 = ld4(dO + i * DLD + 8 * tx), y1 = ld4(dO + i * DLD + 8 * tx + 4);
-      const float y[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int q = 0; q < 8; ++q) z[r][q] = fmaf(x[r], y[q], z[r][q]);
-    }
-    float* Zg = ws.Z + ch * K * V;
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int d = ty + 32 * r;
-      if (d >= K) continue;
-#pragma unroll
-      for (int hlf = 0; hlf < 2; ++hlf) {
-        const int col = 8 * tx + 4 * hlf;
-        if (col < V)
-          st4(Zg + (size_t)d * V + col,
-              make_float4(a.scale * z[r][4 * hlf], a.scale * z[r][4 * hlf + 1],
-                          a.scale * z[r][4 * hlf + 2], a.scale * z[r][4 * hlf + 3]));
-      }
-    }
-  }
   if (tid < C) {
-    // T = (I + A)^{-1}, one column per thread by forward substitution (four partial sums)
+    // T = (I + A)^{-1} in place, row by row, one column per thread: row i of T needs row i of
+    // A and rows < i of T (own column); after the row's reads a barrier, then the row is written
     const int j = tid;
     for (int i = 0; i < C; ++i) {
       float t = i == j ? 1.f : 0.f;
@@ -260,67 +239,82 @@ __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const ChunkArgs 
         float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
         int m = j;
         for (; m + 3 < i; m += 4) {
-          s0 = fmaf(A[i * LDC + m], Tm[m * LDC + j], s0);
-          s1 = fmaf(A[i * LDC + m + 1], Tm[(m + 1) * LDC + j], s1);
-          s2 = fmaf(A[i * LDC + m + 2], Tm[(m + 2) * LDC + j], s2);
-          s3 = fmaf(A[i * LDC + m + 3], Tm[(m + 3) * LDC + j], s3);
+          s0 = fmaf(At[i * LDC + m], At[m * LDC + j], s0);
+          s1 = fmaf(At[i * LDC + m + 1], At[(m + 1) * LDC + j], s1);
+          s2 = fmaf(At[i * LDC + m + 2], At[(m + 2) * LDC + j], s2);
+          s3 = fmaf(At[i * LDC + m + 3], At[(m + 3) * LDC + j], s3);
         }
-        for (; m < i; ++m) s0 = fmaf(A[i * LDC + m], Tm[m * LDC + j], s0);
+        for (; m < i; ++m) s0 = fmaf(At[i * LDC + m], At[m * LDC + j], s0);
         t = -((s0 + s1) + (s2 + s3));
       }
-      Tm[i * LDC + j] = t;
+      asm volatile("bar.sync %0, %1;" ::"n"(kBarT), "n"(C) : "memory");
+      At[i * LDC + j] = t;
     }
   }
-  __syncthreads();
-  {  // dUp = scale P^T dO: rows i = ty, ty + 32, columns 8 tx .. 8 tx + 7 (P[m][i] = 0 for m < i)
-    float u[2][8];
-    zero(u);
-    for (int m = ty; m < C; ++m) {
-      const float x0 = P[m * LDC + ty], x1 = P[m * LDC + ty + 32];
-      const float4 y0 = ld4(dO + m * DLD + 8 * tx), y1 = ld4(dO + m * DLD + 8 * tx + 4);
-      const float y[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+  const size_t ch = (size_t)c * a.Hv + h;
+  const int ty = tid >> 4, tx = tid & 15;   // Z: 32 row groups x 16 groups of 4 columns
+  for (int half = 0; half < 2; ++half) {
+    if (half == 1) {
+      __syncthreads();   // every read of the first half is done
+      load_tile(b.d_o, a.io_dtype, t0, L, a.Hv, h, V, HW, HW, nullptr, Dh, HLD, 0,
+                kPrepThreads / 32);
+      __syncthreads();
+    }
+    const int cbase = half * HW;
+    {  // Z = scale Q^T diag(gamma) dO: rows d = ty + 32 r, columns cbase + 4 tx .. + 3
+      float z[4][4];
+      zero(z);
+      for (int i = 0; i < L; ++i) {
+        const float g = gm[i];
+        const float4 y4 = ld4(Dh + i * HLD + 4 * tx);
+        const float y[4] = {y4.x, y4.y, y4.z, y4.w};
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        u[0][q] = fmaf(x0, y[q], u[0][q]);
-        u[1][q] = fmaf(x1, y[q], u[1][q]);
+        for (int r = 0; r < 4; ++r) {
+          const float x = g * Qn[i * LD + ty + 32 * r];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) z[r][q] = fmaf(x, y[q], z[r][q]);
+        }
+      }
+      const int col = cbase + 4 * tx;
+      float* Zg = ws.Z + ch * K * V;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int d = ty + 32 * r;
+        if (d < K && col < V)
+          st4(Zg + (size_t)d * V + col, make_float4(a.scale * z[r][0], a.scale * z[r][1],
+                                                    a.scale * z[r][2], a.scale * z[r][3]));
       }
     }
-    float* Ug = ws.dUp + ch * C * V;
+    if (half == 0) __syncthreads();   // T (and P) complete before dUp's first use of P
+    {  // dUp = scale P^T dO: rows i = ty, ty + 32, columns cbase + 4 tx .. + 3 (P[m][i] = 0, m < i)
+      float u[2][4];
+      zero(u);
+      for (int m = ty; m < C; ++m) {
+        const float x0 = P[m * LDC + ty], x1 = P[m * LDC + ty + 32];
+        const float4 y4 = ld4(Dh + m * HLD + 4 * tx);
+        const float y[4] = {y4.x, y4.y, y4.z, y4.w};
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int i = ty + 32 * r;
+        for (int q = 0; q < 4; ++q) {
+          u[0][q] = fmaf(x0, y[q], u[0][q]);
+          u[1][q] = fmaf(x1, y[q], u[1][q]);
+        }
+      }
+      const int col = cbase + 4 * tx;
+      float* Ug = ws.dUp + ch * C * V;
+      if (col < V) {
 #pragma unroll
-      for (int hlf = 0; hlf < 2; ++hlf) {
-        const int col = 8 * tx + 4 * hlf;
-        if (col < V)
-          st4(Ug + (size_t)i * V + col,
-              make_float4(a.scale * u[r][4 * hlf], a.scale * u[r][4 * hlf + 1],
-                          a.scale * u[r][4 * hlf + 2], a.scale * u[r][4 * hlf + 3]));
+        for (int r = 0; r < 2; ++r)
+          st4(Ug + (size_t)(ty + 32 * r) * V + col,
+              make_float4(a.scale * u[r][0], a.scale * u[r][1], a.scale * u[r][2], a.scale * u[r][3]));
       }
     }
+    if (cbase + HW >= V) break;   // V <= 64: one half holds every column
   }
   for (int e = tid; e < C * C; e += kPrepThreads) {
     const int i = e / C, j = e - i * C;
-    ws.T[ch * C * C + e] = Tm[i * LDC + j];
+    ws.T[ch * C * C + e] = At[i * LDC + j];
   }
   if (tid < C) ws.G[ch * C + tid] = G[tid];
-  if (need_wu) {  // the inputs of the fp32 forward state pass
-    __syncthreads();
-    for (int e = tid; e < C * KP; e += kPrepThreads) {
-      const int r = e / KP, d = e - r * KP;
-      Kn[r * LD + d] *= bt[r] * gm[r];
-    }
-    load_tile(a.v, a.io_dtype, t0, L, a.Hv, h, V, 0, KP, bt, dO, DLD, 0, kPrepThreads / 32);
-    __syncthreads();
-    const int i0 = 4 * warp;
-    float acc[4][4];
-    zero(acc);  // W = T diag(beta gamma) K  (T lower triangular: columns m <= i)
-    fma_tile<4, 4, LDC, 1, LD, 32>(acc, Tm + i0 * LDC, Kn + lane, 0, i0 + 4);
-    store_rows(ws.W + ch * C * K, K, acc, i0, lane, 1.f);
-    zero(acc);  // U = T diag(beta) V
-    fma_tile<4, 4, LDC, 1, DLD, 32>(acc, Tm + i0 * LDC, dO + lane, 0, i0 + 4);
-    store_rows(ws.U + ch * C * V, V, acc, i0, lane, 1.f);
-  }
 }
 
 // ---------------------------------------------------------------- 4. reverse
@@ -511,230 +505,394 @@ __global__ void __launch_bounds__(kRevThreads, 2) bwd_reverse_kernel(const Chunk
 }
 
 // ---------------------------------------------------------------- 5. grad
+// Per (chunk, value head), 16 warps.  Every product runs on 4 x 4 (or 4 x 2) register blocks
+// with lanes arranged 4 x 8 inside the warp and both operands read as float4 (float2) rows
+// of shared-memory tiles stored with the reduction index outermost, so that each k step costs
+// one broadcast-like and one contiguous wavefront per operand.
+//   [C][KP] outputs (H layout): warp w -> rows 16 (w / 4) + 4 ly, columns 32 (w % 4) + 4 lx
+//   [C][C]  outputs (S layout): warp w -> rows 16 (w / 4) + 4 ly, columns 16 (w % 4) + 2 lx
+// with ly = lane / 8, lx = lane % 8.  Shared memory: region R1 holds the V tiles of phase A
+// (S0, dS transposed, and dO, dX, U' transposed), then q, k transposed (phase B), then
+// F, F^T, E, E^T (phase C); region R2 holds the normalised q, k rows for the whole CTA.
+// Phase A: H1 = dO S0^T, H2 = dX S0^T, H3 = U' dS^T, dO U'^T, dX U'^T (reduce over V);
+// phase B: Q K^T, K K^T, then F, E and the row / column sums of Z (reduce over K);
+// phase C: dQ += F K, dK += F^T Q + (E + E^T) K (reduce over the chunk's tokens).
 constexpr int kGradThreads = 512;
 constexpr int kGradWarps = kGradThreads / 32;
-constexpr size_t kGradSmem = sizeof(float) * (2 * VT * LD + 4 * C * LDT + 2 * C * LD +
-                                              2 * C * LDC + kGradWarps * C + 9 * C + kGradWarps);
+constexpr int RLD = C + 4;  // row stride of tiles indexed by token (float4 along tokens)
+constexpr int kR1A = 2 * VT * KLD + 3 * VT * RLD;
+constexpr int kR1B = 2 * KP * RLD;
+constexpr int kR1C = 4 * C * RLD;
+constexpr int kR1 = kR1A > kR1B ? (kR1A > kR1C ? kR1A : kR1C) : (kR1B > kR1C ? kR1B : kR1C);
+constexpr int kR2 = 2 * C * KLD;
+constexpr int kGradVec = 16 * C + kGradWarps;   // G, beta, gamma, lambda; 3 x [4][C]; red
+constexpr size_t kGradSmem = sizeof(float) * (kR1 + kR2 + kGradVec);
+
+__device__ __forceinline__ float2 ld2(const float* p) { return *reinterpret_cast<const float2*>(p); }
 
 __global__ void __launch_bounds__(kGradThreads) bwd_grad_kernel(const ChunkArgs a, const BwdArgs b,
                                                                 BwdWs ws) {
   extern __shared__ float smem[];
-  float* S0T = smem;            // [VT][LD]  S0 tile, transposed
-  float* dST = S0T + VT * LD;   // [VT][LD]  dS tile, transposed
-  float* dOs = dST + VT * LD;   // [C][LDT]
-  float* dXs = dOs + C * LDT;   // [C][LDT]
-  float* Us = dXs + C * LDT;    // [C][LDT]
-  float* Vs = Us + C * LDT;     // [C][LDT]
-  float* Qn = Vs + C * LDT;     // [C][LD]
-  float* Kn = Qn + C * LD;      // [C][LD]
-  float* Fs = Kn + C * LD;      // [C][LDC]
-  float* Es = Fs + C * LDC;     // [C][LDC]
-  float* colp = Es + C * LDC;   // [warps][C]  per-warp column sums of Z
-  float* G = colp + kGradWarps * C;
-  float* bt = G + C;
-  float* gm = bt + C;           // gamma
-  float* lm = gm + C;           // lambda
-  float* dGr = lm + C;          // dG without the column sums
-  float* om = dGr + C;          // omega_i = lambda_i k_i . dS u'_i
-  float* dbr = om + C;          // dbeta
-  float* cs = dbr + C;          // column sums of Z
-  float* xg = cs + C;           // dG, then dg
-  float* red = xg + C;          // [warps] partial <S0, dS>
+  float* R1 = smem;
+  float* Qn = R1 + kR1;          // [C][KLD] normalised q rows
+  float* Kn = Qn + C * KLD;      // [C][KLD] normalised k rows
+  float* G = Kn + C * KLD;       // [C]
+  float* bt = G + C;             // [C]
+  float* gm = bt + C;            // [C] gamma
+  float* lm = gm + C;            // [C] lambda
+  float* rowp = lm + C;          // [4][C] row partial sums of Z (per column group of warps)
+  float* colp = rowp + 4 * C;    // [4][C] column partial sums of Z (per row group of warps)
+  float* dbp = colp + 4 * C;     // [4][C] partial sum_j dA_ij (K K^T * Gamma)_ij
+  float* red = dbp + 4 * C;      // [warps] partial <S0, dS>
+  // phase A views of R1
+  float* S0T = R1;               // [VT][KLD]
+  float* dST = S0T + VT * KLD;   // [VT][KLD]
+  float* dOT = dST + VT * KLD;   // [VT][RLD]
+  float* dXT = dOT + VT * RLD;   // [VT][RLD]
+  float* UT = dXT + VT * RLD;    // [VT][RLD]
+  // phase B / C views
+  float* QT = R1;                // [KP][RLD]
+  float* KT = QT + KP * RLD;     // [KP][RLD]
+  float* Fs = R1;                // [C][RLD] F[i][j]
+  float* FT = Fs + C * RLD;      // [C][RLD] F[j][i]
+  float* Es = FT + C * RLD;      // [C][RLD] E[i][j]
+  float* ET = Es + C * RLD;      // [C][RLD] E[j][i]
+
   const int c = blockIdx.x, h = blockIdx.y;
   int n, t0, L;
   if (!locate_chunk(a, ws.chunk_off, c, &n, &t0, &L)) return;
   const int K = a.K, V = a.V, hq = h / (a.Hv / a.Hqk);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ly = lane >> 3, lx = lane & 7;
+  const int rS = 16 * (warp >> 2) + 4 * ly;     // first row of this thread (both layouts)
+  const int cH = 32 * (warp & 3) + 4 * lx;      // first column, H layout
+  const int cS = 16 * (warp & 3) + 2 * lx;      // first column, S layout
   const bool l2 = a.use_qk_l2norm != 0;
   const size_t ch = (size_t)c * a.Hv + h;
-  const int i0 = 4 * warp;  // 16 warps x 4 rows
+
+  // normalised q, k rows (warp w: rows 4 w .. 4 w + 3)
   load_gates(a, t0, L, h, G, bt);
+#pragma unroll
+  for (int which = 0; which < 2; ++which) {
+    const void* src = which ? a.k : a.q;
+    float* dst = which ? Kn : Qn;
+    for (int r = 4 * warp; r < 4 * warp + 4; ++r) {
+      float x[4], ss = 0.f;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int d = lane + 32 * m;
+        x[m] = (r < L && d < K) ? load_elem(src, ((size_t)(t0 + r) * a.Hqk + hq) * K + d, a.io_dtype) : 0.f;
+        ss = fmaf(x[m], x[m], ss);
+      }
+      float rn = 1.f;
+      if (l2) rn = 1.0f / sqrtf(warp_sum(ss) + kL2Eps);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) dst[r * KLD + lane + 32 * m] = x[m] * rn;
+    }
+  }
+  __syncthreads();
+  if (tid < C) {
+    gm[tid] = expf(G[tid]);
+    lm[tid] = expf(G[L - 1] - G[tid]);
+  }
+
+  // ---- phase A: products reducing over V, 32 columns at a time
   float H1[4][4], H2[4][4], H3[4][4], OU[4][2], XU[4][2];
   zero(H1);
   zero(H2);
   zero(H3);
   zero(OU);
   zero(XU);
-  float xv[4] = {0.f, 0.f, 0.f, 0.f}, sd = 0.f;
-  // Phase A: the products that reduce over V, one 32-column tile at a time
+  float sd = 0.f, xv = 0.f;
+  const float* Sg = ws.S + ch * K * V;
+  const float* dSg = ws.dS + ch * K * V;
+  const float* Ug = ws.U + ch * C * V;
+  const float* dXg = ws.dX + ch * C * V;
   for (int c0 = 0; c0 < V; c0 += VT) {
     __syncthreads();
-    const float* Sg = ws.S + ch * K * V;
-    const float* dSg = ws.dS + ch * K * V;
-    for (int e = threadIdx.x; e < KP * VT; e += kGradThreads) {
-      const int d = e / VT, cc = e - d * VT;
-      float s0 = 0.f, ds = 0.f;
-      if (d < K && c0 + cc < V) {
-        s0 = Sg[(size_t)d * V + c0 + cc];
-        ds = dSg[(size_t)d * V + c0 + cc];
+    {  // S0, dS tiles transposed: thread -> row d = tid % 128, columns 8 (tid / 128) + 0..7
+      const int d = tid & 127, cg = tid >> 7;
+#pragma unroll
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        const int cc = 8 * cg + 4 * hlf;
+        float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), ds = s0;
+        if (d < K && c0 + cc < V) {
+          s0 = ld4(Sg + (size_t)d * V + c0 + cc);
+          ds = ld4(dSg + (size_t)d * V + c0 + cc);
+        }
+        S0T[(cc + 0) * KLD + d] = s0.x; S0T[(cc + 1) * KLD + d] = s0.y;
+        S0T[(cc + 2) * KLD + d] = s0.z; S0T[(cc + 3) * KLD + d] = s0.w;
+        dST[(cc + 0) * KLD + d] = ds.x; dST[(cc + 1) * KLD + d] = ds.y;
+        dST[(cc + 2) * KLD + d] = ds.z; dST[(cc + 3) * KLD + d] = ds.w;
+        sd = fmaf(s0.x, ds.x, fmaf(s0.y, ds.y, fmaf(s0.z, ds.z, fmaf(s0.w, ds.w, sd))));
       }
-      S0T[cc * LD + d] = s0;
-      dST[cc * LD + d] = ds;
-      sd = fmaf(s0, ds, sd);
     }
-    const float* Ug = ws.U + ch * C * V;
-    const float* dXg = ws.dX + ch * C * V;
-    for (int e = threadIdx.x; e < C * VT; e += kGradThreads) {
-      const int i = e / VT, cc = e - i * VT;
+    {  // dO, dX, U', v tiles transposed: thread -> token i = tid % 64, columns 4 (tid / 64) + 0..3
+      const int i = tid & 63, cg = tid >> 6;
+      const int cc = 4 * cg;
       const bool ok = i < L && c0 + cc < V;
       const size_t tv = ((size_t)(t0 + i) * a.Hv + h) * V + c0 + cc;
-      const float dx = ok ? dXg[(size_t)i * V + c0 + cc] : 0.f;
-      dOs[i * LDT + cc] = ok ? load_elem(b.d_o, tv, a.io_dtype) : 0.f;
-      dXs[i * LDT + cc] = dx;
-      Us[i * LDT + cc] = ok ? Ug[(size_t)i * V + c0 + cc] : 0.f;
-      Vs[i * LDT + cc] = ok ? load_elem(a.v, tv, a.io_dtype) : 0.f;
-      if (ok) store_elem(b.dv, tv, bt[i] * dx, a.io_dtype);
+      float o4[4] = {0.f, 0.f, 0.f, 0.f}, v4[4] = {0.f, 0.f, 0.f, 0.f};
+      float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f), u4 = x4;
+      if (ok) {
+        x4 = ld4(dXg + (size_t)i * V + c0 + cc);
+        u4 = ld4(Ug + (size_t)i * V + c0 + cc);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          o4[q] = load_elem(b.d_o, tv + q, a.io_dtype);
+          v4[q] = load_elem(a.v, tv + q, a.io_dtype);
+        }
+        const float bi = bt[i];
+        store_elem(b.dv, tv + 0, bi * x4.x, a.io_dtype);
+        store_elem(b.dv, tv + 1, bi * x4.y, a.io_dtype);
+        store_elem(b.dv, tv + 2, bi * x4.z, a.io_dtype);
+        store_elem(b.dv, tv + 3, bi * x4.w, a.io_dtype);
+      }
+      const float x[4] = {x4.x, x4.y, x4.z, x4.w}, u[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        dOT[(cc + q) * RLD + i] = o4[q];
+        dXT[(cc + q) * RLD + i] = x[q];
+        UT[(cc + q) * RLD + i] = u[q];
+        xv = fmaf(x[q], v4[q], xv);
+      }
     }
     __syncthreads();
-    fma_tile<4, 4, LDT, 1, LD, 32>(H1, dOs + i0 * LDT, S0T + lane, 0, VT);
-    fma_tile<4, 4, LDT, 1, LD, 32>(H2, dXs + i0 * LDT, S0T + lane, 0, VT);
-    fma_tile<4, 4, LDT, 1, LD, 32>(H3, Us + i0 * LDT, dST + lane, 0, VT);
-    fma_tile<4, 2, LDT, 1, 1, 32 * LDT>(OU, dOs + i0 * LDT, Us + lane * LDT, 0, VT);
-    fma_tile<4, 2, LDT, 1, 1, 32 * LDT>(XU, dXs + i0 * LDT, Us + lane * LDT, 0, VT);
+#pragma unroll 2
+    for (int k = 0; k < VT; ++k) {
+      const float4 ao = ld4(dOT + k * RLD + rS), ax = ld4(dXT + k * RLD + rS);
+      const float4 au = ld4(UT + k * RLD + rS);
+      const float4 bs = ld4(S0T + k * KLD + cH), bd = ld4(dST + k * KLD + cH);
+      const float2 bu = ld2(UT + k * RLD + cS);
+      const float AO[4] = {ao.x, ao.y, ao.z, ao.w}, AX[4] = {ax.x, ax.y, ax.z, ax.w};
+      const float AU[4] = {au.x, au.y, au.z, au.w};
+      const float BS[4] = {bs.x, bs.y, bs.z, bs.w}, BD[4] = {bd.x, bd.y, bd.z, bd.w};
+      const float BU[2] = {bu.x, bu.y};
 #pragma unroll
-    for (int r = 0; r < 4; ++r) xv[r] = fmaf(dXs[(i0 + r) * LDT + lane], Vs[(i0 + r) * LDT + lane], xv[r]);
-  }
-  // Phase B: Q K^T, K K^T and the [C][C] adjoints F, E
-  load_rows(a.q, a.io_dtype, t0, L, a.Hqk, hq, K, l2, Qn, LD);
-  load_rows(a.k, a.io_dtype, t0, L, a.Hqk, hq, K, l2, Kn, LD);
-  zero_cols(Qn, K);
-  zero_cols(Kn, K);
-  sd = warp_sum(sd);
-  if (lane == 0) red[warp] = sd;
-  if (threadIdx.x < C) {
-    gm[threadIdx.x] = expf(G[threadIdx.x]);
-    lm[threadIdx.x] = expf(G[L - 1] - G[threadIdx.x]);
-  }
-  __syncthreads();
-  float rz[4], dba[4];
-  {
-    float QK[4][2], KK[4][2];
-    zero(QK);
-    zero(KK);
-    fma_tile<4, 2, LD, 1, 1, 32 * LD>(QK, Qn + i0 * LD, Kn + lane * LD, 0, K);
-    fma_tile<4, 2, LD, 1, 1, 32 * LD>(KK, Kn + i0 * LD, Kn + lane * LD, 0, K);
-    float cz[2] = {0.f, 0.f};
+      for (int r = 0; r < 4; ++r) {
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int i = i0 + r;
-      rz[r] = 0.f;
-      dba[r] = 0.f;
+        for (int q = 0; q < 4; ++q) {
+          H1[r][q] = fmaf(AO[r], BS[q], H1[r][q]);
+          H2[r][q] = fmaf(AX[r], BS[q], H2[r][q]);
+          H3[r][q] = fmaf(AU[r], BD[q], H3[r][q]);
+        }
 #pragma unroll
-      for (int m = 0; m < 2; ++m) {
-        const int j = lane + 32 * m;
-        const float gij = j <= i ? expf(G[i] - G[j]) : 0.f;
-        const float f = a.scale * OU[r][m] * gij;
-        const float dA = j < i ? -XU[r][m] : 0.f;
-        const float e = bt[i] * gij * dA;
-        const float z = f * QK[r][m] + e * KK[r][m];
-        rz[r] += z;
-        cz[m] += z;
-        dba[r] = fmaf(dA * gij, KK[r][m], dba[r]);
-        Fs[i * LDC + j] = f;
-        Es[i * LDC + j] = e;
-      }
-    }
-    colp[warp * C + lane] = cz[0];
-    colp[warp * C + lane + 32] = cz[1];
-  }
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    rz[r] = warp_sum(rz[r]);
-    dba[r] = warp_sum(dba[r]);
-    xv[r] = warp_sum(xv[r]);
-  }
-  // row dots with the V-reduced products (q_i . S0 dO_i, k_i . S0 dX_i, k_i . dS u'_i)
-  float qh1[4], kh2[4], kh3[4];
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    float x1 = 0.f, x2 = 0.f, x3 = 0.f;
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const float qv = Qn[(i0 + r) * LD + lane + 32 * m], kv = Kn[(i0 + r) * LD + lane + 32 * m];
-      x1 = fmaf(qv, H1[r][m], x1);
-      x2 = fmaf(kv, H2[r][m], x2);
-      x3 = fmaf(kv, H3[r][m], x3);
-    }
-    qh1[r] = warp_sum(x1);
-    kh2[r] = warp_sum(x2);
-    kh3[r] = warp_sum(x3);
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int i = i0 + r;
-      const float omega = lm[i] * kh3[r];
-      om[i] = i < L ? omega : 0.f;
-      dGr[i] = a.scale * gm[i] * qh1[r] - bt[i] * gm[i] * kh2[r] - omega + rz[r];
-      dbr[i] = xv[r] - gm[i] * kh2[r] + dba[r];
-    }
-  }
-  __syncthreads();
-  // Phase C: dQ, dK per value head
-  {
-    float dQ[4][4], dK[4][4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int i = i0 + r;
-        dQ[r][m] = a.scale * gm[i] * H1[r][m];
-        dK[r][m] = lm[i] * H3[r][m] - gm[i] * bt[i] * H2[r][m];
-      }
-    fma_tile<4, 4, LDC, 1, LD, 32>(dQ, Fs + i0 * LDC, Kn + lane, 0, i0 + 4);  // F K       (j <= i)
-    fma_tile<4, 4, 1, LDC, LD, 32>(dK, Fs + i0, Qn + lane, i0, C);            // F^T Q     (j >= i)
-    fma_tile<4, 4, LDC, 1, LD, 32>(dK, Es + i0 * LDC, Kn + lane, 0, i0 + 4);  // E K       (j < i)
-    fma_tile<4, 4, 1, LDC, LD, 32>(dK, Es + i0, Kn + lane, i0, C);            // E^T K     (j > i)
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int i = i0 + r;
-      if (i >= L) continue;
-      float* dq = ws.dQ + ((size_t)(t0 + i) * a.Hv + h) * K;
-      float* dk = ws.dK + ((size_t)(t0 + i) * a.Hv + h) * K;
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int d = lane + 32 * m;
-        if (d < K) {
-          dq[d] = dQ[r][m];
-          dk[d] = dK[r][m];
+        for (int q = 0; q < 2; ++q) {
+          OU[r][q] = fmaf(AO[r], BU[q], OU[r][q]);
+          XU[r][q] = fmaf(AX[r], BU[q], XU[r][q]);
         }
       }
     }
   }
-  // dG: column sums in a fixed order, the exit-state terms on the last row, then the
-  // reverse in-chunk cumulative sum
-  if (threadIdx.x < C) {
-    float s = 0.f;
-    for (int w = 0; w < kGradWarps; ++w) s += colp[w * C + threadIdx.x];
-    cs[threadIdx.x] = s;
+  // row dots of the V-reduced products with the normalised rows: q_i . S0 dO_i,
+  // k_i . S0 dX_i, k_i . dS u'_i (H layout: partial over 4 columns, then over lx and the
+  // four warps sharing the rows)
+  float qh1[4], kh2[4], kh3[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const float4 qv = ld4(Qn + (rS + r) * KLD + cH), kv = ld4(Kn + (rS + r) * KLD + cH);
+    const float Q4[4] = {qv.x, qv.y, qv.z, qv.w}, K4[4] = {kv.x, kv.y, kv.z, kv.w};
+    float x1 = 0.f, x2 = 0.f, x3 = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      x1 = fmaf(Q4[q], H1[r][q], x1);
+      x2 = fmaf(K4[q], H2[r][q], x2);
+      x3 = fmaf(K4[q], H3[r][q], x3);
+    }
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      x1 += __shfl_xor_sync(0xffffffffu, x1, o);
+      x2 += __shfl_xor_sync(0xffffffffu, x2, o);
+      x3 += __shfl_xor_sync(0xffffffffu, x3, o);
+    }
+    qh1[r] = x1;
+    kh2[r] = x2;
+    kh3[r] = x3;
+  }
+  // dQ, dK accumulators (H layout) start from the V-reduced terms
+  float dQ[4][4], dK[4][4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int i = rS + r;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      dQ[r][q] = a.scale * gm[i] * H1[r][q];
+      dK[r][q] = lm[i] * H3[r][q] - gm[i] * bt[i] * H2[r][q];
+    }
+  }
+  sd = warp_sum(sd);
+  if (lane == 0) red[warp] = sd;
+  // partial row dots to shared memory, in the rowp / colp / dbp space (free until phase B)
+  float* rd1 = colp;   // [4][C]
+  float* rd2 = dbp;    // [4][C]
+  float* rd3 = rowp;   // [4][C]
+  if (lx == 0) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      rd1[(warp & 3) * C + rS + r] = qh1[r];
+      rd2[(warp & 3) * C + rS + r] = kh2[r];
+      rd3[(warp & 3) * C + rS + r] = kh3[r];
+    }
+  }
+  __syncthreads();   // phase A tiles are dead; rd* written
+  // the row dots summed in a fixed order, one token per thread (threads < C)
+  float qh1_i = 0.f, kh2_i = 0.f, kh3_i = 0.f;
+  if (tid < C) {
+    qh1_i = rd1[tid] + rd1[C + tid] + rd1[2 * C + tid] + rd1[3 * C + tid];
+    kh2_i = rd2[tid] + rd2[C + tid] + rd2[2 * C + tid] + rd2[3 * C + tid];
+    kh3_i = rd3[tid] + rd3[C + tid] + rd3[2 * C + tid] + rd3[3 * C + tid];
+  }
+  // ---- phase B: q, k transposed into R1; Q K^T, K K^T in the S layout
+  {
+    const int i = tid & 63, dg = tid >> 6;   // token i, features 16 dg .. 16 dg + 15
+#pragma unroll 4
+    for (int e = 0; e < 16; ++e) {
+      const int d = 16 * dg + e;
+      QT[d * RLD + i] = Qn[i * KLD + d];
+      KT[d * RLD + i] = Kn[i * KLD + d];
+    }
+  }
+  __syncthreads();
+  float QK[4][2], KK[4][2];
+  zero(QK);
+  zero(KK);
+#pragma unroll 4
+  for (int d = 0; d < K; ++d) {
+    const float4 aq = ld4(QT + d * RLD + rS), ak = ld4(KT + d * RLD + rS);
+    const float2 bk = ld2(KT + d * RLD + cS);
+    const float AQ[4] = {aq.x, aq.y, aq.z, aq.w}, AK[4] = {ak.x, ak.y, ak.z, ak.w};
+    const float BK[2] = {bk.x, bk.y};
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        QK[r][q] = fmaf(AQ[r], BK[q], QK[r][q]);
+        KK[r][q] = fmaf(AK[r], BK[q], KK[r][q]);
+      }
+  }
+  float F[4][2], E[4][2], rz[4], dba[4], cz[2] = {0.f, 0.f};
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int i = rS + r;
+    rz[r] = 0.f;
+    dba[r] = 0.f;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int j = cS + q;
+      const float gij = j <= i ? expf(G[i] - G[j]) : 0.f;
+      const float f = a.scale * OU[r][q] * gij;
+      const float dA = j < i ? -XU[r][q] : 0.f;
+      const float e = bt[i] * gij * dA;
+      const float z = f * QK[r][q] + e * KK[r][q];
+      F[r][q] = f;
+      E[r][q] = e;
+      rz[r] += z;
+      cz[q] += z;
+      dba[r] = fmaf(dA * gij, KK[r][q], dba[r]);
+    }
+  }
+  // reduce: rows over lx (xor 1, 2, 4), columns over ly (xor 8, 16)
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      rz[r] += __shfl_xor_sync(0xffffffffu, rz[r], o);
+      dba[r] += __shfl_xor_sync(0xffffffffu, dba[r], o);
+    }
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+#pragma unroll
+    for (int o = 8; o < 32; o <<= 1) cz[q] += __shfl_xor_sync(0xffffffffu, cz[q], o);
+  __syncthreads();   // Q^T, K^T reads done (F, E overwrite them); rd* reads done
+  if (lx == 0) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      rowp[(warp & 3) * C + rS + r] = rz[r];
+      dbp[(warp & 3) * C + rS + r] = dba[r];
+    }
+  }
+  if (ly == 0) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) colp[(warp >> 2) * C + cS + q] = cz[q];
+  }
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int j = cS + q;
+    st4(FT + j * RLD + rS, make_float4(F[0][q], F[1][q], F[2][q], F[3][q]));
+    st4(ET + j * RLD + rS, make_float4(E[0][q], E[1][q], E[2][q], E[3][q]));
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    *reinterpret_cast<float2*>(Fs + (rS + r) * RLD + cS) = make_float2(F[r][0], F[r][1]);
+    *reinterpret_cast<float2*>(Es + (rS + r) * RLD + cS) = make_float2(E[r][0], E[r][1]);
+  }
+  __syncthreads();
+  // ---- phase C: dQ += F K;  dK += F^T Q + (E + E^T) K   (H layout)
+#pragma unroll 2
+  for (int j = 0; j < C; ++j) {
+    const float4 f1 = ld4(FT + j * RLD + rS);   // F[i][j]
+    const float4 f2 = ld4(Fs + j * RLD + rS);   // F[j][i]
+    const float4 e1 = ld4(ET + j * RLD + rS);   // E[i][j]
+    const float4 e2 = ld4(Es + j * RLD + rS);   // E[j][i]
+    const float4 bk = ld4(Kn + j * KLD + cH), bq = ld4(Qn + j * KLD + cH);
+    const float A1[4] = {f1.x, f1.y, f1.z, f1.w}, A2[4] = {f2.x, f2.y, f2.z, f2.w};
+    const float A3[4] = {e1.x + e2.x, e1.y + e2.y, e1.z + e2.z, e1.w + e2.w};
+    const float BK[4] = {bk.x, bk.y, bk.z, bk.w}, BQ[4] = {bq.x, bq.y, bq.z, bq.w};
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        dQ[r][q] = fmaf(A1[r], BK[q], dQ[r][q]);
+        dK[r][q] = fmaf(A2[r], BQ[q], fmaf(A3[r], BK[q], dK[r][q]));
+      }
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int i = rS + r;
+    if (i >= L || cH >= K) continue;
+    st4(ws.dQ + ((size_t)(t0 + i) * a.Hv + h) * K + cH, make_float4(dQ[r][0], dQ[r][1], dQ[r][2], dQ[r][3]));
+    st4(ws.dK + ((size_t)(t0 + i) * a.Hv + h) * K + cH, make_float4(dK[r][0], dK[r][1], dK[r][2], dK[r][3]));
+  }
+  // ---- dG, dbeta per token (threads < C hold the row dots), then dg by a suffix sum
+  float* dGv = Fs;    // [C] (phase C reads of F / E are done after the barrier)
+  float* omv = Fs + C;
+  float* xvs = Fs + 2 * C;   // [8][C] xv partials
+  __syncthreads();
+  xvs[(tid >> 6) * C + (tid & 63)] = xv;
+  __syncthreads();
+  if (tid < C) {
+    const int i = tid;
+    float rsum = 0.f, csum = 0.f, db = 0.f, x = 0.f;
+    for (int g = 0; g < 4; ++g) {
+      rsum += rowp[g * C + i];
+      csum += colp[g * C + i];
+      db += dbp[g * C + i];
+    }
+    for (int g = 0; g < 8; ++g) x += xvs[g * C + i];
+    const float omega = i < L ? lm[i] * kh3_i : 0.f;
+    omv[i] = omega;
+    dGv[i] = i < L ? a.scale * gm[i] * qh1_i - bt[i] * gm[i] * kh2_i - omega + rsum - csum : 0.f;
+    if (i < L) b.dbeta[((size_t)(t0 + i)) * a.Hv + h] = x - gm[i] * kh2_i + db;
   }
   __syncthreads();
   if (warp == 0) {
     float sdt = 0.f;
     for (int w = 0; w < kGradWarps; ++w) sdt += red[w];
-    const float omsum = warp_sum(om[lane] + om[lane + 32]);
-    float x0 = lane < L ? dGr[lane] - cs[lane] : 0.f;
-    float x1 = lane + 32 < L ? dGr[lane + 32] - cs[lane + 32] : 0.f;
+    const float omsum = warp_sum(omv[lane] + omv[lane + 32]);
+    float x0 = dGv[lane], x1 = dGv[lane + 32];
     const float extra = gm[L - 1] * sdt + omsum;
     if (lane == L - 1) x0 += extra;
     if (lane + 32 == L - 1) x1 += extra;
-    // suffix sums: dg_i = sum_{j >= i} dG_j
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
+    for (int o = 1; o < 32; o <<= 1) {   // suffix sums: dg_i = sum_{j >= i} dG_j
       const float y0 = __shfl_down_sync(0xffffffffu, x0, o);
       const float y1 = __shfl_down_sync(0xffffffffu, x1, o);
       if (lane + o < 32) { x0 += y0; x1 += y1; }
     }
     x0 += __shfl_sync(0xffffffffu, x1, 0);
     const size_t base = (size_t)t0 * a.Hv + h;
-    if (lane < L) {
-      b.dg[base + (size_t)lane * a.Hv] = x0;
-      b.dbeta[base + (size_t)lane * a.Hv] = dbr[lane];
-    }
-    if (lane + 32 < L) {
-      b.dg[base + (size_t)(lane + 32) * a.Hv] = x1;
-      b.dbeta[base + (size_t)(lane + 32) * a.Hv] = dbr[lane + 32];
-    }
+    if (lane < L) b.dg[base + (size_t)lane * a.Hv] = x0;
+    if (lane + 32 < L) b.dg[base + (size_t)(lane + 32) * a.Hv] = x1;
   }
 }
 
@@ -830,12 +988,14 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
     f.rec_chunk_off = ws.chunk_off;
     if ((err = launch_chunk_tc(f))) return err;
   }
+  if (!tc) {   // fp32 state pass on W, U of the fp32 path's own prep pass
+    if ((err = launch_chunk_prep(a, ws.chunk_off, ws.W, ws.U, ws.G))) return err;
+    if ((err = launch_chunk_states(a, ws.chunk_off, ws.W, ws.U, ws.G, ws.S))) return err;
+  }
   if (NC > 0) {
-    bwd_prep_kernel<<<dim3((unsigned)NC, a.Hv), kPrepThreads, kPrepSmem, a.stream>>>(a, b, ws,
-                                                                                      tc ? 0 : 1);
+    bwd_prep_kernel<<<dim3((unsigned)NC, a.Hv), kPrepThreads, kPrepSmem, a.stream>>>(a, b, ws);
     if ((err = cudaGetLastError())) return err;
   }
-  if (!tc && (err = launch_chunk_states(a, ws.chunk_off, ws.W, ws.U, ws.G, ws.S))) return err;
   const unsigned vtiles = (unsigned)((a.V + VT - 1) / VT);
   if (a.num_seqs > 0) {
     const long long blocks = (long long)vtiles * a.Hv * a.num_seqs;

@@ -264,6 +264,24 @@ size_t chunk_generic_workspace_bytes(int T_total, int num_seqs, int Hv, int K, i
   return total;
 }
 
+cudaError_t launch_chunk_prep(const ChunkArgs& a, int32_t* chunk_off, float* W, float* U,
+                              float* G) {
+  WsLayout ws;
+  ws.chunk_off = chunk_off;
+  ws.W = W;
+  ws.U = U;
+  ws.G = G;
+  ws.S = nullptr;
+  const int T_total = a.cu_seqlens ? a.T : a.B * a.T;
+  const long long NC = max_chunks(T_total, a.num_seqs);
+  const size_t sp = prep_smem(a.K, a.V);
+  cudaError_t err;
+  if ((err = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp))) return err;
+  if (NC <= 0 || a.num_seqs <= 0) return cudaSuccess;
+  chunk_prep_kernel<<<dim3((unsigned)NC, a.Hv), kThreads, sp, a.stream>>>(a, ws);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_chunk_states(const ChunkArgs& a, int32_t* chunk_off, float* W, float* U,
                                 float* G, float* S) {
   WsLayout ws;

@@ -94,6 +94,9 @@ cudaError_t launch_chunk_generic(const ChunkArgs& a);
 // device chunk table (launch_chunk_table).
 cudaError_t launch_chunk_states(const ChunkArgs& a, int32_t* chunk_off, float* W, float* U,
                                 float* G, float* S);
+// The prep pass of the fp32 chunk path on caller-provided buffers: W, U and G per chunk.
+cudaError_t launch_chunk_prep(const ChunkArgs& a, int32_t* chunk_off, float* W, float* U,
+                              float* G);
 
 // Gradients for the backward of the chunkwise rule (all device pointers).
 struct BwdArgs {
