@@ -9,7 +9,9 @@ them padding) on a 512-slot fp32 state cache -- every kernel of the path.
 Prints one JSON line.  ``value`` is chunked-forward tokens/s (B*T per step over
 the chunked-forward time); the decode half is reported under ``decode``.  Beside
 the step, and outside its timed region: the Gated Delta Product (``product``) and
-the chunked backward of the same batch (``backward``).
+the chunked backward of the same batch (``backward``), the decode step replayed from
+a CUDA graph and both halves timed after an L2 flush (under ``decode``), and the
+other chunk workloads (``other_configs``).
 ``--impl reference`` times the fp64 CPU oracle instead (the reference arm).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
@@ -235,6 +237,91 @@ def measure_backward(dev, cin, d, seed, steps=5, warmup=3):
                     "scope": "whole backward call (all six launches)"}}
 
 
+def _median(xs):
+    return statistics.median(xs) if xs else None
+
+
+def measure_extras(dev, chunk, decode, reps=10):
+    """The decode step replayed from a CUDA graph, and the chunked forward and the decode step
+    timed one call at a time after an L2 flush (a 512 MiB write), median over the calls."""
+    res = {}
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            decode()
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        decode()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = 50
+    e0.record()
+    for _ in range(n):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    res["decode_graph_ms"] = e0.elapsed_time(e1) / n
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    for name, fn, k in (("chunk_ms_l2flush", chunk, reps), ("decode_ms_l2flush", decode, 2 * reps)):
+        evs = []
+        for _ in range(k):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        res[name] = _median([a.elapsed_time(b) for a, b in evs])
+    return res
+
+
+def measure_configs(dev, bf16_peak, steps=20, warmup=3):
+    """Chunked-forward throughput on the other chunk workloads: the tiny fp32 case (B=1
+    T=256 Hqk=Hv=2 K=V=64), one 8192-token bf16 sequence, and 32 packed varlen sequences
+    (100-4096 tokens) reading and writing a 64-slot state cache."""
+    from chunked_gated_delta_gdn_gb300 import chunk_fwd_path, chunk_gated_delta_rule, synthetic
+    out = {}
+    for name in ("tiny_fp32", "single_seq_bf16", "varlen_prefill_bf16"):
+        inp = synthetic.workload(name)
+        d = {k: (None if getattr(inp, k) is None else getattr(inp, k).to(dev))
+             for k in ("q", "k", "v", "g", "beta", "initial_state", "cu_seqlens", "state_indices")}
+        B, T, Hqk, K = inp.q.shape
+        Hv, V = inp.v.shape[2:]
+        o = torch.empty_like(d["v"])
+        fin = None if inp.state_indices is not None else torch.empty_like(d["initial_state"])
+
+        def run():
+            chunk_gated_delta_rule(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                   initial_state=d["initial_state"], output_final_state=True,
+                                   use_qk_l2norm_in_kernel=True, cu_seqlens=d["cu_seqlens"],
+                                   state_indices=d["state_indices"], out=o, final_state=fin)
+
+        for _ in range(warmup):
+            run()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            run()
+        e1.record()
+        torch.cuda.synchronize()
+        sec = e0.elapsed_time(e1) / steps / 1000.0
+        tokens = B * T
+        fpt = Hqk * 2 * C_ * K + Hv * (C_ * K + 2 * C_ * V + 6 * K * V)
+        path = chunk_fwd_path(K, V, inp.q.dtype)
+        out[name] = {"tokens": tokens, "ms": sec * 1e3, "tokens_per_s": tokens / sec,
+                     "tflops": fpt * tokens / sec / 1e12, "flop_per_token": fpt,
+                     "tensor_frac": (fpt * tokens / sec / 1e12 / bf16_peak) if path == 1 else None,
+                     "path": "tcgen05 fused" if path == 1 else "fp32 CUDA-core"}
+    return out
+
+
 def _product_ws(T, n_h):
     from chunked_gated_delta_gdn_gb300 import _lib
     return int(_lib.load().gdn_product_chunk_fwd_workspace_size(1, T, n_h, HQK_, HV_, K_, V_, 1,
@@ -315,6 +402,9 @@ def main():
     ap.add_argument("--no-backward", action="store_true",
                     help="skip the chunked-backward measurement reported beside the headline")
     ap.add_argument("--backward-steps", type=int, default=5)
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the CUDA-graph decode, the L2-flushed timings and the other chunk "
+                         "workloads reported beside the headline")
     args = ap.parse_args()
     world, rank, local = dist_env()
     if world > 1:
@@ -452,6 +542,9 @@ def main():
     }
     if args.only is None and not args.no_product:
         line["product"] = measure_product(dev, 1006 + 1000 * rank)
+    if args.only is None and not args.no_extras:
+        line["decode"].update(measure_extras(dev, chunk, decode))
+        line["other_configs"] = measure_configs(dev, bf16_peak)
     if args.only in (None, "backward") and not args.no_backward:
         line["backward"] = measure_backward(dev, cin, d, 1007 + 1000 * rank,
                                             steps=args.backward_steps)

@@ -37,8 +37,8 @@
 //   4. reverse      per (sequence, value head, 32 columns), chunks last to first:
 //                   records dS (the gradient of each chunk's exit state) and dX
 //   5. grad         per (chunk, value head): dv, dbeta, dg, and dQ, dK per value head
-//   6. qk           per token: the group sum and the L2-norm Jacobian -> dq, dk;
-//                   zero gradients for tokens outside every sequence
+//   6. qk           per (token, query/key head): the group sum and the L2-norm Jacobian
+//                   -> dq, dk; zero gradients for tokens outside every sequence
 #include "gdn_chunk_util.cuh"
 
 namespace gdn {
@@ -570,25 +570,34 @@ __global__ void __launch_bounds__(kGradThreads) bwd_grad_kernel(const ChunkArgs 
   const bool l2 = a.use_qk_l2norm != 0;
   const size_t ch = (size_t)c * a.Hv + h;
 
-  // normalised q, k rows (warp w: rows 4 w .. 4 w + 3)
+  // normalised q, k rows (warp w: rows 4 w .. 4 w + 3); every load issued before the norms
   load_gates(a, t0, L, h, G, bt);
+  {
+    float x[2][4][4];
 #pragma unroll
-  for (int which = 0; which < 2; ++which) {
-    const void* src = which ? a.k : a.q;
-    float* dst = which ? Kn : Qn;
-    for (int r = 4 * warp; r < 4 * warp + 4; ++r) {
-      float x[4], ss = 0.f;
+    for (int which = 0; which < 2; ++which)
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int d = lane + 32 * m;
-        x[m] = (r < L && d < K) ? load_elem(src, ((size_t)(t0 + r) * a.Hqk + hq) * K + d, a.io_dtype) : 0.f;
-        ss = fmaf(x[m], x[m], ss);
+      for (int r4 = 0; r4 < 4; ++r4)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int r = 4 * warp + r4, d = lane + 32 * m;
+          x[which][r4][m] = (r < L && d < K)
+                                ? load_elem(which ? a.k : a.q, ((size_t)(t0 + r) * a.Hqk + hq) * K + d,
+                                            a.io_dtype)
+                                : 0.f;
+        }
+#pragma unroll
+    for (int which = 0; which < 2; ++which)
+#pragma unroll
+      for (int r4 = 0; r4 < 4; ++r4) {
+        float ss = 0.f;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) ss = fmaf(x[which][r4][m], x[which][r4][m], ss);
+        const float rn = l2 ? 1.0f / sqrtf(warp_sum(ss) + kL2Eps) : 1.f;
+        float* dst = (which ? Kn : Qn) + (4 * warp + r4) * KLD + lane;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) dst[32 * m] = x[which][r4][m] * rn;
       }
-      float rn = 1.f;
-      if (l2) rn = 1.0f / sqrtf(warp_sum(ss) + kL2Eps);
-#pragma unroll
-      for (int m = 0; m < 4; ++m) dst[r * KLD + lane + 32 * m] = x[m] * rn;
-    }
   }
   __syncthreads();
   if (tid < C) {
@@ -897,60 +906,84 @@ __global__ void __launch_bounds__(kGradThreads) bwd_grad_kernel(const ChunkArgs 
 }
 
 // ---------------------------------------------------------------- 6. qk
-constexpr int kQkThreads = 128;
+// One warp per (token, query/key head), four features per lane: the group sum of the
+// per-value-head dQ, dK in a fixed order, then the L2 norm's Jacobian.  Tokens outside every
+// sequence get zero gradients (dq, dk here; dv, dg, dbeta of the group's value heads too).
+constexpr int kQkThreads = 256;
+
+__device__ __forceinline__ void load4(const void* p, size_t i, int dtype, float (&x)[4]) {
+  if (dtype == GDN_BF16) {
+    const uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(p) + i);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+  } else {
+    const float4 v = ld4(reinterpret_cast<const float*>(p) + i);
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+  }
+}
+
+__device__ __forceinline__ void store4(void* p, size_t i, int dtype, const float (&x)[4]) {
+  if (dtype == GDN_BF16) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]), b = __floats2bfloat162_rn(x[2], x[3]);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p) + i) = u;
+  } else {
+    st4(reinterpret_cast<float*>(p) + i, make_float4(x[0], x[1], x[2], x[3]));
+  }
+}
 
 __global__ void __launch_bounds__(kQkThreads) bwd_qk_kernel(const ChunkArgs a, const BwdArgs b,
                                                             BwdWs ws, int T_total) {
-  const int t = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int N = a.num_seqs, K = a.K, V = a.V;
+  const long long item = (long long)blockIdx.x * (kQkThreads / 32) + (threadIdx.x >> 5);
+  if (item >= (long long)T_total * a.Hqk) return;
+  const int lane = threadIdx.x & 31;
+  const int t = (int)(item / a.Hqk), hq = (int)(item - (long long)t * a.Hqk);
+  const int N = a.num_seqs, K = a.K, V = a.V, grp = a.Hv / a.Hqk;
   int covered = 0;
   if (ws.chunk_off[N + 1]) covered = a.cu_seqlens ? a.cu_seqlens[N] : N * a.T;
   const bool in = t < covered;
-  const int grp = a.Hv / a.Hqk;
   const bool l2 = a.use_qk_l2norm != 0;
-  for (int hq = warp; hq < a.Hqk; hq += kQkThreads / 32) {
+  const int d = 4 * lane;
+  const bool act = d < K;   // K % 4 == 0
 #pragma unroll
-    for (int which = 0; which < 2; ++which) {
-      const void* x_src = which ? a.k : a.q;
-      const float* dsrc = which ? ws.dK : ws.dQ;
-      void* dst = which ? b.dk : b.dq;
-      float dx[4], x[4];
+  for (int which = 0; which < 2; ++which) {
+    const void* x_src = which ? a.k : a.q;
+    const float* dsrc = which ? ws.dK : ws.dQ;
+    float dx[4] = {0.f, 0.f, 0.f, 0.f}, x[4] = {0.f, 0.f, 0.f, 0.f};
+    if (in && act) {
+      for (int hh = hq * grp; hh < (hq + 1) * grp; ++hh) {
+        const float4 v = ld4(dsrc + ((size_t)t * a.Hv + hh) * K + d);
+        dx[0] += v.x; dx[1] += v.y; dx[2] += v.z; dx[3] += v.w;
+      }
+      load4(x_src, ((size_t)t * a.Hqk + hq) * K + d, a.io_dtype, x);
+    }
+    if (l2) {
       float ss = 0.f, xd = 0.f;
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
-        const int d = lane + 32 * m;
-        dx[m] = 0.f;
-        x[m] = 0.f;
-        if (in && d < K) {
-          for (int hh = hq * grp; hh < (hq + 1) * grp; ++hh)
-            dx[m] += dsrc[((size_t)t * a.Hv + hh) * K + d];
-          x[m] = load_elem(x_src, ((size_t)t * a.Hqk + hq) * K + d, a.io_dtype);
-        }
         ss = fmaf(x[m], x[m], ss);
         xd = fmaf(x[m], dx[m], xd);
       }
-      if (l2) {
-        ss = warp_sum(ss);
-        xd = warp_sum(xd);
-        const float rho = 1.0f / sqrtf(ss + kL2Eps);
-        const float c3 = rho * rho * rho * xd;
+      ss = warp_sum(ss);
+      xd = warp_sum(xd);
+      const float rho = 1.0f / sqrtf(ss + kL2Eps);
+      const float c3 = rho * rho * rho * xd;
 #pragma unroll
-        for (int m = 0; m < 4; ++m) dx[m] = rho * dx[m] - c3 * x[m];
-      }
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int d = lane + 32 * m;
-        if (d < K) store_elem(dst, ((size_t)t * a.Hqk + hq) * K + d, dx[m], a.io_dtype);
-      }
+      for (int m = 0; m < 4; ++m) dx[m] = rho * dx[m] - c3 * x[m];
     }
+    if (act) store4(which ? b.dk : b.dq, ((size_t)t * a.Hqk + hq) * K + d, a.io_dtype, dx);
   }
-  if (!in) {  // tokens outside every sequence: zero gradients
-    for (int e = threadIdx.x; e < a.Hv * V; e += kQkThreads)
-      store_elem(b.dv, (size_t)t * a.Hv * V + e, 0.f, a.io_dtype);
-    for (int e = threadIdx.x; e < a.Hv; e += kQkThreads) {
-      b.dg[(size_t)t * a.Hv + e] = 0.f;
-      b.dbeta[(size_t)t * a.Hv + e] = 0.f;
+  if (!in) {   // zero dv, dg, dbeta of this group's value heads
+    const float z[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int hh = hq * grp; hh < (hq + 1) * grp; ++hh) {
+      for (int e = 4 * lane; e < V; e += 128) store4(b.dv, ((size_t)t * a.Hv + hh) * V + e, a.io_dtype, z);
+      if (lane == 0) {
+        b.dg[(size_t)t * a.Hv + hh] = 0.f;
+        b.dbeta[(size_t)t * a.Hv + hh] = 0.f;
+      }
     }
   }
 }
@@ -1008,7 +1041,10 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
     if ((err = cudaGetLastError())) return err;
   }
   if (T_total > 0) {
-    bwd_qk_kernel<<<T_total, kQkThreads, 0, a.stream>>>(a, b, ws, T_total);
+    const long long items = (long long)T_total * a.Hqk;
+    const long long blocks = (items + kQkThreads / 32 - 1) / (kQkThreads / 32);
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    bwd_qk_kernel<<<(unsigned)blocks, kQkThreads, 0, a.stream>>>(a, b, ws, T_total);
     if ((err = cudaGetLastError())) return err;
   }
   return cudaSuccess;
