@@ -487,14 +487,17 @@ def main():
     dec_avg_s = max(dec_sum, 1e-6) / K / 1000.0
     value = world * tokens / chunk_avg_s
 
-    # end to end through the public API: pinned host inputs in, o and the final state out
-    o_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-    f_host = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
+    # end to end through the public API: pinned host inputs in, o and the final state out.
+    # Sequential: copy in, compute, copy out, one step after another on one stream.  Pipelined:
+    # the copy-in of step s + 1 and the copy-out of step s - 1 run on their own streams while
+    # step s computes (double-buffered device tensors); every byte still crosses the link.
+    o_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for _ in range(2)]
+    f_host = [torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True) for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = o_host.numel() * o_host.element_size() + f_host.numel() * f_host.element_size()
-    e2e_val = None
+    d2h = o_host[0].numel() * o_host[0].element_size() + f_host[0].numel() * f_host[0].element_size()
+    e2e_val = e2e_seq = None
     if args.only is None:
-        e2e_steps = max(1, min(K, 5))
+        e2e_steps = max(2, min(K, 6))
         torch.cuda.synchronize()
         barrier(world)
         ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -503,12 +506,54 @@ def main():
             g = {k: v.to(dev, non_blocking=True) for k, v in host.items()}
             oo, ff = chunk_gated_delta_rule(g["q"], g["k"], g["v"], g["g"], g["beta"],
                                             output_final_state=True, use_qk_l2norm_in_kernel=True)
-            o_host.copy_(oo, non_blocking=True)
-            f_host.copy_(ff, non_blocking=True)
+            o_host[0].copy_(oo, non_blocking=True)
+            f_host[0].copy_(ff, non_blocking=True)
+        eb.record(stream)
+        torch.cuda.synchronize()
+        e2e_seq = world * tokens / (max_over_ranks(ea.elapsed_time(eb), world, dev) / e2e_steps / 1000.0)
+        del g, oo, ff
+        # pipelined over three streams
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        bin_ = [{k: torch.empty_like(d[k]) for k in host} for _ in range(2)]
+        bout = [(torch.empty_like(o), torch.empty_like(fin)) for _ in range(2)]
+        in_free, out_free = [None, None], [None, None]
+        torch.cuda.synchronize()
+        barrier(world)
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record(stream)
+        s_in.wait_event(ea)
+        s_out.wait_event(ea)
+        for st in range(e2e_steps):
+            b = st % 2
+            if in_free[b] is not None:
+                s_in.wait_event(in_free[b])      # step st - 2 has finished reading these inputs
+            with torch.cuda.stream(s_in):
+                for k in host:
+                    bin_[b][k].copy_(host[k], non_blocking=True)
+            ev_in = torch.cuda.Event()
+            ev_in.record(s_in)
+            stream.wait_event(ev_in)
+            if out_free[b] is not None:
+                stream.wait_event(out_free[b])   # the copy-out of step st - 2 is done
+            x = bin_[b]
+            chunk_gated_delta_rule(x["q"], x["k"], x["v"], x["g"], x["beta"],
+                                   output_final_state=True, use_qk_l2norm_in_kernel=True,
+                                   out=bout[b][0], final_state=bout[b][1])
+            in_free[b] = torch.cuda.Event()
+            in_free[b].record(stream)
+            s_out.wait_event(in_free[b])
+            with torch.cuda.stream(s_out):
+                o_host[b].copy_(bout[b][0], non_blocking=True)
+                f_host[b].copy_(bout[b][1], non_blocking=True)
+            out_free[b] = torch.cuda.Event()
+            out_free[b].record(s_out)
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
         eb.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(ea.elapsed_time(eb), world, dev) / e2e_steps
         e2e_val = world * tokens / (e2e_ms / 1000.0)
+        del bin_, bout
 
     flops = FLOP_PER_TOKEN * tokens
     alg_bytes = BYTES_PER_TOKEN * tokens + B * HV_ * STATE_BYTES   # + the final state written
@@ -536,7 +581,7 @@ def main():
                    "state_gbs": dec_bytes / dec_avg_s / 1e9,
                    "hbm_frac": dec_bytes / dec_avg_s / 1e9 / hbm_peak},
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "pipelined": True, "value_sequential": e2e_seq},
         "gpu_launches": launches_per_step * K,
         "clocks": clk.summary(),
     }
@@ -544,6 +589,9 @@ def main():
         line["product"] = measure_product(dev, 1006 + 1000 * rank)
     if args.only is None and not args.no_extras:
         line["decode"].update(measure_extras(dev, chunk, decode))
+        gsec = line["decode"]["decode_graph_ms"] / 1000.0
+        line["decode"]["state_gbs_graph"] = dec_bytes / gsec / 1e9
+        line["decode"]["hbm_frac_graph"] = dec_bytes / gsec / 1e9 / hbm_peak
         line["other_configs"] = measure_configs(dev, bf16_peak)
     if args.only in (None, "backward") and not args.no_backward:
         line["backward"] = measure_backward(dev, cin, d, 1007 + 1000 * rank,
