@@ -40,6 +40,7 @@
 //   6. qk           per (token, query/key head): the group sum and the L2-norm Jacobian
 //                   -> dq, dk; zero gradients for tokens outside every sequence
 #include "gdn_chunk_util.cuh"
+#include "gdn_sm100.cuh"
 
 namespace gdn {
 namespace {
@@ -173,6 +174,31 @@ constexpr int kBarT = 1;          // named barrier of the two warps that build T
 
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+
+__device__ __forceinline__ void load4(const void* p, size_t i, int dtype, float (&x)[4]) {
+  if (dtype == GDN_BF16) {
+    const uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(p) + i);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+  } else {
+    const float4 v = ld4(reinterpret_cast<const float*>(p) + i);
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+  }
+}
+
+__device__ __forceinline__ void store4(void* p, size_t i, int dtype, const float (&x)[4]) {
+  if (dtype == GDN_BF16) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]), b = __floats2bfloat162_rn(x[2], x[3]);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p) + i) = u;
+  } else {
+    st4(reinterpret_cast<float*>(p) + i, make_float4(x[0], x[1], x[2], x[3]));
+  }
+}
+
 
 __global__ void __launch_bounds__(kPrepThreads, 2) bwd_prep_kernel(const ChunkArgs a,
                                                                    const BwdArgs b, BwdWs ws) {
@@ -381,26 +407,34 @@ __global__ void __launch_bounds__(kRevThreads, 2) bwd_reverse_kernel(const Chunk
         if (4 * ty + r < K)
           st4(dSg + (size_t)(4 * ty + r) * V + col, make_float4(s[r][0], s[r][1], s[r][2], s[r][3]));
     }
-    // normalised k rows into Kn and Kt (warp w: rows w, w + 8, ...)
-    for (int r = warp; r < C; r += kRevThreads / 32) {
-      float x[4];
-      float ss = 0.f;
+    // normalised k rows into Kn and Kt (warp w: rows w + 8 s; every load issued first)
+    {
+      float x[C / (kRevThreads / 32)][4];
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int d = lane + 32 * m;
-        x[m] = (r < L && d < K) ? load_elem(a.k, ((size_t)(t0 + r) * a.Hqk + hq) * K + d, a.io_dtype) : 0.f;
-        ss = fmaf(x[m], x[m], ss);
-      }
-      if (l2) {
-        ss = warp_sum(ss);
-        const float rn = 1.0f / sqrtf(ss + kL2Eps);
+      for (int s8 = 0; s8 < C / (kRevThreads / 32); ++s8) {
+        const int r = warp + (kRevThreads / 32) * s8;
 #pragma unroll
-        for (int m = 0; m < 4; ++m) x[m] *= rn;
+        for (int m = 0; m < 4; ++m) {
+          const int d = lane + 32 * m;
+          x[s8][m] = (r < L && d < K) ? load_elem(a.k, ((size_t)(t0 + r) * a.Hqk + hq) * K + d, a.io_dtype) : 0.f;
+        }
       }
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        Kn[r * KLD + lane + 32 * m] = x[m];
-        Kt[(lane + 32 * m) * TLD + r] = x[m];
+      for (int s8 = 0; s8 < C / (kRevThreads / 32); ++s8) {
+        const int r = warp + (kRevThreads / 32) * s8;
+        if (l2) {
+          float ss = 0.f;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) ss = fmaf(x[s8][m], x[s8][m], ss);
+          const float rn = 1.0f / sqrtf(warp_sum(ss) + kL2Eps);
+#pragma unroll
+          for (int m = 0; m < 4; ++m) x[s8][m] *= rn;
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          Kn[r * KLD + lane + 32 * m] = x[s8][m];
+          Kt[(lane + 32 * m) * TLD + r] = x[s8][m];
+        }
       }
     }
     load_gates(a, t0, L, h, G, bt);
@@ -905,35 +939,400 @@ __global__ void __launch_bounds__(kGradThreads) bwd_grad_kernel(const ChunkArgs 
   }
 }
 
+// ---------------------------------------------------------------- 5b. grad on the tensor cores
+// bf16 I/O with K = V = 128: the same quantities as bwd_grad_kernel, with every product a
+// tcgen05.mma (bf16 operands in 128-byte-swizzled shared memory, fp32 accumulators in TMEM;
+// S0, dS, U', dX and the normalised q, k rounded to bf16 as the forward's tensor-core path
+// rounds its operands).  One CTA (8 warps) per (chunk, value head); TMEM columns:
+//   R1 [0, 256)   [Q; K] [S0 | dS]        M=128 N=256 K=128  -> q_i . S0 dO_i, k_i . S0 dX_i,
+//                                                               k_i . dS u'_i (row dots)
+//   R2 [256, 320) [dO; dX] U'^T           M=128 N=64  K=128  -> F, dA (and E)
+//   R3 [320, 384) [Q; K] K^T              M=128 N=64  K=128  -> Q K^T, K K^T
+//   R4 [384, 512) [dQ; dK] =  [scale gamma dO | 0 ; -gamma beta dX | lambda U'] [S0 | dS]^T
+//                           + [F; E] K + [0; F^T] Q + [0; E^T] K          (K = 256, 64, 64, 64)
+// F^T and E^T are MN-major A operands whose first 64-row block is a zero tile and whose
+// second is F (resp. E) as stored row-major, so no transposed copy is built.
+namespace tcg {
+using namespace sm100;
+constexpr int kThreads = 256;
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint32_t OFF_QK = 0;          // [q; k] rows, 2 k-halves x 128 rows x 128 B
+constexpr uint32_t OFF_S0 = 32768;      // S0 rows d, 2 c-halves x 128 rows
+constexpr uint32_t OFF_DS = 65536;      // dS rows d (right after S0: [S0 | dS] is one operand)
+constexpr uint32_t OFF_OX = 98304;      // [dO; dX] rows, then [scale gamma dO; -gamma beta dX]
+constexpr uint32_t OFF_LU = 131072;     // [0; lambda U'] rows (right after OX)
+constexpr uint32_t OFF_U = 163840;      // U' rows j, 2 c-halves x 64 rows; then Z^T fp32 [64][64]
+constexpr uint32_t OFF_ZERO = 180224;   // 64 rows x 128 B of zeros
+constexpr uint32_t OFF_FE = 188416;     // [F; E] rows, K = 64 tokens: 128 rows x 128 B
+constexpr uint32_t OFF_VEC = 204800;    // fp32 per-token vectors, 16 x 64
+constexpr uint32_t OFF_BAR = OFF_VEC + 16 * 64 * 4;
+constexpr uint32_t SMEM = OFF_BAR + 64 + 1024;
+constexpr uint32_t T_R1 = 0, T_R2 = 256, T_R3 = 320, T_R4 = 384, T_COLS = 512;
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+// Four values as bf16 at element (row, col) of a K-major tile with 128-element rows split in
+// two 64-element halves of `half` bytes (col % 4 == 0).
+__device__ __forceinline__ void put4(uint8_t* tile, uint32_t half, int row, int col, const float (&x)[4]) {
+  uint2 u;
+  u.x = pack2(x[0], x[1]);
+  u.y = pack2(x[2], x[3]);
+  *reinterpret_cast<uint2*>(tile + (col >> 6) * half + sw128_offset(row, col & 63)) = u;
+}
+__device__ __forceinline__ float get1(const uint8_t* tile, uint32_t half, int row, int col) {
+  return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(tile + (col >> 6) * half +
+                                                                     sw128_offset(row, col & 63)));
+}
+// Scale the 8 bf16 of the 16-byte chunk at p by s.
+__device__ __forceinline__ void scale8(uint8_t* p, float s) {
+  uint4 v = *reinterpret_cast<uint4*>(p);
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[q]));
+    w[q] = pack2(s * f.x, s * f.y);
+  }
+  *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+__device__ __forceinline__ uint64_t kdesc(uint32_t addr) { return sdesc_sw128(addr, 16, 1024); }
+__device__ __forceinline__ uint64_t mndesc(uint32_t addr, uint32_t lbo) {
+  return sdesc_sw128(addr, lbo, 1024);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(const ChunkArgs a, const BwdArgs b,
+                                                                  BwdWs ws) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sb = smem_u32(sm);
+  float* vec = reinterpret_cast<float*>(sm + OFF_VEC);
+  float* G = vec;              float* bt = vec + 64;    float* gm = vec + 128;  float* lm = vec + 192;
+  float* qh1 = vec + 256;      float* kh2 = vec + 320;  float* kh3 = vec + 384; float* rz = vec + 448;
+  float* dba = vec + 512;      float* cs = vec + 576;   float* xvr = vec + 640; float* red = vec + 704;
+  float* dGv = vec + 768;      float* om = vec + 832;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 8);
+  const int c = blockIdx.x, h = blockIdx.y;
+  int n, t0, L;
+  if (!locate_chunk(a, ws.chunk_off, c, &n, &t0, &L)) return;
+  const int Hv = a.Hv, hq = h / (Hv / a.Hqk);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const size_t ch = (size_t)c * Hv + h;
+  const bool l2 = a.use_qk_l2norm != 0;
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tslot, T_COLS);
+    tmem_relinquish();
+  }
+  load_gates(a, t0, L, h, G, bt);
+  // ---- operands to shared memory
+  // Every global load of a batch is issued before any of it is used (the loads of one
+  // thread are independent; issuing them one loop trip at a time would expose the memory
+  // latency once per trip).
+  {  // normalised [q; k] rows: warp w takes rows w + 8 s
+    float x[16][4];
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+      const int r = warp + 8 * s, i = r & 63;
+      x[s][0] = x[s][1] = x[s][2] = x[s][3] = 0.f;
+      if (i < L) load4(r < 64 ? a.q : a.k, ((size_t)(t0 + i) * a.Hqk + hq) * 128 + 4 * lane, a.io_dtype, x[s]);
+    }
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+      float rn = 1.f;
+      if (l2)
+        rn = 1.0f / sqrtf(warp_sum(x[s][0] * x[s][0] + x[s][1] * x[s][1] + x[s][2] * x[s][2] +
+                                   x[s][3] * x[s][3]) + kL2Eps);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) x[s][q] *= rn;
+      put4(sm + OFF_QK, 16384, warp + 8 * s, 4 * lane, x[s]);
+    }
+  }
+  float sd = 0.f;
+  {  // S0, dS rows d (bf16), 8 float4 pairs per batch
+    const float* Sg = ws.S + ch * 128 * 128;
+    const float* dSg = ws.dS + ch * 128 * 128;
+#pragma unroll 1
+    for (int base = 0; base < 16; base += 8) {
+      float4 s0[8], ds[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int e = tid + kThreads * (base + u), d = e >> 5, col = 4 * (e & 31);
+        s0[u] = ld4(Sg + d * 128 + col);
+        ds[u] = ld4(dSg + d * 128 + col);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int e = tid + kThreads * (base + u), d = e >> 5, col = 4 * (e & 31);
+        const float xs[4] = {s0[u].x, s0[u].y, s0[u].z, s0[u].w};
+        const float xd[4] = {ds[u].x, ds[u].y, ds[u].z, ds[u].w};
+        put4(sm + OFF_S0, 16384, d, col, xs);
+        put4(sm + OFF_DS, 16384, d, col, xd);
+        sd += s0[u].x * ds[u].x + s0[u].y * ds[u].y + s0[u].z * ds[u].z + s0[u].w * ds[u].w;
+      }
+    }
+  }
+  {  // dO, dX, U' rows i (one row per warp and trip), 4 trips per batch; dv; dX . v
+    const float* Ug = ws.U + ch * 64 * 128;
+    const float* dXg = ws.dX + ch * 64 * 128;
+    const int col = 4 * lane;
+#pragma unroll 1
+    for (int base = 0; base < 8; base += 4) {
+      float o4[4][4], v4[4][4], x4[4][4], u4[4][4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = warp + 8 * (base + u);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) o4[u][q] = v4[u][q] = x4[u][q] = u4[u][q] = 0.f;
+        if (i < L) {
+          const size_t tv = ((size_t)(t0 + i) * Hv + h) * 128 + col;
+          load4(b.d_o, tv, a.io_dtype, o4[u]);
+          load4(a.v, tv, a.io_dtype, v4[u]);
+          const float4 xx = ld4(dXg + i * 128 + col), uu = ld4(Ug + i * 128 + col);
+          x4[u][0] = xx.x; x4[u][1] = xx.y; x4[u][2] = xx.z; x4[u][3] = xx.w;
+          u4[u][0] = uu.x; u4[u][1] = uu.y; u4[u][2] = uu.z; u4[u][3] = uu.w;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = warp + 8 * (base + u);
+        if (i < L) {
+          const float bi = bt[i];
+          const float dv4[4] = {bi * x4[u][0], bi * x4[u][1], bi * x4[u][2], bi * x4[u][3]};
+          store4(b.dv, ((size_t)(t0 + i) * Hv + h) * 128 + col, a.io_dtype, dv4);
+        }
+        put4(sm + OFF_OX, 16384, i, col, o4[u]);
+        put4(sm + OFF_OX, 16384, 64 + i, col, x4[u]);
+        put4(sm + OFF_U, 8192, i, col, u4[u]);
+        const float xv = warp_sum(x4[u][0] * v4[u][0] + x4[u][1] * v4[u][1] + x4[u][2] * v4[u][2] +
+                                  x4[u][3] * v4[u][3]);
+        if (lane == 0) xvr[i] = xv;
+      }
+    }
+  }
+  for (int e = tid; e < 8192 / 16; e += kThreads)      // the zero tile
+    reinterpret_cast<uint4*>(sm + OFF_ZERO)[e] = make_uint4(0u, 0u, 0u, 0u);
+  for (int e = tid; e < 2 * 8192 / 16; e += kThreads) {   // rows 0-63 of both halves of [0; lambda U']
+    const int hlf = e / (8192 / 16), w = e - hlf * (8192 / 16);
+    reinterpret_cast<uint4*>(sm + OFF_LU + hlf * 16384)[w] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  sd = warp_sum(sd);
+  if (lane == 0) red[warp] = sd;
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = *tslot;
+  bool ok = true;
+  // ---- R1, R2, R3
+  if (tid == 0) {
+    const uint32_t i1 = idesc_bf16(128, 256, false, true), i2 = idesc_bf16(128, 64, false, false);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
+      mma_bf16(tb + T_R1, kdesc(sb + OFF_QK + ko), mndesc(sb + OFF_S0 + ks * 2048, 16384), i1, ks > 0);
+      mma_bf16(tb + T_R2, kdesc(sb + OFF_OX + ko),
+               kdesc(sb + OFF_U + (ks >> 2) * 8192 + (ks & 3) * 32), i2, ks > 0);
+      mma_bf16(tb + T_R3, kdesc(sb + OFF_QK + ko), kdesc(sb + OFF_QK + 8192 + ko), i2, ks > 0);
+    }
+    mma_commit(bar);
+  }
+  if (tid < 64) {
+    gm[tid] = expf(G[tid]);
+    lm[tid] = expf(G[L - 1] - G[tid]);
+  }
+  if (tid == 0) ok = mbar_wait(bar, 0, kWaitNs);
+  if (__syncthreads_or(!ok)) {
+    if (tid == 0) report(a.dev_status, GDN_DEV_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tb, T_COLS);
+    return;
+  }
+  tc_fence_after();
+  const uint32_t loff = (uint32_t)(32 * (warp & 3)) << 16;
+  const int row = 32 * (warp & 3) + lane;   // this thread's TMEM lane
+  // ---- row dots from R1 (warps 0-3: the S0 columns; warps 6-7: the dS columns of k rows)
+  if (warp < 4) {
+    float acc = 0.f;
+#pragma unroll
+    for (int part = 0; part < 4; ++part) {
+      float x[32];
+      tmem_ld32(tb + loff + T_R1 + 32 * part, x);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) acc = fmaf(x[j], get1(sm + OFF_OX, 16384, row, 32 * part + j), acc);
+    }
+    if (row < 64) qh1[row] = acc; else kh2[row - 64] = acc;
+  } else if (warp >= 6) {
+    float acc = 0.f;
+#pragma unroll
+    for (int part = 0; part < 4; ++part) {
+      float x[32];
+      tmem_ld32(tb + loff + T_R1 + 128 + 32 * part, x);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) acc = fmaf(x[j], get1(sm + OFF_U, 8192, row - 64, 32 * part + j), acc);
+    }
+    kh3[row - 64] = acc;
+  }
+  __syncthreads();
+  // ---- R4's scaled operands: [scale gamma dO; -gamma beta dX] in place, lambda U' rows 64-127
+  for (int e = tid; e < 128 * 16; e += kThreads) {
+    const int r = e >> 4, chunk = e & 15, hlf = chunk >> 3, c8 = chunk & 7;
+    const float s = r < 64 ? a.scale * gm[r] : -gm[r - 64] * bt[r - 64];
+    scale8(sm + OFF_OX + hlf * 16384 + r * 128 + ((c8 ^ (r & 7)) << 4), s);
+  }
+  for (int e = tid; e < 64 * 16; e += kThreads) {
+    const int i = e >> 4, chunk = e & 15, hlf = chunk >> 3, c8 = chunk & 7;
+    const uint32_t sw = (uint32_t)((c8 ^ (i & 7)) << 4);
+    uint8_t* dst = sm + OFF_LU + hlf * 16384 + (64 + i) * 128 + sw;
+    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(sm + OFF_U + hlf * 8192 + i * 128 + sw);
+    scale8(dst, lm[i]);
+  }
+  __syncthreads();   // U' is no longer needed: its space holds Z^T
+  float* Zt = reinterpret_cast<float*>(sm + OFF_U);   // Zt[j * 64 + i] = Z[i][j]
+  // ---- F (rows i < 64 of R2 / R3: warps 0-1), then E (rows 64-127: warps 2-3)
+  if (warp < 2) {
+    const int i = row;
+    float acc = 0.f;
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      float x[32], y[32];
+      tmem_ld32(tb + loff + T_R2 + 32 * part, x);
+      tmem_ld32(tb + loff + T_R3 + 32 * part, y);
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) {
+        const int j = 32 * part + jj;
+        const float f = j <= i ? a.scale * x[jj] * expf(G[i] - G[j]) : 0.f;
+        const float z = f * y[jj];
+        acc += z;
+        Zt[j * 64 + i] = z;
+        *reinterpret_cast<__nv_bfloat16*>(sm + OFF_FE + sw128_offset(i, j)) = __float2bfloat16_rn(f);
+      }
+    }
+    rz[i] = acc;
+  }
+  __syncthreads();
+  if (warp == 2 || warp == 3) {
+    const int i = row - 64;
+    float acc = 0.f, db = 0.f;
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      float x[32], y[32];
+      tmem_ld32(tb + loff + T_R2 + 32 * part, x);
+      tmem_ld32(tb + loff + T_R3 + 32 * part, y);
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) {
+        const int j = 32 * part + jj;
+        const float gij = j < i ? expf(G[i] - G[j]) : 0.f;
+        const float dA = -x[jj];
+        const float e = bt[i] * gij * dA;
+        const float z = e * y[jj];
+        acc += z;
+        db = fmaf(dA * gij, y[jj], db);
+        Zt[j * 64 + i] += z;
+        *reinterpret_cast<__nv_bfloat16*>(sm + OFF_FE + sw128_offset(64 + i, j)) = __float2bfloat16_rn(e);
+      }
+    }
+    rz[i] += acc;
+    dba[i] = db;
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid < 64) {   // column sums of Z, fixed order
+    float s = 0.f;
+    for (int i = 0; i < 64; ++i) s += Zt[tid * 64 + i];
+    cs[tid] = s;
+  }
+  // ---- R4 = [dQ; dK]
+  if (tid == 0) {
+    const uint32_t i4 = idesc_bf16(128, 128, false, false), i4c = idesc_bf16(128, 128, false, true);
+    const uint32_t i4d = idesc_bf16(128, 128, true, true);
+#pragma unroll
+    for (int ks = 0; ks < 16; ++ks) {   // [scale gamma dO | 0 ; -gamma beta dX | lambda U'] [S0 | dS]^T
+      const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
+      mma_bf16(tb + T_R4, kdesc(sb + OFF_OX + ko), kdesc(sb + OFF_S0 + ko), i4, ks > 0);
+    }
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      // [F; E] K
+      mma_bf16(tb + T_R4, kdesc(sb + OFF_FE + ks * 32), mndesc(sb + OFF_QK + 8192 + ks * 2048, 16384), i4c, 1);
+      // [0; F^T] Q
+      mma_bf16(tb + T_R4, mndesc(sb + OFF_ZERO + ks * 2048, OFF_FE - OFF_ZERO),
+               mndesc(sb + OFF_QK + ks * 2048, 16384), i4d, 1);
+      // [0; E^T] K
+      mma_bf16(tb + T_R4, mndesc(sb + OFF_ZERO + ks * 2048, OFF_FE + 8192 - OFF_ZERO),
+               mndesc(sb + OFF_QK + 8192 + ks * 2048, 16384), i4d, 1);
+    }
+    mma_commit(bar);
+  }
+  if (tid == 0) ok = mbar_wait(bar, 1, kWaitNs);
+  if (__syncthreads_or(!ok)) {
+    if (tid == 0) report(a.dev_status, GDN_DEV_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tb, T_COLS);
+    return;
+  }
+  tc_fence_after();
+  if (warp < 4) {   // [dQ; dK] rows to the per-value-head scratch
+    const int i = row & 63;
+    float* dst = (row < 64 ? ws.dQ : ws.dK) + ((size_t)(t0 + i) * Hv + h) * 128;
+#pragma unroll
+    for (int part = 0; part < 4; ++part) {
+      float x[32];
+      tmem_ld32(tb + loff + T_R4 + 32 * part, x);
+      if (i < L) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          st4(dst + 32 * part + 4 * q, make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]));
+      }
+    }
+  }
+  // ---- dG, dbeta per token, then dg by a suffix sum
+  if (tid < 64) {
+    const int i = tid;
+    const float omega = i < L ? lm[i] * kh3[i] : 0.f;
+    om[i] = omega;
+    dGv[i] = i < L ? a.scale * gm[i] * qh1[i] - bt[i] * gm[i] * kh2[i] - omega + rz[i] - cs[i] : 0.f;
+    if (i < L) b.dbeta[(size_t)(t0 + i) * Hv + h] = xvr[i] - gm[i] * kh2[i] + dba[i];
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    float sdt = 0.f;
+    for (int w = 0; w < kThreads / 32; ++w) sdt += red[w];
+    const float omsum = warp_sum(om[lane] + om[lane + 32]);
+    float x0 = dGv[lane], x1 = dGv[lane + 32];
+    const float extra = gm[L - 1] * sdt + omsum;
+    if (lane == L - 1) x0 += extra;
+    if (lane + 32 == L - 1) x1 += extra;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y0 = __shfl_down_sync(0xffffffffu, x0, o);
+      const float y1 = __shfl_down_sync(0xffffffffu, x1, o);
+      if (lane + o < 32) { x0 += y0; x1 += y1; }
+    }
+    x0 += __shfl_sync(0xffffffffu, x1, 0);
+    const size_t base = (size_t)t0 * Hv + h;
+    if (lane < L) b.dg[base + (size_t)lane * Hv] = x0;
+    if (lane + 32 < L) b.dg[base + (size_t)(lane + 32) * Hv] = x1;
+    tc_fence_after();
+    tmem_dealloc(tb, T_COLS);
+  }
+}
+}  // namespace tcg
+
 // ---------------------------------------------------------------- 6. qk
 // One warp per (token, query/key head), four features per lane: the group sum of the
 // per-value-head dQ, dK in a fixed order, then the L2 norm's Jacobian.  Tokens outside every
 // sequence get zero gradients (dq, dk here; dv, dg, dbeta of the group's value heads too).
 constexpr int kQkThreads = 256;
-
-__device__ __forceinline__ void load4(const void* p, size_t i, int dtype, float (&x)[4]) {
-  if (dtype == GDN_BF16) {
-    const uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(p) + i);
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
-    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
-    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
-  } else {
-    const float4 v = ld4(reinterpret_cast<const float*>(p) + i);
-    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
-  }
-}
-
-__device__ __forceinline__ void store4(void* p, size_t i, int dtype, const float (&x)[4]) {
-  if (dtype == GDN_BF16) {
-    __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]), b = __floats2bfloat162_rn(x[2], x[3]);
-    uint2 u;
-    u.x = *reinterpret_cast<uint32_t*>(&a);
-    u.y = *reinterpret_cast<uint32_t*>(&b);
-    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p) + i) = u;
-  } else {
-    st4(reinterpret_cast<float*>(p) + i, make_float4(x[0], x[1], x[2], x[3]));
-  }
-}
 
 __global__ void __launch_bounds__(kQkThreads) bwd_qk_kernel(const ChunkArgs a, const BwdArgs b,
                                                             BwdWs ws, int T_total) {
@@ -1006,6 +1405,7 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
   if ((err = cudaFuncSetAttribute(bwd_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem))) return err;
   if ((err = cudaFuncSetAttribute(bwd_reverse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRevSmem))) return err;
   if ((err = cudaFuncSetAttribute(bwd_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGradSmem))) return err;
+  if ((err = cudaFuncSetAttribute(tcg::bwd_grad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcg::SMEM))) return err;
   chunk_table_kernel<<<1, 1024, 0, a.stream>>>(a, ws.chunk_off);
   if ((err = cudaGetLastError())) return err;
   // Forward recompute of the state entering every chunk and of U'.  bf16 with K = V = 128:
@@ -1037,7 +1437,11 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
     if ((err = cudaGetLastError())) return err;
   }
   if (NC > 0) {
-    bwd_grad_kernel<<<dim3((unsigned)NC, a.Hv), kGradThreads, kGradSmem, a.stream>>>(a, b, ws);
+    if (tc) {
+      tcg::bwd_grad_tc_kernel<<<dim3((unsigned)NC, a.Hv), tcg::kThreads, tcg::SMEM, a.stream>>>(a, b, ws);
+    } else {
+      bwd_grad_kernel<<<dim3((unsigned)NC, a.Hv), kGradThreads, kGradSmem, a.stream>>>(a, b, ws);
+    }
     if ((err = cudaGetLastError())) return err;
   }
   if (T_total > 0) {

@@ -102,28 +102,40 @@ __device__ __forceinline__ bool locate_chunk(const ChunkArgs& a, const int32_t* 
 
 // Load rows [t0, t0 + L) of a [T, H, D] tensor (head hd) into dst[kChunk][ld] fp32
 // (ld >= D; the first D entries of each row), L2-normalised per row when asked;
-// rows >= L are zero.  Any whole number of warps; needs a __syncthreads after
+// rows >= L are zero.  D <= 128; any whole number of warps, each taking its rows four at a
+// time with every load of the four issued before the norms.  Needs a __syncthreads after
 // return before the tile is read.
 __device__ void load_rows(const void* src, int dtype, int t0, int L, int H, int hd, int D,
                           bool l2, float* dst, int ld) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int r = warp; r < kChunk; r += blockDim.x >> 5) {
-    float* d = dst + r * ld;
-    if (r >= L) {
-      for (int e = lane; e < D; e += 32) d[e] = 0.f;
-      continue;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  for (int r0 = warp; r0 < kChunk; r0 += 4 * nw) {
+    float x[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int r = r0 + u * nw;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int e = lane + 32 * m;
+        x[u][m] = (r < kChunk && r < L && e < D)
+                      ? load_elem(src, ((size_t)(t0 + r) * H + hd) * D + e, dtype) : 0.f;
+      }
     }
-    const size_t base = ((size_t)(t0 + r) * H + hd) * D;
-    float ss = 0.f;
-    for (int e = lane; e < D; e += 32) {
-      const float x = load_elem(src, base + e, dtype);
-      d[e] = x;
-      ss += x * x;
-    }
-    if (l2) {
-      ss = warp_sum(ss);
-      const float rn = 1.0f / sqrtf(ss + kL2Eps);
-      for (int e = lane; e < D; e += 32) d[e] *= rn;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int r = r0 + u * nw;
+      if (r >= kChunk) break;   // uniform over the warp
+      float rn = 1.f;
+      if (l2 && r < L) {
+        float ss = 0.f;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) ss = fmaf(x[u][m], x[u][m], ss);
+        rn = 1.0f / sqrtf(warp_sum(ss) + kL2Eps);
+      }
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int e = lane + 32 * m;
+        if (e < D) dst[r * ld + e] = x[u][m] * rn;
+      }
     }
   }
 }
