@@ -1192,62 +1192,70 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(const ChunkArg
     *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(sm + OFF_U + hlf * 8192 + i * 128 + sw);
     scale8(dst, lm[i]);
   }
-  __syncthreads();   // U' is no longer needed: its space holds Z^T
-  float* Zt = reinterpret_cast<float*>(sm + OFF_U);   // Zt[j * 64 + i] = Z[i][j]
-  // ---- F (rows i < 64 of R2 / R3: warps 0-1), then E (rows 64-127: warps 2-3)
-  if (warp < 2) {
-    const int i = row;
-    float acc = 0.f;
-#pragma unroll
-    for (int part = 0; part < 2; ++part) {
-      float x[32], y[32];
-      tmem_ld32(tb + loff + T_R2 + 32 * part, x);
-      tmem_ld32(tb + loff + T_R3 + 32 * part, y);
+  // ---- F (rows i < 64 of R2 / R3) and E (rows 64-127), all eight warps at once: a warp
+  //      reaches the TMEM lanes 32 (warp % 4) .. + 31 and takes the column half warp / 4
+  {
+    float* rowp = dGv;          // [2 column halves][128 rows] partial row sums of Z (dGv and om
+                                // are free until the last phase)
+    float* colp = reinterpret_cast<float*>(sm + OFF_U);   // [4 row quarters][64] (U' is dead)
+    float* dbp = colp + 256;    // [2][64] partial dbeta terms
+    const int part = warp >> 2;
+    float x[32], y[32], v[32];
+    tmem_ld32(tb + loff + T_R2 + 32 * part, x);   // dO U'^T or dX U'^T
+    tmem_ld32(tb + loff + T_R3 + 32 * part, y);   // Q K^T or K K^T
+    float racc = 0.f, db = 0.f;
+    if (row < 64) {   // F = scale (dO U'^T) * Gamma on and below the diagonal
+      const int i = row;
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) {
         const int j = 32 * part + jj;
         const float f = j <= i ? a.scale * x[jj] * expf(G[i] - G[j]) : 0.f;
-        const float z = f * y[jj];
-        acc += z;
-        Zt[j * 64 + i] = z;
+        v[jj] = f * y[jj];
+        racc += v[jj];
         *reinterpret_cast<__nv_bfloat16*>(sm + OFF_FE + sw128_offset(i, j)) = __float2bfloat16_rn(f);
       }
-    }
-    rz[i] = acc;
-  }
-  __syncthreads();
-  if (warp == 2 || warp == 3) {
-    const int i = row - 64;
-    float acc = 0.f, db = 0.f;
-#pragma unroll
-    for (int part = 0; part < 2; ++part) {
-      float x[32], y[32];
-      tmem_ld32(tb + loff + T_R2 + 32 * part, x);
-      tmem_ld32(tb + loff + T_R3 + 32 * part, y);
+    } else {          // dA = -(dX U'^T) strictly below, E = beta dA * Gamma
+      const int i = row - 64;
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) {
         const int j = 32 * part + jj;
         const float gij = j < i ? expf(G[i] - G[j]) : 0.f;
         const float dA = -x[jj];
         const float e = bt[i] * gij * dA;
-        const float z = e * y[jj];
-        acc += z;
+        v[jj] = e * y[jj];
+        racc += v[jj];
         db = fmaf(dA * gij, y[jj], db);
-        Zt[j * 64 + i] += z;
         *reinterpret_cast<__nv_bfloat16*>(sm + OFF_FE + sw128_offset(64 + i, j)) = __float2bfloat16_rn(e);
       }
+      dbp[part * 64 + i] = db;
     }
-    rz[i] += acc;
-    dba[i] = db;
+    rowp[part * 128 + row] = racc;
+    // column sums over this warp's 32 rows: a transpose-reduce across the lanes (31 shuffles);
+    // lane l ends with the sum of column 32 part + l
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const bool up = (lane & o) != 0;
+#pragma unroll
+      for (int k = 0; k < o; ++k) {
+        const float send = up ? v[k] : v[k + o];
+        const float keep = up ? v[k + o] : v[k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
+    }
+    colp[(warp & 3) * 64 + 32 * part + lane] = v[0];
   }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (tid < 64) {   // column sums of Z, fixed order
-    float s = 0.f;
-    for (int i = 0; i < 64; ++i) s += Zt[tid * 64 + i];
-    cs[tid] = s;
+  if (tid < 64) {   // per-token sums in a fixed order
+    const float* rowp = dGv;
+    const float* colp = reinterpret_cast<const float*>(sm + OFF_U);
+    const float* dbp = colp + 256;
+    const int i = tid;
+    rz[i] = (rowp[i] + rowp[64 + i]) + (rowp[128 + i] + rowp[192 + i]);
+    dba[i] = dbp[i] + dbp[64 + i];
+    cs[i] = (colp[i] + colp[64 + i]) + (colp[128 + i] + colp[192 + i]);
   }
   // ---- R4 = [dQ; dK]
   if (tid == 0) {
