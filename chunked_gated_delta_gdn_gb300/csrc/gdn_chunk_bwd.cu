@@ -1336,6 +1336,262 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(const ChunkArg
 }
 }  // namespace tcg
 
+// T = (I + A)^{-1} for a strictly lower 64 x 64 A (fp32, row stride LDC), in place, by
+// 16 x 16 blocks: D_b = (I + A_bb)^{-1} by substitution on the four diagonal blocks,
+// L = D A_off (block strictly lower, so L^4 = 0), then T = (I - L + L^2 - L^3) D evaluated
+// as D - L (D - L (D - L D)).  All threads of the CTA call it; Dm ([4][16][17]), Lm and Ym
+// ([64][64]) are scratch.  Fixed summation orders: the result is reproducible.
+__device__ void solve_T_blocked(float* At, float* Dm, float* Lm, float* Ym) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  if (tid < 64) {   // D_b, one column per thread
+    const int bb = tid >> 4, jj = tid & 15, base = 16 * bb;
+    float* D = Dm + bb * 16 * 17;
+    for (int ii = 0; ii < 16; ++ii) {
+      float t = ii == jj ? 1.f : 0.f;
+      if (ii > jj) {
+        float acc = 0.f;
+        for (int m = jj; m < ii; ++m) acc = fmaf(At[(base + ii) * LDC + base + m], D[m * 17 + jj], acc);
+        t = -acc;
+      }
+      D[ii * 17 + jj] = t;
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < 64 * 64; e += nt) {   // L = D A_off; X = D
+    const int i = e >> 6, k = e & 63, bi = i >> 4, bk = k >> 4, ii = i & 15;
+    float acc = 0.f;
+    if (bk < bi) {
+      const float* D = Dm + bi * 16 * 17;
+      for (int m = 0; m <= ii; ++m) acc = fmaf(D[ii * 17 + m], At[(16 * bi + m) * LDC + k], acc);
+    }
+    Lm[e] = acc;
+    Ym[e] = bk == bi ? Dm[bi * 16 * 17 + ii * 17 + (k & 15)] : 0.f;
+  }
+  __syncthreads();
+  for (int it = 0; it < 3; ++it) {   // X <- D - L X, ping-ponging between Ym and At
+    const float* X = (it & 1) ? At : Ym;
+    const bool to_at = (it & 1) == 0;
+    for (int e = tid; e < 64 * 64; e += nt) {
+      const int i = e >> 6, j = e & 63, bi = i >> 4, bj = j >> 4;
+      float acc = bi == bj ? Dm[bi * 16 * 17 + (i & 15) * 17 + (j & 15)] : 0.f;
+      if (bj < bi) {
+        float s = 0.f;
+        for (int m = 16 * bj; m < 16 * bi; ++m)
+          s = fmaf(Lm[i * 64 + m], to_at ? X[m * 64 + j] : X[m * LDC + j], s);
+        acc -= s;
+      }
+      if (to_at) At[i * LDC + j] = acc; else Ym[i * 64 + j] = acc;
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------- 3b. prep on the tensor cores
+// bf16 I/O with K = V = 128: the same outputs as bwd_prep_kernel (T, dUp, Z, G) with the
+// products on tcgen05 (bf16 operands, fp32 accumulators in TMEM):
+//   [Q K^T; K K^T] = [q; k] k^T           M=128 N=64  K=128  -> P (bf16) and A (fp32)
+//   Z   = Q^T diag(gamma) dO               M=128 N=128 K=64   (A: q rows as an MN-major operand)
+//   dUp = [P^T; 0] dO                      M=128 N=128 K=64   (A: P as stored, MN-major, over a
+//                                                              zero tile for rows 64-127)
+// then T = (I + A)^{-1} in fp32 by 16 x 16 blocks.  256 TMEM columns and ~98 KB of shared
+// memory: two CTAs per SM.
+namespace tcp {
+using namespace sm100;
+using tcg::put4;
+using tcg::kdesc;
+using tcg::mndesc;
+constexpr int kThreads = 256;
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint32_t OFF_QK = 0;         // [q; k] rows, 2 k-halves x 128 rows x 128 B
+constexpr uint32_t OFF_DO = 32768;     // dO rows i: 2 c-halves x 64 rows x 128 B
+constexpr uint32_t OFF_DG = 49152;     // diag(gamma) dO, same layout
+constexpr uint32_t OFF_P = 65536;      // P rows i, 64 j per row (bf16)
+constexpr uint32_t OFF_ZERO = 73728;   // 64 rows x 128 B of zeros
+constexpr uint32_t OFF_A = 81920;      // A, then T, fp32 [64][LDC]
+constexpr uint32_t OFF_VEC = OFF_A + 64 * LDC * 4;   // G, beta, gamma
+constexpr uint32_t OFF_BAR = OFF_VEC + 3 * 64 * 4;
+constexpr uint32_t SMEM = OFF_BAR + 64 + 1024;
+constexpr uint32_t T_QK = 0, T_Z = 0, T_UP = 128, T_COLS = 256;
+
+__global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(const ChunkArgs a, const BwdArgs b,
+                                                                  BwdWs ws) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sb = smem_u32(sm);
+  float* At = reinterpret_cast<float*>(sm + OFF_A);
+  float* G = reinterpret_cast<float*>(sm + OFF_VEC);
+  float* bt = G + 64;
+  float* gm = G + 128;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 8);
+  const int c = blockIdx.x, h = blockIdx.y;
+  int n, t0, L;
+  if (!locate_chunk(a, ws.chunk_off, c, &n, &t0, &L)) return;
+  const int Hv = a.Hv, hq = h / (Hv / a.Hqk);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const size_t ch = (size_t)c * Hv + h;
+  const bool l2 = a.use_qk_l2norm != 0;
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tslot, T_COLS);
+    tmem_relinquish();
+  }
+  load_gates(a, t0, L, h, G, bt);
+  {  // normalised [q; k] rows and dO rows (bf16), every load of a thread issued first
+    float x[16][4], o[8][4];
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+      const int r = warp + 8 * s, i = r & 63;
+      x[s][0] = x[s][1] = x[s][2] = x[s][3] = 0.f;
+      if (i < L) load4(r < 64 ? a.q : a.k, ((size_t)(t0 + i) * a.Hqk + hq) * 128 + 4 * lane, a.io_dtype, x[s]);
+    }
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      const int i = warp + 8 * s;
+      o[s][0] = o[s][1] = o[s][2] = o[s][3] = 0.f;
+      if (i < L) load4(b.d_o, ((size_t)(t0 + i) * Hv + h) * 128 + 4 * lane, a.io_dtype, o[s]);
+    }
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+      float rn = 1.f;
+      if (l2)
+        rn = 1.0f / sqrtf(warp_sum(x[s][0] * x[s][0] + x[s][1] * x[s][1] + x[s][2] * x[s][2] +
+                                   x[s][3] * x[s][3]) + kL2Eps);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) x[s][q] *= rn;
+      put4(sm + OFF_QK, 16384, warp + 8 * s, 4 * lane, x[s]);
+    }
+#pragma unroll
+    for (int s = 0; s < 8; ++s) put4(sm + OFF_DO, 8192, warp + 8 * s, 4 * lane, o[s]);
+  }
+  for (int e = tid; e < 8192 / 16; e += kThreads)
+    reinterpret_cast<uint4*>(sm + OFF_ZERO)[e] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = *tslot;
+  if (tid == 0) {   // [Q K^T; K K^T]
+    const uint32_t id = idesc_bf16(128, 64, false, false);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
+      mma_bf16(tb + T_QK, kdesc(sb + OFF_QK + ko), kdesc(sb + OFF_QK + 8192 + ko), id, ks > 0);
+    }
+    mma_commit(bar);
+  }
+  if (tid < 64) gm[tid] = expf(G[tid]);
+  __syncthreads();
+  // diag(gamma) dO while the product runs: 64 rows x 16 chunks of 8 bf16
+  for (int e = tid; e < 64 * 16; e += kThreads) {
+    const int i = e >> 4, chunk = e & 15, hlf = chunk >> 3, c8 = chunk & 7;
+    const uint32_t off = hlf * 8192 + i * 128 + ((c8 ^ (i & 7)) << 4);
+    *reinterpret_cast<uint4*>(sm + OFF_DG + off) = *reinterpret_cast<const uint4*>(sm + OFF_DO + off);
+    tcg::scale8(sm + OFF_DG + off, gm[i]);
+  }
+  bool ok = true;
+  if (tid == 0) ok = mbar_wait(bar, 0, kWaitNs);
+  if (__syncthreads_or(!ok)) {
+    if (tid == 0) report(a.dev_status, GDN_DEV_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tb, T_COLS);
+    return;
+  }
+  tc_fence_after();
+  const uint32_t loff = (uint32_t)(32 * (warp & 3)) << 16;
+  const int row = 32 * (warp & 3) + lane;
+  if (warp < 4) {   // P (rows 0-63, bf16) and A (rows 64-127, fp32), half the columns each pass
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      float x[32];
+      tmem_ld32(tb + loff + T_QK + 32 * part, x);
+      if (row < 64) {
+        const int i = row;
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int j = 32 * part + jj;
+          const float p = j <= i ? x[jj] * expf(G[i] - G[j]) : 0.f;
+          *reinterpret_cast<__nv_bfloat16*>(sm + OFF_P + sw128_offset(i, j)) = __float2bfloat16_rn(p);
+        }
+      } else {
+        const int i = row - 64;
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int j = 32 * part + jj;
+          At[i * LDC + j] = j < i ? bt[i] * x[jj] * expf(G[i] - G[j]) : 0.f;
+        }
+      }
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0) {   // Z = (Q^T) (diag(gamma) dO);  dUp = [P^T; 0] dO
+    const uint32_t id = idesc_bf16(128, 128, true, true);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      mma_bf16(tb + T_Z, mndesc(sb + OFF_QK + ks * 2048, 16384), mndesc(sb + OFF_DG + ks * 2048, 8192),
+               id, ks > 0);
+      mma_bf16(tb + T_UP, mndesc(sb + OFF_P + ks * 2048, OFF_ZERO - OFF_P),
+               mndesc(sb + OFF_DO + ks * 2048, 8192), id, ks > 0);
+    }
+    mma_commit(bar);
+  }
+  if (tid == 0) ok = mbar_wait(bar, 1, kWaitNs);
+  if (__syncthreads_or(!ok)) {
+    if (tid == 0) report(a.dev_status, GDN_DEV_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tb, T_COLS);
+    return;
+  }
+  tc_fence_after();
+  {  // Z rows d (all 128 lanes), dUp rows j < 64; warps w and w + 4 split the columns
+    const int part = warp >> 2;
+    float* Zg = ws.Z + ch * 128 * 128 + (size_t)row * 128 + 64 * part;
+#pragma unroll
+    for (int q2 = 0; q2 < 2; ++q2) {
+      float x[32];
+      tmem_ld32(tb + loff + T_Z + 64 * part + 32 * q2, x);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        st4(Zg + 32 * q2 + 4 * q, make_float4(a.scale * x[4 * q], a.scale * x[4 * q + 1],
+                                              a.scale * x[4 * q + 2], a.scale * x[4 * q + 3]));
+    }
+    if (row < 64) {
+      float* Ug = ws.dUp + ch * 64 * 128 + (size_t)row * 128 + 64 * part;
+#pragma unroll
+      for (int q2 = 0; q2 < 2; ++q2) {
+        float x[32];
+        tmem_ld32(tb + loff + T_UP + 64 * part + 32 * q2, x);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          st4(Ug + 32 * q2 + 4 * q, make_float4(a.scale * x[4 * q], a.scale * x[4 * q + 1],
+                                                a.scale * x[4 * q + 2], a.scale * x[4 * q + 3]));
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();   // the products are done with every tile: they serve as the solve's scratch
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tb, T_COLS);
+  }
+  solve_T_blocked(At, reinterpret_cast<float*>(sm + OFF_P), reinterpret_cast<float*>(sm + OFF_QK),
+                  reinterpret_cast<float*>(sm + OFF_DO));
+  for (int e = tid; e < 64 * 64; e += kThreads) {
+    const int i = e >> 6, j = e & 63;
+    ws.T[ch * 64 * 64 + e] = At[i * LDC + j];
+  }
+  if (tid < 64) ws.G[ch * 64 + tid] = G[tid];
+}
+}  // namespace tcp
+
 // ---------------------------------------------------------------- 6. qk
 // One warp per (token, query/key head), four features per lane: the group sum of the
 // per-value-head dQ, dK in a fixed order, then the L2 norm's Jacobian.  Tokens outside every
@@ -1414,6 +1670,7 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
   if ((err = cudaFuncSetAttribute(bwd_reverse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRevSmem))) return err;
   if ((err = cudaFuncSetAttribute(bwd_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGradSmem))) return err;
   if ((err = cudaFuncSetAttribute(tcg::bwd_grad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcg::SMEM))) return err;
+  if ((err = cudaFuncSetAttribute(tcp::bwd_prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcp::SMEM))) return err;
   chunk_table_kernel<<<1, 1024, 0, a.stream>>>(a, ws.chunk_off);
   if ((err = cudaGetLastError())) return err;
   // Forward recompute of the state entering every chunk and of U'.  bf16 with K = V = 128:
@@ -1434,7 +1691,10 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
     if ((err = launch_chunk_states(a, ws.chunk_off, ws.W, ws.U, ws.G, ws.S))) return err;
   }
   if (NC > 0) {
-    bwd_prep_kernel<<<dim3((unsigned)NC, a.Hv), kPrepThreads, kPrepSmem, a.stream>>>(a, b, ws);
+    if (tc)
+      tcp::bwd_prep_tc_kernel<<<dim3((unsigned)NC, a.Hv), tcp::kThreads, tcp::SMEM, a.stream>>>(a, b, ws);
+    else
+      bwd_prep_kernel<<<dim3((unsigned)NC, a.Hv), kPrepThreads, kPrepSmem, a.stream>>>(a, b, ws);
     if ((err = cudaGetLastError())) return err;
   }
   const unsigned vtiles = (unsigned)((a.V + VT - 1) / VT);
