@@ -62,6 +62,7 @@ struct BwdWs {
   float* dS;           // [NC][Hv][K][V]  gradient of the chunk's exit state
   float* dX;           // [NC][Hv][C][V]
   float* Z;            // [NC][Hv][K][V]  scale Q^T diag(gamma) dO
+  float* XV;           // [NC][Hv][4][C]  partial row dots dX_i . v_i per 32-column slice
   float* dQ;           // [T_total][Hv][K] per value head, before the norm
   float* dK;           // [T_total][Hv][K]
 };
@@ -89,6 +90,7 @@ __host__ __device__ inline BwdWs bwd_layout(void* base, long long NC, int N, int
   w.dS = reinterpret_cast<float*>(take(f * ch * K * V));
   w.dX = reinterpret_cast<float*>(take(f * ch * C * V));
   w.Z = reinterpret_cast<float*>(take(f * ch * K * V));
+  w.XV = reinterpret_cast<float*>(take(f * ch * 4 * C));
   w.dQ = reinterpret_cast<float*>(take(f * (size_t)T_total * Hv * K));
   w.dK = reinterpret_cast<float*>(take(f * (size_t)T_total * Hv * K));
   if (total) *total = off;
@@ -174,6 +176,10 @@ constexpr int kBarT = 1;          // named barrier of the two warps that build T
 
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ uint32_t tcg_pack2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
 
 __device__ __forceinline__ void load4(const void* p, size_t i, int dtype, float (&x)[4]) {
   if (dtype == GDN_BF16) {
@@ -354,6 +360,11 @@ constexpr int KLD = KP + 4;   // [C][KLD]: k rows, float4 reads
 constexpr int TLD = C + 2;    // [KP][TLD]: k transposed, float2 reads
 constexpr size_t kRevSmem = sizeof(float) * (C * KLD + KP * TLD + KP * VT + 2 * C * VT + 2 * C);
 
+// kTiles: dS and dX go out as the bf16 operand tiles of the tensor-core grad pass (K-major,
+// 128-byte swizzled, dv along the rows in two 64-element halves) instead of fp32 [K][V] /
+// [C][V].  Either way the pass also writes dv = diag(beta) dX and the per-slice partial row
+// dots dX_i . v_i.
+template <bool kTiles>
 __global__ void __launch_bounds__(kRevThreads, 2) bwd_reverse_kernel(const ChunkArgs a,
                                                                      const BwdArgs b, BwdWs ws) {
   extern __shared__ float smem[];
@@ -401,11 +412,23 @@ __global__ void __launch_bounds__(kRevThreads, 2) bwd_reverse_kernel(const Chunk
     const size_t ch = (size_t)(first + qc) * a.Hv + h;
     __syncthreads();  // the previous chunk is done with every tile
     if (colok) {      // record dS, the gradient of this chunk's exit state
-      float* dSg = ws.dS + ch * K * V;
+      if (kTiles) {
+        uint8_t* t = reinterpret_cast<uint8_t*>(ws.dS + ch * K * V) + (col >> 6) * 16384 + (col & 7) * 2;
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
-        if (4 * ty + r < K)
-          st4(dSg + (size_t)(4 * ty + r) * V + col, make_float4(s[r][0], s[r][1], s[r][2], s[r][3]));
+        for (int r = 0; r < 4; ++r) {
+          const int d = 4 * ty + r;
+          uint2 u;
+          u.x = tcg_pack2(s[r][0], s[r][1]);
+          u.y = tcg_pack2(s[r][2], s[r][3]);
+          *reinterpret_cast<uint2*>(t + d * 128 + ((((col & 63) >> 3) ^ (d & 7)) << 4)) = u;
+        }
+      } else {
+        float* dSg = ws.dS + ch * K * V;
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+          if (4 * ty + r < K)
+            st4(dSg + (size_t)(4 * ty + r) * V + col, make_float4(s[r][0], s[r][1], s[r][2], s[r][3]));
+      }
     }
     // normalised k rows into Kn and Kt (warp w: rows w + 8 s; every load issued first)
     {
@@ -502,7 +525,32 @@ __global__ void __launch_bounds__(kRevThreads, 2) bwd_reverse_kernel(const Chunk
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const int i = 2 * ty + r;
-        if (colok) st4(dXg + (size_t)i * V + col, make_float4(x[r][0], x[r][1], x[r][2], x[r][3]));
+        float xv = 0.f;
+        if (colok) {
+          if (kTiles) {
+            uint2 u;
+            u.x = tcg_pack2(x[r][0], x[r][1]);
+            u.y = tcg_pack2(x[r][2], x[r][3]);
+            *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(dXg) + (col >> 6) * 8192 + i * 128 +
+                                      ((((col & 63) >> 3) ^ (i & 7)) << 4) + (col & 7) * 2) = u;
+          } else {
+            st4(dXg + (size_t)i * V + col, make_float4(x[r][0], x[r][1], x[r][2], x[r][3]));
+          }
+          if (i < L) {   // dv = beta dX; partial dX . v over this thread's four columns
+            const size_t tv = ((size_t)(t0 + i) * a.Hv + h) * V + col;
+            const float bi = bt[i];
+            const float dv4[4] = {bi * x[r][0], bi * x[r][1], bi * x[r][2], bi * x[r][3]};
+            store4(b.dv, tv, a.io_dtype, dv4);
+            float v4[4];
+            load4(a.v, tv, a.io_dtype, v4);
+            xv = x[r][0] * v4[0] + x[r][1] * v4[1] + x[r][2] * v4[2] + x[r][3] * v4[3];
+          }
+        }
+        // the eight threads of a row (tx = lane % 8) add their partials in a fixed order
+        xv += __shfl_xor_sync(0xffffffffu, xv, 1);
+        xv += __shfl_xor_sync(0xffffffffu, xv, 2);
+        xv += __shfl_xor_sync(0xffffffffu, xv, 4);
+        if (tx == 0) ws.XV[(ch * 4 + (size_t)(c0 / VT)) * C + i] = xv;
         const float w = -expf(G[i]) * bt[i];
         st4(X2 + i * VT + 4 * tx, make_float4(w * x[r][0], w * x[r][1], w * x[r][2], w * x[r][3]));
       }
@@ -646,7 +694,7 @@ __global__ void __launch_bounds__(kGradThreads) bwd_grad_kernel(const ChunkArgs 
   zero(H3);
   zero(OU);
   zero(XU);
-  float sd = 0.f, xv = 0.f;
+  float sd = 0.f;
   const float* Sg = ws.S + ch * K * V;
   const float* dSg = ws.dS + ch * K * V;
   const float* Ug = ws.U + ch * C * V;
@@ -675,21 +723,13 @@ __global__ void __launch_bounds__(kGradThreads) bwd_grad_kernel(const ChunkArgs 
       const int cc = 4 * cg;
       const bool ok = i < L && c0 + cc < V;
       const size_t tv = ((size_t)(t0 + i) * a.Hv + h) * V + c0 + cc;
-      float o4[4] = {0.f, 0.f, 0.f, 0.f}, v4[4] = {0.f, 0.f, 0.f, 0.f};
+      float o4[4] = {0.f, 0.f, 0.f, 0.f};
       float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f), u4 = x4;
       if (ok) {
         x4 = ld4(dXg + (size_t)i * V + c0 + cc);
         u4 = ld4(Ug + (size_t)i * V + c0 + cc);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          o4[q] = load_elem(b.d_o, tv + q, a.io_dtype);
-          v4[q] = load_elem(a.v, tv + q, a.io_dtype);
-        }
-        const float bi = bt[i];
-        store_elem(b.dv, tv + 0, bi * x4.x, a.io_dtype);
-        store_elem(b.dv, tv + 1, bi * x4.y, a.io_dtype);
-        store_elem(b.dv, tv + 2, bi * x4.z, a.io_dtype);
-        store_elem(b.dv, tv + 3, bi * x4.w, a.io_dtype);
+        for (int q = 0; q < 4; ++q) o4[q] = load_elem(b.d_o, tv + q, a.io_dtype);
       }
       const float x[4] = {x4.x, x4.y, x4.z, x4.w}, u[4] = {u4.x, u4.y, u4.z, u4.w};
 #pragma unroll
@@ -697,7 +737,6 @@ __global__ void __launch_bounds__(kGradThreads) bwd_grad_kernel(const ChunkArgs 
         dOT[(cc + q) * RLD + i] = o4[q];
         dXT[(cc + q) * RLD + i] = x[q];
         UT[(cc + q) * RLD + i] = u[q];
-        xv = fmaf(x[q], v4[q], xv);
       }
     }
     __syncthreads();
@@ -899,9 +938,6 @@ __global__ void __launch_bounds__(kGradThreads) bwd_grad_kernel(const ChunkArgs 
   // ---- dG, dbeta per token (threads < C hold the row dots), then dg by a suffix sum
   float* dGv = Fs;    // [C] (phase C reads of F / E are done after the barrier)
   float* omv = Fs + C;
-  float* xvs = Fs + 2 * C;   // [8][C] xv partials
-  __syncthreads();
-  xvs[(tid >> 6) * C + (tid & 63)] = xv;
   __syncthreads();
   if (tid < C) {
     const int i = tid;
@@ -911,7 +947,7 @@ __global__ void __launch_bounds__(kGradThreads) bwd_grad_kernel(const ChunkArgs 
       csum += colp[g * C + i];
       db += dbp[g * C + i];
     }
-    for (int g = 0; g < 8; ++g) x += xvs[g * C + i];
+    for (int g = 0; g < (V + VT - 1) / VT; ++g) x += ws.XV[(ch * 4 + g) * C + i];
     const float omega = i < L ? lm[i] * kh3_i : 0.f;
     omv[i] = omega;
     dGv[i] = i < L ? a.scale * gm[i] * qh1_i - bt[i] * gm[i] * kh2_i - omega + rsum - csum : 0.f;
@@ -1012,7 +1048,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(const ChunkArg
   float* dba = vec + 512;      float* cs = vec + 576;   float* xvr = vec + 640; float* red = vec + 704;
   float* dGv = vec + 768;      float* om = vec + 832;
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 8);
+  uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + OFF_BAR + 8);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 16);
   const int c = blockIdx.x, h = blockIdx.y;
   int n, t0, L;
   if (!locate_chunk(a, ws.chunk_off, c, &n, &t0, &L)) return;
@@ -1022,7 +1059,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(const ChunkArg
   const bool l2 = a.use_qk_l2norm != 0;
   if (tid == 0) {
     mbar_init(bar, 1);
+    mbar_init(bar_ld, 1);
     fence_mbar_init();
+    // the operand tiles the producers wrote: S0, dS (32 KB each), U' (16 KB), and the two
+    // 8 KB halves of dX into rows 64-127 of [dO; dX]
+    const uint8_t* s0 = reinterpret_cast<const uint8_t*>(ws.S + ch * 128 * 128);
+    const uint8_t* ds = reinterpret_cast<const uint8_t*>(ws.dS + ch * 128 * 128);
+    const uint8_t* ug = reinterpret_cast<const uint8_t*>(ws.U + ch * 64 * 128);
+    const uint8_t* xg = reinterpret_cast<const uint8_t*>(ws.dX + ch * 64 * 128);
+    mbar_arrive_expect_tx(bar_ld, 32768 + 32768 + 16384 + 16384);
+    bulk_load(sm + OFF_S0, s0, 32768, bar_ld);
+    bulk_load(sm + OFF_DS, ds, 32768, bar_ld);
+    bulk_load(sm + OFF_U, ug, 16384, bar_ld);
+    bulk_load(sm + OFF_OX + 8192, xg, 8192, bar_ld);
+    bulk_load(sm + OFF_OX + 16384 + 8192, xg + 8192, 8192, bar_ld);
   }
   if (warp == 0) {
     tmem_alloc(tslot, T_COLS);
@@ -1052,67 +1102,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(const ChunkArg
       put4(sm + OFF_QK, 16384, warp + 8 * s, 4 * lane, x[s]);
     }
   }
-  float sd = 0.f;
-  {  // S0, dS rows d (bf16), 8 float4 pairs per batch
-    const float* Sg = ws.S + ch * 128 * 128;
-    const float* dSg = ws.dS + ch * 128 * 128;
-#pragma unroll 1
-    for (int base = 0; base < 16; base += 8) {
-      float4 s0[8], ds[8];
+  {  // dO rows i (bf16) into rows 0-63 of [dO; dX]
+    float o4[8][4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int e = tid + kThreads * (base + u), d = e >> 5, col = 4 * (e & 31);
-        s0[u] = ld4(Sg + d * 128 + col);
-        ds[u] = ld4(dSg + d * 128 + col);
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int e = tid + kThreads * (base + u), d = e >> 5, col = 4 * (e & 31);
-        const float xs[4] = {s0[u].x, s0[u].y, s0[u].z, s0[u].w};
-        const float xd[4] = {ds[u].x, ds[u].y, ds[u].z, ds[u].w};
-        put4(sm + OFF_S0, 16384, d, col, xs);
-        put4(sm + OFF_DS, 16384, d, col, xd);
-        sd += s0[u].x * ds[u].x + s0[u].y * ds[u].y + s0[u].z * ds[u].z + s0[u].w * ds[u].w;
-      }
+    for (int s8 = 0; s8 < 8; ++s8) {
+      const int i = warp + 8 * s8;
+      o4[s8][0] = o4[s8][1] = o4[s8][2] = o4[s8][3] = 0.f;
+      if (i < L) load4(b.d_o, ((size_t)(t0 + i) * Hv + h) * 128 + 4 * lane, a.io_dtype, o4[s8]);
     }
+#pragma unroll
+    for (int s8 = 0; s8 < 8; ++s8) put4(sm + OFF_OX, 16384, warp + 8 * s8, 4 * lane, o4[s8]);
   }
-  {  // dO, dX, U' rows i (one row per warp and trip), 4 trips per batch; dv; dX . v
-    const float* Ug = ws.U + ch * 64 * 128;
-    const float* dXg = ws.dX + ch * 64 * 128;
-    const int col = 4 * lane;
-#pragma unroll 1
-    for (int base = 0; base < 8; base += 4) {
-      float o4[4][4], v4[4][4], x4[4][4], u4[4][4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = warp + 8 * (base + u);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) o4[u][q] = v4[u][q] = x4[u][q] = u4[u][q] = 0.f;
-        if (i < L) {
-          const size_t tv = ((size_t)(t0 + i) * Hv + h) * 128 + col;
-          load4(b.d_o, tv, a.io_dtype, o4[u]);
-          load4(a.v, tv, a.io_dtype, v4[u]);
-          const float4 xx = ld4(dXg + i * 128 + col), uu = ld4(Ug + i * 128 + col);
-          x4[u][0] = xx.x; x4[u][1] = xx.y; x4[u][2] = xx.z; x4[u][3] = xx.w;
-          u4[u][0] = uu.x; u4[u][1] = uu.y; u4[u][2] = uu.z; u4[u][3] = uu.w;
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = warp + 8 * (base + u);
-        if (i < L) {
-          const float bi = bt[i];
-          const float dv4[4] = {bi * x4[u][0], bi * x4[u][1], bi * x4[u][2], bi * x4[u][3]};
-          store4(b.dv, ((size_t)(t0 + i) * Hv + h) * 128 + col, a.io_dtype, dv4);
-        }
-        put4(sm + OFF_OX, 16384, i, col, o4[u]);
-        put4(sm + OFF_OX, 16384, 64 + i, col, x4[u]);
-        put4(sm + OFF_U, 8192, i, col, u4[u]);
-        const float xv = warp_sum(x4[u][0] * v4[u][0] + x4[u][1] * v4[u][1] + x4[u][2] * v4[u][2] +
-                                  x4[u][3] * v4[u][3]);
-        if (lane == 0) xvr[i] = xv;
-      }
-    }
+  if (tid < 64) {   // the row dots dX_i . v_i, from the reverse pass's per-slice partials
+    const float* xp = ws.XV + ch * 4 * 64;
+    xvr[tid] = (xp[tid] + xp[64 + tid]) + (xp[128 + tid] + xp[192 + tid]);
   }
   for (int e = tid; e < 8192 / 16; e += kThreads)      // the zero tile
     reinterpret_cast<uint4*>(sm + OFF_ZERO)[e] = make_uint4(0u, 0u, 0u, 0u);
@@ -1120,14 +1123,37 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(const ChunkArg
     const int hlf = e / (8192 / 16), w = e - hlf * (8192 / 16);
     reinterpret_cast<uint4*>(sm + OFF_LU + hlf * 16384)[w] = make_uint4(0u, 0u, 0u, 0u);
   }
-  sd = warp_sum(sd);
-  if (lane == 0) red[warp] = sd;
   fence_proxy_async_smem();
+  bool ok = true;
+  if (tid == 0) ok = mbar_wait(bar_ld, 0, kWaitNs);   // the bulk copies have landed
   tc_fence_before();
-  __syncthreads();
+  if (__syncthreads_or(!ok)) {
+    if (tid == 0) report(a.dev_status, GDN_DEV_TIMEOUT);
+    if (warp == 0) {
+      tc_fence_after();
+      tmem_dealloc(*tslot, T_COLS);
+    }
+    return;
+  }
   tc_fence_after();
   const uint32_t tb = *tslot;
-  bool ok = true;
+  {  // <S0, dS> over the two tiles (same layout, element by element)
+    float sd = 0.f;
+    const uint4* p0 = reinterpret_cast<const uint4*>(sm + OFF_S0);
+    const uint4* p1 = reinterpret_cast<const uint4*>(sm + OFF_DS);
+    for (int e = tid; e < 32768 / 16; e += kThreads) {
+      const uint4 u0 = p0[e], u1 = p1[e];
+      const uint32_t w0[4] = {u0.x, u0.y, u0.z, u0.w}, w1[4] = {u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w0[q]));
+        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w1[q]));
+        sd = fmaf(f0.x, f1.x, fmaf(f0.y, f1.y, sd));
+      }
+    }
+    sd = warp_sum(sd);
+    if (lane == 0) red[warp] = sd;
+  }
   // ---- R1, R2, R3
   if (tid == 0) {
     const uint32_t i1 = idesc_bf16(128, 256, false, true), i2 = idesc_bf16(128, 64, false, false);
@@ -1667,7 +1693,8 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
   BwdWs ws = bwd_layout(a.workspace, NC, a.num_seqs, a.Hv, a.K, a.V, T_total, nullptr);
   cudaError_t err;
   if ((err = cudaFuncSetAttribute(bwd_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem))) return err;
-  if ((err = cudaFuncSetAttribute(bwd_reverse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRevSmem))) return err;
+  if ((err = cudaFuncSetAttribute(bwd_reverse_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRevSmem))) return err;
+  if ((err = cudaFuncSetAttribute(bwd_reverse_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRevSmem))) return err;
   if ((err = cudaFuncSetAttribute(bwd_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGradSmem))) return err;
   if ((err = cudaFuncSetAttribute(tcg::bwd_grad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcg::SMEM))) return err;
   if ((err = cudaFuncSetAttribute(tcp::bwd_prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcp::SMEM))) return err;
@@ -1701,7 +1728,10 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
   if (a.num_seqs > 0) {
     const long long blocks = (long long)vtiles * a.Hv * a.num_seqs;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    bwd_reverse_kernel<<<(unsigned)blocks, kRevThreads, kRevSmem, a.stream>>>(a, b, ws);
+    if (tc)
+      bwd_reverse_kernel<true><<<(unsigned)blocks, kRevThreads, kRevSmem, a.stream>>>(a, b, ws);
+    else
+      bwd_reverse_kernel<false><<<(unsigned)blocks, kRevThreads, kRevSmem, a.stream>>>(a, b, ws);
     if ((err = cudaGetLastError())) return err;
   }
   if (NC > 0) {

@@ -549,11 +549,16 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
       }
     }
     // ---- S (entry state) -> bf16 S^T in the O2 columns (the next product's A operand);
-    //      S <- exp(G_last) S in TMEM.  Record mode also stores the fp32 entry state.
+    //      S <- exp(G_last) S in TMEM.  Record mode also stores the entry state as a bf16
+    //      tile: rows dk, 64 dv per 128-byte row in two halves, 128-byte swizzled (element
+    //      (dk, dv) at (dv / 64) 16384 + dk 128 + ((dv % 64 / 8) xor (dk % 8)) 16 + (dv % 8) 2)
     {
       const float dl = ex2(vec[VEC_G + L - 1]);
-      float* rec_s = kRecord ? a.rec_states + ((size_t)(rec0 + c) * a.Hv + h) * (size_t)(DK * DV) + row
-                             : nullptr;
+      uint8_t* rec_s = kRecord ? reinterpret_cast<uint8_t*>(a.rec_states +
+                                                            ((size_t)(rec0 + c) * a.Hv + h) * (size_t)(DK * DV)) +
+                                     (row >> 6) * 16384 + (row & 7) * 2
+                               : nullptr;
+      const uint32_t sx = (uint32_t)((row & 63) >> 3) << 4;   // swizzle: sx xor ((dk % 8) 16)
 #pragma unroll
       for (int pair = 0; pair < 2; ++pair) {
         float pk[32];
@@ -564,7 +569,11 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
           tmem_ld32(tbase + lane_off + col, x);
           if (kRecord) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) rec_s[(size_t)(32 * (2 * pair + sub) + j) * DV] = x[j];
+            for (int j = 0; j < 32; ++j) {
+              const int dk = 32 * (2 * pair + sub) + j;   // dk % 8 == j % 8
+              *reinterpret_cast<__nv_bfloat16*>(rec_s + dk * 128 + (sx ^ ((j & 7) << 4))) =
+                  __float2bfloat16_rn(x[j]);
+            }
           }
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
@@ -681,17 +690,23 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     tc_fence_after();
 
     // ---- U'^T -> bf16, packed into the first 32 of its own TMEM columns (A operand);
-    //      record mode stores the fp32 U' rows of the chunk's tokens
+    //      record mode stores U' as a bf16 tile: rows = the chunk's 64 tokens (zero from L on),
+    //      64 dv per 128-byte row in two halves of 8 KB, 128-byte swizzled
     {
       float x[32], y[32], pk[32];
       tmem_ld32(tbase + lane_off + COL_U, x);
       tmem_ld32(tbase + lane_off + COL_U + 32, y);
       if (kRecord) {
-        float* ru = a.rec_u + ((size_t)(rec0 + c) * a.Hv + h) * (size_t)(kChunk * DV) + row;
+        uint8_t* ru = reinterpret_cast<uint8_t*>(a.rec_u + ((size_t)(rec0 + c) * a.Hv + h) *
+                                                               (size_t)(kChunk * DV)) +
+                      (row >> 6) * 8192 + (row & 7) * 2;
+        const uint32_t sx = (uint32_t)((row & 63) >> 3) << 4;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          if (j < L) ru[(size_t)j * DV] = x[j];
-          if (j + 32 < L) ru[(size_t)(j + 32) * DV] = y[j];
+          *reinterpret_cast<__nv_bfloat16*>(ru + j * 128 + (sx ^ ((j & 7) << 4))) =
+              __float2bfloat16_rn(j < L ? x[j] : 0.f);
+          *reinterpret_cast<__nv_bfloat16*>(ru + (j + 32) * 128 + (sx ^ ((j & 7) << 4))) =
+              __float2bfloat16_rn(j + 32 < L ? y[j] : 0.f);
         }
       }
 #pragma unroll

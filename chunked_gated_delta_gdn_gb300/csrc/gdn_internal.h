@@ -47,8 +47,10 @@ struct ChunkArgs {
   cudaStream_t stream;
   GateArgs gates;
   // Record mode of the tensor-core kernel (the backward's forward recompute): when set, the
-  // state entering every chunk goes to rec_states [NC][Hv][K][V] and U' (rows < L) to
-  // rec_u [NC][Hv][64][V], chunk numbering from the device chunk table rec_chunk_off.
+  // state entering every chunk and U' go out as bf16 operand tiles of the backward's
+  // tensor-core grad pass (128-byte swizzled, K-major: rows dk resp. tokens, dv along the
+  // rows in two 64-element halves), one per chunk and head in slots of K V resp. 64 V floats
+  // of rec_states / rec_u; chunk numbering from the device chunk table rec_chunk_off.
   float* rec_states = nullptr;
   float* rec_u = nullptr;
   const int32_t* rec_chunk_off = nullptr;
