@@ -181,6 +181,14 @@ __device__ __forceinline__ uint32_t tcg_pack2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Four bf16 at element i (i % 4 == 0) through the read-only path, as fp32.
+__device__ __forceinline__ void load4b(const void* p, size_t i, float (&x)[4]) {
+  const uint2 u = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(p) + i));
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+}
+
 __device__ __forceinline__ void load4(const void* p, size_t i, int dtype, float (&x)[4]) {
   if (dtype == GDN_BF16) {
     const uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(p) + i);
@@ -436,10 +444,15 @@ __global__ void __launch_bounds__(kRevThreads, 2) bwd_reverse_kernel(const Chunk
 #pragma unroll
       for (int s8 = 0; s8 < C / (kRevThreads / 32); ++s8) {
         const int r = warp + (kRevThreads / 32) * s8;
+        if (kTiles) {   // bf16, K = 128: lane takes features 4 lane .. 4 lane + 3
+          x[s8][0] = x[s8][1] = x[s8][2] = x[s8][3] = 0.f;
+          if (r < L) load4b(a.k, ((size_t)(t0 + r) * a.Hqk + hq) * K + 4 * lane, x[s8]);
+        } else {        // lane takes features lane + 32 m
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const int d = lane + 32 * m;
-          x[s8][m] = (r < L && d < K) ? load_elem(a.k, ((size_t)(t0 + r) * a.Hqk + hq) * K + d, a.io_dtype) : 0.f;
+          for (int m = 0; m < 4; ++m) {
+            const int d = lane + 32 * m;
+            x[s8][m] = (r < L && d < K) ? load_elem(a.k, ((size_t)(t0 + r) * a.Hqk + hq) * K + d, a.io_dtype) : 0.f;
+          }
         }
       }
 #pragma unroll
@@ -455,8 +468,9 @@ __global__ void __launch_bounds__(kRevThreads, 2) bwd_reverse_kernel(const Chunk
         }
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-          Kn[r * KLD + lane + 32 * m] = x[s8][m];
-          Kt[(lane + 32 * m) * TLD + r] = x[s8][m];
+          const int d = kTiles ? 4 * lane + m : lane + 32 * m;
+          Kn[r * KLD + d] = x[s8][m];
+          Kt[d * TLD + r] = x[s8][m];
         }
       }
     }
@@ -1089,7 +1103,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(const ChunkArg
     for (int s = 0; s < 16; ++s) {
       const int r = warp + 8 * s, i = r & 63;
       x[s][0] = x[s][1] = x[s][2] = x[s][3] = 0.f;
-      if (i < L) load4(r < 64 ? a.q : a.k, ((size_t)(t0 + i) * a.Hqk + hq) * 128 + 4 * lane, a.io_dtype, x[s]);
+      if (i < L) load4b(r < 64 ? a.q : a.k, ((size_t)(t0 + i) * a.Hqk + hq) * 128 + 4 * lane, x[s]);
     }
 #pragma unroll
     for (int s = 0; s < 16; ++s) {
@@ -1108,7 +1122,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(const ChunkArg
     for (int s8 = 0; s8 < 8; ++s8) {
       const int i = warp + 8 * s8;
       o4[s8][0] = o4[s8][1] = o4[s8][2] = o4[s8][3] = 0.f;
-      if (i < L) load4(b.d_o, ((size_t)(t0 + i) * Hv + h) * 128 + 4 * lane, a.io_dtype, o4[s8]);
+      if (i < L) load4b(b.d_o, ((size_t)(t0 + i) * Hv + h) * 128 + 4 * lane, o4[s8]);
     }
 #pragma unroll
     for (int s8 = 0; s8 < 8; ++s8) put4(sm + OFF_OX, 16384, warp + 8 * s8, 4 * lane, o4[s8]);
@@ -1472,13 +1486,13 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(const ChunkArg
     for (int s = 0; s < 16; ++s) {
       const int r = warp + 8 * s, i = r & 63;
       x[s][0] = x[s][1] = x[s][2] = x[s][3] = 0.f;
-      if (i < L) load4(r < 64 ? a.q : a.k, ((size_t)(t0 + i) * a.Hqk + hq) * 128 + 4 * lane, a.io_dtype, x[s]);
+      if (i < L) load4b(r < 64 ? a.q : a.k, ((size_t)(t0 + i) * a.Hqk + hq) * 128 + 4 * lane, x[s]);
     }
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
       const int i = warp + 8 * s;
       o[s][0] = o[s][1] = o[s][2] = o[s][3] = 0.f;
-      if (i < L) load4(b.d_o, ((size_t)(t0 + i) * Hv + h) * 128 + 4 * lane, a.io_dtype, o[s]);
+      if (i < L) load4b(b.d_o, ((size_t)(t0 + i) * Hv + h) * 128 + 4 * lane, o[s]);
     }
 #pragma unroll
     for (int s = 0; s < 16; ++s) {
