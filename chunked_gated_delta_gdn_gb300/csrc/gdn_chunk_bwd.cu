@@ -39,6 +39,8 @@
 //   5. grad         per (chunk, value head): dv, dbeta, dg, and dQ, dK per value head
 //   6. qk           per (token, query/key head): the group sum and the L2-norm Jacobian
 //                   -> dq, dk; zero gradients for tokens outside every sequence
+#include <string.h>
+
 #include "gdn_chunk_util.cuh"
 #include "gdn_sm100.cuh"
 
@@ -1427,31 +1429,27 @@ __device__ void solve_T_blocked(float* At, float* Dm, float* Lm, float* Ym) {
 }
 
 // ---------------------------------------------------------------- 3b. prep on the tensor cores
-// bf16 I/O with K = V = 128: the same outputs as bwd_prep_kernel (T, dUp, Z, G) with the
-// products on tcgen05 (bf16 operands, fp32 accumulators in TMEM):
-//   [Q K^T; K K^T] = [q; k] k^T           M=128 N=64  K=128  -> P (bf16) and A (fp32)
-//   Z   = Q^T diag(gamma) dO               M=128 N=128 K=64   (A: q rows as an MN-major operand)
-//   dUp = [P^T; 0] dO                      M=128 N=128 K=64   (A: P as stored, MN-major, over a
-//                                                              zero tile for rows 64-127)
-// then T = (I + A)^{-1} in fp32 by 16 x 16 blocks.  256 TMEM columns and ~98 KB of shared
-// memory: two CTAs per SM.
+// bf16 I/O with K = V = 128, feeding the tensor-core reverse pass: [Q K^T; K K^T] = [q; k] k^T
+// as one tcgen05.mma (M=128 N=64 K=128, bf16 operands, fp32 in TMEM), then on the CUDA cores
+// P = scale (Q K^T * Gamma) on and below the diagonal and A = strict_lower(diag(beta) K K^T *
+// Gamma), and T = (I + A)^{-1} in fp32 by 16 x 16 blocks.  Out, per chunk and value head in the
+// 16 KB slot of ws.T: T as a bf16 tile (rows j, 64 i per 128-byte row, 128-byte swizzled) and
+// P likewise (rows i, 64 j) 8 KB after it; G in ws.G.  64 TMEM columns, two CTAs per SM.
 namespace tcp {
 using namespace sm100;
 using tcg::put4;
 using tcg::kdesc;
-using tcg::mndesc;
 constexpr int kThreads = 256;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t OFF_QK = 0;         // [q; k] rows, 2 k-halves x 128 rows x 128 B
-constexpr uint32_t OFF_DO = 32768;     // dO rows i: 2 c-halves x 64 rows x 128 B
-constexpr uint32_t OFF_DG = 49152;     // diag(gamma) dO, same layout
-constexpr uint32_t OFF_P = 65536;      // P rows i, 64 j per row (bf16)
-constexpr uint32_t OFF_ZERO = 73728;   // 64 rows x 128 B of zeros
-constexpr uint32_t OFF_A = 81920;      // A, then T, fp32 [64][LDC]
-constexpr uint32_t OFF_VEC = OFF_A + 64 * LDC * 4;   // G, beta, gamma
-constexpr uint32_t OFF_BAR = OFF_VEC + 3 * 64 * 4;
+constexpr uint32_t OFF_P = 32768;      // P tile (bf16, scale folded)
+constexpr uint32_t OFF_TT = 40960;     // T tile (bf16)
+constexpr uint32_t OFF_A = 49152;      // A, then T, fp32 [64][LDC]
+constexpr uint32_t OFF_SCR = OFF_A + 64 * LDC * 4;   // solve scratch: D blocks, L, X
+constexpr uint32_t OFF_VEC = OFF_SCR + (4 * 16 * 17 + 2 * 64 * 64) * 4;
+constexpr uint32_t OFF_BAR = OFF_VEC + 2 * 64 * 4;
 constexpr uint32_t SMEM = OFF_BAR + 64 + 1024;
-constexpr uint32_t T_QK = 0, T_Z = 0, T_UP = 128, T_COLS = 256;
+constexpr uint32_t T_COLS = 64;
 
 __global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(const ChunkArgs a, const BwdArgs b,
                                                                   BwdWs ws) {
@@ -1459,9 +1457,9 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(const ChunkArg
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(sm);
   float* At = reinterpret_cast<float*>(sm + OFF_A);
+  float* scr = reinterpret_cast<float*>(sm + OFF_SCR);
   float* G = reinterpret_cast<float*>(sm + OFF_VEC);
   float* bt = G + 64;
-  float* gm = G + 128;
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 8);
   const int c = blockIdx.x, h = blockIdx.y;
@@ -1480,19 +1478,13 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(const ChunkArg
     tmem_relinquish();
   }
   load_gates(a, t0, L, h, G, bt);
-  {  // normalised [q; k] rows and dO rows (bf16), every load of a thread issued first
-    float x[16][4], o[8][4];
+  {  // normalised [q; k] rows (bf16), every load of a thread issued first
+    float x[16][4];
 #pragma unroll
     for (int s = 0; s < 16; ++s) {
       const int r = warp + 8 * s, i = r & 63;
       x[s][0] = x[s][1] = x[s][2] = x[s][3] = 0.f;
       if (i < L) load4b(r < 64 ? a.q : a.k, ((size_t)(t0 + i) * a.Hqk + hq) * 128 + 4 * lane, x[s]);
-    }
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const int i = warp + 8 * s;
-      o[s][0] = o[s][1] = o[s][2] = o[s][3] = 0.f;
-      if (i < L) load4b(b.d_o, ((size_t)(t0 + i) * Hv + h) * 128 + 4 * lane, o[s]);
     }
 #pragma unroll
     for (int s = 0; s < 16; ++s) {
@@ -1504,11 +1496,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(const ChunkArg
       for (int q = 0; q < 4; ++q) x[s][q] *= rn;
       put4(sm + OFF_QK, 16384, warp + 8 * s, 4 * lane, x[s]);
     }
-#pragma unroll
-    for (int s = 0; s < 8; ++s) put4(sm + OFF_DO, 8192, warp + 8 * s, 4 * lane, o[s]);
   }
-  for (int e = tid; e < 8192 / 16; e += kThreads)
-    reinterpret_cast<uint4*>(sm + OFF_ZERO)[e] = make_uint4(0u, 0u, 0u, 0u);
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -1519,18 +1507,9 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(const ChunkArg
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
-      mma_bf16(tb + T_QK, kdesc(sb + OFF_QK + ko), kdesc(sb + OFF_QK + 8192 + ko), id, ks > 0);
+      mma_bf16(tb, kdesc(sb + OFF_QK + ko), kdesc(sb + OFF_QK + 8192 + ko), id, ks > 0);
     }
     mma_commit(bar);
-  }
-  if (tid < 64) gm[tid] = expf(G[tid]);
-  __syncthreads();
-  // diag(gamma) dO while the product runs: 64 rows x 16 chunks of 8 bf16
-  for (int e = tid; e < 64 * 16; e += kThreads) {
-    const int i = e >> 4, chunk = e & 15, hlf = chunk >> 3, c8 = chunk & 7;
-    const uint32_t off = hlf * 8192 + i * 128 + ((c8 ^ (i & 7)) << 4);
-    *reinterpret_cast<uint4*>(sm + OFF_DG + off) = *reinterpret_cast<const uint4*>(sm + OFF_DO + off);
-    tcg::scale8(sm + OFF_DG + off, gm[i]);
   }
   bool ok = true;
   if (tid == 0) ok = mbar_wait(bar, 0, kWaitNs);
@@ -1544,93 +1523,390 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(const ChunkArg
   tc_fence_after();
   const uint32_t loff = (uint32_t)(32 * (warp & 3)) << 16;
   const int row = 32 * (warp & 3) + lane;
-  if (warp < 4) {   // P (rows 0-63, bf16) and A (rows 64-127, fp32), half the columns each pass
+  {  // P (rows 0-63, bf16, scale folded) and A (rows 64-127, fp32); warps w, w + 4 split columns
+    const int part = warp >> 2;
+    float x[32];
+    tmem_ld32(tb + loff + 32 * part, x);
+    if (row < 64) {
+      const int i = row;
 #pragma unroll
-    for (int part = 0; part < 2; ++part) {
-      float x[32];
-      tmem_ld32(tb + loff + T_QK + 32 * part, x);
-      if (row < 64) {
-        const int i = row;
+      for (int jj = 0; jj < 32; ++jj) {
+        const int j = 32 * part + jj;
+        const float p = j <= i ? a.scale * x[jj] * expf(G[i] - G[j]) : 0.f;
+        *reinterpret_cast<__nv_bfloat16*>(sm + OFF_P + sw128_offset(i, j)) = __float2bfloat16_rn(p);
+      }
+    } else {
+      const int i = row - 64;
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int j = 32 * part + jj;
-          const float p = j <= i ? x[jj] * expf(G[i] - G[j]) : 0.f;
-          *reinterpret_cast<__nv_bfloat16*>(sm + OFF_P + sw128_offset(i, j)) = __float2bfloat16_rn(p);
-        }
-      } else {
-        const int i = row - 64;
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int j = 32 * part + jj;
-          At[i * LDC + j] = j < i ? bt[i] * x[jj] * expf(G[i] - G[j]) : 0.f;
-        }
+      for (int jj = 0; jj < 32; ++jj) {
+        const int j = 32 * part + jj;
+        At[i * LDC + j] = j < i ? bt[i] * x[jj] * expf(G[i] - G[j]) : 0.f;
       }
     }
   }
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  if (tid == 0) {   // Z = (Q^T) (diag(gamma) dO);  dUp = [P^T; 0] dO
-    const uint32_t id = idesc_bf16(128, 128, true, true);
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      mma_bf16(tb + T_Z, mndesc(sb + OFF_QK + ks * 2048, 16384), mndesc(sb + OFF_DG + ks * 2048, 8192),
-               id, ks > 0);
-      mma_bf16(tb + T_UP, mndesc(sb + OFF_P + ks * 2048, OFF_ZERO - OFF_P),
-               mndesc(sb + OFF_DO + ks * 2048, 8192), id, ks > 0);
-    }
-    mma_commit(bar);
-  }
-  if (tid == 0) ok = mbar_wait(bar, 1, kWaitNs);
-  if (__syncthreads_or(!ok)) {
-    if (tid == 0) report(a.dev_status, GDN_DEV_TIMEOUT);
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tb, T_COLS);
-    return;
-  }
-  tc_fence_after();
-  {  // Z rows d (all 128 lanes), dUp rows j < 64; warps w and w + 4 split the columns
-    const int part = warp >> 2;
-    float* Zg = ws.Z + ch * 128 * 128 + (size_t)row * 128 + 64 * part;
-#pragma unroll
-    for (int q2 = 0; q2 < 2; ++q2) {
-      float x[32];
-      tmem_ld32(tb + loff + T_Z + 64 * part + 32 * q2, x);
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        st4(Zg + 32 * q2 + 4 * q, make_float4(a.scale * x[4 * q], a.scale * x[4 * q + 1],
-                                              a.scale * x[4 * q + 2], a.scale * x[4 * q + 3]));
-    }
-    if (row < 64) {
-      float* Ug = ws.dUp + ch * 64 * 128 + (size_t)row * 128 + 64 * part;
-#pragma unroll
-      for (int q2 = 0; q2 < 2; ++q2) {
-        float x[32];
-        tmem_ld32(tb + loff + T_UP + 64 * part + 32 * q2, x);
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          st4(Ug + 32 * q2 + 4 * q, make_float4(a.scale * x[4 * q], a.scale * x[4 * q + 1],
-                                                a.scale * x[4 * q + 2], a.scale * x[4 * q + 3]));
-      }
-    }
-  }
-  tc_fence_before();
-  __syncthreads();   // the products are done with every tile: they serve as the solve's scratch
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tb, T_COLS);
   }
-  solve_T_blocked(At, reinterpret_cast<float*>(sm + OFF_P), reinterpret_cast<float*>(sm + OFF_QK),
-                  reinterpret_cast<float*>(sm + OFF_DO));
-  for (int e = tid; e < 64 * 64; e += kThreads) {
-    const int i = e >> 6, j = e & 63;
-    ws.T[ch * 64 * 64 + e] = At[i * LDC + j];
+  solve_T_blocked(At, scr, scr + 4 * 16 * 17, scr + 4 * 16 * 17 + 64 * 64);
+  for (int e = tid; e < 64 * 32; e += kThreads) {   // T as a bf16 tile: rows j, 64 i
+    const int j = e >> 5, i = 2 * (e & 31);
+    *reinterpret_cast<uint32_t*>(sm + OFF_TT + sw128_offset(j, i)) =
+        tcg::pack2(At[j * LDC + i], At[j * LDC + i + 1]);
+  }
+  __syncthreads();
+  uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(ws.T + ch * 64 * 64));
+  const uint4* srcT = reinterpret_cast<const uint4*>(sm + OFF_TT);
+  const uint4* srcP = reinterpret_cast<const uint4*>(sm + OFF_P);
+  for (int e = tid; e < 8192 / 16; e += kThreads) {
+    dst[e] = srcT[e];
+    dst[8192 / 16 + e] = srcP[e];
   }
   if (tid < 64) ws.G[ch * 64 + tid] = G[tid];
 }
 }  // namespace tcp
+
+// ---------------------------------------------------------------- 4b. reverse on the tensor cores
+// bf16 I/O with K = V = 128: one CTA (4 warps) per (sequence, value head), chunks last to
+// first, with dS^T (TMEM lane = value index v, column = key index d) resident in TMEM like the
+// forward's state.  Per chunk (tiles double-buffered one chunk ahead: q, k, dO by TMA, the
+// prep pass's T and P tiles by bulk copy):
+//   Y^T   = dS^T K^T                        M=128 N=64  K=128  (A: bf16 dS^T from TMEM)
+//   dUp^T = dO^T P                          M=128 N=64  K=64   (P carries scale)
+//   dU'^T = dUp^T + Y^T diag(lambda)        -> bf16 into TMEM
+//   dX^T  = dU'^T T                         M=128 N=64  K=64
+//   dS^T <- gamma_L dS^T + dO^T (scale diag(gamma) Q) + dX^T (-diag(gamma beta) K)
+//                                           M=128 N=128 K=64 + 64
+// with the normalised q and k rows scaled in shared memory.  It writes, per chunk, the bf16
+// dS (the gradient of the chunk's exit state) and dX tiles of the grad pass, dv = diag(beta)
+// dX, and the row dots dX_i . v_i (slot 0 of ws.XV, slots 1-3 zero).
+namespace tcr {
+using namespace sm100;
+constexpr int kThreads = 128;
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint32_t ST_Q = 0, ST_K = 16384, ST_KG = 32768, ST_DO = 49152, ST_T = 65536, ST_P = 73728;
+constexpr uint32_t STAGE = 81920;
+constexpr uint32_t STAGE_TX = 3 * 16384 + 2 * 8192;
+constexpr uint32_t OFF_VEC = 2 * STAGE;              // per stage: G[64], beta[64]
+constexpr uint32_t OFF_RED = OFF_VEC + 2 * 128 * 4;  // [4 warps][64]
+constexpr uint32_t OFF_BAR = OFF_RED + 4 * 64 * 4;
+constexpr uint32_t SMEM = OFF_BAR + 64 + 1024;
+constexpr uint32_t C_S = 0, C_SB = 128, C_Y = 192, C_U = 256, C_X = 320, T_COLS = 512;
+
+__device__ __forceinline__ void issue_stage(uint8_t* st, uint64_t* bar, const CUtensorMap* tq,
+                                            const CUtensorMap* tk, const CUtensorMap* to,
+                                            const uint8_t* tp, int t, int hq, int h) {
+  mbar_arrive_expect_tx(bar, STAGE_TX);
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    tma_load_3d(st + ST_Q + hh * 8192, tq, bar, 64 * hh, hq, t);
+    tma_load_3d(st + ST_K + hh * 8192, tk, bar, 64 * hh, hq, t);
+    tma_load_3d(st + ST_DO + hh * 8192, to, bar, 64 * hh, h, t);
+  }
+  bulk_load(st + ST_T, tp, 8192, bar);
+  bulk_load(st + ST_P, tp + 8192, 8192, bar);
+}
+
+// dS^T (fp32, C_S) -> bf16 pairs in C_SB, the A operand of the next Y product.
+__device__ __forceinline__ void pack_state(uint32_t tb, uint32_t loff) {
+#pragma unroll
+  for (int p2 = 0; p2 < 2; ++p2) {
+    float x[32], y[32], pk[32];
+    tmem_ld32(tb + loff + C_S + 64 * p2, x);
+    tmem_ld32(tb + loff + C_S + 64 * p2 + 32, y);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      pk[j] = __uint_as_float(tcg::pack2(x[2 * j], x[2 * j + 1]));
+      pk[16 + j] = __uint_as_float(tcg::pack2(y[2 * j], y[2 * j + 1]));
+    }
+    tmem_st32(tb + loff + C_SB + 32 * p2, pk);
+  }
+}
+
+// Sum over the 32 lanes of each of v[0..31]: lane l ends with the total of v[l] (31 shuffles).
+__device__ __forceinline__ float lane_transpose_sum(float (&v)[32], int lane) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int k = 0; k < o; ++k) {
+      const float send = up ? v[k] : v[k + o];
+      const float keep = up ? v[k + o] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  return v[0];
+}
+
+__global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
+    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+    const __grid_constant__ CUtensorMap tmO, const ChunkArgs a, const BwdArgs b, BwdWs ws) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sb = smem_u32(sm);
+  float* red = reinterpret_cast<float*>(sm + OFF_RED);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + OFF_BAR);   // [2]
+  uint64_t* mmab = full + 2;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 24);
+  const int Hv = a.Hv, h = blockIdx.x % Hv, n = blockIdx.x / Hv, hq = h / (Hv / a.Hqk);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, v = tid;
+  const size_t st_off = ((size_t)n * Hv + h) * 128 * 128;
+  if (!ws.chunk_off[a.num_seqs + 1]) {   // invalid cu_seqlens: zero gradient
+    if (b.d_initial)
+      for (int d = 0; d < 128; ++d) b.d_initial[st_off + (size_t)d * 128 + v] = 0.f;
+    return;
+  }
+  int bos, eos;
+  seq_bounds(a, n, &bos, &eos);
+  const int first = ws.chunk_off[n];
+  const int nch = (eos - bos + C - 1) / C;
+  const uint32_t loff = (uint32_t)(32 * warp) << 16;
+  if (tid == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    mbar_init(mmab, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmO);
+    for (int it = 0; it < 2 && it < nch; ++it) {
+      const int qc = nch - 1 - it;
+      issue_stage(sm + it * STAGE, &full[it], &tmQ, &tmK, &tmO,
+                  reinterpret_cast<const uint8_t*>(ws.T + ((size_t)(first + qc) * Hv + h) * 64 * 64),
+                  bos + qc * C, hq, h);
+    }
+  }
+  if (warp == 0) {
+    tmem_alloc(tslot, T_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = *tslot;
+  {  // dS^T <- d_final^T
+#pragma unroll
+    for (int part = 0; part < 4; ++part) {
+      float x[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        x[j] = b.d_final ? b.d_final[st_off + (size_t)(32 * part + j) * 128 + v] : 0.f;
+      tmem_st32(tb + loff + C_S + 32 * part, x);
+    }
+    pack_state(tb, loff);
+  }
+  if (nch > 0) {   // the first chunk's gates
+    const int t1 = bos + (nch - 1) * C;
+    load_gates(a, t1, min(C, eos - t1), h, reinterpret_cast<float*>(sm + OFF_VEC),
+               reinterpret_cast<float*>(sm + OFF_VEC) + 64);
+  }
+  uint32_t ph = 0;
+  bool failed = false;
+  const uint32_t sxv = (uint32_t)((v & 63) >> 3) << 4;   // this lane's swizzle term
+  for (int it = 0; it < nch; ++it) {
+    const int qc = nch - 1 - it, s = it & 1;
+    const int t0 = bos + qc * C, L = min(C, eos - t0);
+    const size_t ch = (size_t)(first + qc) * Hv + h;
+    uint8_t* st = sm + s * STAGE;
+    const uint32_t sst = sb + s * STAGE;
+    float* G = reinterpret_cast<float*>(sm + OFF_VEC) + s * 128;   // loaded one chunk ahead
+    float* bt = G + 64;
+    bool ok = true;
+    if (tid == 0) ok = mbar_wait(&full[s], (uint32_t)(it >> 1) & 1u, kWaitNs);
+    if (__syncthreads_or(!ok)) { failed = true; break; }
+    {  // norms; r_k k, -gamma beta r_k k, scale gamma r_q q in place; dO rows >= L zeroed
+      const int i = tid >> 1, hh = tid & 1;
+      uint8_t* qrow = st + ST_Q + hh * 8192 + i * 128;
+      uint8_t* krow = st + ST_K + hh * 8192 + i * 128;
+      float sq = 0.f, sk = 0.f;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        const uint4 uq = *reinterpret_cast<const uint4*>(qrow + 16 * c8);
+        const uint4 uk = *reinterpret_cast<const uint4*>(krow + 16 * c8);
+        const uint32_t wq[4] = {uq.x, uq.y, uq.z, uq.w}, wk[4] = {uk.x, uk.y, uk.z, uk.w};
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const float2 fq = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wq[w]));
+          const float2 fk = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wk[w]));
+          sq = fmaf(fq.x, fq.x, fmaf(fq.y, fq.y, sq));
+          sk = fmaf(fk.x, fk.x, fmaf(fk.y, fk.y, sk));
+        }
+      }
+      sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+      sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+      const bool l2 = a.use_qk_l2norm != 0;
+      const float rq = l2 ? 1.0f / sqrtf(sq + kL2Eps) : 1.f, rk = l2 ? 1.0f / sqrtf(sk + kL2Eps) : 1.f;
+      const float gi = expf(G[i]);
+      const float fq = i < L ? a.scale * gi * rq : 0.f;
+      const float fk = i < L ? rk : 0.f;
+      const float fg = i < L ? -gi * bt[i] * rk : 0.f;
+      uint8_t* grow = st + ST_KG + hh * 8192 + i * 128;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        *reinterpret_cast<uint4*>(grow + 16 * c8) = *reinterpret_cast<const uint4*>(krow + 16 * c8);
+        tcg::scale8(grow + 16 * c8, fg);
+        tcg::scale8(krow + 16 * c8, fk);
+        tcg::scale8(qrow + 16 * c8, fq);
+        if (i >= L)
+          *reinterpret_cast<uint4*>(st + ST_DO + hh * 8192 + i * 128 + 16 * c8) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {   // Y^T = dS^T K^T;  dUp^T = dO^T P
+      const uint32_t iy = idesc_bf16(128, 64, false, false), iu = idesc_bf16(128, 64, true, true);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_bf16_ta(tb + C_Y, tb + C_SB + 8 * ks,
+                    tcg::kdesc(sst + ST_K + (ks >> 2) * 8192 + (ks & 3) * 32), iy, ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(tb + C_U, tcg::mndesc(sst + ST_DO + ks * 2048, 8192),
+                 tcg::mndesc(sst + ST_P + ks * 2048, 8192), iu, ks > 0);
+      mma_commit(mmab);
+    }
+    if (it + 1 < nch) {   // the next chunk's gates into the other stage while the products run
+      const int t1 = bos + (qc - 1) * C;
+      float* G1 = reinterpret_cast<float*>(sm + OFF_VEC) + (s ^ 1) * 128;
+      load_gates(a, t1, min(C, eos - t1), h, G1, G1 + 64);
+    }
+    if (tid == 0) ok = mbar_wait(mmab, ph, kWaitNs);
+    ph ^= 1u;
+    if (__syncthreads_or(!ok)) { failed = true; break; }
+    tc_fence_after();
+    {  // dU'^T = dUp^T + Y^T diag(lambda) -> bf16 pairs in C_U
+      const float gl = G[L - 1];
+      float pk[32];
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        float y[32], u[32];
+        tmem_ld32(tb + loff + C_Y + 32 * p, y);
+        tmem_ld32(tb + loff + C_U + 32 * p, u);
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          const int j0 = 32 * p + 2 * jj;
+          pk[16 * p + jj] = __uint_as_float(
+              tcg::pack2(fmaf(expf(gl - G[j0]), y[2 * jj], u[2 * jj]),
+                         fmaf(expf(gl - G[j0 + 1]), y[2 * jj + 1], u[2 * jj + 1])));
+        }
+      }
+      tmem_st32(tb + loff + C_U, pk);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {   // dX^T = dU'^T T
+      const uint32_t ix = idesc_bf16(128, 64, false, true);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16_ta(tb + C_X, tb + C_U + 8 * ks, tcg::mndesc(sst + ST_T + ks * 2048, 8192), ix, ks > 0);
+      mma_commit(mmab);
+    }
+    if (tid == 0) ok = mbar_wait(mmab, ph, kWaitNs);
+    ph ^= 1u;
+    if (__syncthreads_or(!ok)) { failed = true; break; }
+    tc_fence_after();
+    {  // dX: the grad pass's bf16 tile, dv = beta dX, the row dots dX_i . v_i; bf16 dX^T in C_X
+      uint8_t* xt = reinterpret_cast<uint8_t*>(ws.dX + ch * 64 * 128) + (v >> 6) * 8192 + (v & 7) * 2;
+      float pk[32];
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        float x[32], pv[32];
+        // the v loads first, all in flight together (a store to dv in between would order
+        // each load behind it: the compiler cannot tell that v and dv do not overlap)
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int i = 32 * p + jj;
+          pv[jj] = i < L ? load_elem(a.v, ((size_t)(t0 + i) * Hv + h) * 128 + v, a.io_dtype) : 0.f;
+        }
+        tmem_ld32(tb + loff + C_X + 32 * p, x);
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int i = 32 * p + jj;
+          *reinterpret_cast<__nv_bfloat16*>(xt + i * 128 + (sxv ^ ((i & 7) << 4))) = __float2bfloat16_rn(x[jj]);
+          pv[jj] *= x[jj];
+          if (i < L) store_elem(b.dv, ((size_t)(t0 + i) * Hv + h) * 128 + v, bt[i] * x[jj], a.io_dtype);
+        }
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) pk[16 * p + jj] = __uint_as_float(tcg::pack2(x[2 * jj], x[2 * jj + 1]));
+        red[warp * 64 + 32 * p + lane] = lane_transpose_sum(pv, lane);
+      }
+      tmem_st32(tb + loff + C_X, pk);
+    }
+    {  // the bf16 dS tile (gradient of the chunk's exit state), then dS^T <- gamma_L dS^T
+      uint8_t* stile = reinterpret_cast<uint8_t*>(ws.dS + ch * 128 * 128) + (v >> 6) * 16384 + (v & 7) * 2;
+      const float gL = expf(G[L - 1]);
+#pragma unroll
+      for (int part = 0; part < 4; ++part) {
+        float x[32];
+        tmem_ld32(tb + loff + C_S + 32 * part, x);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int d = 32 * part + j;
+          *reinterpret_cast<__nv_bfloat16*>(stile + d * 128 + (sxv ^ ((j & 7) << 4))) = __float2bfloat16_rn(x[j]);
+          x[j] *= gL;
+        }
+        tmem_st32(tb + loff + C_S + 32 * part, x);
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid < 64) {   // the row dots, summed over the four warps in a fixed order
+      float* xv = ws.XV + ch * 4 * 64;
+      xv[tid] = (red[tid] + red[64 + tid]) + (red[128 + tid] + red[192 + tid]);
+      xv[64 + tid] = 0.f;
+      xv[128 + tid] = 0.f;
+      xv[192 + tid] = 0.f;
+    }
+    if (tid == 0) {   // dS^T += dO^T (scale gamma r_q q) + dX^T (-gamma beta r_k k)
+      const uint32_t iq = idesc_bf16(128, 128, true, true), ik = idesc_bf16(128, 128, false, true);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(tb + C_S, tcg::mndesc(sst + ST_DO + ks * 2048, 8192),
+                 tcg::mndesc(sst + ST_Q + ks * 2048, 8192), iq, 1);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16_ta(tb + C_S, tb + C_X + 8 * ks, tcg::mndesc(sst + ST_KG + ks * 2048, 8192), ik, 1);
+      mma_commit(mmab);
+    }
+    if (tid == 0) ok = mbar_wait(mmab, ph, kWaitNs);
+    ph ^= 1u;
+    if (__syncthreads_or(!ok)) { failed = true; break; }
+    tc_fence_after();
+    if (tid == 0 && qc - 2 >= 0) {   // every read of this stage is done: chunk qc - 2 into it
+      issue_stage(st, &full[s], &tmQ, &tmK, &tmO,
+                  reinterpret_cast<const uint8_t*>(ws.T + ((size_t)(first + qc - 2) * Hv + h) * 64 * 64),
+                  bos + (qc - 2) * C, hq, h);
+    }
+    pack_state(tb, loff);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
+  if (failed) {
+    if (tid == 0) report(a.dev_status, GDN_DEV_TIMEOUT);
+  } else if (b.d_initial) {
+#pragma unroll
+    for (int part = 0; part < 4; ++part) {
+      float x[32];
+      tmem_ld32(tb + loff + C_S + 32 * part, x);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) b.d_initial[st_off + (size_t)(32 * part + j) * 128 + v] = x[j];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tb, T_COLS);
+  }
+}
+}  // namespace tcr
 
 // ---------------------------------------------------------------- 6. qk
 // One warp per (token, query/key head), four features per lane: the group sum of the
@@ -1707,7 +1983,7 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
   BwdWs ws = bwd_layout(a.workspace, NC, a.num_seqs, a.Hv, a.K, a.V, T_total, nullptr);
   cudaError_t err;
   if ((err = cudaFuncSetAttribute(bwd_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem))) return err;
-  if ((err = cudaFuncSetAttribute(bwd_reverse_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRevSmem))) return err;
+  if ((err = cudaFuncSetAttribute(tcr::bwd_reverse_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcr::SMEM))) return err;
   if ((err = cudaFuncSetAttribute(bwd_reverse_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRevSmem))) return err;
   if ((err = cudaFuncSetAttribute(bwd_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGradSmem))) return err;
   if ((err = cudaFuncSetAttribute(tcg::bwd_grad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcg::SMEM))) return err;
@@ -1742,10 +2018,20 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
   if (a.num_seqs > 0) {
     const long long blocks = (long long)vtiles * a.Hv * a.num_seqs;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    if (tc)
-      bwd_reverse_kernel<true><<<(unsigned)blocks, kRevThreads, kRevSmem, a.stream>>>(a, b, ws);
-    else
+    if (tc) {
+      CUtensorMap mq, mk, mo;
+      memset(&mq, 0, sizeof(mq));
+      memset(&mk, 0, sizeof(mk));
+      memset(&mo, 0, sizeof(mo));
+      if (!encode_rows_map_bf16(&mq, a.q, a.Hqk, T_total) || !encode_rows_map_bf16(&mk, a.k, a.Hqk, T_total) ||
+          !encode_rows_map_bf16(&mo, b.d_o, a.Hv, T_total))
+        return cudaErrorInvalidValue;
+      const long long ctas = (long long)a.num_seqs * a.Hv;
+      if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+      tcr::bwd_reverse_tc_kernel<<<(unsigned)ctas, tcr::kThreads, tcr::SMEM, a.stream>>>(mq, mk, mo, a, b, ws);
+    } else {
       bwd_reverse_kernel<false><<<(unsigned)blocks, kRevThreads, kRevSmem, a.stream>>>(a, b, ws);
+    }
     if ((err = cudaGetLastError())) return err;
   }
   if (NC > 0) {

@@ -948,6 +948,10 @@ bool encode_map(CUtensorMap* m, const void* base, int H, int T_total) {
 
 }  // namespace
 
+bool encode_rows_map_bf16(CUtensorMap* m, const void* base, int H, int T_total) {
+  return encode_map(m, base, H, T_total);
+}
+
 bool chunk_tc_supported(int K, int V, int io_dtype, int beta_dtype) {
   return K == DK && V == DV && io_dtype == GDN_BF16 &&
          (beta_dtype == GDN_BF16 || beta_dtype == GDN_F32);

@@ -1,6 +1,7 @@
 // gdn_internal.h -- launchers behind the C ABI (not part of the public header).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -118,6 +119,9 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a, const BwdArgs& b);
 
 // Fused tcgen05 / TMEM / TMA path (bf16, K = V = 128).
 bool chunk_tc_supported(int K, int V, int io_dtype, int beta_dtype);
+// TMA map of a [T_total, H, 128] bf16 tensor with 64 x 1 x 64 boxes (64 features of one head
+// for 64 tokens, 128-byte swizzled), zero fill past the last token.
+bool encode_rows_map_bf16(CUtensorMap* m, const void* base, int H, int T_total);
 cudaError_t launch_chunk_tc(const ChunkArgs& a);
 
 cudaError_t launch_decode(const DecodeArgs& a);
