@@ -28,15 +28,20 @@
 // head, in a fixed order) to dq, dk.
 //
 // Launches on the caller's stream, no host sync and no atomics (the result is
-// bitwise reproducible run to run):
+// bitwise reproducible run to run).  Two paths: bf16 with K = V = 128 runs every product on
+// the tcgen05 tensor cores (bf16 operands, fp32 accumulators), everything else in fp32 on the
+// CUDA cores.
 //   1. chunk table  from cu_seqlens, on the device
-//   2. states       the forward recompute of the entry state S0 of every chunk and of U':
-//                   bf16 with K = V = 128, the tensor-core forward kernel in record mode;
-//                   otherwise the prep and state passes of the fp32 chunk path
-//   3. prep         per (chunk, value head): T, dUp = scale P^T dO, Z = scale Q^T diag(gamma) dO
-//   4. reverse      per (sequence, value head, 32 columns), chunks last to first:
-//                   records dS (the gradient of each chunk's exit state) and dX
-//   5. grad         per (chunk, value head): dv, dbeta, dg, and dQ, dK per value head
+//   2. states       the forward recompute of the state entering every chunk and of U':
+//                   tensor cores: the forward kernel in record mode (bf16 operand tiles);
+//                   CUDA cores: the prep and state passes of the fp32 chunk path
+//   3. prep         per (chunk, value head): T = (I + A)^{-1}; tensor cores: P and T as bf16
+//                   tiles; CUDA cores: T, dUp = scale P^T dO, Z = scale Q^T diag(gamma) dO
+//   4. reverse      chunks last to first, recording dS (the gradient of each chunk's exit
+//                   state) and dX, writing dv and the row dots dX_i . v_i; tensor cores: one
+//                   CTA per (sequence, value head), dS^T in TMEM; CUDA cores: per (sequence,
+//                   value head, 32 columns)
+//   5. grad         per (chunk, value head): dbeta, dg, and dQ, dK per value head
 //   6. qk           per (token, query/key head): the group sum and the L2-norm Jacobian
 //                   -> dq, dk; zero gradients for tokens outside every sequence
 #include <string.h>
@@ -178,10 +183,6 @@ constexpr int kBarT = 1;          // named barrier of the two warps that build T
 
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
-__device__ __forceinline__ uint32_t tcg_pack2(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
 
 // Four bf16 at element i (i % 4 == 0) through the read-only path, as fp32.
 __device__ __forceinline__ void load4b(const void* p, size_t i, float (&x)[4]) {
@@ -370,11 +371,7 @@ constexpr int KLD = KP + 4;   // [C][KLD]: k rows, float4 reads
 constexpr int TLD = C + 2;    // [KP][TLD]: k transposed, float2 reads
 constexpr size_t kRevSmem = sizeof(float) * (C * KLD + KP * TLD + KP * VT + 2 * C * VT + 2 * C);
 
-// kTiles: dS and dX go out as the bf16 operand tiles of the tensor-core grad pass (K-major,
-// 128-byte swizzled, dv along the rows in two 64-element halves) instead of fp32 [K][V] /
-// [C][V].  Either way the pass also writes dv = diag(beta) dX and the per-slice partial row
-// dots dX_i . v_i.
-template <bool kTiles>
+// The pass also writes dv = diag(beta) dX and the per-slice partial row dots dX_i . v_i.
 __global__ void __launch_bounds__(kRevThreads, 2) bwd_reverse_kernel(const ChunkArgs a,
                                                                      const BwdArgs b, BwdWs ws) {
   extern __shared__ float smem[];
@@ -422,23 +419,11 @@ __global__ void __launch_bounds__(kRevThreads, 2) bwd_reverse_kernel(const Chunk
     const size_t ch = (size_t)(first + qc) * a.Hv + h;
     __syncthreads();  // the previous chunk is done with every tile
     if (colok) {      // record dS, the gradient of this chunk's exit state
-      if (kTiles) {
-        uint8_t* t = reinterpret_cast<uint8_t*>(ws.dS + ch * K * V) + (col >> 6) * 16384 + (col & 7) * 2;
+      float* dSg = ws.dS + ch * K * V;
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int d = 4 * ty + r;
-          uint2 u;
-          u.x = tcg_pack2(s[r][0], s[r][1]);
-          u.y = tcg_pack2(s[r][2], s[r][3]);
-          *reinterpret_cast<uint2*>(t + d * 128 + ((((col & 63) >> 3) ^ (d & 7)) << 4)) = u;
-        }
-      } else {
-        float* dSg = ws.dS + ch * K * V;
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-          if (4 * ty + r < K)
-            st4(dSg + (size_t)(4 * ty + r) * V + col, make_float4(s[r][0], s[r][1], s[r][2], s[r][3]));
-      }
+      for (int r = 0; r < 4; ++r)
+        if (4 * ty + r < K)
+          st4(dSg + (size_t)(4 * ty + r) * V + col, make_float4(s[r][0], s[r][1], s[r][2], s[r][3]));
     }
     // normalised k rows into Kn and Kt (warp w: rows w + 8 s; every load issued first)
     {
@@ -446,15 +431,10 @@ __global__ void __launch_bounds__(kRevThreads, 2) bwd_reverse_kernel(const Chunk
 #pragma unroll
       for (int s8 = 0; s8 < C / (kRevThreads / 32); ++s8) {
         const int r = warp + (kRevThreads / 32) * s8;
-        if (kTiles) {   // bf16, K = 128: lane takes features 4 lane .. 4 lane + 3
-          x[s8][0] = x[s8][1] = x[s8][2] = x[s8][3] = 0.f;
-          if (r < L) load4b(a.k, ((size_t)(t0 + r) * a.Hqk + hq) * K + 4 * lane, x[s8]);
-        } else {        // lane takes features lane + 32 m
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const int d = lane + 32 * m;
-            x[s8][m] = (r < L && d < K) ? load_elem(a.k, ((size_t)(t0 + r) * a.Hqk + hq) * K + d, a.io_dtype) : 0.f;
-          }
+        for (int m = 0; m < 4; ++m) {   // lane takes features lane + 32 m
+          const int d = lane + 32 * m;
+          x[s8][m] = (r < L && d < K) ? load_elem(a.k, ((size_t)(t0 + r) * a.Hqk + hq) * K + d, a.io_dtype) : 0.f;
         }
       }
 #pragma unroll
@@ -470,7 +450,7 @@ __global__ void __launch_bounds__(kRevThreads, 2) bwd_reverse_kernel(const Chunk
         }
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-          const int d = kTiles ? 4 * lane + m : lane + 32 * m;
+          const int d = lane + 32 * m;
           Kn[r * KLD + d] = x[s8][m];
           Kt[d * TLD + r] = x[s8][m];
         }
@@ -543,15 +523,7 @@ __global__ void __launch_bounds__(kRevThreads, 2) bwd_reverse_kernel(const Chunk
         const int i = 2 * ty + r;
         float xv = 0.f;
         if (colok) {
-          if (kTiles) {
-            uint2 u;
-            u.x = tcg_pack2(x[r][0], x[r][1]);
-            u.y = tcg_pack2(x[r][2], x[r][3]);
-            *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(dXg) + (col >> 6) * 8192 + i * 128 +
-                                      ((((col & 63) >> 3) ^ (i & 7)) << 4) + (col & 7) * 2) = u;
-          } else {
-            st4(dXg + (size_t)i * V + col, make_float4(x[r][0], x[r][1], x[r][2], x[r][3]));
-          }
+          st4(dXg + (size_t)i * V + col, make_float4(x[r][0], x[r][1], x[r][2], x[r][3]));
           if (i < L) {   // dv = beta dX; partial dX . v over this thread's four columns
             const size_t tv = ((size_t)(t0 + i) * a.Hv + h) * V + col;
             const float bi = bt[i];
@@ -1984,7 +1956,7 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
   cudaError_t err;
   if ((err = cudaFuncSetAttribute(bwd_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem))) return err;
   if ((err = cudaFuncSetAttribute(tcr::bwd_reverse_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcr::SMEM))) return err;
-  if ((err = cudaFuncSetAttribute(bwd_reverse_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRevSmem))) return err;
+  if ((err = cudaFuncSetAttribute(bwd_reverse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRevSmem))) return err;
   if ((err = cudaFuncSetAttribute(bwd_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGradSmem))) return err;
   if ((err = cudaFuncSetAttribute(tcg::bwd_grad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcg::SMEM))) return err;
   if ((err = cudaFuncSetAttribute(tcp::bwd_prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcp::SMEM))) return err;
@@ -2030,7 +2002,7 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
       if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
       tcr::bwd_reverse_tc_kernel<<<(unsigned)ctas, tcr::kThreads, tcr::SMEM, a.stream>>>(mq, mk, mo, a, b, ws);
     } else {
-      bwd_reverse_kernel<false><<<(unsigned)blocks, kRevThreads, kRevSmem, a.stream>>>(a, b, ws);
+      bwd_reverse_kernel<<<(unsigned)blocks, kRevThreads, kRevSmem, a.stream>>>(a, b, ws);
     }
     if ((err = cudaGetLastError())) return err;
   }
