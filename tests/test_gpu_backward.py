@@ -64,6 +64,16 @@ CASES = {
     # the GatedDeltaNet gate parameterisation (strong decays)
     "bf16_mixer_gates": dict(B=2, T=300, Hqk=1, Hv=2, K=128, V=128, dtype=torch.bfloat16,
                              init="randn", gates="mixer", seed=3106),
+    # tensor-core path edges: many short sequences (partial chunks, TMA boxes reaching into the
+    # next sequence), empty sequences first and last, equal head counts
+    "bf16_many_short": dict(lengths=[0, 1, 2, 63, 64, 65, 5, 127, 0], Hqk=2, Hv=2, K=128, V=128,
+                            dtype=torch.bfloat16, init="randn", seed=3114),
+    # tensor-core path without an initial state or a final-state gradient
+    "bf16_no_init_no_dfinal": dict(B=1, T=200, Hqk=2, Hv=4, K=128, V=128, dtype=torch.bfloat16,
+                                   init="none", seed=3115),
+    # tensor-core path without the in-kernel norm (unit-norm rows given), explicit scale
+    "bf16_no_l2": dict(B=1, T=130, Hqk=1, Hv=2, K=128, V=128, dtype=torch.bfloat16,
+                       init="randn", use_qk_l2norm=False, scale=0.2, seed=3116),
 }
 
 
@@ -81,7 +91,8 @@ def test_backward_matches_oracle(case):
     if not inp.use_qk_l2norm:
         inp.q, inp.k = unit_rows(inp.q), unit_rows(inp.k)
     d_o, dfin = synthetic.output_grads(inp, seed=CASES[case]["seed"] + 1,
-                                       d_final=case != "fp32_no_l2_no_init")
+                                       d_final=case not in ("fp32_no_l2_no_init",
+                                                            "bf16_no_init_no_dfinal"))
     check(inp, d_o, dfin, TOL[inp.q.dtype], case)
 
 
@@ -95,9 +106,10 @@ def test_backward_is_bitwise_deterministic():
         assert torch.equal(x, y), name
 
 
-def test_tokens_past_the_last_sequence_get_zero_gradients():
-    inp = synthetic.chunk_inputs(lengths=[70, 50], Hqk=1, Hv=2, K=64, V=64,
-                                 dtype=torch.float32, init="randn", seed=3109)
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_tokens_past_the_last_sequence_get_zero_gradients(dtype):
+    inp = synthetic.chunk_inputs(lengths=[70, 50], Hqk=1, Hv=2, K=128, V=128,
+                                 dtype=dtype, init="randn", seed=3109)
     T = inp.q.shape[1]
     pad = 40   # 40 trailing tokens that belong to no sequence
     grow = lambda x, fill=0.0: torch.cat([x, torch.full((1, pad) + tuple(x.shape[2:]), fill,
@@ -113,7 +125,7 @@ def test_tokens_past_the_last_sequence_get_zero_gradients():
         if name != "d_initial_state":
             assert torch.count_nonzero(x[:, T:]).item() == 0, name
             x = x[:, :T]
-        assert rel_l2(f64(x), r) <= TOL[torch.float32], name
+        assert rel_l2(f64(x), r) <= TOL[dtype], name
 
 
 def test_autograd_op_runs_the_backward_kernel():
