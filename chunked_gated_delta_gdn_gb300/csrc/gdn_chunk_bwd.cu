@@ -1350,86 +1350,170 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(const ChunkArg
 }
 }  // namespace tcg
 
-// T = (I + A)^{-1} for a strictly lower 64 x 64 A (fp32, row stride LDC), in place, by
-// 16 x 16 blocks: D_b = (I + A_bb)^{-1} by substitution on the four diagonal blocks,
-// L = D A_off (block strictly lower, so L^4 = 0), then T = (I - L + L^2 - L^3) D evaluated
-// as D - L (D - L (D - L D)).  All threads of the CTA call it; Dm ([4][16][17]), Lm and Ym
-// ([64][64]) are scratch.  Fixed summation orders: the result is reproducible.
-__device__ void solve_T_blocked(float* At, float* Dm, float* Lm, float* Ym) {
-  const int tid = threadIdx.x, nt = blockDim.x;
-  if (tid < 64) {   // D_b, one column per thread
-    const int bb = tid >> 4, jj = tid & 15, base = 16 * bb;
-    float* D = Dm + bb * 16 * 17;
-    for (int ii = 0; ii < 16; ++ii) {
-      float t = ii == jj ? 1.f : 0.f;
-      if (ii > jj) {
-        float acc = 0.f;
-        for (int m = jj; m < ii; ++m) acc = fmaf(At[(base + ii) * LDC + base + m], D[m * 17 + jj], acc);
-        t = -acc;
-      }
-      D[ii * 17 + jj] = t;
-    }
-  }
-  __syncthreads();
-  for (int e = tid; e < 64 * 64; e += nt) {   // L = D A_off; X = D
-    const int i = e >> 6, k = e & 63, bi = i >> 4, bk = k >> 4, ii = i & 15;
-    float acc = 0.f;
-    if (bk < bi) {
-      const float* D = Dm + bi * 16 * 17;
-      for (int m = 0; m <= ii; ++m) acc = fmaf(D[ii * 17 + m], At[(16 * bi + m) * LDC + k], acc);
-    }
-    Lm[e] = acc;
-    Ym[e] = bk == bi ? Dm[bi * 16 * 17 + ii * 17 + (k & 15)] : 0.f;
-  }
-  __syncthreads();
-  for (int it = 0; it < 3; ++it) {   // X <- D - L X, ping-ponging between Ym and At
-    const float* X = (it & 1) ? At : Ym;
-    const bool to_at = (it & 1) == 0;
-    for (int e = tid; e < 64 * 64; e += nt) {
-      const int i = e >> 6, j = e & 63, bi = i >> 4, bj = j >> 4;
-      float acc = bi == bj ? Dm[bi * 16 * 17 + (i & 15) * 17 + (j & 15)] : 0.f;
-      if (bj < bi) {
-        float s = 0.f;
-        for (int m = 16 * bj; m < 16 * bi; ++m)
-          s = fmaf(Lm[i * 64 + m], to_at ? X[m * 64 + j] : X[m * LDC + j], s);
-        acc -= s;
-      }
-      if (to_at) At[i * LDC + j] = acc; else Ym[i * 64 + j] = acc;
-    }
-    __syncthreads();
-  }
-}
-
-// ---------------------------------------------------------------- 3b. prep on the tensor cores
-// bf16 I/O with K = V = 128, feeding the tensor-core reverse pass: [Q K^T; K K^T] = [q; k] k^T
-// as one tcgen05.mma (M=128 N=64 K=128, bf16 operands, fp32 in TMEM), then on the CUDA cores
-// P = scale (Q K^T * Gamma) on and below the diagonal and A = strict_lower(diag(beta) K K^T *
-// Gamma), and T = (I + A)^{-1} in fp32 by 16 x 16 blocks.  Out, per chunk and value head in the
-// 16 KB slot of ws.T: T as a bf16 tile (rows j, 64 i per 128-byte row, 128-byte swizzled) and
-// P likewise (rows i, 64 j) 8 KB after it; G in ws.G.  64 TMEM columns, two CTAs per SM.
 namespace tcp {
 using namespace sm100;
 using tcg::put4;
 using tcg::kdesc;
 constexpr int kThreads = 256;
 constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int TD_LD = 20;              // diagonal blocks of T, column-major [4][16][TD_LD]
 constexpr uint32_t OFF_QK = 0;         // [q; k] rows, 2 k-halves x 128 rows x 128 B
 constexpr uint32_t OFF_P = 32768;      // P tile (bf16, scale folded)
 constexpr uint32_t OFF_TT = 40960;     // T tile (bf16)
-constexpr uint32_t OFF_A = 49152;      // A, then T, fp32 [64][LDC]
-constexpr uint32_t OFF_SCR = OFF_A + 64 * LDC * 4;   // solve scratch: D blocks, L, X
-constexpr uint32_t OFF_VEC = OFF_SCR + (4 * 16 * 17 + 2 * 64 * 64) * 4;
+constexpr uint32_t OFF_A = 49152;      // A, fp32 [64][64], 16-byte-group swizzled (a_idx)
+constexpr uint32_t OFF_TD = OFF_A + 64 * 64 * 4;
+constexpr uint32_t OFF_VEC = OFF_TD + 4 * 16 * TD_LD * 4;
 constexpr uint32_t OFF_BAR = OFF_VEC + 2 * 64 * 4;
 constexpr uint32_t SMEM = OFF_BAR + 64 + 1024;
 constexpr uint32_t T_COLS = 64;
+
+// 2^x on the special-function unit (arguments here are <= 0 where the value is kept).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// fp32 A tile: element (i, j) at i * 64 + 4 * ((j / 4) ^ (i % 16)) + j % 4, so that 16-byte
+// groups stay contiguous and the row-parallel accesses of the solve hit distinct banks.
+__device__ __forceinline__ int a_idx(int i, int j) {
+  return i * 64 + ((((j >> 2) ^ (i & 15)) << 2) | (j & 3));
+}
+__device__ __forceinline__ void put_t(uint8_t* tt, int i, int j, float v) {
+  *reinterpret_cast<__nv_bfloat16*>(tt + sw128_offset(i, j)) = __float2bfloat16_rn(v);
+}
+
+// T = (I + A)^{-1} for the strictly lower 64 x 64 A in sA (fp32, a_idx layout), by 16 x 16
+// blocks, into the bf16 tile tt (element (i, j) at sw128_offset(i, j); the caller zeroes it
+// first, so the upper triangle stays zero).  With D_b = (I + A_bb)^{-1} and L = D A_off
+// (block strictly lower, so L^4 = 0): T = (I - L + L^2 - L^3) D.  All 256 threads call it;
+// sTd ([4][16][TD_LD]) is scratch and sA is overwritten.  Fixed summation orders: the result
+// is reproducible.
+__device__ void solve_T_tile(float* sA, float* sTd, uint8_t* tt) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  // step 1: per block row b, one right-looking substitution (I + A_bb) X = R for the
+  //      right-hand sides R = [I | A_b0 | .. | A_b,b-1], one column per thread (16 (b + 1)
+  //      columns in block row b, 160 in all): X = [D_b | L_b0 | ..].  D_b goes to sTd and
+  //      to the diagonal block of T; L_bq replaces A_bq column by column.
+  if (tid < 160) {
+    const int b = tid < 16 ? 0 : (tid < 48 ? 1 : (tid < 96 ? 2 : 3));
+    const int j = tid - 8 * b * (b + 1);            // column of R
+    const bool ident = j < 16;
+    const int cq = j - 16;                          // column of A
+    // A[16 b + i][16 b + m] = ab[i / 4][64 i + 4 ((m / 4) ^ (i % 4)) + m % 4]
+    const float* ab[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) ab[k] = sA + 1024 * b + (((4 * b) ^ (4 * k)) << 2);
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = ident ? ((i == j) ? 1.f : 0.f) : sA[a_idx(16 * b + i, cq)];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {   // columns m = 4 g .. 4 g + 3 of A_bb, one float4 per row
+      float4 ag[16];
+#pragma unroll
+      for (int i = 4 * g + 1; i < 16; ++i)
+        ag[i] = *reinterpret_cast<const float4*>(ab[i >> 2] + 64 * i + ((g ^ (i & 3)) << 2));
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int m = 4 * g + e;
+#pragma unroll
+        for (int i = m + 1; i < 16; ++i) {
+          const float am = e == 0 ? ag[i].x : (e == 1 ? ag[i].y : (e == 2 ? ag[i].z : ag[i].w));
+          x[i] = fmaf(-am, x[m], x[i]);
+        }
+      }
+    }
+    if (!ident) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) sA[a_idx(16 * b + i, cq)] = x[i];
+    } else {
+#pragma unroll
+      for (int i4 = 0; i4 < 4; ++i4)
+        *reinterpret_cast<float4*>(&sTd[(b * 16 + j) * TD_LD + 4 * i4]) =
+            make_float4(x[4 * i4], x[4 * i4 + 1], x[4 * i4 + 2], x[4 * i4 + 3]);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) put_t(tt, 16 * b + i, 16 * b + j, x[i]);   // column j of D_b
+    }
+  }
+  __syncthreads();
+  // step 2: (L^2)_20 = L_21 L_10, (L^2)_31 = L_32 L_21, (L^2)_30 - (L^3)_30 with
+  //      (L^3)_30 = (L^2)_31 L_10; thread (r, c) = (tid / 16, tid % 16), so a half-warp holds
+  //      a whole row of (L^2)_31 and passes it round by shuffles.  Results go to the
+  //      upper-triangle blocks (0, 2), (1, 3), (0, 3) of sA, which nothing else uses.
+  {
+    const int r = tid >> 4, c = tid & 15, hb = lane & 16;
+    float l21r[16], l32r[16], l31r[16];   // rows r of L_21, L_32, L_31
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float4 p = *reinterpret_cast<const float4*>(&sA[(32 + r) * 64 + (((4 + u) ^ r) << 2)]);
+      const float4 q = *reinterpret_cast<const float4*>(&sA[(48 + r) * 64 + (((8 + u) ^ r) << 2)]);
+      const float4 w = *reinterpret_cast<const float4*>(&sA[(48 + r) * 64 + (((4 + u) ^ r) << 2)]);
+      l21r[4 * u] = p.x; l21r[4 * u + 1] = p.y; l21r[4 * u + 2] = p.z; l21r[4 * u + 3] = p.w;
+      l32r[4 * u] = q.x; l32r[4 * u + 1] = q.y; l32r[4 * u + 2] = q.z; l32r[4 * u + 3] = q.w;
+      l31r[4 * u] = w.x; l31r[4 * u + 1] = w.y; l31r[4 * u + 2] = w.z; l31r[4 * u + 3] = w.w;
+    }
+    float l10c[16];
+    float m20 = 0.f, m31 = 0.f, m30 = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      l10c[k] = sA[a_idx(16 + k, c)];
+      m20 = fmaf(l21r[k], l10c[k], m20);
+      m31 = fmaf(l32r[k], sA[a_idx(32 + k, 16 + c)], m31);
+      m30 = fmaf(l31r[k], l10c[k], fmaf(l32r[k], sA[a_idx(32 + k, c)], m30));
+    }
+    float n30 = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) n30 = fmaf(__shfl_sync(0xffffffffu, m31, k + hb), l10c[k], n30);
+    sA[a_idx(r, 32 + c)] = m20;
+    sA[a_idx(16 + r, 48 + c)] = m31;
+    sA[a_idx(r, 48 + c)] = m30 - n30;
+  }
+  __syncthreads();
+  // step 3: T_bq = X_bq D_q, X = -L + L^2 - L^3, for the six blocks below the diagonal;
+  //      thread (r, c) computes T_bq[r][c] for all of them
+  {
+    const int r = tid >> 4, c = tid & 15;
+    float dq[3][16];   // column c of D_0, D_1, D_2
+#pragma unroll
+    for (int q = 0; q < 3; ++q)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float4 d4 = *reinterpret_cast<const float4*>(&sTd[(q * 16 + c) * TD_LD + 4 * u]);
+        dq[q][4 * u] = d4.x; dq[q][4 * u + 1] = d4.y; dq[q][4 * u + 2] = d4.z; dq[q][4 * u + 3] = d4.w;
+      }
+#pragma unroll
+    for (int pr = 0; pr < 6; ++pr) {   // (1,0) (2,0) (3,0) (2,1) (3,1) (3,2)
+      const int b = pr < 3 ? pr + 1 : (pr < 5 ? pr - 1 : 3);
+      const int q = pr < 3 ? 0 : (pr < 5 ? 1 : 2);
+      float xr[16];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float4 l4 = *reinterpret_cast<const float4*>(&sA[(16 * b + r) * 64 + (((4 * q + u) ^ r) << 2)]);
+        xr[4 * u] = -l4.x; xr[4 * u + 1] = -l4.y; xr[4 * u + 2] = -l4.z; xr[4 * u + 3] = -l4.w;
+        if (b - q >= 2) {   // + (L^2 - L^3)_bq, stored at block (q, b)
+          const float4 m4 = *reinterpret_cast<const float4*>(&sA[(16 * q + r) * 64 + (((4 * b + u) ^ r) << 2)]);
+          xr[4 * u] += m4.x; xr[4 * u + 1] += m4.y; xr[4 * u + 2] += m4.z; xr[4 * u + 3] += m4.w;
+        }
+      }
+      float ta = 0.f, tb = 0.f;
+#pragma unroll
+      for (int k = 0; k < 16; k += 2) {
+        ta = fmaf(xr[k], dq[q][k], ta);
+        tb = fmaf(xr[k + 1], dq[q][k + 1], tb);
+      }
+      put_t(tt, 16 * b + r, 16 * q + c, ta + tb);
+    }
+  }
+}
+
 
 __global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(const ChunkArgs a, const BwdArgs b,
                                                                   BwdWs ws) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(sm);
-  float* At = reinterpret_cast<float*>(sm + OFF_A);
-  float* scr = reinterpret_cast<float*>(sm + OFF_SCR);
+  float* sA = reinterpret_cast<float*>(sm + OFF_A);
+  float* sTd = reinterpret_cast<float*>(sm + OFF_TD);
   float* G = reinterpret_cast<float*>(sm + OFF_VEC);
   float* bt = G + 64;
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
@@ -1469,6 +1553,9 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(const ChunkArg
       put4(sm + OFF_QK, 16384, warp + 8 * s, 4 * lane, x[s]);
     }
   }
+  // the T tile starts from zero: the solve writes its lower triangle only
+  for (int e = tid; e < 8192 / 16; e += kThreads)
+    reinterpret_cast<uint4*>(sm + OFF_TT)[e] = make_uint4(0u, 0u, 0u, 0u);
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -1495,25 +1582,37 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(const ChunkArg
   tc_fence_after();
   const uint32_t loff = (uint32_t)(32 * (warp & 3)) << 16;
   const int row = 32 * (warp & 3) + lane;
-  {  // P (rows 0-63, bf16, scale folded) and A (rows 64-127, fp32); warps w, w + 4 split columns
-    const int part = warp >> 2;
+  {  // P (rows 0-63, bf16, scale folded) and A (rows 64-127, fp32, a_idx layout); warps w and
+     // w + 4 split the columns.  Rows 0-31 against columns 32-63 lie above the diagonal: zero.
+    const int part = warp >> 2, j0 = 32 * part;
+    const bool zero_tile = ((warp & 1) == 0) && part == 1;
     float x[32];
-    tmem_ld32(tb + loff + 32 * part, x);
-    if (row < 64) {
-      const int i = row;
+    tmem_ld32(tb + loff + j0, x);
+    const int i = row & 63;
+    const float gi = G[i];
+    const int lim = row < 64 ? i + 1 : i;   // P keeps j <= i, A keeps j < i
+    const float f = row < 64 ? a.scale : bt[i];
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
-        const int j = 32 * part + jj;
-        const float p = j <= i ? a.scale * x[jj] * expf(G[i] - G[j]) : 0.f;
-        *reinterpret_cast<__nv_bfloat16*>(sm + OFF_P + sw128_offset(i, j)) = __float2bfloat16_rn(p);
+    for (int jj = 0; jj < 32; ++jj) {
+      const int j = j0 + jj;
+      const float e = f * x[jj] * ex2((gi - G[j]) * kLog2e);
+      x[jj] = (!zero_tile && j < lim) ? e : 0.f;
+    }
+    if (row < 64) {
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        uint4 u;
+        u.x = tcg::pack2(x[8 * m], x[8 * m + 1]);
+        u.y = tcg::pack2(x[8 * m + 2], x[8 * m + 3]);
+        u.z = tcg::pack2(x[8 * m + 4], x[8 * m + 5]);
+        u.w = tcg::pack2(x[8 * m + 6], x[8 * m + 7]);
+        *reinterpret_cast<uint4*>(sm + OFF_P + sw128_offset(i, j0 + 8 * m)) = u;
       }
     } else {
-      const int i = row - 64;
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
-        const int j = 32 * part + jj;
-        At[i * LDC + j] = j < i ? bt[i] * x[jj] * expf(G[i] - G[j]) : 0.f;
-      }
+      for (int m = 0; m < 8; ++m)
+        *reinterpret_cast<float4*>(&sA[a_idx(i, j0 + 4 * m)]) =
+            make_float4(x[4 * m], x[4 * m + 1], x[4 * m + 2], x[4 * m + 3]);
     }
   }
   tc_fence_before();
@@ -1522,12 +1621,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(const ChunkArg
     tc_fence_after();
     tmem_dealloc(tb, T_COLS);
   }
-  solve_T_blocked(At, scr, scr + 4 * 16 * 17, scr + 4 * 16 * 17 + 64 * 64);
-  for (int e = tid; e < 64 * 32; e += kThreads) {   // T as a bf16 tile: rows j, 64 i
-    const int j = e >> 5, i = 2 * (e & 31);
-    *reinterpret_cast<uint32_t*>(sm + OFF_TT + sw128_offset(j, i)) =
-        tcg::pack2(At[j * LDC + i], At[j * LDC + i + 1]);
-  }
+  solve_T_tile(sA, sTd, sm + OFF_TT);
   __syncthreads();
   uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(ws.T + ch * 64 * 64));
   const uint4* srcT = reinterpret_cast<const uint4*>(sm + OFF_TT);
