@@ -68,6 +68,8 @@ constexpr uint32_t OFF_KT = 131072;     // K~^T: the K rows scaled by exp(G_last
 constexpr uint32_t OFF_A = 147456;      // fp32 A [64][64], 16-byte-group swizzled; the solve
                                         // overwrites its strictly-lower blocks with those of T
 constexpr uint32_t OFF_P = 163840;      // 2 x P, K-major B [64 i][64 j]
+constexpr uint32_t OFF_REC = 180224;    // record mode: staging of the entry-state tile's second
+                                        // half, then of the U' tile (16 KB)
 constexpr uint32_t OFF_TW = 196608;     // (T diag(beta exp(G) r_k))^T, MN-major B [64 j][64 i]
 constexpr uint32_t OFF_TU = 204800;     // (T diag(beta))^T, MN-major B
 constexpr uint32_t OFF_VEC = 212992;    // 2 x per-token fp32 vectors [8][64]
@@ -104,6 +106,7 @@ constexpr uint32_t OFF_TSLOT = OFF_FLAG + 8;              // TMEM base address
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(OFF_TSLOT + 4 <= SMEM_USED, "barrier block");
 static_assert(STAGE_TX == 49152, "stage bytes");
+static_assert(OFF_P + 2 * 8192 <= OFF_REC && OFF_REC + 16384 <= OFF_TW, "record staging");
 
 // fp32 A tile: element (i, j) at i * 64 + 4 * ((j / 4) ^ (i % 16)) + j % 4, so that
 // 16-byte groups stay contiguous and the row-parallel accesses of the solve hit
@@ -548,17 +551,49 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
                  sdesc_sw128(sbase + OFF_TU + ks * 2048, 8192, 1024), id, ks > 0);
       }
     }
+    // ---- record mode: the entry state as a bf16 tile, rows dk, 64 dv per 128-byte row in two
+    //      16 KB halves, 128-byte swizzled (element (dk, dv) at (dv / 64) 16384 + dk 128 +
+    //      ((dv % 64 / 8) xor (dk % 8)) 16 + (dv % 8) 2): 16x256b TMEM loads give each thread the
+    //      stmatrix .trans fragment (as in the output epilogue), the halves are staged at OFF_S
+    //      and OFF_REC and leave by two bulk copies
+    if (kRecord) {
+      const int mblk = lane >> 3, rr = lane & 7;
+      const int d0 = 32 * wq + 8 * mblk;
+      const uint32_t st_base = sbase + (d0 < 64 ? OFF_S : OFF_REC) + rr * 128 +
+                               ((((d0 & 63) >> 3) ^ rr) << 4);
+#pragma unroll 1
+      for (int pass = 0; pass < 4; ++pass) {   // dk 32 pass .. 32 pass + 31
+        uint32_t a0[16], a1[16];
+        tmem_ld16x256b_x4(tbase + lane_off + COL_S + 32 * pass, a0);                 // dv 0-15
+        tmem_ld16x256b_x4(tbase + lane_off + (16u << 16) + COL_S + 32 * pass, a1);   // dv 16-31
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {   // dk group 4 pass + j
+          uint32_t f[4];
+#pragma unroll
+          for (int mm = 0; mm < 4; ++mm) {
+            const uint32_t* x = (mm >> 1) ? a1 : a0;
+            const int k = 4 * j + 2 * (mm & 1);
+            __nv_bfloat162 p = __floats2bfloat162_rn(__uint_as_float(x[k]), __uint_as_float(x[k + 1]));
+            f[mm] = *reinterpret_cast<uint32_t*>(&p);
+          }
+          stmatrix_x4_trans(st_base + (4 * pass + j) * 1024, f);
+        }
+      }
+      fence_proxy_async_smem();
+      group_sync(kBarState, kStateThreads);
+      if (leader) {
+        uint8_t* g = reinterpret_cast<uint8_t*>(a.rec_states +
+                                                ((size_t)(rec0 + c) * a.Hv + h) * (size_t)(DK * DV));
+        bulk_store(g, sm + OFF_S, 16384);
+        bulk_store(g + 16384, sm + OFF_REC, 16384);
+        tma_store_commit();
+      }
+    }
     // ---- S (entry state) -> bf16 S^T in the O2 columns (the next product's A operand);
-    //      S <- exp(G_last) S in TMEM.  Record mode also stores the entry state as a bf16
-    //      tile: rows dk, 64 dv per 128-byte row in two halves, 128-byte swizzled (element
-    //      (dk, dv) at (dv / 64) 16384 + dk 128 + ((dv % 64 / 8) xor (dk % 8)) 16 + (dv % 8) 2)
+    //      S <- exp(G_last) S in TMEM
     {
       const float dl = ex2(vec[VEC_G + L - 1]);
-      uint8_t* rec_s = kRecord ? reinterpret_cast<uint8_t*>(a.rec_states +
-                                                            ((size_t)(rec0 + c) * a.Hv + h) * (size_t)(DK * DV)) +
-                                     (row >> 6) * 16384 + (row & 7) * 2
-                               : nullptr;
-      const uint32_t sx = (uint32_t)((row & 63) >> 3) << 4;   // swizzle: sx xor ((dk % 8) 16)
 #pragma unroll
       for (int pair = 0; pair < 2; ++pair) {
         float pk[32];
@@ -567,14 +602,6 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
           float x[32];
           const uint32_t col = COL_S + 32 * (2 * pair + sub);
           tmem_ld32(tbase + lane_off + col, x);
-          if (kRecord) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int dk = 32 * (2 * pair + sub) + j;   // dk % 8 == j % 8
-              *reinterpret_cast<__nv_bfloat16*>(rec_s + dk * 128 + (sx ^ ((j & 7) << 4))) =
-                  __float2bfloat16_rn(x[j]);
-            }
-          }
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
             __nv_bfloat162 p2 = __floats2bfloat162_rn(x[2 * jj], x[2 * jj + 1]);
@@ -689,26 +716,49 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     if (group_sync_or(kBarState, kStateThreads, !ok || flag_set(flag))) { failed = true; break; }
     tc_fence_after();
 
-    // ---- U'^T -> bf16, packed into the first 32 of its own TMEM columns (A operand);
-    //      record mode stores U' as a bf16 tile: rows = the chunk's 64 tokens (zero from L on),
-    //      64 dv per 128-byte row in two halves of 8 KB, 128-byte swizzled
+    // ---- record mode: U' as a bf16 tile, rows = the chunk's 64 tokens (zero from L on), 64 dv
+    //      per 128-byte row in two 8 KB halves, 128-byte swizzled; staged at OFF_REC once the
+    //      entry-state tile has left it, then one bulk copy
+    if (kRecord) {
+      if (leader) tma_store_wait_read();
+      group_sync(kBarState, kStateThreads);
+      const int mblk = lane >> 3, rr = lane & 7;
+      const int d0 = 32 * wq + 8 * mblk;
+      const uint32_t st_base = sbase + OFF_REC + (d0 >> 6) * 8192 + rr * 128 +
+                               ((((d0 & 63) >> 3) ^ rr) << 4);
+#pragma unroll 1
+      for (int pass = 0; pass < 2; ++pass) {   // tokens 32 pass .. 32 pass + 31
+        uint32_t a0[16], a1[16];
+        tmem_ld16x256b_x4(tbase + lane_off + COL_U + 32 * pass, a0);
+        tmem_ld16x256b_x4(tbase + lane_off + (16u << 16) + COL_U + 32 * pass, a1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {   // token group 4 pass + j; this lane's tokens t, t + 1
+          const int t = 32 * pass + 8 * j + 2 * (lane & 3);
+          uint32_t f[4];
+#pragma unroll
+          for (int mm = 0; mm < 4; ++mm) {
+            const uint32_t* x = (mm >> 1) ? a1 : a0;
+            const int k = 4 * j + 2 * (mm & 1);
+            __nv_bfloat162 p = __floats2bfloat162_rn(t < L ? __uint_as_float(x[k]) : 0.f,
+                                                     t + 1 < L ? __uint_as_float(x[k + 1]) : 0.f);
+            f[mm] = *reinterpret_cast<uint32_t*>(&p);
+          }
+          stmatrix_x4_trans(st_base + (4 * pass + j) * 1024, f);
+        }
+      }
+      fence_proxy_async_smem();
+      group_sync(kBarState, kStateThreads);
+      if (leader) {
+        bulk_store(a.rec_u + ((size_t)(rec0 + c) * a.Hv + h) * (size_t)(kChunk * DV), sm + OFF_REC, 16384);
+        tma_store_commit();
+      }
+    }
+    // ---- U'^T -> bf16, packed into the first 32 of its own TMEM columns (A operand)
     {
       float x[32], y[32], pk[32];
       tmem_ld32(tbase + lane_off + COL_U, x);
       tmem_ld32(tbase + lane_off + COL_U + 32, y);
-      if (kRecord) {
-        uint8_t* ru = reinterpret_cast<uint8_t*>(a.rec_u + ((size_t)(rec0 + c) * a.Hv + h) *
-                                                               (size_t)(kChunk * DV)) +
-                      (row >> 6) * 8192 + (row & 7) * 2;
-        const uint32_t sx = (uint32_t)((row & 63) >> 3) << 4;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          *reinterpret_cast<__nv_bfloat16*>(ru + j * 128 + (sx ^ ((j & 7) << 4))) =
-              __float2bfloat16_rn(j < L ? x[j] : 0.f);
-          *reinterpret_cast<__nv_bfloat16*>(ru + (j + 32) * 128 + (sx ^ ((j & 7) << 4))) =
-              __float2bfloat16_rn(j + 32 < L ? y[j] : 0.f);
-        }
-      }
 #pragma unroll
       for (int jj = 0; jj < 16; ++jj) {
         __nv_bfloat162 p0 = __floats2bfloat162_rn(x[2 * jj], x[2 * jj + 1]);
