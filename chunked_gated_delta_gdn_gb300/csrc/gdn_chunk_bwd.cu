@@ -1066,19 +1066,25 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(const ChunkArg
     tmem_alloc(tslot, T_COLS);
     tmem_relinquish();
   }
-  load_gates(a, t0, L, h, G, bt);
   // ---- operands to shared memory
-  // Every global load of a batch is issued before any of it is used (the loads of one
-  // thread are independent; issuing them one loop trip at a time would expose the memory
-  // latency once per trip).
-  {  // normalised [q; k] rows: warp w takes rows w + 8 s
-    float x[16][4];
+  // Every global load is issued before any of it is used: the q, k and dO rows of this
+  // thread in one batch, then the gates (warp 0) while they are in flight (issuing them one
+  // loop trip or one batch at a time would expose the memory latency once per trip).
+  {  // normalised [q; k] rows: warp w takes rows w + 8 s; dO rows i into rows 0-63 of [dO; dX]
+    float x[16][4], o4[8][4];
 #pragma unroll
     for (int s = 0; s < 16; ++s) {
       const int r = warp + 8 * s, i = r & 63;
       x[s][0] = x[s][1] = x[s][2] = x[s][3] = 0.f;
       if (i < L) load4b(r < 64 ? a.q : a.k, ((size_t)(t0 + i) * a.Hqk + hq) * 128 + 4 * lane, x[s]);
     }
+#pragma unroll
+    for (int s8 = 0; s8 < 8; ++s8) {
+      const int i = warp + 8 * s8;
+      o4[s8][0] = o4[s8][1] = o4[s8][2] = o4[s8][3] = 0.f;
+      if (i < L) load4b(b.d_o, ((size_t)(t0 + i) * Hv + h) * 128 + 4 * lane, o4[s8]);
+    }
+    load_gates(a, t0, L, h, G, bt);
 #pragma unroll
     for (int s = 0; s < 16; ++s) {
       float rn = 1.f;
@@ -1088,15 +1094,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(const ChunkArg
 #pragma unroll
       for (int q = 0; q < 4; ++q) x[s][q] *= rn;
       put4(sm + OFF_QK, 16384, warp + 8 * s, 4 * lane, x[s]);
-    }
-  }
-  {  // dO rows i (bf16) into rows 0-63 of [dO; dX]
-    float o4[8][4];
-#pragma unroll
-    for (int s8 = 0; s8 < 8; ++s8) {
-      const int i = warp + 8 * s8;
-      o4[s8][0] = o4[s8][1] = o4[s8][2] = o4[s8][3] = 0.f;
-      if (i < L) load4b(b.d_o, ((size_t)(t0 + i) * Hv + h) * 128 + 4 * lane, o4[s8]);
     }
 #pragma unroll
     for (int s8 = 0; s8 < 8; ++s8) put4(sm + OFF_OX, 16384, warp + 8 * s8, 4 * lane, o4[s8]);
@@ -1533,8 +1530,8 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(const ChunkArg
     tmem_alloc(tslot, T_COLS);
     tmem_relinquish();
   }
-  load_gates(a, t0, L, h, G, bt);
-  {  // normalised [q; k] rows (bf16), every load of a thread issued first
+  {  // normalised [q; k] rows (bf16), every load of a thread issued first, then the gates
+     // (warp 0) while they are in flight
     float x[16][4];
 #pragma unroll
     for (int s = 0; s < 16; ++s) {
@@ -1542,6 +1539,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(const ChunkArg
       x[s][0] = x[s][1] = x[s][2] = x[s][3] = 0.f;
       if (i < L) load4b(r < 64 ? a.q : a.k, ((size_t)(t0 + i) * a.Hqk + hq) * 128 + 4 * lane, x[s]);
     }
+    load_gates(a, t0, L, h, G, bt);
 #pragma unroll
     for (int s = 0; s < 16; ++s) {
       float rn = 1.f;
