@@ -1656,8 +1656,41 @@ constexpr uint32_t STAGE_TX = 3 * 16384 + 2 * 8192;
 constexpr uint32_t OFF_VEC = 2 * STAGE;              // per stage: G[64], beta[64]
 constexpr uint32_t OFF_RED = OFF_VEC + 2 * 128 * 4;  // [4 warps][64]
 constexpr uint32_t OFF_BAR = OFF_RED + 4 * 64 * 4;
-constexpr uint32_t SMEM = OFF_BAR + 64 + 1024;
+constexpr uint32_t OFF_STG_S = (OFF_BAR + 64 + 1023) / 1024 * 1024;   // staging: the dS tile (32 KB)
+constexpr uint32_t OFF_STG_X = OFF_STG_S + 32768;                     // and the dX tile (16 KB)
+constexpr uint32_t SMEM = OFF_STG_X + 16384 + 1024;
+static_assert(SMEM <= 232448, "shared memory budget");
 constexpr uint32_t C_S = 0, C_SB = 128, C_Y = 192, C_U = 256, C_X = 320, T_COLS = 512;
+
+// Stage `passes` x 32 TMEM columns starting at `col` (fp32, lane = v) as bf16 rows of a
+// 128-byte-swizzled tile at shared address `tile`: TMEM column j of lane v goes to row j,
+// element v of a 64-element half (halves `half` bytes apart).  16x256b loads hand each thread
+// the fragment of stmatrix .trans (rows j, 2 (t % 4) and + 1 of each 8-column group; v = t / 4
+// and t / 4 + 8 of each 16-lane half), which writes the 8 x 8 blocks transposed.
+__device__ __forceinline__ void stage_tile(uint32_t tb, uint32_t loff, uint32_t col, int passes,
+                                           uint32_t tile, uint32_t half, int warp, int lane) {
+  const int mblk = lane >> 3, rr = lane & 7;
+  const int d0 = 32 * warp + 8 * mblk;
+  const uint32_t st_base = tile + (d0 >> 6) * half + rr * 128 + ((((d0 & 63) >> 3) ^ rr) << 4);
+#pragma unroll 1
+  for (int pass = 0; pass < passes; ++pass) {
+    uint32_t a0[16], a1[16];
+    tmem_ld16x256b_x4(tb + loff + col + 32 * pass, a0);                 // v 0-15 of the warp
+    tmem_ld16x256b_x4(tb + loff + (16u << 16) + col + 32 * pass, a1);   // v 16-31
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {   // column group 4 pass + j
+      uint32_t f[4];
+#pragma unroll
+      for (int mm = 0; mm < 4; ++mm) {
+        const uint32_t* x = (mm >> 1) ? a1 : a0;
+        const int k = 4 * j + 2 * (mm & 1);
+        f[mm] = tcg::pack2(__uint_as_float(x[k]), __uint_as_float(x[k + 1]));
+      }
+      stmatrix_x4_trans(st_base + (4 * pass + j) * 1024, f);
+    }
+  }
+}
 
 __device__ __forceinline__ void issue_stage(uint8_t* st, uint64_t* bar, const CUtensorMap* tq,
                                             const CUtensorMap* tk, const CUtensorMap* to,
@@ -1768,7 +1801,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
   }
   uint32_t ph = 0;
   bool failed = false;
-  const uint32_t sxv = (uint32_t)((v & 63) >> 3) << 4;   // this lane's swizzle term
   for (int it = 0; it < nch; ++it) {
     const int qc = nch - 1 - it, s = it & 1;
     const int t0 = bos + qc * C, L = min(C, eos - t0);
@@ -1869,13 +1901,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
       for (int ks = 0; ks < 4; ++ks)
         mma_bf16_ta(tb + C_X, tb + C_U + 8 * ks, tcg::mndesc(sst + ST_T + ks * 2048, 8192), ix, ks > 0);
       mma_commit(mmab);
+      tma_store_wait_read();   // the previous chunk's dS and dX tiles have left the staging buffers
     }
     if (tid == 0) ok = mbar_wait(mmab, ph, kWaitNs);
     ph ^= 1u;
     if (__syncthreads_or(!ok)) { failed = true; break; }
     tc_fence_after();
-    {  // dX: the grad pass's bf16 tile, dv = beta dX, the row dots dX_i . v_i; bf16 dX^T in C_X
-      uint8_t* xt = reinterpret_cast<uint8_t*>(ws.dX + ch * 64 * 128) + (v >> 6) * 8192 + (v & 7) * 2;
+    // the grad pass's bf16 tiles, staged for bulk copies: dX (rows = the chunk's tokens, 64 v
+    // per 128-byte row in two 8 KB halves) and dS, the gradient of the chunk's exit state (rows d,
+    // two 16 KB halves), both 128-byte swizzled
+    stage_tile(tb, loff, C_X, 2, sb + OFF_STG_X, 8192, warp, lane);
+    stage_tile(tb, loff, C_S, 4, sb + OFF_STG_S, 16384, warp, lane);
+    fence_proxy_async_smem();
+    {  // dv = beta dX, the row dots dX_i . v_i; bf16 dX^T in C_X
       float pk[32];
 #pragma unroll
       for (int p = 0; p < 2; ++p) {
@@ -1891,7 +1929,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
           const int i = 32 * p + jj;
-          *reinterpret_cast<__nv_bfloat16*>(xt + i * 128 + (sxv ^ ((i & 7) << 4))) = __float2bfloat16_rn(x[jj]);
           pv[jj] *= x[jj];
           if (i < L) store_elem(b.dv, ((size_t)(t0 + i) * Hv + h) * 128 + v, bt[i] * x[jj], a.io_dtype);
         }
@@ -1901,25 +1938,27 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
       }
       tmem_st32(tb + loff + C_X, pk);
     }
-    {  // the bf16 dS tile (gradient of the chunk's exit state), then dS^T <- gamma_L dS^T
-      uint8_t* stile = reinterpret_cast<uint8_t*>(ws.dS + ch * 128 * 128) + (v >> 6) * 16384 + (v & 7) * 2;
+    {  // dS^T <- gamma_L dS^T
       const float gL = expf(G[L - 1]);
 #pragma unroll
       for (int part = 0; part < 4; ++part) {
         float x[32];
         tmem_ld32(tb + loff + C_S + 32 * part, x);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int d = 32 * part + j;
-          *reinterpret_cast<__nv_bfloat16*>(stile + d * 128 + (sxv ^ ((j & 7) << 4))) = __float2bfloat16_rn(x[j]);
-          x[j] *= gL;
-        }
+        for (int j = 0; j < 32; ++j) x[j] *= gL;
         tmem_st32(tb + loff + C_S + 32 * part, x);
       }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (tid == 0) {
+      uint8_t* gs = reinterpret_cast<uint8_t*>(ws.dS + ch * 128 * 128);
+      bulk_store(gs, sm + OFF_STG_S, 16384);
+      bulk_store(gs + 16384, sm + OFF_STG_S + 16384, 16384);
+      bulk_store(ws.dX + ch * 64 * 128, sm + OFF_STG_X, 16384);
+      tma_store_commit();
+    }
     if (tid < 64) {   // the row dots, summed over the four warps in a fixed order
       float* xv = ws.XV + ch * 4 * 64;
       xv[tid] = (red[tid] + red[64 + tid]) + (red[128 + tid] + red[192 + tid]);
@@ -1952,6 +1991,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
     __syncthreads();
     tc_fence_after();
   }
+  if (tid == 0) tma_store_wait_all();   // the staged tiles are written before the CTA exits
   if (failed) {
     if (tid == 0) report(a.dev_status, GDN_DEV_TIMEOUT);
   } else if (b.d_initial) {
