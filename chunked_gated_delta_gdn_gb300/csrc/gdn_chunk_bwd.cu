@@ -1650,13 +1650,14 @@ namespace tcr {
 using namespace sm100;
 constexpr int kThreads = 128;
 constexpr uint64_t kWaitNs = 2000000000ull;
-constexpr uint32_t ST_Q = 0, ST_K = 16384, ST_KG = 32768, ST_DO = 49152, ST_T = 65536, ST_P = 73728;
+constexpr uint32_t ST_Q = 0, ST_K = 16384, ST_V = 32768, ST_DO = 49152, ST_T = 65536, ST_P = 73728;
 constexpr uint32_t STAGE = 81920;
-constexpr uint32_t STAGE_TX = 3 * 16384 + 2 * 8192;
+constexpr uint32_t STAGE_TX = 4 * 16384 + 2 * 8192;
 constexpr uint32_t OFF_VEC = 2 * STAGE;              // per stage: G[64], beta[64]
 constexpr uint32_t OFF_RED = OFF_VEC + 2 * 128 * 4;  // [4 warps][64]
 constexpr uint32_t OFF_BAR = OFF_RED + 4 * 64 * 4;
-constexpr uint32_t OFF_STG_S = (OFF_BAR + 64 + 1023) / 1024 * 1024;   // staging: the dS tile (32 KB)
+constexpr uint32_t OFF_FG = OFF_BAR + 64;                             // -gamma beta per token
+constexpr uint32_t OFF_STG_S = (OFF_FG + 256 + 1023) / 1024 * 1024;   // staging: the dS tile (32 KB)
 constexpr uint32_t OFF_STG_X = OFF_STG_S + 32768;                     // and the dX tile (16 KB)
 constexpr uint32_t SMEM = OFF_STG_X + 16384 + 1024;
 static_assert(SMEM <= 232448, "shared memory budget");
@@ -1693,13 +1694,15 @@ __device__ __forceinline__ void stage_tile(uint32_t tb, uint32_t loff, uint32_t 
 }
 
 __device__ __forceinline__ void issue_stage(uint8_t* st, uint64_t* bar, const CUtensorMap* tq,
-                                            const CUtensorMap* tk, const CUtensorMap* to,
-                                            const uint8_t* tp, int t, int hq, int h) {
+                                            const CUtensorMap* tk, const CUtensorMap* tv,
+                                            const CUtensorMap* to, const uint8_t* tp, int t,
+                                            int hq, int h) {
   mbar_arrive_expect_tx(bar, STAGE_TX);
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
     tma_load_3d(st + ST_Q + hh * 8192, tq, bar, 64 * hh, hq, t);
     tma_load_3d(st + ST_K + hh * 8192, tk, bar, 64 * hh, hq, t);
+    tma_load_3d(st + ST_V + hh * 8192, tv, bar, 64 * hh, h, t);
     tma_load_3d(st + ST_DO + hh * 8192, to, bar, 64 * hh, h, t);
   }
   bulk_load(st + ST_T, tp, 8192, bar);
@@ -1739,7 +1742,8 @@ __device__ __forceinline__ float lane_transpose_sum(float (&v)[32], int lane) {
 
 __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-    const __grid_constant__ CUtensorMap tmO, const ChunkArgs a, const BwdArgs b, BwdWs ws) {
+    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+    const ChunkArgs a, const BwdArgs b, BwdWs ws) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(sm);
@@ -1767,10 +1771,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
     fence_mbar_init();
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmO);
     for (int it = 0; it < 2 && it < nch; ++it) {
       const int qc = nch - 1 - it;
-      issue_stage(sm + it * STAGE, &full[it], &tmQ, &tmK, &tmO,
+      issue_stage(sm + it * STAGE, &full[it], &tmQ, &tmK, &tmV, &tmO,
                   reinterpret_cast<const uint8_t*>(ws.T + ((size_t)(first + qc) * Hv + h) * 64 * 64),
                   bos + qc * C, hq, h);
     }
@@ -1812,7 +1817,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
     bool ok = true;
     if (tid == 0) ok = mbar_wait(&full[s], (uint32_t)(it >> 1) & 1u, kWaitNs);
     if (__syncthreads_or(!ok)) { failed = true; break; }
-    {  // norms; r_k k, -gamma beta r_k k, scale gamma r_q q in place; dO rows >= L zeroed
+    {  // norms; r_k k and scale gamma r_q q in place, -gamma beta per token; dO rows >= L zeroed
       const int i = tid >> 1, hh = tid & 1;
       uint8_t* qrow = st + ST_Q + hh * 8192 + i * 128;
       uint8_t* krow = st + ST_K + hh * 8192 + i * 128;
@@ -1837,12 +1842,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
       const float gi = expf(G[i]);
       const float fq = i < L ? a.scale * gi * rq : 0.f;
       const float fk = i < L ? rk : 0.f;
-      const float fg = i < L ? -gi * bt[i] * rk : 0.f;
-      uint8_t* grow = st + ST_KG + hh * 8192 + i * 128;
+      // (the k rows already carry r_k)
+      if (hh == 0) reinterpret_cast<float*>(sm + OFF_FG)[i] = i < L ? -gi * bt[i] : 0.f;
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8) {
-        *reinterpret_cast<uint4*>(grow + 16 * c8) = *reinterpret_cast<const uint4*>(krow + 16 * c8);
-        tcg::scale8(grow + 16 * c8, fg);
         tcg::scale8(krow + 16 * c8, fk);
         tcg::scale8(qrow + 16 * c8, fq);
         if (i >= L)
@@ -1913,17 +1916,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
     stage_tile(tb, loff, C_X, 2, sb + OFF_STG_X, 8192, warp, lane);
     stage_tile(tb, loff, C_S, 4, sb + OFF_STG_S, 16384, warp, lane);
     fence_proxy_async_smem();
-    {  // dv = beta dX, the row dots dX_i . v_i; bf16 dX^T in C_X
+    {  // dv = beta dX, the row dots dX_i . v_i (v from the stage's tile); bf16
+       // dX^T diag(-gamma beta) in C_X, the A operand of the dS update
+      const float* fgv = reinterpret_cast<const float*>(sm + OFF_FG);
+      const uint8_t* vcol = st + ST_V + (v >> 6) * 8192 + (v & 7) * 2;
+      const uint32_t sxv = (uint32_t)((v & 63) >> 3);   // this lane's 16-byte group before the swizzle
       float pk[32];
 #pragma unroll
       for (int p = 0; p < 2; ++p) {
         float x[32], pv[32];
-        // the v loads first, all in flight together (a store to dv in between would order
-        // each load behind it: the compiler cannot tell that v and dv do not overlap)
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
           const int i = 32 * p + jj;
-          pv[jj] = i < L ? load_elem(a.v, ((size_t)(t0 + i) * Hv + h) * 128 + v, a.io_dtype) : 0.f;
+          pv[jj] = i < L ? __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                               vcol + i * 128 + ((sxv ^ (i & 7)) << 4)))
+                         : 0.f;
         }
         tmem_ld32(tb + loff + C_X + 32 * p, x);
 #pragma unroll
@@ -1933,7 +1940,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
           if (i < L) store_elem(b.dv, ((size_t)(t0 + i) * Hv + h) * 128 + v, bt[i] * x[jj], a.io_dtype);
         }
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) pk[16 * p + jj] = __uint_as_float(tcg::pack2(x[2 * jj], x[2 * jj + 1]));
+        for (int jj = 0; jj < 16; ++jj) {
+          const int i = 32 * p + 2 * jj;
+          pk[16 * p + jj] = __uint_as_float(tcg::pack2(x[2 * jj] * fgv[i], x[2 * jj + 1] * fgv[i + 1]));
+        }
         red[warp * 64 + 32 * p + lane] = lane_transpose_sum(pv, lane);
       }
       tmem_st32(tb + loff + C_X, pk);
@@ -1966,7 +1976,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
       xv[128 + tid] = 0.f;
       xv[192 + tid] = 0.f;
     }
-    if (tid == 0) {   // dS^T += dO^T (scale gamma r_q q) + dX^T (-gamma beta r_k k)
+    if (tid == 0) {   // dS^T += dO^T (scale gamma r_q q) + (dX^T diag(-gamma beta)) (r_k k)
       const uint32_t iq = idesc_bf16(128, 128, true, true), ik = idesc_bf16(128, 128, false, true);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
@@ -1974,7 +1984,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
                  tcg::mndesc(sst + ST_Q + ks * 2048, 8192), iq, 1);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_bf16_ta(tb + C_S, tb + C_X + 8 * ks, tcg::mndesc(sst + ST_KG + ks * 2048, 8192), ik, 1);
+        mma_bf16_ta(tb + C_S, tb + C_X + 8 * ks, tcg::mndesc(sst + ST_K + ks * 2048, 8192), ik, 1);
       mma_commit(mmab);
     }
     if (tid == 0) ok = mbar_wait(mmab, ph, kWaitNs);
@@ -1982,7 +1992,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
     if (__syncthreads_or(!ok)) { failed = true; break; }
     tc_fence_after();
     if (tid == 0 && qc - 2 >= 0) {   // every read of this stage is done: chunk qc - 2 into it
-      issue_stage(st, &full[s], &tmQ, &tmK, &tmO,
+      issue_stage(st, &full[s], &tmQ, &tmK, &tmV, &tmO,
                   reinterpret_cast<const uint8_t*>(ws.T + ((size_t)(first + qc - 2) * Hv + h) * 64 * 64),
                   bos + (qc - 2) * C, hq, h);
     }
@@ -2123,16 +2133,17 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
     const long long blocks = (long long)vtiles * a.Hv * a.num_seqs;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     if (tc) {
-      CUtensorMap mq, mk, mo;
+      CUtensorMap mq, mk, mv, mo;
       memset(&mq, 0, sizeof(mq));
       memset(&mk, 0, sizeof(mk));
+      memset(&mv, 0, sizeof(mv));
       memset(&mo, 0, sizeof(mo));
       if (!encode_rows_map_bf16(&mq, a.q, a.Hqk, T_total) || !encode_rows_map_bf16(&mk, a.k, a.Hqk, T_total) ||
-          !encode_rows_map_bf16(&mo, b.d_o, a.Hv, T_total))
+          !encode_rows_map_bf16(&mv, a.v, a.Hv, T_total) || !encode_rows_map_bf16(&mo, b.d_o, a.Hv, T_total))
         return cudaErrorInvalidValue;
       const long long ctas = (long long)a.num_seqs * a.Hv;
       if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-      tcr::bwd_reverse_tc_kernel<<<(unsigned)ctas, tcr::kThreads, tcr::SMEM, a.stream>>>(mq, mk, mo, a, b, ws);
+      tcr::bwd_reverse_tc_kernel<<<(unsigned)ctas, tcr::kThreads, tcr::SMEM, a.stream>>>(mq, mk, mv, mo, a, b, ws);
     } else {
       bwd_reverse_kernel<<<(unsigned)blocks, kRevThreads, kRevSmem, a.stream>>>(a, b, ws);
     }
