@@ -997,6 +997,13 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+constexpr float kLog2eG = 1.4426950408889634f;
+// 2^x on the special-function unit (the arguments are <= 0 where the value is kept).
+__device__ __forceinline__ float ex2g(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 // Four values as bf16 at element (row, col) of a K-major tile with 128-element rows split in
 // two 64-element halves of `half` bytes (col % 4 == 0).
 __device__ __forceinline__ void put4(uint8_t* tile, uint32_t half, int row, int col, const float (&x)[4]) {
@@ -1034,7 +1041,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(const ChunkArg
   float* G = vec;              float* bt = vec + 64;    float* gm = vec + 128;  float* lm = vec + 192;
   float* qh1 = vec + 256;      float* kh2 = vec + 320;  float* kh3 = vec + 384; float* rz = vec + 448;
   float* dba = vec + 512;      float* cs = vec + 576;   float* xvr = vec + 640; float* red = vec + 704;
-  float* dGv = vec + 768;      float* om = vec + 832;
+  float* dGv = vec + 768;      float* om = vec + 832;   float* g2 = vec + 896;
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + OFF_BAR + 8);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 16);
@@ -1155,6 +1162,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(const ChunkArg
   if (tid < 64) {
     gm[tid] = expf(G[tid]);
     lm[tid] = expf(G[L - 1] - G[tid]);
+    g2[tid] = G[tid] * kLog2eG;   // base-2 log-decay for the F / E factors
   }
   if (tid == 0) ok = mbar_wait(bar, 0, kWaitNs);
   if (__syncthreads_or(!ok)) {
@@ -1215,30 +1223,42 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(const ChunkArg
     tmem_ld32(tb + loff + T_R2 + 32 * part, x);   // dO U'^T or dX U'^T
     tmem_ld32(tb + loff + T_R3 + 32 * part, y);   // Q K^T or K K^T
     float racc = 0.f, db = 0.f;
+    float fe[32];
     if (row < 64) {   // F = scale (dO U'^T) * Gamma on and below the diagonal
       const int i = row;
+      const float gi = g2[i];
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) {
         const int j = 32 * part + jj;
-        const float f = j <= i ? a.scale * x[jj] * expf(G[i] - G[j]) : 0.f;
-        v[jj] = f * y[jj];
+        const float e = a.scale * x[jj] * ex2g(gi - g2[j]);
+        fe[jj] = j <= i ? e : 0.f;
+        v[jj] = fe[jj] * y[jj];
         racc += v[jj];
-        *reinterpret_cast<__nv_bfloat16*>(sm + OFF_FE + sw128_offset(i, j)) = __float2bfloat16_rn(f);
       }
     } else {          // dA = -(dX U'^T) strictly below, E = beta dA * Gamma
       const int i = row - 64;
+      const float gi = g2[i];
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) {
         const int j = 32 * part + jj;
-        const float gij = j < i ? expf(G[i] - G[j]) : 0.f;
+        const float e2 = ex2g(gi - g2[j]);
+        const float gij = j < i ? e2 : 0.f;
         const float dA = -x[jj];
-        const float e = bt[i] * gij * dA;
-        v[jj] = e * y[jj];
+        fe[jj] = bt[i] * gij * dA;
+        v[jj] = fe[jj] * y[jj];
         racc += v[jj];
         db = fmaf(dA * gij, y[jj], db);
-        *reinterpret_cast<__nv_bfloat16*>(sm + OFF_FE + sw128_offset(64 + i, j)) = __float2bfloat16_rn(e);
       }
       dbp[part * 64 + i] = db;
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {   // the F / E row as bf16, 8 columns per 16-byte store
+      uint4 u;
+      u.x = pack2(fe[8 * m], fe[8 * m + 1]);
+      u.y = pack2(fe[8 * m + 2], fe[8 * m + 3]);
+      u.z = pack2(fe[8 * m + 4], fe[8 * m + 5]);
+      u.w = pack2(fe[8 * m + 6], fe[8 * m + 7]);
+      *reinterpret_cast<uint4*>(sm + OFF_FE + sw128_offset(row, 32 * part + 8 * m)) = u;
     }
     rowp[part * 128 + row] = racc;
     // column sums over this warp's 32 rows: a transpose-reduce across the lanes (31 shuffles);
