@@ -1012,10 +1012,6 @@ __device__ __forceinline__ void put4(uint8_t* tile, uint32_t half, int row, int 
   u.y = pack2(x[2], x[3]);
   *reinterpret_cast<uint2*>(tile + (col >> 6) * half + sw128_offset(row, col & 63)) = u;
 }
-__device__ __forceinline__ float get1(const uint8_t* tile, uint32_t half, int row, int col) {
-  return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(tile + (col >> 6) * half +
-                                                                     sw128_offset(row, col & 63)));
-}
 // Scale the 8 bf16 of the 16-byte chunk at p by s.
 __device__ __forceinline__ void scale8(uint8_t* p, float s) {
   uint4 v = *reinterpret_cast<uint4*>(p);
@@ -1176,26 +1172,31 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(const ChunkArg
   const uint32_t loff = (uint32_t)(32 * (warp & 3)) << 16;
   const int row = 32 * (warp & 3) + lane;   // this thread's TMEM lane
   // ---- row dots from R1 (warps 0-3: the S0 columns; warps 6-7: the dS columns of k rows)
-  if (warp < 4) {
+  if (warp < 4 || warp >= 6) {   // 8 columns of the bf16 row per 16-byte load
+    const bool s0 = warp < 4;
+    const uint8_t* tile = s0 ? sm + OFF_OX : sm + OFF_U;
+    const uint32_t half = s0 ? 16384u : 8192u;
+    const int r = s0 ? row : row - 64;
     float acc = 0.f;
 #pragma unroll
     for (int part = 0; part < 4; ++part) {
       float x[32];
-      tmem_ld32(tb + loff + T_R1 + 32 * part, x);
+      tmem_ld32(tb + loff + T_R1 + (s0 ? 0 : 128) + 32 * part, x);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) acc = fmaf(x[j], get1(sm + OFF_OX, 16384, row, 32 * part + j), acc);
+      for (int m = 0; m < 4; ++m) {
+        const int col = 32 * part + 8 * m;
+        const uint4 u = *reinterpret_cast<const uint4*>(tile + (col >> 6) * half + sw128_offset(r, col & 63));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[q]));
+          acc = fmaf(x[8 * m + 2 * q], f.x, fmaf(x[8 * m + 2 * q + 1], f.y, acc));
+        }
+      }
     }
-    if (row < 64) qh1[row] = acc; else kh2[row - 64] = acc;
-  } else if (warp >= 6) {
-    float acc = 0.f;
-#pragma unroll
-    for (int part = 0; part < 4; ++part) {
-      float x[32];
-      tmem_ld32(tb + loff + T_R1 + 128 + 32 * part, x);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) acc = fmaf(x[j], get1(sm + OFF_U, 8192, row - 64, 32 * part + j), acc);
-    }
-    kh3[row - 64] = acc;
+    if (!s0) kh3[row - 64] = acc;
+    else if (row < 64) qh1[row] = acc;
+    else kh2[row - 64] = acc;
   }
   __syncthreads();
   // ---- R4's scaled operands: [scale gamma dO; -gamma beta dX] in place, lambda U' rows 64-127
@@ -1897,7 +1898,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
     ph ^= 1u;
     if (__syncthreads_or(!ok)) { failed = true; break; }
     tc_fence_after();
-    {  // dU'^T = dUp^T + Y^T diag(lambda) -> bf16 pairs in C_U
+    {  // dU'^T = dUp^T + Y^T diag(lambda) -> bf16 pairs in C_U (lambda_j = 2^((G_L - G_j) log2 e))
       const float gl = G[L - 1];
       float pk[32];
 #pragma unroll
@@ -1909,8 +1910,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
         for (int jj = 0; jj < 16; ++jj) {
           const int j0 = 32 * p + 2 * jj;
           pk[16 * p + jj] = __uint_as_float(
-              tcg::pack2(fmaf(expf(gl - G[j0]), y[2 * jj], u[2 * jj]),
-                         fmaf(expf(gl - G[j0 + 1]), y[2 * jj + 1], u[2 * jj + 1])));
+              tcg::pack2(fmaf(tcg::ex2g((gl - G[j0]) * tcg::kLog2eG), y[2 * jj], u[2 * jj]),
+                         fmaf(tcg::ex2g((gl - G[j0 + 1]) * tcg::kLog2eG), y[2 * jj + 1], u[2 * jj + 1])));
         }
       }
       tmem_st32(tb + loff + C_U, pk);
