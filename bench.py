@@ -22,6 +22,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -119,16 +120,24 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def kernel_code_hash(path):
+    """sha256 (16 hex digits) of a CUDA source with its comments and whitespace removed: a
+    comment-only edit keeps the hash, any change to the code changes it."""
+    txt = open(path).read()
+    txt = re.sub(r"/\*.*?\*/", " ", txt, flags=re.S)
+    txt = re.sub(r"//[^\n]*", " ", txt)
+    return hashlib.sha256(" ".join(txt.split()).encode()).hexdigest()[:16]
+
+
 def traffic_record():
     """DRAM bytes per launch of the fused chunk kernel from the committed ncu
-    summary, if it was taken on the current kernel source (else None)."""
+    summary, if it was taken on the current kernel code (else None)."""
     p = os.path.join(ROOT, "profiles", "chunk_tc_traffic.json")
     src = os.path.join(ROOT, "chunked_gated_delta_gdn_gb300", "csrc", "gdn_chunk_tc.cu")
     if not os.path.exists(p):
         return None
     rec = json.load(open(p))
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    if rec.get("kernel_source_sha256_16") != h:
+    if rec.get("kernel_code_sha256_16") != kernel_code_hash(src):
         return None
     return rec.get("dram_bytes_per_full_launch")
 

@@ -1656,17 +1656,18 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(const ChunkArg
 // ---------------------------------------------------------------- 4b. reverse on the tensor cores
 // bf16 I/O with K = V = 128: one CTA (4 warps) per (sequence, value head), chunks last to
 // first, with dS^T (TMEM lane = value index v, column = key index d) resident in TMEM like the
-// forward's state.  Per chunk (tiles double-buffered one chunk ahead: q, k, dO by TMA, the
+// forward's state.  Per chunk (tiles double-buffered one chunk ahead: q, k, v, dO by TMA, the
 // prep pass's T and P tiles by bulk copy):
 //   Y^T   = dS^T K^T                        M=128 N=64  K=128  (A: bf16 dS^T from TMEM)
 //   dUp^T = dO^T P                          M=128 N=64  K=64   (P carries scale)
 //   dU'^T = dUp^T + Y^T diag(lambda)        -> bf16 into TMEM
 //   dX^T  = dU'^T T                         M=128 N=64  K=64
-//   dS^T <- gamma_L dS^T + dO^T (scale diag(gamma) Q) + dX^T (-diag(gamma beta) K)
+//   dS^T <- gamma_L dS^T + dO^T (scale diag(gamma) Q) + (dX^T diag(-gamma beta)) K
 //                                           M=128 N=128 K=64 + 64
-// with the normalised q and k rows scaled in shared memory.  It writes, per chunk, the bf16
-// dS (the gradient of the chunk's exit state) and dX tiles of the grad pass, dv = diag(beta)
-// dX, and the row dots dX_i . v_i (slot 0 of ws.XV, slots 1-3 zero).
+// with the normalised q and k rows scaled in shared memory and -gamma beta folded into the bf16
+// dX^T operand.  It writes, per chunk, the bf16 dS (the gradient of the chunk's exit state) and
+// dX tiles of the grad pass (staged in shared memory, bulk copies), dv = diag(beta) dX, and the
+// row dots dX_i . v_i (slot 0 of ws.XV, slots 1-3 zero).
 namespace tcr {
 using namespace sm100;
 constexpr int kThreads = 128;

@@ -537,7 +537,8 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     bool ok = true;
     if (leader) {
       ok = mbar_wait(&bars[B_READY + s], (uint32_t)(c >> 1) & 1u, kWaitLimitNs);
-      tma_store_wait_read();   // the previous output tile (staged where S^T goes) has been read
+      // the previous chunk's staged tiles (output; in record mode also U') have been read
+      tma_store_wait_read();
     }
     if (group_sync_or(kBarState, kStateThreads, !ok || flag_set(flag))) { failed = true; break; }
     tc_fence_after();
