@@ -42,17 +42,17 @@
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 #include "gdn_sm100.cuh"
+#include "gdn_tc_prep.cuh"
 
 namespace gdn {
 namespace {
 
 using namespace sm100;
 
-constexpr int kPrepThreads = 256;   // warps 0-7
 constexpr int kStateThreads = 128;  // warps 8-11
 constexpr int kTcThreads = kPrepThreads + kStateThreads;
 constexpr int kBarPrep = 1, kBarState = 2;   // named barrier ids
-constexpr int DK = 128, DV = 128;
+constexpr int DK = kTcDK, DV = kTcDV;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // Shared memory map (bytes from a 1024-byte-aligned base).
@@ -73,15 +73,11 @@ constexpr uint32_t OFF_REC = 180224;    // record mode: staging of the entry-sta
 constexpr uint32_t OFF_TW = 196608;     // (T diag(beta exp(G) r_k))^T, MN-major B [64 j][64 i]
 constexpr uint32_t OFF_TU = 204800;     // (T diag(beta))^T, MN-major B
 constexpr uint32_t OFF_VEC = 212992;    // 2 x per-token fp32 vectors [8][64]
-constexpr uint32_t VEC_G = 0, VEC_BETA = 64, VEC_RQ = 128, VEC_RK = 192, VEC_SW = 256,
-                   VEC_DL = 320, VEC_QS = 384, VEC_H = 448, VEC_FLOATS = 512;
-constexpr uint32_t OFF_TD = OFF_VEC + 2 * 4 * VEC_FLOATS;  // diagonal blocks of T, column-major,
-constexpr int TD_LD = 20;                                  // [4 blocks][16 columns][20 (16 rows + pad)]
-constexpr uint32_t OFF_BAR = OFF_TD + 4 * 16 * TD_LD * 4;
+constexpr uint32_t OFF_TD = OFF_VEC + 2 * 4 * VEC_FLOATS;  // diagonal blocks of T
+constexpr uint32_t OFF_BAR = OFF_TD + kTdBytes;
 constexpr uint32_t SMEM_USED = OFF_BAR + 256;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base
 
-constexpr uint32_t STAGE_TX = QK_STAGE + V_STAGE;  // Q + K + V bytes per stage = 48 KB
 
 // TMEM columns (fp32, 128 lanes).  COL_S holds S^T for the whole sequence.  Three products
 // read their A operand from TMEM as bf16 (two per 32-bit column): S^T (in the O2 columns,
@@ -105,112 +101,8 @@ constexpr uint32_t OFF_TSLOT = OFF_FLAG + 8;              // TMEM base address
 
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(OFF_TSLOT + 4 <= SMEM_USED, "barrier block");
-static_assert(STAGE_TX == 49152, "stage bytes");
+static_assert(QK_STAGE == kQkStageBytes && V_STAGE == kVStageBytes, "stage bytes");
 static_assert(OFF_P + 2 * 8192 <= OFF_REC && OFF_REC + 16384 <= OFF_TW, "record staging");
-
-// fp32 A tile: element (i, j) at i * 64 + 4 * ((j / 4) ^ (i % 16)) + j % 4, so that
-// 16-byte groups stay contiguous and the row-parallel accesses of the solve hit
-// distinct banks.
-__device__ __forceinline__ int a_idx(int i, int j) {
-  return i * 64 + ((((j >> 2) ^ (i & 15)) << 2) | (j & 3));
-}
-
-__device__ __forceinline__ void store_bf16x8(uint8_t* p, const float* v) {
-  __nv_bfloat162 b0 = __floats2bfloat162_rn(v[0], v[1]);
-  __nv_bfloat162 b1 = __floats2bfloat162_rn(v[2], v[3]);
-  __nv_bfloat162 b2 = __floats2bfloat162_rn(v[4], v[5]);
-  __nv_bfloat162 b3 = __floats2bfloat162_rn(v[6], v[7]);
-  uint4 u;
-  u.x = *reinterpret_cast<uint32_t*>(&b0);
-  u.y = *reinterpret_cast<uint32_t*>(&b1);
-  u.z = *reinterpret_cast<uint32_t*>(&b2);
-  u.w = *reinterpret_cast<uint32_t*>(&b3);
-  *reinterpret_cast<uint4*>(p) = u;
-}
-
-// Issue the TMA loads of the chunk starting at token t into stage s.
-__device__ __forceinline__ void issue_chunk_loads(uint8_t* sm, uint64_t* bar, const CUtensorMap* tq,
-                                                  const CUtensorMap* tk, const CUtensorMap* tv,
-                                                  int s, int t, int hq, int h) {
-  mbar_arrive_expect_tx(bar, STAGE_TX);
-  uint8_t* qk = sm + OFF_QK + s * QK_STAGE;
-  uint8_t* vv = sm + OFF_V + s * V_STAGE;
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    tma_load_3d(qk + hh * 16384, tq, bar, 64 * hh, hq, t);
-    tma_load_3d(qk + hh * 16384 + 8192, tk, bar, 64 * hh, hq, t);
-    tma_load_3d(vv + hh * 8192, tv, bar, 64 * hh, h, t);
-  }
-}
-
-// g and beta of tokens t0 + lane and t0 + lane + 32, clamped to a valid token:
-// loaded one chunk ahead and masked (zero past the chunk end) where used, so the
-// loads never stall the issuing warp.
-__device__ __forceinline__ float ld_f32_early(const float* p) {
-  float v;
-  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
-  return v;
-}
-__device__ __forceinline__ float ld_bf16_early(const void* p) {
-  unsigned short v;
-  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
-  return __bfloat162float(__ushort_as_bfloat16(v));
-}
-// (volatile loads stay where they are issued: the compiler cannot sink them to
-// their use one chunk later and expose the memory latency there)
-__device__ __forceinline__ float ld_early(const void* base, size_t i, int dtype) {
-  return dtype == GDN_BF16 ? ld_bf16_early(reinterpret_cast<const __nv_bfloat16*>(base) + i)
-                           : ld_f32_early(reinterpret_cast<const float*>(base) + i);
-}
-// Raw gate inputs of tokens t0 + lane and t0 + lane + 32: g and beta, or, with
-// fused gates, the features a and b (turned into g and beta where used).
-__device__ __forceinline__ void load_gates(const ChunkArgs& a, int t0, int h, int lane,
-                                           int T_total, float* g, float* b) {
-  const size_t ta = (size_t)min(t0 + lane, T_total - 1), tb = (size_t)min(t0 + lane + 32, T_total - 1);
-  if (a.gates.mode == kGatesFused) {
-    g[0] = ld_early(a.gates.a, ta * a.Hv + h, a.gates.ab_dtype);
-    g[1] = ld_early(a.gates.a, tb * a.Hv + h, a.gates.ab_dtype);
-    b[0] = ld_early(a.gates.b, ta * a.Hv + h, a.gates.ab_dtype);
-    b[1] = ld_early(a.gates.b, tb * a.Hv + h, a.gates.ab_dtype);
-  } else {
-    g[0] = ld_f32_early(a.g + ta * a.Hv + h);
-    g[1] = ld_f32_early(a.g + tb * a.Hv + h);
-    b[0] = ld_early(a.beta, ta * a.Hv + h, a.beta_dtype);
-    b[1] = ld_early(a.beta, tb * a.Hv + h, a.beta_dtype);
-  }
-}
-
-// 2^x on the special-function unit (inputs here are <= 0 or moderate).
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-constexpr float kLog2e = 1.4426950408889634f;
-
-__device__ __forceinline__ bool flag_set(const int* f) {
-  return *reinterpret_cast<const volatile int*>(f) != 0;
-}
-__device__ __forceinline__ void set_flag(int* f) { *reinterpret_cast<volatile int*>(f) = 1; }
-
-// D1 = [Q;K][Q;K]^T of the stage at shared address qk_a: the stage holds Q rows 0-63 and
-// K rows 64-127, so one descriptor serves as A and as the N = 128 B.  Issued by one thread.
-__device__ __forceinline__ void issue_d1(uint32_t d_tmem, uint32_t qk_a, uint64_t* bar) {
-  const uint32_t id1 = idesc_bf16(128, 128, false, false);
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    const uint64_t d = sdesc_sw128(qk_a + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-    mma_bf16(d_tmem, d, d, id1, ks > 0);
-  }
-  mma_commit(bar);
-}
-
-// log2(x) on the special-function unit
-__device__ __forceinline__ float lg2(float x) {
-  float y;
-  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 // =================================================================== prep group
 // Warps 0-7.  For each chunk: D1 = [Q;K][Q;K]^T, gates, norms (from the diagonal of
@@ -219,9 +111,6 @@ __device__ __forceinline__ float lg2(float x) {
 __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int bos, int eos,
                            int nchunks, int h) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quad = warp & 3, chalf = warp >> 2;
-  const int row = 32 * quad + lane;
-  const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
   const uint32_t sbase = smem_u32(sm);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   int* flag = reinterpret_cast<int*>(sm + OFF_FLAG);
@@ -231,7 +120,7 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
   const int T_total = a.cu_seqlens ? a.T : a.B * a.T;
   constexpr int kGateWarp = 1;   // not the leader's warp: gates overlap the MMA issue
   float gq[2], bq[2];
-  if (warp == kGateWarp) load_gates(a, bos, h, lane, T_total, gq, bq);
+  if (warp == kGateWarp) prefetch_gates(a, bos, h, lane, T_total, gq, bq);
   const bool fused = a.gates.mode == kGatesFused;
   const float expA = fused ? expf(a.gates.A_log[h]) : 0.f;
   const float dtb = fused ? a.gates.dt_bias[h] : 0.f;
@@ -258,28 +147,9 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
       tc_fence_after();
       issue_d1(tbase + COL_D1, qk_a, &bars[B_MMA_P]);
     }
-
     // ---- gates: in-chunk cumulative log-decay and beta; prefetch the next chunk's
-    if (warp == kGateWarp) {
-      if (fused) {   // g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b)
-        gq[0] = -expA * softplus_f(gq[0] + dtb);
-        gq[1] = -expA * softplus_f(gq[1] + dtb);
-        bq[0] = sigmoid_f(bq[0]);
-        bq[1] = sigmoid_f(bq[1]);
-      }
-      float g0 = lane < L ? gq[0] : 0.f, g1 = lane + 32 < L ? gq[1] : 0.f;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float x0 = __shfl_up_sync(0xffffffffu, g0, o);
-        const float x1 = __shfl_up_sync(0xffffffffu, g1, o);
-        if (lane >= o) { g0 += x0; g1 += x1; }
-      }
-      g1 += __shfl_sync(0xffffffffu, g0, 31);
-      vec[VEC_G + lane] = g0 * kLog2e; vec[VEC_G + lane + 32] = g1 * kLog2e;   // base-2 log-decay
-      vec[VEC_BETA + lane] = lane < L ? bq[0] : 0.f;
-      vec[VEC_BETA + lane + 32] = lane + 32 < L ? bq[1] : 0.f;
-      if (c + 1 < nchunks) load_gates(a, t0 + kChunk, h, lane, T_total, gq, bq);
-    }
+    if (warp == kGateWarp)
+      gates_step(a, vec, gq, bq, L, lane, fused, expA, dtb, c + 1 < nchunks, t0 + kChunk, h, T_total);
     if (leader) {
       ok = mbar_wait(&bars[B_MMA_P], (uint32_t)c & 1u, kWaitLimitNs);   // one D1 commit per chunk
       if (c >= 2) ok = ok && mbar_wait(&bars[B_P_FREE + s], (uint32_t)((c - 2) >> 1) & 1u, kWaitLimitNs);
@@ -287,218 +157,14 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
     if (group_sync_or(kBarPrep, kPrepThreads, !ok || flag_set(flag))) { if (leader) set_flag(flag); return; }
     tc_fence_after();
 
-    // ---- inverse L2 norms from the diagonal of D1 (lane i, column i: |q_i|^2 for i < 64,
-    //      |k_{i-64}|^2 above) and the per-token scalars built from them
-    float x[32];
-    tmem_ld32(tbase + lane_off + COL_D1 + 64 + 32 * chalf, x);   // Q K^T | K K^T, for P and A
-    if (chalf == 0) {
-      float dg[32];
-      tmem_ld32(tbase + lane_off + COL_D1 + 32 * quad, dg);
-      float d2 = dg[0];
-#pragma unroll
-      for (int jj = 1; jj < 32; ++jj) d2 = (lane == jj) ? dg[jj] : d2;
-      const float r = a.use_qk_l2norm ? rsqrtf(d2 + kL2Eps) : 1.0f;
-      const int i = row & 63;
-      const float gi = vec[VEC_G + i];
-      if (quad < 2) {
-        vec[VEC_RQ + i] = r;
-        vec[VEC_QS + i] = a.scale * ex2(gi) * r;
-      } else {
-        vec[VEC_RK + i] = r;
-        vec[VEC_SW + i] = vec[VEC_BETA + i] * ex2(gi) * r;
-        vec[VEC_DL + i] = ex2(vec[VEC_G + L - 1] - gi) * r;
-        vec[VEC_H + i] = gi - lg2(r);   // column factor r_k[j] 2^-G_j as an exponent
-      }
-    }
-    group_sync(kBarPrep, kPrepThreads);
-
-    // ---- P (bf16, rows 0-63 of D1, scale folded in) and A (fp32, rows 64-127 of D1); the
-    //      row and column factors enter as exponents: x * 2^(G_i + log2 f_i - H_j)
-    {
-      const int j0 = 32 * chalf;
-      float hj[32];
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const float4 h4 = *reinterpret_cast<const float4*>(vec + VEC_H + j0 + 4 * m);
-        hj[4 * m] = h4.x; hj[4 * m + 1] = h4.y; hj[4 * m + 2] = h4.z; hj[4 * m + 3] = h4.w;
-      }
-      const bool zero_tile = ((quad & 1) == 0) && chalf == 1;   // rows 0-31 x cols 32-63
-      if (quad < 2) {
-        const int i = row;
-        // row factor scale r_q[i] (zero past the chunk end: lg2(0) = -inf gives exact zeros)
-        const float ui = vec[VEC_G + i] + lg2((i < L) ? a.scale * vec[VEC_RQ + i] : 0.f);
-        if (zero_tile) {
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) x[jj] = 0.f;
-        } else {
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            const float e = x[jj] * ex2(ui - hj[jj]);
-            x[jj] = (j0 + jj <= i) ? e : 0.f;
-          }
-        }
-        uint8_t* dst = sm + OFF_P + s * 8192;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) store_bf16x8(dst + sw128_offset(i, j0 + 8 * m), &x[8 * m]);
-      } else {
-        const int i = row - 64;
-        const float vi = vec[VEC_G + i] + lg2(vec[VEC_BETA + i] * vec[VEC_RK + i]);   // beta r_k[i]
-        if (zero_tile) {
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) x[jj] = 0.f;
-        } else {
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            const float e = x[jj] * ex2(vi - hj[jj]);
-            x[jj] = (j0 + jj < i) ? e : 0.f;
-          }
-        }
-#pragma unroll
-        for (int m = 0; m < 8; ++m)
-          *reinterpret_cast<float4*>(&sA[a_idx(i, j0 + 4 * m)]) =
-              make_float4(x[4 * m], x[4 * m + 1], x[4 * m + 2], x[4 * m + 3]);
-      }
-    }
+    // ---- norms, P (to this chunk's P buffer) and A from D1
+    norms_p_a<kBarPrep>(a, tbase + COL_D1, vec, sA, sm + OFF_P + s * 8192, L);
     tc_fence_before();
     if (leader && c >= 1) ok = mbar_wait(&bars[B_WU], (uint32_t)(c - 1) & 1u, kWaitLimitNs);   // Tw, Tu free
     if (group_sync_or(kBarPrep, kPrepThreads, !ok || flag_set(flag))) { if (leader) set_flag(flag); return; }
 
-    // ---- T = (I + A)^{-1} in fp32 on the CUDA cores.  With D_b = (I + A_bb)^{-1} and
-    //      L = D A_off (block strictly lower, so L^4 = 0): T = (I - L + L^2 - L^3) D.
-    // step 1: per block row b, one right-looking substitution (I + A_bb) X = R for the
-    //      right-hand sides R = [I | A_b0 | .. | A_b,b-1], one column per thread (16 (b + 1)
-    //      columns in block row b, 160 in all): X = [D_b | L_b0 | ..].  D_b goes to sTd and
-    //      to the diagonal blocks of Tw / Tu; L_bq replaces A_bq column by column.
-    if (tid < 160) {
-      const int b = tid < 16 ? 0 : (tid < 48 ? 1 : (tid < 96 ? 2 : 3));
-      const int j = tid - 8 * b * (b + 1);            // column of R
-      const bool ident = j < 16;
-      const int cq = j - 16;                          // column of A: block q = cq / 16, c = cq % 16
-      // A[16 b + i][16 b + m] = ab[i / 4][64 i + 4 ((m / 4) ^ (i % 4)) + m % 4]
-      const float* ab[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) ab[k] = sA + 1024 * b + (((4 * b) ^ (4 * k)) << 2);
-      float x[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) x[i] = ident ? ((i == j) ? 1.f : 0.f) : sA[a_idx(16 * b + i, cq)];
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {   // columns m = 4 g .. 4 g + 3 of A_bb, one float4 per row
-        float4 ag[16];
-#pragma unroll
-        for (int i = 4 * g + 1; i < 16; ++i)
-          ag[i] = *reinterpret_cast<const float4*>(ab[i >> 2] + 64 * i + ((g ^ (i & 3)) << 2));
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int m = 4 * g + e;
-#pragma unroll
-          for (int i = m + 1; i < 16; ++i) {
-            const float am = e == 0 ? ag[i].x : (e == 1 ? ag[i].y : (e == 2 ? ag[i].z : ag[i].w));
-            x[i] = fmaf(-am, x[m], x[i]);
-          }
-        }
-      }
-      if (!ident) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) sA[a_idx(16 * b + i, cq)] = x[i];
-      } else {
-#pragma unroll
-        for (int i4 = 0; i4 < 4; ++i4)
-          *reinterpret_cast<float4*>(&sTd[(b * 16 + j) * TD_LD + 4 * i4]) =
-              make_float4(x[4 * i4], x[4 * i4 + 1], x[4 * i4 + 2], x[4 * i4 + 3]);
-        // row jr = 16 b + j of (T diag(beta exp(G) r_k))^T and (T diag(beta))^T: the zeros
-        // before the diagonal block and the diagonal block itself
-        const int jr = 16 * b + j;
-        const float sw = vec[VEC_SW + jr], sb = vec[VEC_BETA + jr];
-        float w[16], u[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) { w[i] = x[i] * sw; u[i] = x[i] * sb; }
-        store_bf16x8(sm + OFF_TW + sw128_offset(jr, 16 * b), w);
-        store_bf16x8(sm + OFF_TW + sw128_offset(jr, 16 * b + 8), w + 8);
-        store_bf16x8(sm + OFF_TU + sw128_offset(jr, 16 * b), u);
-        store_bf16x8(sm + OFF_TU + sw128_offset(jr, 16 * b + 8), u + 8);
-        const float zeros[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int i8 = 0; i8 < 2 * b; ++i8) {
-          store_bf16x8(sm + OFF_TW + sw128_offset(jr, 8 * i8), zeros);
-          store_bf16x8(sm + OFF_TU + sw128_offset(jr, 8 * i8), zeros);
-        }
-      }
-    }
-    group_sync(kBarPrep, kPrepThreads);
-    // step 2: (L^2)_20 = L_21 L_10, (L^2)_31 = L_32 L_21, (L^2)_30 - (L^3)_30 with
-    //      (L^3)_30 = (L^2)_31 L_10; thread (r, c) = (tid / 16, tid % 16), so a half-warp holds
-    //      a whole row of (L^2)_31 and passes it round by shuffles.  Results go to the
-    //      upper-triangle blocks (0, 2), (1, 3), (0, 3), which nothing else uses.
-    {
-      const int r = tid >> 4, c = tid & 15, hb = lane & 16;
-      float l21r[16], l32r[16], l31r[16];   // rows r of L_21, L_32, L_31
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float4 p = *reinterpret_cast<const float4*>(&sA[(32 + r) * 64 + (((4 + u) ^ r) << 2)]);
-        const float4 q = *reinterpret_cast<const float4*>(&sA[(48 + r) * 64 + (((8 + u) ^ r) << 2)]);
-        const float4 w = *reinterpret_cast<const float4*>(&sA[(48 + r) * 64 + (((4 + u) ^ r) << 2)]);
-        l21r[4 * u] = p.x; l21r[4 * u + 1] = p.y; l21r[4 * u + 2] = p.z; l21r[4 * u + 3] = p.w;
-        l32r[4 * u] = q.x; l32r[4 * u + 1] = q.y; l32r[4 * u + 2] = q.z; l32r[4 * u + 3] = q.w;
-        l31r[4 * u] = w.x; l31r[4 * u + 1] = w.y; l31r[4 * u + 2] = w.z; l31r[4 * u + 3] = w.w;
-      }
-      float l10c[16];
-      float m20 = 0.f, m31 = 0.f, m30 = 0.f;
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        l10c[k] = sA[a_idx(16 + k, c)];
-        m20 = fmaf(l21r[k], l10c[k], m20);
-        m31 = fmaf(l32r[k], sA[a_idx(32 + k, 16 + c)], m31);
-        m30 = fmaf(l31r[k], l10c[k], fmaf(l32r[k], sA[a_idx(32 + k, c)], m30));
-      }
-      float n30 = 0.f;
-#pragma unroll
-      for (int k = 0; k < 16; ++k) n30 = fmaf(__shfl_sync(0xffffffffu, m31, k + hb), l10c[k], n30);
-      sA[a_idx(r, 32 + c)] = m20;
-      sA[a_idx(16 + r, 48 + c)] = m31;
-      sA[a_idx(r, 48 + c)] = m30 - n30;
-    }
-    group_sync(kBarPrep, kPrepThreads);
-    // step 3: T_bq = X_bq D_q, X = -L + L^2 - L^3, for the six blocks below the diagonal;
-    //      thread (r, c) computes T_bq[r][c] for all of them, written as the Tw^T / Tu^T
-    //      entries at row j = 16 q + c, column i = 16 b + r
-    {
-      const int r = tid >> 4, c = tid & 15;
-      float dq[3][16];   // column c of D_0, D_1, D_2
-#pragma unroll
-      for (int q = 0; q < 3; ++q)
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float4 d4 = *reinterpret_cast<const float4*>(&sTd[(q * 16 + c) * TD_LD + 4 * u]);
-          dq[q][4 * u] = d4.x; dq[q][4 * u + 1] = d4.y; dq[q][4 * u + 2] = d4.z; dq[q][4 * u + 3] = d4.w;
-        }
-      __nv_bfloat16* tw = reinterpret_cast<__nv_bfloat16*>(sm + OFF_TW);
-      __nv_bfloat16* tu = reinterpret_cast<__nv_bfloat16*>(sm + OFF_TU);
-#pragma unroll
-      for (int pr = 0; pr < 6; ++pr) {   // (1,0) (2,0) (3,0) (2,1) (3,1) (3,2)
-        const int b = pr < 3 ? pr + 1 : (pr < 5 ? pr - 1 : 3);
-        const int q = pr < 3 ? 0 : (pr < 5 ? 1 : 2);
-        float xr[16];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float4 l4 = *reinterpret_cast<const float4*>(&sA[(16 * b + r) * 64 + (((4 * q + u) ^ r) << 2)]);
-          xr[4 * u] = -l4.x; xr[4 * u + 1] = -l4.y; xr[4 * u + 2] = -l4.z; xr[4 * u + 3] = -l4.w;
-          if (b - q >= 2) {   // + (L^2 - L^3)_bq, stored at block (q, b)
-            const float4 m4 = *reinterpret_cast<const float4*>(&sA[(16 * q + r) * 64 + (((4 * b + u) ^ r) << 2)]);
-            xr[4 * u] += m4.x; xr[4 * u + 1] += m4.y; xr[4 * u + 2] += m4.z; xr[4 * u + 3] += m4.w;
-          }
-        }
-        float ta = 0.f, tb = 0.f;
-#pragma unroll
-        for (int k = 0; k < 16; k += 2) {
-          ta = fmaf(xr[k], dq[q][k], ta);
-          tb = fmaf(xr[k + 1], dq[q][k + 1], tb);
-        }
-        const float tv = ta + tb;
-        const int jr = 16 * q + c, i = 16 * b + r;
-        const uint32_t o = sw128_offset(jr, i) >> 1;
-        tw[o] = __float2bfloat16_rn(tv * vec[VEC_SW + jr]);
-        tu[o] = __float2bfloat16_rn(tv * vec[VEC_BETA + jr]);
-      }
-    }
+    // ---- T = (I + A)^{-1} as the Tw / Tu operands
+    solve_t<kBarPrep>(sA, sTd, vec, sm + OFF_TW, sm + OFF_TU);
     fence_proxy_async_smem();
     group_sync(kBarPrep, kPrepThreads);
 
@@ -604,10 +270,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
           const uint32_t col = COL_S + 32 * (2 * pair + sub);
           tmem_ld32(tbase + lane_off + col, x);
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            __nv_bfloat162 p2 = __floats2bfloat162_rn(x[2 * jj], x[2 * jj + 1]);
-            pk[16 * sub + jj] = __uint_as_float(*reinterpret_cast<uint32_t*>(&p2));
-          }
+          for (int jj = 0; jj < 16; ++jj) pk[16 * sub + jj] = __uint_as_float(pack_bf16x2(x[2 * jj], x[2 * jj + 1]));
 #pragma unroll
           for (int j = 0; j < 32; ++j) x[j] *= dl;
           tmem_st32(tbase + lane_off + col, x);
@@ -671,7 +334,8 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     // P of chunk c has been copied: the prep group may overwrite it
     if (leader) {
       if (c + 2 < nchunks)
-        issue_chunk_loads(sm, &bars[B_FULL + s], tq, tk, tv, s, t0 + 2 * kChunk, hq, h);
+        issue_chunk_loads(sm + OFF_QK + s * QK_STAGE, sm + OFF_V + s * V_STAGE, &bars[B_FULL + s], tq, tk,
+                          tv, t0 + 2 * kChunk, hq, h);
       mbar_arrive(&bars[B_P_FREE + s]);
     }
     tc_fence_after();
@@ -937,9 +601,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      issue_chunk_loads(sm, &bars[B_FULL + 0], &tmQ, &tmK, &tmV, 0, bos, hq, h);
+      issue_chunk_loads(sm + OFF_QK, sm + OFF_V, &bars[B_FULL + 0], &tmQ, &tmK, &tmV, bos, hq, h);
       if (nchunks > 1)
-        issue_chunk_loads(sm, &bars[B_FULL + 1], &tmQ, &tmK, &tmV, 1, bos + kChunk, hq, h);
+        issue_chunk_loads(sm + OFF_QK + QK_STAGE, sm + OFF_V + V_STAGE, &bars[B_FULL + 1], &tmQ, &tmK,
+                          &tmV, bos + kChunk, hq, h);
     }
     prep_group(a, sm, tbase, bos, eos, nchunks, h);
   } else {
@@ -1009,6 +674,7 @@ bool chunk_tc_supported(int K, int V, int io_dtype, int beta_dtype) {
 }
 
 cudaError_t launch_chunk_tc(const ChunkArgs& a) {
+  const bool rec = a.rec_states && a.rec_u && a.rec_chunk_off;
   const int T_total = a.cu_seqlens ? a.T : a.B * a.T;
   CUtensorMap mq, mk, mv, mo;
   memset(&mq, 0, sizeof(mq));
@@ -1020,7 +686,6 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a) {
         !encode_map(&mv, a.v, a.Hv, T_total) || !encode_map(&mo, a.o, a.Hv, T_total))
       return cudaErrorInvalidValue;
   }
-  const bool rec = a.rec_states && a.rec_u && a.rec_chunk_off;
   cudaError_t err = rec ? cudaFuncSetAttribute(chunk_tc_kernel<true>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)SMEM_BYTES)
