@@ -120,13 +120,34 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def kernel_code_hash(path):
-    """sha256 (16 hex digits) of a CUDA source with its comments and whitespace removed: a
-    comment-only edit keeps the hash, any change to the code changes it."""
+def _code_text(path):
+    """A CUDA source with its comments and whitespace removed."""
     txt = open(path).read()
     txt = re.sub(r"/\*.*?\*/", " ", txt, flags=re.S)
     txt = re.sub(r"//[^\n]*", " ", txt)
-    return hashlib.sha256(" ".join(txt.split()).encode()).hexdigest()[:16]
+    return " ".join(txt.split())
+
+
+def _local_sources(path, seen=None):
+    """path and, recursively, every file it includes with #include "..." from its own folder."""
+    seen = set() if seen is None else seen
+    path = os.path.abspath(path)
+    if path in seen or not os.path.exists(path):
+        return seen
+    seen.add(path)
+    for inc in re.findall(r'^\s*#\s*include\s+"([^"]+)"', open(path).read(), flags=re.M):
+        _local_sources(os.path.join(os.path.dirname(path), inc), seen)
+    return seen
+
+
+def kernel_code_hash(path):
+    """sha256 (16 hex digits) of a CUDA source and the local headers it includes (sorted by
+    name), comments and whitespace removed: a comment-only edit keeps the hash, any change to
+    the code of the kernel or of a header it includes changes it."""
+    h = hashlib.sha256()
+    for f in sorted(_local_sources(path), key=os.path.basename):
+        h.update(_code_text(f).encode() + b"\0")
+    return h.hexdigest()[:16]
 
 
 def traffic_record():

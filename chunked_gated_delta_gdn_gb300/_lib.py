@@ -18,12 +18,13 @@ _lib = None
 GDN_OK, GDN_ERR_NULL, GDN_ERR_SHAPE, GDN_ERR_DTYPE, GDN_ERR_LAYOUT = 0, 1, 2, 3, 4
 GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA, GDN_ERR_WORKSPACE = 5, 6, 7
 GDN_F32, GDN_BF16 = 0, 1
-GDN_DEV_BAD_SLOT, GDN_DEV_BAD_CU_SEQLENS = 1, 2
+GDN_DEV_BAD_SLOT, GDN_DEV_BAD_CU_SEQLENS, GDN_DEV_TIMEOUT = 1, 2, 4
 
 EXPORTS = ("gdn_chunk_fwd", "gdn_chunk_fwd_workspace_size", "gdn_chunk_fwd_path", "gdn_decode",
            "gdn_chunk_fwd_gated", "gdn_decode_gated", "gdn_decode_multi", "gdn_chunk_fwd_noalloc",
            "gdn_product_chunk_fwd", "gdn_product_chunk_fwd_workspace_size", "gdn_product_decode",
-           "gdn_chunk_bwd", "gdn_chunk_bwd_workspace_size", "gdn_status_string", "gdn_version")
+           "gdn_chunk_bwd", "gdn_chunk_bwd_workspace_size", "gdn_selftest_wait_timeout",
+           "gdn_status_string", "gdn_version")
 
 
 class GdnError(RuntimeError):
@@ -83,6 +84,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.gdn_chunk_bwd.restype = i
         lib.gdn_chunk_bwd_workspace_size.argtypes = [i, i, i, i, i, i, i, i, i]
         lib.gdn_chunk_bwd_workspace_size.restype = sz
+        lib.gdn_selftest_wait_timeout.argtypes = [vp, ctypes.c_ulonglong, i, vp, vp]
+        lib.gdn_selftest_wait_timeout.restype = i
         lib.gdn_status_string.argtypes = [i]
         lib.gdn_status_string.restype = ctypes.c_char_p
         lib.gdn_version.argtypes = []

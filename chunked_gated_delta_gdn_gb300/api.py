@@ -18,7 +18,8 @@ __all__ = ["chunk_gated_delta_rule", "gated_delta_decode", "gated_delta_decode_m
            "chunk_gated_delta_rule_fused_gates", "chunk_gated_delta_product",
            "gated_delta_product_decode", "chunk_gated_delta_rule_bwd",
            "chunk_gated_delta_rule_trainable",
-           "gated_delta_decode_fused_gates", "chunk_workspace_size", "chunk_fwd_path", "GdnError"]
+           "gated_delta_decode_fused_gates", "chunk_workspace_size", "chunk_fwd_path", "GdnError",
+           "GdnDeviceError"]
 
 GdnError = _lib.GdnError
 
@@ -52,6 +53,48 @@ def _stream(device) -> int:
     return torch.cuda.current_stream(device).cuda_stream
 
 
+class GdnDeviceError(RuntimeError):
+    """A kernel reported bad data or a timed-out wait through its device status word
+    (GDN_DEV_* bits; raised by ``check=True``)."""
+
+    NAMES = {1: "GDN_DEV_BAD_SLOT", 2: "GDN_DEV_BAD_CU_SEQLENS", 4: "GDN_DEV_TIMEOUT"}
+
+    def __init__(self, fn: str, bits: int):
+        self.bits = bits
+        names = [n for b, n in self.NAMES.items() if bits & b] or ["0x%x" % bits]
+        super().__init__("%s reported %s" % (fn, " | ".join(names)))
+
+
+def _status(dev_status, check, dev):
+    """The device status word passed to the C ABI: the caller's, else a fresh one when
+    ``check`` asks for the call's device-side errors, else none."""
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32, dev, (1,))
+        return dev_status
+    if check:
+        return torch.zeros(1, dtype=torch.int32, device=dev)
+    return None
+
+
+def _raise_on_status(fn, status, check):
+    """With ``check``: wait for the call (its stream) and raise GdnDeviceError if any GDN_DEV_*
+    bit is set.  Without it the status is left for the caller to read."""
+    if check and status is not None:
+        bits = int(status.item())   # synchronises with the call's stream
+        if bits:
+            raise GdnDeviceError(fn, bits)
+
+
+DEVICE_ERRORS_DOC = """
+    Device-side errors -- a slot index out of range, a cu_seqlens that is not monotone
+    within [0, T], a bounded in-kernel wait that timed out -- skip the affected unit (its
+    outputs are then left partly written) and are reported only through the device status
+    word: pass ``dev_status`` (a [1] int32 CUDA tensor; GDN_DEV_* bits are OR-ed into it) and
+    read it after the stream has run, or pass ``check=True`` to have this call synchronise
+    and raise GdnDeviceError.  Without either, such errors are silent.
+"""
+
+
 def chunk_fwd_path(K: int, V: int, dtype=torch.bfloat16, beta_dtype=None) -> int:
     """1: fused tcgen05 kernel; 0: fp32 CUDA-core chunk kernels; -1: rejected."""
     return _lib.load().gdn_chunk_fwd_path(K, V, _DT[dtype], _DT[beta_dtype or dtype])
@@ -69,7 +112,7 @@ def chunk_workspace_size(B, T, Hqk, Hv, K, V, num_seqs, dtype=torch.bfloat16,
 def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, chunk_size=64, initial_state=None,
                            output_final_state=False, use_qk_l2norm_in_kernel=False,
                            cu_seqlens=None, *, state_indices=None, out=None, final_state=None,
-                           workspace=None, dev_status=None,
+                           workspace=None, dev_status=None, check=False,
                            **kwargs) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """Chunkwise gated delta rule forward through ``gdn_chunk_fwd``.
 
@@ -133,8 +176,7 @@ def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, chunk_size=64, initial_
     if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    if dev_status is not None:
-        _need(dev_status, "dev_status", torch.int32, dev, (1,))
+    dev_status = _status(dev_status, check, dev)
     st = L.gdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), B, T, Hqk, Hv, K, V,
                          _DT[dt], bdt, _scale(scale), int(chunk_size), _ptr(initial_state),
                          int(bool(output_final_state)), _ptr(final_state),
@@ -142,13 +184,14 @@ def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, chunk_size=64, initial_
                          _ptr(state_indices), num_slots, _ptr(out), _ptr(workspace), ws_bytes,
                          _ptr(dev_status), _stream(dev))
     _lib.check("gdn_chunk_fwd", st)
+    _raise_on_status("gdn_chunk_fwd", dev_status, check)
     return out, final_state
 
 
 def chunk_gated_delta_rule_bwd(q, k, v, g, beta, d_o, d_final_state=None, scale=None,
                                chunk_size=64, initial_state=None, use_qk_l2norm_in_kernel=False,
                                cu_seqlens=None, *, need_d_initial_state=True, workspace=None,
-                               dev_status=None):
+                               dev_status=None, check=False):
     """Gradients of :func:`chunk_gated_delta_rule` through ``gdn_chunk_bwd``.
 
     Takes the forward's inputs (no slot cache) plus ``d_o`` [B, T, Hv, V] (the
@@ -196,8 +239,7 @@ def chunk_gated_delta_rule_bwd(q, k, v, g, beta, d_o, d_final_state=None, scale=
     if workspace is None or workspace.numel() * workspace.element_size() < need:
         workspace = torch.empty(max(int(need), 1), dtype=torch.uint8, device=dev)
     ws_bytes = workspace.numel() * workspace.element_size()
-    if dev_status is not None:
-        _need(dev_status, "dev_status", torch.int32, dev, (1,))
+    dev_status = _status(dev_status, check, dev)
     st = L.gdn_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), B, T, Hqk, Hv, K, V,
                          _DT[dt], bdt, _scale(scale), int(chunk_size), _ptr(initial_state),
                          int(bool(use_qk_l2norm_in_kernel)), _ptr(cu_seqlens), N, _ptr(d_o),
@@ -205,6 +247,7 @@ def chunk_gated_delta_rule_bwd(q, k, v, g, beta, d_o, d_final_state=None, scale=
                          _ptr(dbeta), _ptr(dh0), _ptr(workspace), ws_bytes, _ptr(dev_status),
                          _stream(dev))
     _lib.check("gdn_chunk_bwd", st)
+    _raise_on_status("gdn_chunk_bwd", dev_status, check)
     return dq, dk, dv, dg, dbeta, dh0
 
 
@@ -245,7 +288,7 @@ def chunk_gated_delta_rule_trainable(q, k, v, g, beta, scale=None, initial_state
 
 
 def gated_delta_decode(q, k, v, g, beta, ssm_state, batch_indices=None, scale=None,
-                       use_qk_l2norm_in_kernel=True, *, out=None, dev_status=None) -> torch.Tensor:
+                       use_qk_l2norm_in_kernel=True, *, out=None, dev_status=None, check=False) -> torch.Tensor:
     """One decode token per request through ``gdn_decode``; ``ssm_state`` is updated in place.
 
     q, k [n, Hqk, K]; v [n, Hv, V]; g [n, Hv] fp32; beta [n, Hv];
@@ -272,14 +315,14 @@ def gated_delta_decode(q, k, v, g, beta, ssm_state, batch_indices=None, scale=No
     if out is None:
         out = torch.empty((n, Hv, V), dtype=dt, device=dev)
     _need(out, "out", dt, dev, (n, Hv, V))
-    if dev_status is not None:
-        _need(dev_status, "dev_status", torch.int32, dev, (1,))
+    dev_status = _status(dev_status, check, dev)
     st = _lib.load().gdn_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(ssm_state),
                                 ssm_state.shape[0], _ptr(batch_indices), n, Hqk, Hv, K, V,
                                 _DT[dt], _DT[beta.dtype], _scale(scale),
                                 int(bool(use_qk_l2norm_in_kernel)), _ptr(out), _ptr(dev_status),
                                 _stream(dev))
     _lib.check("gdn_decode", st)
+    _raise_on_status("gdn_decode", dev_status, check)
     return out
 
 
@@ -295,7 +338,7 @@ def chunk_gated_delta_rule_fused_gates(q, k, v, a, b, A_log, dt_bias, scale=None
                                        initial_state=None, output_final_state=False,
                                        use_qk_l2norm_in_kernel=False, cu_seqlens=None, *,
                                        state_indices=None, out=None, final_state=None,
-                                       workspace=None, dev_status=None, **kwargs):
+                                       workspace=None, dev_status=None, check=False, **kwargs):
     """Chunked forward with the gates computed in the kernels (``gdn_chunk_fwd_gated``):
     g = -exp(A_log) * softplus(a + dt_bias), beta = sigmoid(b), with a, b [B, T, Hv]
     and A_log, dt_bias [Hv] fp32.  Everything else as :func:`chunk_gated_delta_rule`."""
@@ -336,6 +379,7 @@ def chunk_gated_delta_rule_fused_gates(q, k, v, a, b, A_log, dt_bias, scale=None
     if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    dev_status = _status(dev_status, check, dev)
     st = _lib.load().gdn_chunk_fwd_gated(
         _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), ab_dt, _ptr(A_log), _ptr(dt_bias), B, T,
         Hqk, Hv, K, V, _DT[dt], _scale(scale), int(chunk_size), _ptr(initial_state),
@@ -343,12 +387,13 @@ def chunk_gated_delta_rule_fused_gates(q, k, v, a, b, A_log, dt_bias, scale=None
         _ptr(cu_seqlens), N, _ptr(state_indices), num_slots, _ptr(out), _ptr(workspace), ws_bytes,
         _ptr(dev_status), _stream(dev))
     _lib.check("gdn_chunk_fwd_gated", st)
+    _raise_on_status("gdn_chunk_fwd_gated", dev_status, check)
     return out, final_state
 
 
 def gated_delta_decode_fused_gates(q, k, v, a, b, A_log, dt_bias, ssm_state, batch_indices=None,
                                    scale=None, use_qk_l2norm_in_kernel=True, *, out=None,
-                                   dev_status=None):
+                                   dev_status=None, check=False):
     """Decode step with the gates computed in the kernel (``gdn_decode_gated``); a, b [n, Hv]."""
     _need(q, "q", (torch.float32, torch.bfloat16))
     dev, dt = q.device, q.dtype
@@ -362,18 +407,20 @@ def gated_delta_decode_fused_gates(q, k, v, a, b, A_log, dt_bias, ssm_state, bat
         _need(batch_indices, "batch_indices", torch.int32, dev, (n,))
     if out is None:
         out = torch.empty((n, Hv, V), dtype=dt, device=dev)
+    dev_status = _status(dev_status, check, dev)
     st = _lib.load().gdn_decode_gated(
         _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), ab_dt, _ptr(A_log), _ptr(dt_bias),
         _ptr(ssm_state), ssm_state.shape[0], _ptr(batch_indices), n, Hqk, Hv, K, V, _DT[dt],
         _scale(scale), int(bool(use_qk_l2norm_in_kernel)), _ptr(out), _ptr(dev_status),
         _stream(dev))
     _lib.check("gdn_decode_gated", st)
+    _raise_on_status("gdn_decode_gated", dev_status, check)
     return out
 
 
 def gated_delta_decode_multi(q, k, v, g, beta, ssm_state, batch_indices=None, scale=None,
                              use_qk_l2norm_in_kernel=True, output_intermediate_states=False, *,
-                             out=None, intermediate_states=None, dev_status=None):
+                             out=None, intermediate_states=None, dev_status=None, check=False):
     """L decode tokens per request through ``gdn_decode_multi``.
 
     q, k [n, L, Hqk, K]; v [n, L, Hv, V]; g [n, L, Hv] fp32; beta [n, L, Hv];
@@ -399,19 +446,21 @@ def gated_delta_decode_multi(q, k, v, g, beta, ssm_state, batch_indices=None, sc
         intermediate_states = torch.empty((n, L, Hv, K, V), dtype=torch.float32, device=dev)
     if intermediate_states is not None:
         _need(intermediate_states, "intermediate_states", torch.float32, dev, (n, L, Hv, K, V))
+    dev_status = _status(dev_status, check, dev)
     st = _lib.load().gdn_decode_multi(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(ssm_state), ssm_state.shape[0],
         _ptr(batch_indices), n, L, Hqk, Hv, K, V, _DT[dt], _DT[beta.dtype], _scale(scale),
         int(bool(use_qk_l2norm_in_kernel)), _ptr(out), _ptr(intermediate_states),
         _ptr(dev_status), _stream(dev))
     _lib.check("gdn_decode_multi", st)
+    _raise_on_status("gdn_decode_multi", dev_status, check)
     return out, intermediate_states
 
 
 def chunk_gated_delta_product(q, k, v, g, beta, scale=None, chunk_size=64, initial_state=None,
                               output_final_state=False, use_qk_l2norm_in_kernel=False,
                               cu_seqlens=None, *, state_indices=None, out=None, final_state=None,
-                              workspace=None, dev_status=None,
+                              workspace=None, dev_status=None, check=False,
                               **kwargs) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """Gated Delta Product forward through ``gdn_product_chunk_fwd``: n_h delta-rule writes
     per token ("Megatron-Core API: core.ssm.gated_delta_product", GatedDeltaProductMixer).
@@ -469,8 +518,7 @@ def chunk_gated_delta_product(q, k, v, g, beta, scale=None, chunk_size=64, initi
     if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    if dev_status is not None:
-        _need(dev_status, "dev_status", torch.int32, dev, (1,))
+    dev_status = _status(dev_status, check, dev)
     st = L.gdn_product_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), B, T, n_h, Hqk,
                                  Hv, K, V, _DT[dt], _DT[beta.dtype], _scale(scale),
                                  int(chunk_size), _ptr(initial_state),
@@ -479,12 +527,13 @@ def chunk_gated_delta_product(q, k, v, g, beta, scale=None, chunk_size=64, initi
                                  _ptr(state_indices), num_slots, _ptr(out), _ptr(workspace),
                                  ws_bytes, _ptr(dev_status), _stream(dev))
     _lib.check("gdn_product_chunk_fwd", st)
+    _raise_on_status("gdn_product_chunk_fwd", dev_status, check)
     return out, final_state
 
 
 def gated_delta_product_decode(q, k, v, g, beta, ssm_state, batch_indices=None, scale=None,
                                use_qk_l2norm_in_kernel=True, output_intermediate_states=False, *,
-                               out=None, intermediate_states=None, dev_status=None):
+                               out=None, intermediate_states=None, dev_status=None, check=False):
     """One Gated Delta Product token per request through ``gdn_product_decode``.
 
     q [n, Hqk, K]; k [n, n_h, Hqk, K]; v [n, n_h, Hv, V]; g [n, Hv] fp32; beta [n, n_h, Hv];
@@ -512,10 +561,18 @@ def gated_delta_product_decode(q, k, v, g, beta, ssm_state, batch_indices=None, 
         intermediate_states = torch.empty((n, n_h, Hv, K, V), dtype=torch.float32, device=dev)
     if intermediate_states is not None:
         _need(intermediate_states, "intermediate_states", torch.float32, dev, (n, n_h, Hv, K, V))
+    dev_status = _status(dev_status, check, dev)
     st = _lib.load().gdn_product_decode(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(ssm_state), ssm_state.shape[0],
         _ptr(batch_indices), n, n_h, Hqk, Hv, K, V, _DT[dt], _DT[beta.dtype], _scale(scale),
         int(bool(use_qk_l2norm_in_kernel)), _ptr(out), _ptr(intermediate_states),
         _ptr(dev_status), _stream(dev))
     _lib.check("gdn_product_decode", st)
+    _raise_on_status("gdn_product_decode", dev_status, check)
     return out, intermediate_states
+
+
+for _fn in (chunk_gated_delta_rule, chunk_gated_delta_rule_bwd, gated_delta_decode,
+            chunk_gated_delta_rule_fused_gates, gated_delta_decode_fused_gates,
+            gated_delta_decode_multi, chunk_gated_delta_product, gated_delta_product_decode):
+    _fn.__doc__ = (_fn.__doc__ or "").rstrip() + "\n" + DEVICE_ERRORS_DOC

@@ -8,8 +8,6 @@
 // middle of a step because it would synchronise the device.  This entry point
 // gives them the same computation with the scratch taken from one file-scope
 // device array instead, so nothing is allocated per call.
-#include <mutex>
-
 #include "gdn.h"
 #include "gdn_internal.h"
 
@@ -18,25 +16,25 @@ namespace {
 // The scratch: one array per device that loads the library, held until exit.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[GDN_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices];
-cudaError_t g_scratch_err[kMaxDevices];
-std::once_flag g_scratch_once[kMaxDevices];
-
-// Device address of g_noalloc_scratch on the current device.  In host code the
-// array's name is only a host-side stand-in, so its device address is looked
-// up once per device, with that device current, and cached.
+// Device address of g_noalloc_scratch in the current context, looked up on every call.  In host
+// code the array's name is only a host-side stand-in; cudaGetSymbolAddress, with the device
+// current, gives the address in that device's context.  Nothing is cached: after a context is
+// torn down and created again (cudaDeviceReset) the module is loaded anew, possibly at another
+// address, and a lookup that failed once is simply tried again on the next call.  The lookup
+// is a host-side table query once the module is loaded; the first call on a device may load
+// the module, which is why that first call must come before any stream capture.
 cudaError_t scratch_on_current_device(void** out) {
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::call_once(g_scratch_once[dev], [dev] {
-    g_scratch_err[dev] = cudaGetSymbolAddress(&g_scratch_addr[dev], g_noalloc_scratch);
-  });
-  if (g_scratch_err[dev] != cudaSuccess) return g_scratch_err[dev];
-  *out = g_scratch_addr[dev];
-  return cudaSuccess;
+  return cudaGetSymbolAddress(out, g_noalloc_scratch);
+}
+
+// The stream's device, which must be the current one: the scratch address is the current
+// device's.  The NULL stream is the current device's.
+bool stream_on_current_device(void* stream) {
+  if (!stream) return true;
+  int cur = 0, sdev = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess) return false;
+  if (cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &sdev) != cudaSuccess) return false;
+  return sdev == cur;
 }
 
 }  // namespace
@@ -58,6 +56,7 @@ extern "C" gdn_status_t gdn_chunk_fwd_noalloc(
                          nullptr, 0, dev_status, stream);
   }
   if (need > (size_t)GDN_NOALLOC_SCRATCH_BYTES) return GDN_ERR_WORKSPACE;
+  if (!stream_on_current_device(stream)) return GDN_ERR_CUDA;
   void* scratch = nullptr;
   if (scratch_on_current_device(&scratch) != cudaSuccess) return GDN_ERR_CUDA;
   return gdn_chunk_fwd(q, k, v, g, beta, B, T, Hqk, Hv, K, V, io_dtype, beta_dtype, scale,

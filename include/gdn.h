@@ -298,9 +298,13 @@ gdn_status_t gdn_product_decode(const void* q, const void* k, const void* v, con
  *     anything is launched; other argument errors as in gdn_chunk_fwd.
  *   - Cases the tensor-core kernel serves (bf16, K = V = 128) need no scratch
  *     and run exactly as through gdn_chunk_fwd.
- *   - The first call on a device looks up the array's device address on the
- *     current device (cudaGetSymbolAddress, once per device); make that first
- *     call before any stream capture.  `stream` must belong to the current device.
+ *   - Every call looks up the array's device address in the current context
+ *     (cudaGetSymbolAddress; nothing is cached, so a context created again after
+ *     cudaDeviceReset is handled and a failed lookup is retried on the next call).
+ *     The first call on a device may load the module: make it before any stream
+ *     capture.  `stream` must belong to the current device (NULL: the current
+ *     device's default stream); a stream of another device is rejected with
+ *     GDN_ERR_CUDA before any launch.
  *   - Every call on a device shares the one array.  No scratch contents need to
  *     start at zero (each launch writes everything it later reads), but calls
  *     whose work overlaps on the GPU (different streams, or concurrent host
@@ -360,6 +364,27 @@ gdn_status_t gdn_chunk_bwd(const void* q, const void* k, const void* v, const fl
 /* Device scratch (bytes) gdn_chunk_bwd needs; (size_t)-1 for rejected sizes. */
 size_t gdn_chunk_bwd_workspace_size(int B, int T, int Hqk, int Hv, int K, int V, int num_seqs,
                                     gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype);
+
+/*
+ * gdn_selftest_wait_timeout -- the bounded wait of the fused kernels, run on its own.
+ *
+ * The sources have no counterpart for this entry point: it tests the failure detection of
+ * this library.  Every mbarrier wait inside the tensor-core kernels has a time limit; a wait
+ * that runs out sets GDN_DEV_TIMEOUT in *dev_status and the kernel returns instead of
+ * hanging.  This launches one thread that waits, with the same helper and nothing else in
+ * flight, on an mbarrier that nobody arrives on (arrive_first = 0: the wait gives up after
+ * limit_ns and GDN_DEV_TIMEOUT is OR-ed into *dev_status) or that the thread has already
+ * arrived on (arrive_first = 1: the wait succeeds, nothing is reported).
+ *
+ *   dev_status  device int (required) receiving GDN_DEV_* bits.
+ *   limit_ns    the wait's limit, 1 ns .. 100 ms (else GDN_ERR_SHAPE).
+ *   waited_ns   NULL or a device unsigned long long receiving the time the wait took
+ *               (global timer).
+ *   stream      CUDA stream (cudaStream_t) of the current device; the call is asynchronous.
+ */
+gdn_status_t gdn_selftest_wait_timeout(int* dev_status, unsigned long long limit_ns,
+                                       int arrive_first, unsigned long long* waited_ns,
+                                       void* stream);
 
 /* Static, NUL-terminated name of a status code ("GDN_OK", ...). */
 const char* gdn_status_string(gdn_status_t status);

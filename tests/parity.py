@@ -87,14 +87,29 @@ def oracle_chunk(inp, pairs=None, nthreads=0, batch=256):
     return res
 
 
+def chunk_rel_l2(x, ref, C=64):
+    """Largest relative L2 error over the C-token chunks of a sequence ([L, V] arrays).  A
+    fault confined to one chunk (a wrong buffer parity, one bad tile) moves the whole-sequence
+    error of a 512-chunk sequence by only about 1/sqrt(512) of its local size; per chunk it
+    shows at full size.  Chunks whose reference is exactly zero are compared in absolute terms."""
+    worst = 0.0
+    for c0 in range(0, len(ref), C):
+        r, g = ref[c0:c0 + C], x[c0:c0 + C]
+        den = np.linalg.norm(r)
+        err = np.linalg.norm(g - r)
+        worst = max(worst, err / den if den > 0 else err)
+    return worst
+
+
 def compare_chunk(inp, o_gpu, fin_gpu, ref, tol, label=""):
-    """Compare sampled (sequence, head) pairs.  fin_gpu indexed by slot or by sequence.
-    Returns (max rel-L2 of o, max rel-L2 of final state)."""
+    """Compare (sequence, head) pairs: relative L2 of o over each whole sequence and over each
+    of its 64-token chunks, and of the final state.  fin_gpu indexed by slot or by sequence.
+    Returns (max rel-L2 of o, max per-chunk rel-L2 of o, max rel-L2 of the final state)."""
     B, T = inp.q.shape[:2]
     Hv, V = inp.v.shape[2], inp.v.shape[3]
     o_flat = o_gpu.reshape(B * T, Hv, V)
     bounds = seq_bounds(inp)
-    worst_o, worst_f = 0.0, 0.0
+    worst_o, worst_c, worst_f = 0.0, 0.0, 0.0
     for (n, h), r in ref.items():
         s, e = bounds[n]
         og = f64(o_flat[s:e, h])
@@ -103,11 +118,17 @@ def compare_chunk(inp, o_gpu, fin_gpu, ref, tol, label=""):
             continue
         o_ref, f_ref = r
         if e > s:
+            assert np.isfinite(og).all(), "%s: sequence %d head %d has unwritten output" % (label, n, h)
             worst_o = max(worst_o, rel_l2(og, o_ref))
+            worst_c = max(worst_c, chunk_rel_l2(og, o_ref))
         if fin_gpu is not None:
             slot = n if inp.state_indices is None else int(inp.state_indices[n])
-            worst_f = max(worst_f, rel_l2(f64(fin_gpu[slot, h]), f_ref))
-    print("%s: max rel-L2 o=%.3e final=%.3e (tol %.1e)" % (label, worst_o, worst_f, tol))
+            fg = f64(fin_gpu[slot, h])
+            assert np.isfinite(fg).all(), "%s: final state %d head %d unwritten" % (label, n, h)
+            worst_f = max(worst_f, rel_l2(fg, f_ref))
+    print("%s: max rel-L2 o=%.3e (per 64-token chunk %.3e) final=%.3e (tol %.1e)"
+          % (label, worst_o, worst_c, worst_f, tol))
     assert worst_o <= tol, "%s: o rel-L2 %.3e > %.1e" % (label, worst_o, tol)
+    assert worst_c <= tol, "%s: per-chunk o rel-L2 %.3e > %.1e" % (label, worst_c, tol)
     assert worst_f <= tol, "%s: final-state rel-L2 %.3e > %.1e" % (label, worst_f, tol)
-    return worst_o, worst_f
+    return worst_o, worst_c, worst_f

@@ -183,3 +183,9 @@ def test_backward_entry_point_rejects_bad_arguments():
     assert bwd_call(ws=FAKE, wsb=need - 1) == _lib.GDN_ERR_WORKSPACE
     assert bwd_call(ws=FAKE + 8, wsb=need) == _lib.GDN_ERR_LAYOUT
     assert bwd_call(T=0, N=0, B=1, cu=FAKE) == _lib.GDN_OK
+
+
+def test_wait_selftest_validates_on_the_host():
+    """Argument errors of the bounded-wait self-test return before any launch (no GPU needed)."""
+    lib = _lib.load()
+    assert lib.gdn_selftest_wait_timeout(None, 1000, 0, None, None) == _lib.GDN_ERR_NULL

@@ -1,5 +1,5 @@
 """Host-side pieces of bench.py (CPU only): the code hash that keys the committed DRAM-traffic
-record, and the record lookup itself."""
+record (the kernel source and the local headers it includes), and the record lookup itself."""
 import json
 import os
 
@@ -49,3 +49,22 @@ def test_traffic_record_is_null_unless_the_code_matches(tmp_path, monkeypatch):
     assert bench.traffic_record() is None
     os.remove(prof / "chunk_tc_traffic.json")
     assert bench.traffic_record() is None
+
+
+def test_header_edits_change_the_code_hash_and_void_the_record(tmp_path, monkeypatch):
+    prof = tmp_path / "profiles"
+    src = tmp_path / "chunked_gated_delta_gdn_gb300" / "csrc"
+    prof.mkdir()
+    src.mkdir(parents=True)
+    header = "// tile sizes\nconstexpr int kBox = 64;\n"
+    (src / "tiles.cuh").write_text(header)
+    (src / "gdn_chunk_tc.cu").write_text('#include "tiles.cuh"\n#include <cuda.h>\n' + KERNEL)
+    rec = {"kernel_code_sha256_16": bench.kernel_code_hash(str(src / "gdn_chunk_tc.cu")),
+           "dram_bytes_per_full_launch": 99}
+    (prof / "chunk_tc_traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_record() == 99
+    (src / "tiles.cuh").write_text(header.replace("// tile sizes", "// box edge"))
+    assert bench.traffic_record() == 99            # comment edit in the header: still current
+    (src / "tiles.cuh").write_text(header.replace("64", "128"))
+    assert bench.traffic_record() is None          # code edit in the header: stale

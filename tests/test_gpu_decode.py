@@ -18,10 +18,18 @@ def run_case(inp, label):
     state_gpu = inp.ssm_state.to(dev)
     before = state_gpu.clone()
     idx = None if inp.batch_indices is None else inp.batch_indices.to(dev)
+    # the output lives between two canary rows, every element NaN before the call: padding
+    # rows must come back as written zeros, the canaries bit-identical
+    n_req, Hv, V = inp.v.shape
+    buf = torch.full((n_req + 2, Hv, V), float("nan"), dtype=inp.v.dtype, device=dev)
+    canary = buf[[0, n_req + 1]].clone()
     o = gated_delta_decode(inp.q.to(dev), inp.k.to(dev), inp.v.to(dev), inp.g.to(dev),
                            inp.beta.to(dev), state_gpu, idx, scale=inp.scale,
-                           use_qk_l2norm_in_kernel=inp.use_qk_l2norm)
+                           use_qk_l2norm_in_kernel=inp.use_qk_l2norm, out=buf[1:n_req + 1])
     torch.cuda.synchronize()
+    ibits = torch.int16 if buf.dtype == torch.bfloat16 else torch.int32
+    assert torch.equal(buf[[0, n_req + 1]].view(ibits), canary.view(ibits)), "decode wrote outside o"
+    assert torch.isfinite(o.float()).all(), "decode left output rows unwritten"
     cache = f64(inp.ssm_state).copy()
     o_ref = oracle.decode(inp.q, inp.k, inp.v, inp.g, inp.beta, cache, inp.batch_indices,
                           scale=inp.scale, use_qk_l2norm_in_kernel=inp.use_qk_l2norm)
@@ -43,7 +51,8 @@ def run_case(inp, label):
     if pad:
         bits = o[pad].contiguous().view(torch.int16 if o.dtype == torch.bfloat16 else torch.int32)
         assert torch.count_nonzero(bits).item() == 0
-    # slots not named by any request are byte-identical
+    # slots not named by any request are byte-identical (the canaries of the cache: every
+    # neighbour of a written slot that no request names)
     untouched = sorted(set(range(state_gpu.shape[0])) - set(used))
     if untouched:
         assert torch.equal(state_gpu[untouched].view(torch.int32),

@@ -76,8 +76,10 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     need = lib.gdn_chunk_fwd_workspace_size(1, 1 << 16, 4, 8, 128, 128, 1, _lib.GDN_F32,
                                             _lib.GDN_F32)
     assert need > NOALLOC_MAX
-    fake = 1 << 20   # never dereferenced: the size check comes first
-    st = noalloc_fn()(fake, fake, fake, fake, fake, 1, 1 << 16, 4, 8, 128, 128, _lib.GDN_F32,
-                      _lib.GDN_F32, float("nan"), 64, None, 0, None, 1, None, 1, None, 0, fake,
+    # no tensors at all: a correct build rejects the size first (GDN_ERR_WORKSPACE); if that
+    # check ever regressed, the NULL pointers stop the call in host code (GDN_ERR_NULL) before
+    # any launch
+    st = noalloc_fn()(None, None, None, None, None, 1, 1 << 16, 4, 8, 128, 128, _lib.GDN_F32,
+                      _lib.GDN_F32, float("nan"), 64, None, 0, None, 1, None, 1, None, 0, None,
                       None, None)
     assert st == _lib.GDN_ERR_WORKSPACE
