@@ -182,7 +182,8 @@ size_t gdn_chunk_bwd_workspace_size(int B, int T, int Hqk, int Hv, int K, int V,
                                     gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype) {
   if (check_chunk_shapes(B, T, Hqk, Hv, K, V, io_dtype, beta_dtype) != GDN_OK || num_seqs < 0)
     return (size_t)-1;
-  return gdn::chunk_bwd_workspace_bytes((int)((long long)B * T), num_seqs, Hv, K, V);
+  return gdn::chunk_bwd_workspace_bytes((int)((long long)B * T), num_seqs, Hv, K, V,
+                                        gdn::chunk_bwd_uses_tc(K, V, io_dtype, beta_dtype));
 }
 
 gdn_status_t gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
@@ -213,7 +214,8 @@ gdn_status_t gdn_chunk_bwd(const void* q, const void* k, const void* v, const fl
       (d_initial_state && !aligned16(d_initial_state)))
     return GDN_ERR_LAYOUT;
   if (num_seqs == 0 && T_total == 0) return GDN_OK;
-  const size_t need = gdn::chunk_bwd_workspace_bytes((int)T_total, num_seqs, Hv, K, V);
+  const size_t need = gdn::chunk_bwd_workspace_bytes((int)T_total, num_seqs, Hv, K, V,
+                                                     gdn::chunk_bwd_uses_tc(K, V, io_dtype, beta_dtype));
   if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE;
   if (!aligned16(workspace)) return GDN_ERR_LAYOUT;
 

@@ -58,26 +58,31 @@ constexpr int LD = KP + 1;            // row stride of [C][KP] tiles (odd: colum
 constexpr int LDC = C + 1;            // row stride of [C][C] tiles
 constexpr int VT = 32;                // V columns per V tile
 
+// Scratch of the backward.  The fp32 path keeps fp32 tiles in every slot; the tensor-core path
+// (bf16, K = V = 128) keeps bf16 operand tiles in the S, dS, U, dX slots (half the fp32 size:
+// the per-(chunk, head) strides sS, sdS, sU, sdX are in floats), T and P together in the T slot,
+// and has no W, dUp or Z.
 struct BwdWs {
   int32_t* chunk_off;  // [N + 2]
-  float* W;            // [NC][Hv][C][K]
+  float* W;            // [NC][Hv][C][K]          (fp32 path)
   float* U;            // [NC][Hv][C][V]  U, then U'
   float* G;            // [NC][Hv][C]
   float* S;            // [NC][Hv][K][V]  state at chunk entry
   float* T;            // [NC][Hv][C][C]
-  float* dUp;          // [NC][Hv][C][V]  scale P^T dO
+  float* dUp;          // [NC][Hv][C][V]  scale P^T dO   (fp32 path)
   float* dS;           // [NC][Hv][K][V]  gradient of the chunk's exit state
   float* dX;           // [NC][Hv][C][V]
-  float* Z;            // [NC][Hv][K][V]  scale Q^T diag(gamma) dO
+  float* Z;            // [NC][Hv][K][V]  scale Q^T diag(gamma) dO   (fp32 path)
   float* XV;           // [NC][Hv][4][C]  partial row dots dX_i . v_i per 32-column slice
   float* dQ;           // [T_total][Hv][K] per value head, before the norm
   float* dK;           // [T_total][Hv][K]
+  size_t sS, sdS, sU, sdX;   // slot strides (floats) per (chunk, head) of S, dS, U, dX
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 __host__ __device__ inline BwdWs bwd_layout(void* base, long long NC, int N, int Hv, int K, int V,
-                                            long long T_total, size_t* total) {
+                                            long long T_total, bool tc, size_t* total) {
   BwdWs w;
   char* p = reinterpret_cast<char*>(base);
   size_t off = 0;
@@ -87,16 +92,19 @@ __host__ __device__ inline BwdWs bwd_layout(void* base, long long NC, int N, int
     return r;
   };
   const size_t f = sizeof(float), ch = (size_t)NC * Hv;
+  const size_t tile = tc ? 2 : 1;   // bf16 tiles take half an fp32 slot
+  w.sS = w.sdS = (size_t)K * V / tile;
+  w.sU = w.sdX = (size_t)C * V / tile;
   w.chunk_off = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (size_t)(N + 2)));
-  w.W = reinterpret_cast<float*>(take(f * ch * C * K));
-  w.U = reinterpret_cast<float*>(take(f * ch * C * V));
+  w.W = tc ? nullptr : reinterpret_cast<float*>(take(f * ch * C * K));
+  w.U = reinterpret_cast<float*>(take(f * ch * w.sU));
   w.G = reinterpret_cast<float*>(take(f * ch * C));
-  w.S = reinterpret_cast<float*>(take(f * ch * K * V));
+  w.S = reinterpret_cast<float*>(take(f * ch * w.sS));
   w.T = reinterpret_cast<float*>(take(f * ch * C * C));
-  w.dUp = reinterpret_cast<float*>(take(f * ch * C * V));
-  w.dS = reinterpret_cast<float*>(take(f * ch * K * V));
-  w.dX = reinterpret_cast<float*>(take(f * ch * C * V));
-  w.Z = reinterpret_cast<float*>(take(f * ch * K * V));
+  w.dUp = tc ? nullptr : reinterpret_cast<float*>(take(f * ch * C * V));
+  w.dS = reinterpret_cast<float*>(take(f * ch * w.sdS));
+  w.dX = reinterpret_cast<float*>(take(f * ch * w.sdX));
+  w.Z = tc ? nullptr : reinterpret_cast<float*>(take(f * ch * K * V));
   w.XV = reinterpret_cast<float*>(take(f * ch * 4 * C));
   w.dQ = reinterpret_cast<float*>(take(f * (size_t)T_total * Hv * K));
   w.dK = reinterpret_cast<float*>(take(f * (size_t)T_total * Hv * K));
@@ -1054,10 +1062,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(const ChunkArg
     fence_mbar_init();
     // the operand tiles the producers wrote: S0, dS (32 KB each), U' (16 KB), and the two
     // 8 KB halves of dX into rows 64-127 of [dO; dX]
-    const uint8_t* s0 = reinterpret_cast<const uint8_t*>(ws.S + ch * 128 * 128);
-    const uint8_t* ds = reinterpret_cast<const uint8_t*>(ws.dS + ch * 128 * 128);
-    const uint8_t* ug = reinterpret_cast<const uint8_t*>(ws.U + ch * 64 * 128);
-    const uint8_t* xg = reinterpret_cast<const uint8_t*>(ws.dX + ch * 64 * 128);
+    const uint8_t* s0 = reinterpret_cast<const uint8_t*>(ws.S + ch * ws.sS);
+    const uint8_t* ds = reinterpret_cast<const uint8_t*>(ws.dS + ch * ws.sdS);
+    const uint8_t* ug = reinterpret_cast<const uint8_t*>(ws.U + ch * ws.sU);
+    const uint8_t* xg = reinterpret_cast<const uint8_t*>(ws.dX + ch * ws.sdX);
     mbar_arrive_expect_tx(bar_ld, 32768 + 32768 + 16384 + 16384);
     bulk_load(sm + OFF_S0, s0, 32768, bar_ld);
     bulk_load(sm + OFF_DS, ds, 32768, bar_ld);
@@ -1985,10 +1993,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
     __syncthreads();
     tc_fence_after();
     if (tid == 0) {
-      uint8_t* gs = reinterpret_cast<uint8_t*>(ws.dS + ch * 128 * 128);
+      uint8_t* gs = reinterpret_cast<uint8_t*>(ws.dS + ch * ws.sdS);
       bulk_store(gs, sm + OFF_STG_S, 16384);
       bulk_store(gs + 16384, sm + OFF_STG_S + 16384, 16384);
-      bulk_store(ws.dX + ch * 64 * 128, sm + OFF_STG_X, 16384);
+      bulk_store(ws.dX + ch * ws.sdX, sm + OFF_STG_X, 16384);
       tma_store_commit();
     }
     if (tid < 64) {   // the row dots, summed over the four warps in a fixed order
@@ -2105,10 +2113,14 @@ __global__ void __launch_bounds__(kQkThreads) bwd_qk_kernel(const ChunkArgs a, c
 
 }  // namespace
 
-size_t chunk_bwd_workspace_bytes(int T_total, int num_seqs, int Hv, int K, int V) {
+size_t chunk_bwd_workspace_bytes(int T_total, int num_seqs, int Hv, int K, int V, bool tc) {
   size_t total = 0;
-  bwd_layout(nullptr, max_chunks(T_total, num_seqs), num_seqs, Hv, K, V, T_total, &total);
+  bwd_layout(nullptr, max_chunks(T_total, num_seqs), num_seqs, Hv, K, V, T_total, tc, &total);
   return total;
+}
+
+bool chunk_bwd_uses_tc(int K, int V, int io_dtype, int beta_dtype) {
+  return chunk_tc_supported(K, V, io_dtype, beta_dtype);
 }
 
 cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
@@ -2116,7 +2128,9 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
   a.final_state = nullptr;  // the forward state pass records entry states only
   const int T_total = a.cu_seqlens ? a.T : a.B * a.T;
   const long long NC = max_chunks(T_total, a.num_seqs);
-  BwdWs ws = bwd_layout(a.workspace, NC, a.num_seqs, a.Hv, a.K, a.V, T_total, nullptr);
+  // bf16 with K = V = 128 (given gates): every product on the tensor cores
+  const bool tc = chunk_bwd_uses_tc(a.K, a.V, a.io_dtype, a.beta_dtype) && a.gates.mode == kGatesGiven;
+  BwdWs ws = bwd_layout(a.workspace, NC, a.num_seqs, a.Hv, a.K, a.V, T_total, tc, nullptr);
   cudaError_t err;
   if ((err = cudaFuncSetAttribute(bwd_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem))) return err;
   if ((err = cudaFuncSetAttribute(tcr::bwd_reverse_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcr::SMEM))) return err;
@@ -2129,8 +2143,6 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
   // Forward recompute of the state entering every chunk and of U'.  bf16 with K = V = 128:
   // the tensor-core kernel in record mode (its output goes to scratch that the dQ buffer
   // reuses later); otherwise the fp32 state pass on W, U from the prep kernel.
-  const bool tc = chunk_tc_supported(a.K, a.V, a.io_dtype, a.beta_dtype) &&
-                  a.gates.mode == kGatesGiven;
   if (tc && T_total > 0) {
     ChunkArgs f = a;
     f.o = ws.dQ;   // [T_total][Hv][V] bf16 fits in [T_total][Hv][K] fp32

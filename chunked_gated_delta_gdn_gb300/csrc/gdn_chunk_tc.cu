@@ -251,7 +251,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
       group_sync(kBarState, kStateThreads);
       if (leader) {
         uint8_t* g = reinterpret_cast<uint8_t*>(a.rec_states +
-                                                ((size_t)(rec0 + c) * a.Hv + h) * (size_t)(DK * DV));
+                                                ((size_t)(rec0 + c) * a.Hv + h) * (size_t)(DK * DV / 2));
         bulk_store(g, sm + OFF_S, 16384);
         bulk_store(g + 16384, sm + OFF_REC, 16384);
         tma_store_commit();
@@ -415,7 +415,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
       fence_proxy_async_smem();
       group_sync(kBarState, kStateThreads);
       if (leader) {
-        bulk_store(a.rec_u + ((size_t)(rec0 + c) * a.Hv + h) * (size_t)(kChunk * DV), sm + OFF_REC, 16384);
+        bulk_store(a.rec_u + ((size_t)(rec0 + c) * a.Hv + h) * (size_t)(kChunk * DV / 2), sm + OFF_REC, 16384);
         tma_store_commit();
       }
     }

@@ -50,8 +50,9 @@ struct ChunkArgs {
   // Record mode of the tensor-core kernel (the backward's forward recompute): when set, the
   // state entering every chunk and U' go out as bf16 operand tiles of the backward's
   // tensor-core grad pass (128-byte swizzled, K-major: rows dk resp. tokens, dv along the
-  // rows in two 64-element halves), one per chunk and head in slots of K V resp. 64 V floats
-  // of rec_states / rec_u; chunk numbering from the device chunk table rec_chunk_off.
+  // rows in two 64-element halves), one per chunk and head in slots of K V / 2 resp. 64 V / 2
+  // floats (32 KB / 16 KB) of rec_states / rec_u; chunk numbering from the device chunk table
+  // rec_chunk_off.
   float* rec_states = nullptr;
   float* rec_u = nullptr;
   const int32_t* rec_chunk_off = nullptr;
@@ -113,8 +114,11 @@ struct BwdArgs {
   float* d_initial;       // [N, Hv, K, V] or NULL
 };
 
-// Backward of the chunkwise rule on the fp32 CUDA cores (given gates, no slot cache).
-size_t chunk_bwd_workspace_bytes(int T_total, int num_seqs, int Hv, int K, int V);
+// Backward of the chunkwise rule (given gates, no slot cache): every product on the tensor
+// cores for bf16 with K = V = 128 (tc), else fp32 on the CUDA cores; the two paths lay their
+// scratch out differently.
+bool chunk_bwd_uses_tc(int K, int V, int io_dtype, int beta_dtype);
+size_t chunk_bwd_workspace_bytes(int T_total, int num_seqs, int Hv, int K, int V, bool tc);
 cudaError_t launch_chunk_bwd(const ChunkArgs& a, const BwdArgs& b);
 
 // Fused tcgen05 / TMEM / TMA path (bf16, K = V = 128).

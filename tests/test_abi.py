@@ -189,3 +189,20 @@ def test_wait_selftest_validates_on_the_host():
     """Argument errors of the bounded-wait self-test return before any launch (no GPU needed)."""
     lib = _lib.load()
     assert lib.gdn_selftest_wait_timeout(None, 1000, 0, None, None) == _lib.GDN_ERR_NULL
+
+
+def test_backward_workspace_is_sized_per_path():
+    """The tensor-core backward (bf16, K = V = 128) keeps bf16 operand tiles and none of the
+    fp32 path's W / dUp / Z slots: its scratch is well under half of the fp32 layout's."""
+    lib = _lib.load()
+    args = (4, 32768, 16, 32, 128, 128, 4)
+    tc = lib.gdn_chunk_bwd_workspace_size(*args, _lib.GDN_BF16, _lib.GDN_BF16)
+    fp = lib.gdn_chunk_bwd_workspace_size(*args, _lib.GDN_F32, _lib.GDN_F32)
+    print("backward scratch at 4 x 32768 tokens: %.2f GB (tensor cores), %.2f GB (fp32)"
+          % (tc / 1e9, fp / 1e9))
+    assert tc < 0.45 * fp
+    # per (chunk, head): bf16 S, dS (32 KB each), U', dX (16 KB each), T and P (16 KB), the row
+    # dots and G; per token and value head: fp32 dQ and dK
+    NC, Hv = 32768 * 4 // 64 + 4, 32
+    floor = NC * Hv * (32768 * 2 + 16384 * 3) + 2 * 4 * 32768 * Hv * 128 * 4
+    assert floor <= tc <= floor * 1.03
