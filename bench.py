@@ -15,6 +15,9 @@ other chunk workloads (``other_configs``).
 ``--impl reference`` times the fp64 CPU oracle instead (the reference arm).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
+
+Defaults: 10 warm-up steps, then 50 timed steps; the per-step medians are reported beside the
+means (``chunk_ms_median``, ``decode.ms_median``).
 """
 from __future__ import annotations
 
@@ -173,6 +176,66 @@ def cpu_oracle_sample(inp, tokens, nthreads=0):
     oracle.recurrent(*args, use_qk_l2norm_in_kernel=True, nthreads=nthreads)
     dt = time.perf_counter() - t
     return dt, (nthreads or oracle.max_threads())
+
+
+def _median_time(fn, reps=3):
+    ts = []
+    for _ in range(reps):
+        t = time.perf_counter()
+        fn()
+        ts.append(time.perf_counter() - t)
+    return statistics.median(ts)
+
+
+def measure_cpu_baselines(long_inp, dec_inp, sample_tokens=1024, reps=3):
+    """The fp64 oracle, as it stands, on every workload at 1 thread and on all host cores
+    (median of `reps` runs each), on a bounded sample: the first `sample_tokens` tokens of the
+    packed token axis of the 8192-token, varlen and long-context workloads (their sequences cut
+    at the sample end), the tiny fp32 case and the decode step whole.  Tokens/s for the chunk
+    workloads, real requests/s for decode.  long_inp / dec_inp: the benchmark's own inputs."""
+    import oracle
+    from chunked_gated_delta_gdn_gb300 import synthetic
+    cores = oracle.max_threads()
+    out = {"kind": "oracle", "cores": cores, "reps": reps, "statistic": "median"}
+    work = [("tiny_fp32", synthetic.workload("tiny_fp32")),
+            ("single_seq_bf16", synthetic.workload("single_seq_bf16")),
+            ("varlen_prefill_bf16", synthetic.workload("varlen_prefill_bf16")),
+            ("long_context_bf16", long_inp)]
+    for name, inp in work:
+        B, T = inp.q.shape[:2]
+        whole = name == "tiny_fp32"
+        n_tok = T if whole else min(sample_tokens, T)
+        pick = (lambda x: x) if whole else (lambda x: x[0:1, 0:n_tok])
+        args = [pick(x) for x in (inp.q, inp.k, inp.v, inp.g, inp.beta)]
+        kw = dict(scale=inp.scale, use_qk_l2norm_in_kernel=inp.use_qk_l2norm)
+        if inp.cu_seqlens is not None:
+            cu = [int(x) for x in inp.cu_seqlens.tolist() if x < n_tok] + [n_tok]
+            kw["cu_seqlens"] = np.array(cu)
+            if inp.initial_state is not None and inp.state_indices is not None:
+                slots = inp.state_indices[:len(cu) - 1].long()
+                kw["initial_state"] = inp.initial_state[slots].double().numpy()
+        elif inp.initial_state is not None:
+            kw["initial_state"] = (inp.initial_state if whole else inp.initial_state[0:1]).double().numpy()
+        tokens = n_tok * (B if whole else 1)
+        res = {"sample": ("whole workload, %d tokens" if whole else "first %d tokens") % tokens +
+                         ", all %d value heads" % inp.v.shape[2]}
+        for label, nt in (("tokens_per_s_1thread", 1), ("tokens_per_s_all_cores", 0)):
+            res[label] = tokens / _median_time(lambda: oracle.recurrent(*args, nthreads=nt, **kw), reps)
+        out[name] = res
+    n_real = int((dec_inp.batch_indices >= 0).sum())
+    res = {"sample": "the whole step: %d requests (%d real), 512-slot cache" % (dec_inp.q.shape[0], n_real)}
+    base = dec_inp.ssm_state.double().numpy()
+    for label, nt in (("requests_per_s_1thread", 1), ("requests_per_s_all_cores", 0)):
+        ts = []
+        for _ in range(reps):
+            cache = base.copy()   # the oracle updates the cache in place; copied outside the timing
+            t = time.perf_counter()
+            oracle.decode(dec_inp.q, dec_inp.k, dec_inp.v, dec_inp.g, dec_inp.beta, cache,
+                          dec_inp.batch_indices, nthreads=nt)
+            ts.append(time.perf_counter() - t)
+        res[label] = n_real / statistics.median(ts)
+    out["decode_bf16"] = res
+    return out
 
 
 def measure_product(dev, seed, steps=10, warmup=3):
@@ -417,8 +480,8 @@ def run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
@@ -526,22 +589,38 @@ def main():
     f_host = [torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True) for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = o_host[0].numel() * o_host[0].element_size() + f_host[0].numel() * f_host[0].element_size()
-    e2e_val = e2e_seq = None
+    e2e_val = e2e_seq = link = dec_e2e = None
     if args.only is None:
         e2e_steps = max(2, min(K, 6))
         torch.cuda.synchronize()
         barrier(world)
         ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        phase = []   # per step: after the copy-in, after the call, after the copy-out
         ea.record(stream)
         for _ in range(e2e_steps):
+            p0 = torch.cuda.Event(enable_timing=True)
+            p0.record(stream)
             g = {k: v.to(dev, non_blocking=True) for k, v in host.items()}
+            p1 = torch.cuda.Event(enable_timing=True)
+            p1.record(stream)
             oo, ff = chunk_gated_delta_rule(g["q"], g["k"], g["v"], g["g"], g["beta"],
                                             output_final_state=True, use_qk_l2norm_in_kernel=True)
+            p2 = torch.cuda.Event(enable_timing=True)
+            p2.record(stream)
             o_host[0].copy_(oo, non_blocking=True)
             f_host[0].copy_(ff, non_blocking=True)
+            p3 = torch.cuda.Event(enable_timing=True)
+            p3.record(stream)
+            phase.append((p0, p1, p2, p3))
         eb.record(stream)
         torch.cuda.synchronize()
         e2e_seq = world * tokens / (max_over_ranks(ea.elapsed_time(eb), world, dev) / e2e_steps / 1000.0)
+        h2d_ms = _median([a.elapsed_time(b) for a, b, _, _ in phase])
+        d2h_ms = _median([c.elapsed_time(e) for _, _, c, e in phase])
+        link = {"h2d_gbs": h2d / (h2d_ms / 1e3) / 1e9, "d2h_gbs": d2h / (d2h_ms / 1e3) / 1e9,
+                "h2d_ms": h2d_ms, "d2h_ms": d2h_ms,
+                "how": "pinned host <-> device copies of one step, median over the sequential "
+                       "end-to-end steps (CUDA events around the copies)"}
         del g, oo, ff
         # pipelined over three streams
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -585,6 +664,33 @@ def main():
         e2e_ms = max_over_ranks(ea.elapsed_time(eb), world, dev) / e2e_steps
         e2e_val = world * tokens / (e2e_ms / 1000.0)
         del bin_, bout
+        # decode end to end: the step's inputs (q, k, v, g, beta, batch_indices) from pinned
+        # host memory, the step on the resident state cache, o back into pinned host memory
+        dhost = {k: getattr(din, k).pin_memory() for k in ("q", "k", "v", "g", "beta", "batch_indices")}
+        od_host = torch.empty(od.shape, dtype=od.dtype, pin_memory=True)
+
+        def dec_e2e_step():
+            x = {k: v.to(dev, non_blocking=True) for k, v in dhost.items()}
+            od_host.copy_(gated_delta_decode(x["q"], x["k"], x["v"], x["g"], x["beta"],
+                                             dd["ssm_state"], x["batch_indices"]), non_blocking=True)
+
+        for _ in range(3):
+            dec_e2e_step()
+        dsteps = max(5, min(K, 50))
+        torch.cuda.synchronize()
+        barrier(world)
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record(stream)
+        for _ in range(dsteps):
+            dec_e2e_step()
+        eb.record(stream)
+        torch.cuda.synchronize()
+        dms = max_over_ranks(ea.elapsed_time(eb), world, dev) / dsteps
+        dec_e2e = {"value": world * n_real / (dms / 1e3), "unit": "requests/s",
+                   "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in dhost.values()),
+                   "d2h_bytes_per_step": od_host.numel() * od_host.element_size(), "ms": dms,
+                   "how": "inputs copied in from pinned host memory and o copied out every step, "
+                          "the state cache resident on the device; %d steps" % dsteps}
 
     flops = FLOP_PER_TOKEN * tokens
     alg_bytes = BYTES_PER_TOKEN * tokens + B * HV_ * STATE_BYTES   # + the final state written
@@ -607,12 +713,15 @@ def main():
                    "frac": achieved_tf / bf16_peak, "flop_per_token": FLOP_PER_TOKEN,
                    "peak_source": peak_src},
         "chunk_ms": chunk_avg_s * 1000.0,
-        "decode": {"ms": dec_avg_s * 1000.0, "requests_per_s": world * n_real / dec_avg_s,
+        "chunk_ms_median": max_over_ranks(_median(chunk_ms), world, dev),
+        "decode": {"ms": dec_avg_s * 1000.0, "ms_median": max_over_ranks(_median(dec_ms), world, dev),
+                   "requests_per_s": world * n_real / dec_avg_s,
                    "tokens_per_s_incl_padding": world * din.q.shape[0] / dec_avg_s,
                    "state_gbs": dec_bytes / dec_avg_s / 1e9,
                    "hbm_frac": dec_bytes / dec_avg_s / 1e9 / hbm_peak},
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "pipelined": True, "value_sequential": e2e_seq},
+                "d2h_bytes_per_step": d2h, "pipelined": True, "value_sequential": e2e_seq,
+                "link": link, "decode": dec_e2e},
         "gpu_launches": launches_per_step * K,
         "clocks": clk.summary(),
     }
@@ -635,11 +744,15 @@ def main():
             line["decode"] = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sample = 8192
-        dt, cores = cpu_oracle_sample(cin, sample)
-        line["cpu_baseline"] = {"value": sample / dt, "unit": "tokens/s", "cores": cores,
-                                "kind": "oracle",
+        times, cores = [], 1
+        for _ in range(3):
+            dt, cores = cpu_oracle_sample(cin, sample)
+            times.append(dt)
+        line["cpu_baseline"] = {"value": sample / statistics.median(times), "unit": "tokens/s",
+                                "cores": cores, "kind": "oracle",
                                 "sample": "first %d tokens of sequence 0 of the same batch, all "
-                                          "32 value heads (fp64 recurrence)" % sample}
+                                          "32 value heads (fp64 recurrence), median of 3" % sample,
+                                "per_config": measure_cpu_baselines(cin, din)}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

@@ -90,9 +90,13 @@ static int check_common(int Hqk, int Hv, int K, int V, const int64_t* cu, int N)
   return ORACLE_OK;
 }
 
+/* OpenMP threads of a call: nthreads > 0 as given, 0 the process default (the count OpenMP
+   had before the first call set it), so a one-thread call does not stick to later calls. */
+static int g_default_threads = 0;
 static void set_threads(int nthreads) {
 #ifdef _OPENMP
-  if (nthreads > 0) omp_set_num_threads(nthreads);
+  if (g_default_threads == 0) g_default_threads = omp_get_max_threads();
+  omp_set_num_threads(nthreads > 0 ? nthreads : g_default_threads);
 #else
   (void)nthreads;
 #endif
@@ -378,7 +382,7 @@ int gdn_oracle_decode(const double* q, const double* k, const double* v, const d
 /* Threads an OpenMP region will use (1 without OpenMP). */
 int gdn_oracle_max_threads(void) {
 #ifdef _OPENMP
-  return omp_get_max_threads();
+  return g_default_threads ? g_default_threads : omp_get_max_threads();
 #else
   return 1;
 #endif
