@@ -68,7 +68,7 @@ constexpr uint32_t OFF_KT = 131072;     // K~^T: the K rows scaled by exp(G_last
 constexpr uint32_t OFF_A = 147456;      // fp32 A [64][64], 16-byte-group swizzled; the solve
                                         // overwrites its strictly-lower blocks with those of T
 constexpr uint32_t OFF_P = 163840;      // 2 x P, K-major B [64 i][64 j]
-constexpr uint32_t OFF_REC = 180224;    // record mode: staging of the entry-state tile's second
+constexpr uint32_t OFF_REC = 180224;    // (forward mode: the second Tw / Tu buffer)    // record mode: staging of the entry-state tile's second
                                         // half, then of the U' tile (16 KB)
 constexpr uint32_t OFF_TW = 196608;     // (T diag(beta exp(G) r_k))^T, MN-major B [64 j][64 i]
 constexpr uint32_t OFF_TU = 204800;     // (T diag(beta))^T, MN-major B
@@ -91,10 +91,11 @@ enum {
   B_MMA_P = 2,      // prep group's D1 commits
   B_MMA_S = 3,      // state group's MMA commits
   B_READY = 4,      // [2] prep -> state: chunk ready (vectors, P, Tw / Tu in shared memory)
-  B_WU = 6,         // state -> prep: the MMAs reading Tw / Tu are done (both free again)
+  B_WU = 6,         // [2 by buffer, see B_WU1] state -> prep: the MMAs reading Tw / Tu are done
   B_P_FREE = 7,     // [2] state -> prep: P copied out (its buffer free)
   B_VEC_FREE = 9,   // [2] state -> prep: chunk finished (per-token vectors free)
-  B_COUNT = 11
+  B_WU1 = 11,       // forward mode: as B_WU, for the second Tw / Tu buffer
+  B_COUNT = 12
 };
 constexpr uint32_t OFF_FLAG = OFF_BAR + 8 * B_COUNT;      // int: a group timed out
 constexpr uint32_t OFF_TSLOT = OFF_FLAG + 8;              // TMEM base address
@@ -104,10 +105,20 @@ static_assert(OFF_TSLOT + 4 <= SMEM_USED, "barrier block");
 static_assert(QK_STAGE == kQkStageBytes && V_STAGE == kVStageBytes, "stage bytes");
 static_assert(OFF_P + 2 * 8192 <= OFF_REC && OFF_REC + 16384 <= OFF_TW, "record staging");
 
+// The Tw / Tu operands of chunk c: one buffer in record mode; two, by chunk parity, in forward
+// mode, the second in the record-staging space that forward mode does not use.
+template <bool kRecord>
+__device__ __forceinline__ uint32_t tw_off(int c) { return (!kRecord && (c & 1)) ? OFF_REC : OFF_TW; }
+template <bool kRecord>
+__device__ __forceinline__ uint32_t tu_off(int c) { return (!kRecord && (c & 1)) ? OFF_REC + 8192 : OFF_TU; }
+template <bool kRecord>
+__device__ __forceinline__ int wu_bar(int c) { return (!kRecord && (c & 1)) ? B_WU1 : B_WU; }
+
 // =================================================================== prep group
 // Warps 0-7.  For each chunk: D1 = [Q;K][Q;K]^T, gates, norms (from the diagonal of
 // D1), P, A, and T = (I+A)^{-1} as bf16 Tw / Tu operands; then hands the chunk to the
 // state group and moves on.
+template <bool kRecord>
 __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int bos, int eos,
                            int nchunks, int h) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -160,11 +171,13 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
     // ---- norms, P (to this chunk's P buffer) and A from D1
     norms_p_a<kBarPrep>(a, tbase + COL_D1, vec, sA, sm + OFF_P + s * 8192, L);
     tc_fence_before();
-    if (leader && c >= 1) ok = mbar_wait(&bars[B_WU], (uint32_t)(c - 1) & 1u, kWaitLimitNs);   // Tw, Tu free
+    // Tw, Tu free: released by chunk c - 1 (one buffer) or c - 2 (forward mode, two buffers)
+    if (leader && c >= (kRecord ? 1 : 2))
+      ok = mbar_wait(&bars[wu_bar<kRecord>(c)], (uint32_t)(kRecord ? (c - 1) : ((c - 2) >> 1)) & 1u, kWaitLimitNs);
     if (group_sync_or(kBarPrep, kPrepThreads, !ok || flag_set(flag))) { if (leader) set_flag(flag); return; }
 
     // ---- T = (I + A)^{-1} as the Tw / Tu operands
-    solve_t<kBarPrep>(sA, sTd, vec, sm + OFF_TW, sm + OFF_TU);
+    solve_t<kBarPrep>(sA, sTd, vec, sm + tw_off<kRecord>(c), sm + tu_off<kRecord>(c));
     fence_proxy_async_smem();
     group_sync(kBarPrep, kPrepThreads);
 
@@ -215,7 +228,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         mma_bf16(tbase + COL_U, sdesc_sw128(v_a + ks * 2048, 8192, 1024),
-                 sdesc_sw128(sbase + OFF_TU + ks * 2048, 8192, 1024), id, ks > 0);
+                 sdesc_sw128(sbase + tu_off<kRecord>(c) + ks * 2048, 8192, 1024), id, ks > 0);
       }
     }
     // ---- record mode: the entry state as a bf16 tile, rows dk, 64 dv per 128-byte row in two
@@ -371,9 +384,9 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         mma_bf16_ta(tbase + COL_U, tbase + COL_Y + 8 * ks,
-                    sdesc_sw128(sbase + OFF_TW + ks * 2048, 8192, 1024), id4, 1);
+                    sdesc_sw128(sbase + tw_off<kRecord>(c) + ks * 2048, 8192, 1024), id4, 1);
       }
-      mma_commit(&bars[B_WU]);
+      mma_commit(&bars[wu_bar<kRecord>(c)]);
       mma_commit(&bars[B_MMA_S]);
     }
     if (leader) ok = mbar_wait(&bars[B_MMA_S], ps, kWaitLimitNs);
@@ -606,7 +619,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         issue_chunk_loads(sm + OFF_QK + QK_STAGE, sm + OFF_V + V_STAGE, &bars[B_FULL + 1], &tmQ, &tmK,
                           &tmV, bos + kChunk, hq, h);
     }
-    prep_group(a, sm, tbase, bos, eos, nchunks, h);
+    prep_group<kRecord>(a, sm, tbase, bos, eos, nchunks, h);
   } else {
     // Initial state -> TMEM (S^T: lane = value index, columns = key index).
     const int row = 32 * ((tid - kPrepThreads) >> 5) + (tid & 31);
