@@ -65,11 +65,24 @@ int gdn_chunk_fwd_path(int K, int V, gdn_dtype_t io_dtype, gdn_dtype_t beta_dtyp
   return gdn::chunk_tc_supported(K, V, io_dtype, beta_dtype) ? 1 : 0;
 }
 
+// SM count of the current device, 0 when there is none.
+static int current_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return gdn::device_sm_count(dev);
+}
+
 size_t gdn_chunk_fwd_workspace_size(int B, int T, int Hqk, int Hv, int K, int V, int num_seqs,
                                     gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype) {
   if (check_chunk_shapes(B, T, Hqk, Hv, K, V, io_dtype, beta_dtype) != GDN_OK || num_seqs < 0)
     return (size_t)-1;
-  if (gdn::chunk_tc_supported(K, V, io_dtype, beta_dtype)) return 0;
+  if (gdn::chunk_tc_supported(K, V, io_dtype, beta_dtype)) {
+    const int N = num_seqs > 0 ? num_seqs : B;
+    return gdn::chunk_tc_plan_bytes(N, Hv, gdn::chunk_tc_segments(N, Hv, current_sm_count()));
+  }
   const long long T_total = (long long)B * T;
   return gdn::chunk_generic_workspace_bytes((int)T_total, num_seqs, Hv, K, V);
 }
@@ -126,7 +139,7 @@ static gdn_status_t chunk_impl(const void* q, const void* k, const void* v, cons
 
   cudaError_t err;
   if (gdn::chunk_tc_supported(K, V, io_dtype, beta_dtype)) {
-    err = gdn::launch_chunk_tc(a);
+    err = gdn::launch_chunk_tc_planned(a);
   } else {
     const size_t need = gdn::chunk_generic_workspace_bytes((int)T_total, num_seqs, Hv, K, V);
     if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE;

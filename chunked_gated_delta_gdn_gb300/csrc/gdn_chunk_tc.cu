@@ -39,6 +39,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
+
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 #include "gdn_sm100.cuh"
@@ -191,7 +193,7 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
 // state, [O1 | Y] = S^T [Q; K]^T, U' = U - Y Tw^T, [O2 | S^T] += U'^T [P; K~^T]^T, output.
 template <bool kRecord>
 __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int bos, int eos,
-                            int nchunks, int h, int hq, size_t st_off, long long rec0,
+                            int nchunks, int h, int hq, float* fin, int uflags, long long rec0,
                             const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                             const CUtensorMap* to) {
   const int tid = threadIdx.x - kPrepThreads, wq = tid >> 5, lane = tid & 31;
@@ -348,7 +350,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     if (leader) {
       if (c + 2 < nchunks)
         issue_chunk_loads(sm + OFF_QK + s * QK_STAGE, sm + OFF_V + s * V_STAGE, &bars[B_FULL + s], tq, tk,
-                          tv, t0 + 2 * kChunk, hq, h);
+                          tv, t0 + 2 * kChunk, hq, h, !(uflags & kUnitZeroV));
       mbar_arrive(&bars[B_P_FREE + s]);
     }
     tc_fence_after();
@@ -467,8 +469,10 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
 
     // ---- o = scale exp(G) r_q O1 + O2 (P carries scale r_q): a full chunk is staged as a
     //      bf16 tile (two 128-byte-swizzled [64 tokens][64 dv] halves) and written by one
-    //      TMA store; the last, partial chunk of a sequence is stored row by row
-    if (L == kChunk) {
+    //      TMA store; the last, partial chunk of a sequence is stored row by row (neither for a
+    //      unit that writes no output)
+    if (uflags & kUnitNoOut) {
+    } else if (L == kChunk) {
       // 16x256b loads hand each thread dv (t/4, t/4 + 8 of a 16-lane half) x tokens
       // (2 (t%4), +1 of each 8-token group): the fragment of stmatrix .trans, which writes
       // 8 x 8 (token, dv) blocks as 16-byte rows of the swizzled staging tile.  Lane l gives
@@ -538,14 +542,20 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
       set_flag(flag);
       mbar_wait(&bars[B_MMA_S], ps ^ 1u, kWaitLimitNs);   // last commit, if any, has landed
     }
-  } else if (a.final_state) {
+  } else if (fin) {
     tc_fence_after();
 #pragma unroll
     for (int part = 0; part < 4; ++part) {
       float x[32];
       tmem_ld32(tbase + lane_off + COL_S + 32 * part, x);
+      if (uflags & kUnitFinT) {   // [V][K]: this thread's row, 32 consecutive floats
+        float4* dst = reinterpret_cast<float4*>(fin + (size_t)row * DK + 32 * part);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) a.final_state[st_off + (size_t)(32 * part + j) * DV + row] = x[j];
+        for (int j = 0; j < 8; ++j) dst[j] = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) fin[(size_t)(32 * part + j) * DV + row] = x[j];
+      }
     }
   }
 }
@@ -562,37 +572,62 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_TSLOT);
 
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int h = blockIdx.x % a.Hv, n = blockIdx.x / a.Hv;
-  const int hq = h / (a.Hv / a.Hqk);
-  const int T_total = a.cu_seqlens ? a.T : a.B * a.T;
-  int bos, eos;
-  if (a.cu_seqlens) { bos = a.cu_seqlens[n]; eos = a.cu_seqlens[n + 1]; }
-  else { bos = n * a.T; eos = bos + a.T; }
-  if (bos < 0 || eos < bos || eos > T_total) {
-    if (tid == 0) report(a.dev_status, GDN_DEV_BAD_CU_SEQLENS);
-    return;
-  }
-  int slot = n;
-  if (a.state_indices) {
-    slot = a.state_indices[n];
-    if (slot < 0 || slot >= a.num_slots) {   // padding sequence: zero rows, no state access
-      if (slot != -1 && tid == 0) report(a.dev_status, GDN_DEV_BAD_SLOT);
-      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.o);
-      for (int e = tid; e < (eos - bos) * DV; e += kTcThreads) {
-        const int t = e / DV, d = e - t * DV;
-        o[((size_t)(bos + t) * a.Hv + h) * DV + d] = __float2bfloat16_rn(0.f);
-      }
+  int n, h, bos, eos, uflags = 0;
+  const float* init;   // entry state [K][V] (NULL: zero)
+  float* fin;          // exit state [K][V] (NULL: not written)
+  bool padding = false;
+  if (a.units) {   // planned launch: the unit table says what this CTA runs
+    if ((int)blockIdx.x >= *a.unit_count) return;
+    const TcUnit u = a.units[blockIdx.x];
+    n = u.n; h = u.h; bos = u.bos; eos = u.eos; uflags = u.flags;
+    init = u.init; fin = u.fin;
+    if (uflags & kUnitSkip) return;
+    padding = (uflags & kUnitPadding) != 0;
+  } else {
+    h = blockIdx.x % a.Hv; n = blockIdx.x / a.Hv;
+    const int T_total = a.cu_seqlens ? a.T : a.B * a.T;
+    if (a.cu_seqlens) { bos = a.cu_seqlens[n]; eos = a.cu_seqlens[n + 1]; }
+    else { bos = n * a.T; eos = bos + a.T; }
+    if (bos < 0 || eos < bos || eos > T_total) {
+      if (tid == 0) report(a.dev_status, GDN_DEV_BAD_CU_SEQLENS);
       return;
     }
+    int slot = n;
+    if (a.state_indices) {
+      slot = a.state_indices[n];
+      if (slot < 0 || slot >= a.num_slots) {   // padding sequence
+        if (slot != -1 && tid == 0) report(a.dev_status, GDN_DEV_BAD_SLOT);
+        padding = true;
+        slot = 0;
+      }
+    }
+    const size_t st_off = ((size_t)slot * a.Hv + h) * (size_t)(DK * DV);
+    init = a.initial_state ? a.initial_state + st_off : nullptr;
+    fin = a.final_state ? a.final_state + st_off : nullptr;
   }
-  const size_t st_off = ((size_t)slot * a.Hv + h) * (size_t)(DK * DV);
-  const int nchunks = (eos - bos + kChunk - 1) / kChunk;
-  if (nchunks == 0) {   // empty sequence: the state passes through unchanged
-    if (a.final_state) {
-      for (int e = tid; e < DK * DV; e += kTcThreads)
-        a.final_state[st_off + e] = a.initial_state ? a.initial_state[st_off + e] : 0.f;
+  if (padding) {   // padding sequence: zero rows, no state access
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.o);
+    for (int e = tid; e < (eos - bos) * DV; e += kTcThreads) {
+      const int t = e / DV, d = e - t * DV;
+      o[((size_t)(bos + t) * a.Hv + h) * DV + d] = __float2bfloat16_rn(0.f);
     }
     return;
+  }
+  const int hq = h / (a.Hv / a.Hqk);
+  const bool identity = (uflags & kUnitIdentity) != 0;
+  const int nchunks = (eos - bos + kChunk - 1) / kChunk;
+  if (nchunks == 0) {   // empty range: the state passes through unchanged
+    if (fin) {
+      for (int e = tid; e < DK * DV; e += kTcThreads)
+        fin[e] = identity ? ((e / DV == e % DV) ? 1.f : 0.f) : (init ? init[e] : 0.f);
+    }
+    return;
+  }
+  const bool load_v = !(uflags & kUnitZeroV);
+  if (!load_v) {   // v = 0: both V stages stay zero (no V loads are issued)
+    uint4* vz = reinterpret_cast<uint4*>(sm + OFF_V);
+    for (int e = tid; e < (int)(2 * V_STAGE / 16); e += kTcThreads) vz[e] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
   }
 
   if (tid == 0) {
@@ -614,10 +649,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      issue_chunk_loads(sm + OFF_QK, sm + OFF_V, &bars[B_FULL + 0], &tmQ, &tmK, &tmV, bos, hq, h);
+      issue_chunk_loads(sm + OFF_QK, sm + OFF_V, &bars[B_FULL + 0], &tmQ, &tmK, &tmV, bos, hq, h, load_v);
       if (nchunks > 1)
         issue_chunk_loads(sm + OFF_QK + QK_STAGE, sm + OFF_V + V_STAGE, &bars[B_FULL + 1], &tmQ, &tmK,
-                          &tmV, bos + kChunk, hq, h);
+                          &tmV, bos + kChunk, hq, h, load_v);
     }
     prep_group<kRecord>(a, sm, tbase, bos, eos, nchunks, h);
   } else {
@@ -629,11 +664,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float x[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        x[j] = a.initial_state ? a.initial_state[st_off + (size_t)(32 * part + j) * DV + row] : 0.f;
+        x[j] = identity ? (32 * part + j == row ? 1.f : 0.f)
+                        : (init ? init[(size_t)(32 * part + j) * DV + row] : 0.f);
       tmem_st32(tbase + lane_off + COL_S + 32 * part, x);
     }
     const long long rec0 = kRecord ? a.rec_chunk_off[n] : 0;
-    state_group<kRecord>(a, sm, tbase, bos, eos, nchunks, h, hq, st_off, rec0, &tmQ, &tmK, &tmV,
+    state_group<kRecord>(a, sm, tbase, bos, eos, nchunks, h, hq, fin, uflags, rec0, &tmQ, &tmK, &tmV,
                          &tmO);
   }
 
@@ -699,14 +735,21 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a) {
         !encode_map(&mv, a.v, a.Hv, T_total) || !encode_map(&mo, a.o, a.Hv, T_total))
       return cudaErrorInvalidValue;
   }
-  cudaError_t err = rec ? cudaFuncSetAttribute(chunk_tc_kernel<true>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)SMEM_BYTES)
-                        : cudaFuncSetAttribute(chunk_tc_kernel<false>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)SMEM_BYTES);
+  // the shared-memory attribute, set once per device and kernel
+  static std::atomic<bool> attr_set[2][64];
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  const long long blocks = (long long)a.num_seqs * a.Hv;
+  if (dev >= 64 || !attr_set[rec][dev].load(std::memory_order_relaxed)) {
+    err = rec ? cudaFuncSetAttribute(chunk_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)SMEM_BYTES)
+              : cudaFuncSetAttribute(chunk_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    if (dev < 64) attr_set[rec][dev].store(true, std::memory_order_relaxed);
+  }
+  const long long blocks = a.units ? (long long)a.unit_cap : (long long)a.num_seqs * a.Hv;
+  if (a.units && rec) return cudaErrorInvalidValue;   // record mode runs whole sequences
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   if (rec)

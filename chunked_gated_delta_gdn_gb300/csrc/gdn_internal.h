@@ -25,6 +25,26 @@ struct GateArgs {
   const float* dt_bias;    // [Hv]
 };
 
+// One unit of work of the tensor-core forward when it runs from a unit table (the planned
+// launch): value head h of the token range [bos, eos) of sequence n, chunked from bos.
+// init / fin: the [K][V] fp32 state entering / leaving the range (NULL: a zero entry state /
+// no exit state written).  flags: kUnit* below.
+struct TcUnit {
+  const float* init;
+  float* fin;
+  int n, h, bos, eos;
+  int flags;
+  int pad_;
+};
+enum {
+  kUnitZeroV = 1,      // v read as zero (no V loads): the transition run of a segment
+  kUnitIdentity = 2,   // entry state = identity (K = V): with kUnitZeroV, the segment's K x K map
+  kUnitNoOut = 4,      // o not written
+  kUnitPadding = 8,    // padding sequence: o rows of the range zeroed, no state access
+  kUnitSkip = 16,      // rejected sequence (bad cu_seqlens): nothing written
+  kUnitFinT = 32       // exit state written transposed ([V][K])
+};
+
 struct ChunkArgs {
   const void* q;
   const void* k;
@@ -56,6 +76,10 @@ struct ChunkArgs {
   float* rec_states = nullptr;
   float* rec_u = nullptr;
   const int32_t* rec_chunk_off = nullptr;
+  // Planned launch: CTA i runs units[i] when i < *unit_count (device memory), else exits.
+  const TcUnit* units = nullptr;
+  const int* unit_count = nullptr;
+  int unit_cap = 0;   // CTAs launched (an upper bound of *unit_count)
 };
 
 struct DecodeArgs {
@@ -127,6 +151,17 @@ bool chunk_tc_supported(int K, int V, int io_dtype, int beta_dtype);
 // for 64 tokens, 128-byte swizzled), zero fill past the last token.
 bool encode_rows_map_bf16(CUtensorMap* m, const void* base, int H, int T_total);
 cudaError_t launch_chunk_tc(const ChunkArgs& a);
+// The planned forward (a.workspace): sequences sorted longest first, and, when the batch has
+// too few (sequence, head) chains to fill the GPU, sequences of at least 2 s chunks split into
+// s segments joined through the linearity of the chunk map S -> M S + B (a transition and a
+// contribution run per middle segment, a scan, then every segment run from its exact entry
+// state).  Falls back to launch_chunk_tc when the workspace is smaller than
+// chunk_tc_plan_bytes.  num_sms: the SM count the plan is sized for.
+int chunk_tc_segments(int num_seqs, int Hv, int num_sms);
+// SM count of device dev (cached per device), 0 if it cannot be read.
+int device_sm_count(int dev);
+size_t chunk_tc_plan_bytes(int num_seqs, int Hv, int segments);
+cudaError_t launch_chunk_tc_planned(const ChunkArgs& a);
 
 cudaError_t launch_decode(const DecodeArgs& a);
 

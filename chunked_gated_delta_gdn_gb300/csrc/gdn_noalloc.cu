@@ -55,7 +55,9 @@ extern "C" gdn_status_t gdn_chunk_fwd_noalloc(
                          use_qk_l2norm, cu_seqlens, num_seqs, state_indices, num_slots, o,
                          nullptr, 0, dev_status, stream);
   }
-  if (need > (size_t)GDN_NOALLOC_SCRATCH_BYTES) return GDN_ERR_WORKSPACE;
+  // the tensor-core path runs without its launch plan when the plan does not fit
+  if (need > (size_t)GDN_NOALLOC_SCRATCH_BYTES && gdn_chunk_fwd_path(K, V, io_dtype, beta_dtype) != 1)
+    return GDN_ERR_WORKSPACE;
   if (!stream_on_current_device(stream)) return GDN_ERR_CUDA;
   void* scratch = nullptr;
   if (scratch_on_current_device(&scratch) != cudaSuccess) return GDN_ERR_CUDA;

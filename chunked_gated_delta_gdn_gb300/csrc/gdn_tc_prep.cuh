@@ -94,16 +94,18 @@ __device__ __forceinline__ bool flag_set(const int* f) {
 }
 __device__ __forceinline__ void set_flag(int* f) { *reinterpret_cast<volatile int*>(f) = 1; }
 
-// Issue the TMA loads of the chunk starting at token t into one stage.
+// Issue the TMA loads of the chunk starting at token t into one stage (without V when
+// load_v is false: the stage's V tile then keeps whatever it holds, zeros for a v = 0 run).
 __device__ __forceinline__ void issue_chunk_loads(uint8_t* qk, uint8_t* vv, uint64_t* bar,
                                                   const CUtensorMap* tq, const CUtensorMap* tk,
-                                                  const CUtensorMap* tv, int t, int hq, int h) {
-  mbar_arrive_expect_tx(bar, kStageTx);
+                                                  const CUtensorMap* tv, int t, int hq, int h,
+                                                  bool load_v = true) {
+  mbar_arrive_expect_tx(bar, load_v ? kStageTx : kQkStageBytes);
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
     tma_load_3d(qk + hh * 16384, tq, bar, 64 * hh, hq, t);
     tma_load_3d(qk + hh * 16384 + 8192, tk, bar, 64 * hh, hq, t);
-    tma_load_3d(vv + hh * 8192, tv, bar, 64 * hh, h, t);
+    if (load_v) tma_load_3d(vv + hh * 8192, tv, bar, 64 * hh, h, t);
   }
 }
 

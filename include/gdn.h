@@ -108,9 +108,18 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype_t;
  *   num_slots   slots in the cache when state_indices is given.
  *   o           [B, T, Hv, V] io_dtype, device, written completely.
  *   workspace, workspace_bytes  device scratch of at least
- *               gdn_chunk_fwd_workspace_size(...) bytes (may be NULL when that
- *               size is 0).  Not read before it is written; may be reused once
- *               the call's work on `stream` has finished.
+ *               gdn_chunk_fwd_workspace_size(...) bytes, 256-byte aligned for the
+ *               tensor-core path.  Not read before it is written; may be reused
+ *               once the call's work on `stream` has finished.  The tensor-core
+ *               path also runs without it (NULL or smaller than that size): it
+ *               then skips its launch plan -- longest sequences first, and, when
+ *               the batch has fewer than a third as many (sequence, head) chains
+ *               as the GPU has SMs, every sequence of at least 2 s chunks split
+ *               into s segments that run concurrently and are joined exactly
+ *               through the linearity of the chunk map (a per-segment transition
+ *               and contribution, a scan, and a second pass from each segment's
+ *               entry state).  The plan is built on the device from cu_seqlens,
+ *               so a captured graph replays it for any lengths.
  *   dev_status  NULL or a device int receiving GDN_DEV_* bits.
  *   stream      cudaStream_t.
  */
@@ -124,9 +133,11 @@ gdn_status_t gdn_chunk_fwd(const void* q, const void* k, const void* v, const fl
                            void* stream);
 
 /*
- * Device scratch (bytes) gdn_chunk_fwd needs for these sizes; 0 when the fused
- * tensor-core kernel serves them.  num_seqs is N (B when cu_seqlens is NULL).
- * Returns (size_t)-1 for sizes gdn_chunk_fwd would reject.
+ * Device scratch (bytes) gdn_chunk_fwd needs for these sizes: the CUDA-core
+ * path's scratch, or the tensor-core path's launch plan (unit tables and, when
+ * sequences split, 64 KB per segment matrix), sized for the SM count of the
+ * current device.  num_seqs is N (B when cu_seqlens is NULL).  Returns
+ * (size_t)-1 for sizes gdn_chunk_fwd would reject.
  */
 size_t gdn_chunk_fwd_workspace_size(int B, int T, int Hqk, int Hv, int K, int V, int num_seqs,
                                     gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype);
@@ -295,9 +306,11 @@ gdn_status_t gdn_product_decode(const void* q, const void* k, const void* v, con
  * allocated or freed per call.
  *   - Sizes whose scratch need (gdn_chunk_fwd_workspace_size) exceeds
  *     GDN_NOALLOC_SCRATCH_BYTES are rejected with GDN_ERR_WORKSPACE before
- *     anything is launched; other argument errors as in gdn_chunk_fwd.
- *   - Cases the tensor-core kernel serves (bf16, K = V = 128) need no scratch
- *     and run exactly as through gdn_chunk_fwd.
+ *     anything is launched when the CUDA-core path serves them; other argument
+ *     errors as in gdn_chunk_fwd.
+ *   - Cases the tensor-core kernel serves (bf16, K = V = 128) get the static
+ *     array as their workspace and run exactly as through gdn_chunk_fwd (without
+ *     the launch plan when it does not fit).
  *   - Every call looks up the array's device address in the current context
  *     (cudaGetSymbolAddress; nothing is cached, so a context created again after
  *     cudaDeviceReset is handled and a failed lookup is retried on the next call).

@@ -50,7 +50,11 @@ def test_path_selection_and_workspace_sizes():
     assert ws >= 4 * nc * 2 * (64 * 64 + 64 * 64 + 64 + 64 * 64)
     assert lib.gdn_chunk_fwd_workspace_size(1, 256, 2, 3, 64, 64, 1, 0, 0) == (1 << 64) - 1
     if tc == 1:
-        assert lib.gdn_chunk_fwd_workspace_size(4, 32768, 16, 32, 128, 128, 4, 1, 1) == 0
+        # the tensor-core path's launch plan: unit tables of 40-byte entries, 256-byte aligned
+        # parts; with 128 chains (more than a third of any GB300's SMs) nothing splits, so there
+        # are no segment matrices
+        ws = lib.gdn_chunk_fwd_workspace_size(4, 32768, 16, 32, 128, 128, 4, 1, 1)
+        assert 128 * 40 <= ws < 128 * 40 + 4 * 256
 
 
 FAKE = 1 << 20   # never dereferenced: every call below fails validation first
