@@ -38,3 +38,23 @@ def compute_gates(a, b, A_log, dt_bias):
     g = -np.exp(A_log) * softplus(a + dt_bias)
     beta = sigmoid(b)
     return g, beta
+
+
+def gates_backward(a, b, A_log, dt_bias, dg, dbeta):
+    """Gradients of a loss through the gates, given its gradients dg, dbeta w.r.t. g and beta
+    ([..., Hv]).  With x = a + dt_bias[h]:
+        d softplus(x) / dx = sigmoid(x),     d sigmoid(b) / db = sigmoid(b) (1 - sigmoid(b)),
+        dg / da = dg / d dt_bias = -exp(A_log) sigmoid(x),     dg / dA_log = g,
+    so da = dg * (-exp(A_log) sigmoid(x)), db = dbeta * beta (1 - beta), and the per-head
+    parameters collect over every leading index: dA_log[h] = sum dg * g,
+    ddt_bias[h] = sum da.  Returns (da, db, dA_log, ddt_bias) as float64 arrays."""
+    f64 = lambda x: (x.detach().cpu().double().numpy() if hasattr(x, "detach")
+                     else np.asarray(x, dtype=np.float64))
+    a, b, A_log, dt_bias, dg, dbeta = (f64(x) for x in (a, b, A_log, dt_bias, dg, dbeta))
+    x = a + dt_bias
+    g = -np.exp(A_log) * softplus(x)
+    beta = sigmoid(b)
+    da = dg * (-np.exp(A_log) * sigmoid(x))
+    db = dbeta * beta * (1.0 - beta)
+    lead = tuple(range(da.ndim - 1))
+    return da, db, (dg * g).sum(axis=lead), da.sum(axis=lead)

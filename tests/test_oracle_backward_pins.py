@@ -122,3 +122,62 @@ def test_backward_mutant_is_caught(tmp_path, name):
                     str(path), "-o", str(so), "-lm"], check=True)
     lib = oracle.load_library(str(so))
     assert max(finite_difference_errors(lib=lib, l2=True)) > 1e-4
+
+
+def test_gates_backward_matches_finite_differences():
+    """oracle.gates.gates_backward composed with the adjoint gives the gradient of a loss of the
+    fused-gate forward w.r.t. the raw features a, b and the per-head parameters A_log, dt_bias:
+    central differences of that loss through oracle.gates.compute_gates and the recurrence."""
+    from oracle import gates
+    rng = np.random.default_rng(41)
+    T, Hqk, Hv, K, V = 7, 1, 2, 3, 2
+    cu = np.array([0, 3, 3, 7])
+    q, k = rng.standard_normal((1, T, Hqk, K)), rng.standard_normal((1, T, Hqk, K))
+    v = rng.standard_normal((1, T, Hv, V))
+    init = 0.3 * rng.standard_normal((3, Hv, K, V))
+    a, b = rng.standard_normal((1, T, Hv)), rng.standard_normal((1, T, Hv))
+    A_log = np.log(rng.uniform(1.0, 16.0, Hv))
+    dt_bias = 0.5 * rng.standard_normal(Hv)
+    do, dfin = rng.standard_normal((1, T, Hv, V)), rng.standard_normal((3, Hv, K, V))
+
+    def loss(a, b, A_log, dt_bias):
+        g, beta = gates.compute_gates(a, b, A_log, dt_bias)
+        o, f = oracle.recurrent(q, k, v, g, beta, initial_state=init, cu_seqlens=cu,
+                                use_qk_l2norm_in_kernel=True)
+        return float((o * do).sum() + (f * dfin).sum())
+
+    g, beta = gates.compute_gates(a, b, A_log, dt_bias)
+    _, _, _, dg, dbeta, _ = oracle.backward(q, k, v, g, beta, do, dfin, initial_state=init,
+                                            cu_seqlens=cu, use_qk_l2norm_in_kernel=True)
+    grads = gates.gates_backward(a, b, A_log, dt_bias, dg, dbeta)
+    args = [a, b, A_log, dt_bias]
+    for ai, (x, gx) in enumerate(zip(args, grads)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += 1e-6
+            xm[idx] -= 1e-6
+            ap, am = list(args), list(args)
+            ap[ai], am[ai] = xp, xm
+            num[idx] = (loss(*ap) - loss(*am)) / 2e-6
+        err = float(np.abs(num - gx).max() / max(1e-12, np.abs(num).max()))
+        assert err < 1e-6, (("da", "db", "dA_log", "ddt_bias")[ai], err)
+
+
+def test_gates_backward_special_values():
+    """Closed forms: at a + dt_bias = 0 the softplus slope is 1/2, at b = 0 the sigmoid slope
+    is 1/4, and the parameter gradients are the sums over every token of one head."""
+    from oracle import gates
+    Hv = 3
+    dt_bias = np.array([0.2, -1.0, 0.7])
+    a = np.broadcast_to(-dt_bias, (2, 5, Hv)).copy()
+    b = np.zeros((2, 5, Hv))
+    A_log = np.log(np.array([1.0, 2.0, 8.0]))
+    dg = np.arange(30.0).reshape(2, 5, Hv) / 7.0
+    dbeta = np.ones((2, 5, Hv))
+    da, db, dA_log, ddt_bias = gates.gates_backward(a, b, A_log, dt_bias, dg, dbeta)
+    np.testing.assert_allclose(da, -dg * np.exp(A_log) * 0.5, rtol=1e-15)
+    np.testing.assert_allclose(db, 0.25, rtol=1e-15)
+    g = -np.exp(A_log) * np.log(2.0)
+    np.testing.assert_allclose(dA_log, dg.sum(axis=(0, 1)) * g, rtol=1e-14)
+    np.testing.assert_allclose(ddt_bias, da.sum(axis=(0, 1)), rtol=1e-14)
