@@ -23,7 +23,8 @@ GDN_DEV_BAD_SLOT, GDN_DEV_BAD_CU_SEQLENS, GDN_DEV_TIMEOUT = 1, 2, 4
 EXPORTS = ("gdn_chunk_fwd", "gdn_chunk_fwd_workspace_size", "gdn_chunk_fwd_path", "gdn_decode",
            "gdn_chunk_fwd_gated", "gdn_decode_gated", "gdn_decode_multi", "gdn_chunk_fwd_noalloc",
            "gdn_product_chunk_fwd", "gdn_product_chunk_fwd_workspace_size", "gdn_product_decode",
-           "gdn_chunk_bwd", "gdn_chunk_bwd_workspace_size", "gdn_selftest_wait_timeout",
+           "gdn_chunk_bwd", "gdn_chunk_bwd_workspace_size", "gdn_chunk_bwd_gated",
+           "gdn_chunk_bwd_gated_workspace_size", "gdn_selftest_wait_timeout",
            "gdn_status_string", "gdn_version")
 
 
@@ -84,6 +85,12 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.gdn_chunk_bwd.restype = i
         lib.gdn_chunk_bwd_workspace_size.argtypes = [i, i, i, i, i, i, i, i, i]
         lib.gdn_chunk_bwd_workspace_size.restype = sz
+        lib.gdn_chunk_bwd_gated.argtypes = [vp, vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, i, i, f,
+                                            i, vp, i, vp, i, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                            vp, vp, sz, vp, vp]
+        lib.gdn_chunk_bwd_gated.restype = i
+        lib.gdn_chunk_bwd_gated_workspace_size.argtypes = [i, i, i, i, i, i, i, i]
+        lib.gdn_chunk_bwd_gated_workspace_size.restype = sz
         lib.gdn_selftest_wait_timeout.argtypes = [vp, ctypes.c_ulonglong, i, vp, vp]
         lib.gdn_selftest_wait_timeout.restype = i
         lib.gdn_status_string.argtypes = [i]

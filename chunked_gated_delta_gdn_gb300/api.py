@@ -18,7 +18,9 @@ __all__ = ["chunk_gated_delta_rule", "gated_delta_decode", "gated_delta_decode_m
            "chunk_gated_delta_rule_fused_gates", "chunk_gated_delta_product",
            "gated_delta_product_decode", "chunk_gated_delta_rule_bwd",
            "chunk_gated_delta_rule_trainable",
-           "gated_delta_decode_fused_gates", "chunk_workspace_size", "chunk_fwd_path", "GdnError",
+           "gated_delta_decode_fused_gates", "chunk_gated_delta_rule_bwd_fused_gates",
+           "chunk_gated_delta_rule_fused_gates_trainable", "chunk_workspace_size", "chunk_fwd_path",
+           "GdnError",
            "GdnDeviceError"]
 
 GdnError = _lib.GdnError
@@ -389,6 +391,99 @@ def chunk_gated_delta_rule_fused_gates(q, k, v, a, b, A_log, dt_bias, scale=None
     _lib.check("gdn_chunk_fwd_gated", st)
     _raise_on_status("gdn_chunk_fwd_gated", dev_status, check)
     return out, final_state
+
+
+def chunk_gated_delta_rule_bwd_fused_gates(q, k, v, a, b, A_log, dt_bias, d_o,
+                                           d_final_state=None, scale=None, chunk_size=64,
+                                           initial_state=None, use_qk_l2norm_in_kernel=False,
+                                           cu_seqlens=None, *, need_d_initial_state=True,
+                                           workspace=None, dev_status=None, check=False):
+    """Gradients of :func:`chunk_gated_delta_rule_fused_gates` through ``gdn_chunk_bwd_gated``.
+
+    Returns ``(dq, dk, dv, da, db, dA_log, ddt_bias, d_initial_state)``: dq, dk, dv in q's
+    dtype; da, db [B, T, Hv] and dA_log, ddt_bias [Hv] fp32; d_initial_state fp32
+    [N, Hv, K, V] (None when ``need_d_initial_state`` is False).  No slot cache."""
+    _need(q, "q", (torch.float32, torch.bfloat16))
+    dev, dt = q.device, q.dtype
+    if q.dim() != 4 or v.dim() != 4:
+        raise ValueError("q must be [B, T, Hqk, K] and v [B, T, Hv, V]")
+    B, T, Hqk, K = q.shape
+    Hv, V = v.shape[2], v.shape[3]
+    _need(k, "k", dt, dev, q.shape)
+    _need(v, "v", dt, dev)
+    ab_dt = _gate_args(a, b, A_log, dt_bias, dev, dt, (B, T), Hv)
+    _need(d_o, "d_o", dt, dev, (B, T, Hv, V))
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+        if B != 1:
+            raise ValueError("cu_seqlens requires B == 1")
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    st_shape = (N, Hv, K, V)
+    if initial_state is not None:
+        _need(initial_state, "initial_state", torch.float32, dev, st_shape)
+    if d_final_state is not None:
+        _need(d_final_state, "d_final_state", torch.float32, dev, st_shape)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    da = torch.empty((B, T, Hv), dtype=torch.float32, device=dev)
+    db = torch.empty((B, T, Hv), dtype=torch.float32, device=dev)
+    dA_log = torch.empty(Hv, dtype=torch.float32, device=dev)
+    ddt_bias = torch.empty(Hv, dtype=torch.float32, device=dev)
+    dh0 = torch.empty(st_shape, dtype=torch.float32, device=dev) if need_d_initial_state else None
+    L = _lib.load()
+    need = L.gdn_chunk_bwd_gated_workspace_size(B, T, Hqk, Hv, K, V, N, _DT[dt])
+    if need == (1 << 64) - 1:
+        raise ValueError("sizes rejected by gdn_chunk_bwd_gated")
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(int(need), 1), dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    dev_status = _status(dev_status, check, dev)
+    st = L.gdn_chunk_bwd_gated(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), ab_dt, _ptr(A_log), _ptr(dt_bias), B, T,
+        Hqk, Hv, K, V, _DT[dt], _scale(scale), int(chunk_size), _ptr(initial_state),
+        int(bool(use_qk_l2norm_in_kernel)), _ptr(cu_seqlens), N, _ptr(d_o), _ptr(d_final_state),
+        _ptr(dq), _ptr(dk), _ptr(dv), _ptr(da), _ptr(db), _ptr(dA_log), _ptr(ddt_bias),
+        _ptr(dh0), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(dev))
+    _lib.check("gdn_chunk_bwd_gated", st)
+    _raise_on_status("gdn_chunk_bwd_gated", dev_status, check)
+    return dq, dk, dv, da, db, dA_log, ddt_bias, dh0
+
+
+class _ChunkGatedDeltaRuleFusedGates(torch.autograd.Function):
+    """gdn_chunk_fwd_gated forward, gdn_chunk_bwd_gated backward."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, a, b, A_log, dt_bias, initial_state, scale, output_final_state,
+                use_l2, cu_seqlens):
+        o, fin = chunk_gated_delta_rule_fused_gates(
+            q, k, v, a, b, A_log, dt_bias, scale=scale, initial_state=initial_state,
+            output_final_state=output_final_state, use_qk_l2norm_in_kernel=use_l2,
+            cu_seqlens=cu_seqlens)
+        ctx.save_for_backward(q, k, v, a, b, A_log, dt_bias, initial_state, cu_seqlens)
+        ctx.scale, ctx.use_l2 = scale, use_l2
+        return o, fin
+
+    @staticmethod
+    def backward(ctx, d_o, d_fin):
+        q, k, v, a, b, A_log, dt_bias, init, cu = ctx.saved_tensors
+        dq, dk, dv, da, db, dA, ddt, dh0 = chunk_gated_delta_rule_bwd_fused_gates(
+            q, k, v, a, b, A_log, dt_bias, d_o.contiguous(),
+            None if d_fin is None else d_fin.contiguous(), scale=ctx.scale, initial_state=init,
+            use_qk_l2norm_in_kernel=ctx.use_l2, cu_seqlens=cu,
+            need_d_initial_state=init is not None and ctx.needs_input_grad[7])
+        return (dq, dk, dv, da.to(a.dtype), db.to(b.dtype), dA, ddt, dh0, None, None, None, None)
+
+
+def chunk_gated_delta_rule_fused_gates_trainable(q, k, v, a, b, A_log, dt_bias, scale=None,
+                                                 initial_state=None, output_final_state=False,
+                                                 use_qk_l2norm_in_kernel=False, cu_seqlens=None):
+    """:func:`chunk_gated_delta_rule_fused_gates` as a differentiable op (torch autograd): the
+    forward is gdn_chunk_fwd_gated, the backward gdn_chunk_bwd_gated, so gradients reach the
+    gate features a, b and the parameters A_log, dt_bias."""
+    return _ChunkGatedDeltaRuleFusedGates.apply(q, k, v, a, b, A_log, dt_bias, initial_state,
+                                                scale, output_final_state,
+                                                use_qk_l2norm_in_kernel, cu_seqlens)
 
 
 def gated_delta_decode_fused_gates(q, k, v, a, b, A_log, dt_bias, ssm_state, batch_indices=None,

@@ -65,6 +65,8 @@ int gdn_chunk_fwd_path(int K, int V, gdn_dtype_t io_dtype, gdn_dtype_t beta_dtyp
   return gdn::chunk_tc_supported(K, V, io_dtype, beta_dtype) ? 1 : 0;
 }
 
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
 // SM count of the current device, 0 when there is none.
 static int current_sm_count() {
   int dev = 0;
@@ -258,6 +260,70 @@ gdn_status_t gdn_chunk_bwd(const void* q, const void* k, const void* v, const fl
   return gdn::launch_chunk_bwd(a, b) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+size_t gdn_chunk_bwd_gated_workspace_size(int B, int T, int Hqk, int Hv, int K, int V,
+                                          int num_seqs, gdn_dtype_t io_dtype) {
+  const size_t inner = gdn_chunk_bwd_workspace_size(B, T, Hqk, Hv, K, V, num_seqs, io_dtype, GDN_F32);
+  if (inner == (size_t)-1 || Hv > 256) return (size_t)-1;
+  return ((inner + 255) & ~(size_t)255) + gdn::gates_bwd_extra_bytes((long long)B * T, Hv);
+}
+
+gdn_status_t gdn_chunk_bwd_gated(const void* q, const void* k, const void* v, const void* a,
+                                 const void* b, gdn_dtype_t ab_dtype, const float* A_log,
+                                 const float* dt_bias, int B, int T, int Hqk, int Hv, int K, int V,
+                                 gdn_dtype_t io_dtype, float scale, int chunk_size,
+                                 const float* initial_state, int use_qk_l2norm,
+                                 const int32_t* cu_seqlens, int num_seqs, const void* d_o,
+                                 const float* d_final_state, void* dq, void* dk, void* dv,
+                                 float* da, float* db, float* dA_log, float* ddt_bias,
+                                 float* d_initial_state, void* workspace, size_t workspace_bytes,
+                                 int* dev_status, void* stream) {
+  gdn_status_t st = check_chunk_shapes(B, T, Hqk, Hv, K, V, io_dtype, GDN_F32);
+  if (st != GDN_OK) return st;
+  if (Hv > 256) return GDN_ERR_UNSUPPORTED;
+  const long long T_total = (long long)B * T;
+  st = check_gate_args(a, b, ab_dtype, A_log, dt_bias, io_dtype, T_total);
+  if (st != GDN_OK) return st;
+  if (!A_log || !dt_bias || !dA_log || !ddt_bias || (T_total > 0 && (!da || !db)))
+    return GDN_ERR_NULL;
+  if (((uintptr_t)da & 3u) || ((uintptr_t)db & 3u) || ((uintptr_t)dA_log & 3u) ||
+      ((uintptr_t)ddt_bias & 3u))
+    return GDN_ERR_LAYOUT;
+  if (chunk_size != 64) return GDN_ERR_UNSUPPORTED;
+  if (cu_seqlens && (B != 1 || num_seqs < 0)) return GDN_ERR_SHAPE;
+  const int N = cu_seqlens ? num_seqs : B;
+  const size_t need = gdn_chunk_bwd_gated_workspace_size(B, T, Hqk, Hv, K, V, N, io_dtype);
+  if (need == (size_t)-1) return GDN_ERR_SHAPE;
+  if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE;
+  if (((uintptr_t)workspace & 255u) != 0) return GDN_ERR_LAYOUT;
+  const size_t inner = gdn_chunk_bwd_workspace_size(B, T, Hqk, Hv, K, V, N, io_dtype, GDN_F32);
+  uint8_t* w = reinterpret_cast<uint8_t*>(workspace);
+  const size_t part = align256((size_t)T_total * Hv * sizeof(float));
+  size_t off = align256(inner);
+  float* g = reinterpret_cast<float*>(w + off); off += part;
+  float* beta = reinterpret_cast<float*>(w + off); off += part;
+  float* dg = reinterpret_cast<float*>(w + off); off += part;
+  float* dbeta = reinterpret_cast<float*>(w + off); off += part;
+  float* partial = reinterpret_cast<float*>(w + off);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  gdn::GateArgs gates{};
+  gates.mode = gdn::kGatesFused;
+  gates.a = a;
+  gates.b = b;
+  gates.ab_dtype = ab_dtype;
+  gates.A_log = A_log;
+  gates.dt_bias = dt_bias;
+  if (gdn::launch_gates_materialise(gates, T_total, Hv, g, beta, s) != cudaSuccess) return GDN_ERR_CUDA;
+  st = gdn_chunk_bwd(q, k, v, g, beta, B, T, Hqk, Hv, K, V, io_dtype, GDN_F32, scale, chunk_size,
+                     initial_state, use_qk_l2norm, cu_seqlens, num_seqs, d_o, d_final_state, dq,
+                     dk, dv, dg, dbeta, d_initial_state, workspace, inner, dev_status, stream);
+  if (st != GDN_OK) return st;
+  return gdn::launch_gates_bwd(gates, dg, dbeta, T_total, Hv, da, db, dA_log, ddt_bias, partial,
+                               s) == cudaSuccess
+             ? GDN_OK
+             : GDN_ERR_CUDA;
+}
+
 static gdn_status_t decode_impl(const void* q, const void* k, const void* v, const float* g,
                                 const void* beta, float* ssm_state, int num_slots,
                                 const int32_t* batch_indices, int n, int Hqk, int Hv, int K, int V,
@@ -343,7 +409,6 @@ gdn_status_t gdn_decode_gated(const void* q, const void* k, const void* v, const
 
 // ---- Gated Delta Product ("Megatron-Core API: core.ssm.gated_delta_product")
 
-static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Workspace of the product's chunk forward: q', g', o' over the T * n_h writes, the scaled
 // cu_seqlens, then the chunk kernels' own workspace for the write sequence.

@@ -165,6 +165,17 @@ cudaError_t launch_chunk_tc_planned(const ChunkArgs& a);
 
 cudaError_t launch_decode(const DecodeArgs& a);
 
+// Backward through the fused gates: g and beta materialised (fp32) from the gate features, and
+// the chain rule from dg, dbeta to da, db ([T_total, Hv] fp32) and dA_log, ddt_bias ([Hv],
+// deterministic sums).  Hv <= 256.  gates_bwd_extra_bytes: the scratch for g, beta, dg, dbeta
+// and the per-CTA partial sums (each part 256-byte aligned, in that order).
+size_t gates_bwd_extra_bytes(long long T_total, int Hv);
+cudaError_t launch_gates_materialise(const GateArgs& ga, long long T_total, int Hv, float* g,
+                                     float* beta, cudaStream_t stream);
+cudaError_t launch_gates_bwd(const GateArgs& ga, const float* dg, const float* dbeta,
+                             long long T_total, int Hv, float* da, float* db, float* dA_log,
+                             float* ddt_bias, float* partial, cudaStream_t stream);
+
 // Gated Delta Product as the gated delta rule over the sequence of writes: q' (the query on
 // the last write of each token), g' (the decay on the first), n_h * cu_seqlens, and the
 // output rows of the last writes gathered back.

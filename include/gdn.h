@@ -379,6 +379,42 @@ size_t gdn_chunk_bwd_workspace_size(int B, int T, int Hqk, int Hv, int K, int V,
                                     gdn_dtype_t io_dtype, gdn_dtype_t beta_dtype);
 
 /*
+ * gdn_chunk_bwd_gated -- backward of gdn_chunk_fwd_gated: the gradients reach the gate
+ * features and the per-head gate parameters ("Megatron-Core API: core.ssm.gated_delta_net.gdn",
+ * GatedDeltaNet._compute_gates: "the per-head log-decay g and the write strength beta" from
+ * A_log and dt_bias).  With x = a + dt_bias[h] and the chunked backward's dg, dbeta:
+ *     da = dg * (-exp(A_log[h]) * sigmoid(x)),       db = dbeta * beta * (1 - beta),
+ *     dA_log[h] = sum over every token of dg * g,     ddt_bias[h] = sum over every token of da,
+ * the derivative of g = -exp(A_log) softplus(x) and beta = sigmoid(b).  g and beta are evaluated
+ * in fp32 as the fused forward evaluates them; the two sums are deterministic (fixed-order
+ * per-CTA partials added in block order in fp64), so the whole call is bitwise reproducible.
+ *
+ * Arguments: those of gdn_chunk_bwd with the fused-gate inputs of gdn_chunk_fwd_gated (a, b
+ * [B, T, Hv] ab_dtype = GDN_F32 or io_dtype; A_log, dt_bias [Hv] fp32) in place of g and beta.
+ *   dq, dk, dv, d_initial_state  as gdn_chunk_bwd.
+ *   da, db        [B, T, Hv] fp32, device, written completely (zero past the last sequence).
+ *   dA_log, ddt_bias  [Hv] fp32, device.
+ *   workspace     gdn_chunk_bwd_gated_workspace_size(...) bytes, 256-byte aligned: the chunked
+ *                 backward's scratch followed by g, beta, dg, dbeta (4 bytes per token and head
+ *                 each) and the partial sums.
+ * Hv must be at most 256 (GDN_ERR_UNSUPPORTED).  Other errors as gdn_chunk_bwd.
+ */
+gdn_status_t gdn_chunk_bwd_gated(const void* q, const void* k, const void* v, const void* a,
+                                 const void* b, gdn_dtype_t ab_dtype, const float* A_log,
+                                 const float* dt_bias, int B, int T, int Hqk, int Hv, int K, int V,
+                                 gdn_dtype_t io_dtype, float scale, int chunk_size,
+                                 const float* initial_state, int use_qk_l2norm,
+                                 const int32_t* cu_seqlens, int num_seqs, const void* d_o,
+                                 const float* d_final_state, void* dq, void* dk, void* dv,
+                                 float* da, float* db, float* dA_log, float* ddt_bias,
+                                 float* d_initial_state, void* workspace, size_t workspace_bytes,
+                                 int* dev_status, void* stream);
+
+/* Workspace (bytes) of gdn_chunk_bwd_gated; (size_t)-1 for sizes it would reject. */
+size_t gdn_chunk_bwd_gated_workspace_size(int B, int T, int Hqk, int Hv, int K, int V,
+                                          int num_seqs, gdn_dtype_t io_dtype);
+
+/*
  * gdn_selftest_wait_timeout -- the bounded wait of the fused kernels, run on its own.
  *
  * The sources have no counterpart for this entry point: it tests the failure detection of
