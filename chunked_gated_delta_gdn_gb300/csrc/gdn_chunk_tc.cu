@@ -107,6 +107,24 @@ static_assert(OFF_TSLOT + 4 <= SMEM_USED, "barrier block");
 static_assert(QK_STAGE == kQkStageBytes && V_STAGE == kVStageBytes, "stage bytes");
 static_assert(OFF_P + 2 * 8192 <= OFF_REC && OFF_REC + 16384 <= OFF_TW, "record staging");
 
+// Stage timestamps for the per-chunk cycle budget (a diagnostic build, -DGDN_CHUNK_STAMPS):
+// the leader of each group records clock64 at the stage boundaries of chunks 32 .. 95 in the
+// first and the last CTA of a forward-mode launch (gdn_chunk_stamps_read copies them out).
+// Without the define the stamps compile to nothing.
+#ifdef GDN_CHUNK_STAMPS
+__device__ unsigned long long g_chunk_stamps[2][2][64][16];
+#define GDN_STAMP(grp, p)                                                                       \
+  do {                                                                                          \
+    const int stamp_cta_ = blockIdx.x == 0 ? 0 : (blockIdx.x == gridDim.x - 1 ? 1 : -1);        \
+    if (!kRecord && leader && stamp_cta_ >= 0 && c >= 32 && c < 96)                             \
+      g_chunk_stamps[stamp_cta_][grp][c - 32][p] = clock64();                                   \
+  } while (0)
+#else
+#define GDN_STAMP(grp, p) \
+  do {                    \
+  } while (0)
+#endif
+
 // The Tw / Tu operands of chunk c: one buffer in record mode; two, by chunk parity, in forward
 // mode, the second in the record-staging space that forward mode does not use.
 template <bool kRecord>
@@ -144,6 +162,7 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
     const int L = min(kChunk, eos - t0);
     float* vec = reinterpret_cast<float*>(sm + OFF_VEC) + s * VEC_FLOATS;
     const uint32_t qk_a = sbase + OFF_QK + s * QK_STAGE;
+    GDN_STAMP(0, 0);
 
     // ---- per-token vectors of chunk c - 2 released; this chunk's tiles landed
     // (one thread polls each mbarrier; the rest of the group sleeps in the named barrier)
@@ -153,12 +172,14 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
       ok = ok && mbar_wait(&bars[B_FULL + s], (uint32_t)(c >> 1) & 1u, kWaitLimitNs);
     }
     if (group_sync_or(kBarPrep, kPrepThreads, !ok || flag_set(flag))) { if (leader) set_flag(flag); return; }
+    GDN_STAMP(0, 1);
 
     // ---- MMA: D1 = [Q;K][Q;K]^T.  (Issuing it earlier, during the previous chunk, measured
     //      slower: an MMA issue into the busy tensor pipe stalls the issuing thread.)
     if (leader) {
       tc_fence_after();
       issue_d1(tbase + COL_D1, qk_a, &bars[B_MMA_P]);
+      GDN_STAMP(0, 2);
     }
     // ---- gates: in-chunk cumulative log-decay and beta; prefetch the next chunk's
     if (warp == kGateWarp)
@@ -169,22 +190,71 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
     }
     if (group_sync_or(kBarPrep, kPrepThreads, !ok || flag_set(flag))) { if (leader) set_flag(flag); return; }
     tc_fence_after();
+    GDN_STAMP(0, 3);
 
     // ---- norms, P (to this chunk's P buffer) and A from D1
     norms_p_a<kBarPrep>(a, tbase + COL_D1, vec, sA, sm + OFF_P + s * 8192, L);
     tc_fence_before();
+    GDN_STAMP(0, 4);
     // Tw, Tu free: released by chunk c - 1 (one buffer) or c - 2 (forward mode, two buffers)
     if (leader && c >= (kRecord ? 1 : 2))
       ok = mbar_wait(&bars[wu_bar<kRecord>(c)], (uint32_t)(kRecord ? (c - 1) : ((c - 2) >> 1)) & 1u, kWaitLimitNs);
     if (group_sync_or(kBarPrep, kPrepThreads, !ok || flag_set(flag))) { if (leader) set_flag(flag); return; }
 
     // ---- T = (I + A)^{-1} as the Tw / Tu operands
+    GDN_STAMP(0, 5);
     solve_t<kBarPrep>(sA, sTd, vec, sm + tw_off<kRecord>(c), sm + tu_off<kRecord>(c));
     fence_proxy_async_smem();
     group_sync(kBarPrep, kPrepThreads);
 
     // ---- hand chunk c to the state group (which runs the W / U products) and move on
+    GDN_STAMP(0, 6);
     if (leader) mbar_arrive(&bars[B_READY + s]);
+  }
+}
+
+// Cold paths of the state group, kept out of line so the per-chunk code stays compact.
+__device__ __noinline__ void load_state_tmem(uint32_t taddr, int row, const float* init, bool identity) {
+#pragma unroll 1
+  for (int part = 0; part < 4; ++part) {
+    float x[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      x[j] = identity ? (32 * part + j == row ? 1.f : 0.f)
+                      : (init ? init[(size_t)(32 * part + j) * DV + row] : 0.f);
+    tmem_st32(taddr + 32 * part, x);
+  }
+}
+
+__device__ __noinline__ void store_state_tmem(uint32_t taddr, int row, float* fin, bool transposed) {
+#pragma unroll 1
+  for (int part = 0; part < 4; ++part) {
+    float x[32];
+    tmem_ld32(taddr + 32 * part, x);
+    if (transposed) {   // [V][K]: this thread's row, 32 consecutive floats
+      float4* dst = reinterpret_cast<float4*>(fin + (size_t)row * DK + 32 * part);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) dst[j] = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) fin[(size_t)(32 * part + j) * DV + row] = x[j];
+    }
+  }
+}
+
+// The last, partial chunk of a sequence: o rows t < L written one by one.
+__device__ __noinline__ void store_partial_output(__nv_bfloat16* out, uint32_t o1, uint32_t o2,
+                                                  const float* qs, int L, size_t row0, size_t stride) {
+#pragma unroll 1
+  for (int half = 0; half < 2; ++half) {
+    float x[32], y[32];
+    tmem_ld32(o1 + 32 * half, x);
+    tmem_ld32(o2 + 32 * half, y);
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) {
+      const int t = 32 * half + jj;
+      if (t < L) out[row0 + (size_t)t * stride] = __float2bfloat16_rn(fmaf(qs[t], x[jj], y[jj]));
+    }
   }
 }
 
@@ -214,6 +284,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     float* vec = reinterpret_cast<float*>(sm + OFF_VEC) + s * VEC_FLOATS;
     const uint32_t qk_a = sbase + OFF_QK + s * QK_STAGE;
     const uint32_t v_a = sbase + OFF_V + s * V_STAGE;
+    GDN_STAMP(1, 0);
 
     bool ok = true;
     if (leader) {
@@ -223,6 +294,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     }
     if (group_sync_or(kBarState, kStateThreads, !ok || flag_set(flag))) { failed = true; break; }
     tc_fence_after();
+    GDN_STAMP(1, 1);
 
     // ---- MMA: U^T = V^T Tu^T (operands MN-major), running while the state is converted
     if (leader) {
@@ -232,6 +304,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
         mma_bf16(tbase + COL_U, sdesc_sw128(v_a + ks * 2048, 8192, 1024),
                  sdesc_sw128(sbase + tu_off<kRecord>(c) + ks * 2048, 8192, 1024), id, ks > 0);
       }
+      GDN_STAMP(1, 2);
     }
     // ---- record mode: the entry state as a bf16 tile, rows dk, 64 dv per 128-byte row in two
     //      16 KB halves, 128-byte swizzled (element (dk, dv) at (dv / 64) 16384 + dk 128 +
@@ -276,7 +349,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     //      S <- exp(G_last) S in TMEM
     {
       const float dl = ex2(vec[VEC_G + L - 1]);
-#pragma unroll
+#pragma unroll 1
       for (int pair = 0; pair < 2; ++pair) {
         float pk[32];
 #pragma unroll
@@ -295,6 +368,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     }
     tc_fence_before();
     group_sync(kBarState, kStateThreads);
+    GDN_STAMP(1, 3);
 
     // ---- MMA: [O1 | Y] = S^T [Q; K]^T, one N = 128 product over the stage as loaded (A, the
     //      bf16 S^T, from TMEM)
@@ -308,6 +382,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
                     id5, ks > 0);
       }
       mma_commit(&bars[B_MMA_S]);
+      GDN_STAMP(1, 4);
     }
     // ---- while [O1 | Y] runs: P copied next to K~^T, and K~^T built from the stage's K rows,
     //      scaled by exp(G_last - G_t) r_k[t] and transposed in 8 x 8 blocks (ldmatrix,
@@ -323,7 +398,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
       // fragment register m holds token 8 (2 wq + (m & 1)) + lane / 4
       const float dl0 = vec[VEC_DL + 16 * wq + (lane >> 2)];
       const float dl1 = vec[VEC_DL + 16 * wq + 8 + (lane >> 2)];
-#pragma unroll
+#pragma unroll 2
       for (int it = 0; it < 8; ++it) {
         const int dg = 2 * it + (mi >> 1);       // dk group of the matrix this lane addresses
         const int tok = 8 * tg + rr, dk = 8 * dg;
@@ -342,9 +417,11 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
       }
     }
     fence_proxy_async_smem();
+    GDN_STAMP(1, 5);
     if (leader) ok = mbar_wait(&bars[B_MMA_S], ps, kWaitLimitNs);
     ps ^= 1u;
     if (group_sync_or(kBarState, kStateThreads, !ok || flag_set(flag))) { failed = true; break; }
+    GDN_STAMP(1, 6);
     // every read of stage s is done (U, D1, [O1 | Y], the K copy): load chunk c + 2 into it;
     // P of chunk c has been copied: the prep group may overwrite it
     if (leader) {
@@ -378,6 +455,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     }
     tc_fence_before();
     group_sync(kBarState, kStateThreads);
+    GDN_STAMP(1, 7);
 
     // ---- MMA: U'^T = U^T + (-Y) Tw^T (Tw MN-major); then Tw / Tu are free for the prep group
     if (leader) {
@@ -390,11 +468,13 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
       }
       mma_commit(&bars[wu_bar<kRecord>(c)]);
       mma_commit(&bars[B_MMA_S]);
+      GDN_STAMP(1, 8);
     }
     if (leader) ok = mbar_wait(&bars[B_MMA_S], ps, kWaitLimitNs);
     ps ^= 1u;
     if (group_sync_or(kBarState, kStateThreads, !ok || flag_set(flag))) { failed = true; break; }
     tc_fence_after();
+    GDN_STAMP(1, 9);
 
     // ---- record mode: U' as a bf16 tile, rows = the chunk's 64 tokens (zero from L on), 64 dv
     //      per 128-byte row in two 8 KB halves, 128-byte swizzled; staged at OFF_REC once the
@@ -450,6 +530,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     }
     tc_fence_before();
     group_sync(kBarState, kStateThreads);
+    GDN_STAMP(1, 10);
 
     // ---- MMA: [O2 | S^T] += U'^T [P; K~^T]^T, one N = 192 product (A, the bf16 U', from TMEM)
     if (leader) {
@@ -461,11 +542,13 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
                     sdesc_sw128(sbase + OFF_PF + ks * 32, 16, 1024), id67, 1);
       }
       mma_commit(&bars[B_MMA_S]);
+      GDN_STAMP(1, 11);
     }
     if (leader) ok = mbar_wait(&bars[B_MMA_S], ps, kWaitLimitNs);
     ps ^= 1u;
     if (group_sync_or(kBarState, kStateThreads, !ok || flag_set(flag))) { failed = true; break; }
     tc_fence_after();
+    GDN_STAMP(1, 12);
 
     // ---- o = scale exp(G) r_q O1 + O2 (P carries scale r_q): a full chunk is staged as a
     //      bf16 tile (two 128-byte-swizzled [64 tokens][64 dv] halves) and written by one
@@ -482,7 +565,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
       const uint32_t st_base = sbase + OFF_S + (d0 >> 6) * 8192 + rr * 128 +
                                ((((d0 & 63) >> 3) ^ rr) << 4);
       const float* qs = vec + VEC_QS + 2 * (lane & 3);   // scale r_q exp(G): factor of O1
-#pragma unroll
+#pragma unroll 1
       for (int pass = 0; pass < 2; ++pass) {   // tokens 32 pass .. 32 pass + 31
         uint32_t a0[16], a1[16], b0[16], b1[16];
         tmem_ld16x256b_x4(tbase + lane_off + COL_O1 + 32 * pass, a0);                  // dv 0-15
@@ -517,22 +600,12 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
         tma_store_commit();
       }
     } else {
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float x[32], y[32];
-        tmem_ld32(tbase + lane_off + COL_O1 + 32 * half, x);
-        tmem_ld32(tbase + lane_off + COL_O2 + 32 * half, y);
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int t = 32 * half + jj;
-          if (t < L)
-            out[((size_t)(t0 + t) * a.Hv + h) * DV + row] =
-                __float2bfloat16_rn(fmaf(vec[VEC_QS + t], x[jj], y[jj]));
-        }
-      }
+      store_partial_output(out, tbase + lane_off + COL_O1, tbase + lane_off + COL_O2, vec + VEC_QS, L,
+                           ((size_t)t0 * a.Hv + h) * DV + row, (size_t)a.Hv * DV);
     }
     tc_fence_before();
     group_sync(kBarState, kStateThreads);
+    GDN_STAMP(1, 13);
     if (leader) mbar_arrive(&bars[B_VEC_FREE + s]);
   }
 
@@ -544,19 +617,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     }
   } else if (fin) {
     tc_fence_after();
-#pragma unroll
-    for (int part = 0; part < 4; ++part) {
-      float x[32];
-      tmem_ld32(tbase + lane_off + COL_S + 32 * part, x);
-      if (uflags & kUnitFinT) {   // [V][K]: this thread's row, 32 consecutive floats
-        float4* dst = reinterpret_cast<float4*>(fin + (size_t)row * DK + 32 * part);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) dst[j] = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) fin[(size_t)(32 * part + j) * DV + row] = x[j];
-      }
-    }
+    store_state_tmem(tbase + lane_off + COL_S, row, fin, (uflags & kUnitFinT) != 0);
   }
 }
 
@@ -659,15 +720,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // Initial state -> TMEM (S^T: lane = value index, columns = key index).
     const int row = 32 * ((tid - kPrepThreads) >> 5) + (tid & 31);
     const uint32_t lane_off = (uint32_t)(32 * ((tid - kPrepThreads) >> 5)) << 16;
-#pragma unroll
-    for (int part = 0; part < 4; ++part) {
-      float x[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        x[j] = identity ? (32 * part + j == row ? 1.f : 0.f)
-                        : (init ? init[(size_t)(32 * part + j) * DV + row] : 0.f);
-      tmem_st32(tbase + lane_off + COL_S + 32 * part, x);
-    }
+    load_state_tmem(tbase + lane_off + COL_S, row, init, identity);
     const long long rec0 = kRecord ? a.rec_chunk_off[n] : 0;
     state_group<kRecord>(a, sm, tbase, bos, eos, nchunks, h, hq, fin, uflags, rec0, &tmQ, &tmK, &tmV,
                          &tmO);
@@ -760,3 +813,11 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a) {
 }
 
 }  // namespace gdn
+
+#ifdef GDN_CHUNK_STAMPS
+// The stage timestamps of the last forward-mode launch of the stamped build
+// ([2 CTAs][prep, state][chunks 32 .. 95][16] clock64 values); returns a cudaError_t.
+extern "C" int gdn_chunk_stamps_read(void* host) {
+  return (int)cudaMemcpyFromSymbol(host, gdn::g_chunk_stamps, sizeof(gdn::g_chunk_stamps));
+}
+#endif

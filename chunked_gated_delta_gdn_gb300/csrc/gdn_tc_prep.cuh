@@ -227,36 +227,23 @@ __device__ __forceinline__ void norms_p_a(const ChunkArgs& a, uint32_t d1, float
     const float4 h4 = *reinterpret_cast<const float4*>(vec + VEC_H + j0 + 4 * m);
     hj[4 * m] = h4.x; hj[4 * m + 1] = h4.y; hj[4 * m + 2] = h4.z; hj[4 * m + 3] = h4.w;
   }
-  const bool zero_tile = ((quad & 1) == 0) && chalf == 1;   // rows 0-31 x cols 32-63
-  if (quad < 2) {
-    const int i = row;
-    // row factor scale r_q[i] (zero past the chunk end: lg2(0) = -inf gives exact zeros)
-    const float ui = vec[VEC_G + i] + lg2((i < L) ? a.scale * vec[VEC_RQ + i] : 0.f);
-    if (zero_tile) {
+  // one code path for both halves: P rows (quads 0-1) keep j <= i with the row factor scale r_q[i]
+  // (zero past the chunk end: lg2(0) = -inf gives exact zeros), A rows (quads 2-3) keep j < i with
+  // the row factor beta r_k[i]; both as exponents
+  const bool is_p = quad < 2;
+  const int i = is_p ? row : row - 64;
+  const float base = vec[VEC_G + i] + lg2(is_p ? ((i < L) ? a.scale * vec[VEC_RQ + i] : 0.f)
+                                               : vec[VEC_BETA + i] * vec[VEC_RK + i]);
+  const int lim = is_p ? i : i - 1;
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj) x[jj] = 0.f;
-    } else {
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
-        const float e = x[jj] * ex2(ui - hj[jj]);
-        x[jj] = (j0 + jj <= i) ? e : 0.f;
-      }
-    }
+  for (int jj = 0; jj < 32; ++jj) {
+    const float e = x[jj] * ex2(base - hj[jj]);
+    x[jj] = (j0 + jj <= lim) ? e : 0.f;
+  }
+  if (is_p) {
 #pragma unroll
     for (int m = 0; m < 4; ++m) store_bf16x8(p_dst + sw128_offset(i, j0 + 8 * m), &x[8 * m]);
   } else {
-    const int i = row - 64;
-    const float vi = vec[VEC_G + i] + lg2(vec[VEC_BETA + i] * vec[VEC_RK + i]);   // beta r_k[i]
-    if (zero_tile) {
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) x[jj] = 0.f;
-    } else {
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
-        const float e = x[jj] * ex2(vi - hj[jj]);
-        x[jj] = (j0 + jj < i) ? e : 0.f;
-      }
-    }
 #pragma unroll
     for (int m = 0; m < 8; ++m)
       *reinterpret_cast<float4*>(&sA[a_idx(i, j0 + 4 * m)]) =
