@@ -19,8 +19,8 @@
 //                                          M=128 N=64  K=64    (accumulates on U^T; this is
 //                                                               U - W S with W = Tw K; -Y is
 //                                                               read from TMEM as bf16)
-//   [O2 | S^T] += U'^T [P; K~^T]^T        M=128 N=192 K=64    (O2 columns zeroed first;
-//                                                               K~ = diag(exp(G_last - G) r_k) K,
+//   O2 = U'^T P^T                          M=128 N=64  K=64
+//   S^T += U'^T K~                         M=128 N=128 K=64    (K~ = diag(exp(G_last - G) r_k) K,
 //                                                               S^T decayed by exp(G_last) before)
 //   o   = scale exp(G) r_q * O1 + O2
 //
@@ -63,10 +63,9 @@ constexpr uint32_t QK_STAGE = 32768;
 constexpr uint32_t OFF_V = 65536;       // 2 stages x 16 KB: [dv half][64 tokens][128 B]
 constexpr uint32_t V_STAGE = 16384;
 constexpr uint32_t OFF_S = 98304;       // the bf16 output tile staged for its TMA store (16 KB)
-constexpr uint32_t OFF_PF = 122880;     // copy of this chunk's P (8 KB), directly followed by
 constexpr uint32_t OFF_KT = 131072;     // K~^T: the K rows scaled by exp(G_last - G_t) r_k[t],
-                                        // transposed, K-major [128 dk rows][64 tokens]: together
-                                        // [P; K~^T] is the N = 192 B operand of the last product
+                                        // transposed, K-major [128 dk rows][64 tokens] (the B
+                                        // operand of the state update; the 8 KB below are free)
 constexpr uint32_t OFF_A = 147456;      // fp32 A [64][64], 16-byte-group swizzled; the solve
                                         // overwrites its strictly-lower blocks with those of T
 constexpr uint32_t OFF_P = 163840;      // 2 x P, K-major B [64 i][64 j]
@@ -94,7 +93,7 @@ enum {
   B_MMA_S = 3,      // state group's MMA commits
   B_READY = 4,      // [2] prep -> state: chunk ready (vectors, P, Tw / Tu in shared memory)
   B_WU = 6,         // [2 by buffer, see B_WU1] state -> prep: the MMAs reading Tw / Tu are done
-  B_P_FREE = 7,     // [2] state -> prep: P copied out (its buffer free)
+  B_P_FREE = 7,     // [2] state -> prep: the O2 product has read P (its buffer free)
   B_VEC_FREE = 9,   // [2] state -> prep: chunk finished (per-token vectors free)
   B_WU1 = 11,       // forward mode: as B_WU, for the second Tw / Tu buffer
   B_COUNT = 12
@@ -260,7 +259,7 @@ __device__ __noinline__ void store_partial_output(__nv_bfloat16* out, uint32_t o
 
 // =================================================================== state group
 // Warps 8-11.  For each chunk: U^T = V^T Tu^T, S -> bf16 operand and decay of the TMEM
-// state, [O1 | Y] = S^T [Q; K]^T, U' = U - Y Tw^T, [O2 | S^T] += U'^T [P; K~^T]^T, output.
+// state, [O1 | Y] = S^T [Q; K]^T, U' = U - Y Tw^T, O2 = U'^T P^T, S^T += U'^T K~, output.
 template <bool kRecord>
 __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int bos, int eos,
                             int nchunks, int h, int hq, float* fin, int uflags, long long rec0,
@@ -384,14 +383,10 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
       mma_commit(&bars[B_MMA_S]);
       GDN_STAMP(1, 4);
     }
-    // ---- while [O1 | Y] runs: P copied next to K~^T, and K~^T built from the stage's K rows,
+    // ---- while [O1 | Y] runs: K~^T built from the stage's K rows,
     //      scaled by exp(G_last - G_t) r_k[t] and transposed in 8 x 8 blocks (ldmatrix,
     //      stmatrix .trans); warp wq takes tokens 16 wq .. 16 wq + 15.  Then the stage is free.
     {
-      const uint4* psrc = reinterpret_cast<const uint4*>(sm + OFF_P + s * 8192);
-      uint4* pdst = reinterpret_cast<uint4*>(sm + OFF_PF);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) pdst[tid + 128 * e] = psrc[tid + 128 * e];
       const int mi = lane >> 3, rr = lane & 7;   // matrix this lane addresses, row within it
       const int tg = 2 * wq + (mi & 1);          // its token group (8 tokens)
       const uint32_t kst = sbase + OFF_QK + s * QK_STAGE + 8192;
@@ -422,13 +417,11 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     ps ^= 1u;
     if (group_sync_or(kBarState, kStateThreads, !ok || flag_set(flag))) { failed = true; break; }
     GDN_STAMP(1, 6);
-    // every read of stage s is done (U, D1, [O1 | Y], the K copy): load chunk c + 2 into it;
-    // P of chunk c has been copied: the prep group may overwrite it
+    // every read of stage s is done (U, D1, [O1 | Y], the K copy): load chunk c + 2 into it
     if (leader) {
       if (c + 2 < nchunks)
         issue_chunk_loads(sm + OFF_QK + s * QK_STAGE, sm + OFF_V + s * V_STAGE, &bars[B_FULL + s], tq, tk,
                           tv, t0 + 2 * kChunk, hq, h, !(uflags & kUnitZeroV));
-      mbar_arrive(&bars[B_P_FREE + s]);
     }
     tc_fence_after();
 
@@ -445,13 +438,6 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
         pk[16 + jj] = __uint_as_float(*reinterpret_cast<uint32_t*>(&p1));
       }
       tmem_st32(tbase + lane_off + COL_Y, pk);
-      // the O2 columns (the bf16 S^T, read by now) start from zero: the last product
-      // accumulates O2 and S^T in one go
-      float z[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) z[j] = 0.f;
-      tmem_st32(tbase + lane_off + COL_O2, z);
-      tmem_st32(tbase + lane_off + COL_O2 + 32, z);
     }
     tc_fence_before();
     group_sync(kBarState, kStateThreads);
@@ -532,15 +518,18 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     group_sync(kBarState, kStateThreads);
     GDN_STAMP(1, 10);
 
-    // ---- MMA: [O2 | S^T] += U'^T [P; K~^T]^T, one N = 192 product (A, the bf16 U', from TMEM)
+    // ---- MMA: O2 = U'^T P^T (from zero) and S^T += U'^T K~ (A, the bf16 U', from TMEM)
     if (leader) {
       tc_fence_after();
-      const uint32_t id67 = idesc_bf16(128, 192, false, false);
+      const uint32_t id2 = idesc_bf16(128, 64, false, false), idS = idesc_bf16(128, 128, false, false);
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
+      for (int ks = 0; ks < 4; ++ks)
         mma_bf16_ta(tbase + COL_O2, tbase + COL_U + 8 * ks,
-                    sdesc_sw128(sbase + OFF_PF + ks * 32, 16, 1024), id67, 1);
-      }
+                    sdesc_sw128(sbase + OFF_P + s * 8192 + ks * 32, 16, 1024), id2, ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16_ta(tbase + COL_S, tbase + COL_U + 8 * ks,
+                    sdesc_sw128(sbase + OFF_KT + ks * 32, 16, 1024), idS, 1);
       mma_commit(&bars[B_MMA_S]);
       GDN_STAMP(1, 11);
     }
@@ -548,6 +537,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     ps ^= 1u;
     if (group_sync_or(kBarState, kStateThreads, !ok || flag_set(flag))) { failed = true; break; }
     tc_fence_after();
+    if (leader) mbar_arrive(&bars[B_P_FREE + s]);   // the O2 product has read P
     GDN_STAMP(1, 12);
 
     // ---- o = scale exp(G) r_q O1 + O2 (P carries scale r_q): a full chunk is staged as a

@@ -25,9 +25,9 @@ PREP = ["loop top", "wait: per-token vectors free, TMA stage landed", "D1 issue 
         "wait: D1 done, P buffer free", "norms, P, A from D1", "wait: Tw / Tu buffer free",
         "solve T = (I + A)^-1 -> Tw, Tu"]
 STATE = ["loop top", "wait: chunk ready (prep)", "U issue (4 MMAs)", "S -> bf16 S^T, decay S",
-         "[O1|Y] issue (8 MMAs)", "P copy, K~^T build", "wait: [O1|Y] done", "-Y -> bf16, O2 zeroed",
-         "U' issue (4 MMAs)", "wait: U' done", "U' -> bf16", "[O2|S^T] issue (4 MMAs)",
-         "wait: [O2|S^T] done", "output epilogue"]
+         "[O1|Y] issue (8 MMAs)", "K~^T build", "wait: [O1|Y] done", "-Y -> bf16",
+         "U' issue (4 MMAs)", "wait: U' done", "U' -> bf16", "O2, S^T issue (4 + 4 MMAs)",
+         "wait: O2, S^T done", "output epilogue"]
 
 
 def run(B: int, T: int, reps: int = 3):
