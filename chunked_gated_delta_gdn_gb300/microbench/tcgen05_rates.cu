@@ -35,7 +35,7 @@ struct Out { unsigned long long v[128]; };
 // operand sources (the chunk kernel's products in brackets)
 enum Src { SS_KK = 0,   // A, B in smem, K-major           [D1 = [Q;K][Q;K]^T]
            SS_MM = 1,   // A, B in smem, MN-major          [U^T = V^T Tu^T]
-           TS_K = 2,    // A in TMEM, B smem K-major       [[O1|Y] = S^T [Q;K]^T, [O2|S^T]]
+           TS_K = 2,    // A in TMEM, B smem K-major       [[O1|Y] = S^T [Q;K]^T, O2, S^T update]
            TS_MN = 3 }; // A in TMEM, B smem MN-major      [U'^T += (-Y) Tw^T]
 
 template <int kSrc, int kN>
@@ -94,7 +94,9 @@ __global__ void __launch_bounds__(128, 1) rates_kernel(unsigned long long* out) 
 }
 
 // Part B: warp 0 times 64 N = 128 SS instructions (three repetitions) while warps 4-11 run
-// mma.sync tf32 (mode 1; mode 0: idle), stopping when warp 0 is done or after 2^20 rounds.
+// mma.sync tf32 (mode 1; mode 0: idle), stopping when warp 0 is done or after 2^20 rounds.  Mode
+// 2: no tcgen05 work; warp 0 only waits 14,100 cycles (about the time of mode 1) and the other
+// warps run mma.sync meanwhile.
 __global__ void __launch_bounds__(384, 1) interference_kernel(Out* out, int mode) {
   extern __shared__ __align__(1024) uint8_t raw[];
   uint8_t* sm = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
@@ -116,7 +118,12 @@ __global__ void __launch_bounds__(384, 1) interference_kernel(Out* out, int mode
     const unsigned long long tw = clk();
     while (clk() - tw < 2000) {}   // let the other warps start
     uint32_t phase = 0;
-    for (int rep = 0; rep < 3; ++rep) {
+    if (mode == 2) {
+      const unsigned long long t0 = clk();
+      while (clk() - t0 < 14100) {}
+      out->v[80] = clk() - t0;
+    }
+    for (int rep = 0; rep < 3 && mode != 2; ++rep) {
       if (tid == 0) {
         tc_fence_after();
         const unsigned long long t0 = clk();
@@ -130,7 +137,7 @@ __global__ void __launch_bounds__(384, 1) interference_kernel(Out* out, int mode
       phase ^= 1u;
     }
     if (tid == 0) *stop = 1;
-  } else if (warp >= 4 && mode == 1) {
+  } else if (warp >= 4 && mode >= 1) {
     float d0[4] = {0, 0, 0, 0}, d1[4] = {0, 0, 0, 0};
     uint32_t a[4], b[2];
     for (int j = 0; j < 4; ++j) a[j] = to_tf32(0.001f * (tid + j));
@@ -191,9 +198,9 @@ int main() {
   bad |= run_config<SS_KK, 256, 8>(dv, ss_kk, "-");
   bad |= run_config<SS_MM, 64, 4>(dv, ss_mm, "U^T = V^T Tu^T");
   bad |= run_config<SS_MM, 128, 4>(dv, ss_mm, "-");
-  bad |= run_config<TS_K, 64, 4>(dv, ts_k, "-");
-  bad |= run_config<TS_K, 128, 8>(dv, ts_k, "[O1|Y] = S^T [Q;K]^T");
-  bad |= run_config<TS_K, 192, 4>(dv, ts_k, "[O2|S^T] += U'^T [P;K~^T]^T");
+  bad |= run_config<TS_K, 64, 4>(dv, ts_k, "O2 = U'^T P^T");
+  bad |= run_config<TS_K, 128, 8>(dv, ts_k, "[O1|Y] = S^T [Q;K]^T; S^T += U'^T K~ (4 instr)");
+  bad |= run_config<TS_K, 192, 4>(dv, ts_k, "-");
   bad |= run_config<TS_K, 256, 8>(dv, ts_k, "-");
   bad |= run_config<TS_MN, 64, 4>(dv, ts_mn, "U'^T = U^T + (-Y) Tw^T");
   bad |= run_config<TS_MN, 128, 4>(dv, ts_mn, "-");
@@ -207,15 +214,18 @@ int main() {
   printf("\n## B. 64 N = 128 tcgen05.mma while other warps run mma.sync (tf32 m16n8k8)\n\n");
   printf("| other warps | 64 MMAs (3 repetitions) | mma.sync completed meanwhile (8 warps) |\n");
   printf("|---|---|---|\n");
-  for (int mode = 0; mode < 2; ++mode) {
+  for (int mode = 0; mode < 3; ++mode) {
     cudaMemset(d, 0, sizeof(Out));
     interference_kernel<<<1, 384, kSmem>>>(d, mode);
     if (check(cudaDeviceSynchronize(), "interference_kernel")) return 1;
     cudaMemcpy(&h, d, sizeof(Out), cudaMemcpyDeviceToHost);
     unsigned long long n = 0;
     for (int w = 0; w < 8; ++w) n += h.v[96 + w];
-    printf("| %s | %llu %llu %llu | %llu |\n", mode ? "8 warps of mma.sync" : "idle", h.v[80],
-           h.v[81], h.v[82], n);
+    if (mode == 2)
+      printf("| 8 warps of mma.sync, no tcgen05 work (window %llu cycles) | - | %llu |\n", h.v[80], n);
+    else
+      printf("| %s | %llu %llu %llu | %llu |\n", mode ? "8 warps of mma.sync" : "idle", h.v[80],
+             h.v[81], h.v[82], n);
   }
   cudaFree(d);
   return 0;
