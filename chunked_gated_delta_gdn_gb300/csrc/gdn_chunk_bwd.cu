@@ -985,6 +985,21 @@ __global__ void __launch_bounds__(kGradThreads) bwd_grad_kernel(const ChunkArgs 
 // F^T and E^T are MN-major A operands whose first 64-row block is a zero tile and whose
 // second is F (resp. E) as stored row-major, so no transposed copy is built.
 namespace tcg {
+
+// Store 16 consecutive 32-bit columns of this thread's lane and wait for the store.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
 using namespace sm100;
 constexpr int kThreads = 256;
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -1678,13 +1693,13 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(const ChunkArg
 // row dots dX_i . v_i (slot 0 of ws.XV, slots 1-3 zero).
 namespace tcr {
 using namespace sm100;
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;    // two warps per TMEM lane quarter
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t ST_Q = 0, ST_K = 16384, ST_V = 32768, ST_DO = 49152, ST_T = 65536, ST_P = 73728;
 constexpr uint32_t STAGE = 81920;
 constexpr uint32_t STAGE_TX = 4 * 16384 + 2 * 8192;
 constexpr uint32_t OFF_VEC = 2 * STAGE;              // per stage: G[64], beta[64]
-constexpr uint32_t OFF_RED = OFF_VEC + 2 * 128 * 4;  // [4 warps][64]
+constexpr uint32_t OFF_RED = OFF_VEC + 2 * 128 * 4;  // [4 lane quarters][64]
 constexpr uint32_t OFF_BAR = OFF_RED + 4 * 64 * 4;
 constexpr uint32_t OFF_FG = OFF_BAR + 64;                             // -gamma beta per token
 constexpr uint32_t OFF_STG_S = (OFF_FG + 256 + 1023) / 1024 * 1024;   // staging: the dS tile (32 KB)
@@ -1693,18 +1708,18 @@ constexpr uint32_t SMEM = OFF_STG_X + 16384 + 1024;
 static_assert(SMEM <= 232448, "shared memory budget");
 constexpr uint32_t C_S = 0, C_SB = 128, C_Y = 192, C_U = 256, C_X = 320, T_COLS = 512;
 
-// Stage `passes` x 32 TMEM columns starting at `col` (fp32, lane = v) as bf16 rows of a
+// Stage passes pass0 .. pass0 + npass - 1 of 32 TMEM columns from `col` (fp32, lane = v) as bf16 rows of a
 // 128-byte-swizzled tile at shared address `tile`: TMEM column j of lane v goes to row j,
 // element v of a 64-element half (halves `half` bytes apart).  16x256b loads hand each thread
 // the fragment of stmatrix .trans (rows j, 2 (t % 4) and + 1 of each 8-column group; v = t / 4
 // and t / 4 + 8 of each 16-lane half), which writes the 8 x 8 blocks transposed.
-__device__ __forceinline__ void stage_tile(uint32_t tb, uint32_t loff, uint32_t col, int passes,
-                                           uint32_t tile, uint32_t half, int warp, int lane) {
+__device__ __forceinline__ void stage_tile(uint32_t tb, uint32_t loff, uint32_t col, int pass0,
+                                           int npass, uint32_t tile, uint32_t half, int wq, int lane) {
   const int mblk = lane >> 3, rr = lane & 7;
-  const int d0 = 32 * warp + 8 * mblk;
+  const int d0 = 32 * wq + 8 * mblk;
   const uint32_t st_base = tile + (d0 >> 6) * half + rr * 128 + ((((d0 & 63) >> 3) ^ rr) << 4);
 #pragma unroll 1
-  for (int pass = 0; pass < passes; ++pass) {
+  for (int pass = pass0; pass < pass0 + npass; ++pass) {
     uint32_t a0[16], a1[16];
     tmem_ld16x256b_x4(tb + loff + col + 32 * pass, a0);                 // v 0-15 of the warp
     tmem_ld16x256b_x4(tb + loff + (16u << 16) + col + 32 * pass, a1);   // v 16-31
@@ -1739,10 +1754,10 @@ __device__ __forceinline__ void issue_stage(uint8_t* st, uint64_t* bar, const CU
   bulk_load(st + ST_P, tp + 8192, 8192, bar);
 }
 
-// dS^T (fp32, C_S) -> bf16 pairs in C_SB, the A operand of the next Y product.
-__device__ __forceinline__ void pack_state(uint32_t tb, uint32_t loff) {
-#pragma unroll
-  for (int p2 = 0; p2 < 2; ++p2) {
+// dS^T (fp32, C_S) -> bf16 pairs in C_SB, the A operand of the next Y product: columns
+// 64 p2 .. 64 p2 + 63 for warp group p2.
+__device__ __forceinline__ void pack_state(uint32_t tb, uint32_t loff, int p2) {
+  {
     float x[32], y[32], pk[32];
     tmem_ld32(tb + loff + C_S + 64 * p2, x);
     tmem_ld32(tb + loff + C_S + 64 * p2 + 32, y);
@@ -1782,18 +1797,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
   uint64_t* mmab = full + 2;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 24);
   const int Hv = a.Hv, h = blockIdx.x % Hv, n = blockIdx.x / Hv, hq = h / (Hv / a.Hqk);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, v = tid;
+  // warp group wg = warp / 4 takes half of the columns of every TMEM pass; wq = warp % 4 is the
+  // lane quarter (the value indices v) the warp may access
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wq = warp & 3, wg = warp >> 2;
+  const int v = 32 * wq + lane;
   const size_t st_off = ((size_t)n * Hv + h) * 128 * 128;
   if (!ws.chunk_off[a.num_seqs + 1]) {   // invalid cu_seqlens: zero gradient
     if (b.d_initial)
-      for (int d = 0; d < 128; ++d) b.d_initial[st_off + (size_t)d * 128 + v] = 0.f;
+      for (int d = wg; d < 128; d += 2) b.d_initial[st_off + (size_t)d * 128 + v] = 0.f;
     return;
   }
   int bos, eos;
   seq_bounds(a, n, &bos, &eos);
   const int first = ws.chunk_off[n];
   const int nch = (eos - bos + C - 1) / C;
-  const uint32_t loff = (uint32_t)(32 * warp) << 16;
+  const uint32_t loff = (uint32_t)(32 * wq) << 16;
   if (tid == 0) {
     mbar_init(&full[0], 1);
     mbar_init(&full[1], 1);
@@ -1818,16 +1836,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = *tslot;
-  {  // dS^T <- d_final^T
+  {  // dS^T <- d_final^T (warp group wg: columns 64 wg .. 64 wg + 63)
 #pragma unroll
-    for (int part = 0; part < 4; ++part) {
+    for (int part = 2 * wg; part < 2 * wg + 2; ++part) {
       float x[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j)
         x[j] = b.d_final ? b.d_final[st_off + (size_t)(32 * part + j) * 128 + v] : 0.f;
       tmem_st32(tb + loff + C_S + 32 * part, x);
     }
-    pack_state(tb, loff);
+    pack_state(tb, loff, wg);
   }
   if (nch > 0) {   // the first chunk's gates
     const int t1 = bos + (nch - 1) * C;
@@ -1848,12 +1866,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
     if (tid == 0) ok = mbar_wait(&full[s], (uint32_t)(it >> 1) & 1u, kWaitNs);
     if (__syncthreads_or(!ok)) { failed = true; break; }
     {  // norms; r_k k and scale gamma r_q q in place, -gamma beta per token; dO rows >= L zeroed
-      const int i = tid >> 1, hh = tid & 1;
+      const int i = tid >> 2, qq = tid & 3, hh = qq >> 1, c0 = 4 * (qq & 1);   // a quarter row
       uint8_t* qrow = st + ST_Q + hh * 8192 + i * 128;
       uint8_t* krow = st + ST_K + hh * 8192 + i * 128;
       float sq = 0.f, sk = 0.f;
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
+      for (int c8 = c0; c8 < c0 + 4; ++c8) {
         const uint4 uq = *reinterpret_cast<const uint4*>(qrow + 16 * c8);
         const uint4 uk = *reinterpret_cast<const uint4*>(krow + 16 * c8);
         const uint32_t wq[4] = {uq.x, uq.y, uq.z, uq.w}, wk[4] = {uk.x, uk.y, uk.z, uk.w};
@@ -1867,15 +1885,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
       }
       sq += __shfl_xor_sync(0xffffffffu, sq, 1);
       sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+      sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+      sk += __shfl_xor_sync(0xffffffffu, sk, 2);
       const bool l2 = a.use_qk_l2norm != 0;
       const float rq = l2 ? 1.0f / sqrtf(sq + kL2Eps) : 1.f, rk = l2 ? 1.0f / sqrtf(sk + kL2Eps) : 1.f;
       const float gi = expf(G[i]);
       const float fq = i < L ? a.scale * gi * rq : 0.f;
       const float fk = i < L ? rk : 0.f;
       // (the k rows already carry r_k)
-      if (hh == 0) reinterpret_cast<float*>(sm + OFF_FG)[i] = i < L ? -gi * bt[i] : 0.f;
+      if (qq == 0) reinterpret_cast<float*>(sm + OFF_FG)[i] = i < L ? -gi * bt[i] : 0.f;
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
+      for (int c8 = c0; c8 < c0 + 4; ++c8) {
         tcg::scale8(krow + 16 * c8, fk);
         tcg::scale8(qrow + 16 * c8, fq);
         if (i >= L)
@@ -1909,21 +1929,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
     tc_fence_after();
     {  // dU'^T = dUp^T + Y^T diag(lambda) -> bf16 pairs in C_U (lambda_j = 2^((G_L - G_j) log2 e))
       const float gl = G[L - 1];
-      float pk[32];
-#pragma unroll
-      for (int p = 0; p < 2; ++p) {
+      float pk[16];
+      {
+        const int p = wg;   // tokens 32 p .. 32 p + 31
         float y[32], u[32];
         tmem_ld32(tb + loff + C_Y + 32 * p, y);
         tmem_ld32(tb + loff + C_U + 32 * p, u);
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
           const int j0 = 32 * p + 2 * jj;
-          pk[16 * p + jj] = __uint_as_float(
+          pk[jj] = __uint_as_float(
               tcg::pack2(fmaf(tcg::ex2g((gl - G[j0]) * tcg::kLog2eG), y[2 * jj], u[2 * jj]),
                          fmaf(tcg::ex2g((gl - G[j0 + 1]) * tcg::kLog2eG), y[2 * jj + 1], u[2 * jj + 1])));
         }
       }
-      tmem_st32(tb + loff + C_U, pk);
+      tc_fence_before();
+      __syncthreads();   // both groups have read their fp32 columns
+      tc_fence_after();
+      tcg::tmem_st16(tb + loff + C_U + 16 * wg, pk);
     }
     tc_fence_before();
     __syncthreads();
@@ -1943,17 +1966,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
     // the grad pass's bf16 tiles, staged for bulk copies: dX (rows = the chunk's tokens, 64 v
     // per 128-byte row in two 8 KB halves) and dS, the gradient of the chunk's exit state (rows d,
     // two 16 KB halves), both 128-byte swizzled
-    stage_tile(tb, loff, C_X, 2, sb + OFF_STG_X, 8192, warp, lane);
-    stage_tile(tb, loff, C_S, 4, sb + OFF_STG_S, 16384, warp, lane);
+    stage_tile(tb, loff, C_X, wg, 1, sb + OFF_STG_X, 8192, wq, lane);
+    stage_tile(tb, loff, C_S, 2 * wg, 2, sb + OFF_STG_S, 16384, wq, lane);
     fence_proxy_async_smem();
     {  // dv = beta dX, the row dots dX_i . v_i (v from the stage's tile); bf16
        // dX^T diag(-gamma beta) in C_X, the A operand of the dS update
       const float* fgv = reinterpret_cast<const float*>(sm + OFF_FG);
       const uint8_t* vcol = st + ST_V + (v >> 6) * 8192 + (v & 7) * 2;
       const uint32_t sxv = (uint32_t)((v & 63) >> 3);   // this lane's 16-byte group before the swizzle
-      float pk[32];
-#pragma unroll
-      for (int p = 0; p < 2; ++p) {
+      float pk[16];
+      {
+        const int p = wg;
         float x[32], pv[32];
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
@@ -1972,16 +1995,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
           const int i = 32 * p + 2 * jj;
-          pk[16 * p + jj] = __uint_as_float(tcg::pack2(x[2 * jj] * fgv[i], x[2 * jj + 1] * fgv[i + 1]));
+          pk[jj] = __uint_as_float(tcg::pack2(x[2 * jj] * fgv[i], x[2 * jj + 1] * fgv[i + 1]));
         }
-        red[warp * 64 + 32 * p + lane] = lane_transpose_sum(pv, lane);
+        red[wq * 64 + 32 * p + lane] = lane_transpose_sum(pv, lane);
       }
-      tmem_st32(tb + loff + C_X, pk);
+      tc_fence_before();
+      __syncthreads();   // both groups have read their fp32 columns
+      tc_fence_after();
+      tcg::tmem_st16(tb + loff + C_X + 16 * wg, pk);
     }
     {  // dS^T <- gamma_L dS^T
       const float gL = expf(G[L - 1]);
 #pragma unroll
-      for (int part = 0; part < 4; ++part) {
+      for (int part = 2 * wg; part < 2 * wg + 2; ++part) {
         float x[32];
         tmem_ld32(tb + loff + C_S + 32 * part, x);
 #pragma unroll
@@ -2026,7 +2052,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
                   reinterpret_cast<const uint8_t*>(ws.T + ((size_t)(first + qc - 2) * Hv + h) * 64 * 64),
                   bos + (qc - 2) * C, hq, h);
     }
-    pack_state(tb, loff);
+    pack_state(tb, loff, wg);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -2036,7 +2062,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
     if (tid == 0) report(a.dev_status, GDN_DEV_TIMEOUT);
   } else if (b.d_initial) {
 #pragma unroll
-    for (int part = 0; part < 4; ++part) {
+    for (int part = 2 * wg; part < 2 * wg + 2; ++part) {
       float x[32];
       tmem_ld32(tb + loff + C_S + 32 * part, x);
 #pragma unroll

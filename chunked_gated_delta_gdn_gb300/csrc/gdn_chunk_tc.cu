@@ -108,14 +108,14 @@ static_assert(OFF_P + 2 * 8192 <= OFF_REC && OFF_REC + 16384 <= OFF_TW, "record 
 
 // Stage timestamps for the per-chunk cycle budget (a diagnostic build, -DGDN_CHUNK_STAMPS):
 // the leader of each group records clock64 at the stage boundaries of chunks 32 .. 95 in the
-// first and the last CTA of a forward-mode launch (gdn_chunk_stamps_read copies them out).
+// first and the last CTA of a launch, in either mode (gdn_chunk_stamps_read copies them out).
 // Without the define the stamps compile to nothing.
 #ifdef GDN_CHUNK_STAMPS
 __device__ unsigned long long g_chunk_stamps[2][2][64][16];
 #define GDN_STAMP(grp, p)                                                                       \
   do {                                                                                          \
     const int stamp_cta_ = blockIdx.x == 0 ? 0 : (blockIdx.x == gridDim.x - 1 ? 1 : -1);        \
-    if (!kRecord && leader && stamp_cta_ >= 0 && c >= 32 && c < 96)                             \
+    if (leader && stamp_cta_ >= 0 && c >= 32 && c < 96)                                         \
       g_chunk_stamps[stamp_cta_][grp][c - 32][p] = clock64();                                   \
   } while (0)
 #else

@@ -1,6 +1,11 @@
-"""Per-chunk cycle budget of the fused chunk kernel's forward mode, from stage timestamps.
+"""Per-chunk cycle budget of the fused chunk kernel, from stage timestamps.
 
-    python -m chunked_gated_delta_gdn_gb300.microbench.chunk_stage_budget [--B 4] [--T 8192]
+    python -m chunked_gated_delta_gdn_gb300.microbench.chunk_stage_budget [--B 4] [--T 8192] [--record]
+
+With --record the kernel runs in record mode, as the first launch of the backward (gdn_chunk_bwd):
+the state group then also stages the entry state and U' of every chunk as bf16 tiles for the
+backward's later kernels, inside its "S -> bf16" and "U' -> bf16" rows, and waits at the top of
+each chunk until the previous chunk's tiles have left shared memory.
 
 Builds the ``stamps`` variant of the library (the same sources with -DGDN_CHUNK_STAMPS: the
 leader of each warp group records clock64 at its stage boundaries for chunks 32 .. 95 of the
@@ -30,13 +35,18 @@ STATE = ["loop top", "wait: chunk ready (prep)", "U issue (4 MMAs)", "S -> bf16 
          "wait: O2, S^T done", "output epilogue"]
 
 
-def run(B: int, T: int, reps: int = 3):
+def run(B: int, T: int, reps: int = 3, record: bool = False):
     path = build.build(variant="stamps")
     lib = ctypes.CDLL(path)
     vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.gdn_chunk_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp, i, vp,
                                   i, vp, i, vp, i, vp, vp, sz, vp, vp]
     lib.gdn_chunk_fwd.restype = i
+    lib.gdn_chunk_bwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp, i, vp, i,
+                                  vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
+    lib.gdn_chunk_bwd.restype = i
+    lib.gdn_chunk_bwd_workspace_size.argtypes = [i, i, i, i, i, i, i, i, i]
+    lib.gdn_chunk_bwd_workspace_size.restype = sz
     lib.gdn_chunk_stamps_read.argtypes = [vp]
     lib.gdn_chunk_stamps_read.restype = i
     inp = synthetic.workload("long_context_bf16", B=B, T=T)
@@ -48,12 +58,27 @@ def run(B: int, T: int, reps: int = 3):
     o = torch.empty_like(d["v"])
     fin = torch.empty(B, Hv, K, V, device=dev)
     stream = torch.cuda.current_stream(dev).cuda_stream
+    if record:
+        d_o = torch.randn_like(d["v"], dtype=torch.float32).to(d["v"].dtype)
+        grads = [torch.empty_like(d[x]) for x in ("q", "k", "v")]
+        dg = torch.empty(B, T, Hv, device=dev)
+        db = torch.empty(B, T, Hv, device=dev)
+        need = lib.gdn_chunk_bwd_workspace_size(B, T, Hqk, Hv, K, V, B, 1, 1)
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
     for _ in range(reps):
-        st = lib.gdn_chunk_fwd(d["q"].data_ptr(), d["k"].data_ptr(), d["v"].data_ptr(),
-                               d["g"].data_ptr(), d["beta"].data_ptr(), B, T, Hqk, Hv, K, V, 1, 1,
-                               float("nan"), 64, None if init is None else init.data_ptr(), 1,
-                               fin.data_ptr(),
-                               1, None, B, None, 0, o.data_ptr(), None, 0, None, stream)
+        if record:
+            st = lib.gdn_chunk_bwd(d["q"].data_ptr(), d["k"].data_ptr(), d["v"].data_ptr(),
+                                   d["g"].data_ptr(), d["beta"].data_ptr(), B, T, Hqk, Hv, K, V, 1,
+                                   1, float("nan"), 64, None if init is None else init.data_ptr(),
+                                   1, None, B, d_o.data_ptr(), None, grads[0].data_ptr(),
+                                   grads[1].data_ptr(), grads[2].data_ptr(), dg.data_ptr(),
+                                   db.data_ptr(), None, ws.data_ptr(), need, None, stream)
+        else:
+            st = lib.gdn_chunk_fwd(d["q"].data_ptr(), d["k"].data_ptr(), d["v"].data_ptr(),
+                                   d["g"].data_ptr(), d["beta"].data_ptr(), B, T, Hqk, Hv, K, V, 1,
+                                   1, float("nan"), 64, None if init is None else init.data_ptr(), 1,
+                                   fin.data_ptr(), 1, None, B, None, 0, o.data_ptr(), None, 0, None,
+                                   stream)
         assert st == 0, st
     torch.cuda.synchronize(dev)
     buf = np.zeros((2, 2, 64, 16), dtype=np.uint64)
@@ -74,11 +99,13 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--B", type=int, default=4)
     ap.add_argument("--T", type=int, default=8192)
+    ap.add_argument("--record", action="store_true")
     args = ap.parse_args()
     assert args.T >= 96 * 64, "stamps cover chunks 32 .. 95"
-    buf = run(args.B, args.T)
+    buf = run(args.B, args.T, record=args.record)
+    mode = "record mode (the backward's forward recompute)" if args.record else "forward mode"
     for cta, label in ((0, "first CTA"), (1, "last CTA")):
-        print("\n### %s (B=%d, T=%d, chunks 32-95, median cycles)\n" % (label, args.B, args.T))
+        print("\n### %s, %s (B=%d, T=%d, chunks 32-95, median cycles)\n" % (mode, label, args.B, args.T))
         for grp, (gname, names) in enumerate((("prep group (warps 0-7)", PREP),
                                               ("state group (warps 8-11)", STATE))):
             rows, period = budget(buf[cta, grp], names)
