@@ -1064,7 +1064,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(const ChunkArg
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + OFF_BAR + 8);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 16);
-  const int c = blockIdx.x, h = blockIdx.y;
+  // one CTA per (chunk, value head), heads fastest: the CTAs running together read the
+  // same tokens (adjacent rows), and the two value heads of a query/key head share its
+  // q, k rows through L2
+  const int h = (int)(blockIdx.x % (unsigned)a.Hv), c = (int)(blockIdx.x / (unsigned)a.Hv);
   int n, t0, L;
   if (!locate_chunk(a, ws.chunk_off, c, &n, &t0, &L)) return;
   const int Hv = a.Hv, hq = h / (Hv / a.Hqk);
@@ -1559,7 +1562,10 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(const ChunkArg
   float* bt = G + 64;
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 8);
-  const int c = blockIdx.x, h = blockIdx.y;
+  // one CTA per (chunk, value head), heads fastest: the CTAs running together read the
+  // same tokens (adjacent rows), and the two value heads of a query/key head share its
+  // q, k rows through L2
+  const int h = (int)(blockIdx.x % (unsigned)a.Hv), c = (int)(blockIdx.x / (unsigned)a.Hv);
   int n, t0, L;
   if (!locate_chunk(a, ws.chunk_off, c, &n, &t0, &L)) return;
   const int Hv = a.Hv, hq = h / (Hv / a.Hqk);
@@ -2181,9 +2187,10 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
     if ((err = launch_chunk_prep(a, ws.chunk_off, ws.W, ws.U, ws.G))) return err;
     if ((err = launch_chunk_states(a, ws.chunk_off, ws.W, ws.U, ws.G, ws.S))) return err;
   }
+  if (tc && NC * a.Hv > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   if (NC > 0) {
     if (tc)
-      tcp::bwd_prep_tc_kernel<<<dim3((unsigned)NC, a.Hv), tcp::kThreads, tcp::SMEM, a.stream>>>(a, b, ws);
+      tcp::bwd_prep_tc_kernel<<<(unsigned)(NC * a.Hv), tcp::kThreads, tcp::SMEM, a.stream>>>(a, b, ws);
     else
       bwd_prep_kernel<<<dim3((unsigned)NC, a.Hv), kPrepThreads, kPrepSmem, a.stream>>>(a, b, ws);
     if ((err = cudaGetLastError())) return err;
@@ -2211,7 +2218,7 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
   }
   if (NC > 0) {
     if (tc) {
-      tcg::bwd_grad_tc_kernel<<<dim3((unsigned)NC, a.Hv), tcg::kThreads, tcg::SMEM, a.stream>>>(a, b, ws);
+      tcg::bwd_grad_tc_kernel<<<(unsigned)(NC * a.Hv), tcg::kThreads, tcg::SMEM, a.stream>>>(a, b, ws);
     } else {
       bwd_grad_kernel<<<dim3((unsigned)NC, a.Hv), kGradThreads, kGradSmem, a.stream>>>(a, b, ws);
     }
