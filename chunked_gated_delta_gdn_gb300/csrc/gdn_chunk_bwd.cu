@@ -1051,8 +1051,9 @@ __device__ __forceinline__ uint64_t mndesc(uint32_t addr, uint32_t lbo) {
   return sdesc_sw128(addr, lbo, 1024);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(const ChunkArgs a, const BwdArgs b,
-                                                                  BwdWs ws) {
+__global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
+    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+    const __grid_constant__ CUtensorMap tmO, const ChunkArgs a, const BwdArgs b, BwdWs ws) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(sm);
@@ -1084,49 +1085,27 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(const ChunkArg
     const uint8_t* ds = reinterpret_cast<const uint8_t*>(ws.dS + ch * ws.sdS);
     const uint8_t* ug = reinterpret_cast<const uint8_t*>(ws.U + ch * ws.sU);
     const uint8_t* xg = reinterpret_cast<const uint8_t*>(ws.dX + ch * ws.sdX);
-    mbar_arrive_expect_tx(bar_ld, 32768 + 32768 + 16384 + 16384);
+    mbar_arrive_expect_tx(bar_ld, 32768 + 32768 + 16384 + 16384 + 3 * 16384);
     bulk_load(sm + OFF_S0, s0, 32768, bar_ld);
     bulk_load(sm + OFF_DS, ds, 32768, bar_ld);
     bulk_load(sm + OFF_U, ug, 16384, bar_ld);
     bulk_load(sm + OFF_OX + 8192, xg, 8192, bar_ld);
     bulk_load(sm + OFF_OX + 16384 + 8192, xg + 8192, 8192, bar_ld);
+    // the chunk's q, k rows into [q; k] and its dO rows into rows 0-63 of [dO; dX], by TMA
+    // (64 features x 64 tokens a box, zero past the last token; rows past the chunk end are
+    // cleared below)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      tma_load_3d(sm + OFF_QK + hh * 16384, &tmQ, bar_ld, 64 * hh, hq, t0);
+      tma_load_3d(sm + OFF_QK + hh * 16384 + 8192, &tmK, bar_ld, 64 * hh, hq, t0);
+      tma_load_3d(sm + OFF_OX + hh * 16384, &tmO, bar_ld, 64 * hh, h, t0);
+    }
   }
   if (warp == 0) {
     tmem_alloc(tslot, T_COLS);
     tmem_relinquish();
   }
-  // ---- operands to shared memory
-  // Every global load is issued before any of it is used: the q, k and dO rows of this
-  // thread in one batch, then the gates (warp 0) while they are in flight (issuing them one
-  // loop trip or one batch at a time would expose the memory latency once per trip).
-  {  // normalised [q; k] rows: warp w takes rows w + 8 s; dO rows i into rows 0-63 of [dO; dX]
-    float x[16][4], o4[8][4];
-#pragma unroll
-    for (int s = 0; s < 16; ++s) {
-      const int r = warp + 8 * s, i = r & 63;
-      x[s][0] = x[s][1] = x[s][2] = x[s][3] = 0.f;
-      if (i < L) load4b(r < 64 ? a.q : a.k, ((size_t)(t0 + i) * a.Hqk + hq) * 128 + 4 * lane, x[s]);
-    }
-#pragma unroll
-    for (int s8 = 0; s8 < 8; ++s8) {
-      const int i = warp + 8 * s8;
-      o4[s8][0] = o4[s8][1] = o4[s8][2] = o4[s8][3] = 0.f;
-      if (i < L) load4b(b.d_o, ((size_t)(t0 + i) * Hv + h) * 128 + 4 * lane, o4[s8]);
-    }
-    load_gates(a, t0, L, h, G, bt);
-#pragma unroll
-    for (int s = 0; s < 16; ++s) {
-      float rn = 1.f;
-      if (l2)
-        rn = 1.0f / sqrtf(warp_sum(x[s][0] * x[s][0] + x[s][1] * x[s][1] + x[s][2] * x[s][2] +
-                                   x[s][3] * x[s][3]) + kL2Eps);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) x[s][q] *= rn;
-      put4(sm + OFF_QK, 16384, warp + 8 * s, 4 * lane, x[s]);
-    }
-#pragma unroll
-    for (int s8 = 0; s8 < 8; ++s8) put4(sm + OFF_OX, 16384, warp + 8 * s8, 4 * lane, o4[s8]);
-  }
+  load_gates(a, t0, L, h, G, bt);
   if (tid < 64) {   // the row dots dX_i . v_i, from the reverse pass's per-slice partials
     const float* xp = ws.XV + ch * 4 * 64;
     xvr[tid] = (xp[tid] + xp[64 + tid]) + (xp[128 + tid] + xp[192 + tid]);
@@ -1151,6 +1130,33 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(const ChunkArg
   }
   tc_fence_after();
   const uint32_t tb = *tslot;
+  {  // [q; k] rows normalised in place (thread: one row half, 128 rows x 2 halves); rows past
+     // the chunk end cleared, in [q; k] and in the dO rows
+    const int r = tid >> 1, hh = tid & 1, i = r & 63;
+    uint8_t* rowp = sm + OFF_QK + hh * 16384 + r * 128;
+    float ss = 0.f;
+#pragma unroll
+    for (int c8 = 0; c8 < 8; ++c8) {
+      const uint4 u = *reinterpret_cast<const uint4*>(rowp + 16 * c8);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[q]));
+        ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+      }
+    }
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    const float rn = i < L ? (l2 ? 1.0f / sqrtf(ss + kL2Eps) : 1.f) : 0.f;
+#pragma unroll
+    for (int c8 = 0; c8 < 8; ++c8) scale8(rowp + 16 * c8, rn);
+    for (int e = tid; e < 2 * 64 * 8; e += kThreads) {
+      const int hf = e >> 9, ii = (e >> 3) & 63, c8 = e & 7;
+      if (ii >= L)
+        *reinterpret_cast<uint4*>(sm + OFF_OX + hf * 16384 + ii * 128 + 16 * c8) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
   {  // <S0, dS> over the two tiles (same layout, element by element)
     float sd = 0.f;
     const uint4* p0 = reinterpret_cast<const uint4*>(sm + OFF_S0);
@@ -2218,7 +2224,14 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
   }
   if (NC > 0) {
     if (tc) {
-      tcg::bwd_grad_tc_kernel<<<(unsigned)(NC * a.Hv), tcg::kThreads, tcg::SMEM, a.stream>>>(a, b, ws);
+      CUtensorMap gq, gk, go;
+      memset(&gq, 0, sizeof(gq));
+      memset(&gk, 0, sizeof(gk));
+      memset(&go, 0, sizeof(go));
+      if (!encode_rows_map_bf16(&gq, a.q, a.Hqk, T_total) || !encode_rows_map_bf16(&gk, a.k, a.Hqk, T_total) ||
+          !encode_rows_map_bf16(&go, b.d_o, a.Hv, T_total))
+        return cudaErrorInvalidValue;
+      tcg::bwd_grad_tc_kernel<<<(unsigned)(NC * a.Hv), tcg::kThreads, tcg::SMEM, a.stream>>>(gq, gk, go, a, b, ws);
     } else {
       bwd_grad_kernel<<<dim3((unsigned)NC, a.Hv), kGradThreads, kGradSmem, a.stream>>>(a, b, ws);
     }
