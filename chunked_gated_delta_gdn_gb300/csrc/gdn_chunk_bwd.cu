@@ -1557,8 +1557,9 @@ __device__ void solve_T_tile(float* sA, float* sTd, uint8_t* tt) {
 }
 
 
-__global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(const ChunkArgs a, const BwdArgs b,
-                                                                  BwdWs ws) {
+__global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(
+    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK, const ChunkArgs a,
+    const BwdArgs b, BwdWs ws) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(sm);
@@ -1568,6 +1569,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(const ChunkArg
   float* bt = G + 64;
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 8);
+  uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + OFF_BAR + 16);
   // one CTA per (chunk, value head), heads fastest: the CTAs running together read the
   // same tokens (adjacent rows), and the two value heads of a query/key head share its
   // q, k rows through L2
@@ -1580,36 +1582,55 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(const ChunkArg
   const bool l2 = a.use_qk_l2norm != 0;
   if (tid == 0) {
     mbar_init(bar, 1);
+    mbar_init(bar_ld, 1);
     fence_mbar_init();
+    // the chunk's q, k rows into [q; k] by TMA (64 features x 64 tokens a box, zero past the
+    // last token; rows past the chunk end are cleared below)
+    mbar_arrive_expect_tx(bar_ld, 2 * 16384);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      tma_load_3d(sm + OFF_QK + hh * 16384, &tmQ, bar_ld, 64 * hh, hq, t0);
+      tma_load_3d(sm + OFF_QK + hh * 16384 + 8192, &tmK, bar_ld, 64 * hh, hq, t0);
+    }
   }
   if (warp == 0) {
     tmem_alloc(tslot, T_COLS);
     tmem_relinquish();
   }
-  {  // normalised [q; k] rows (bf16), every load of a thread issued first, then the gates
-     // (warp 0) while they are in flight
-    float x[16][4];
-#pragma unroll
-    for (int s = 0; s < 16; ++s) {
-      const int r = warp + 8 * s, i = r & 63;
-      x[s][0] = x[s][1] = x[s][2] = x[s][3] = 0.f;
-      if (i < L) load4b(r < 64 ? a.q : a.k, ((size_t)(t0 + i) * a.Hqk + hq) * 128 + 4 * lane, x[s]);
-    }
-    load_gates(a, t0, L, h, G, bt);
-#pragma unroll
-    for (int s = 0; s < 16; ++s) {
-      float rn = 1.f;
-      if (l2)
-        rn = 1.0f / sqrtf(warp_sum(x[s][0] * x[s][0] + x[s][1] * x[s][1] + x[s][2] * x[s][2] +
-                                   x[s][3] * x[s][3]) + kL2Eps);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) x[s][q] *= rn;
-      put4(sm + OFF_QK, 16384, warp + 8 * s, 4 * lane, x[s]);
-    }
-  }
+  load_gates(a, t0, L, h, G, bt);
   // the T tile starts from zero: the solve writes its lower triangle only
   for (int e = tid; e < 8192 / 16; e += kThreads)
     reinterpret_cast<uint4*>(sm + OFF_TT)[e] = make_uint4(0u, 0u, 0u, 0u);
+  bool ok = true;
+  if (tid == 0) ok = mbar_wait(bar_ld, 0, kWaitNs);   // the q, k tiles have landed
+  if (__syncthreads_or(!ok)) {
+    if (tid == 0) report(a.dev_status, GDN_DEV_TIMEOUT);
+    if (warp == 0) {
+      tc_fence_after();
+      tmem_dealloc(*tslot, T_COLS);
+    }
+    return;
+  }
+  {  // [q; k] rows normalised in place (thread: one row half, 128 rows x 2 halves), rows past
+     // the chunk end cleared
+    const int r = tid >> 1, hh = tid & 1, i = r & 63;
+    uint8_t* rowp = sm + OFF_QK + hh * 16384 + r * 128;
+    float ss = 0.f;
+#pragma unroll
+    for (int c8 = 0; c8 < 8; ++c8) {
+      const uint4 u = *reinterpret_cast<const uint4*>(rowp + 16 * c8);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[q]));
+        ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+      }
+    }
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    const float rn = i < L ? (l2 ? 1.0f / sqrtf(ss + kL2Eps) : 1.f) : 0.f;
+#pragma unroll
+    for (int c8 = 0; c8 < 8; ++c8) tcg::scale8(rowp + 16 * c8, rn);
+  }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -1624,7 +1645,6 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(const ChunkArg
     }
     mma_commit(bar);
   }
-  bool ok = true;
   if (tid == 0) ok = mbar_wait(bar, 0, kWaitNs);
   if (__syncthreads_or(!ok)) {
     if (tid == 0) report(a.dev_status, GDN_DEV_TIMEOUT);
@@ -2195,8 +2215,14 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
   }
   if (tc && NC * a.Hv > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   if (NC > 0) {
-    if (tc)
-      tcp::bwd_prep_tc_kernel<<<(unsigned)(NC * a.Hv), tcp::kThreads, tcp::SMEM, a.stream>>>(a, b, ws);
+    if (tc) {
+      CUtensorMap pq, pk;
+      memset(&pq, 0, sizeof(pq));
+      memset(&pk, 0, sizeof(pk));
+      if (!encode_rows_map_bf16(&pq, a.q, a.Hqk, T_total) || !encode_rows_map_bf16(&pk, a.k, a.Hqk, T_total))
+        return cudaErrorInvalidValue;
+      tcp::bwd_prep_tc_kernel<<<(unsigned)(NC * a.Hv), tcp::kThreads, tcp::SMEM, a.stream>>>(pq, pk, a, b, ws);
+    }
     else
       bwd_prep_kernel<<<dim3((unsigned)NC, a.Hv), kPrepThreads, kPrepSmem, a.stream>>>(a, b, ws);
     if ((err = cudaGetLastError())) return err;
