@@ -1157,6 +1157,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
   }
   fence_proxy_async_smem();
   __syncthreads();
+  // ---- R1, R2, R3 (issued first: the dot below runs meanwhile)
+  if (tid == 0) {
+    const uint32_t i1 = idesc_bf16(128, 256, false, true), i2 = idesc_bf16(128, 64, false, false);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
+      mma_bf16(tb + T_R1, kdesc(sb + OFF_QK + ko), mndesc(sb + OFF_S0 + ks * 2048, 16384), i1, ks > 0);
+      mma_bf16(tb + T_R2, kdesc(sb + OFF_OX + ko),
+               kdesc(sb + OFF_U + (ks >> 2) * 8192 + (ks & 3) * 32), i2, ks > 0);
+      mma_bf16(tb + T_R3, kdesc(sb + OFF_QK + ko), kdesc(sb + OFF_QK + 8192 + ko), i2, ks > 0);
+    }
+    mma_commit(bar);
+  }
   {  // <S0, dS> over the two tiles (same layout, element by element)
     float sd = 0.f;
     const uint4* p0 = reinterpret_cast<const uint4*>(sm + OFF_S0);
@@ -1173,19 +1186,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     }
     sd = warp_sum(sd);
     if (lane == 0) red[warp] = sd;
-  }
-  // ---- R1, R2, R3
-  if (tid == 0) {
-    const uint32_t i1 = idesc_bf16(128, 256, false, true), i2 = idesc_bf16(128, 64, false, false);
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
-      mma_bf16(tb + T_R1, kdesc(sb + OFF_QK + ko), mndesc(sb + OFF_S0 + ks * 2048, 16384), i1, ks > 0);
-      mma_bf16(tb + T_R2, kdesc(sb + OFF_OX + ko),
-               kdesc(sb + OFF_U + (ks >> 2) * 8192 + (ks & 3) * 32), i2, ks > 0);
-      mma_bf16(tb + T_R3, kdesc(sb + OFF_QK + ko), kdesc(sb + OFF_QK + 8192 + ko), i2, ks > 0);
-    }
-    mma_commit(bar);
   }
   if (tid < 64) {
     gm[tid] = expf(G[tid]);
@@ -1352,18 +1352,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     return;
   }
   tc_fence_after();
-  if (warp < 4) {   // [dQ; dK] rows to the per-value-head scratch
+  if (warp < 4) {   // [dQ; dK] rows to the per-value-head scratch: each thread stages its row in
+                    // the operand space the products no longer read (528-byte stride), then one
+                    // 512-byte bulk copy
     const int i = row & 63;
-    float* dst = (row < 64 ? ws.dQ : ws.dK) + ((size_t)(t0 + i) * Hv + h) * 128;
+    uint8_t* srow = sm + OFF_S0 + row * 528;
 #pragma unroll
     for (int part = 0; part < 4; ++part) {
       float x[32];
       tmem_ld32(tb + loff + T_R4 + 32 * part, x);
-      if (i < L) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          st4(dst + 32 * part + 4 * q, make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]));
-      }
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<float4*>(srow + 128 * part + 16 * q) =
+            make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+    }
+    if (i < L) {
+      fence_proxy_async_smem();
+      bulk_store((row < 64 ? ws.dQ : ws.dK) + ((size_t)(t0 + i) * Hv + h) * 128, srow, 512);
+      tma_store_commit();
     }
   }
   // ---- dG, dbeta per token, then dg by a suffix sum
@@ -1374,6 +1380,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     dGv[i] = i < L ? a.scale * gm[i] * qh1[i] - bt[i] * gm[i] * kh2[i] - omega + rz[i] - cs[i] : 0.f;
     if (i < L) b.dbeta[(size_t)(t0 + i) * Hv + h] = xvr[i] - gm[i] * kh2[i] + dba[i];
   }
+  if (warp < 4) tma_store_wait_all();   // the staged rows are written before the CTA exits
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
