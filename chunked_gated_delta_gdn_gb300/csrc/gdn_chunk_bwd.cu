@@ -1105,10 +1105,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     tmem_alloc(tslot, T_COLS);
     tmem_relinquish();
   }
-  load_gates(a, t0, L, h, G, bt);
-  if (tid < 64) {   // the row dots dX_i . v_i, from the reverse pass's per-slice partials
+  // the gates (warp 1) and the row dots (warps 2-3) load while warp 0 issues the copies
+  if (warp == 1) load_gates(a, t0, L, h, G, bt, lane);
+  if (tid >= 64 && tid < 128) {   // the row dots dX_i . v_i, from the reverse pass's per-slice partials
+    const int i = tid - 64;
     const float* xp = ws.XV + ch * 4 * 64;
-    xvr[tid] = (xp[tid] + xp[64 + tid]) + (xp[128 + tid] + xp[192 + tid]);
+    xvr[i] = (xp[i] + xp[64 + i]) + (xp[128 + i] + xp[192 + i]);
   }
   for (int e = tid; e < 8192 / 16; e += kThreads)      // the zero tile
     reinterpret_cast<uint4*>(sm + OFF_ZERO)[e] = make_uint4(0u, 0u, 0u, 0u);
@@ -1135,8 +1137,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     const int r = tid >> 1, hh = tid & 1, i = r & 63;
     uint8_t* rowp = sm + OFF_QK + hh * 16384 + r * 128;
     float ss = 0.f;
+    // 16-byte chunks in an order rotated by the row: the warp's accesses spread over the banks
 #pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8) {
+    for (int j = 0; j < 8; ++j) {
+      const int c8 = (j + r) & 7;
       const uint4 u = *reinterpret_cast<const uint4*>(rowp + 16 * c8);
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -1148,7 +1152,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     ss += __shfl_xor_sync(0xffffffffu, ss, 1);
     const float rn = i < L ? (l2 ? 1.0f / sqrtf(ss + kL2Eps) : 1.f) : 0.f;
 #pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8) scale8(rowp + 16 * c8, rn);
+    for (int j = 0; j < 8; ++j) scale8(rowp + 16 * ((j + r) & 7), rn);
     for (int e = tid; e < 2 * 64 * 8; e += kThreads) {
       const int hf = e >> 9, ii = (e >> 3) & 63, c8 = e & 7;
       if (ii >= L)
@@ -1623,8 +1627,10 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(
     const int r = tid >> 1, hh = tid & 1, i = r & 63;
     uint8_t* rowp = sm + OFF_QK + hh * 16384 + r * 128;
     float ss = 0.f;
+    // 16-byte chunks in an order rotated by the row: the warp's accesses spread over the banks
 #pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8) {
+    for (int j = 0; j < 8; ++j) {
+      const int c8 = (j + r) & 7;
       const uint4 u = *reinterpret_cast<const uint4*>(rowp + 16 * c8);
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -1636,7 +1642,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(
     ss += __shfl_xor_sync(0xffffffffu, ss, 1);
     const float rn = i < L ? (l2 ? 1.0f / sqrtf(ss + kL2Eps) : 1.f) : 0.f;
 #pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8) tcg::scale8(rowp + 16 * c8, rn);
+    for (int j = 0; j < 8; ++j) tcg::scale8(rowp + 16 * ((j + r) & 7), rn);
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -1909,8 +1915,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
       uint8_t* qrow = st + ST_Q + hh * 8192 + i * 128;
       uint8_t* krow = st + ST_K + hh * 8192 + i * 128;
       float sq = 0.f, sk = 0.f;
+      // the quarter's 16-byte chunks in an order rotated by the row (bank spread)
 #pragma unroll
-      for (int c8 = c0; c8 < c0 + 4; ++c8) {
+      for (int jj = 0; jj < 4; ++jj) {
+        const int c8 = c0 + ((jj + i) & 3);
         const uint4 uq = *reinterpret_cast<const uint4*>(qrow + 16 * c8);
         const uint4 uk = *reinterpret_cast<const uint4*>(krow + 16 * c8);
         const uint32_t wq[4] = {uq.x, uq.y, uq.z, uq.w}, wk[4] = {uk.x, uk.y, uk.z, uk.w};
@@ -1934,7 +1942,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
       // (the k rows already carry r_k)
       if (qq == 0) reinterpret_cast<float*>(sm + OFF_FG)[i] = i < L ? -gi * bt[i] : 0.f;
 #pragma unroll
-      for (int c8 = c0; c8 < c0 + 4; ++c8) {
+      for (int jj = 0; jj < 4; ++jj) {
+        const int c8 = c0 + ((jj + i) & 3);
         tcg::scale8(krow + 16 * c8, fk);
         tcg::scale8(qrow + 16 * c8, fq);
         if (i >= L)

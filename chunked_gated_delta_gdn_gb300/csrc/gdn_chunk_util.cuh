@@ -153,10 +153,9 @@ __device__ __forceinline__ void gate_values(const ChunkArgs& a, size_t i, int h,
 }
 
 // In-chunk inclusive cumsum of g (rows >= L get the last valid value) and beta
-// (zero for rows >= L).  Done by warp 0.
-__device__ void load_gates(const ChunkArgs& a, int t0, int L, int h, float* G, float* bt) {
-  if (threadIdx.x >= 32) return;
-  const int lane = threadIdx.x;
+// (zero for rows >= L).  Done by one whole warp (lane = its lane index).
+__device__ void load_gates(const ChunkArgs& a, int t0, int L, int h, float* G, float* bt,
+                           int lane) {
   float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
   if (lane < L) gate_values(a, (size_t)(t0 + lane) * a.Hv + h, h, &g0, &b0);
   if (lane + 32 < L) gate_values(a, (size_t)(t0 + lane + 32) * a.Hv + h, h, &g1, &b1);
@@ -171,6 +170,10 @@ __device__ void load_gates(const ChunkArgs& a, int t0, int L, int h, float* G, f
   G[lane + 32] = g1;
   bt[lane] = b0;
   bt[lane + 32] = b1;
+}
+// The same on warp 0 of the block (the other threads return at once).
+__device__ void load_gates(const ChunkArgs& a, int t0, int L, int h, float* G, float* bt) {
+  if (threadIdx.x < 32) load_gates(a, t0, L, h, G, bt, (int)threadIdx.x);
 }
 
 }  // namespace
