@@ -66,7 +66,7 @@ struct BwdWs {
   int32_t* chunk_off;  // [N + 2]
   float* W;            // [NC][Hv][C][K]          (fp32 path)
   float* U;            // [NC][Hv][C][V]  U, then U'
-  float* G;            // [NC][Hv][C]
+  float* G;            // [NC][Hv][C] (fp32 path); [NC][Hv][kRvFloats] (tensor-core path)
   float* S;            // [NC][Hv][K][V]  state at chunk entry
   float* T;            // [NC][Hv][C][C]
   float* dUp;          // [NC][Hv][C][V]  scale P^T dO   (fp32 path)
@@ -78,6 +78,16 @@ struct BwdWs {
   float* dK;           // [T_total][Hv][K]
   size_t sS, sdS, sU, sdX;   // slot strides (floats) per (chunk, head) of S, dS, U, dX
 };
+
+// The tensor-core path's per-(chunk, value head) vectors in the G slot, written by the prep
+// pass for the reverse pass (zero at tokens past the chunk end):
+//   [kRvCq + i]    scale gamma_i r_q,i      the q rows of the dS update
+//   [kRvW + j]     lambda_j r_k,j           the columns of Y^T = dS^T K^T over raw k rows
+//   [kRvF + i]     -gamma_i beta_i r_k,i    the dX^T operand of the dS update (raw k rows)
+//   [kRvBeta + i]  beta_i                   dv = diag(beta) dX
+//   [kRvGl]        gamma_L = e^{G_{L-1}}    the decay of dS across the chunk
+// with r_q, r_k the l2-norm reciprocals (1 without the norm) and lambda_j = e^{G_{L-1} - G_j}.
+constexpr int kRvCq = 0, kRvW = 64, kRvF = 128, kRvBeta = 192, kRvGl = 256, kRvFloats = 320;
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -98,7 +108,7 @@ __host__ __device__ inline BwdWs bwd_layout(void* base, long long NC, int N, int
   w.chunk_off = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (size_t)(N + 2)));
   w.W = tc ? nullptr : reinterpret_cast<float*>(take(f * ch * C * K));
   w.U = reinterpret_cast<float*>(take(f * ch * w.sU));
-  w.G = reinterpret_cast<float*>(take(f * ch * C));
+  w.G = reinterpret_cast<float*>(take(f * ch * (tc ? kRvFloats : C)));
   w.S = reinterpret_cast<float*>(take(f * ch * w.sS));
   w.T = reinterpret_cast<float*>(take(f * ch * C * C));
   w.dUp = tc ? nullptr : reinterpret_cast<float*>(take(f * ch * C * V));
@@ -1107,11 +1117,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
   }
   // the gates (warp 1) and the row dots (warps 2-3) load while warp 0 issues the copies
   if (warp == 1) load_gates(a, t0, L, h, G, bt, lane);
-  if (tid >= 64 && tid < 128) {   // the row dots dX_i . v_i, from the reverse pass's per-slice partials
-    const int i = tid - 64;
-    const float* xp = ws.XV + ch * 4 * 64;
-    xvr[i] = (xp[i] + xp[64 + i]) + (xp[128 + i] + xp[192 + i]);
-  }
+  if (tid >= 64 && tid < 128)   // the row dots dX_i . v_i of the reverse pass (slot 0)
+    xvr[tid - 64] = ws.XV[ch * 4 * 64 + tid - 64];
   for (int e = tid; e < 8192 / 16; e += kThreads)      // the zero tile
     reinterpret_cast<uint4*>(sm + OFF_ZERO)[e] = make_uint4(0u, 0u, 0u, 0u);
   for (int e = tid; e < 2 * 8192 / 16; e += kThreads) {   // rows 0-63 of both halves of [0; lambda U']
@@ -1424,8 +1431,8 @@ constexpr uint32_t OFF_P = 32768;      // P tile (bf16, scale folded)
 constexpr uint32_t OFF_TT = 40960;     // T tile (bf16)
 constexpr uint32_t OFF_A = 49152;      // A, fp32 [64][64], 16-byte-group swizzled (a_idx)
 constexpr uint32_t OFF_TD = OFF_A + 64 * 64 * 4;
-constexpr uint32_t OFF_VEC = OFF_TD + 4 * 16 * TD_LD * 4;
-constexpr uint32_t OFF_BAR = OFF_VEC + 2 * 64 * 4;
+constexpr uint32_t OFF_VEC = OFF_TD + 4 * 16 * TD_LD * 4;   // G[64], beta[64], row norms [128]
+constexpr uint32_t OFF_BAR = OFF_VEC + 4 * 64 * 4;
 constexpr uint32_t SMEM = OFF_BAR + 64 + 1024;
 constexpr uint32_t T_COLS = 64;
 
@@ -1578,6 +1585,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(
   float* sTd = reinterpret_cast<float*>(sm + OFF_TD);
   float* G = reinterpret_cast<float*>(sm + OFF_VEC);
   float* bt = G + 64;
+  float* rnv = G + 128;   // r_q (rows 0-63), r_k (rows 64-127); zero past the chunk end
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 8);
   uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + OFF_BAR + 16);
@@ -1641,6 +1649,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(
     }
     ss += __shfl_xor_sync(0xffffffffu, ss, 1);
     const float rn = i < L ? (l2 ? 1.0f / sqrtf(ss + kL2Eps) : 1.f) : 0.f;
+    if (hh == 0) rnv[r] = rn;
 #pragma unroll
     for (int j = 0; j < 8; ++j) tcg::scale8(rowp + 16 * ((j + r) & 7), rn);
   }
@@ -1717,57 +1726,78 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(
     dst[e] = srcT[e];
     dst[8192 / 16 + e] = srcP[e];
   }
-  if (tid < 64) ws.G[ch * 64 + tid] = G[tid];
+  if (tid < 64) {   // the reverse pass's per-token vectors (zero past the chunk end)
+    const int i = tid;
+    const bool in = i < L;
+    const float gi = expf(G[i]), rq = rnv[i], rk = rnv[64 + i];
+    float* rv = ws.G + ch * kRvFloats;
+    rv[kRvCq + i] = in ? a.scale * gi * rq : 0.f;
+    rv[kRvW + i] = in ? ex2((G[L - 1] - G[i]) * kLog2e) * rk : 0.f;
+    rv[kRvF + i] = in ? -gi * bt[i] * rk : 0.f;
+    rv[kRvBeta + i] = in ? bt[i] : 0.f;
+    if (i == 0) rv[kRvGl] = expf(G[L - 1]);
+  }
 }
 }  // namespace tcp
 
 // ---------------------------------------------------------------- 4b. reverse on the tensor cores
-// bf16 I/O with K = V = 128: one CTA (4 warps) per (sequence, value head), chunks last to
+// bf16 I/O with K = V = 128: one CTA (8 warps) per (sequence, value head), chunks last to
 // first, with dS^T (TMEM lane = value index v, column = key index d) resident in TMEM like the
-// forward's state.  Per chunk (tiles double-buffered one chunk ahead: q, k, v, dO by TMA, the
-// prep pass's T and P tiles by bulk copy):
-//   Y^T   = dS^T K^T                        M=128 N=64  K=128  (A: bf16 dS^T from TMEM)
+// forward's state.  Per chunk (tiles double-buffered one chunk ahead: q, k, v, dO by TMA; the
+// prep pass's T and P tiles and per-token vectors by bulk copy):
+//   Y^T   = dS^T K^T                        M=128 N=64  K=128  (A: bf16 dS^T from TMEM; raw k)
 //   dUp^T = dO^T P                          M=128 N=64  K=64   (P carries scale)
-//   dU'^T = dUp^T + Y^T diag(lambda)        -> bf16 into TMEM
+//   dU'^T = dUp^T + Y^T diag(lambda r_k)    -> bf16 into TMEM
 //   dX^T  = dU'^T T                         M=128 N=64  K=64
-//   dS^T <- gamma_L dS^T + dO^T (scale diag(gamma) Q) + (dX^T diag(-gamma beta)) K
+//   dS^T <- gamma_L dS^T + dO^T (scale diag(gamma r_q) Q) + (dX^T diag(-gamma beta r_k)) K
 //                                           M=128 N=128 K=64 + 64
-// with the normalised q and k rows scaled in shared memory and -gamma beta folded into the bf16
-// dX^T operand.  It writes, per chunk, the bf16 dS (the gradient of the chunk's exit state) and
-// dX tiles of the grad pass (staged in shared memory, bulk copies), dv = diag(beta) dX, and the
-// row dots dX_i . v_i (slot 0 of ws.XV, slots 1-3 zero).
+// The l2-norm reciprocals r_q, r_k and the gates enter as per-token fp32 factors: the k rows
+// stay raw, the q rows are scaled in shared memory while the first products run, and
+// -gamma beta r_k is folded into the bf16 dX^T operand.  It writes, per chunk, the bf16 dS (the
+// gradient of the chunk's exit state) and dX tiles of the grad pass (staged in shared memory,
+// bulk copies), dv = diag(beta) dX (staged over the v tile, TMA store) and the row dots
+// dX_i . v_i (slot 0 of ws.XV).
 namespace tcr {
 using namespace sm100;
 constexpr int kThreads = 256;    // two warps per TMEM lane quarter
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t ST_Q = 0, ST_K = 16384, ST_V = 32768, ST_DO = 49152, ST_T = 65536, ST_P = 73728;
-constexpr uint32_t STAGE = 81920;
-constexpr uint32_t STAGE_TX = 4 * 16384 + 2 * 8192;
-constexpr uint32_t OFF_VEC = 2 * STAGE;              // per stage: G[64], beta[64]
-constexpr uint32_t OFF_RED = OFF_VEC + 2 * 128 * 4;  // [4 lane quarters][64]
+constexpr uint32_t ST_VEC = 81920;                        // the prep pass's per-token vectors
+constexpr uint32_t VEC_BYTES = kRvFloats * 4;
+constexpr uint32_t STAGE = (ST_VEC + VEC_BYTES + 1023) / 1024 * 1024;
+constexpr uint32_t STAGE_TX = 4 * 16384 + 16384 + VEC_BYTES;
+constexpr uint32_t OFF_RED = 2 * STAGE;              // [4 lane quarters][64]
 constexpr uint32_t OFF_BAR = OFF_RED + 4 * 64 * 4;
-constexpr uint32_t OFF_FG = OFF_BAR + 64;                             // -gamma beta per token
-constexpr uint32_t OFF_STG_S = (OFF_FG + 256 + 1023) / 1024 * 1024;   // staging: the dS tile (32 KB)
+constexpr uint32_t OFF_STG_S = (OFF_BAR + 64 + 1023) / 1024 * 1024;   // staging: the dS tile (32 KB)
 constexpr uint32_t OFF_STG_X = OFF_STG_S + 32768;                     // and the dX tile (16 KB)
 constexpr uint32_t SMEM = OFF_STG_X + 16384 + 1024;
 static_assert(SMEM <= 232448, "shared memory budget");
+static_assert(ST_P == ST_T + 8192, "T and P arrive by one bulk copy");
 constexpr uint32_t C_S = 0, C_SB = 128, C_Y = 192, C_U = 256, C_X = 320, T_COLS = 512;
 
-// Stage passes pass0 .. pass0 + npass - 1 of 32 TMEM columns from `col` (fp32, lane = v) as bf16 rows of a
-// 128-byte-swizzled tile at shared address `tile`: TMEM column j of lane v goes to row j,
-// element v of a 64-element half (halves `half` bytes apart).  16x256b loads hand each thread
-// the fragment of stmatrix .trans (rows j, 2 (t % 4) and + 1 of each 8-column group; v = t / 4
-// and t / 4 + 8 of each 16-lane half), which writes the 8 x 8 blocks transposed.
-__device__ __forceinline__ void stage_tile(uint32_t tb, uint32_t loff, uint32_t col, int pass0,
-                                           int npass, uint32_t tile, uint32_t half, int wq, int lane) {
+// Shared-memory offset, within a 128-byte-swizzled tile of 64-element halves `half` bytes
+// apart, of the 8 x 8 block that lane `lane` of warp quarter wq addresses for stmatrix /
+// ldmatrix .trans in column group 0: matrix i = lane / 8 covers elements 32 wq + 8 i .. + 7 of
+// rows r = lane % 8 (add 1024 per further group of 8 rows).
+__device__ __forceinline__ uint32_t frag_off(int wq, int lane, uint32_t half) {
   const int mblk = lane >> 3, rr = lane & 7;
   const int d0 = 32 * wq + 8 * mblk;
-  const uint32_t st_base = tile + (d0 >> 6) * half + rr * 128 + ((((d0 & 63) >> 3) ^ rr) << 4);
+  return (d0 >> 6) * half + rr * 128 + ((((d0 & 63) >> 3) ^ rr) << 4);
+}
+
+// dS^T (fp32, C_S; lane = v, column = d) as the bf16 rows d of the grad pass's dS tile (two
+// 16 KB halves), then scaled in TMEM by gamma_L.  Passes 2 p, 2 p + 1 of 32 columns (p = warp
+// group).  16x256b loads hand each thread the fragment of stmatrix .trans (columns j, 2 (t%4)
+// and + 1 of each 8-column group; v = t / 4 and t / 4 + 8 of each 16-lane half), which writes
+// the 8 x 8 blocks transposed.
+__device__ __forceinline__ void stage_state(uint32_t tb, uint32_t loff, int p, uint32_t tile,
+                                            float gl, int wq, int lane) {
+  const uint32_t st_base = tile + frag_off(wq, lane, 16384);
 #pragma unroll 1
-  for (int pass = pass0; pass < pass0 + npass; ++pass) {
+  for (int pass = 2 * p; pass < 2 * p + 2; ++pass) {
     uint32_t a0[16], a1[16];
-    tmem_ld16x256b_x4(tb + loff + col + 32 * pass, a0);                 // v 0-15 of the warp
-    tmem_ld16x256b_x4(tb + loff + (16u << 16) + col + 32 * pass, a1);   // v 16-31
+    tmem_ld16x256b_x4(tb + loff + C_S + 32 * pass, a0);                 // v 0-15 of the warp
+    tmem_ld16x256b_x4(tb + loff + (16u << 16) + C_S + 32 * pass, a1);   // v 16-31
     tmem_wait_ld();
 #pragma unroll
     for (int j = 0; j < 4; ++j) {   // column group 4 pass + j
@@ -1780,13 +1810,75 @@ __device__ __forceinline__ void stage_tile(uint32_t tb, uint32_t loff, uint32_t 
       }
       stmatrix_x4_trans(st_base + (4 * pass + j) * 1024, f);
     }
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      a0[e] = __float_as_uint(gl * __uint_as_float(a0[e]));
+      a1[e] = __float_as_uint(gl * __uint_as_float(a1[e]));
+    }
+    tmem_st16x256b_x4(tb + loff + C_S + 32 * pass, a0);
+    tmem_st16x256b_x4(tb + loff + (16u << 16) + C_S + 32 * pass, a1);
   }
+  tmem_wait_st();
+}
+
+// dX^T (fp32, C_X; column = token) for tokens 32 p .. 32 p + 31 (p = warp group): the bf16 dX
+// rows of the grad pass's tile at `xtile`, dv = beta_i dX_i written over the v rows at `vtile`
+// (the same fragment positions, read first), and the row dots dX_i . v_i over this warp's 32 v
+// into red[wq][i].
+__device__ __forceinline__ void stage_dx(uint32_t tb, uint32_t loff, int p, uint32_t xtile,
+                                         uint32_t vtile, const float* beta, float* red, int wq,
+                                         int lane) {
+  const uint32_t off = frag_off(wq, lane, 8192);
+  uint32_t a0[16], a1[16];
+  tmem_ld16x256b_x4(tb + loff + C_X + 32 * p, a0);
+  tmem_ld16x256b_x4(tb + loff + (16u << 16) + C_X + 32 * p, a1);
+  tmem_wait_ld();
+  const int tq = 2 * (lane & 3);
+  float dot[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {   // column group 4 p + j: this thread's tokens i0, i0 + 1
+    const int i0 = 32 * p + 8 * j + tq;
+    const float b0 = beta[i0], b1 = beta[i0 + 1];
+    const uint32_t blk = (4 * p + j) * 1024 + off;
+    uint32_t vv[4], fx[4], fv[4];
+    ldmatrix_x4_trans(vtile + blk, vv);
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int mm = 0; mm < 4; ++mm) {
+      const uint32_t* x = (mm >> 1) ? a1 : a0;
+      const int k = 4 * j + 2 * (mm & 1);
+      const float x0 = __uint_as_float(x[k]), x1 = __uint_as_float(x[k + 1]);
+      const float2 vf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vv[mm]));
+      fx[mm] = tcg::pack2(x0, x1);
+      fv[mm] = tcg::pack2(b0 * x0, b1 * x1);
+      s0 = fmaf(x0, vf.x, s0);
+      s1 = fmaf(x1, vf.y, s1);
+    }
+    stmatrix_x4_trans(xtile + blk, fx);
+    stmatrix_x4_trans(vtile + blk, fv);
+    dot[2 * j] = s0;
+    dot[2 * j + 1] = s1;
+  }
+  // sum over the 8 lanes of equal lane % 4 (the warp's 32 v), as a transpose: lane l ends
+  // with the total of dot[l / 4]
+#pragma unroll
+  for (int o = 16, n = 4; o >= 4; o >>= 1, n >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int k = 0; k < n; ++k) {
+      const float send = up ? dot[k] : dot[k + n];
+      const float keep = up ? dot[k + n] : dot[k];
+      dot[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  const int idx = lane >> 2;
+  red[wq * 64 + 32 * p + 8 * (idx >> 1) + tq + (idx & 1)] = dot[0];
 }
 
 __device__ __forceinline__ void issue_stage(uint8_t* st, uint64_t* bar, const CUtensorMap* tq,
                                             const CUtensorMap* tk, const CUtensorMap* tv,
-                                            const CUtensorMap* to, const uint8_t* tp, int t,
-                                            int hq, int h) {
+                                            const CUtensorMap* to, const uint8_t* tp,
+                                            const float* rv, int t, int hq, int h) {
   mbar_arrive_expect_tx(bar, STAGE_TX);
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
@@ -1795,8 +1887,8 @@ __device__ __forceinline__ void issue_stage(uint8_t* st, uint64_t* bar, const CU
     tma_load_3d(st + ST_V + hh * 8192, tv, bar, 64 * hh, h, t);
     tma_load_3d(st + ST_DO + hh * 8192, to, bar, 64 * hh, h, t);
   }
-  bulk_load(st + ST_T, tp, 8192, bar);
-  bulk_load(st + ST_P, tp + 8192, 8192, bar);
+  bulk_load(st + ST_T, tp, 16384, bar);
+  bulk_load(st + ST_VEC, rv, VEC_BYTES, bar);
 }
 
 // dS^T (fp32, C_S) -> bf16 pairs in C_SB, the A operand of the next Y product: columns
@@ -1815,25 +1907,10 @@ __device__ __forceinline__ void pack_state(uint32_t tb, uint32_t loff, int p2) {
   }
 }
 
-// Sum over the 32 lanes of each of v[0..31]: lane l ends with the total of v[l] (31 shuffles).
-__device__ __forceinline__ float lane_transpose_sum(float (&v)[32], int lane) {
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    const bool up = (lane & o) != 0;
-#pragma unroll
-    for (int k = 0; k < o; ++k) {
-      const float send = up ? v[k] : v[k + o];
-      const float keep = up ? v[k + o] : v[k];
-      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-    }
-  }
-  return v[0];
-}
-
 __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-    const ChunkArgs a, const BwdArgs b, BwdWs ws) {
+    const __grid_constant__ CUtensorMap tmDV, const ChunkArgs a, const BwdArgs b, BwdWs ws) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(sm);
@@ -1857,6 +1934,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
   const int first = ws.chunk_off[n];
   const int nch = (eos - bos + C - 1) / C;
   const uint32_t loff = (uint32_t)(32 * wq) << 16;
+  // the tiles of iteration it (chunk nch - 1 - it) into stage it % 2
+  auto issue = [&](int it) {
+    const int qc = nch - 1 - it;
+    const size_t ch = (size_t)(first + qc) * Hv + h;
+    issue_stage(sm + (it & 1) * STAGE, &full[it & 1], &tmQ, &tmK, &tmV, &tmO,
+                reinterpret_cast<const uint8_t*>(ws.T + ch * 64 * 64), ws.G + ch * kRvFloats,
+                bos + qc * C, hq, h);
+  };
   if (tid == 0) {
     mbar_init(&full[0], 1);
     mbar_init(&full[1], 1);
@@ -1866,13 +1951,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmO);
-    for (int it = 0; it < 2 && it < nch; ++it) {
-      const int qc = nch - 1 - it;
-      issue_stage(sm + it * STAGE, &full[it], &tmQ, &tmK, &tmV, &tmO,
-                  reinterpret_cast<const uint8_t*>(ws.T + ((size_t)(first + qc) * Hv + h) * 64 * 64),
-                  bos + qc * C, hq, h);
-    }
+    tma_prefetch_desc(&tmDV);
+    for (int it = 0; it < 2 && it < nch; ++it) issue(it);
   }
+  int issued = nch < 2 ? nch : 2;   // iterations whose tiles were requested (uniform)
   if (warp == 0) {
     tmem_alloc(tslot, T_COLS);
     tmem_relinquish();
@@ -1892,67 +1974,32 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
     }
     pack_state(tb, loff, wg);
   }
-  if (nch > 0) {   // the first chunk's gates
-    const int t1 = bos + (nch - 1) * C;
-    load_gates(a, t1, min(C, eos - t1), h, reinterpret_cast<float*>(sm + OFF_VEC),
-               reinterpret_cast<float*>(sm + OFF_VEC) + 64);
-  }
   uint32_t ph = 0;
   bool failed = false;
-  for (int it = 0; it < nch; ++it) {
+  int it = 0;
+  for (; it < nch; ++it) {
     const int qc = nch - 1 - it, s = it & 1;
     const int t0 = bos + qc * C, L = min(C, eos - t0);
     const size_t ch = (size_t)(first + qc) * Hv + h;
     uint8_t* st = sm + s * STAGE;
     const uint32_t sst = sb + s * STAGE;
-    float* G = reinterpret_cast<float*>(sm + OFF_VEC) + s * 128;   // loaded one chunk ahead
-    float* bt = G + 64;
+    const float* vec = reinterpret_cast<const float*>(st + ST_VEC);
     bool ok = true;
     if (tid == 0) ok = mbar_wait(&full[s], (uint32_t)(it >> 1) & 1u, kWaitNs);
     if (__syncthreads_or(!ok)) { failed = true; break; }
-    {  // norms; r_k k and scale gamma r_q q in place, -gamma beta per token; dO rows >= L zeroed
-      const int i = tid >> 2, qq = tid & 3, hh = qq >> 1, c0 = 4 * (qq & 1);   // a quarter row
-      uint8_t* qrow = st + ST_Q + hh * 8192 + i * 128;
-      uint8_t* krow = st + ST_K + hh * 8192 + i * 128;
-      float sq = 0.f, sk = 0.f;
-      // the quarter's 16-byte chunks in an order rotated by the row (bank spread)
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const int c8 = c0 + ((jj + i) & 3);
-        const uint4 uq = *reinterpret_cast<const uint4*>(qrow + 16 * c8);
-        const uint4 uk = *reinterpret_cast<const uint4*>(krow + 16 * c8);
-        const uint32_t wq[4] = {uq.x, uq.y, uq.z, uq.w}, wk[4] = {uk.x, uk.y, uk.z, uk.w};
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const float2 fq = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wq[w]));
-          const float2 fk = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wk[w]));
-          sq = fmaf(fq.x, fq.x, fmaf(fq.y, fq.y, sq));
-          sk = fmaf(fk.x, fk.x, fmaf(fk.y, fk.y, sk));
+    if (L < C) {   // the sequence's last chunk: rows past its end (the next sequence's) cleared
+      for (int e = tid; e < 2 * 64 * 8; e += kThreads) {
+        const int hh = e >> 9, i = (e >> 3) & 63, c8 = e & 7;
+        if (i >= L) {
+          const uint32_t o = hh * 8192 + i * 128 + 16 * c8;
+          *reinterpret_cast<uint4*>(st + ST_Q + o) = make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(st + ST_K + o) = make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(st + ST_DO + o) = make_uint4(0u, 0u, 0u, 0u);
         }
       }
-      sq += __shfl_xor_sync(0xffffffffu, sq, 1);
-      sk += __shfl_xor_sync(0xffffffffu, sk, 1);
-      sq += __shfl_xor_sync(0xffffffffu, sq, 2);
-      sk += __shfl_xor_sync(0xffffffffu, sk, 2);
-      const bool l2 = a.use_qk_l2norm != 0;
-      const float rq = l2 ? 1.0f / sqrtf(sq + kL2Eps) : 1.f, rk = l2 ? 1.0f / sqrtf(sk + kL2Eps) : 1.f;
-      const float gi = expf(G[i]);
-      const float fq = i < L ? a.scale * gi * rq : 0.f;
-      const float fk = i < L ? rk : 0.f;
-      // (the k rows already carry r_k)
-      if (qq == 0) reinterpret_cast<float*>(sm + OFF_FG)[i] = i < L ? -gi * bt[i] : 0.f;
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const int c8 = c0 + ((jj + i) & 3);
-        tcg::scale8(krow + 16 * c8, fk);
-        tcg::scale8(qrow + 16 * c8, fq);
-        if (i >= L)
-          *reinterpret_cast<uint4*>(st + ST_DO + hh * 8192 + i * 128 + 16 * c8) = make_uint4(0u, 0u, 0u, 0u);
-      }
+      fence_proxy_async_smem();
+      __syncthreads();
     }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
     tc_fence_after();
     if (tid == 0) {   // Y^T = dS^T K^T;  dUp^T = dO^T P
       const uint32_t iy = idesc_bf16(128, 64, false, false), iu = idesc_bf16(128, 64, true, true);
@@ -1965,18 +2012,26 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
         mma_bf16(tb + C_U, tcg::mndesc(sst + ST_DO + ks * 2048, 8192),
                  tcg::mndesc(sst + ST_P + ks * 2048, 8192), iu, ks > 0);
       mma_commit(mmab);
+    } else {
+      // while the products run: the next iteration's tiles into the other stage (its last
+      // reads, and the dv store out of it, finished before the previous iteration ended) and
+      // the q rows scaled by scale gamma_i r_q,i for the dS update
+      if (tid == kThreads - 32 && it >= 1 && it + 1 < nch) issue(it + 1);
+      if (warp > 0) {
+        for (int e = tid - 32; e < 64 * 16; e += kThreads - 32) {
+          const int i = e >> 4, hh = (e >> 3) & 1, c8 = e & 7;
+          tcg::scale8(st + ST_Q + hh * 8192 + i * 128 + 16 * c8, vec[kRvCq + i]);
+        }
+        fence_proxy_async_smem();
+      }
     }
-    if (it + 1 < nch) {   // the next chunk's gates into the other stage while the products run
-      const int t1 = bos + (qc - 1) * C;
-      float* G1 = reinterpret_cast<float*>(sm + OFF_VEC) + (s ^ 1) * 128;
-      load_gates(a, t1, min(C, eos - t1), h, G1, G1 + 64);
-    }
+    if (it >= 1 && it + 1 < nch) issued = it + 2;
     if (tid == 0) ok = mbar_wait(mmab, ph, kWaitNs);
     ph ^= 1u;
     if (__syncthreads_or(!ok)) { failed = true; break; }
     tc_fence_after();
-    {  // dU'^T = dUp^T + Y^T diag(lambda) -> bf16 pairs in C_U (lambda_j = 2^((G_L - G_j) log2 e))
-      const float gl = G[L - 1];
+    {  // dU'^T = dUp^T + Y^T diag(lambda r_k) -> bf16 pairs in C_U
+      const float* w = vec + kRvW;
       float pk[16];
       {
         const int p = wg;   // tokens 32 p .. 32 p + 31
@@ -1986,9 +2041,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
           const int j0 = 32 * p + 2 * jj;
-          pk[jj] = __uint_as_float(
-              tcg::pack2(fmaf(tcg::ex2g((gl - G[j0]) * tcg::kLog2eG), y[2 * jj], u[2 * jj]),
-                         fmaf(tcg::ex2g((gl - G[j0 + 1]) * tcg::kLog2eG), y[2 * jj + 1], u[2 * jj + 1])));
+          pk[jj] = __uint_as_float(tcg::pack2(fmaf(w[j0], y[2 * jj], u[2 * jj]),
+                                              fmaf(w[j0 + 1], y[2 * jj + 1], u[2 * jj + 1])));
         }
       }
       tc_fence_before();
@@ -2005,7 +2059,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
       for (int ks = 0; ks < 4; ++ks)
         mma_bf16_ta(tb + C_X, tb + C_U + 8 * ks, tcg::mndesc(sst + ST_T + ks * 2048, 8192), ix, ks > 0);
       mma_commit(mmab);
-      tma_store_wait_read();   // the previous chunk's dS and dX tiles have left the staging buffers
     }
     if (tid == 0) ok = mbar_wait(mmab, ph, kWaitNs);
     ph ^= 1u;
@@ -2013,55 +2066,27 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
     tc_fence_after();
     // the grad pass's bf16 tiles, staged for bulk copies: dX (rows = the chunk's tokens, 64 v
     // per 128-byte row in two 8 KB halves) and dS, the gradient of the chunk's exit state (rows d,
-    // two 16 KB halves), both 128-byte swizzled
-    stage_tile(tb, loff, C_X, wg, 1, sb + OFF_STG_X, 8192, wq, lane);
-    stage_tile(tb, loff, C_S, 2 * wg, 2, sb + OFF_STG_S, 16384, wq, lane);
+    // two 16 KB halves), both 128-byte swizzled; dv over the v tile; dS^T <- gamma_L dS^T
+    stage_dx(tb, loff, wg, sb + OFF_STG_X, sst + ST_V, vec + kRvBeta, red, wq, lane);
+    stage_state(tb, loff, wg, sb + OFF_STG_S, vec[kRvGl], wq, lane);
     fence_proxy_async_smem();
-    {  // dv = beta dX, the row dots dX_i . v_i (v from the stage's tile); bf16
-       // dX^T diag(-gamma beta) in C_X, the A operand of the dS update
-      const float* fgv = reinterpret_cast<const float*>(sm + OFF_FG);
-      const uint8_t* vcol = st + ST_V + (v >> 6) * 8192 + (v & 7) * 2;
-      const uint32_t sxv = (uint32_t)((v & 63) >> 3);   // this lane's 16-byte group before the swizzle
+    {  // bf16 dX^T diag(-gamma beta r_k) in C_X, the A operand of the dS update
+      const float* fv = vec + kRvF;
       float pk[16];
       {
         const int p = wg;
-        float x[32], pv[32];
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int i = 32 * p + jj;
-          pv[jj] = i < L ? __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
-                               vcol + i * 128 + ((sxv ^ (i & 7)) << 4)))
-                         : 0.f;
-        }
+        float x[32];
         tmem_ld32(tb + loff + C_X + 32 * p, x);
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int i = 32 * p + jj;
-          pv[jj] *= x[jj];
-          if (i < L) store_elem(b.dv, ((size_t)(t0 + i) * Hv + h) * 128 + v, bt[i] * x[jj], a.io_dtype);
-        }
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
           const int i = 32 * p + 2 * jj;
-          pk[jj] = __uint_as_float(tcg::pack2(x[2 * jj] * fgv[i], x[2 * jj + 1] * fgv[i + 1]));
+          pk[jj] = __uint_as_float(tcg::pack2(x[2 * jj] * fv[i], x[2 * jj + 1] * fv[i + 1]));
         }
-        red[wq * 64 + 32 * p + lane] = lane_transpose_sum(pv, lane);
       }
       tc_fence_before();
       __syncthreads();   // both groups have read their fp32 columns
       tc_fence_after();
       tcg::tmem_st16(tb + loff + C_X + 16 * wg, pk);
-    }
-    {  // dS^T <- gamma_L dS^T
-      const float gL = expf(G[L - 1]);
-#pragma unroll
-      for (int part = 2 * wg; part < 2 * wg + 2; ++part) {
-        float x[32];
-        tmem_ld32(tb + loff + C_S + 32 * part, x);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] *= gL;
-        tmem_st32(tb + loff + C_S + 32 * part, x);
-      }
     }
     tc_fence_before();
     __syncthreads();
@@ -2071,16 +2096,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
       bulk_store(gs, sm + OFF_STG_S, 16384);
       bulk_store(gs + 16384, sm + OFF_STG_S + 16384, 16384);
       bulk_store(ws.dX + ch * ws.sdX, sm + OFF_STG_X, 16384);
+      if (L == C) {   // dv rows by TMA (a chunk ending earlier must not touch the next sequence)
+        tma_store_3d(&tmDV, st + ST_V, 0, h, t0);
+        tma_store_3d(&tmDV, st + ST_V + 8192, 64, h, t0);
+      }
       tma_store_commit();
     }
-    if (tid < 64) {   // the row dots, summed over the four warps in a fixed order
-      float* xv = ws.XV + ch * 4 * 64;
-      xv[tid] = (red[tid] + red[64 + tid]) + (red[128 + tid] + red[192 + tid]);
-      xv[64 + tid] = 0.f;
-      xv[128 + tid] = 0.f;
-      xv[192 + tid] = 0.f;
+    if (L < C) {   // dv rows i < L of the sequence's last chunk, 16 bytes a store
+      for (int e = tid; e < 64 * 16; e += kThreads) {
+        const int i = e >> 4, hh = (e >> 3) & 1, c8 = e & 7;
+        if (i < L)
+          *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(b.dv) +
+                                    (((size_t)(t0 + i) * Hv + h) * 128 + 64 * hh + 8 * c8) * 2) =
+              *reinterpret_cast<const uint4*>(st + ST_V + hh * 8192 + i * 128 + ((c8 ^ (i & 7)) << 4));
+      }
     }
-    if (tid == 0) {   // dS^T += dO^T (scale gamma r_q q) + (dX^T diag(-gamma beta)) (r_k k)
+    if (tid < 64)   // the row dots, summed over the four lane quarters in a fixed order
+      ws.XV[ch * 4 * 64 + tid] = (red[tid] + red[64 + tid]) + (red[128 + tid] + red[192 + tid]);
+    if (tid == 0) {   // dS^T += dO^T (scale gamma r_q q) + (dX^T diag(-gamma beta r_k)) k
       const uint32_t iq = idesc_bf16(128, 128, true, true), ik = idesc_bf16(128, 128, false, true);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
@@ -2091,24 +2124,28 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
         mma_bf16_ta(tb + C_S, tb + C_X + 8 * ks, tcg::mndesc(sst + ST_K + ks * 2048, 8192), ik, 1);
       mma_commit(mmab);
     }
-    if (tid == 0) ok = mbar_wait(mmab, ph, kWaitNs);
+    if (tid == 0) {
+      ok = mbar_wait(mmab, ph, kWaitNs);
+      // the staged tiles and the dv rows have left shared memory: the staging buffers and this
+      // stage may be refilled once the iteration ends
+      tma_store_wait_read();
+    }
     ph ^= 1u;
     if (__syncthreads_or(!ok)) { failed = true; break; }
     tc_fence_after();
-    if (tid == 0 && qc - 2 >= 0) {   // every read of this stage is done: chunk qc - 2 into it
-      issue_stage(st, &full[s], &tmQ, &tmK, &tmV, &tmO,
-                  reinterpret_cast<const uint8_t*>(ws.T + ((size_t)(first + qc - 2) * Hv + h) * 64 * 64),
-                  bos + (qc - 2) * C, hq, h);
-    }
     pack_state(tb, loff, wg);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
   }
-  if (tid == 0) tma_store_wait_all();   // the staged tiles are written before the CTA exits
-  if (failed) {
-    if (tid == 0) report(a.dev_status, GDN_DEV_TIMEOUT);
-  } else if (b.d_initial) {
+  if (tid == 0) {
+    tma_store_wait_all();   // the staged tiles are written before the CTA exits
+    if (failed) {   // tiles still in flight land before the shared memory is released
+      for (int k = it; k < issued; ++k) mbar_wait(&full[k & 1], (uint32_t)(k >> 1) & 1u, kWaitNs);
+      report(a.dev_status, GDN_DEV_TIMEOUT);
+    }
+  }
+  if (!failed && b.d_initial) {
 #pragma unroll
     for (int part = 2 * wg; part < 2 * wg + 2; ++part) {
       float x[32];
@@ -2248,17 +2285,19 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
     const long long blocks = (long long)vtiles * a.Hv * a.num_seqs;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     if (tc) {
-      CUtensorMap mq, mk, mv, mo;
+      CUtensorMap mq, mk, mv, mo, mdv;
       memset(&mq, 0, sizeof(mq));
       memset(&mk, 0, sizeof(mk));
       memset(&mv, 0, sizeof(mv));
       memset(&mo, 0, sizeof(mo));
+      memset(&mdv, 0, sizeof(mdv));
       if (!encode_rows_map_bf16(&mq, a.q, a.Hqk, T_total) || !encode_rows_map_bf16(&mk, a.k, a.Hqk, T_total) ||
-          !encode_rows_map_bf16(&mv, a.v, a.Hv, T_total) || !encode_rows_map_bf16(&mo, b.d_o, a.Hv, T_total))
+          !encode_rows_map_bf16(&mv, a.v, a.Hv, T_total) || !encode_rows_map_bf16(&mo, b.d_o, a.Hv, T_total) ||
+          !encode_rows_map_bf16(&mdv, b.dv, a.Hv, T_total))
         return cudaErrorInvalidValue;
       const long long ctas = (long long)a.num_seqs * a.Hv;
       if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-      tcr::bwd_reverse_tc_kernel<<<(unsigned)ctas, tcr::kThreads, tcr::SMEM, a.stream>>>(mq, mk, mv, mo, a, b, ws);
+      tcr::bwd_reverse_tc_kernel<<<(unsigned)ctas, tcr::kThreads, tcr::SMEM, a.stream>>>(mq, mk, mv, mo, mdv, a, b, ws);
     } else {
       bwd_reverse_kernel<<<(unsigned)blocks, kRevThreads, kRevSmem, a.stream>>>(a, b, ws);
     }

@@ -235,6 +235,18 @@ __device__ __forceinline__ void tmem_ld16x256b_x4(uint32_t taddr, uint32_t (&r)[
         "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
+// The inverse of tmem_ld16x256b_x4 (same register fragment; no wait).
+__device__ __forceinline__ void tmem_st16x256b_x4(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -244,6 +256,16 @@ __device__ __forceinline__ void tmem_wait_ld() {
 // 2 (t%4) + 1 of matrix i (low half first) -- the fragment stmatrix takes.
 __device__ __forceinline__ void ldmatrix_x4(uint32_t saddr, uint32_t (&f)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(f[0]), "=r"(f[1]), "=r"(f[2]), "=r"(f[3])
+               : "r"(saddr)
+               : "memory");
+}
+
+// Four 8 x 8 b16 matrices loaded transposed: lane 8 i + r gives the shared address of memory
+// row r of matrix i; register i of thread t receives memory rows 2 (t%4) and 2 (t%4) + 1 of
+// column t/4 (low half first) -- the fragment stmatrix_x4_trans stores at the same addresses.
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t saddr, uint32_t (&f)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(f[0]), "=r"(f[1]), "=r"(f[2]), "=r"(f[3])
                : "r"(saddr)
                : "memory");
