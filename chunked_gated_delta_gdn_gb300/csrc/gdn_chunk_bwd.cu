@@ -1760,6 +1760,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(
 namespace tcr {
 using namespace sm100;
 constexpr int kThreads = 256;    // two warps per TMEM lane quarter
+constexpr int kStorer = 32;      // the thread that issues (and waits for) the bulk stores
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t ST_Q = 0, ST_K = 16384, ST_V = 32768, ST_DO = 49152, ST_T = 65536, ST_P = 73728;
 constexpr uint32_t ST_VEC = 81920;                        // the prep pass's per-token vectors
@@ -2061,6 +2062,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
       mma_commit(mmab);
     }
     if (tid == 0) ok = mbar_wait(mmab, ph, kWaitNs);
+    if (tid == kStorer) tma_store_wait_read();   // the previous tiles have left the staging buffers
     ph ^= 1u;
     if (__syncthreads_or(!ok)) { failed = true; break; }
     tc_fence_after();
@@ -2091,15 +2093,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (tid == 0) {
-      uint8_t* gs = reinterpret_cast<uint8_t*>(ws.dS + ch * ws.sdS);
-      bulk_store(gs, sm + OFF_STG_S, 16384);
-      bulk_store(gs + 16384, sm + OFF_STG_S + 16384, 16384);
-      bulk_store(ws.dX + ch * ws.sdX, sm + OFF_STG_X, 16384);
+    if (tid == kStorer) {   // beside the dS update: dv first (its own group), then dS and dX
       if (L == C) {   // dv rows by TMA (a chunk ending earlier must not touch the next sequence)
         tma_store_3d(&tmDV, st + ST_V, 0, h, t0);
         tma_store_3d(&tmDV, st + ST_V + 8192, 64, h, t0);
       }
+      tma_store_commit();
+      uint8_t* gs = reinterpret_cast<uint8_t*>(ws.dS + ch * ws.sdS);
+      bulk_store(gs, sm + OFF_STG_S, 16384);
+      bulk_store(gs + 16384, sm + OFF_STG_S + 16384, 16384);
+      bulk_store(ws.dX + ch * ws.sdX, sm + OFF_STG_X, 16384);
       tma_store_commit();
     }
     if (L < C) {   // dv rows i < L of the sequence's last chunk, 16 bytes a store
@@ -2111,8 +2114,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
               *reinterpret_cast<const uint4*>(st + ST_V + hh * 8192 + i * 128 + ((c8 ^ (i & 7)) << 4));
       }
     }
-    if (tid < 64)   // the row dots, summed over the four lane quarters in a fixed order
-      ws.XV[ch * 4 * 64 + tid] = (red[tid] + red[64 + tid]) + (red[128 + tid] + red[192 + tid]);
+    if (tid >= 64 && tid < 128) {   // the row dots, summed over the lane quarters in a fixed order
+      const int i = tid - 64;
+      ws.XV[ch * 4 * 64 + i] = (red[i] + red[64 + i]) + (red[128 + i] + red[192 + i]);
+    }
     if (tid == 0) {   // dS^T += dO^T (scale gamma r_q q) + (dX^T diag(-gamma beta r_k)) k
       const uint32_t iq = idesc_bf16(128, 128, true, true), ik = idesc_bf16(128, 128, false, true);
 #pragma unroll
@@ -2124,12 +2129,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
         mma_bf16_ta(tb + C_S, tb + C_X + 8 * ks, tcg::mndesc(sst + ST_K + ks * 2048, 8192), ik, 1);
       mma_commit(mmab);
     }
-    if (tid == 0) {
-      ok = mbar_wait(mmab, ph, kWaitNs);
-      // the staged tiles and the dv rows have left shared memory: the staging buffers and this
-      // stage may be refilled once the iteration ends
-      tma_store_wait_read();
-    }
+    if (tid == 0) ok = mbar_wait(mmab, ph, kWaitNs);
+    // the dv rows have left the stage, which the next iteration refills (the staged dS and dX
+    // tiles may still be in flight: they are waited for before the next staging)
+    if (tid == kStorer) tma_store_wait_read_allbut1();
     ph ^= 1u;
     if (__syncthreads_or(!ok)) { failed = true; break; }
     tc_fence_after();
@@ -2138,8 +2141,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
     __syncthreads();
     tc_fence_after();
   }
+  if (tid == kStorer) tma_store_wait_all();   // the stored tiles are written before the CTA exits
   if (tid == 0) {
-    tma_store_wait_all();   // the staged tiles are written before the CTA exits
     if (failed) {   // tiles still in flight land before the shared memory is released
       for (int k = it; k < issued; ++k) mbar_wait(&full[k & 1], (uint32_t)(k >> 1) & 1u, kWaitNs);
       report(a.dev_status, GDN_DEV_TIMEOUT);
