@@ -1025,6 +1025,8 @@ constexpr uint32_t OFF_VEC = 204800;    // fp32 per-token vectors, 16 x 64
 constexpr uint32_t OFF_BAR = OFF_VEC + 16 * 64 * 4;
 constexpr uint32_t SMEM = OFF_BAR + 64 + 1024;
 constexpr uint32_t T_R1 = 0, T_R2 = 256, T_R3 = 320, T_R4 = 384, T_COLS = 512;
+constexpr int kTmaThread = 160;   // issues the TMA loads and stores (thread 0: the bulk loads, MMAs)
+constexpr int kTmemWarp = 4;      // allocates and frees the tensor memory
 
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -1045,16 +1047,19 @@ __device__ __forceinline__ void put4(uint8_t* tile, uint32_t half, int row, int 
   u.y = pack2(x[2], x[3]);
   *reinterpret_cast<uint2*>(tile + (col >> 6) * half + sw128_offset(row, col & 63)) = u;
 }
-// Scale the 8 bf16 of the 16-byte chunk at p by s.
-__device__ __forceinline__ void scale8(uint8_t* p, float s) {
-  uint4 v = *reinterpret_cast<uint4*>(p);
+// The 8 bf16 of a 16-byte chunk scaled by s.
+__device__ __forceinline__ uint4 scaled8(uint4 v, float s) {
   uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[q]));
     w[q] = pack2(s * f.x, s * f.y);
   }
-  *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+// Scale the 8 bf16 of the 16-byte chunk at p by s.
+__device__ __forceinline__ void scale8(uint8_t* p, float s) {
+  *reinterpret_cast<uint4*>(p) = scaled8(*reinterpret_cast<const uint4*>(p), s);
 }
 __device__ __forceinline__ uint64_t kdesc(uint32_t addr) { return sdesc_sw128(addr, 16, 1024); }
 __device__ __forceinline__ uint64_t mndesc(uint32_t addr, uint32_t lbo) {
@@ -1063,7 +1068,8 @@ __device__ __forceinline__ uint64_t mndesc(uint32_t addr, uint32_t lbo) {
 
 __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-    const __grid_constant__ CUtensorMap tmO, const ChunkArgs a, const BwdArgs b, BwdWs ws) {
+    const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmDQ,
+    const __grid_constant__ CUtensorMap tmDK, const ChunkArgs a, const BwdArgs b, BwdWs ws) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(sm);
@@ -1073,8 +1079,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
   float* dba = vec + 512;      float* cs = vec + 576;   float* xvr = vec + 640; float* red = vec + 704;
   float* dGv = vec + 768;      float* om = vec + 832;   float* g2 = vec + 896;
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-  uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + OFF_BAR + 8);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 16);
+  uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + OFF_BAR + 8);    // the bulk loads
+  uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + OFF_BAR + 16);  // the TMA loads
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 24);
   // one CTA per (chunk, value head), heads fastest: the CTAs running together read the
   // same tokens (adjacent rows), and the two value heads of a query/key head share its
   // q, k rows through L2
@@ -1088,30 +1095,36 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
   if (tid == 0) {
     mbar_init(bar, 1);
     mbar_init(bar_ld, 1);
+    mbar_init(bar_tma, 1);
     fence_mbar_init();
+  }
+  __syncthreads();   // the barriers are initialised before any copy is issued
+  if (tid == 0) {
     // the operand tiles the producers wrote: S0, dS (32 KB each), U' (16 KB), and the two
     // 8 KB halves of dX into rows 64-127 of [dO; dX]
     const uint8_t* s0 = reinterpret_cast<const uint8_t*>(ws.S + ch * ws.sS);
     const uint8_t* ds = reinterpret_cast<const uint8_t*>(ws.dS + ch * ws.sdS);
     const uint8_t* ug = reinterpret_cast<const uint8_t*>(ws.U + ch * ws.sU);
     const uint8_t* xg = reinterpret_cast<const uint8_t*>(ws.dX + ch * ws.sdX);
-    mbar_arrive_expect_tx(bar_ld, 32768 + 32768 + 16384 + 16384 + 3 * 16384);
+    mbar_arrive_expect_tx(bar_ld, 32768 + 32768 + 16384 + 16384);
     bulk_load(sm + OFF_S0, s0, 32768, bar_ld);
     bulk_load(sm + OFF_DS, ds, 32768, bar_ld);
     bulk_load(sm + OFF_U, ug, 16384, bar_ld);
     bulk_load(sm + OFF_OX + 8192, xg, 8192, bar_ld);
     bulk_load(sm + OFF_OX + 16384 + 8192, xg + 8192, 8192, bar_ld);
+  } else if (tid == kTmaThread) {
     // the chunk's q, k rows into [q; k] and its dO rows into rows 0-63 of [dO; dX], by TMA
     // (64 features x 64 tokens a box, zero past the last token; rows past the chunk end are
     // cleared below)
+    mbar_arrive_expect_tx(bar_tma, 3 * 16384);
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-      tma_load_3d(sm + OFF_QK + hh * 16384, &tmQ, bar_ld, 64 * hh, hq, t0);
-      tma_load_3d(sm + OFF_QK + hh * 16384 + 8192, &tmK, bar_ld, 64 * hh, hq, t0);
-      tma_load_3d(sm + OFF_OX + hh * 16384, &tmO, bar_ld, 64 * hh, h, t0);
+      tma_load_3d(sm + OFF_QK + hh * 16384, &tmQ, bar_tma, 64 * hh, hq, t0);
+      tma_load_3d(sm + OFF_QK + hh * 16384 + 8192, &tmK, bar_tma, 64 * hh, hq, t0);
+      tma_load_3d(sm + OFF_OX + hh * 16384, &tmO, bar_tma, 64 * hh, h, t0);
     }
   }
-  if (warp == 0) {
+  if (warp == kTmemWarp) {
     tmem_alloc(tslot, T_COLS);
     tmem_relinquish();
   }
@@ -1127,11 +1140,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
   }
   fence_proxy_async_smem();
   bool ok = true;
-  if (tid == 0) ok = mbar_wait(bar_ld, 0, kWaitNs);   // the bulk copies have landed
+  if (tid == 0) ok = mbar_wait(bar_ld, 0, kWaitNs) && mbar_wait(bar_tma, 0, kWaitNs);   // landed
   tc_fence_before();
   if (__syncthreads_or(!ok)) {
     if (tid == 0) report(a.dev_status, GDN_DEV_TIMEOUT);
-    if (warp == 0) {
+    if (warp == kTmemWarp) {
       tc_fence_after();
       tmem_dealloc(*tslot, T_COLS);
     }
@@ -1144,12 +1157,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     const int r = tid >> 1, hh = tid & 1, i = r & 63;
     uint8_t* rowp = sm + OFF_QK + hh * 16384 + r * 128;
     float ss = 0.f;
-    // 16-byte chunks in an order rotated by the row: the warp's accesses spread over the banks
+    // 16-byte chunks in an order rotated by the row (the warp's accesses spread over the
+    // banks), kept in registers for the scaling
+    uint4 u[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) u[j] = *reinterpret_cast<const uint4*>(rowp + 16 * ((j + r) & 7));
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int c8 = (j + r) & 7;
-      const uint4 u = *reinterpret_cast<const uint4*>(rowp + 16 * c8);
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      const uint32_t w[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[q]));
@@ -1159,7 +1174,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     ss += __shfl_xor_sync(0xffffffffu, ss, 1);
     const float rn = i < L ? (l2 ? 1.0f / sqrtf(ss + kL2Eps) : 1.f) : 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) scale8(rowp + 16 * ((j + r) & 7), rn);
+    for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(rowp + 16 * ((j + r) & 7)) = scaled8(u[j], rn);
     for (int e = tid; e < 2 * 64 * 8; e += kThreads) {
       const int hf = e >> 9, ii = (e >> 3) & 63, c8 = e & 7;
       if (ii >= L)
@@ -1181,11 +1196,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     }
     mma_commit(bar);
   }
-  {  // <S0, dS> over the two tiles (same layout, element by element)
+  if (warp > 0) {  // <S0, dS> over the two tiles (same layout, element by element), by the
+                   // warps that do not issue the products
     float sd = 0.f;
     const uint4* p0 = reinterpret_cast<const uint4*>(sm + OFF_S0);
     const uint4* p1 = reinterpret_cast<const uint4*>(sm + OFF_DS);
-    for (int e = tid; e < 32768 / 16; e += kThreads) {
+#pragma unroll 4
+    for (int e = tid - 32; e < 32768 / 16; e += kThreads - 32) {
       const uint4 u0 = p0[e], u1 = p1[e];
       const uint32_t w0[4] = {u0.x, u0.y, u0.z, u0.w}, w1[4] = {u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
@@ -1208,7 +1225,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     if (tid == 0) report(a.dev_status, GDN_DEV_TIMEOUT);
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tb, T_COLS);
+    if (warp == kTmemWarp) tmem_dealloc(tb, T_COLS);
     return;
   }
   tc_fence_after();
@@ -1243,17 +1260,30 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
   }
   __syncthreads();
   // ---- R4's scaled operands: [scale gamma dO; -gamma beta dX] in place, lambda U' rows 64-127
-  for (int e = tid; e < 128 * 16; e += kThreads) {
-    const int r = e >> 4, chunk = e & 15, hlf = chunk >> 3, c8 = chunk & 7;
-    const float s = r < 64 ? a.scale * gm[r] : -gm[r - 64] * bt[r - 64];
-    scale8(sm + OFF_OX + hlf * 16384 + r * 128 + ((c8 ^ (r & 7)) << 4), s);
-  }
-  for (int e = tid; e < 64 * 16; e += kThreads) {
-    const int i = e >> 4, chunk = e & 15, hlf = chunk >> 3, c8 = chunk & 7;
-    const uint32_t sw = (uint32_t)((c8 ^ (i & 7)) << 4);
-    uint8_t* dst = sm + OFF_LU + hlf * 16384 + (64 + i) * 128 + sw;
-    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(sm + OFF_U + hlf * 8192 + i * 128 + sw);
-    scale8(dst, lm[i]);
+  {  // (every load of a thread before its stores)
+    uint4 u[8], w[4];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int e = tid + kThreads * k, r = e >> 4, chunk = e & 15;
+      u[k] = *reinterpret_cast<const uint4*>(sm + OFF_OX + (chunk >> 3) * 16384 + r * 128 + (chunk & 7) * 16);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int e = tid + kThreads * k, i = e >> 4, chunk = e & 15;
+      w[k] = *reinterpret_cast<const uint4*>(sm + OFF_U + (chunk >> 3) * 8192 + i * 128 + (chunk & 7) * 16);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int e = tid + kThreads * k, r = e >> 4, chunk = e & 15;
+      const float s = r < 64 ? a.scale * gm[r] : -gm[r - 64] * bt[r - 64];
+      *reinterpret_cast<uint4*>(sm + OFF_OX + (chunk >> 3) * 16384 + r * 128 + (chunk & 7) * 16) = scaled8(u[k], s);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {   // (U' and [0; lambda U'] share the swizzle: row i = 64 + i mod 8)
+      const int e = tid + kThreads * k, i = e >> 4, chunk = e & 15;
+      *reinterpret_cast<uint4*>(sm + OFF_LU + (chunk >> 3) * 16384 + (64 + i) * 128 + (chunk & 7) * 16) =
+          scaled8(w[k], lm[i]);
+    }
   }
   // ---- F (rows i < 64 of R2 / R3) and E (rows 64-127), all eight warps at once: a warp
   //      reaches the TMEM lanes 32 (warp % 4) .. + 31 and takes the column half warp / 4
@@ -1359,28 +1389,43 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     if (tid == 0) report(a.dev_status, GDN_DEV_TIMEOUT);
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tb, T_COLS);
+    if (warp == kTmemWarp) tmem_dealloc(tb, T_COLS);
     return;
   }
   tc_fence_after();
-  if (warp < 4) {   // [dQ; dK] rows to the per-value-head scratch: each thread stages its row in
-                    // the operand space the products no longer read (528-byte stride), then one
-                    // 512-byte bulk copy
+  {  // [dQ; dK] rows to the per-value-head scratch: R4 staged by all eight warps (two column
+     // parts each) as 32-column fp32 boxes, 128-byte swizzled, in the operand space the products
+     // no longer read (dQ rows: boxes 0-3, dK rows: boxes 4-7, 8 KB each)
     const int i = row & 63;
-    uint8_t* srow = sm + OFF_S0 + row * 528;
-#pragma unroll
-    for (int part = 0; part < 4; ++part) {
+    uint8_t* rbase = sm + OFF_S0 + (row >> 6) * 32768 + i * 128;
+#pragma unroll 1
+    for (int part = 2 * (warp >> 2); part < 2 * (warp >> 2) + 2; ++part) {
       float x[32];
       tmem_ld32(tb + loff + T_R4 + 32 * part, x);
 #pragma unroll
       for (int q = 0; q < 8; ++q)
-        *reinterpret_cast<float4*>(srow + 128 * part + 16 * q) =
+        *reinterpret_cast<float4*>(rbase + part * 8192 + ((q ^ (i & 7)) << 4)) =
             make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
     }
-    if (i < L) {
-      fence_proxy_async_smem();
-      bulk_store((row < 64 ? ws.dQ : ws.dK) + ((size_t)(t0 + i) * Hv + h) * 128, srow, 512);
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  if (L == C) {   // eight TMA stores
+    if (tid == kTmaThread) {
+#pragma unroll
+      for (int part = 0; part < 4; ++part) {
+        tma_store_3d(&tmDQ, sm + OFF_S0 + part * 8192, 32 * part, h, t0);
+        tma_store_3d(&tmDK, sm + OFF_S0 + 32768 + part * 8192, 32 * part, h, t0);
+      }
       tma_store_commit();
+    }
+  } else {   // a chunk ending early: rows i < L only (the next ones are another sequence's)
+    for (int e = tid; e < 2 * 64 * 32; e += kThreads) {
+      const int hf = e >> 11, i = (e >> 5) & 63, part = (e >> 3) & 3, q = e & 7;
+      if (i < L)
+        *reinterpret_cast<float4*>((hf ? ws.dK : ws.dQ) + ((size_t)(t0 + i) * Hv + h) * 128 + 32 * part + 4 * q) =
+            *reinterpret_cast<const float4*>(sm + OFF_S0 + hf * 32768 + part * 8192 + i * 128 + ((q ^ (i & 7)) << 4));
     }
   }
   // ---- dG, dbeta per token, then dg by a suffix sum
@@ -1391,12 +1436,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     dGv[i] = i < L ? a.scale * gm[i] * qh1[i] - bt[i] * gm[i] * kh2[i] - omega + rz[i] - cs[i] : 0.f;
     if (i < L) b.dbeta[(size_t)(t0 + i) * Hv + h] = xvr[i] - gm[i] * kh2[i] + dba[i];
   }
-  if (warp < 4) tma_store_wait_all();   // the staged rows are written before the CTA exits
-  tc_fence_before();
+  if (tid == kTmaThread) tma_store_wait_read();   // the staged rows have left shared memory
   __syncthreads();
+  if (warp == kTmemWarp) {
+    tc_fence_after();
+    tmem_dealloc(tb, T_COLS);
+  }
   if (warp == 0) {
     float sdt = 0.f;
-    for (int w = 0; w < kThreads / 32; ++w) sdt += red[w];
+    for (int w = 1; w < kThreads / 32; ++w) sdt += red[w];
     const float omsum = warp_sum(om[lane] + om[lane + 32]);
     float x0 = dGv[lane], x1 = dGv[lane + 32];
     const float extra = gm[L - 1] * sdt + omsum;
@@ -1412,8 +1460,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     const size_t base = (size_t)t0 * Hv + h;
     if (lane < L) b.dg[base + (size_t)lane * Hv] = x0;
     if (lane + 32 < L) b.dg[base + (size_t)(lane + 32) * Hv] = x1;
-    tc_fence_after();
-    tmem_dealloc(tb, T_COLS);
   }
 }
 }  // namespace tcg
@@ -2308,14 +2354,17 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
   }
   if (NC > 0) {
     if (tc) {
-      CUtensorMap gq, gk, go;
+      CUtensorMap gq, gk, go, gdq, gdk;
       memset(&gq, 0, sizeof(gq));
       memset(&gk, 0, sizeof(gk));
       memset(&go, 0, sizeof(go));
+      memset(&gdq, 0, sizeof(gdq));
+      memset(&gdk, 0, sizeof(gdk));
       if (!encode_rows_map_bf16(&gq, a.q, a.Hqk, T_total) || !encode_rows_map_bf16(&gk, a.k, a.Hqk, T_total) ||
-          !encode_rows_map_bf16(&go, b.d_o, a.Hv, T_total))
+          !encode_rows_map_bf16(&go, b.d_o, a.Hv, T_total) || !encode_rows_map_f32(&gdq, ws.dQ, a.Hv, T_total) ||
+          !encode_rows_map_f32(&gdk, ws.dK, a.Hv, T_total))
         return cudaErrorInvalidValue;
-      tcg::bwd_grad_tc_kernel<<<(unsigned)(NC * a.Hv), tcg::kThreads, tcg::SMEM, a.stream>>>(gq, gk, go, a, b, ws);
+      tcg::bwd_grad_tc_kernel<<<(unsigned)(NC * a.Hv), tcg::kThreads, tcg::SMEM, a.stream>>>(gq, gk, go, gdq, gdk, a, b, ws);
     } else {
       bwd_grad_kernel<<<dim3((unsigned)NC, a.Hv), kGradThreads, kGradSmem, a.stream>>>(a, b, ws);
     }

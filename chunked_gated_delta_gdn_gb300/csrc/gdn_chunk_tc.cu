@@ -124,14 +124,16 @@ __device__ unsigned long long g_chunk_stamps[2][2][64][16];
   } while (0)
 #endif
 
-// The Tw / Tu operands of chunk c: one buffer in record mode; two, by chunk parity, in forward
-// mode, the second in the record-staging space that forward mode does not use.
+// The Tw / Tu operands of chunk c: two buffers by chunk parity, the second in space the mode
+// does not use otherwise (forward mode: the record staging; record mode, which writes no
+// output: the P buffers).
 template <bool kRecord>
-__device__ __forceinline__ uint32_t tw_off(int c) { return (!kRecord && (c & 1)) ? OFF_REC : OFF_TW; }
+__device__ __forceinline__ uint32_t tw_off(int c) { return (c & 1) ? (kRecord ? OFF_P : OFF_REC) : OFF_TW; }
 template <bool kRecord>
-__device__ __forceinline__ uint32_t tu_off(int c) { return (!kRecord && (c & 1)) ? OFF_REC + 8192 : OFF_TU; }
-template <bool kRecord>
-__device__ __forceinline__ int wu_bar(int c) { return (!kRecord && (c & 1)) ? B_WU1 : B_WU; }
+__device__ __forceinline__ uint32_t tu_off(int c) {
+  return (c & 1) ? (kRecord ? OFF_P + 8192 : OFF_REC + 8192) : OFF_TU;
+}
+__device__ __forceinline__ int wu_bar(int c) { return (c & 1) ? B_WU1 : B_WU; }
 
 // =================================================================== prep group
 // Warps 0-7.  For each chunk: D1 = [Q;K][Q;K]^T, gates, norms (from the diagonal of
@@ -185,19 +187,18 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
       gates_step(a, vec, gq, bq, L, lane, fused, expA, dtb, c + 1 < nchunks, t0 + kChunk, h, T_total);
     if (leader) {
       ok = mbar_wait(&bars[B_MMA_P], (uint32_t)c & 1u, kWaitLimitNs);   // one D1 commit per chunk
-      if (c >= 2) ok = ok && mbar_wait(&bars[B_P_FREE + s], (uint32_t)((c - 2) >> 1) & 1u, kWaitLimitNs);
+      if (!kRecord && c >= 2) ok = ok && mbar_wait(&bars[B_P_FREE + s], (uint32_t)((c - 2) >> 1) & 1u, kWaitLimitNs);
     }
     if (group_sync_or(kBarPrep, kPrepThreads, !ok || flag_set(flag))) { if (leader) set_flag(flag); return; }
     tc_fence_after();
     GDN_STAMP(0, 3);
 
-    // ---- norms, P (to this chunk's P buffer) and A from D1
-    norms_p_a<kBarPrep>(a, tbase + COL_D1, vec, sA, sm + OFF_P + s * 8192, L);
+    // ---- norms, P (to this chunk's P buffer; none in record mode) and A from D1
+    norms_p_a<kBarPrep>(a, tbase + COL_D1, vec, sA, kRecord ? nullptr : sm + OFF_P + s * 8192, L);
     tc_fence_before();
     GDN_STAMP(0, 4);
-    // Tw, Tu free: released by chunk c - 1 (one buffer) or c - 2 (forward mode, two buffers)
-    if (leader && c >= (kRecord ? 1 : 2))
-      ok = mbar_wait(&bars[wu_bar<kRecord>(c)], (uint32_t)(kRecord ? (c - 1) : ((c - 2) >> 1)) & 1u, kWaitLimitNs);
+    // Tw, Tu free: this buffer released by chunk c - 2
+    if (leader && c >= 2) ok = mbar_wait(&bars[wu_bar(c)], (uint32_t)((c - 2) >> 1) & 1u, kWaitLimitNs);
     if (group_sync_or(kBarPrep, kPrepThreads, !ok || flag_set(flag))) { if (leader) set_flag(flag); return; }
 
     // ---- T = (I + A)^{-1} as the Tw / Tu operands
@@ -370,15 +371,15 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     GDN_STAMP(1, 3);
 
     // ---- MMA: [O1 | Y] = S^T [Q; K]^T, one N = 128 product over the stage as loaded (A, the
-    //      bf16 S^T, from TMEM)
+    //      bf16 S^T, from TMEM); record mode, without output: Y = S^T K^T alone (N = 64)
     if (leader) {
       tc_fence_after();
-      const uint32_t id5 = idesc_bf16(128, 128, false, false);
+      const uint32_t id5 = kRecord ? idesc_bf16(128, 64, false, false) : idesc_bf16(128, 128, false, false);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-        mma_bf16_ta(tbase + COL_O1, tbase + COL_O2 + 8 * ks, sdesc_sw128(qk_a + off, 16, 1024),
-                    id5, ks > 0);
+        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32 + (kRecord ? 8192 : 0);
+        mma_bf16_ta(tbase + (kRecord ? COL_Y : COL_O1), tbase + COL_O2 + 8 * ks,
+                    sdesc_sw128(qk_a + off, 16, 1024), id5, ks > 0);
       }
       mma_commit(&bars[B_MMA_S]);
       GDN_STAMP(1, 4);
@@ -452,7 +453,7 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
         mma_bf16_ta(tbase + COL_U, tbase + COL_Y + 8 * ks,
                     sdesc_sw128(sbase + tw_off<kRecord>(c) + ks * 2048, 8192, 1024), id4, 1);
       }
-      mma_commit(&bars[wu_bar<kRecord>(c)]);
+      mma_commit(&bars[wu_bar(c)]);
       mma_commit(&bars[B_MMA_S]);
       GDN_STAMP(1, 8);
     }
@@ -518,14 +519,17 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     group_sync(kBarState, kStateThreads);
     GDN_STAMP(1, 10);
 
-    // ---- MMA: O2 = U'^T P^T (from zero) and S^T += U'^T K~ (A, the bf16 U', from TMEM)
+    // ---- MMA: O2 = U'^T P^T (from zero; not in record mode) and S^T += U'^T K~ (A, the bf16
+    //      U', from TMEM)
     if (leader) {
       tc_fence_after();
       const uint32_t id2 = idesc_bf16(128, 64, false, false), idS = idesc_bf16(128, 128, false, false);
+      if (!kRecord) {
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_bf16_ta(tbase + COL_O2, tbase + COL_U + 8 * ks,
-                    sdesc_sw128(sbase + OFF_P + s * 8192 + ks * 32, 16, 1024), id2, ks > 0);
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16_ta(tbase + COL_O2, tbase + COL_U + 8 * ks,
+                      sdesc_sw128(sbase + OFF_P + s * 8192 + ks * 32, 16, 1024), id2, ks > 0);
+      }
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
         mma_bf16_ta(tbase + COL_S, tbase + COL_U + 8 * ks,
@@ -537,14 +541,14 @@ __device__ void state_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int
     ps ^= 1u;
     if (group_sync_or(kBarState, kStateThreads, !ok || flag_set(flag))) { failed = true; break; }
     tc_fence_after();
-    if (leader) mbar_arrive(&bars[B_P_FREE + s]);   // the O2 product has read P
+    if (!kRecord && leader) mbar_arrive(&bars[B_P_FREE + s]);   // the O2 product has read P
     GDN_STAMP(1, 12);
 
     // ---- o = scale exp(G) r_q O1 + O2 (P carries scale r_q): a full chunk is staged as a
     //      bf16 tile (two 128-byte-swizzled [64 tokens][64 dv] halves) and written by one
     //      TMA store; the last, partial chunk of a sequence is stored row by row (neither for a
-    //      unit that writes no output)
-    if (uflags & kUnitNoOut) {
+    //      unit that writes no output, nor in record mode)
+    if (kRecord || (uflags & kUnitNoOut)) {
     } else if (L == kChunk) {
       // 16x256b loads hand each thread dv (t/4, t/4 + 8 of a 16-lane half) x tokens
       // (2 (t%4), +1 of each 8-token group): the fragment of stmatrix .trans, which writes
@@ -758,6 +762,18 @@ bool encode_map(CUtensorMap* m, const void* base, int H, int T_total) {
 
 bool encode_rows_map_bf16(CUtensorMap* m, const void* base, int H, int T_total) {
   return encode_map(m, base, H, T_total);
+}
+
+bool encode_rows_map_f32(CUtensorMap* m, const void* base, int H, int T_total) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)T_total};
+  cuuint64_t strides[2] = {128 * 4, (cuuint64_t)H * 128 * 4};
+  cuuint32_t box[3] = {32, 1, 64};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool chunk_tc_supported(int K, int V, int io_dtype, int beta_dtype) {

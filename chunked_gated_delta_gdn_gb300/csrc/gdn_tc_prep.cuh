@@ -187,8 +187,8 @@ __device__ __forceinline__ void gates_step(const ChunkArgs& a, float* vec, float
 
 // After D1 of the chunk has landed in TMEM at d1 (and the gates are in vec): the inverse
 // norms from its diagonal (lane i, column i: |q_i|^2 for i < 64, |k_{i-64}|^2 above) and the
-// per-token scalars built from them, then P (bf16, K-major rows i, to p_dst) and A (fp32, to
-// sA).  The row and column factors enter as exponents: x * 2^(G_i + log2 f_i - H_j).
+// per-token scalars built from them, then P (bf16, K-major rows i, to p_dst; none when p_dst
+// is null) and A (fp32, to sA).  The row and column factors enter as exponents: x * 2^(G_i + log2 f_i - H_j).
 // Synchronises the group once in the middle; the caller syncs before P, A or vec are read.
 template <int kBar>
 __device__ __forceinline__ void norms_p_a(const ChunkArgs& a, uint32_t d1, float* vec, float* sA,
@@ -220,6 +220,8 @@ __device__ __forceinline__ void norms_p_a(const ChunkArgs& a, uint32_t d1, float
   }
   group_sync(kBar, kPrepThreads);
 
+  const bool is_p = quad < 2;
+  if (is_p && !p_dst) return;   // no P wanted
   const int j0 = 32 * chalf;
   float hj[32];
 #pragma unroll
@@ -230,7 +232,6 @@ __device__ __forceinline__ void norms_p_a(const ChunkArgs& a, uint32_t d1, float
   // one code path for both halves: P rows (quads 0-1) keep j <= i with the row factor scale r_q[i]
   // (zero past the chunk end: lg2(0) = -inf gives exact zeros), A rows (quads 2-3) keep j < i with
   // the row factor beta r_k[i]; both as exponents
-  const bool is_p = quad < 2;
   const int i = is_p ? row : row - 64;
   const float base = vec[VEC_G + i] + lg2(is_p ? ((i < L) ? a.scale * vec[VEC_RQ + i] : 0.f)
                                                : vec[VEC_BETA + i] * vec[VEC_RK + i]);
