@@ -74,8 +74,8 @@ struct BwdWs {
   float* dX;           // [NC][Hv][C][V]
   float* Z;            // [NC][Hv][K][V]  scale Q^T diag(gamma) dO   (fp32 path)
   float* XV;           // [NC][Hv][4][C]  partial row dots dX_i . v_i per 32-column slice
-  float* dQ;           // [T_total][Hv][K] per value head, before the norm
-  float* dK;           // [T_total][Hv][K]
+  float* dQ;           // [T_total][Hv][K] per value head, before the norm   (fp32 path)
+  float* dK;           // [T_total][Hv][K]                                   (fp32 path)
   size_t sS, sdS, sU, sdX;   // slot strides (floats) per (chunk, head) of S, dS, U, dX
 };
 
@@ -116,8 +116,8 @@ __host__ __device__ inline BwdWs bwd_layout(void* base, long long NC, int N, int
   w.dX = reinterpret_cast<float*>(take(f * ch * w.sdX));
   w.Z = tc ? nullptr : reinterpret_cast<float*>(take(f * ch * K * V));
   w.XV = reinterpret_cast<float*>(take(f * ch * 4 * C));
-  w.dQ = reinterpret_cast<float*>(take(f * (size_t)T_total * Hv * K));
-  w.dK = reinterpret_cast<float*>(take(f * (size_t)T_total * Hv * K));
+  w.dQ = tc ? nullptr : reinterpret_cast<float*>(take(f * (size_t)T_total * Hv * K));
+  w.dK = tc ? nullptr : reinterpret_cast<float*>(take(f * (size_t)T_total * Hv * K));
   if (total) *total = off;
   return w;
 }
@@ -202,13 +202,6 @@ constexpr int kBarT = 1;          // named barrier of the two warps that build T
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 
-// Four bf16 at element i (i % 4 == 0) through the read-only path, as fp32.
-__device__ __forceinline__ void load4b(const void* p, size_t i, float (&x)[4]) {
-  const uint2 u = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(p) + i));
-  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
-  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
-  x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
-}
 
 __device__ __forceinline__ void load4(const void* p, size_t i, int dtype, float (&x)[4]) {
   if (dtype == GDN_BF16) {
@@ -985,15 +978,20 @@ __global__ void __launch_bounds__(kGradThreads) bwd_grad_kernel(const ChunkArgs 
 // bf16 I/O with K = V = 128: the same quantities as bwd_grad_kernel, with every product a
 // tcgen05.mma (bf16 operands in 128-byte-swizzled shared memory, fp32 accumulators in TMEM;
 // S0, dS, U', dX and the normalised q, k rounded to bf16 as the forward's tensor-core path
-// rounds its operands).  One CTA (8 warps) per (chunk, value head); TMEM columns:
+// rounds its operands).  One CTA (8 warps) per (chunk, query/key head), which takes the value
+// heads of the group in order; TMEM columns:
 //   R1 [0, 256)   [Q; K] [S0 | dS]        M=128 N=256 K=128  -> q_i . S0 dO_i, k_i . S0 dX_i,
 //                                                               k_i . dS u'_i (row dots)
 //   R2 [256, 320) [dO; dX] U'^T           M=128 N=64  K=128  -> F, dA (and E)
-//   R3 [320, 384) [Q; K] K^T              M=128 N=64  K=128  -> Q K^T, K K^T
-//   R4 [384, 512) [dQ; dK] =  [scale gamma dO | 0 ; -gamma beta dX | lambda U'] [S0 | dS]^T
+//   R3 [320, 384) [Q; K] K^T              M=128 N=64  K=128  -> Q K^T, K K^T (once: the same
+//                                                               for every head of the group)
+//   R4 [384, 512) [dQ; dK] += [scale gamma dO | 0 ; -gamma beta dX | lambda U'] [S0 | dS]^T
 //                           + [F; E] K + [0; F^T] Q + [0; E^T] K          (K = 256, 64, 64, 64)
-// F^T and E^T are MN-major A operands whose first 64-row block is a zero tile and whose
-// second is F (resp. E) as stored row-major, so no transposed copy is built.
+// R4 accumulates over the group's value heads, which gives the group sum of the gradients of
+// the normalised q, k rows; the epilogue applies the L2 norm's Jacobian
+// dq = r (dq^ - q^ (q^ . dq^)) and writes dq, dk as bf16.  F^T and E^T are MN-major A operands
+// whose first 64-row block is a zero tile and whose second is F (resp. E) as stored row-major,
+// so no transposed copy is built.
 namespace tcg {
 
 // Store 16 consecutive 32-bit columns of this thread's lane and wait for the store.
@@ -1018,12 +1016,13 @@ constexpr uint32_t OFF_S0 = 32768;      // S0 rows d, 2 c-halves x 128 rows
 constexpr uint32_t OFF_DS = 65536;      // dS rows d (right after S0: [S0 | dS] is one operand)
 constexpr uint32_t OFF_OX = 98304;      // [dO; dX] rows, then [scale gamma dO; -gamma beta dX]
 constexpr uint32_t OFF_LU = 131072;     // [0; lambda U'] rows (right after OX)
-constexpr uint32_t OFF_U = 163840;      // U' rows j, 2 c-halves x 64 rows; then Z^T fp32 [64][64]
+constexpr uint32_t OFF_U = 163840;      // U' rows j, 2 c-halves x 64 rows
 constexpr uint32_t OFF_ZERO = 180224;   // 64 rows x 128 B of zeros
 constexpr uint32_t OFF_FE = 188416;     // [F; E] rows, K = 64 tokens: 128 rows x 128 B
-constexpr uint32_t OFF_VEC = 204800;    // fp32 per-token vectors, 16 x 64
-constexpr uint32_t OFF_BAR = OFF_VEC + 16 * 64 * 4;
+constexpr uint32_t OFF_VEC = 204800;    // fp32 per-token vectors and scratch, 28 x 64
+constexpr uint32_t OFF_BAR = OFF_VEC + 28 * 64 * 4;
 constexpr uint32_t SMEM = OFF_BAR + 64 + 1024;
+static_assert(SMEM <= 232448, "shared memory budget");
 constexpr uint32_t T_R1 = 0, T_R2 = 256, T_R3 = 320, T_R4 = 384, T_COLS = 512;
 constexpr int kTmaThread = 160;   // issues the TMA loads and stores (thread 0: the bulk loads, MMAs)
 constexpr int kTmemWarp = 4;      // allocates and frees the tensor memory
@@ -1038,14 +1037,6 @@ __device__ __forceinline__ float ex2g(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-// Four values as bf16 at element (row, col) of a K-major tile with 128-element rows split in
-// two 64-element halves of `half` bytes (col % 4 == 0).
-__device__ __forceinline__ void put4(uint8_t* tile, uint32_t half, int row, int col, const float (&x)[4]) {
-  uint2 u;
-  u.x = pack2(x[0], x[1]);
-  u.y = pack2(x[2], x[3]);
-  *reinterpret_cast<uint2*>(tile + (col >> 6) * half + sw128_offset(row, col & 63)) = u;
 }
 // The 8 bf16 of a 16-byte chunk scaled by s.
 __device__ __forceinline__ uint4 scaled8(uint4 v, float s) {
@@ -1066,6 +1057,39 @@ __device__ __forceinline__ uint64_t mndesc(uint32_t addr, uint32_t lbo) {
   return sdesc_sw128(addr, lbo, 1024);
 }
 
+// The operand tiles of value head h that the producers wrote (S0, dS, U', dX; bulk copies on
+// `bar_ld`, issued by thread 0) and its dO rows (TMA on `bar_tma`, issued by kTmaThread; with
+// the group's q, k rows for the first head).
+__device__ __forceinline__ void issue_head_loads(uint8_t* sm, const BwdWs& ws, const CUtensorMap* tmQ,
+                                                 const CUtensorMap* tmK, const CUtensorMap* tmO,
+                                                 uint64_t* bar_ld, uint64_t* bar_tma, size_t ch,
+                                                 int h, int hq, int t0, bool qk, int tid) {
+  if (tid == 0) {
+    const uint8_t* s0 = reinterpret_cast<const uint8_t*>(ws.S + ch * ws.sS);
+    const uint8_t* ds = reinterpret_cast<const uint8_t*>(ws.dS + ch * ws.sdS);
+    const uint8_t* ug = reinterpret_cast<const uint8_t*>(ws.U + ch * ws.sU);
+    const uint8_t* xg = reinterpret_cast<const uint8_t*>(ws.dX + ch * ws.sdX);
+    mbar_arrive_expect_tx(bar_ld, 32768 + 32768 + 16384 + 16384);
+    bulk_load(sm + OFF_S0, s0, 32768, bar_ld);
+    bulk_load(sm + OFF_DS, ds, 32768, bar_ld);
+    bulk_load(sm + OFF_U, ug, 16384, bar_ld);
+    bulk_load(sm + OFF_OX + 8192, xg, 8192, bar_ld);   // dX: rows 64-127 of [dO; dX]
+    bulk_load(sm + OFF_OX + 16384 + 8192, xg + 8192, 8192, bar_ld);
+  } else if (tid == kTmaThread) {
+    // 64 features x 64 tokens a box, zero past the last token (rows past the chunk end are
+    // cleared after the loads land)
+    mbar_arrive_expect_tx(bar_tma, (qk ? 3 : 1) * 16384);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      if (qk) {
+        tma_load_3d(sm + OFF_QK + hh * 16384, tmQ, bar_tma, 64 * hh, hq, t0);
+        tma_load_3d(sm + OFF_QK + hh * 16384 + 8192, tmK, bar_tma, 64 * hh, hq, t0);
+      }
+      tma_load_3d(sm + OFF_OX + hh * 16384, tmO, bar_tma, 64 * hh, h, t0);
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
     const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmDQ,
@@ -1078,20 +1102,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
   float* qh1 = vec + 256;      float* kh2 = vec + 320;  float* kh3 = vec + 384; float* rz = vec + 448;
   float* dba = vec + 512;      float* cs = vec + 576;   float* xvr = vec + 640; float* red = vec + 704;
   float* dGv = vec + 768;      float* om = vec + 832;   float* g2 = vec + 896;
+  float* rnv = vec + 1024;     // [128] the rows' L2-norm reciprocals (zero past the chunk end)
+  float* colp = vec + 1152;    // [4 row quarters][64] column sums of Z; then [2][128] row dots
+  float* dbp = vec + 1408;     // [2][64] partial dbeta terms
+  float* rowp = vec + 1536;    // [2 column halves][128 rows] partial row sums of Z
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + OFF_BAR + 8);    // the bulk loads
   uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + OFF_BAR + 16);  // the TMA loads
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 24);
-  // one CTA per (chunk, value head), heads fastest: the CTAs running together read the
-  // same tokens (adjacent rows), and the two value heads of a query/key head share its
-  // q, k rows through L2
-  const int h = (int)(blockIdx.x % (unsigned)a.Hv), c = (int)(blockIdx.x / (unsigned)a.Hv);
+  // one CTA per (chunk, query/key head), heads fastest: the CTAs running together read the
+  // same tokens (adjacent rows)
+  const int Hqk = a.Hqk, Hv = a.Hv, grp = Hv / Hqk;
+  const int hq = (int)(blockIdx.x % (unsigned)Hqk), c = (int)(blockIdx.x / (unsigned)Hqk);
   int n, t0, L;
   if (!locate_chunk(a, ws.chunk_off, c, &n, &t0, &L)) return;
-  const int Hv = a.Hv, hq = h / (Hv / a.Hqk);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const size_t ch = (size_t)c * Hv + h;
   const bool l2 = a.use_qk_l2norm != 0;
+  const uint32_t loff = (uint32_t)(32 * (warp & 3)) << 16;
+  const int row = 32 * (warp & 3) + lane;   // this thread's TMEM lane
   if (tid == 0) {
     mbar_init(bar, 1);
     mbar_init(bar_ld, 1);
@@ -1099,39 +1127,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     fence_mbar_init();
   }
   __syncthreads();   // the barriers are initialised before any copy is issued
-  if (tid == 0) {
-    // the operand tiles the producers wrote: S0, dS (32 KB each), U' (16 KB), and the two
-    // 8 KB halves of dX into rows 64-127 of [dO; dX]
-    const uint8_t* s0 = reinterpret_cast<const uint8_t*>(ws.S + ch * ws.sS);
-    const uint8_t* ds = reinterpret_cast<const uint8_t*>(ws.dS + ch * ws.sdS);
-    const uint8_t* ug = reinterpret_cast<const uint8_t*>(ws.U + ch * ws.sU);
-    const uint8_t* xg = reinterpret_cast<const uint8_t*>(ws.dX + ch * ws.sdX);
-    mbar_arrive_expect_tx(bar_ld, 32768 + 32768 + 16384 + 16384);
-    bulk_load(sm + OFF_S0, s0, 32768, bar_ld);
-    bulk_load(sm + OFF_DS, ds, 32768, bar_ld);
-    bulk_load(sm + OFF_U, ug, 16384, bar_ld);
-    bulk_load(sm + OFF_OX + 8192, xg, 8192, bar_ld);
-    bulk_load(sm + OFF_OX + 16384 + 8192, xg + 8192, 8192, bar_ld);
-  } else if (tid == kTmaThread) {
-    // the chunk's q, k rows into [q; k] and its dO rows into rows 0-63 of [dO; dX], by TMA
-    // (64 features x 64 tokens a box, zero past the last token; rows past the chunk end are
-    // cleared below)
-    mbar_arrive_expect_tx(bar_tma, 3 * 16384);
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      tma_load_3d(sm + OFF_QK + hh * 16384, &tmQ, bar_tma, 64 * hh, hq, t0);
-      tma_load_3d(sm + OFF_QK + hh * 16384 + 8192, &tmK, bar_tma, 64 * hh, hq, t0);
-      tma_load_3d(sm + OFF_OX + hh * 16384, &tmO, bar_tma, 64 * hh, h, t0);
-    }
-  }
+  issue_head_loads(sm, ws, &tmQ, &tmK, &tmO, bar_ld, bar_tma, (size_t)c * Hv + hq * grp, hq * grp, hq,
+                   t0, true, tid);
   if (warp == kTmemWarp) {
     tmem_alloc(tslot, T_COLS);
     tmem_relinquish();
   }
-  // the gates (warp 1) and the row dots (warps 2-3) load while warp 0 issues the copies
-  if (warp == 1) load_gates(a, t0, L, h, G, bt, lane);
-  if (tid >= 64 && tid < 128)   // the row dots dX_i . v_i of the reverse pass (slot 0)
-    xvr[tid - 64] = ws.XV[ch * 4 * 64 + tid - 64];
   for (int e = tid; e < 8192 / 16; e += kThreads)      // the zero tile
     reinterpret_cast<uint4*>(sm + OFF_ZERO)[e] = make_uint4(0u, 0u, 0u, 0u);
   for (int e = tid; e < 2 * 8192 / 16; e += kThreads) {   // rows 0-63 of both halves of [0; lambda U']
@@ -1139,334 +1140,380 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     reinterpret_cast<uint4*>(sm + OFF_LU + hlf * 16384)[w] = make_uint4(0u, 0u, 0u, 0u);
   }
   fence_proxy_async_smem();
-  bool ok = true;
-  if (tid == 0) ok = mbar_wait(bar_ld, 0, kWaitNs) && mbar_wait(bar_tma, 0, kWaitNs);   // landed
   tc_fence_before();
-  if (__syncthreads_or(!ok)) {
-    if (tid == 0) report(a.dev_status, GDN_DEV_TIMEOUT);
-    if (warp == kTmemWarp) {
-      tc_fence_after();
-      tmem_dealloc(*tslot, T_COLS);
-    }
-    return;
-  }
+  __syncthreads();
   tc_fence_after();
   const uint32_t tb = *tslot;
-  {  // [q; k] rows normalised in place (thread: one row half, 128 rows x 2 halves); rows past
-     // the chunk end cleared, in [q; k] and in the dO rows
-    const int r = tid >> 1, hh = tid & 1, i = r & 63;
-    uint8_t* rowp = sm + OFF_QK + hh * 16384 + r * 128;
-    float ss = 0.f;
-    // 16-byte chunks in an order rotated by the row (the warp's accesses spread over the
-    // banks), kept in registers for the scaling
-    uint4 u[8];
+  bool ok = true, failed = false;
+  int last = 0;   // the last head whose tiles were requested
+
+  for (int hi = 0; hi < grp; ++hi) {
+    const int h = hq * grp + hi;
+    const size_t ch = (size_t)c * Hv + h;
+    const uint32_t ph = (uint32_t)hi & 1u;   // phase of the head's loads
+    // the gates (warp 1) and the row dots (warps 2-3) load while the copies land
+    if (warp == 1) load_gates(a, t0, L, h, G, bt, lane);
+    if (tid >= 64 && tid < 128)   // the row dots dX_i . v_i of the reverse pass (slot 0)
+      xvr[tid - 64] = ws.XV[ch * 4 * 64 + tid - 64];
+    if (tid == 0) ok = mbar_wait(bar_ld, ph, kWaitNs) && mbar_wait(bar_tma, ph, kWaitNs);   // landed
+    if (__syncthreads_or(!ok)) { failed = true; break; }
+    if (hi == 0) {  // [q; k] rows normalised in place (thread: one row half, 128 rows x 2
+                    // halves), rows past the chunk end cleared
+      const int r = tid >> 1, hh = tid & 1, i = r & 63;
+      uint8_t* rowq = sm + OFF_QK + hh * 16384 + r * 128;
+      float ss = 0.f;
+      // 16-byte chunks in an order rotated by the row (the warp's accesses spread over the
+      // banks), kept in registers for the scaling
+      uint4 u[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) u[j] = *reinterpret_cast<const uint4*>(rowp + 16 * ((j + r) & 7));
+      for (int j = 0; j < 8; ++j) u[j] = *reinterpret_cast<const uint4*>(rowq + 16 * ((j + r) & 7));
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t w[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[q]));
-        ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
-      }
-    }
-    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-    const float rn = i < L ? (l2 ? 1.0f / sqrtf(ss + kL2Eps) : 1.f) : 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(rowp + 16 * ((j + r) & 7)) = scaled8(u[j], rn);
-    for (int e = tid; e < 2 * 64 * 8; e += kThreads) {
-      const int hf = e >> 9, ii = (e >> 3) & 63, c8 = e & 7;
-      if (ii >= L)
-        *reinterpret_cast<uint4*>(sm + OFF_OX + hf * 16384 + ii * 128 + 16 * c8) = make_uint4(0u, 0u, 0u, 0u);
-    }
-  }
-  fence_proxy_async_smem();
-  __syncthreads();
-  // ---- R1, R2, R3 (issued first: the dot below runs meanwhile)
-  if (tid == 0) {
-    const uint32_t i1 = idesc_bf16(128, 256, false, true), i2 = idesc_bf16(128, 64, false, false);
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
-      mma_bf16(tb + T_R1, kdesc(sb + OFF_QK + ko), mndesc(sb + OFF_S0 + ks * 2048, 16384), i1, ks > 0);
-      mma_bf16(tb + T_R2, kdesc(sb + OFF_OX + ko),
-               kdesc(sb + OFF_U + (ks >> 2) * 8192 + (ks & 3) * 32), i2, ks > 0);
-      mma_bf16(tb + T_R3, kdesc(sb + OFF_QK + ko), kdesc(sb + OFF_QK + 8192 + ko), i2, ks > 0);
-    }
-    mma_commit(bar);
-  }
-  if (warp > 0) {  // <S0, dS> over the two tiles (same layout, element by element), by the
-                   // warps that do not issue the products
-    float sd = 0.f;
-    const uint4* p0 = reinterpret_cast<const uint4*>(sm + OFF_S0);
-    const uint4* p1 = reinterpret_cast<const uint4*>(sm + OFF_DS);
-#pragma unroll 4
-    for (int e = tid - 32; e < 32768 / 16; e += kThreads - 32) {
-      const uint4 u0 = p0[e], u1 = p1[e];
-      const uint32_t w0[4] = {u0.x, u0.y, u0.z, u0.w}, w1[4] = {u1.x, u1.y, u1.z, u1.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w0[q]));
-        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w1[q]));
-        sd = fmaf(f0.x, f1.x, fmaf(f0.y, f1.y, sd));
-      }
-    }
-    sd = warp_sum(sd);
-    if (lane == 0) red[warp] = sd;
-  }
-  if (tid < 64) {
-    gm[tid] = expf(G[tid]);
-    lm[tid] = expf(G[L - 1] - G[tid]);
-    g2[tid] = G[tid] * kLog2eG;   // base-2 log-decay for the F / E factors
-  }
-  if (tid == 0) ok = mbar_wait(bar, 0, kWaitNs);
-  if (__syncthreads_or(!ok)) {
-    if (tid == 0) report(a.dev_status, GDN_DEV_TIMEOUT);
-    tc_fence_before();
-    __syncthreads();
-    if (warp == kTmemWarp) tmem_dealloc(tb, T_COLS);
-    return;
-  }
-  tc_fence_after();
-  const uint32_t loff = (uint32_t)(32 * (warp & 3)) << 16;
-  const int row = 32 * (warp & 3) + lane;   // this thread's TMEM lane
-  // ---- row dots from R1 (warps 0-3: the S0 columns; warps 6-7: the dS columns of k rows)
-  if (warp < 4 || warp >= 6) {   // 8 columns of the bf16 row per 16-byte load
-    const bool s0 = warp < 4;
-    const uint8_t* tile = s0 ? sm + OFF_OX : sm + OFF_U;
-    const uint32_t half = s0 ? 16384u : 8192u;
-    const int r = s0 ? row : row - 64;
-    float acc = 0.f;
-#pragma unroll
-    for (int part = 0; part < 4; ++part) {
-      float x[32];
-      tmem_ld32(tb + loff + T_R1 + (s0 ? 0 : 128) + 32 * part, x);
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int col = 32 * part + 8 * m;
-        const uint4 u = *reinterpret_cast<const uint4*>(tile + (col >> 6) * half + sw128_offset(r, col & 63));
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t w[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[q]));
-          acc = fmaf(x[8 * m + 2 * q], f.x, fmaf(x[8 * m + 2 * q + 1], f.y, acc));
+          ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
         }
       }
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      const float rn = i < L ? (l2 ? 1.0f / sqrtf(ss + kL2Eps) : 1.f) : 0.f;
+      if (hh == 0) rnv[r] = rn;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(rowq + 16 * ((j + r) & 7)) = scaled8(u[j], rn);
     }
-    if (!s0) kh3[row - 64] = acc;
-    else if (row < 64) qh1[row] = acc;
-    else kh2[row - 64] = acc;
-  }
-  __syncthreads();
-  // ---- R4's scaled operands: [scale gamma dO; -gamma beta dX] in place, lambda U' rows 64-127
-  {  // (every load of a thread before its stores)
-    uint4 u[8], w[4];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int e = tid + kThreads * k, r = e >> 4, chunk = e & 15;
-      u[k] = *reinterpret_cast<const uint4*>(sm + OFF_OX + (chunk >> 3) * 16384 + r * 128 + (chunk & 7) * 16);
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int e = tid + kThreads * k, i = e >> 4, chunk = e & 15;
-      w[k] = *reinterpret_cast<const uint4*>(sm + OFF_U + (chunk >> 3) * 8192 + i * 128 + (chunk & 7) * 16);
-    }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int e = tid + kThreads * k, r = e >> 4, chunk = e & 15;
-      const float s = r < 64 ? a.scale * gm[r] : -gm[r - 64] * bt[r - 64];
-      *reinterpret_cast<uint4*>(sm + OFF_OX + (chunk >> 3) * 16384 + r * 128 + (chunk & 7) * 16) = scaled8(u[k], s);
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {   // (U' and [0; lambda U'] share the swizzle: row i = 64 + i mod 8)
-      const int e = tid + kThreads * k, i = e >> 4, chunk = e & 15;
-      *reinterpret_cast<uint4*>(sm + OFF_LU + (chunk >> 3) * 16384 + (64 + i) * 128 + (chunk & 7) * 16) =
-          scaled8(w[k], lm[i]);
-    }
-  }
-  // ---- F (rows i < 64 of R2 / R3) and E (rows 64-127), all eight warps at once: a warp
-  //      reaches the TMEM lanes 32 (warp % 4) .. + 31 and takes the column half warp / 4
-  {
-    float* rowp = dGv;          // [2 column halves][128 rows] partial row sums of Z (dGv and om
-                                // are free until the last phase)
-    float* colp = reinterpret_cast<float*>(sm + OFF_U);   // [4 row quarters][64] (U' is dead)
-    float* dbp = colp + 256;    // [2][64] partial dbeta terms
-    const int part = warp >> 2;
-    float x[32], y[32], v[32];
-    tmem_ld32(tb + loff + T_R2 + 32 * part, x);   // dO U'^T or dX U'^T
-    tmem_ld32(tb + loff + T_R3 + 32 * part, y);   // Q K^T or K K^T
-    float racc = 0.f, db = 0.f;
-    float fe[32];
-    if (row < 64) {   // F = scale (dO U'^T) * Gamma on and below the diagonal
-      const int i = row;
-      const float gi = g2[i];
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
-        const int j = 32 * part + jj;
-        const float e = a.scale * x[jj] * ex2g(gi - g2[j]);
-        fe[jj] = j <= i ? e : 0.f;
-        v[jj] = fe[jj] * y[jj];
-        racc += v[jj];
-      }
-    } else {          // dA = -(dX U'^T) strictly below, E = beta dA * Gamma
-      const int i = row - 64;
-      const float gi = g2[i];
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
-        const int j = 32 * part + jj;
-        const float e2 = ex2g(gi - g2[j]);
-        const float gij = j < i ? e2 : 0.f;
-        const float dA = -x[jj];
-        fe[jj] = bt[i] * gij * dA;
-        v[jj] = fe[jj] * y[jj];
-        racc += v[jj];
-        db = fmaf(dA * gij, y[jj], db);
-      }
-      dbp[part * 64 + i] = db;
-    }
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {   // the F / E row as bf16, 8 columns per 16-byte store
-      uint4 u;
-      u.x = pack2(fe[8 * m], fe[8 * m + 1]);
-      u.y = pack2(fe[8 * m + 2], fe[8 * m + 3]);
-      u.z = pack2(fe[8 * m + 4], fe[8 * m + 5]);
-      u.w = pack2(fe[8 * m + 6], fe[8 * m + 7]);
-      *reinterpret_cast<uint4*>(sm + OFF_FE + sw128_offset(row, 32 * part + 8 * m)) = u;
-    }
-    rowp[part * 128 + row] = racc;
-    // column sums over this warp's 32 rows: a transpose-reduce across the lanes (31 shuffles);
-    // lane l ends with the sum of column 32 part + l
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-      const bool up = (lane & o) != 0;
-#pragma unroll
-      for (int k = 0; k < o; ++k) {
-        const float send = up ? v[k] : v[k + o];
-        const float keep = up ? v[k + o] : v[k];
-        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    if (L < C) {   // dO rows past the chunk end (the next sequence's) cleared
+      for (int e = tid; e < 2 * 64 * 8; e += kThreads) {
+        const int hf = e >> 9, ii = (e >> 3) & 63, c8 = e & 7;
+        if (ii >= L)
+          *reinterpret_cast<uint4*>(sm + OFF_OX + hf * 16384 + ii * 128 + 16 * c8) = make_uint4(0u, 0u, 0u, 0u);
       }
     }
-    colp[(warp & 3) * 64 + 32 * part + lane] = v[0];
-  }
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (tid < 64) {   // per-token sums in a fixed order
-    const float* rowp = dGv;
-    const float* colp = reinterpret_cast<const float*>(sm + OFF_U);
-    const float* dbp = colp + 256;
-    const int i = tid;
-    rz[i] = (rowp[i] + rowp[64 + i]) + (rowp[128 + i] + rowp[192 + i]);
-    dba[i] = dbp[i] + dbp[64 + i];
-    cs[i] = (colp[i] + colp[64 + i]) + (colp[128 + i] + colp[192 + i]);
-  }
-  // ---- R4 = [dQ; dK]
-  if (tid == 0) {
-    const uint32_t i4 = idesc_bf16(128, 128, false, false), i4c = idesc_bf16(128, 128, false, true);
-    const uint32_t i4d = idesc_bf16(128, 128, true, true);
-#pragma unroll
-    for (int ks = 0; ks < 16; ++ks) {   // [scale gamma dO | 0 ; -gamma beta dX | lambda U'] [S0 | dS]^T
-      const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
-      mma_bf16(tb + T_R4, kdesc(sb + OFF_OX + ko), kdesc(sb + OFF_S0 + ko), i4, ks > 0);
-    }
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      // [F; E] K
-      mma_bf16(tb + T_R4, kdesc(sb + OFF_FE + ks * 32), mndesc(sb + OFF_QK + 8192 + ks * 2048, 16384), i4c, 1);
-      // [0; F^T] Q
-      mma_bf16(tb + T_R4, mndesc(sb + OFF_ZERO + ks * 2048, OFF_FE - OFF_ZERO),
-               mndesc(sb + OFF_QK + ks * 2048, 16384), i4d, 1);
-      // [0; E^T] K
-      mma_bf16(tb + T_R4, mndesc(sb + OFF_ZERO + ks * 2048, OFF_FE + 8192 - OFF_ZERO),
-               mndesc(sb + OFF_QK + 8192 + ks * 2048, 16384), i4d, 1);
-    }
-    mma_commit(bar);
-  }
-  if (tid == 0) ok = mbar_wait(bar, 1, kWaitNs);
-  if (__syncthreads_or(!ok)) {
-    if (tid == 0) report(a.dev_status, GDN_DEV_TIMEOUT);
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (warp == kTmemWarp) tmem_dealloc(tb, T_COLS);
+    tc_fence_after();
+    // ---- R1, R2 (and R3 for the first head), issued first: the dot below runs meanwhile
+    if (tid == 0) {
+      const uint32_t i1 = idesc_bf16(128, 256, false, true), i2 = idesc_bf16(128, 64, false, false);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
+        mma_bf16(tb + T_R1, kdesc(sb + OFF_QK + ko), mndesc(sb + OFF_S0 + ks * 2048, 16384), i1, ks > 0);
+        mma_bf16(tb + T_R2, kdesc(sb + OFF_OX + ko),
+                 kdesc(sb + OFF_U + (ks >> 2) * 8192 + (ks & 3) * 32), i2, ks > 0);
+        if (hi == 0)
+          mma_bf16(tb + T_R3, kdesc(sb + OFF_QK + ko), kdesc(sb + OFF_QK + 8192 + ko), i2, ks > 0);
+      }
+      mma_commit(bar);
+    }
+    if (warp > 0) {  // <S0, dS> over the two tiles (same layout, element by element), by the
+                     // warps that do not issue the products
+      float sd = 0.f;
+      const uint4* p0 = reinterpret_cast<const uint4*>(sm + OFF_S0);
+      const uint4* p1 = reinterpret_cast<const uint4*>(sm + OFF_DS);
+#pragma unroll 4
+      for (int e = tid - 32; e < 32768 / 16; e += kThreads - 32) {
+        const uint4 u0 = p0[e], u1 = p1[e];
+        const uint32_t w0[4] = {u0.x, u0.y, u0.z, u0.w}, w1[4] = {u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w0[q]));
+          const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w1[q]));
+          sd = fmaf(f0.x, f1.x, fmaf(f0.y, f1.y, sd));
+        }
+      }
+      sd = warp_sum(sd);
+      if (lane == 0) red[warp] = sd;
+    }
+    if (tid < 64) {
+      gm[tid] = expf(G[tid]);
+      lm[tid] = expf(G[L - 1] - G[tid]);
+      g2[tid] = G[tid] * kLog2eG;   // base-2 log-decay for the F / E factors
+    }
+    if (tid == 0) ok = mbar_wait(bar, 0, kWaitNs);
+    if (__syncthreads_or(!ok)) { failed = true; break; }
+    tc_fence_after();
+    // ---- row dots from R1 (warps 0-3: the S0 columns; warps 6-7: the dS columns of k rows)
+    if (warp < 4 || warp >= 6) {   // 8 columns of the bf16 row per 16-byte load
+      const bool s0 = warp < 4;
+      const uint8_t* tile = s0 ? sm + OFF_OX : sm + OFF_U;
+      const uint32_t half = s0 ? 16384u : 8192u;
+      const int r = s0 ? row : row - 64;
+      float acc = 0.f;
+#pragma unroll
+      for (int part = 0; part < 4; ++part) {
+        float x[32];
+        tmem_ld32(tb + loff + T_R1 + (s0 ? 0 : 128) + 32 * part, x);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int col = 32 * part + 8 * m;
+          const uint4 u = *reinterpret_cast<const uint4*>(tile + (col >> 6) * half + sw128_offset(r, col & 63));
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[q]));
+            acc = fmaf(x[8 * m + 2 * q], f.x, fmaf(x[8 * m + 2 * q + 1], f.y, acc));
+          }
+        }
+      }
+      if (!s0) kh3[row - 64] = acc;
+      else if (row < 64) qh1[row] = acc;
+      else kh2[row - 64] = acc;
+    }
+    __syncthreads();
+    // ---- R4's scaled operands: [scale gamma dO; -gamma beta dX] in place, lambda U' rows
+    //      64-127 (every load of a thread before its stores)
+    {
+      uint4 u[8], w[4];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int e = tid + kThreads * k, r = e >> 4, chunk = e & 15;
+        u[k] = *reinterpret_cast<const uint4*>(sm + OFF_OX + (chunk >> 3) * 16384 + r * 128 + (chunk & 7) * 16);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int e = tid + kThreads * k, i = e >> 4, chunk = e & 15;
+        w[k] = *reinterpret_cast<const uint4*>(sm + OFF_U + (chunk >> 3) * 8192 + i * 128 + (chunk & 7) * 16);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int e = tid + kThreads * k, r = e >> 4, chunk = e & 15;
+        const float s = r < 64 ? a.scale * gm[r] : -gm[r - 64] * bt[r - 64];
+        *reinterpret_cast<uint4*>(sm + OFF_OX + (chunk >> 3) * 16384 + r * 128 + (chunk & 7) * 16) = scaled8(u[k], s);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {   // (U' and [0; lambda U'] share the swizzle: row i = 64 + i mod 8)
+        const int e = tid + kThreads * k, i = e >> 4, chunk = e & 15;
+        *reinterpret_cast<uint4*>(sm + OFF_LU + (chunk >> 3) * 16384 + (64 + i) * 128 + (chunk & 7) * 16) =
+            scaled8(w[k], lm[i]);
+      }
+    }
+    // ---- F (rows i < 64 of R2 / R3) and E (rows 64-127), all eight warps at once: a warp
+    //      reaches the TMEM lanes 32 (warp % 4) .. + 31 and takes the column half warp / 4
+    {
+      const int part = warp >> 2;
+      float x[32], y[32], v[32];
+      tmem_ld32(tb + loff + T_R2 + 32 * part, x);   // dO U'^T or dX U'^T
+      tmem_ld32(tb + loff + T_R3 + 32 * part, y);   // Q K^T or K K^T
+      float racc = 0.f, db = 0.f;
+      float fe[32];
+      if (row < 64) {   // F = scale (dO U'^T) * Gamma on and below the diagonal
+        const int i = row;
+        const float gi = g2[i];
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int j = 32 * part + jj;
+          const float e = a.scale * x[jj] * ex2g(gi - g2[j]);
+          fe[jj] = j <= i ? e : 0.f;
+          v[jj] = fe[jj] * y[jj];
+          racc += v[jj];
+        }
+      } else {          // dA = -(dX U'^T) strictly below, E = beta dA * Gamma
+        const int i = row - 64;
+        const float gi = g2[i];
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int j = 32 * part + jj;
+          const float e2 = ex2g(gi - g2[j]);
+          const float gij = j < i ? e2 : 0.f;
+          const float dA = -x[jj];
+          fe[jj] = bt[i] * gij * dA;
+          v[jj] = fe[jj] * y[jj];
+          racc += v[jj];
+          db = fmaf(dA * gij, y[jj], db);
+        }
+        dbp[part * 64 + i] = db;
+      }
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {   // the F / E row as bf16, 8 columns per 16-byte store
+        uint4 u;
+        u.x = pack2(fe[8 * m], fe[8 * m + 1]);
+        u.y = pack2(fe[8 * m + 2], fe[8 * m + 3]);
+        u.z = pack2(fe[8 * m + 4], fe[8 * m + 5]);
+        u.w = pack2(fe[8 * m + 6], fe[8 * m + 7]);
+        *reinterpret_cast<uint4*>(sm + OFF_FE + sw128_offset(row, 32 * part + 8 * m)) = u;
+      }
+      rowp[part * 128 + row] = racc;
+      // column sums over this warp's 32 rows: a transpose-reduce across the lanes (31 shuffles);
+      // lane l ends with the sum of column 32 part + l
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int k = 0; k < o; ++k) {
+          const float send = up ? v[k] : v[k + o];
+          const float keep = up ? v[k + o] : v[k];
+          v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      }
+      colp[(warp & 3) * 64 + 32 * part + lane] = v[0];
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid < 64) {   // per-token sums in a fixed order
+      const int i = tid;
+      rz[i] = (rowp[i] + rowp[64 + i]) + (rowp[128 + i] + rowp[192 + i]);
+      dba[i] = dbp[i] + dbp[64 + i];
+      cs[i] = (colp[i] + colp[64 + i]) + (colp[128 + i] + colp[192 + i]);
+    }
+    // ---- R4 += [dQ; dK] of this value head
+    if (tid == 0) {
+      const uint32_t i4 = idesc_bf16(128, 128, false, false), i4c = idesc_bf16(128, 128, false, true);
+      const uint32_t i4d = idesc_bf16(128, 128, true, true);
+#pragma unroll
+      for (int ks = 0; ks < 16; ++ks) {   // [scale gamma dO | 0 ; -gamma beta dX | lambda U'] [S0 | dS]^T
+        const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
+        mma_bf16(tb + T_R4, kdesc(sb + OFF_OX + ko), kdesc(sb + OFF_S0 + ko), i4, ks > 0 || hi > 0);
+      }
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        // [F; E] K
+        mma_bf16(tb + T_R4, kdesc(sb + OFF_FE + ks * 32), mndesc(sb + OFF_QK + 8192 + ks * 2048, 16384), i4c, 1);
+        // [0; F^T] Q
+        mma_bf16(tb + T_R4, mndesc(sb + OFF_ZERO + ks * 2048, OFF_FE - OFF_ZERO),
+                 mndesc(sb + OFF_QK + ks * 2048, 16384), i4d, 1);
+        // [0; E^T] K
+        mma_bf16(tb + T_R4, mndesc(sb + OFF_ZERO + ks * 2048, OFF_FE + 8192 - OFF_ZERO),
+                 mndesc(sb + OFF_QK + 8192 + ks * 2048, 16384), i4d, 1);
+      }
+      mma_commit(bar);
+    }
+    if (tid == 0) ok = mbar_wait(bar, 1, kWaitNs);
+    if (__syncthreads_or(!ok)) { failed = true; break; }
+    tc_fence_after();
+    // every operand of this head has been read: the next head's tiles load meanwhile
+    if (hi + 1 < grp) {
+      issue_head_loads(sm, ws, &tmQ, &tmK, &tmO, bar_ld, bar_tma, ch + 1, h + 1, hq, t0, false, tid);
+      last = hi + 1;
+    }
+    // ---- dG, dbeta per token, then dg by a suffix sum
+    if (tid < 64) {
+      const int i = tid;
+      const float omega = i < L ? lm[i] * kh3[i] : 0.f;
+      om[i] = omega;
+      dGv[i] = i < L ? a.scale * gm[i] * qh1[i] - bt[i] * gm[i] * kh2[i] - omega + rz[i] - cs[i] : 0.f;
+      if (i < L) b.dbeta[(size_t)(t0 + i) * Hv + h] = xvr[i] - gm[i] * kh2[i] + dba[i];
+    }
+    __syncthreads();
+    if (warp == 0) {
+      float sdt = 0.f;
+      for (int w = 1; w < kThreads / 32; ++w) sdt += red[w];
+      const float omsum = warp_sum(om[lane] + om[lane + 32]);
+      float x0 = dGv[lane], x1 = dGv[lane + 32];
+      const float extra = gm[L - 1] * sdt + omsum;
+      if (lane == L - 1) x0 += extra;
+      if (lane + 32 == L - 1) x1 += extra;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y0 = __shfl_down_sync(0xffffffffu, x0, o);
+        const float y1 = __shfl_down_sync(0xffffffffu, x1, o);
+        if (lane + o < 32) { x0 += y0; x1 += y1; }
+      }
+      x0 += __shfl_sync(0xffffffffu, x1, 0);
+      const size_t base = (size_t)t0 * Hv + h;
+      if (lane < L) b.dg[base + (size_t)lane * Hv] = x0;
+      if (lane + 32 < L) b.dg[base + (size_t)(lane + 32) * Hv] = x1;
+    }
+    __syncthreads();   // the per-token vectors are read before the next head rewrites them
+  }
+  if (failed) {
+    if (tid == 0) {   // copies still in flight land before the shared memory is released
+      mbar_wait(bar_ld, (uint32_t)last & 1u, kWaitNs);
+      report(a.dev_status, GDN_DEV_TIMEOUT);
+    } else if (tid == kTmaThread) {
+      mbar_wait(bar_tma, (uint32_t)last & 1u, kWaitNs);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kTmemWarp) {
+      tc_fence_after();
+      tmem_dealloc(tb, T_COLS);
+    }
     return;
   }
-  tc_fence_after();
-  {  // [dQ; dK] rows to the per-value-head scratch: R4 staged by all eight warps (two column
-     // parts each) as 32-column fp32 boxes, 128-byte swizzled, in the operand space the products
-     // no longer read (dQ rows: boxes 0-3, dK rows: boxes 4-7, 8 KB each)
-    const int i = row & 63;
-    uint8_t* rbase = sm + OFF_S0 + (row >> 6) * 32768 + i * 128;
-#pragma unroll 1
-    for (int part = 2 * (warp >> 2); part < 2 * (warp >> 2) + 2; ++part) {
-      float x[32];
-      tmem_ld32(tb + loff + T_R4 + 32 * part, x);
+  // ---- dq, dk: the L2 norm's Jacobian on the group sums in R4 (rows 0-63: q, 64-127: k),
+  //      dx = r (dx^ - x^ (x^ . dx^)) with x^ the normalised row in [q; k]; warp group g takes
+  //      the columns 64 g .. 64 g + 63 (the k-half g of [q; k]) and the halves' partial dots
+  //      meet in shared memory.  The bf16 rows are staged (128-byte-swizzled [64 tokens][64
+  //      features] halves: dq at OFF_S0, dk at OFF_S0 + 16 KB) for TMA stores.
+  {
+    const int g = warp >> 2, i = row & 63;
+    float* pd = colp;   // [2][128]
+    const uint8_t* xrow = sm + OFF_QK + g * 16384 + row * 128;
+    float d0[32], d1[32];   // the row's 64 columns of R4
+    tmem_ld32(tb + loff + T_R4 + 64 * g, d0);
+    tmem_ld32(tb + loff + T_R4 + 64 * g + 32, d1);
+    float xh[64];
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        *reinterpret_cast<float4*>(rbase + part * 8192 + ((q ^ (i & 7)) << 4)) =
-            make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+    for (int c8 = 0; c8 < 8; ++c8) {   // the row's 16-byte chunk c8 sits at c8 ^ (row % 8)
+      const uint4 u = *reinterpret_cast<const uint4*>(xrow + ((c8 ^ (row & 7)) << 4));
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[q]));
+        xh[8 * c8 + 2 * q] = f.x;
+        xh[8 * c8 + 2 * q + 1] = f.y;
+      }
+    }
+    float p = 0.f;
+#pragma unroll
+    for (int e = 0; e < 64; ++e) p = fmaf(xh[e], e < 32 ? d0[e] : d1[e - 32], p);
+    pd[g * 128 + row] = p;
+    __syncthreads();
+    const float r = rnv[row];
+    const float xd = pd[row] + pd[128 + row];
+    uint8_t* srow = sm + OFF_S0 + (row >> 6) * 16384 + g * 8192 + i * 128;
+#pragma unroll
+    for (int c8 = 0; c8 < 8; ++c8) {
+      float o[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int k = 8 * c8 + e;
+        const float dk = k < 32 ? d0[k] : d1[k - 32];
+        o[e] = l2 ? r * fmaf(-xd, xh[k], dk) : dk;
+      }
+      uint4 u;
+      u.x = pack2(o[0], o[1]);
+      u.y = pack2(o[2], o[3]);
+      u.z = pack2(o[4], o[5]);
+      u.w = pack2(o[6], o[7]);
+      *reinterpret_cast<uint4*>(srow + ((c8 ^ (i & 7)) << 4)) = u;
     }
   }
   fence_proxy_async_smem();
   tc_fence_before();
-  __syncthreads();
-  if (L == C) {   // eight TMA stores
-    if (tid == kTmaThread) {
-#pragma unroll
-      for (int part = 0; part < 4; ++part) {
-        tma_store_3d(&tmDQ, sm + OFF_S0 + part * 8192, 32 * part, h, t0);
-        tma_store_3d(&tmDK, sm + OFF_S0 + 32768 + part * 8192, 32 * part, h, t0);
-      }
-      tma_store_commit();
-    }
-  } else {   // a chunk ending early: rows i < L only (the next ones are another sequence's)
-    for (int e = tid; e < 2 * 64 * 32; e += kThreads) {
-      const int hf = e >> 11, i = (e >> 5) & 63, part = (e >> 3) & 3, q = e & 7;
-      if (i < L)
-        *reinterpret_cast<float4*>((hf ? ws.dK : ws.dQ) + ((size_t)(t0 + i) * Hv + h) * 128 + 32 * part + 4 * q) =
-            *reinterpret_cast<const float4*>(sm + OFF_S0 + hf * 32768 + part * 8192 + i * 128 + ((q ^ (i & 7)) << 4));
-    }
-  }
-  // ---- dG, dbeta per token, then dg by a suffix sum
-  if (tid < 64) {
-    const int i = tid;
-    const float omega = i < L ? lm[i] * kh3[i] : 0.f;
-    om[i] = omega;
-    dGv[i] = i < L ? a.scale * gm[i] * qh1[i] - bt[i] * gm[i] * kh2[i] - omega + rz[i] - cs[i] : 0.f;
-    if (i < L) b.dbeta[(size_t)(t0 + i) * Hv + h] = xvr[i] - gm[i] * kh2[i] + dba[i];
-  }
-  if (tid == kTmaThread) tma_store_wait_read();   // the staged rows have left shared memory
   __syncthreads();
   if (warp == kTmemWarp) {
     tc_fence_after();
     tmem_dealloc(tb, T_COLS);
   }
-  if (warp == 0) {
-    float sdt = 0.f;
-    for (int w = 1; w < kThreads / 32; ++w) sdt += red[w];
-    const float omsum = warp_sum(om[lane] + om[lane + 32]);
-    float x0 = dGv[lane], x1 = dGv[lane + 32];
-    const float extra = gm[L - 1] * sdt + omsum;
-    if (lane == L - 1) x0 += extra;
-    if (lane + 32 == L - 1) x1 += extra;
+  if (L == C) {   // four TMA stores
+    if (tid == kTmaThread) {
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y0 = __shfl_down_sync(0xffffffffu, x0, o);
-      const float y1 = __shfl_down_sync(0xffffffffu, x1, o);
-      if (lane + o < 32) { x0 += y0; x1 += y1; }
+      for (int hh = 0; hh < 2; ++hh) {
+        tma_store_3d(&tmDQ, sm + OFF_S0 + hh * 8192, 64 * hh, hq, t0);
+        tma_store_3d(&tmDK, sm + OFF_S0 + 16384 + hh * 8192, 64 * hh, hq, t0);
+      }
+      tma_store_commit();
+      tma_store_wait_read();   // the staged rows have left shared memory
     }
-    x0 += __shfl_sync(0xffffffffu, x1, 0);
-    const size_t base = (size_t)t0 * Hv + h;
-    if (lane < L) b.dg[base + (size_t)lane * Hv] = x0;
-    if (lane + 32 < L) b.dg[base + (size_t)(lane + 32) * Hv] = x1;
+  } else {   // a chunk ending early: rows i < L only (the next ones are another sequence's)
+    for (int e = tid; e < 2 * 64 * 16; e += kThreads) {
+      const int hf = e >> 10, i = (e >> 4) & 63, hh = (e >> 3) & 1, c8 = e & 7;
+      if (i < L)
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(hf ? b.dk : b.dq) +
+                                  (((size_t)(t0 + i) * Hqk + hq) * 128 + 64 * hh + 8 * c8) * 2) =
+            *reinterpret_cast<const uint4*>(sm + OFF_S0 + hf * 16384 + hh * 8192 + i * 128 + ((c8 ^ (i & 7)) << 4));
+    }
   }
 }
 }  // namespace tcg
 
 namespace tcp {
 using namespace sm100;
-using tcg::put4;
 using tcg::kdesc;
 constexpr int kThreads = 256;
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -2271,6 +2318,37 @@ __global__ void __launch_bounds__(kQkThreads) bwd_qk_kernel(const ChunkArgs a, c
   }
 }
 
+// Tokens outside every sequence (past cu_seqlens[N], or every token when cu_seqlens is
+// invalid) get zero gradients: dq, dk and the group's dv, dg, dbeta.  The tensor-core path's
+// passes write every token inside a sequence; this one clears the rest, one warp per (token,
+// query/key head) in a grid-stride loop.
+constexpr int kUncoveredBlocks = 256;
+__global__ void __launch_bounds__(kQkThreads) bwd_uncovered_kernel(const ChunkArgs a, const BwdArgs b,
+                                                                   BwdWs ws, int T_total) {
+  const int N = a.num_seqs, K = a.K, V = a.V, grp = a.Hv / a.Hqk;
+  int covered = 0;
+  if (ws.chunk_off[N + 1]) covered = a.cu_seqlens ? a.cu_seqlens[N] : N * a.T;
+  covered = min(max(covered, 0), T_total);
+  const long long items = (long long)(T_total - covered) * a.Hqk;
+  const long long step = (long long)gridDim.x * (kQkThreads / 32);
+  const int lane = threadIdx.x & 31;
+  const float z[4] = {0.f, 0.f, 0.f, 0.f};
+  for (long long it = (long long)blockIdx.x * (kQkThreads / 32) + (threadIdx.x >> 5); it < items; it += step) {
+    const int t = covered + (int)(it / a.Hqk), hq = (int)(it % a.Hqk);
+    for (int e = 4 * lane; e < K; e += 128) {
+      store4(b.dq, ((size_t)t * a.Hqk + hq) * K + e, a.io_dtype, z);
+      store4(b.dk, ((size_t)t * a.Hqk + hq) * K + e, a.io_dtype, z);
+    }
+    for (int hh = hq * grp; hh < (hq + 1) * grp; ++hh) {
+      for (int e = 4 * lane; e < V; e += 128) store4(b.dv, ((size_t)t * a.Hv + hh) * V + e, a.io_dtype, z);
+      if (lane == 0) {
+        b.dg[(size_t)t * a.Hv + hh] = 0.f;
+        b.dbeta[(size_t)t * a.Hv + hh] = 0.f;
+      }
+    }
+  }
+}
+
 }  // namespace
 
 size_t chunk_bwd_workspace_bytes(int T_total, int num_seqs, int Hv, int K, int V, bool tc) {
@@ -2301,11 +2379,11 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
   chunk_table_kernel<<<1, 1024, 0, a.stream>>>(a, ws.chunk_off);
   if ((err = cudaGetLastError())) return err;
   // Forward recompute of the state entering every chunk and of U'.  bf16 with K = V = 128:
-  // the tensor-core kernel in record mode (its output goes to scratch that the dQ buffer
-  // reuses later); otherwise the fp32 state pass on W, U from the prep kernel.
+  // the tensor-core kernel in record mode (no output); otherwise the fp32 state pass on W, U
+  // from the prep kernel.
   if (tc && T_total > 0) {
     ChunkArgs f = a;
-    f.o = ws.dQ;   // [T_total][Hv][V] bf16 fits in [T_total][Hv][K] fp32
+    f.o = nullptr;
     f.rec_states = ws.S;
     f.rec_u = ws.U;
     f.rec_chunk_off = ws.chunk_off;
@@ -2316,6 +2394,7 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
     if ((err = launch_chunk_states(a, ws.chunk_off, ws.W, ws.U, ws.G, ws.S))) return err;
   }
   if (tc && NC * a.Hv > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  if (tc && a.Hv % a.Hqk != 0) return cudaErrorInvalidValue;
   if (NC > 0) {
     if (tc) {
       CUtensorMap pq, pk;
@@ -2361,20 +2440,25 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
       memset(&gdq, 0, sizeof(gdq));
       memset(&gdk, 0, sizeof(gdk));
       if (!encode_rows_map_bf16(&gq, a.q, a.Hqk, T_total) || !encode_rows_map_bf16(&gk, a.k, a.Hqk, T_total) ||
-          !encode_rows_map_bf16(&go, b.d_o, a.Hv, T_total) || !encode_rows_map_f32(&gdq, ws.dQ, a.Hv, T_total) ||
-          !encode_rows_map_f32(&gdk, ws.dK, a.Hv, T_total))
+          !encode_rows_map_bf16(&go, b.d_o, a.Hv, T_total) || !encode_rows_map_bf16(&gdq, b.dq, a.Hqk, T_total) ||
+          !encode_rows_map_bf16(&gdk, b.dk, a.Hqk, T_total))
         return cudaErrorInvalidValue;
-      tcg::bwd_grad_tc_kernel<<<(unsigned)(NC * a.Hv), tcg::kThreads, tcg::SMEM, a.stream>>>(gq, gk, go, gdq, gdk, a, b, ws);
+      // one CTA per (chunk, query/key head)
+      tcg::bwd_grad_tc_kernel<<<(unsigned)(NC * a.Hqk), tcg::kThreads, tcg::SMEM, a.stream>>>(gq, gk, go, gdq, gdk, a, b, ws);
     } else {
       bwd_grad_kernel<<<dim3((unsigned)NC, a.Hv), kGradThreads, kGradSmem, a.stream>>>(a, b, ws);
     }
     if ((err = cudaGetLastError())) return err;
   }
   if (T_total > 0) {
-    const long long items = (long long)T_total * a.Hqk;
-    const long long blocks = (items + kQkThreads / 32 - 1) / (kQkThreads / 32);
-    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    bwd_qk_kernel<<<(unsigned)blocks, kQkThreads, 0, a.stream>>>(a, b, ws, T_total);
+    if (tc) {   // the grad pass wrote dq, dk of every token in a sequence; clear the rest
+      bwd_uncovered_kernel<<<kUncoveredBlocks, kQkThreads, 0, a.stream>>>(a, b, ws, T_total);
+    } else {
+      const long long items = (long long)T_total * a.Hqk;
+      const long long blocks = (items + kQkThreads / 32 - 1) / (kQkThreads / 32);
+      if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+      bwd_qk_kernel<<<(unsigned)blocks, kQkThreads, 0, a.stream>>>(a, b, ws, T_total);
+    }
     if ((err = cudaGetLastError())) return err;
   }
   return cudaSuccess;

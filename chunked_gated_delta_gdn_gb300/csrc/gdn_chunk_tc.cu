@@ -660,9 +660,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     init = a.initial_state ? a.initial_state + st_off : nullptr;
     fin = a.final_state ? a.final_state + st_off : nullptr;
   }
-  if (padding) {   // padding sequence: zero rows, no state access
+  if (padding) {   // padding sequence: zero rows (no output in record mode), no state access
     __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.o);
-    for (int e = tid; e < (eos - bos) * DV; e += kTcThreads) {
+    for (int e = tid; !kRecord && e < (eos - bos) * DV; e += kTcThreads) {
       const int t = e / DV, d = e - t * DV;
       o[((size_t)(bos + t) * a.Hv + h) * DV + d] = __float2bfloat16_rn(0.f);
     }
@@ -764,18 +764,6 @@ bool encode_rows_map_bf16(CUtensorMap* m, const void* base, int H, int T_total) 
   return encode_map(m, base, H, T_total);
 }
 
-bool encode_rows_map_f32(CUtensorMap* m, const void* base, int H, int T_total) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)T_total};
-  cuuint64_t strides[2] = {128 * 4, (cuuint64_t)H * 128 * 4};
-  cuuint32_t box[3] = {32, 1, 64};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool chunk_tc_supported(int K, int V, int io_dtype, int beta_dtype) {
   return K == DK && V == DV && io_dtype == GDN_BF16 &&
          (beta_dtype == GDN_BF16 || beta_dtype == GDN_F32);
@@ -789,9 +777,9 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a) {
   memset(&mk, 0, sizeof(mk));
   memset(&mv, 0, sizeof(mv));
   memset(&mo, 0, sizeof(mo));
-  if (T_total > 0) {
+  if (T_total > 0) {   // (record mode writes no output: no map for it)
     if (!encode_map(&mq, a.q, a.Hqk, T_total) || !encode_map(&mk, a.k, a.Hqk, T_total) ||
-        !encode_map(&mv, a.v, a.Hv, T_total) || !encode_map(&mo, a.o, a.Hv, T_total))
+        !encode_map(&mv, a.v, a.Hv, T_total) || (!rec && !encode_map(&mo, a.o, a.Hv, T_total)))
       return cudaErrorInvalidValue;
   }
   // the shared-memory attribute, set once per device and kernel

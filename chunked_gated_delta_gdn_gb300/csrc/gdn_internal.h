@@ -150,9 +150,6 @@ bool chunk_tc_supported(int K, int V, int io_dtype, int beta_dtype);
 // TMA map of a [T_total, H, 128] bf16 tensor with 64 x 1 x 64 boxes (64 features of one head
 // for 64 tokens, 128-byte swizzled), zero fill past the last token.
 bool encode_rows_map_bf16(CUtensorMap* m, const void* base, int H, int T_total);
-// The same for a [T_total, H, 128] fp32 tensor with 32 x 1 x 64 boxes (32 features, 128 bytes a
-// row, 128-byte swizzled).
-bool encode_rows_map_f32(CUtensorMap* m, const void* base, int H, int T_total);
 cudaError_t launch_chunk_tc(const ChunkArgs& a);
 // The planned forward (a.workspace): sequences sorted longest first, and, when the batch has
 // too few (sequence, head) chains to fill the GPU, sequences of at least 2 s chunks split into

@@ -71,6 +71,9 @@ CASES = {
     # tensor-core path without an initial state or a final-state gradient
     "bf16_no_init_no_dfinal": dict(B=1, T=200, Hqk=2, Hv=4, K=128, V=128, dtype=torch.bfloat16,
                                    init="none", seed=3115),
+    # tensor-core path with four value heads per query/key head (one grad CTA sums them all)
+    "bf16_group_of_four": dict(lengths=[190, 64, 33], Hqk=1, Hv=4, K=128, V=128,
+                               dtype=torch.bfloat16, init="randn", seed=3117),
     # tensor-core path without the in-kernel norm (unit-norm rows given), explicit scale
     "bf16_no_l2": dict(B=1, T=130, Hqk=1, Hv=2, K=128, V=128, dtype=torch.bfloat16,
                        init="randn", use_qk_l2norm=False, scale=0.2, seed=3116),
