@@ -33,17 +33,21 @@
 // CUDA cores.
 //   1. chunk table  from cu_seqlens, on the device
 //   2. states       the forward recompute of the state entering every chunk and of U':
-//                   tensor cores: the forward kernel in record mode (bf16 operand tiles);
+//                   tensor cores: the forward kernel in record mode (bf16 operand tiles, and
+//                   for the reverse pass T^T, P and its per-token vectors);
 //                   CUDA cores: the prep and state passes of the fp32 chunk path
-//   3. prep         per (chunk, value head): T = (I + A)^{-1}; tensor cores: P and T as bf16
-//                   tiles; CUDA cores: T, dUp = scale P^T dO, Z = scale Q^T diag(gamma) dO
+//   3. prep         CUDA cores only, per (chunk, value head): T = (I + A)^{-1},
+//                   dUp = scale P^T dO, Z = scale Q^T diag(gamma) dO
 //   4. reverse      chunks last to first, recording dS (the gradient of each chunk's exit
 //                   state) and dX, writing dv and the row dots dX_i . v_i; tensor cores: one
 //                   CTA per (sequence, value head), dS^T in TMEM; CUDA cores: per (sequence,
 //                   value head, 32 columns)
-//   5. grad         per (chunk, value head): dbeta, dg, and dQ, dK per value head
-//   6. qk           per (token, query/key head): the group sum and the L2-norm Jacobian
-//                   -> dq, dk; zero gradients for tokens outside every sequence
+//   5. grad         dbeta, dg; tensor cores: per (chunk, query/key head), the group's value
+//                   heads summed in TMEM and the L2-norm Jacobian applied -> dq, dk; CUDA
+//                   cores: per (chunk, value head), dQ, dK per value head
+//   6. qk           CUDA cores: per (token, query/key head), the group sum and the L2-norm
+//                   Jacobian -> dq, dk; zero gradients for tokens outside every sequence
+//                   (tensor cores: only that zeroing)
 #include <string.h>
 
 #include "gdn_chunk_util.cuh"
@@ -78,16 +82,6 @@ struct BwdWs {
   float* dK;           // [T_total][Hv][K]                                   (fp32 path)
   size_t sS, sdS, sU, sdX;   // slot strides (floats) per (chunk, head) of S, dS, U, dX
 };
-
-// The tensor-core path's per-(chunk, value head) vectors in the G slot, written by the prep
-// pass for the reverse pass (zero at tokens past the chunk end):
-//   [kRvCq + i]    scale gamma_i r_q,i      the q rows of the dS update
-//   [kRvW + j]     lambda_j r_k,j           the columns of Y^T = dS^T K^T over raw k rows
-//   [kRvF + i]     -gamma_i beta_i r_k,i    the dX^T operand of the dS update (raw k rows)
-//   [kRvBeta + i]  beta_i                   dv = diag(beta) dX
-//   [kRvGl]        gamma_L = e^{G_{L-1}}    the decay of dS across the chunk
-// with r_q, r_k the l2-norm reciprocals (1 without the norm) and lambda_j = e^{G_{L-1} - G_j}.
-constexpr int kRvCq = 0, kRvW = 64, kRvF = 128, kRvBeta = 192, kRvGl = 256, kRvFloats = 320;
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -1512,327 +1506,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
 }
 }  // namespace tcg
 
-namespace tcp {
-using namespace sm100;
-using tcg::kdesc;
-constexpr int kThreads = 256;
-constexpr uint64_t kWaitNs = 2000000000ull;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr int TD_LD = 20;              // diagonal blocks of T, column-major [4][16][TD_LD]
-constexpr uint32_t OFF_QK = 0;         // [q; k] rows, 2 k-halves x 128 rows x 128 B
-constexpr uint32_t OFF_P = 32768;      // P tile (bf16, scale folded)
-constexpr uint32_t OFF_TT = 40960;     // T tile (bf16)
-constexpr uint32_t OFF_A = 49152;      // A, fp32 [64][64], 16-byte-group swizzled (a_idx)
-constexpr uint32_t OFF_TD = OFF_A + 64 * 64 * 4;
-constexpr uint32_t OFF_VEC = OFF_TD + 4 * 16 * TD_LD * 4;   // G[64], beta[64], row norms [128]
-constexpr uint32_t OFF_BAR = OFF_VEC + 4 * 64 * 4;
-constexpr uint32_t SMEM = OFF_BAR + 64 + 1024;
-constexpr uint32_t T_COLS = 64;
-
-// 2^x on the special-function unit (arguments here are <= 0 where the value is kept).
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-// fp32 A tile: element (i, j) at i * 64 + 4 * ((j / 4) ^ (i % 16)) + j % 4, so that 16-byte
-// groups stay contiguous and the row-parallel accesses of the solve hit distinct banks.
-__device__ __forceinline__ int a_idx(int i, int j) {
-  return i * 64 + ((((j >> 2) ^ (i & 15)) << 2) | (j & 3));
-}
-__device__ __forceinline__ void put_t(uint8_t* tt, int i, int j, float v) {
-  *reinterpret_cast<__nv_bfloat16*>(tt + sw128_offset(i, j)) = __float2bfloat16_rn(v);
-}
-
-// T = (I + A)^{-1} for the strictly lower 64 x 64 A in sA (fp32, a_idx layout), by 16 x 16
-// blocks, into the bf16 tile tt (element (i, j) at sw128_offset(i, j); the caller zeroes it
-// first, so the upper triangle stays zero).  With D_b = (I + A_bb)^{-1} and L = D A_off
-// (block strictly lower, so L^4 = 0): T = (I - L + L^2 - L^3) D.  All 256 threads call it;
-// sTd ([4][16][TD_LD]) is scratch and sA is overwritten.  Fixed summation orders: the result
-// is reproducible.
-__device__ void solve_T_tile(float* sA, float* sTd, uint8_t* tt) {
-  const int tid = threadIdx.x, lane = tid & 31;
-  // step 1: per block row b, one right-looking substitution (I + A_bb) X = R for the
-  //      right-hand sides R = [I | A_b0 | .. | A_b,b-1], one column per thread (16 (b + 1)
-  //      columns in block row b, 160 in all): X = [D_b | L_b0 | ..].  D_b goes to sTd and
-  //      to the diagonal block of T; L_bq replaces A_bq column by column.
-  if (tid < 160) {
-    const int b = tid < 16 ? 0 : (tid < 48 ? 1 : (tid < 96 ? 2 : 3));
-    const int j = tid - 8 * b * (b + 1);            // column of R
-    const bool ident = j < 16;
-    const int cq = j - 16;                          // column of A
-    // A[16 b + i][16 b + m] = ab[i / 4][64 i + 4 ((m / 4) ^ (i % 4)) + m % 4]
-    const float* ab[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) ab[k] = sA + 1024 * b + (((4 * b) ^ (4 * k)) << 2);
-    float x[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = ident ? ((i == j) ? 1.f : 0.f) : sA[a_idx(16 * b + i, cq)];
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {   // columns m = 4 g .. 4 g + 3 of A_bb, one float4 per row
-      float4 ag[16];
-#pragma unroll
-      for (int i = 4 * g + 1; i < 16; ++i)
-        ag[i] = *reinterpret_cast<const float4*>(ab[i >> 2] + 64 * i + ((g ^ (i & 3)) << 2));
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int m = 4 * g + e;
-#pragma unroll
-        for (int i = m + 1; i < 16; ++i) {
-          const float am = e == 0 ? ag[i].x : (e == 1 ? ag[i].y : (e == 2 ? ag[i].z : ag[i].w));
-          x[i] = fmaf(-am, x[m], x[i]);
-        }
-      }
-    }
-    if (!ident) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) sA[a_idx(16 * b + i, cq)] = x[i];
-    } else {
-#pragma unroll
-      for (int i4 = 0; i4 < 4; ++i4)
-        *reinterpret_cast<float4*>(&sTd[(b * 16 + j) * TD_LD + 4 * i4]) =
-            make_float4(x[4 * i4], x[4 * i4 + 1], x[4 * i4 + 2], x[4 * i4 + 3]);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) put_t(tt, 16 * b + i, 16 * b + j, x[i]);   // column j of D_b
-    }
-  }
-  __syncthreads();
-  // step 2: (L^2)_20 = L_21 L_10, (L^2)_31 = L_32 L_21, (L^2)_30 - (L^3)_30 with
-  //      (L^3)_30 = (L^2)_31 L_10; thread (r, c) = (tid / 16, tid % 16), so a half-warp holds
-  //      a whole row of (L^2)_31 and passes it round by shuffles.  Results go to the
-  //      upper-triangle blocks (0, 2), (1, 3), (0, 3) of sA, which nothing else uses.
-  {
-    const int r = tid >> 4, c = tid & 15, hb = lane & 16;
-    float l21r[16], l32r[16], l31r[16];   // rows r of L_21, L_32, L_31
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float4 p = *reinterpret_cast<const float4*>(&sA[(32 + r) * 64 + (((4 + u) ^ r) << 2)]);
-      const float4 q = *reinterpret_cast<const float4*>(&sA[(48 + r) * 64 + (((8 + u) ^ r) << 2)]);
-      const float4 w = *reinterpret_cast<const float4*>(&sA[(48 + r) * 64 + (((4 + u) ^ r) << 2)]);
-      l21r[4 * u] = p.x; l21r[4 * u + 1] = p.y; l21r[4 * u + 2] = p.z; l21r[4 * u + 3] = p.w;
-      l32r[4 * u] = q.x; l32r[4 * u + 1] = q.y; l32r[4 * u + 2] = q.z; l32r[4 * u + 3] = q.w;
-      l31r[4 * u] = w.x; l31r[4 * u + 1] = w.y; l31r[4 * u + 2] = w.z; l31r[4 * u + 3] = w.w;
-    }
-    float l10c[16];
-    float m20 = 0.f, m31 = 0.f, m30 = 0.f;
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      l10c[k] = sA[a_idx(16 + k, c)];
-      m20 = fmaf(l21r[k], l10c[k], m20);
-      m31 = fmaf(l32r[k], sA[a_idx(32 + k, 16 + c)], m31);
-      m30 = fmaf(l31r[k], l10c[k], fmaf(l32r[k], sA[a_idx(32 + k, c)], m30));
-    }
-    float n30 = 0.f;
-#pragma unroll
-    for (int k = 0; k < 16; ++k) n30 = fmaf(__shfl_sync(0xffffffffu, m31, k + hb), l10c[k], n30);
-    sA[a_idx(r, 32 + c)] = m20;
-    sA[a_idx(16 + r, 48 + c)] = m31;
-    sA[a_idx(r, 48 + c)] = m30 - n30;
-  }
-  __syncthreads();
-  // step 3: T_bq = X_bq D_q, X = -L + L^2 - L^3, for the six blocks below the diagonal;
-  //      thread (r, c) computes T_bq[r][c] for all of them
-  {
-    const int r = tid >> 4, c = tid & 15;
-    float dq[3][16];   // column c of D_0, D_1, D_2
-#pragma unroll
-    for (int q = 0; q < 3; ++q)
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float4 d4 = *reinterpret_cast<const float4*>(&sTd[(q * 16 + c) * TD_LD + 4 * u]);
-        dq[q][4 * u] = d4.x; dq[q][4 * u + 1] = d4.y; dq[q][4 * u + 2] = d4.z; dq[q][4 * u + 3] = d4.w;
-      }
-#pragma unroll
-    for (int pr = 0; pr < 6; ++pr) {   // (1,0) (2,0) (3,0) (2,1) (3,1) (3,2)
-      const int b = pr < 3 ? pr + 1 : (pr < 5 ? pr - 1 : 3);
-      const int q = pr < 3 ? 0 : (pr < 5 ? 1 : 2);
-      float xr[16];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float4 l4 = *reinterpret_cast<const float4*>(&sA[(16 * b + r) * 64 + (((4 * q + u) ^ r) << 2)]);
-        xr[4 * u] = -l4.x; xr[4 * u + 1] = -l4.y; xr[4 * u + 2] = -l4.z; xr[4 * u + 3] = -l4.w;
-        if (b - q >= 2) {   // + (L^2 - L^3)_bq, stored at block (q, b)
-          const float4 m4 = *reinterpret_cast<const float4*>(&sA[(16 * q + r) * 64 + (((4 * b + u) ^ r) << 2)]);
-          xr[4 * u] += m4.x; xr[4 * u + 1] += m4.y; xr[4 * u + 2] += m4.z; xr[4 * u + 3] += m4.w;
-        }
-      }
-      float ta = 0.f, tb = 0.f;
-#pragma unroll
-      for (int k = 0; k < 16; k += 2) {
-        ta = fmaf(xr[k], dq[q][k], ta);
-        tb = fmaf(xr[k + 1], dq[q][k + 1], tb);
-      }
-      put_t(tt, 16 * b + r, 16 * q + c, ta + tb);
-    }
-  }
-}
-
-
-__global__ void __launch_bounds__(kThreads, 2) bwd_prep_tc_kernel(
-    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK, const ChunkArgs a,
-    const BwdArgs b, BwdWs ws) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const uint32_t sb = smem_u32(sm);
-  float* sA = reinterpret_cast<float*>(sm + OFF_A);
-  float* sTd = reinterpret_cast<float*>(sm + OFF_TD);
-  float* G = reinterpret_cast<float*>(sm + OFF_VEC);
-  float* bt = G + 64;
-  float* rnv = G + 128;   // r_q (rows 0-63), r_k (rows 64-127); zero past the chunk end
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 8);
-  uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + OFF_BAR + 16);
-  // one CTA per (chunk, value head), heads fastest: the CTAs running together read the
-  // same tokens (adjacent rows), and the two value heads of a query/key head share its
-  // q, k rows through L2
-  const int h = (int)(blockIdx.x % (unsigned)a.Hv), c = (int)(blockIdx.x / (unsigned)a.Hv);
-  int n, t0, L;
-  if (!locate_chunk(a, ws.chunk_off, c, &n, &t0, &L)) return;
-  const int Hv = a.Hv, hq = h / (Hv / a.Hqk);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const size_t ch = (size_t)c * Hv + h;
-  const bool l2 = a.use_qk_l2norm != 0;
-  if (tid == 0) {
-    mbar_init(bar, 1);
-    mbar_init(bar_ld, 1);
-    fence_mbar_init();
-    // the chunk's q, k rows into [q; k] by TMA (64 features x 64 tokens a box, zero past the
-    // last token; rows past the chunk end are cleared below)
-    mbar_arrive_expect_tx(bar_ld, 2 * 16384);
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      tma_load_3d(sm + OFF_QK + hh * 16384, &tmQ, bar_ld, 64 * hh, hq, t0);
-      tma_load_3d(sm + OFF_QK + hh * 16384 + 8192, &tmK, bar_ld, 64 * hh, hq, t0);
-    }
-  }
-  if (warp == 0) {
-    tmem_alloc(tslot, T_COLS);
-    tmem_relinquish();
-  }
-  load_gates(a, t0, L, h, G, bt);
-  // the T tile starts from zero: the solve writes its lower triangle only
-  for (int e = tid; e < 8192 / 16; e += kThreads)
-    reinterpret_cast<uint4*>(sm + OFF_TT)[e] = make_uint4(0u, 0u, 0u, 0u);
-  bool ok = true;
-  if (tid == 0) ok = mbar_wait(bar_ld, 0, kWaitNs);   // the q, k tiles have landed
-  if (__syncthreads_or(!ok)) {
-    if (tid == 0) report(a.dev_status, GDN_DEV_TIMEOUT);
-    if (warp == 0) {
-      tc_fence_after();
-      tmem_dealloc(*tslot, T_COLS);
-    }
-    return;
-  }
-  {  // [q; k] rows normalised in place (thread: one row half, 128 rows x 2 halves), rows past
-     // the chunk end cleared
-    const int r = tid >> 1, hh = tid & 1, i = r & 63;
-    uint8_t* rowp = sm + OFF_QK + hh * 16384 + r * 128;
-    float ss = 0.f;
-    // 16-byte chunks in an order rotated by the row: the warp's accesses spread over the banks
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int c8 = (j + r) & 7;
-      const uint4 u = *reinterpret_cast<const uint4*>(rowp + 16 * c8);
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[q]));
-        ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
-      }
-    }
-    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-    const float rn = i < L ? (l2 ? 1.0f / sqrtf(ss + kL2Eps) : 1.f) : 0.f;
-    if (hh == 0) rnv[r] = rn;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) tcg::scale8(rowp + 16 * ((j + r) & 7), rn);
-  }
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tb = *tslot;
-  if (tid == 0) {   // [Q K^T; K K^T]
-    const uint32_t id = idesc_bf16(128, 64, false, false);
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
-      mma_bf16(tb, kdesc(sb + OFF_QK + ko), kdesc(sb + OFF_QK + 8192 + ko), id, ks > 0);
-    }
-    mma_commit(bar);
-  }
-  if (tid == 0) ok = mbar_wait(bar, 0, kWaitNs);
-  if (__syncthreads_or(!ok)) {
-    if (tid == 0) report(a.dev_status, GDN_DEV_TIMEOUT);
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tb, T_COLS);
-    return;
-  }
-  tc_fence_after();
-  const uint32_t loff = (uint32_t)(32 * (warp & 3)) << 16;
-  const int row = 32 * (warp & 3) + lane;
-  {  // P (rows 0-63, bf16, scale folded) and A (rows 64-127, fp32, a_idx layout); warps w and
-     // w + 4 split the columns.  Rows 0-31 against columns 32-63 lie above the diagonal: zero.
-    const int part = warp >> 2, j0 = 32 * part;
-    const bool zero_tile = ((warp & 1) == 0) && part == 1;
-    float x[32];
-    tmem_ld32(tb + loff + j0, x);
-    const int i = row & 63;
-    const float gi = G[i];
-    const int lim = row < 64 ? i + 1 : i;   // P keeps j <= i, A keeps j < i
-    const float f = row < 64 ? a.scale : bt[i];
-#pragma unroll
-    for (int jj = 0; jj < 32; ++jj) {
-      const int j = j0 + jj;
-      const float e = f * x[jj] * ex2((gi - G[j]) * kLog2e);
-      x[jj] = (!zero_tile && j < lim) ? e : 0.f;
-    }
-    if (row < 64) {
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        uint4 u;
-        u.x = tcg::pack2(x[8 * m], x[8 * m + 1]);
-        u.y = tcg::pack2(x[8 * m + 2], x[8 * m + 3]);
-        u.z = tcg::pack2(x[8 * m + 4], x[8 * m + 5]);
-        u.w = tcg::pack2(x[8 * m + 6], x[8 * m + 7]);
-        *reinterpret_cast<uint4*>(sm + OFF_P + sw128_offset(i, j0 + 8 * m)) = u;
-      }
-    } else {
-#pragma unroll
-      for (int m = 0; m < 8; ++m)
-        *reinterpret_cast<float4*>(&sA[a_idx(i, j0 + 4 * m)]) =
-            make_float4(x[4 * m], x[4 * m + 1], x[4 * m + 2], x[4 * m + 3]);
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0) {
-    tc_fence_after();
-    tmem_dealloc(tb, T_COLS);
-  }
-  solve_T_tile(sA, sTd, sm + OFF_TT);
-  __syncthreads();
-  uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(ws.T + ch * 64 * 64));
-  const uint4* srcT = reinterpret_cast<const uint4*>(sm + OFF_TT);
-  const uint4* srcP = reinterpret_cast<const uint4*>(sm + OFF_P);
-  for (int e = tid; e < 8192 / 16; e += kThreads) {
-    dst[e] = srcT[e];
-    dst[8192 / 16 + e] = srcP[e];
-  }
-  if (tid < 64) {   // the reverse pass's per-token vectors (zero past the chunk end)
-    const int i = tid;
-    const bool in = i < L;
-    const float gi = expf(G[i]), rq = rnv[i], rk = rnv[64 + i];
-    float* rv = ws.G + ch * kRvFloats;
-    rv[kRvCq + i] = in ? a.scale * gi * rq : 0.f;
-    rv[kRvW + i] = in ? ex2((G[L - 1] - G[i]) * kLog2e) * rk : 0.f;
-    rv[kRvF + i] = in ? -gi * bt[i] * rk : 0.f;
-    rv[kRvBeta + i] = in ? bt[i] : 0.f;
-    if (i == 0) rv[kRvGl] = expf(G[L - 1]);
-  }
-}
-}  // namespace tcp
-
 // ---------------------------------------------------------------- 4b. reverse on the tensor cores
 // bf16 I/O with K = V = 128: one CTA (8 warps) per (sequence, value head), chunks last to
 // first, with dS^T (TMEM lane = value index v, column = key index d) resident in TMEM like the
@@ -2147,11 +1820,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (tid == 0) {   // dX^T = dU'^T T
-      const uint32_t ix = idesc_bf16(128, 64, false, true);
+    if (tid == 0) {   // dX^T = dU'^T T (the stage holds T^T: a K-major B operand)
+      const uint32_t ix = idesc_bf16(128, 64, false, false);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_bf16_ta(tb + C_X, tb + C_U + 8 * ks, tcg::mndesc(sst + ST_T + ks * 2048, 8192), ix, ks > 0);
+        mma_bf16_ta(tb + C_X, tb + C_U + 8 * ks, tcg::kdesc(sst + ST_T + ks * 32), ix, ks > 0);
       mma_commit(mmab);
     }
     if (tid == 0) ok = mbar_wait(mmab, ph, kWaitNs);
@@ -2375,7 +2048,6 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
   if ((err = cudaFuncSetAttribute(bwd_reverse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRevSmem))) return err;
   if ((err = cudaFuncSetAttribute(bwd_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGradSmem))) return err;
   if ((err = cudaFuncSetAttribute(tcg::bwd_grad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcg::SMEM))) return err;
-  if ((err = cudaFuncSetAttribute(tcp::bwd_prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcp::SMEM))) return err;
   chunk_table_kernel<<<1, 1024, 0, a.stream>>>(a, ws.chunk_off);
   if ((err = cudaGetLastError())) return err;
   // Forward recompute of the state entering every chunk and of U'.  bf16 with K = V = 128:
@@ -2386,6 +2058,8 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
     f.o = nullptr;
     f.rec_states = ws.S;
     f.rec_u = ws.U;
+    f.rec_tp = ws.T;      // T^T and P for the reverse pass
+    f.rec_vec = ws.G;     // and its per-token vectors
     f.rec_chunk_off = ws.chunk_off;
     if ((err = launch_chunk_tc(f))) return err;
   }
@@ -2395,17 +2069,8 @@ cudaError_t launch_chunk_bwd(const ChunkArgs& a_in, const BwdArgs& b) {
   }
   if (tc && NC * a.Hv > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   if (tc && a.Hv % a.Hqk != 0) return cudaErrorInvalidValue;
-  if (NC > 0) {
-    if (tc) {
-      CUtensorMap pq, pk;
-      memset(&pq, 0, sizeof(pq));
-      memset(&pk, 0, sizeof(pk));
-      if (!encode_rows_map_bf16(&pq, a.q, a.Hqk, T_total) || !encode_rows_map_bf16(&pk, a.k, a.Hqk, T_total))
-        return cudaErrorInvalidValue;
-      tcp::bwd_prep_tc_kernel<<<(unsigned)(NC * a.Hv), tcp::kThreads, tcp::SMEM, a.stream>>>(pq, pk, a, b, ws);
-    }
-    else
-      bwd_prep_kernel<<<dim3((unsigned)NC, a.Hv), kPrepThreads, kPrepSmem, a.stream>>>(a, b, ws);
+  if (NC > 0 && !tc) {   // (the tensor-core path's record-mode forward wrote T, P and the vectors)
+    bwd_prep_kernel<<<dim3((unsigned)NC, a.Hv), kPrepThreads, kPrepSmem, a.stream>>>(a, b, ws);
     if ((err = cudaGetLastError())) return err;
   }
   const unsigned vtiles = (unsigned)((a.V + VT - 1) / VT);

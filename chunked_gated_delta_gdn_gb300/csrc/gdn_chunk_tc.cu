@@ -63,6 +63,7 @@ constexpr uint32_t QK_STAGE = 32768;
 constexpr uint32_t OFF_V = 65536;       // 2 stages x 16 KB: [dv half][64 tokens][128 B]
 constexpr uint32_t V_STAGE = 16384;
 constexpr uint32_t OFF_S = 98304;       // the bf16 output tile staged for its TMA store (16 KB)
+constexpr uint32_t OFF_RT = 114688;     // record mode: T^T and P staged for one bulk copy (16 KB)
 constexpr uint32_t OFF_KT = 131072;     // K~^T: the K rows scaled by exp(G_last - G_t) r_k[t],
                                         // transposed, K-major [128 dk rows][64 tokens] (the B
                                         // operand of the state update; the 8 KB below are free)
@@ -105,6 +106,7 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(OFF_TSLOT + 4 <= SMEM_USED, "barrier block");
 static_assert(QK_STAGE == kQkStageBytes && V_STAGE == kVStageBytes, "stage bytes");
 static_assert(OFF_P + 2 * 8192 <= OFF_REC && OFF_REC + 16384 <= OFF_TW, "record staging");
+static_assert(OFF_S + 16384 <= OFF_RT && OFF_RT + 16384 <= OFF_KT, "record staging of T^T, P");
 
 // Stage timestamps for the per-chunk cycle budget (a diagnostic build, -DGDN_CHUNK_STAMPS):
 // the leader of each group records clock64 at the stage boundaries of chunks 32 .. 95 in the
@@ -141,7 +143,7 @@ __device__ __forceinline__ int wu_bar(int c) { return (c & 1) ? B_WU1 : B_WU; }
 // state group and moves on.
 template <bool kRecord>
 __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int bos, int eos,
-                           int nchunks, int h) {
+                           int nchunks, int h, long long rec0) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t sbase = smem_u32(sm);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
@@ -187,25 +189,43 @@ __device__ void prep_group(const ChunkArgs& a, uint8_t* sm, uint32_t tbase, int 
       gates_step(a, vec, gq, bq, L, lane, fused, expA, dtb, c + 1 < nchunks, t0 + kChunk, h, T_total);
     if (leader) {
       ok = mbar_wait(&bars[B_MMA_P], (uint32_t)c & 1u, kWaitLimitNs);   // one D1 commit per chunk
+      if (kRecord) tma_store_wait_read();   // the previous chunk's T^T, P have left the staging
       if (!kRecord && c >= 2) ok = ok && mbar_wait(&bars[B_P_FREE + s], (uint32_t)((c - 2) >> 1) & 1u, kWaitLimitNs);
     }
     if (group_sync_or(kBarPrep, kPrepThreads, !ok || flag_set(flag))) { if (leader) set_flag(flag); return; }
     tc_fence_after();
     GDN_STAMP(0, 3);
 
-    // ---- norms, P (to this chunk's P buffer; none in record mode) and A from D1
-    norms_p_a<kBarPrep>(a, tbase + COL_D1, vec, sA, kRecord ? nullptr : sm + OFF_P + s * 8192, L);
+    // ---- norms, P (to this chunk's P buffer; in record mode to the staging for the backward)
+    //      and A from D1
+    norms_p_a<kBarPrep>(a, tbase + COL_D1, vec, sA, kRecord ? sm + OFF_RT + 8192 : sm + OFF_P + s * 8192, L);
     tc_fence_before();
     GDN_STAMP(0, 4);
     // Tw, Tu free: this buffer released by chunk c - 2
     if (leader && c >= 2) ok = mbar_wait(&bars[wu_bar(c)], (uint32_t)((c - 2) >> 1) & 1u, kWaitLimitNs);
     if (group_sync_or(kBarPrep, kPrepThreads, !ok || flag_set(flag))) { if (leader) set_flag(flag); return; }
+    if (kRecord && tid < 64) {   // the reverse pass's per-token vectors (zero past the chunk end)
+      const int i = tid;
+      const bool in = i < L;
+      float* rv = a.rec_vec + ((size_t)(rec0 + c) * a.Hv + h) * kRvFloats;
+      rv[kRvCq + i] = in ? vec[VEC_QS + i] : 0.f;
+      rv[kRvW + i] = in ? vec[VEC_DL + i] : 0.f;
+      rv[kRvF + i] = in ? -vec[VEC_SW + i] : 0.f;
+      rv[kRvBeta + i] = in ? vec[VEC_BETA + i] : 0.f;
+      if (i == 0) rv[kRvGl] = ex2(vec[VEC_G + L - 1]);
+    }
 
     // ---- T = (I + A)^{-1} as the Tw / Tu operands
     GDN_STAMP(0, 5);
-    solve_t<kBarPrep>(sA, sTd, vec, sm + tw_off<kRecord>(c), sm + tu_off<kRecord>(c));
+    solve_t<kBarPrep>(sA, sTd, vec, sm + tw_off<kRecord>(c), sm + tu_off<kRecord>(c),
+                      kRecord ? sm + OFF_RT : nullptr);
     fence_proxy_async_smem();
     group_sync(kBarPrep, kPrepThreads);
+    if (kRecord && leader) {   // T^T and P of the chunk for the backward's reverse pass
+      bulk_store(reinterpret_cast<uint8_t*>(a.rec_tp) + ((size_t)(rec0 + c) * a.Hv + h) * 16384,
+                 sm + OFF_RT, 16384);
+      tma_store_commit();
+    }
 
     // ---- hand chunk c to the state group (which runs the W / U products) and move on
     GDN_STAMP(0, 6);
@@ -709,7 +729,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         issue_chunk_loads(sm + OFF_QK + QK_STAGE, sm + OFF_V + V_STAGE, &bars[B_FULL + 1], &tmQ, &tmK,
                           &tmV, bos + kChunk, hq, h, load_v);
     }
-    prep_group<kRecord>(a, sm, tbase, bos, eos, nchunks, h);
+    prep_group<kRecord>(a, sm, tbase, bos, eos, nchunks, h, kRecord ? a.rec_chunk_off[n] : 0);
+    if (kRecord && tid == 0) tma_store_wait_all();   // the staged T^T, P tiles are written
   } else {
     // Initial state -> TMEM (S^T: lane = value index, columns = key index).
     const int row = 32 * ((tid - kPrepThreads) >> 5) + (tid & 31);

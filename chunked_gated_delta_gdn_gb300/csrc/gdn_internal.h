@@ -45,6 +45,16 @@ enum {
   kUnitFinT = 32       // exit state written transposed ([V][K])
 };
 
+// The reverse pass's per-(chunk, value head) vectors (zero at tokens past the chunk end):
+//   [kRvCq + i]    scale gamma_i r_q,i      the q rows of the dS update
+//   [kRvW + j]     lambda_j r_k,j           the columns of Y^T = dS^T K^T over raw k rows
+//   [kRvF + i]     -gamma_i beta_i r_k,i    the dX^T operand of the dS update (raw k rows)
+//   [kRvBeta + i]  beta_i                   dv = diag(beta) dX
+//   [kRvGl]        gamma_L = e^{G_{L-1}}    the decay of dS across the chunk
+// with r_q, r_k the l2-norm reciprocals (1 without the norm), G the in-chunk cumulative
+// log-decay and lambda_j = e^{G_{L-1} - G_j}.
+constexpr int kRvCq = 0, kRvW = 64, kRvF = 128, kRvBeta = 192, kRvGl = 256, kRvFloats = 320;
+
 struct ChunkArgs {
   const void* q;
   const void* k;
@@ -76,6 +86,12 @@ struct ChunkArgs {
   float* rec_states = nullptr;
   float* rec_u = nullptr;
   const int32_t* rec_chunk_off = nullptr;
+  // and, for the reverse pass, per chunk and head: T = (I + A)^{-1} transposed (element (i, j)
+  // = T[j][i], the layout of a K-major B operand) and P (element (i, j) = P[i][j]), both bf16
+  // 128-byte swizzled [64][64] tiles, together in a 16 KB slot of rec_tp; the per-token vectors
+  // of the reverse pass (kRv* below) in a slot of kRvFloats floats of rec_vec
+  float* rec_tp = nullptr;
+  float* rec_vec = nullptr;
   // Planned launch: CTA i runs units[i] when i < *unit_count (device memory), else exits.
   const TcUnit* units = nullptr;
   const int* unit_count = nullptr;

@@ -277,10 +277,11 @@ __device__ __forceinline__ void mma16(float (&acc)[2][4], FA fa, FB fb, int lane
 // diagonal T_bq = X_bq D_q with X_10 = -L_10, X_21 = -L_21, X_32 = -L_32, X_20 = -L_20 + L_21 L_10,
 // X_31 = -L_31 + L_32 L_21, X_30 = -L_30 + L_31 L_10 - L_32 X_20.  Written as the bf16 operands
 // tw = (T diag(VEC_SW))^T and tu = (T diag(VEC_BETA))^T (MN-major [64 j][64 i], 128-byte
-// swizzled).  sA is overwritten.  Synchronises the group after steps 1a and 1b; the caller
+// swizzled), and T^T itself to tt_b unless that is null.  sA is overwritten.  Synchronises the group after steps 1a and 1b; the caller
 // fences and syncs before the operands are read.
 template <int kBar>
-__device__ void solve_t(float* sA, float* sTd, const float* vec, uint8_t* tw_b, uint8_t* tu_b) {
+__device__ void solve_t(float* sA, float* sTd, const float* vec, uint8_t* tw_b, uint8_t* tu_b,
+                        uint8_t* tt_b) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // step 1a (CUDA cores): the diagonal-block inverses D_b = (I + A_bb)^{-1}, one column per
   //      thread by a right-looking substitution (warp w < 2: lanes 0-15 block 2 w, lanes 16-31
@@ -326,10 +327,15 @@ __device__ void solve_t(float* sA, float* sTd, const float* vec, uint8_t* tw_b, 
     store_bf16x8(tw_b + sw128_offset(jr, 16 * b + 8), w + 8);
     store_bf16x8(tu_b + sw128_offset(jr, 16 * b), u);
     store_bf16x8(tu_b + sw128_offset(jr, 16 * b + 8), u + 8);
+    if (tt_b) {
+      store_bf16x8(tt_b + sw128_offset(jr, 16 * b), x);
+      store_bf16x8(tt_b + sw128_offset(jr, 16 * b + 8), x + 8);
+    }
     const float zeros[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int i8 = 0; i8 < 2 * b; ++i8) {
       store_bf16x8(tw_b + sw128_offset(jr, 8 * i8), zeros);
       store_bf16x8(tu_b + sw128_offset(jr, 8 * i8), zeros);
+      if (tt_b) store_bf16x8(tt_b + sw128_offset(jr, 8 * i8), zeros);
     }
   }
   group_sync(kBar, kPrepThreads);
@@ -448,6 +454,14 @@ __device__ void solve_t(float* sA, float* sTd, const float* vec, uint8_t* tw_b, 
     const uint32_t off = sw128_offset(16 * q + 8 * (m >> 1) + r, 16 * b + 8 * (m & 1));
     stmatrix_x4_trans(smem_u32(tw_b) + off, fw);
     stmatrix_x4_trans(smem_u32(tu_b) + off, fu);
+    if (tt_b) {
+      uint32_t ft[4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) ft[2 * nt + h] = pack_bf16x2(acc[nt][2 * h], acc[nt][2 * h + 1]);
+      stmatrix_x4_trans(smem_u32(tt_b) + off, ft);
+    }
   }
 }
 
