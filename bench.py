@@ -291,7 +291,8 @@ def measure_product(dev, seed, steps=10, warmup=3):
 def measure_backward(dev, cin, d, seed, steps=5, warmup=3):
     """The chunked backward (gdn_chunk_bwd: dq, dk, dv, dg, dbeta, d_initial_state) on the
     headline batch with seeded upstream gradients d_o ~ N(0, 1) (bf16) and d_final ~ N(0, 1).
-    CUDA events on the current stream, after warm-up; the whole call (six launches)."""
+    CUDA events on the current stream, after warm-up; the whole call (five launches: chunk
+    table, record-mode forward, reverse, grad, clearing of tokens outside every sequence)."""
     from chunked_gated_delta_gdn_gb300 import _lib, chunk_gated_delta_rule_bwd, synthetic
     B, T = cin.q.shape[:2]
     d_o, dfin = synthetic.output_grads(cin, seed=seed)
@@ -323,12 +324,12 @@ def measure_backward(dev, cin, d, seed, steps=5, warmup=3):
     # tensor peak; the fp32 path would be bound by the CUDA cores' fp32 FMA rate
     return {"workload": "backward of the headline batch (B=%d T=%d Hqk=16 Hv=32 K=V=128 bf16 "
                         "I/O, fp32 accumulation), d_o and d_final_state given" % (B, T),
-            "ms": sec * 1e3, "tokens_per_s": tokens / sec, "launches": 6, "steps": steps,
+            "ms": sec * 1e3, "tokens_per_s": tokens / sec, "launches": 5, "steps": steps,
             "workspace_bytes": need,
             "roofline": {"bound": "tensor", "achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s",
                          "frac": tf / bf16_peak, "flop_per_token": BWD_FLOP_PER_TOKEN,
                          "peak_source": peak_src,
-                         "scope": "whole backward call (all six launches)"}}
+                         "scope": "whole backward call (all five launches)"}}
 
 
 def _median(xs):
