@@ -1093,8 +1093,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
   const uint32_t sb = smem_u32(sm);
   float* vec = reinterpret_cast<float*>(sm + OFF_VEC);
   float* G = vec;              float* bt = vec + 64;    float* gm = vec + 128;  float* lm = vec + 192;
-  float* qh1 = vec + 256;      float* kh2 = vec + 320;  float* kh3 = vec + 384; float* rz = vec + 448;
-  float* dba = vec + 512;      float* cs = vec + 576;   float* xvr = vec + 640; float* red = vec + 704;
+  float* qh1 = vec + 256;      float* kh2 = vec + 320;  float* kh3 = vec + 384;
+  float* xvr = vec + 640;      float* red = vec + 704;
   float* dGv = vec + 768;      float* om = vec + 832;   float* g2 = vec + 896;
   float* rnv = vec + 1024;     // [128] the rows' L2-norm reciprocals (zero past the chunk end)
   float* colp = vec + 1152;    // [4 row quarters][64] column sums of Z; then [2][128] row dots
@@ -1347,13 +1347,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (tid < 64) {   // per-token sums in a fixed order
-      const int i = tid;
-      rz[i] = (rowp[i] + rowp[64 + i]) + (rowp[128 + i] + rowp[192 + i]);
-      dba[i] = dbp[i] + dbp[64 + i];
-      cs[i] = (colp[i] + colp[64 + i]) + (colp[128 + i] + colp[192 + i]);
-    }
-    // ---- R4 += [dQ; dK] of this value head
+    // ---- R4 += [dQ; dK] of this value head (thread 0), and beside it (warps 2-3) dG, dbeta per
+    //      token, then dg by a suffix sum
     if (tid == 0) {
       const uint32_t i4 = idesc_bf16(128, 128, false, false), i4c = idesc_bf16(128, 128, false, true);
       const uint32_t i4d = idesc_bf16(128, 128, true, true);
@@ -1374,25 +1369,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
                  mndesc(sb + OFF_QK + 8192 + ks * 2048, 16384), i4d, 1);
       }
       mma_commit(bar);
-    }
-    if (tid == 0) ok = mbar_wait(bar, 1, kWaitNs);
-    if (__syncthreads_or(!ok)) { failed = true; break; }
-    tc_fence_after();
-    // every operand of this head has been read: the next head's tiles load meanwhile
-    if (hi + 1 < grp) {
-      issue_head_loads(sm, ws, &tmQ, &tmK, &tmO, bar_ld, bar_tma, ch + 1, h + 1, hq, t0, false, tid);
-      last = hi + 1;
-    }
-    // ---- dG, dbeta per token, then dg by a suffix sum
-    if (tid < 64) {
-      const int i = tid;
+    } else if (warp == 2 || warp == 3) {
+      const int i = tid - 64;
+      // per-token sums in a fixed order
+      const float rzi = (rowp[i] + rowp[64 + i]) + (rowp[128 + i] + rowp[192 + i]);
+      const float dbai = dbp[i] + dbp[64 + i];
+      const float csi = (colp[i] + colp[64 + i]) + (colp[128 + i] + colp[192 + i]);
       const float omega = i < L ? lm[i] * kh3[i] : 0.f;
       om[i] = omega;
-      dGv[i] = i < L ? a.scale * gm[i] * qh1[i] - bt[i] * gm[i] * kh2[i] - omega + rz[i] - cs[i] : 0.f;
-      if (i < L) b.dbeta[(size_t)(t0 + i) * Hv + h] = xvr[i] - gm[i] * kh2[i] + dba[i];
+      dGv[i] = i < L ? a.scale * gm[i] * qh1[i] - bt[i] * gm[i] * kh2[i] - omega + rzi - csi : 0.f;
+      if (i < L) b.dbeta[(size_t)(t0 + i) * Hv + h] = xvr[i] - gm[i] * kh2[i] + dbai;
+      group_sync(1, 64);   // warps 2-3: every token's dG is in place
     }
-    __syncthreads();
-    if (warp == 0) {
+    if (warp == 2) {
       float sdt = 0.f;
       for (int w = 1; w < kThreads / 32; ++w) sdt += red[w];
       const float omsum = warp_sum(om[lane] + om[lane + 32]);
@@ -1411,7 +1400,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
       if (lane < L) b.dg[base + (size_t)lane * Hv] = x0;
       if (lane + 32 < L) b.dg[base + (size_t)(lane + 32) * Hv] = x1;
     }
-    __syncthreads();   // the per-token vectors are read before the next head rewrites them
+    if (tid == 0) ok = mbar_wait(bar, 1, kWaitNs);
+    // (the barrier also orders the per-token vectors' last reads before the next head's writes)
+    if (__syncthreads_or(!ok)) { failed = true; break; }
+    tc_fence_after();
+    // every operand of this head has been read: the next head's tiles load meanwhile
+    if (hi + 1 < grp) {
+      issue_head_loads(sm, ws, &tmQ, &tmK, &tmO, bar_ld, bar_tma, ch + 1, h + 1, hq, t0, false, tid);
+      last = hi + 1;
+    }
   }
   if (failed) {
     if (tid == 0) {   // copies still in flight land before the shared memory is released
