@@ -85,6 +85,33 @@ struct BwdWs {
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Stage timestamps of the tensor-core reverse and grad passes (a diagnostic build,
+// -DGDN_CHUNK_STAMPS): thread 0 records clock64 at the stage boundaries of iterations 32 .. 95
+// in the first eight CTAs of the reverse pass, and of the first two value heads (slots 0 .. 12)
+// and the epilogue (slots 13 .. 15 of head 0) in CTAs 4000 .. 4007 of the grad pass
+// (gdn_bwd_stamps_read copies them out).  Without the define the stamps compile to nothing.
+#ifdef GDN_CHUNK_STAMPS
+__device__ unsigned long long g_rev_stamps[8][64][16];
+__device__ unsigned long long g_grad_stamps[8][2][16];
+#define GDN_RSTAMP(p)                                                               \
+  do {                                                                              \
+    if (tid == 0 && blockIdx.x < 8 && it >= 32 && it < 96)                          \
+      g_rev_stamps[blockIdx.x][it - 32][p] = clock64();                             \
+  } while (0)
+#define GDN_GSTAMP(hd, p)                                                           \
+  do {                                                                              \
+    if (tid == 0 && blockIdx.x >= 4000 && blockIdx.x < 4008 && (hd) < 2)            \
+      g_grad_stamps[blockIdx.x - 4000][hd][p] = clock64();                          \
+  } while (0)
+#else
+#define GDN_RSTAMP(p) \
+  do {                \
+  } while (0)
+#define GDN_GSTAMP(hd, p) \
+  do {                    \
+  } while (0)
+#endif
+
 __host__ __device__ inline BwdWs bwd_layout(void* base, long long NC, int N, int Hv, int K, int V,
                                             long long T_total, bool tc, size_t* total) {
   BwdWs w;
@@ -1149,8 +1176,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     if (warp == 1) load_gates(a, t0, L, h, G, bt, lane);
     if (tid >= 64 && tid < 128)   // the row dots dX_i . v_i of the reverse pass (slot 0)
       xvr[tid - 64] = ws.XV[ch * 4 * 64 + tid - 64];
+    GDN_GSTAMP(hi, 0);
     if (tid == 0) ok = mbar_wait(bar_ld, ph, kWaitNs) && mbar_wait(bar_tma, ph, kWaitNs);   // landed
     if (__syncthreads_or(!ok)) { failed = true; break; }
+    GDN_GSTAMP(hi, 1);
     if (hi == 0) {  // [q; k] rows normalised in place (thread: one row half, 128 rows x 2
                     // halves), rows past the chunk end cleared
       const int r = tid >> 1, hh = tid & 1, i = r & 63;
@@ -1176,6 +1205,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
 #pragma unroll
       for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(rowq + 16 * ((j + r) & 7)) = scaled8(u[j], rn);
     }
+    GDN_GSTAMP(hi, 2);
     if (L < C) {   // dO rows past the chunk end (the next sequence's) cleared
       for (int e = tid; e < 2 * 64 * 8; e += kThreads) {
         const int hf = e >> 9, ii = (e >> 3) & 63, c8 = e & 7;
@@ -1187,6 +1217,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    GDN_GSTAMP(hi, 3);
     // ---- R1, R2 (and R3 for the first head), issued first: the dot below runs meanwhile
     if (tid == 0) {
       const uint32_t i1 = idesc_bf16(128, 256, false, true), i2 = idesc_bf16(128, 64, false, false);
@@ -1201,6 +1232,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
       }
       mma_commit(bar);
     }
+    GDN_GSTAMP(hi, 4);
     if (warp > 0) {  // <S0, dS> over the two tiles (same layout, element by element), by the
                      // warps that do not issue the products
       float sd = 0.f;
@@ -1225,9 +1257,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
       lm[tid] = expf(G[L - 1] - G[tid]);
       g2[tid] = G[tid] * kLog2eG;   // base-2 log-decay for the F / E factors
     }
+    GDN_GSTAMP(hi, 5);
     if (tid == 0) ok = mbar_wait(bar, 0, kWaitNs);
     if (__syncthreads_or(!ok)) { failed = true; break; }
     tc_fence_after();
+    GDN_GSTAMP(hi, 6);
     // ---- row dots from R1 (warps 0-3: the S0 columns; warps 6-7: the dS columns of k rows)
     if (warp < 4 || warp >= 6) {   // 8 columns of the bf16 row per 16-byte load
       const bool s0 = warp < 4;
@@ -1256,6 +1290,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
       else kh2[row - 64] = acc;
     }
     __syncthreads();
+    GDN_GSTAMP(hi, 7);
     // ---- R4's scaled operands: [scale gamma dO; -gamma beta dX] in place, lambda U' rows
     //      64-127 (every load of a thread before its stores)
     {
@@ -1283,6 +1318,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
             scaled8(w[k], lm[i]);
       }
     }
+    GDN_GSTAMP(hi, 8);
     // ---- F (rows i < 64 of R2 / R3) and E (rows 64-127), all eight warps at once: a warp
     //      reaches the TMEM lanes 32 (warp % 4) .. + 31 and takes the column half warp / 4
     {
@@ -1347,6 +1383,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    GDN_GSTAMP(hi, 9);
     // ---- R4 += [dQ; dK] of this value head (thread 0), and beside it (warps 2-3) dG, dbeta per
     //      token, then dg by a suffix sum
     if (tid == 0) {
@@ -1400,15 +1437,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
       if (lane < L) b.dg[base + (size_t)lane * Hv] = x0;
       if (lane + 32 < L) b.dg[base + (size_t)(lane + 32) * Hv] = x1;
     }
+    GDN_GSTAMP(hi, 10);
     if (tid == 0) ok = mbar_wait(bar, 1, kWaitNs);
     // (the barrier also orders the per-token vectors' last reads before the next head's writes)
     if (__syncthreads_or(!ok)) { failed = true; break; }
     tc_fence_after();
+    GDN_GSTAMP(hi, 11);
     // every operand of this head has been read: the next head's tiles load meanwhile
     if (hi + 1 < grp) {
       issue_head_loads(sm, ws, &tmQ, &tmK, &tmO, bar_ld, bar_tma, ch + 1, h + 1, hq, t0, false, tid);
       last = hi + 1;
     }
+    GDN_GSTAMP(hi, 12);
   }
   if (failed) {
     if (tid == 0) {   // copies still in flight land before the shared memory is released
@@ -1425,6 +1465,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     }
     return;
   }
+  GDN_GSTAMP(0, 13);
   // ---- dq, dk: the L2 norm's Jacobian on the group sums in R4 (rows 0-63: q, 64-127: k),
   //      dx = r (dx^ - x^ (x^ . dx^)) with x^ the normalised row in [q; k]; warp group g takes
   //      the columns 64 g .. 64 g + 63 (the k-half g of [q; k]) and the halves' partial dots
@@ -1481,6 +1522,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     tc_fence_after();
     tmem_dealloc(tb, T_COLS);
   }
+  GDN_GSTAMP(0, 14);
   if (L == C) {   // four TMA stores
     if (tid == kTmaThread) {
 #pragma unroll
@@ -1749,8 +1791,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
     const uint32_t sst = sb + s * STAGE;
     const float* vec = reinterpret_cast<const float*>(st + ST_VEC);
     bool ok = true;
+    GDN_RSTAMP(0);
     if (tid == 0) ok = mbar_wait(&full[s], (uint32_t)(it >> 1) & 1u, kWaitNs);
     if (__syncthreads_or(!ok)) { failed = true; break; }
+    GDN_RSTAMP(1);
     if (L < C) {   // the sequence's last chunk: rows past its end (the next sequence's) cleared
       for (int e = tid; e < 2 * 64 * 8; e += kThreads) {
         const int hh = e >> 9, i = (e >> 3) & 63, c8 = e & 7;
@@ -1765,6 +1809,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
       __syncthreads();
     }
     tc_fence_after();
+    GDN_RSTAMP(2);
     if (tid == 0) {   // Y^T = dS^T K^T;  dUp^T = dO^T P
       const uint32_t iy = idesc_bf16(128, 64, false, false), iu = idesc_bf16(128, 64, true, true);
 #pragma unroll
@@ -1789,11 +1834,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
         fence_proxy_async_smem();
       }
     }
+    GDN_RSTAMP(3);
     if (it >= 1 && it + 1 < nch) issued = it + 2;
     if (tid == 0) ok = mbar_wait(mmab, ph, kWaitNs);
     ph ^= 1u;
     if (__syncthreads_or(!ok)) { failed = true; break; }
     tc_fence_after();
+    GDN_RSTAMP(4);
     {  // dU'^T = dUp^T + Y^T diag(lambda r_k) -> bf16 pairs in C_U
       const float* w = vec + kRvW;
       float pk[16];
@@ -1817,6 +1864,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    GDN_RSTAMP(5);
     if (tid == 0) {   // dX^T = dU'^T T (the stage holds T^T: a K-major B operand)
       const uint32_t ix = idesc_bf16(128, 64, false, false);
 #pragma unroll
@@ -1832,9 +1880,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
     // the grad pass's bf16 tiles, staged for bulk copies: dX (rows = the chunk's tokens, 64 v
     // per 128-byte row in two 8 KB halves) and dS, the gradient of the chunk's exit state (rows d,
     // two 16 KB halves), both 128-byte swizzled; dv over the v tile; dS^T <- gamma_L dS^T
+    GDN_RSTAMP(6);
     stage_dx(tb, loff, wg, sb + OFF_STG_X, sst + ST_V, vec + kRvBeta, red, wq, lane);
+    GDN_RSTAMP(7);
     stage_state(tb, loff, wg, sb + OFF_STG_S, vec[kRvGl], wq, lane);
     fence_proxy_async_smem();
+    GDN_RSTAMP(8);
     {  // bf16 dX^T diag(-gamma beta r_k) in C_X, the A operand of the dS update
       const float* fv = vec + kRvF;
       float pk[16];
@@ -1856,6 +1907,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    GDN_RSTAMP(9);
     if (tid == kStorer) {   // beside the dS update: dv first (its own group), then dS and dX
       if (L == C) {   // dv rows by TMA (a chunk ending earlier must not touch the next sequence)
         tma_store_3d(&tmDV, st + ST_V, 0, h, t0);
@@ -1881,6 +1933,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
       const int i = tid - 64;
       ws.XV[ch * 4 * 64 + i] = (red[i] + red[64 + i]) + (red[128 + i] + red[192 + i]);
     }
+    GDN_RSTAMP(10);
     if (tid == 0) {   // dS^T += dO^T (scale gamma r_q q) + (dX^T diag(-gamma beta r_k)) k
       const uint32_t iq = idesc_bf16(128, 128, true, true), ik = idesc_bf16(128, 128, false, true);
 #pragma unroll
@@ -1899,10 +1952,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_tc_kernel(
     ph ^= 1u;
     if (__syncthreads_or(!ok)) { failed = true; break; }
     tc_fence_after();
+    GDN_RSTAMP(11);
     pack_state(tb, loff, wg);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    GDN_RSTAMP(12);
   }
   if (tid == kStorer) tma_store_wait_all();   // the stored tiles are written before the CTA exits
   if (tid == 0) {
@@ -2020,6 +2075,17 @@ __global__ void __launch_bounds__(kQkThreads) bwd_uncovered_kernel(const ChunkAr
 }
 
 }  // namespace
+
+#ifdef GDN_CHUNK_STAMPS
+// The stage timestamps of the last tensor-core backward of the stamped build: the reverse pass's
+// [8 CTAs][iterations 32 .. 95][16] and the grad pass's [8 CTAs][2 heads][16] clock64 values;
+// returns a cudaError_t.
+extern "C" int gdn_bwd_stamps_read(void* rev, void* grad) {
+  cudaError_t e = cudaMemcpyFromSymbol(rev, g_rev_stamps, sizeof(g_rev_stamps));
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(grad, g_grad_stamps, sizeof(g_grad_stamps));
+  return (int)e;
+}
+#endif
 
 size_t chunk_bwd_workspace_bytes(int T_total, int num_seqs, int Hv, int K, int V, bool tc) {
   size_t total = 0;
