@@ -340,8 +340,10 @@ gdn_status_t gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, 
  * torch_chunk_gated_delta_rule, whose deterministic mode is the reason it exists;
  * "Megatron-Core API: core.ssm.gated_delta_product", _gdp_chunk_forward, shared by
  * training and prefill).  The sources print no backward: this returns the exact
- * gradients of gdn_chunk_fwd's outputs, computed chunkwise in fp32 on the CUDA
- * cores, with no atomics (bitwise identical from run to run).
+ * gradients of gdn_chunk_fwd's outputs, computed chunkwise with fp32 accumulation
+ * (bf16 I/O with K = V = 128: every product on the tcgen05 tensor cores with bf16
+ * operands; otherwise fp32 on the CUDA cores), with no atomics (bitwise identical
+ * from run to run).
  *
  * Forward arguments (q, k, v, g, beta, B, T, Hqk, Hv, K, V, io_dtype, beta_dtype,
  * scale, chunk_size = 64, initial_state [N, Hv, K, V] or NULL, use_qk_l2norm,
@@ -361,8 +363,10 @@ gdn_status_t gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, 
  * gradient is written as zero.
  *   workspace, workspace_bytes  device scratch of at least
  *                gdn_chunk_bwd_workspace_size(...) bytes, 16-byte aligned, owned
- *                by the caller (about 4 (3 K V + 3 C V + C K + C C + C) bytes per
- *                chunk of C = 64 tokens and value head, plus 8 Hv K bytes per token).
+ *                by the caller: per chunk of C = 64 tokens and value head, about
+ *                2 (2 K V + 2 C V) + 4 (C C + 4 C + 320) bytes on the tensor-core path,
+ *                4 (3 K V + 3 C V + C K + C C + 5 C) bytes on the CUDA-core path, which
+ *                also keeps 8 Hv K bytes per token.
  * Errors as gdn_chunk_fwd: host-side checks return a status before any launch.
  */
 gdn_status_t gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
