@@ -1007,7 +1007,9 @@ __global__ void __launch_bounds__(kGradThreads) bwd_grad_kernel(const ChunkArgs 
 //   R3 [320, 384) [Q; K] K^T              M=128 N=64  K=128  -> Q K^T, K K^T (once: the same
 //                                                               for every head of the group)
 //   R4 [384, 512) [dQ; dK] += [scale gamma dO | 0 ; -gamma beta dX | lambda U'] [S0 | dS]^T
-//                           + [F; E] K + [0; F^T] Q + [0; E^T] K          (K = 256, 64, 64, 64)
+//                           + [F; E] K + [0; F^T] Q + [0; E^T] K          (K = 256, 64, 64, 64;
+//                             the first A operand built as bf16 in R1's columns once the row dots
+//                             have read them)
 // R4 accumulates over the group's value heads, which gives the group sum of the gradients of
 // the normalised q, k rows; the epilogue applies the L2 norm's Jacobian
 // dq = r (dq^ - q^ (q^ . dq^)) and writes dq, dk as bf16.  F^T and E^T are MN-major A operands
@@ -1035,12 +1037,11 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t OFF_QK = 0;          // [q; k] rows, 2 k-halves x 128 rows x 128 B
 constexpr uint32_t OFF_S0 = 32768;      // S0 rows d, 2 c-halves x 128 rows
 constexpr uint32_t OFF_DS = 65536;      // dS rows d (right after S0: [S0 | dS] is one operand)
-constexpr uint32_t OFF_OX = 98304;      // [dO; dX] rows, then [scale gamma dO; -gamma beta dX]
-constexpr uint32_t OFF_LU = 131072;     // [0; lambda U'] rows (right after OX)
-constexpr uint32_t OFF_U = 163840;      // U' rows j, 2 c-halves x 64 rows
-constexpr uint32_t OFF_ZERO = 180224;   // 64 rows x 128 B of zeros
-constexpr uint32_t OFF_FE = 188416;     // [F; E] rows, K = 64 tokens: 128 rows x 128 B
-constexpr uint32_t OFF_VEC = 204800;    // fp32 per-token vectors and scratch, 28 x 64
+constexpr uint32_t OFF_OX = 98304;      // [dO; dX] rows
+constexpr uint32_t OFF_U = 131072;      // U' rows j, 2 c-halves x 64 rows
+constexpr uint32_t OFF_ZERO = 147456;   // 64 rows x 128 B of zeros
+constexpr uint32_t OFF_FE = 155648;     // [F; E] rows, K = 64 tokens: 128 rows x 128 B
+constexpr uint32_t OFF_VEC = 172032;    // fp32 per-token vectors and scratch, 28 x 64
 constexpr uint32_t OFF_BAR = OFF_VEC + 28 * 64 * 4;
 constexpr uint32_t SMEM = OFF_BAR + 64 + 1024;
 static_assert(SMEM <= 232448, "shared memory budget");
@@ -1078,37 +1079,26 @@ __device__ __forceinline__ uint64_t mndesc(uint32_t addr, uint32_t lbo) {
   return sdesc_sw128(addr, lbo, 1024);
 }
 
-// The operand tiles of value head h that the producers wrote (S0, dS, U', dX; bulk copies on
-// `bar_ld`, issued by thread 0) and its dO rows (TMA on `bar_tma`, issued by kTmaThread; with
-// the group's q, k rows for the first head).
-__device__ __forceinline__ void issue_head_loads(uint8_t* sm, const BwdWs& ws, const CUtensorMap* tmQ,
-                                                 const CUtensorMap* tmK, const CUtensorMap* tmO,
-                                                 uint64_t* bar_ld, uint64_t* bar_tma, size_t ch,
-                                                 int h, int hq, int t0, bool qk, int tid) {
-  if (tid == 0) {
-    const uint8_t* s0 = reinterpret_cast<const uint8_t*>(ws.S + ch * ws.sS);
-    const uint8_t* ds = reinterpret_cast<const uint8_t*>(ws.dS + ch * ws.sdS);
-    const uint8_t* ug = reinterpret_cast<const uint8_t*>(ws.U + ch * ws.sU);
-    const uint8_t* xg = reinterpret_cast<const uint8_t*>(ws.dX + ch * ws.sdX);
-    mbar_arrive_expect_tx(bar_ld, 32768 + 32768 + 16384 + 16384);
-    bulk_load(sm + OFF_S0, s0, 32768, bar_ld);
-    bulk_load(sm + OFF_DS, ds, 32768, bar_ld);
-    bulk_load(sm + OFF_U, ug, 16384, bar_ld);
-    bulk_load(sm + OFF_OX + 8192, xg, 8192, bar_ld);   // dX: rows 64-127 of [dO; dX]
-    bulk_load(sm + OFF_OX + 16384 + 8192, xg + 8192, 8192, bar_ld);
-  } else if (tid == kTmaThread) {
-    // 64 features x 64 tokens a box, zero past the last token (rows past the chunk end are
-    // cleared after the loads land)
-    mbar_arrive_expect_tx(bar_tma, (qk ? 3 : 1) * 16384);
+// The operand tiles of value head h (chunk unit ch, first token t0), issued by thread 0: part A,
+// the rows [dO; dX] (dO by TMA, dX by bulk copy) and U' (bulk), on `bar_a`; part B, S0 and dS
+// (bulk), on `bar_b`.  Part A's space is free once R4's operand has been built in TMEM, part B's
+// once R4 has run.
+__device__ __forceinline__ void issue_loads_a(uint8_t* sm, const BwdWs& ws, const CUtensorMap* tmO,
+                                              uint64_t* bar_a, size_t ch, int h, int t0) {
+  const uint8_t* ug = reinterpret_cast<const uint8_t*>(ws.U + ch * ws.sU);
+  const uint8_t* xg = reinterpret_cast<const uint8_t*>(ws.dX + ch * ws.sdX);
+  mbar_arrive_expect_tx(bar_a, 16384 + 16384 + 2 * 8192);
+  bulk_load(sm + OFF_U, ug, 16384, bar_a);
+  bulk_load(sm + OFF_OX + 8192, xg, 8192, bar_a);   // dX: rows 64-127 of [dO; dX]
+  bulk_load(sm + OFF_OX + 16384 + 8192, xg + 8192, 8192, bar_a);
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      if (qk) {
-        tma_load_3d(sm + OFF_QK + hh * 16384, tmQ, bar_tma, 64 * hh, hq, t0);
-        tma_load_3d(sm + OFF_QK + hh * 16384 + 8192, tmK, bar_tma, 64 * hh, hq, t0);
-      }
-      tma_load_3d(sm + OFF_OX + hh * 16384, tmO, bar_tma, 64 * hh, h, t0);
-    }
-  }
+  for (int hh = 0; hh < 2; ++hh)   // 64 features x 64 tokens a box, zero past the last token
+    tma_load_3d(sm + OFF_OX + hh * 16384, tmO, bar_a, 64 * hh, h, t0);
+}
+__device__ __forceinline__ void issue_loads_b(uint8_t* sm, const BwdWs& ws, uint64_t* bar_b, size_t ch) {
+  mbar_arrive_expect_tx(bar_b, 2 * 32768);
+  bulk_load(sm + OFF_S0, reinterpret_cast<const uint8_t*>(ws.S + ch * ws.sS), 32768, bar_b);
+  bulk_load(sm + OFF_DS, reinterpret_cast<const uint8_t*>(ws.dS + ch * ws.sdS), 32768, bar_b);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
@@ -1128,9 +1118,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
   float* dbp = vec + 1408;     // [2][64] partial dbeta terms
   float* rowp = vec + 1536;    // [2 column halves][128 rows] partial row sums of Z
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-  uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + OFF_BAR + 8);    // the bulk loads
-  uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + OFF_BAR + 16);  // the TMA loads
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 24);
+  uint64_t* bar_a = reinterpret_cast<uint64_t*>(sm + OFF_BAR + 8);     // a head's dO, dX, U'
+  uint64_t* bar_b = reinterpret_cast<uint64_t*>(sm + OFF_BAR + 16);    // a head's S0, dS
+  uint64_t* bar_qk = reinterpret_cast<uint64_t*>(sm + OFF_BAR + 24);   // the group's q, k
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_BAR + 32);
   // one CTA per (chunk, query/key head), heads fastest: the CTAs running together read the
   // same tokens (adjacent rows)
   const int Hqk = a.Hqk, Hv = a.Hv, grp = Hv / Hqk;
@@ -1143,30 +1134,36 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
   const int row = 32 * (warp & 3) + lane;   // this thread's TMEM lane
   if (tid == 0) {
     mbar_init(bar, 1);
-    mbar_init(bar_ld, 1);
-    mbar_init(bar_tma, 1);
+    mbar_init(bar_a, 1);
+    mbar_init(bar_b, 1);
+    mbar_init(bar_qk, 1);
     fence_mbar_init();
   }
   __syncthreads();   // the barriers are initialised before any copy is issued
-  issue_head_loads(sm, ws, &tmQ, &tmK, &tmO, bar_ld, bar_tma, (size_t)c * Hv + hq * grp, hq * grp, hq,
-                   t0, true, tid);
+  if (tid == 0) {    // the first value head's tiles
+    issue_loads_a(sm, ws, &tmO, bar_a, (size_t)c * Hv + hq * grp, hq * grp, t0);
+    issue_loads_b(sm, ws, bar_b, (size_t)c * Hv + hq * grp);
+  } else if (tid == kTmaThread) {   // the chunk's q, k rows into [q; k] by TMA
+    mbar_arrive_expect_tx(bar_qk, 2 * 16384);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      tma_load_3d(sm + OFF_QK + hh * 16384, &tmQ, bar_qk, 64 * hh, hq, t0);
+      tma_load_3d(sm + OFF_QK + hh * 16384 + 8192, &tmK, bar_qk, 64 * hh, hq, t0);
+    }
+  }
   if (warp == kTmemWarp) {
     tmem_alloc(tslot, T_COLS);
     tmem_relinquish();
   }
   for (int e = tid; e < 8192 / 16; e += kThreads)      // the zero tile
     reinterpret_cast<uint4*>(sm + OFF_ZERO)[e] = make_uint4(0u, 0u, 0u, 0u);
-  for (int e = tid; e < 2 * 8192 / 16; e += kThreads) {   // rows 0-63 of both halves of [0; lambda U']
-    const int hlf = e / (8192 / 16), w = e - hlf * (8192 / 16);
-    reinterpret_cast<uint4*>(sm + OFF_LU + hlf * 16384)[w] = make_uint4(0u, 0u, 0u, 0u);
-  }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = *tslot;
   bool ok = true, failed = false;
-  int last = 0;   // the last head whose tiles were requested
+  int last_a = 0, last_b = 0;   // the last heads whose part A / part B tiles were requested
 
   for (int hi = 0; hi < grp; ++hi) {
     const int h = hq * grp + hi;
@@ -1177,7 +1174,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     if (tid >= 64 && tid < 128)   // the row dots dX_i . v_i of the reverse pass (slot 0)
       xvr[tid - 64] = ws.XV[ch * 4 * 64 + tid - 64];
     GDN_GSTAMP(hi, 0);
-    if (tid == 0) ok = mbar_wait(bar_ld, ph, kWaitNs) && mbar_wait(bar_tma, ph, kWaitNs);   // landed
+    if (tid == 0)   // landed
+      ok = mbar_wait(bar_a, ph, kWaitNs) && mbar_wait(bar_b, ph, kWaitNs) &&
+           (hi > 0 || mbar_wait(bar_qk, 0, kWaitNs));
     if (__syncthreads_or(!ok)) { failed = true; break; }
     GDN_GSTAMP(hi, 1);
     if (hi == 0) {  // [q; k] rows normalised in place (thread: one row half, 128 rows x 2
@@ -1289,35 +1288,58 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
       else if (row < 64) qh1[row] = acc;
       else kh2[row - 64] = acc;
     }
-    __syncthreads();
+    tc_fence_before();
+    __syncthreads();   // R1 has been read out: its columns take R4's operand
+    tc_fence_after();
     GDN_GSTAMP(hi, 7);
-    // ---- R4's scaled operands: [scale gamma dO; -gamma beta dX] in place, lambda U' rows
-    //      64-127 (every load of a thread before its stores)
+    // ---- R4's A operand in TMEM, in R1's columns (read out by the row dots):
+    //      [scale gamma dO | 0 ; -gamma beta dX | lambda U'] as bf16 pairs, K = 256 (the v of S0,
+    //      then the v of dS); thread: its TMEM lane's row, the v half warp / 4 of each part.  A
+    //      row's 16-byte chunks sit at chunk ^ (row % 8), so the warp's reads of one chunk index
+    //      spread over the banks.
     {
-      uint4 u[8], w[4];
+      const int g = warp >> 2;
+      float pk[32];
+      {
+        const float sc = row < 64 ? a.scale * gm[row] : -gm[row - 64] * bt[row - 64];
+        const uint8_t* orow = sm + OFF_OX + g * 16384 + row * 128;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int e = tid + kThreads * k, r = e >> 4, chunk = e & 15;
-        u[k] = *reinterpret_cast<const uint4*>(sm + OFF_OX + (chunk >> 3) * 16384 + r * 128 + (chunk & 7) * 16);
-      }
+        for (int c8 = 0; c8 < 8; ++c8) {
+          const uint4 u = *reinterpret_cast<const uint4*>(orow + ((c8 ^ (row & 7)) << 4));
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int e = tid + kThreads * k, i = e >> 4, chunk = e & 15;
-        w[k] = *reinterpret_cast<const uint4*>(sm + OFF_U + (chunk >> 3) * 8192 + i * 128 + (chunk & 7) * 16);
+          for (int q = 0; q < 4; ++q) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[q]));
+            pk[4 * c8 + q] = __uint_as_float(pack2(sc * f.x, sc * f.y));
+          }
+        }
+        tmem_st32(tb + loff + T_R1 + 32 * g, pk);
       }
+      if (row < 64) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int e = tid + kThreads * k, r = e >> 4, chunk = e & 15;
-        const float s = r < 64 ? a.scale * gm[r] : -gm[r - 64] * bt[r - 64];
-        *reinterpret_cast<uint4*>(sm + OFF_OX + (chunk >> 3) * 16384 + r * 128 + (chunk & 7) * 16) = scaled8(u[k], s);
-      }
+        for (int j = 0; j < 32; ++j) pk[j] = 0.f;
+      } else {
+        const int i = row - 64;
+        const float li = lm[i];
+        const uint8_t* urow = sm + OFF_U + g * 8192 + i * 128;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {   // (U' and [0; lambda U'] share the swizzle: row i = 64 + i mod 8)
-        const int e = tid + kThreads * k, i = e >> 4, chunk = e & 15;
-        *reinterpret_cast<uint4*>(sm + OFF_LU + (chunk >> 3) * 16384 + (64 + i) * 128 + (chunk & 7) * 16) =
-            scaled8(w[k], lm[i]);
+        for (int c8 = 0; c8 < 8; ++c8) {
+          const uint4 u = *reinterpret_cast<const uint4*>(urow + ((c8 ^ (i & 7)) << 4));
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[q]));
+            pk[4 * c8 + q] = __uint_as_float(pack2(li * f.x, li * f.y));
+          }
+        }
       }
+      tmem_st32(tb + loff + T_R1 + 64 + 32 * g, pk);
     }
+    tc_fence_before();
+    __syncthreads();   // [dO; dX] and U' have been read: the next head's load into their space
+    tc_fence_after();
+    if (tid == 0 && hi + 1 < grp) issue_loads_a(sm, ws, &tmO, bar_a, ch + 1, h + 1, t0);
+    if (hi + 1 < grp) last_a = hi + 1;
     GDN_GSTAMP(hi, 8);
     // ---- F (rows i < 64 of R2 / R3) and E (rows 64-127), all eight warps at once: a warp
     //      reaches the TMEM lanes 32 (warp % 4) .. + 31 and takes the column half warp / 4
@@ -1392,7 +1414,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
 #pragma unroll
       for (int ks = 0; ks < 16; ++ks) {   // [scale gamma dO | 0 ; -gamma beta dX | lambda U'] [S0 | dS]^T
         const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
-        mma_bf16(tb + T_R4, kdesc(sb + OFF_OX + ko), kdesc(sb + OFF_S0 + ko), i4, ks > 0 || hi > 0);
+        mma_bf16_ta(tb + T_R4, tb + T_R1 + 8 * ks, kdesc(sb + OFF_S0 + ko), i4, ks > 0 || hi > 0);
       }
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
@@ -1443,19 +1465,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     if (__syncthreads_or(!ok)) { failed = true; break; }
     tc_fence_after();
     GDN_GSTAMP(hi, 11);
-    // every operand of this head has been read: the next head's tiles load meanwhile
+    // S0, dS have been read: the next head's load into their space meanwhile
     if (hi + 1 < grp) {
-      issue_head_loads(sm, ws, &tmQ, &tmK, &tmO, bar_ld, bar_tma, ch + 1, h + 1, hq, t0, false, tid);
-      last = hi + 1;
+      if (tid == 0) issue_loads_b(sm, ws, bar_b, ch + 1);
+      last_b = hi + 1;
     }
     GDN_GSTAMP(hi, 12);
   }
   if (failed) {
     if (tid == 0) {   // copies still in flight land before the shared memory is released
-      mbar_wait(bar_ld, (uint32_t)last & 1u, kWaitNs);
+      mbar_wait(bar_a, (uint32_t)last_a & 1u, kWaitNs);
+      mbar_wait(bar_b, (uint32_t)last_b & 1u, kWaitNs);
+      mbar_wait(bar_qk, 0, kWaitNs);
       report(a.dev_status, GDN_DEV_TIMEOUT);
-    } else if (tid == kTmaThread) {
-      mbar_wait(bar_tma, (uint32_t)last & 1u, kWaitNs);
     }
     tc_fence_before();
     __syncthreads();
