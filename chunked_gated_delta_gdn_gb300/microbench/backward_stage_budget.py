@@ -48,7 +48,7 @@ GRAD = [
     "gamma, lambda factors",
     "wait: R1-R3 done",
     "row dots",
-    "R4 operands scaled",
+    "R4's first operand built in TMEM; the next head's dO, dX, U' issued",
     "F, E",
     "R4 issue (warps 2-3: dG, dbeta, dg)",
     "wait: R4 done",
