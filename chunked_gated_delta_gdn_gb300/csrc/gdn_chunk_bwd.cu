@@ -87,8 +87,9 @@ __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size
 
 // Stage timestamps of the tensor-core reverse and grad passes (a diagnostic build,
 // -DGDN_CHUNK_STAMPS): thread 0 records clock64 at the stage boundaries of iterations 32 .. 95
-// in the first eight CTAs of the reverse pass, and of the first two value heads (slots 0 .. 12)
-// and the epilogue (slots 13 .. 15 of head 0) in CTAs 4000 .. 4007 of the grad pass
+// in the first eight CTAs of the reverse pass, and the grad pass's issuing thread (256) those of
+// the first two value heads (slots 0 .. 12) and the epilogue (slots 13 .. 15 of head 0) in CTAs
+// 4000 .. 4007
 // (gdn_bwd_stamps_read copies them out).  Without the define the stamps compile to nothing.
 #ifdef GDN_CHUNK_STAMPS
 __device__ unsigned long long g_rev_stamps[8][64][16];
@@ -100,7 +101,7 @@ __device__ unsigned long long g_grad_stamps[8][2][16];
   } while (0)
 #define GDN_GSTAMP(hd, p)                                                           \
   do {                                                                              \
-    if (tid == 0 && blockIdx.x >= 4000 && blockIdx.x < 4008 && (hd) < 2)            \
+    if (tid == 256 && blockIdx.x >= 4000 && blockIdx.x < 4008 && (hd) < 2)          \
       g_grad_stamps[blockIdx.x - 4000][hd][p] = clock64();                          \
   } while (0)
 #else
@@ -1032,7 +1033,9 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 using namespace sm100;
-constexpr int kThreads = 256;
+constexpr int kWorkThreads = 256;          // warps 0-7: two per TMEM lane quarter
+constexpr int kThreads = kWorkThreads + 32;   // and warp 8, which issues the copies and the MMAs
+constexpr int kIssuer = kWorkThreads;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t OFF_QK = 0;          // [q; k] rows, 2 k-halves x 128 rows x 128 B
 constexpr uint32_t OFF_S0 = 32768;      // S0 rows d, 2 c-halves x 128 rows
@@ -1046,7 +1049,7 @@ constexpr uint32_t OFF_BAR = OFF_VEC + 28 * 64 * 4;
 constexpr uint32_t SMEM = OFF_BAR + 64 + 1024;
 static_assert(SMEM <= 232448, "shared memory budget");
 constexpr uint32_t T_R1 = 0, T_R2 = 256, T_R3 = 320, T_R4 = 384, T_COLS = 512;
-constexpr int kTmaThread = 160;   // issues the TMA loads and stores (thread 0: the bulk loads, MMAs)
+constexpr int kTmaThread = 160;   // issues the q, k loads and the TMA stores
 constexpr int kTmemWarp = 4;      // allocates and frees the tensor memory
 
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
@@ -1132,7 +1135,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
   const bool l2 = a.use_qk_l2norm != 0;
   const uint32_t loff = (uint32_t)(32 * (warp & 3)) << 16;
   const int row = 32 * (warp & 3) + lane;   // this thread's TMEM lane
-  if (tid == 0) {
+  if (tid == kIssuer) {
     mbar_init(bar, 1);
     mbar_init(bar_a, 1);
     mbar_init(bar_b, 1);
@@ -1140,7 +1143,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     fence_mbar_init();
   }
   __syncthreads();   // the barriers are initialised before any copy is issued
-  if (tid == 0) {    // the first value head's tiles
+  if (tid == kIssuer) {    // the first value head's tiles
     issue_loads_a(sm, ws, &tmO, bar_a, (size_t)c * Hv + hq * grp, hq * grp, t0);
     issue_loads_b(sm, ws, bar_b, (size_t)c * Hv + hq * grp);
   } else if (tid == kTmaThread) {   // the chunk's q, k rows into [q; k] by TMA
@@ -1174,13 +1177,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     if (tid >= 64 && tid < 128)   // the row dots dX_i . v_i of the reverse pass (slot 0)
       xvr[tid - 64] = ws.XV[ch * 4 * 64 + tid - 64];
     GDN_GSTAMP(hi, 0);
-    if (tid == 0)   // landed
+    if (tid == kIssuer)   // landed
       ok = mbar_wait(bar_a, ph, kWaitNs) && mbar_wait(bar_b, ph, kWaitNs) &&
            (hi > 0 || mbar_wait(bar_qk, 0, kWaitNs));
     if (__syncthreads_or(!ok)) { failed = true; break; }
     GDN_GSTAMP(hi, 1);
-    if (hi == 0) {  // [q; k] rows normalised in place (thread: one row half, 128 rows x 2
-                    // halves), rows past the chunk end cleared
+    if (hi == 0 && tid < kWorkThreads) {  // [q; k] rows normalised in place (thread: one row
+                                          // half, 128 rows x 2 halves)
       const int r = tid >> 1, hh = tid & 1, i = r & 63;
       uint8_t* rowq = sm + OFF_QK + hh * 16384 + r * 128;
       float ss = 0.f;
@@ -1218,7 +1221,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     tc_fence_after();
     GDN_GSTAMP(hi, 3);
     // ---- R1, R2 (and R3 for the first head), issued first: the dot below runs meanwhile
-    if (tid == 0) {
+    if (tid == kIssuer) {
       const uint32_t i1 = idesc_bf16(128, 256, false, true), i2 = idesc_bf16(128, 64, false, false);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
@@ -1232,13 +1235,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
       mma_commit(bar);
     }
     GDN_GSTAMP(hi, 4);
-    if (warp > 0) {  // <S0, dS> over the two tiles (same layout, element by element), by the
-                     // warps that do not issue the products
+    if (tid < kWorkThreads) {  // <S0, dS> over the two tiles (same layout, element by element)
       float sd = 0.f;
       const uint4* p0 = reinterpret_cast<const uint4*>(sm + OFF_S0);
       const uint4* p1 = reinterpret_cast<const uint4*>(sm + OFF_DS);
 #pragma unroll 4
-      for (int e = tid - 32; e < 32768 / 16; e += kThreads - 32) {
+      for (int e = tid; e < 32768 / 16; e += kWorkThreads) {
         const uint4 u0 = p0[e], u1 = p1[e];
         const uint32_t w0[4] = {u0.x, u0.y, u0.z, u0.w}, w1[4] = {u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
@@ -1257,12 +1259,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
       g2[tid] = G[tid] * kLog2eG;   // base-2 log-decay for the F / E factors
     }
     GDN_GSTAMP(hi, 5);
-    if (tid == 0) ok = mbar_wait(bar, 0, kWaitNs);
+    if (tid == kIssuer) ok = mbar_wait(bar, 0, kWaitNs);
     if (__syncthreads_or(!ok)) { failed = true; break; }
     tc_fence_after();
     GDN_GSTAMP(hi, 6);
     // ---- row dots from R1 (warps 0-3: the S0 columns; warps 6-7: the dS columns of k rows)
-    if (warp < 4 || warp >= 6) {   // 8 columns of the bf16 row per 16-byte load
+    if (warp < 4 || warp == 6 || warp == 7) {   // 8 columns of the bf16 row per 16-byte load
       const bool s0 = warp < 4;
       const uint8_t* tile = s0 ? sm + OFF_OX : sm + OFF_U;
       const uint32_t half = s0 ? 16384u : 8192u;
@@ -1297,7 +1299,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     //      then the v of dS); thread: its TMEM lane's row, the v half warp / 4 of each part.  A
     //      row's 16-byte chunks sit at chunk ^ (row % 8), so the warp's reads of one chunk index
     //      spread over the banks.
-    {
+    if (warp < 8) {
       const int g = warp >> 2;
       float pk[32];
       {
@@ -1338,12 +1340,22 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     tc_fence_before();
     __syncthreads();   // [dO; dX] and U' have been read: the next head's load into their space
     tc_fence_after();
-    if (tid == 0 && hi + 1 < grp) issue_loads_a(sm, ws, &tmO, bar_a, ch + 1, h + 1, t0);
+    if (tid == kIssuer) {
+      if (hi + 1 < grp) issue_loads_a(sm, ws, &tmO, bar_a, ch + 1, h + 1, t0);
+      // R4's part over [S0 | dS], beside F and E: [scale gamma dO | 0 ; -gamma beta dX |
+      // lambda U'] [S0 | dS]^T
+      const uint32_t i4 = idesc_bf16(128, 128, false, false);
+#pragma unroll
+      for (int ks = 0; ks < 16; ++ks) {
+        const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
+        mma_bf16_ta(tb + T_R4, tb + T_R1 + 8 * ks, kdesc(sb + OFF_S0 + ko), i4, ks > 0 || hi > 0);
+      }
+    }
     if (hi + 1 < grp) last_a = hi + 1;
     GDN_GSTAMP(hi, 8);
-    // ---- F (rows i < 64 of R2 / R3) and E (rows 64-127), all eight warps at once: a warp
-    //      reaches the TMEM lanes 32 (warp % 4) .. + 31 and takes the column half warp / 4
-    {
+    // ---- F (rows i < 64 of R2 / R3) and E (rows 64-127), warps 0-7 at once: a warp reaches
+    //      the TMEM lanes 32 (warp % 4) .. + 31 and takes the column half warp / 4
+    if (warp < 8) {
       const int part = warp >> 2;
       float x[32], y[32], v[32];
       tmem_ld32(tb + loff + T_R2 + 32 * part, x);   // dO U'^T or dX U'^T
@@ -1406,16 +1418,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     __syncthreads();
     tc_fence_after();
     GDN_GSTAMP(hi, 9);
-    // ---- R4 += [dQ; dK] of this value head (thread 0), and beside it (warps 2-3) dG, dbeta per
-    //      token, then dg by a suffix sum
-    if (tid == 0) {
-      const uint32_t i4 = idesc_bf16(128, 128, false, false), i4c = idesc_bf16(128, 128, false, true);
-      const uint32_t i4d = idesc_bf16(128, 128, true, true);
-#pragma unroll
-      for (int ks = 0; ks < 16; ++ks) {   // [scale gamma dO | 0 ; -gamma beta dX | lambda U'] [S0 | dS]^T
-        const uint32_t ko = (ks >> 2) * 16384 + (ks & 3) * 32;
-        mma_bf16_ta(tb + T_R4, tb + T_R1 + 8 * ks, kdesc(sb + OFF_S0 + ko), i4, ks > 0 || hi > 0);
-      }
+    // ---- the rest of R4 += [dQ; dK] of this value head (the issuer), and beside it (warps 2-3) dG,
+    //      dbeta per token, then dg by a suffix sum
+    if (tid == kIssuer) {
+      const uint32_t i4c = idesc_bf16(128, 128, false, true), i4d = idesc_bf16(128, 128, true, true);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         // [F; E] K
@@ -1442,7 +1448,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
     }
     if (warp == 2) {
       float sdt = 0.f;
-      for (int w = 1; w < kThreads / 32; ++w) sdt += red[w];
+      for (int w = 0; w < kWorkThreads / 32; ++w) sdt += red[w];
       const float omsum = warp_sum(om[lane] + om[lane + 32]);
       float x0 = dGv[lane], x1 = dGv[lane + 32];
       const float extra = gm[L - 1] * sdt + omsum;
@@ -1460,20 +1466,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
       if (lane + 32 < L) b.dg[base + (size_t)(lane + 32) * Hv] = x1;
     }
     GDN_GSTAMP(hi, 10);
-    if (tid == 0) ok = mbar_wait(bar, 1, kWaitNs);
+    if (tid == kIssuer) ok = mbar_wait(bar, 1, kWaitNs);
     // (the barrier also orders the per-token vectors' last reads before the next head's writes)
     if (__syncthreads_or(!ok)) { failed = true; break; }
     tc_fence_after();
     GDN_GSTAMP(hi, 11);
     // S0, dS have been read: the next head's load into their space meanwhile
     if (hi + 1 < grp) {
-      if (tid == 0) issue_loads_b(sm, ws, bar_b, ch + 1);
+      if (tid == kIssuer) issue_loads_b(sm, ws, bar_b, ch + 1);
       last_b = hi + 1;
     }
     GDN_GSTAMP(hi, 12);
   }
   if (failed) {
-    if (tid == 0) {   // copies still in flight land before the shared memory is released
+    if (tid == kIssuer) {   // copies still in flight land before the shared memory is released
       mbar_wait(bar_a, (uint32_t)last_a & 1u, kWaitNs);
       mbar_wait(bar_b, (uint32_t)last_b & 1u, kWaitNs);
       mbar_wait(bar_qk, 0, kWaitNs);
@@ -1493,14 +1499,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
   //      the columns 64 g .. 64 g + 63 (the k-half g of [q; k]) and the halves' partial dots
   //      meet in shared memory.  The bf16 rows are staged (128-byte-swizzled [64 tokens][64
   //      features] halves: dq at OFF_S0, dk at OFF_S0 + 16 KB) for TMA stores.
-  {
-    const int g = warp >> 2, i = row & 63;
-    float* pd = colp;   // [2][128]
+  const bool epi = warp < 8;   // (the issuer warp has no TMEM lanes here)
+  const int g = warp >> 2, i = row & 63;
+  float* pd = colp;   // [2][128]
+  float d0[32], d1[32];   // the row's 64 columns of R4
+  float xh[64];
+  if (epi) {
     const uint8_t* xrow = sm + OFF_QK + g * 16384 + row * 128;
-    float d0[32], d1[32];   // the row's 64 columns of R4
     tmem_ld32(tb + loff + T_R4 + 64 * g, d0);
     tmem_ld32(tb + loff + T_R4 + 64 * g + 32, d1);
-    float xh[64];
 #pragma unroll
     for (int c8 = 0; c8 < 8; ++c8) {   // the row's 16-byte chunk c8 sits at c8 ^ (row % 8)
       const uint4 u = *reinterpret_cast<const uint4*>(xrow + ((c8 ^ (row & 7)) << 4));
@@ -1516,7 +1523,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_grad_tc_kernel(
 #pragma unroll
     for (int e = 0; e < 64; ++e) p = fmaf(xh[e], e < 32 ? d0[e] : d1[e - 32], p);
     pd[g * 128 + row] = p;
-    __syncthreads();
+  }
+  __syncthreads();
+  if (epi) {
     const float r = rnv[row];
     const float xd = pd[row] + pd[128 + row];
     uint8_t* srow = sm + OFF_S0 + (row >> 6) * 16384 + g * 8192 + i * 128;

@@ -8,13 +8,15 @@ gdn_chunk_bwd on the long-context shape at a smaller length through it, and prin
 - the reverse pass's per-chunk budget: thread 0 of the first eight CTAs (one per (sequence,
   value head)) records clock64 at every stage boundary of iterations 32 .. 95; the table gives
   the median cycles of each stage over those 512 chunks, and the period (loop top to loop top);
-- the grad pass's budget per value head: thread 0 of CTAs 4000 .. 4007 (one per (chunk,
-  query/key head), taking its two value heads in turn) records the same for each head and for
-  the epilogue; the table gives the median over the eight CTAs.
+- the grad pass's budget per value head: its issuing thread (warp 8) in CTAs 4000 .. 4007 (one
+  per (chunk, query/key head), taking its two value heads in turn) records the same for each head
+  and for the epilogue; the table gives the median over the eight CTAs.
 
-Thread 0 issues the MMAs and the bulk copies, so an "issue" row is the time it spends issuing
-(blocked at about the tensor pipe's rate) while the other warps run the concurrent work named in
-the row; a "wait" row includes the barrier that follows it.
+The recording thread issues the MMAs and the bulk copies (thread 0 in the reverse pass, the
+issuer warp in the grad pass), so an "issue" row is the time it spends issuing (blocked at about
+the tensor pipe's rate) while the other warps run the work named in the row; a stage done by the
+other warps alone shows as the recording thread's wait for it; a "wait" row includes the barrier
+that follows it.
 """
 from __future__ import annotations
 
@@ -42,17 +44,17 @@ REVERSE = [
 ]
 GRAD = [
     "wait: the head's tiles landed",
-    "q, k normalised in place (first head)",
-    "partial-chunk clearing",
-    "R1, R2 (R3) issue (others: <S0, dS>)",
+    "(the issuer passes the norms)",
+    "wait: q, k normalised in place (first head); partial-chunk clearing",
+    "R1, R2 (R3) issue (warps 0-7: <S0, dS>)",
     "gamma, lambda factors",
     "wait: R1-R3 done",
     "row dots",
-    "R4's first operand built in TMEM; the next head's dO, dX, U' issued",
-    "F, E",
-    "R4 issue (warps 2-3: dG, dbeta, dg)",
+    "wait: R4's first operand built in TMEM; the next head's dO, dX, U' and R4 over [S0 | dS] issued (warps 0-7: F, E)",
+    "wait: F, E done",
+    "the rest of R4 issued (warps 2-3: dG, dbeta, dg)",
     "wait: R4 done",
-    "next head's loads issued",
+    "next head's S0, dS issued",
 ]
 
 
