@@ -593,6 +593,14 @@ def main():
     e2e_val = e2e_seq = link = dec_e2e = None
     if args.only is None:
         e2e_steps = max(2, min(K, 6))
+        # one untimed step first: the caching allocator's first blocks of these sizes (GBs) are
+        # device allocations, which would otherwise land in the first timed step
+        g = {k: v.to(dev, non_blocking=True) for k, v in host.items()}
+        oo, ff = chunk_gated_delta_rule(g["q"], g["k"], g["v"], g["g"], g["beta"],
+                                        output_final_state=True, use_qk_l2norm_in_kernel=True)
+        o_host[0].copy_(oo, non_blocking=True)
+        f_host[0].copy_(ff, non_blocking=True)
+        del g, oo, ff
         torch.cuda.synchronize()
         barrier(world)
         ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
