@@ -64,8 +64,9 @@ constexpr int VT = 32;                // V columns per V tile
 
 // Scratch of the backward.  The fp32 path keeps fp32 tiles in every slot; the tensor-core path
 // (bf16, K = V = 128) keeps bf16 operand tiles in the S, dS, U, dX slots (half the fp32 size:
-// the per-(chunk, head) strides sS, sdS, sU, sdX are in floats), T and P together in the T slot,
-// and has no W, dUp or Z.
+// the per-(chunk, head) strides sS, sdS, sU, sdX are in floats), T^T and P together in the T
+// slot, the reverse pass's per-token vectors in the G slot, and has no W, dUp, Z or per-token dQ,
+// dK.
 struct BwdWs {
   int32_t* chunk_off;  // [N + 2]
   float* W;            // [NC][Hv][C][K]          (fp32 path)
