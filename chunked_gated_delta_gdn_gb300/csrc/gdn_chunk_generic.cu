@@ -60,12 +60,13 @@ __host__ __device__ inline WsLayout ws_layout(void* base, long long NC, int N, i
 }
 
 // ---------------------------------------------------------------- 2. prep
-// smem: Kn[C][K], X[C][K + V], A[C][C], G[C], bt[C]
+// smem: Kn[C][K + 1] (rows padded by one float: the K K^T loop reads 32 rows at one column
+// per warp, which then fall in 32 different banks), X[C][K + V], A[C][C], G[C], bt[C]
 __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(const ChunkArgs a, WsLayout ws) {
   extern __shared__ float smem[];
-  const int K = a.K, V = a.V, M = K + V;
+  const int K = a.K, V = a.V, M = K + V, ldk = K + 1;
   float* Kn = smem;
-  float* X = Kn + C * K;
+  float* X = Kn + C * ldk;
   float* A = X + C * M;
   float* G = A + C * C;
   float* bt = G + C;
@@ -74,7 +75,7 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(const ChunkArgs a,
   if (!locate_chunk(a, ws.chunk_off, c, &n, &t0, &L)) return;
   if (a.state_indices && seq_slot(a, n) < 0) return;
   const int hq = h / (a.Hv / a.Hqk);
-  load_rows(a.k, a.io_dtype, t0, L, a.Hqk, hq, K, a.use_qk_l2norm != 0, Kn, K);
+  load_rows(a.k, a.io_dtype, t0, L, a.Hqk, hq, K, a.use_qk_l2norm != 0, Kn, ldk);
   load_gates(a, t0, L, h, G, bt);
   __syncthreads();
   // A (strictly lower) and the right-hand side [diag(beta exp G) Kn | diag(beta) V].
@@ -83,7 +84,7 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(const ChunkArgs a,
     float val = 0.f;
     if (j < i) {
       float kk = 0.f;
-      for (int d = 0; d < K; ++d) kk += Kn[i * K + d] * Kn[j * K + d];
+      for (int d = 0; d < K; ++d) kk += Kn[i * ldk + d] * Kn[j * ldk + d];
       val = bt[i] * kk * expf(G[i] - G[j]);
     }
     A[e] = val;
@@ -92,7 +93,7 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(const ChunkArgs a,
     const int i = e / M, col = e - i * M;
     float x = 0.f;
     if (i < L) {
-      x = col < K ? bt[i] * expf(G[i]) * Kn[i * K + col]
+      x = col < K ? bt[i] * expf(G[i]) * Kn[i * ldk + col]
                   : bt[i] * load_elem(a.v, ((size_t)(t0 + i) * a.Hv + h) * V + (col - K), a.io_dtype);
     }
     X[e] = x;
@@ -103,9 +104,14 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(const ChunkArgs a,
   const size_t ch = (size_t)c * a.Hv + h;
   for (int col = threadIdx.x; col < M; col += kThreads) {
     for (int i = 1; i < L; ++i) {
-      float acc = X[i * M + col];
-      for (int j = 0; j < i; ++j) acc -= A[i * C + j] * X[j * M + col];
-      X[i * M + col] = acc;
+      float acc0 = X[i * M + col], acc1 = 0.f;   // two partial sums: half the dependent chain
+      int j = 0;
+      for (; j + 1 < i; j += 2) {
+        acc0 -= A[i * C + j] * X[j * M + col];
+        acc1 -= A[i * C + j + 1] * X[(j + 1) * M + col];
+      }
+      if (j < i) acc0 -= A[i * C + j] * X[j * M + col];
+      X[i * M + col] = acc0 + acc1;
     }
     if (col < K) {
       float* Wd = ws.W + ch * C * K;
@@ -119,7 +125,8 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(const ChunkArgs a,
 }
 
 // ---------------------------------------------------------------- 3. state
-// Per (sequence, head, 32-column tile).  smem: S[K][32], W[C][K], U[C][32], Kn[C][K], G[C]
+// Per (sequence, head, 32-column tile).  smem: S[K][32], W[C][K], U[C][32], Kn[C][K], G[C],
+// then dl[C] = exp(G_last - G_t) of the chunk
 __global__ void __launch_bounds__(kThreads) chunk_state_kernel(const ChunkArgs a, WsLayout ws) {
   extern __shared__ float smem[];
   const int K = a.K, V = a.V;
@@ -176,10 +183,13 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(const ChunkArgs a
     // S <- exp(G_last) S + sum_t exp(G_last - G_t) Kn_t U'_t
     const float gl = G[L - 1];
     const float dl = expf(gl);
+    float* dlt = G + C;
+    if (threadIdx.x < C) dlt[threadIdx.x] = threadIdx.x < L ? expf(gl - G[threadIdx.x]) : 0.f;
+    __syncthreads();
     for (int e = threadIdx.x; e < K * kVT; e += kThreads) {
       const int d = e / kVT, cc = e - d * kVT;
       float acc = dl * S[e];
-      for (int t = 0; t < L; ++t) acc += expf(gl - G[t]) * Kn[t * K + d] * U[t * kVT + cc];
+      for (int t = 0; t < L; ++t) acc += dlt[t] * Kn[t * K + d] * U[t * kVT + cc];
       S[e] = acc;
     }
   }
@@ -193,13 +203,14 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(const ChunkArgs a
 }
 
 // ---------------------------------------------------------------- 4. output
-// Per (chunk, head, 32-column tile).  smem: Qn[C][K], Kn[C][K], S[K][32], U[C][32], P[C][C], G[C]
+// Per (chunk, head, 32-column tile).  smem: Qn[C][K + 1], Kn[C][K + 1] (rows padded as in the
+// prep), S[K][32], U[C][32], P[C][C], G[C]
 __global__ void __launch_bounds__(kThreads) chunk_output_kernel(const ChunkArgs a, WsLayout ws) {
   extern __shared__ float smem[];
-  const int K = a.K, V = a.V;
+  const int K = a.K, V = a.V, ldk = K + 1;
   float* Qn = smem;
-  float* Kn = Qn + C * K;
-  float* S = Kn + C * K;
+  float* Kn = Qn + C * ldk;
+  float* S = Kn + C * ldk;
   float* U = S + K * kVT;
   float* P = U + C * kVT;
   float* G = P + C * C;
@@ -216,8 +227,8 @@ __global__ void __launch_bounds__(kThreads) chunk_output_kernel(const ChunkArgs 
   }
   const int hq = h / (a.Hv / a.Hqk);
   const size_t ch = (size_t)c * a.Hv + h;
-  load_rows(a.q, a.io_dtype, t0, L, a.Hqk, hq, K, a.use_qk_l2norm != 0, Qn, K);
-  load_rows(a.k, a.io_dtype, t0, L, a.Hqk, hq, K, a.use_qk_l2norm != 0, Kn, K);
+  load_rows(a.q, a.io_dtype, t0, L, a.Hqk, hq, K, a.use_qk_l2norm != 0, Qn, ldk);
+  load_rows(a.k, a.io_dtype, t0, L, a.Hqk, hq, K, a.use_qk_l2norm != 0, Kn, ldk);
   const float* Sg = ws.S + ch * K * V;
   for (int e = threadIdx.x; e < K * kVT; e += kThreads) {
     const int d = e / kVT, cc = e - d * kVT;
@@ -235,7 +246,7 @@ __global__ void __launch_bounds__(kThreads) chunk_output_kernel(const ChunkArgs 
     float val = 0.f;
     if (j <= i && i < L) {
       float qk = 0.f;
-      for (int d = 0; d < K; ++d) qk += Qn[i * K + d] * Kn[j * K + d];
+      for (int d = 0; d < K; ++d) qk += Qn[i * ldk + d] * Kn[j * ldk + d];
       val = qk * expf(G[i] - G[j]);
     }
     P[e] = val;
@@ -245,16 +256,16 @@ __global__ void __launch_bounds__(kThreads) chunk_output_kernel(const ChunkArgs 
     const int i = e / kVT, cc = e - i * kVT;
     if (cc >= vt) continue;
     float qs = 0.f;
-    for (int d = 0; d < K; ++d) qs += Qn[i * K + d] * S[d * kVT + cc];
+    for (int d = 0; d < K; ++d) qs += Qn[i * ldk + d] * S[d * kVT + cc];
     float acc = expf(G[i]) * qs;
     for (int j = 0; j <= i; ++j) acc += P[i * C + j] * U[j * kVT + cc];
     store_elem(a.o, ((size_t)(t0 + i) * a.Hv + h) * V + c0 + cc, a.scale * acc, a.io_dtype);
   }
 }
 
-size_t prep_smem(int K, int V) { return sizeof(float) * ((size_t)C * K + (size_t)C * (K + V) + C * C + 2 * C); }
-size_t state_smem(int K) { return sizeof(float) * ((size_t)K * kVT + (size_t)C * K + C * kVT + (size_t)C * K + C); }
-size_t output_smem(int K) { return sizeof(float) * (2 * (size_t)C * K + (size_t)K * kVT + C * kVT + C * C + C); }
+size_t prep_smem(int K, int V) { return sizeof(float) * ((size_t)C * (K + 1) + (size_t)C * (K + V) + C * C + 2 * C); }
+size_t state_smem(int K) { return sizeof(float) * ((size_t)K * kVT + (size_t)C * K + C * kVT + (size_t)C * K + 2 * C); }
+size_t output_smem(int K) { return sizeof(float) * (2 * (size_t)C * (K + 1) + (size_t)K * kVT + C * kVT + C * C + C); }
 
 }  // namespace
 
