@@ -59,6 +59,29 @@ __host__ __device__ inline WsLayout ws_layout(void* base, long long NC, int N, i
   return w;
 }
 
+// acc[r][s] = sum_d X[ti + 16 r][d] Y[tj + 16 s][d] over d < K, for the 64 x 64 products of the
+// chunk (rows of X and Y at stride ld in shared memory).  Thread t takes ti = t / 16 and
+// tj = t % 16: its rows and columns are 16 apart, so with an odd ld a warp's reads of Y fall in
+// 16 different banks and those of X are broadcasts; each read feeds four FMAs.
+__device__ __forceinline__ void gram64(const float* X, const float* Y, int ld, int K, float (&acc)[4][4]) {
+  const int ti = threadIdx.x >> 4, tj = threadIdx.x & 15;
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[r][q] = 0.f;
+  for (int d = 0; d < K; ++d) {
+    float x[4], y[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) x[r] = X[(ti + 16 * r) * ld + d];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) y[q] = Y[(tj + 16 * q) * ld + d];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[r][q] = fmaf(x[r], y[q], acc[r][q]);
+  }
+}
+
 // ---------------------------------------------------------------- 2. prep
 // smem: Kn[C][K + 1] (rows padded by one float: the K K^T loop reads 32 rows at one column
 // per warp, which then fall in 32 different banks), X[C][K + V], A[C][C], G[C], bt[C]
@@ -79,15 +102,17 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(const ChunkArgs a,
   load_gates(a, t0, L, h, G, bt);
   __syncthreads();
   // A (strictly lower) and the right-hand side [diag(beta exp G) Kn | diag(beta) V].
-  for (int e = threadIdx.x; e < C * C; e += kThreads) {
-    const int i = e / C, j = e - i * C;
-    float val = 0.f;
-    if (j < i) {
-      float kk = 0.f;
-      for (int d = 0; d < K; ++d) kk += Kn[i * ldk + d] * Kn[j * ldk + d];
-      val = bt[i] * kk * expf(G[i] - G[j]);
-    }
-    A[e] = val;
+  {
+    float acc[4][4];
+    gram64(Kn, Kn, ldk, K, acc);
+    const int ti = threadIdx.x >> 4, tj = threadIdx.x & 15;
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int i = ti + 16 * r, j = tj + 16 * q;
+        A[i * C + j] = j < i ? bt[i] * acc[r][q] * expf(G[i] - G[j]) : 0.f;
+      }
   }
   for (int e = threadIdx.x; e < C * M; e += kThreads) {
     const int i = e / M, col = e - i * M;
@@ -125,14 +150,16 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(const ChunkArgs a,
 }
 
 // ---------------------------------------------------------------- 3. state
-// Per (sequence, head, 32-column tile).  smem: S[K][32], W[C][K], U[C][32], Kn[C][K], G[C],
-// then dl[C] = exp(G_last - G_t) of the chunk
+// Per (sequence, head, 32-column tile).  smem: S[K][32], W[C][K + 1] (rows padded by one float),
+// U[C][32], Kn[C][K], G[C], then dl[C] = exp(G_last - G_t) of the chunk.  Both products are
+// register-blocked: thread t takes rows t / 8 + 32 r and the four columns 4 (t % 8) .. + 3 (read
+// as one float4 of S or U').
 __global__ void __launch_bounds__(kThreads) chunk_state_kernel(const ChunkArgs a, WsLayout ws) {
   extern __shared__ float smem[];
-  const int K = a.K, V = a.V;
+  const int K = a.K, V = a.V, ldw = K + 1;
   float* S = smem;
   float* W = S + K * kVT;
-  float* U = W + C * K;
+  float* U = W + C * ldw;
   float* Kn = U + C * kVT;
   float* G = Kn + C * K;
   const int n = blockIdx.x, h = blockIdx.y, c0 = blockIdx.z * kVT;
@@ -159,7 +186,7 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(const ChunkArgs a
       if (cc < vt) Srec[(size_t)d * V + c0 + cc] = S[e];
     }
     const float* Wg = ws.W + ch * C * K;
-    for (int e = threadIdx.x; e < C * K; e += kThreads) W[e] = Wg[e];
+    for (int e = threadIdx.x; e < C * K; e += kThreads) W[(e / K) * ldw + e % K] = Wg[e];
     float* Ug = ws.U + ch * C * V;
     for (int e = threadIdx.x; e < C * kVT; e += kThreads) {
       const int i = e / kVT, cc = e - i * kVT;
@@ -169,11 +196,27 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(const ChunkArgs a
     load_rows(a.k, a.io_dtype, t0, L, a.Hqk, hq, K, a.use_qk_l2norm != 0, Kn, K);
     __syncthreads();
     // U' = U - W S   (rows >= L of W and U are zero, so U' is zero there)
-    for (int e = threadIdx.x; e < C * kVT; e += kThreads) {
-      const int i = e / kVT, cc = e - i * kVT;
-      float acc = U[e];
-      for (int d = 0; d < K; ++d) acc -= W[i * K + d] * S[d * kVT + cc];
-      U[e] = acc;
+    const int ti = threadIdx.x >> 3, c4 = 4 * (threadIdx.x & 7);
+    {
+      float acc[2][4];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const float4 u = *reinterpret_cast<const float4*>(U + (ti + 32 * r) * kVT + c4);
+        acc[r][0] = u.x; acc[r][1] = u.y; acc[r][2] = u.z; acc[r][3] = u.w;
+      }
+      for (int d = 0; d < K; ++d) {
+        const float4 sv = *reinterpret_cast<const float4*>(S + d * kVT + c4);
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const float w = W[(ti + 32 * r) * ldw + d];
+          acc[r][0] = fmaf(-w, sv.x, acc[r][0]); acc[r][1] = fmaf(-w, sv.y, acc[r][1]);
+          acc[r][2] = fmaf(-w, sv.z, acc[r][2]); acc[r][3] = fmaf(-w, sv.w, acc[r][3]);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+        *reinterpret_cast<float4*>(U + (ti + 32 * r) * kVT + c4) =
+            make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
     }
     __syncthreads();
     for (int e = threadIdx.x; e < C * kVT; e += kThreads) {
@@ -186,11 +229,32 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(const ChunkArgs a
     float* dlt = G + C;
     if (threadIdx.x < C) dlt[threadIdx.x] = threadIdx.x < L ? expf(gl - G[threadIdx.x]) : 0.f;
     __syncthreads();
-    for (int e = threadIdx.x; e < K * kVT; e += kThreads) {
-      const int d = e / kVT, cc = e - d * kVT;
-      float acc = dl * S[e];
-      for (int t = 0; t < L; ++t) acc += dlt[t] * Kn[t * K + d] * U[t * kVT + cc];
-      S[e] = acc;
+    {   // rows d = ti + 32 r < K
+      float acc[4][4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int d = ti + 32 * r;
+        float4 sv = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (d < K) sv = *reinterpret_cast<const float4*>(S + d * kVT + c4);
+        acc[r][0] = dl * sv.x; acc[r][1] = dl * sv.y; acc[r][2] = dl * sv.z; acc[r][3] = dl * sv.w;
+      }
+      for (int t = 0; t < L; ++t) {
+        const float4 uv = *reinterpret_cast<const float4*>(U + t * kVT + c4);
+        const float wt = dlt[t];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int d = ti + 32 * r;
+          const float kw = d < K ? wt * Kn[t * K + d] : 0.f;
+          acc[r][0] = fmaf(kw, uv.x, acc[r][0]); acc[r][1] = fmaf(kw, uv.y, acc[r][1]);
+          acc[r][2] = fmaf(kw, uv.z, acc[r][2]); acc[r][3] = fmaf(kw, uv.w, acc[r][3]);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int d = ti + 32 * r;
+        if (d < K)
+          *reinterpret_cast<float4*>(S + d * kVT + c4) = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+      }
     }
   }
   __syncthreads();
@@ -204,16 +268,17 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(const ChunkArgs a
 
 // ---------------------------------------------------------------- 4. output
 // Per (chunk, head, 32-column tile).  smem: Qn[C][K + 1], Kn[C][K + 1] (rows padded as in the
-// prep), S[K][32], U[C][32], P[C][C], G[C]
+// prep), S[K][32], U[C][32], P[C][C + 1], G[C].  P by gram64; the output register-blocked as in
+// the state kernel (rows t / 8 and t / 8 + 32, four columns a thread).
 __global__ void __launch_bounds__(kThreads) chunk_output_kernel(const ChunkArgs a, WsLayout ws) {
   extern __shared__ float smem[];
-  const int K = a.K, V = a.V, ldk = K + 1;
+  const int K = a.K, V = a.V, ldk = K + 1, ldp = C + 1;
   float* Qn = smem;
   float* Kn = Qn + C * ldk;
   float* S = Kn + C * ldk;
   float* U = S + K * kVT;
   float* P = U + C * kVT;
-  float* G = P + C * C;
+  float* G = P + C * ldp;
   const int c = blockIdx.x, h = blockIdx.y, c0 = blockIdx.z * kVT;
   const int vt = min(kVT, V - c0);
   int n, t0, L;
@@ -241,31 +306,59 @@ __global__ void __launch_bounds__(kThreads) chunk_output_kernel(const ChunkArgs 
   }
   if (threadIdx.x < C) G[threadIdx.x] = ws.G[ch * C + threadIdx.x];
   __syncthreads();
-  for (int e = threadIdx.x; e < C * C; e += kThreads) {
-    const int i = e / C, j = e - i * C;
-    float val = 0.f;
-    if (j <= i && i < L) {
-      float qk = 0.f;
-      for (int d = 0; d < K; ++d) qk += Qn[i * ldk + d] * Kn[j * ldk + d];
-      val = qk * expf(G[i] - G[j]);
-    }
-    P[e] = val;
+  {
+    float acc[4][4];
+    gram64(Qn, Kn, ldk, K, acc);
+    const int ti = threadIdx.x >> 4, tj = threadIdx.x & 15;
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int i = ti + 16 * r, j = tj + 16 * q;
+        P[i * ldp + j] = (j <= i && i < L) ? acc[r][q] * expf(G[i] - G[j]) : 0.f;
+      }
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < L * kVT; e += kThreads) {
-    const int i = e / kVT, cc = e - i * kVT;
-    if (cc >= vt) continue;
-    float qs = 0.f;
-    for (int d = 0; d < K; ++d) qs += Qn[i * ldk + d] * S[d * kVT + cc];
-    float acc = expf(G[i]) * qs;
-    for (int j = 0; j <= i; ++j) acc += P[i * C + j] * U[j * kVT + cc];
-    store_elem(a.o, ((size_t)(t0 + i) * a.Hv + h) * V + c0 + cc, a.scale * acc, a.io_dtype);
+  const int ti = threadIdx.x >> 3, c4 = 4 * (threadIdx.x & 7);
+  float qs[2][4], acc[2][4];
+#pragma unroll
+  for (int r = 0; r < 2; ++r)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) { qs[r][q] = 0.f; acc[r][q] = 0.f; }
+  for (int d = 0; d < K; ++d) {
+    const float4 sv = *reinterpret_cast<const float4*>(S + d * kVT + c4);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const float x = Qn[(ti + 32 * r) * ldk + d];
+      qs[r][0] = fmaf(x, sv.x, qs[r][0]); qs[r][1] = fmaf(x, sv.y, qs[r][1]);
+      qs[r][2] = fmaf(x, sv.z, qs[r][2]); qs[r][3] = fmaf(x, sv.w, qs[r][3]);
+    }
+  }
+  for (int j = 0; j < L; ++j) {   // P is zero above the diagonal and past the chunk end
+    const float4 uv = *reinterpret_cast<const float4*>(U + j * kVT + c4);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const float pv = P[(ti + 32 * r) * ldp + j];
+      acc[r][0] = fmaf(pv, uv.x, acc[r][0]); acc[r][1] = fmaf(pv, uv.y, acc[r][1]);
+      acc[r][2] = fmaf(pv, uv.z, acc[r][2]); acc[r][3] = fmaf(pv, uv.w, acc[r][3]);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int i = ti + 32 * r;
+    if (i >= L) continue;
+    const float eg = expf(G[i]);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (c4 + q < vt)
+        store_elem(a.o, ((size_t)(t0 + i) * a.Hv + h) * V + c0 + c4 + q, a.scale * fmaf(eg, qs[r][q], acc[r][q]),
+                   a.io_dtype);
   }
 }
 
 size_t prep_smem(int K, int V) { return sizeof(float) * ((size_t)C * (K + 1) + (size_t)C * (K + V) + C * C + 2 * C); }
-size_t state_smem(int K) { return sizeof(float) * ((size_t)K * kVT + (size_t)C * K + C * kVT + (size_t)C * K + 2 * C); }
-size_t output_smem(int K) { return sizeof(float) * (2 * (size_t)C * (K + 1) + (size_t)K * kVT + C * kVT + C * C + C); }
+size_t state_smem(int K) { return sizeof(float) * ((size_t)K * kVT + (size_t)C * (K + 1) + C * kVT + (size_t)C * K + 2 * C); }
+size_t output_smem(int K) { return sizeof(float) * (2 * (size_t)C * (K + 1) + (size_t)K * kVT + C * kVT + (size_t)C * (C + 1) + C); }
 
 }  // namespace
 
