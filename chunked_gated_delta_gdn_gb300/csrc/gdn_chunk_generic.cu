@@ -176,24 +176,71 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(const ChunkArgs a
     S[e] = (a.initial_state && cc < vt) ? a.initial_state[st_off + (size_t)d * V + c0 + cc] : 0.f;
   }
   const int first = ws.chunk_off[n];
+  // The next chunk's W, U tile, G and raw k rows are loaded into registers while the current
+  // chunk computes (k rows: warp w takes rows w + 8 u, lane l the elements l + 32 m).
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float wr[32], ur[8], kr[8][4], gr = 0.f;
+  auto fetch = [&](size_t chn, int t0n, int Ln) {
+    const float* Wg = ws.W + chn * C * K;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int e = threadIdx.x + kThreads * j;
+      wr[j] = e < C * K ? Wg[e] : 0.f;
+    }
+    const float* Ug = ws.U + chn * C * V;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = threadIdx.x + kThreads * j, i = e / kVT, cc = e - i * kVT;
+      ur[j] = cc < vt ? Ug[(size_t)i * V + c0 + cc] : 0.f;
+    }
+    if (threadIdx.x < C) gr = ws.G[chn * C + threadIdx.x];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int r = warp + 8 * u;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int e = lane + 32 * m;
+        kr[u][m] = (r < Ln && e < K) ? load_elem(a.k, ((size_t)(t0n + r) * a.Hqk + hq) * K + e, a.io_dtype) : 0.f;
+      }
+    }
+  };
+  if (bos < eos) fetch((size_t)first * a.Hv + h, bos, min(C, eos - bos));
   for (int t0 = bos, ci = first; t0 < eos; t0 += C, ++ci) {
     const int L = min(C, eos - t0);
     const size_t ch = (size_t)ci * a.Hv + h;
     __syncthreads();
     float* Srec = ws.S + ch * K * V;
+    float* Ug = ws.U + ch * C * V;
     for (int e = threadIdx.x; e < K * kVT; e += kThreads) {
       const int d = e / kVT, cc = e - d * kVT;
       if (cc < vt) Srec[(size_t)d * V + c0 + cc] = S[e];
     }
-    const float* Wg = ws.W + ch * C * K;
-    for (int e = threadIdx.x; e < C * K; e += kThreads) W[(e / K) * ldw + e % K] = Wg[e];
-    float* Ug = ws.U + ch * C * V;
-    for (int e = threadIdx.x; e < C * kVT; e += kThreads) {
-      const int i = e / kVT, cc = e - i * kVT;
-      U[e] = cc < vt ? Ug[(size_t)i * V + c0 + cc] : 0.f;
+    // this chunk's operands from the registers into shared memory (k rows normalised)
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int e = threadIdx.x + kThreads * j;
+      if (e < C * K) W[(e / K) * ldw + e % K] = wr[j];
     }
-    if (threadIdx.x < C) G[threadIdx.x] = ws.G[ch * C + threadIdx.x];
-    load_rows(a.k, a.io_dtype, t0, L, a.Hqk, hq, K, a.use_qk_l2norm != 0, Kn, K);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) U[threadIdx.x + kThreads * j] = ur[j];
+    if (threadIdx.x < C) G[threadIdx.x] = gr;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int r = warp + 8 * u;
+      float rn = 1.f;
+      if (a.use_qk_l2norm && r < L) {
+        float ss = 0.f;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) ss = fmaf(kr[u][m], kr[u][m], ss);
+        rn = 1.0f / sqrtf(warp_sum(ss) + kL2Eps);
+      }
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int e = lane + 32 * m;
+        if (e < K) Kn[r * K + e] = kr[u][m] * rn;
+      }
+    }
+    if (t0 + C < eos) fetch(ch + a.Hv, t0 + C, min(C, eos - t0 - C));   // the next chunk's, in flight
     __syncthreads();
     // U' = U - W S   (rows >= L of W and U are zero, so U' is zero there)
     const int ti = threadIdx.x >> 3, c4 = 4 * (threadIdx.x & 7);
