@@ -154,6 +154,7 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(const ChunkArgs a,
 // U[C][32], Kn[C][K], G[C], then dl[C] = exp(G_last - G_t) of the chunk.  Both products are
 // register-blocked: thread t takes rows t / 8 + 32 r and the four columns 4 (t % 8) .. + 3 (read
 // as one float4 of S or U').
+template <int RK>   // rows of the state update a thread takes: K <= 32 RK
 __global__ void __launch_bounds__(kThreads) chunk_state_kernel(const ChunkArgs a, WsLayout ws) {
   extern __shared__ float smem[];
   const int K = a.K, V = a.V, ldw = K + 1;
@@ -179,6 +180,7 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(const ChunkArgs a
   // The next chunk's W, U tile, G and raw k rows are loaded into registers while the current
   // chunk computes (k rows: warp w takes rows w + 8 u, lane l the elements l + 32 m).
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w_row_step = kThreads / K, w_col_step = kThreads - w_row_step * K;
   float wr[32], ur[8], kr[8][4], gr = 0.f;
   auto fetch = [&](size_t chn, int t0n, int Ln) {
     const float* Wg = ws.W + chn * C * K;
@@ -215,11 +217,17 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(const ChunkArgs a
       const int d = e / kVT, cc = e - d * kVT;
       if (cc < vt) Srec[(size_t)d * V + c0 + cc] = S[e];
     }
-    // this chunk's operands from the registers into shared memory (k rows normalised)
+    // this chunk's operands from the registers into shared memory (k rows normalised); element
+    // e = t + 256 j of W sits at row e / K, column e % K, stepped without a division per element
+    {
+      int wrow = threadIdx.x / K, wcol = threadIdx.x - wrow * K;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int e = threadIdx.x + kThreads * j;
-      if (e < C * K) W[(e / K) * ldw + e % K] = wr[j];
+      for (int j = 0; j < 32; ++j) {
+        if (threadIdx.x + kThreads * j < C * K) W[wrow * ldw + wcol] = wr[j];
+        wrow += w_row_step;
+        wcol += w_col_step;
+        if (wcol >= K) { wcol -= K; ++wrow; }
+      }
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) U[threadIdx.x + kThreads * j] = ur[j];
@@ -277,9 +285,9 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(const ChunkArgs a
     if (threadIdx.x < C) dlt[threadIdx.x] = threadIdx.x < L ? expf(gl - G[threadIdx.x]) : 0.f;
     __syncthreads();
     {   // rows d = ti + 32 r < K
-      float acc[4][4];
+      float acc[RK][4];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
+      for (int r = 0; r < RK; ++r) {
         const int d = ti + 32 * r;
         float4 sv = make_float4(0.f, 0.f, 0.f, 0.f);
         if (d < K) sv = *reinterpret_cast<const float4*>(S + d * kVT + c4);
@@ -289,7 +297,7 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(const ChunkArgs a
         const float4 uv = *reinterpret_cast<const float4*>(U + t * kVT + c4);
         const float wt = dlt[t];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
+        for (int r = 0; r < RK; ++r) {
           const int d = ti + 32 * r;
           const float kw = d < K ? wt * Kn[t * K + d] : 0.f;
           acc[r][0] = fmaf(kw, uv.x, acc[r][0]); acc[r][1] = fmaf(kw, uv.y, acc[r][1]);
@@ -297,7 +305,7 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(const ChunkArgs a
         }
       }
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
+      for (int r = 0; r < RK; ++r) {
         const int d = ti + 32 * r;
         if (d < K)
           *reinterpret_cast<float4*>(S + d * kVT + c4) = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
@@ -403,6 +411,21 @@ __global__ void __launch_bounds__(kThreads) chunk_output_kernel(const ChunkArgs 
   }
 }
 
+// The state pass for K <= 64 (two rows of the update a thread) or up to 128 (four).
+cudaError_t launch_state_kernel(const ChunkArgs& a, const WsLayout& ws, size_t ss) {
+  const unsigned vtiles = (unsigned)((a.V + kVT - 1) / kVT);
+  const dim3 grid(a.num_seqs, a.Hv, vtiles);
+  cudaError_t err;
+  if (a.K <= 64) {
+    if ((err = cudaFuncSetAttribute(chunk_state_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss))) return err;
+    chunk_state_kernel<2><<<grid, kThreads, ss, a.stream>>>(a, ws);
+  } else {
+    if ((err = cudaFuncSetAttribute(chunk_state_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss))) return err;
+    chunk_state_kernel<4><<<grid, kThreads, ss, a.stream>>>(a, ws);
+  }
+  return cudaGetLastError();
+}
+
 size_t prep_smem(int K, int V) { return sizeof(float) * ((size_t)C * (K + 1) + (size_t)C * (K + V) + C * C + 2 * C); }
 size_t state_smem(int K) { return sizeof(float) * ((size_t)K * kVT + (size_t)C * (K + 1) + C * kVT + (size_t)C * K + 2 * C); }
 size_t output_smem(int K) { return sizeof(float) * (2 * (size_t)C * (K + 1) + (size_t)K * kVT + C * kVT + (size_t)C * (C + 1) + C); }
@@ -443,11 +466,8 @@ cudaError_t launch_chunk_states(const ChunkArgs& a, int32_t* chunk_off, float* W
   ws.S = S;
   const size_t ss = state_smem(a.K);
   cudaError_t err;
-  if ((err = cudaFuncSetAttribute(chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss))) return err;
   if (a.num_seqs <= 0) return cudaSuccess;
-  const unsigned vtiles = (unsigned)((a.V + kVT - 1) / kVT);
-  chunk_state_kernel<<<dim3(a.num_seqs, a.Hv, vtiles), kThreads, ss, a.stream>>>(a, ws);
-  return cudaGetLastError();
+  return launch_state_kernel(a, ws, ss);
 }
 
 cudaError_t launch_chunk_generic(const ChunkArgs& a) {
@@ -457,7 +477,6 @@ cudaError_t launch_chunk_generic(const ChunkArgs& a) {
   cudaError_t err;
   const size_t sp = prep_smem(a.K, a.V), ss = state_smem(a.K), so = output_smem(a.K);
   if ((err = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp))) return err;
-  if ((err = cudaFuncSetAttribute(chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss))) return err;
   if ((err = cudaFuncSetAttribute(chunk_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)so))) return err;
   chunk_table_kernel<<<1, 1024, 0, a.stream>>>(a, ws.chunk_off);
   if ((err = cudaGetLastError())) return err;
@@ -466,10 +485,7 @@ cudaError_t launch_chunk_generic(const ChunkArgs& a) {
     if ((err = cudaGetLastError())) return err;
   }
   const unsigned vtiles = (unsigned)((a.V + kVT - 1) / kVT);
-  if (a.num_seqs > 0) {
-    chunk_state_kernel<<<dim3(a.num_seqs, a.Hv, vtiles), kThreads, ss, a.stream>>>(a, ws);
-    if ((err = cudaGetLastError())) return err;
-  }
+  if (a.num_seqs > 0 && (err = launch_state_kernel(a, ws, ss))) return err;
   if (NC > 0 && a.num_seqs > 0) {
     chunk_output_kernel<<<dim3((unsigned)NC, a.Hv, vtiles), kThreads, so, a.stream>>>(a, ws);
     if ((err = cudaGetLastError())) return err;
