@@ -83,25 +83,38 @@ __device__ __forceinline__ void gram64(const float* X, const float* Y, int ld, i
 }
 
 // ---------------------------------------------------------------- 2. prep
-// smem: Kn[C][K + 1] (rows padded by one float: the K K^T loop reads 32 rows at one column
-// per warp, which then fall in 32 different banks), X[C][K + V], A[C][C], G[C], bt[C]
-__global__ void __launch_bounds__(kThreads) chunk_prep_kernel(const ChunkArgs a, WsLayout ws) {
+// smem: Kn[C][K + 1] (rows padded by one float: the K K^T product reads 32 rows at one column
+// per warp, which then fall in 32 different banks), A[C][C], G[C], bt[C], be[C] = beta exp(G).
+// Thread t owns column t of [W | U] (K + V <= 256 columns): it builds the column of the
+// right-hand side [diag(beta exp G) Kn | diag(beta) V] in registers and solves (I + A) x = rhs
+// there by a right-looking substitution, four columns of A at a time (each float4 of A is a
+// broadcast read that feeds four FMAs); rows past the chunk end are zero in A and in the
+// right-hand side, so every column runs all 64 rows.
+__global__ void __launch_bounds__(kThreads, 2) chunk_prep_kernel(const ChunkArgs a, WsLayout ws) {
   extern __shared__ float smem[];
   const int K = a.K, V = a.V, M = K + V, ldk = K + 1;
   float* Kn = smem;
-  float* X = Kn + C * ldk;
-  float* A = X + C * M;
+  float* A = Kn + C * ldk;   // 16-byte aligned: C (K + 1) floats before it
   float* G = A + C * C;
   float* bt = G + C;
+  float* be = bt + C;
   const int c = blockIdx.x, h = blockIdx.y;
   int n, t0, L;
   if (!locate_chunk(a, ws.chunk_off, c, &n, &t0, &L)) return;
   if (a.state_indices && seq_slot(a, n) < 0) return;
   const int hq = h / (a.Hv / a.Hqk);
+  const int col = threadIdx.x;
+  // this column's V entries, issued before the K K^T product
+  float x[C];
+#pragma unroll
+  for (int i = 0; i < C; ++i)
+    x[i] = (col >= K && col < M && i < L)
+               ? load_elem(a.v, ((size_t)(t0 + i) * a.Hv + h) * V + (col - K), a.io_dtype) : 0.f;
   load_rows(a.k, a.io_dtype, t0, L, a.Hqk, hq, K, a.use_qk_l2norm != 0, Kn, ldk);
   load_gates(a, t0, L, h, G, bt);
   __syncthreads();
-  // A (strictly lower) and the right-hand side [diag(beta exp G) Kn | diag(beta) V].
+  if (threadIdx.x < C) be[threadIdx.x] = bt[threadIdx.x] * expf(G[threadIdx.x]);
+  // A (strictly lower)
   {
     float acc[4][4];
     gram64(Kn, Kn, ldk, K, acc);
@@ -114,39 +127,49 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(const ChunkArgs a,
         A[i * C + j] = j < i ? bt[i] * acc[r][q] * expf(G[i] - G[j]) : 0.f;
       }
   }
-  for (int e = threadIdx.x; e < C * M; e += kThreads) {
-    const int i = e / M, col = e - i * M;
-    float x = 0.f;
-    if (i < L) {
-      x = col < K ? bt[i] * expf(G[i]) * Kn[i * ldk + col]
-                  : bt[i] * load_elem(a.v, ((size_t)(t0 + i) * a.Hv + h) * V + (col - K), a.io_dtype);
-    }
-    X[e] = x;
-  }
   __syncthreads();
-  // Forward substitution, one column of [W | U] per thread (columns are
-  // independent, so no barrier is needed inside the sweep).
-  const size_t ch = (size_t)c * a.Hv + h;
-  for (int col = threadIdx.x; col < M; col += kThreads) {
-    for (int i = 1; i < L; ++i) {
-      float acc0 = X[i * M + col], acc1 = 0.f;   // two partial sums: half the dependent chain
-      int j = 0;
-      for (; j + 1 < i; j += 2) {
-        acc0 -= A[i * C + j] * X[j * M + col];
-        acc1 -= A[i * C + j + 1] * X[(j + 1) * M + col];
-      }
-      if (j < i) acc0 -= A[i * C + j] * X[j * M + col];
-      X[i * M + col] = acc0 + acc1;
+  if (col < M) {
+    // the right-hand side (rows >= L of be and bt are zero)
+    if (col < K) {
+#pragma unroll
+      for (int i = 0; i < C; ++i) x[i] = be[i] * Kn[i * ldk + col];
+    } else {
+#pragma unroll
+      for (int i = 0; i < C; ++i) x[i] *= bt[i];
     }
+#pragma unroll
+    for (int g = 0; g < C / 4; ++g) {
+      const int m0 = 4 * g;
+      // the diagonal block: rows m0 + 1 .. m0 + 3 by the columns before them
+#pragma unroll
+      for (int r = 1; r < 4; ++r) {
+        const float4 av = *reinterpret_cast<const float4*>(A + (m0 + r) * C + m0);
+        const float aa[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+        for (int e = 0; e < r; ++e) x[m0 + r] = fmaf(-aa[e], x[m0 + e], x[m0 + r]);
+      }
+      // the rows below the block by its four columns
+#pragma unroll
+      for (int i = m0 + 4; i < C; ++i) {
+        const float4 av = *reinterpret_cast<const float4*>(A + i * C + m0);
+        x[i] = fmaf(-av.x, x[m0], x[i]);
+        x[i] = fmaf(-av.y, x[m0 + 1], x[i]);
+        x[i] = fmaf(-av.z, x[m0 + 2], x[i]);
+        x[i] = fmaf(-av.w, x[m0 + 3], x[i]);
+      }
+    }
+    const size_t ch = (size_t)c * a.Hv + h;
     if (col < K) {
       float* Wd = ws.W + ch * C * K;
-      for (int i = 0; i < C; ++i) Wd[i * K + col] = X[i * M + col];
+#pragma unroll
+      for (int i = 0; i < C; ++i) Wd[i * K + col] = x[i];
     } else {
       float* Ud = ws.U + ch * C * V;
-      for (int i = 0; i < C; ++i) Ud[i * V + (col - K)] = X[i * M + col];
+#pragma unroll
+      for (int i = 0; i < C; ++i) Ud[i * V + (col - K)] = x[i];
     }
   }
-  if (threadIdx.x < C) ws.G[ch * C + threadIdx.x] = G[threadIdx.x];
+  if (threadIdx.x < C) ws.G[((size_t)c * a.Hv + h) * C + threadIdx.x] = G[threadIdx.x];
 }
 
 // ---------------------------------------------------------------- 3. state
@@ -426,7 +449,7 @@ cudaError_t launch_state_kernel(const ChunkArgs& a, const WsLayout& ws, size_t s
   return cudaGetLastError();
 }
 
-size_t prep_smem(int K, int V) { return sizeof(float) * ((size_t)C * (K + 1) + (size_t)C * (K + V) + C * C + 2 * C); }
+size_t prep_smem(int K, int V) { (void)V; return sizeof(float) * ((size_t)C * (K + 1) + C * C + 3 * C); }
 size_t state_smem(int K) { return sizeof(float) * ((size_t)K * kVT + (size_t)C * (K + 1) + C * kVT + (size_t)C * K + 2 * C); }
 size_t output_smem(int K) { return sizeof(float) * (2 * (size_t)C * (K + 1) + (size_t)K * kVT + C * kVT + (size_t)C * (C + 1) + C); }
 
