@@ -632,14 +632,17 @@ def main():
         eb.record(stream)
         torch.cuda.synchronize()
         e2e_seq = world * tokens / (max_over_ranks(ea.elapsed_time(eb), world, dev) / e2e_steps / 1000.0)
-        h2d_ms = _median([a.elapsed_time(b) for a, b, _, _ in phase])
-        call_ms = _median([b.elapsed_time(c) for _, b, c, _ in phase])
-        d2h_ms = _median([c.elapsed_time(e) for _, _, c, e in phase])
+        h2d_all = [a.elapsed_time(b) for a, b, _, _ in phase]
+        call_all = [b.elapsed_time(c) for _, b, c, _ in phase]
+        d2h_all = [c.elapsed_time(e) for _, _, c, e in phase]
+        h2d_ms, call_ms, d2h_ms = _median(h2d_all), _median(call_all), _median(d2h_all)
         link = {"h2d_gbs": h2d / (h2d_ms / 1e3) / 1e9, "d2h_gbs": d2h / (d2h_ms / 1e3) / 1e9,
                 "h2d_ms": h2d_ms, "d2h_ms": d2h_ms, "call_ms": call_ms,
-                "how": "pinned host <-> device copies of one step, median over the sequential "
-                       "end-to-end steps (CUDA events around the copies); call_ms: the call "
-                       "between them"}
+                "h2d_ms_max": max(h2d_all), "d2h_ms_max": max(d2h_all), "call_ms_max": max(call_all),
+                "how": "pinned host <-> device copies of one step, median (and slowest) over the "
+                       "sequential end-to-end steps (CUDA events around the copies); call_ms: the "
+                       "call between them. The host link and host memory are shared with other "
+                       "jobs on the machine, so single slow steps show up in the maxima"}
         del g, oo, ff
         # pipelined over three streams
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
