@@ -345,20 +345,23 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(const ChunkArgs a
 }
 
 // ---------------------------------------------------------------- 4. output
-// Per (chunk, head, 32-column tile).  smem: Qn[C][K + 1], Kn[C][K + 1] (rows padded as in the
-// prep), S[K][32], U[C][32], P[C][C + 1], G[C].  P by gram64; the output register-blocked as in
-// the state kernel (rows t / 8 and t / 8 + 32, four columns a thread).
+// Per (chunk, head, TW-column tile; TW = 64 when V <= 64, so that P and the q, k rows are formed
+// once per chunk and head, else 32).  smem: Qn[C][K + 1], Kn[C][K + 1] (rows padded as in the
+// prep), S[K][TW], U[C][TW], P[C][C + 1], G[C].  P by gram64; the output register-blocked: thread
+// t takes the four columns 4 (t % (TW / 4)) .. + 3 of rows t / (TW / 4) + (1024 / TW) r.
+template <int TW>
 __global__ void __launch_bounds__(kThreads) chunk_output_kernel(const ChunkArgs a, WsLayout ws) {
+  constexpr int CG = TW / 4, RS = kThreads / CG, RR = C / RS;
   extern __shared__ float smem[];
   const int K = a.K, V = a.V, ldk = K + 1, ldp = C + 1;
   float* Qn = smem;
   float* Kn = Qn + C * ldk;
   float* S = Kn + C * ldk;
-  float* U = S + K * kVT;
-  float* P = U + C * kVT;
+  float* U = S + K * TW;
+  float* P = U + C * TW;
   float* G = P + C * ldp;
-  const int c = blockIdx.x, h = blockIdx.y, c0 = blockIdx.z * kVT;
-  const int vt = min(kVT, V - c0);
+  const int c = blockIdx.x, h = blockIdx.y, c0 = blockIdx.z * TW;
+  const int vt = min(TW, V - c0);
   int n, t0, L;
   if (!locate_chunk(a, ws.chunk_off, c, &n, &t0, &L)) return;
   if (a.state_indices && seq_slot(a, n) < 0) {  // padding sequence: zero rows
@@ -373,13 +376,13 @@ __global__ void __launch_bounds__(kThreads) chunk_output_kernel(const ChunkArgs 
   load_rows(a.q, a.io_dtype, t0, L, a.Hqk, hq, K, a.use_qk_l2norm != 0, Qn, ldk);
   load_rows(a.k, a.io_dtype, t0, L, a.Hqk, hq, K, a.use_qk_l2norm != 0, Kn, ldk);
   const float* Sg = ws.S + ch * K * V;
-  for (int e = threadIdx.x; e < K * kVT; e += kThreads) {
-    const int d = e / kVT, cc = e - d * kVT;
+  for (int e = threadIdx.x; e < K * TW; e += kThreads) {
+    const int d = e / TW, cc = e - d * TW;
     S[e] = cc < vt ? Sg[(size_t)d * V + c0 + cc] : 0.f;
   }
   const float* Ug = ws.U + ch * C * V;
-  for (int e = threadIdx.x; e < C * kVT; e += kThreads) {
-    const int i = e / kVT, cc = e - i * kVT;
+  for (int e = threadIdx.x; e < C * TW; e += kThreads) {
+    const int i = e / TW, cc = e - i * TW;
     U[e] = cc < vt ? Ug[(size_t)i * V + c0 + cc] : 0.f;
   }
   if (threadIdx.x < C) G[threadIdx.x] = ws.G[ch * C + threadIdx.x];
@@ -397,33 +400,33 @@ __global__ void __launch_bounds__(kThreads) chunk_output_kernel(const ChunkArgs 
       }
   }
   __syncthreads();
-  const int ti = threadIdx.x >> 3, c4 = 4 * (threadIdx.x & 7);
-  float qs[2][4], acc[2][4];
+  const int ti = threadIdx.x / CG, c4 = 4 * (threadIdx.x % CG);
+  float qs[RR][4], acc[RR][4];
 #pragma unroll
-  for (int r = 0; r < 2; ++r)
+  for (int r = 0; r < RR; ++r)
 #pragma unroll
     for (int q = 0; q < 4; ++q) { qs[r][q] = 0.f; acc[r][q] = 0.f; }
   for (int d = 0; d < K; ++d) {
-    const float4 sv = *reinterpret_cast<const float4*>(S + d * kVT + c4);
+    const float4 sv = *reinterpret_cast<const float4*>(S + d * TW + c4);
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const float x = Qn[(ti + 32 * r) * ldk + d];
+    for (int r = 0; r < RR; ++r) {
+      const float x = Qn[(ti + RS * r) * ldk + d];
       qs[r][0] = fmaf(x, sv.x, qs[r][0]); qs[r][1] = fmaf(x, sv.y, qs[r][1]);
       qs[r][2] = fmaf(x, sv.z, qs[r][2]); qs[r][3] = fmaf(x, sv.w, qs[r][3]);
     }
   }
   for (int j = 0; j < L; ++j) {   // P is zero above the diagonal and past the chunk end
-    const float4 uv = *reinterpret_cast<const float4*>(U + j * kVT + c4);
+    const float4 uv = *reinterpret_cast<const float4*>(U + j * TW + c4);
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const float pv = P[(ti + 32 * r) * ldp + j];
+    for (int r = 0; r < RR; ++r) {
+      const float pv = P[(ti + RS * r) * ldp + j];
       acc[r][0] = fmaf(pv, uv.x, acc[r][0]); acc[r][1] = fmaf(pv, uv.y, acc[r][1]);
       acc[r][2] = fmaf(pv, uv.z, acc[r][2]); acc[r][3] = fmaf(pv, uv.w, acc[r][3]);
     }
   }
 #pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int i = ti + 32 * r;
+  for (int r = 0; r < RR; ++r) {
+    const int i = ti + RS * r;
     if (i >= L) continue;
     const float eg = expf(G[i]);
 #pragma unroll
@@ -451,7 +454,23 @@ cudaError_t launch_state_kernel(const ChunkArgs& a, const WsLayout& ws, size_t s
 
 size_t prep_smem(int K, int V) { (void)V; return sizeof(float) * ((size_t)C * (K + 1) + C * C + 3 * C); }
 size_t state_smem(int K) { return sizeof(float) * ((size_t)K * kVT + (size_t)C * (K + 1) + C * kVT + (size_t)C * K + 2 * C); }
-size_t output_smem(int K) { return sizeof(float) * (2 * (size_t)C * (K + 1) + (size_t)K * kVT + C * kVT + (size_t)C * (C + 1) + C); }
+size_t output_smem(int K, int TW) { return sizeof(float) * (2 * (size_t)C * (K + 1) + (size_t)K * TW + C * TW + (size_t)C * (C + 1) + C); }
+
+// The output pass: one CTA per (chunk, head, 64 columns) when V <= 64, else per 32 columns.
+cudaError_t launch_output_kernel(const ChunkArgs& a, const WsLayout& ws, long long NC) {
+  const int TW = a.V <= 64 ? 64 : kVT;
+  const size_t so = output_smem(a.K, TW);
+  const dim3 grid((unsigned)NC, a.Hv, (unsigned)((a.V + TW - 1) / TW));
+  cudaError_t err;
+  if (TW == 64) {
+    if ((err = cudaFuncSetAttribute(chunk_output_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)so))) return err;
+    chunk_output_kernel<64><<<grid, kThreads, so, a.stream>>>(a, ws);
+  } else {
+    if ((err = cudaFuncSetAttribute(chunk_output_kernel<kVT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)so))) return err;
+    chunk_output_kernel<kVT><<<grid, kThreads, so, a.stream>>>(a, ws);
+  }
+  return cudaGetLastError();
+}
 
 }  // namespace
 
@@ -487,10 +506,8 @@ cudaError_t launch_chunk_states(const ChunkArgs& a, int32_t* chunk_off, float* W
   ws.U = U;
   ws.G = G;
   ws.S = S;
-  const size_t ss = state_smem(a.K);
-  cudaError_t err;
   if (a.num_seqs <= 0) return cudaSuccess;
-  return launch_state_kernel(a, ws, ss);
+  return launch_state_kernel(a, ws, state_smem(a.K));
 }
 
 cudaError_t launch_chunk_generic(const ChunkArgs& a) {
@@ -498,21 +515,16 @@ cudaError_t launch_chunk_generic(const ChunkArgs& a) {
   const long long NC = max_chunks(T_total, a.num_seqs);
   WsLayout ws = ws_layout(a.workspace, NC, a.num_seqs, a.Hv, a.K, a.V, nullptr);
   cudaError_t err;
-  const size_t sp = prep_smem(a.K, a.V), ss = state_smem(a.K), so = output_smem(a.K);
+  const size_t sp = prep_smem(a.K, a.V), ss = state_smem(a.K);
   if ((err = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp))) return err;
-  if ((err = cudaFuncSetAttribute(chunk_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)so))) return err;
   chunk_table_kernel<<<1, 1024, 0, a.stream>>>(a, ws.chunk_off);
   if ((err = cudaGetLastError())) return err;
   if (NC > 0 && a.num_seqs > 0) {
     chunk_prep_kernel<<<dim3((unsigned)NC, a.Hv), kThreads, sp, a.stream>>>(a, ws);
     if ((err = cudaGetLastError())) return err;
   }
-  const unsigned vtiles = (unsigned)((a.V + kVT - 1) / kVT);
   if (a.num_seqs > 0 && (err = launch_state_kernel(a, ws, ss))) return err;
-  if (NC > 0 && a.num_seqs > 0) {
-    chunk_output_kernel<<<dim3((unsigned)NC, a.Hv, vtiles), kThreads, so, a.stream>>>(a, ws);
-    if ((err = cudaGetLastError())) return err;
-  }
+  if (NC > 0 && a.num_seqs > 0 && (err = launch_output_kernel(a, ws, NC))) return err;
   return cudaSuccess;
 }
 
