@@ -19,6 +19,8 @@
 // registers.  In product mode (the Gated Delta Product's decode step, same page) the L
 // entries are the n_h writes of one token: the decay goes with the first write, the
 // request's single query reads the state after the last, and only that output is written.
+#include <atomic>
+
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 
@@ -183,9 +185,22 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode128_kernel(const Deco
     __stcs(reinterpret_cast<float4*>(Sp + (size_t)(row0 + 4 * m) * V + col), S[m]);
 }
 
-// Any accepted K, V (<= 128): reductions by column threads, then an elementwise
-// update pass over the state.  Reads the state twice; used off the main shapes.
+// 16-byte asynchronous copy global -> shared (no register round trip), and the wait for them.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
+
+// Any K, V (the boundary holds both to multiples of 4 floats): the K x V fp32 state is staged in
+// shared memory once per (request, value head) by float4 loads, every token of the request
+// updates it there, and it is written back once.  S^T k and S^T q: thread t takes column t % V
+// of the rows t / V + G j (G = 256 / V row groups); the groups' partial sums meet in shared
+// memory.  Dynamic shared memory: K V + 2 * 256 floats.
 __global__ void __launch_bounds__(kDecodeThreads) decode_generic_kernel(const DecodeArgs a) {
+  extern __shared__ __align__(16) float dsm[];
   const int K = a.K, V = a.V;
   const int h = blockIdx.x % a.Hv;
   const int i = blockIdx.x / a.Hv;
@@ -197,12 +212,20 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_generic_kernel(const De
     return;
   }
   const int hq = h / (a.Hv / a.Hqk);
+  float* S = dsm;                        // [K][V]
+  float* pr = S + K * V;                 // [G][V] partial S^T k
+  float* pp = pr + kDecodeThreads;       // [G][V] partial S^T q
   __shared__ float sq[GDN_MAX_HEAD_DIM], sk[GDN_MAX_HEAD_DIM], su[GDN_MAX_HEAD_DIM];
   __shared__ float part[3][kDecodeThreads / 32];
   float* Sp = a.state + ((size_t)s * a.Hv + h) * (size_t)K * V;
+  const int n4 = K * V / 4;
+  float4* S4 = reinterpret_cast<float4*>(S);
+  // the state streams into shared memory while the first token's q, k are read and normalised
+  for (int e = tid; e < n4; e += kDecodeThreads) cp_async16(S4 + e, reinterpret_cast<const float4*>(Sp) + e);
+  const int G = kDecodeThreads / V, c = tid % V, g = tid / V;
   for (int t = 0; t < a.L; ++t) {
     const int it = i * a.L + t;
-    if (t > 0) __syncthreads();
+    __syncthreads();   // the previous token's sq / sk / su settled
     const size_t qk_off = ((size_t)it * a.Hqk + hq) * K;
     const size_t q_off = a.product ? ((size_t)i * a.Hqk + hq) * K : qk_off;
     float xq = 0.f, xk = 0.f;
@@ -231,26 +254,44 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_generic_kernel(const De
     const float dec = expf(gv);
     const bool write_o = !a.product || t == a.L - 1;
     const size_t o_row = a.product ? (size_t)i * a.Hv + h : hv_off;
+    if (t == 0) {   // the staged state landed (each thread waits for its own copies, then all)
+      cp_async_wait_all();
+      __syncthreads();
+    }
+    if (g < G) {
+      float r = 0.f, p = 0.f;
+      for (int row = g; row < K; row += G) {
+        const float x = S[row * V + c];
+        r = fmaf(x, sk[row], r);
+        p = fmaf(x, sq[row], p);
+      }
+      pr[g * V + c] = r;
+      pp[g * V + c] = p;
+    }
+    __syncthreads();
     if (tid < V) {
       float r = 0.f, p = 0.f;
-      for (int row = 0; row < K; ++row) {
-        const float x = Sp[(size_t)row * V + tid];
-        r += x * sk[row];
-        p += x * sq[row];
-      }
+      for (int gg = 0; gg < G; ++gg) { r += pr[gg * V + tid]; p += pp[gg * V + tid]; }
       const float u = bt * (load_elem(a.v, hv_off * V + tid, a.io_dtype) - dec * r);
       su[tid] = u;
       if (write_o) store_elem(a.o, o_row * V + tid, a.scale * (dec * p + kq * u), a.io_dtype);
     }
     __syncthreads();
-    float* inter = a.intermediate ? a.intermediate + hv_off * (size_t)K * V : nullptr;
-    for (int e = tid; e < K * V; e += blockDim.x) {
-      const int row = e / V, c = e - row * V;
-      const float nv = dec * Sp[e] + sk[row] * su[c];
-      Sp[e] = nv;
-      if (inter) inter[e] = nv;
+    float4* inter = a.intermediate ? reinterpret_cast<float4*>(a.intermediate + hv_off * (size_t)K * V) : nullptr;
+    for (int e = tid; e < n4; e += kDecodeThreads) {
+      const int row = (4 * e) / V, c0 = 4 * e - row * V;
+      const float kr = sk[row];
+      float4 x = S4[e];
+      x.x = fmaf(dec, x.x, kr * su[c0]);
+      x.y = fmaf(dec, x.y, kr * su[c0 + 1]);
+      x.z = fmaf(dec, x.z, kr * su[c0 + 2]);
+      x.w = fmaf(dec, x.w, kr * su[c0 + 3]);
+      S4[e] = x;
+      if (inter) __stcs(inter + e, x);
     }
   }
+  __syncthreads();
+  for (int e = tid; e < n4; e += kDecodeThreads) __stcs(reinterpret_cast<float4*>(Sp) + e, S4[e]);
 }
 
 }  // namespace
@@ -259,10 +300,22 @@ cudaError_t launch_decode(const DecodeArgs& a) {
   if (a.n == 0 || a.L == 0) return cudaSuccess;
   const long long blocks = (long long)a.n * a.Hv;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  if (a.K == 128 && a.V == 128)
+  if (a.K == 128 && a.V == 128) {
     decode128_kernel<<<(unsigned)blocks, kDecodeThreads, 0, a.stream>>>(a);
-  else
-    decode_generic_kernel<<<(unsigned)blocks, kDecodeThreads, 0, a.stream>>>(a);
+  } else {
+    const int smem = (a.K * a.V + 2 * kDecodeThreads) * (int)sizeof(float);
+    static std::atomic<bool> attr_set[64];
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev >= 64 || !attr_set[dev].load(std::memory_order_relaxed)) {
+      err = cudaFuncSetAttribute(decode_generic_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (GDN_MAX_HEAD_DIM * GDN_MAX_HEAD_DIM + 2 * kDecodeThreads) * (int)sizeof(float));
+      if (err != cudaSuccess) return err;
+      if (dev < 64) attr_set[dev].store(true, std::memory_order_relaxed);
+    }
+    decode_generic_kernel<<<(unsigned)blocks, kDecodeThreads, smem, a.stream>>>(a);
+  }
   return cudaGetLastError();
 }
 
