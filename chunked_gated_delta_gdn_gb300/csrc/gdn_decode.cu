@@ -195,16 +195,17 @@ __device__ __forceinline__ void cp_async_wait_all() {
 }
 
 // Any K, V (the boundary holds both to multiples of 4 floats): the K x V fp32 state is staged in
-// shared memory once per (request, value head) by float4 loads, every token of the request
-// updates it there, and it is written back once.  S^T k and S^T q: thread t takes column t % V
-// of the rows t / V + G j (G = 256 / V row groups); the groups' partial sums meet in shared
-// memory.  Dynamic shared memory: K V + 2 * 256 floats.
+// shared memory once per (request, value head) by 16-byte cp.async copies, every token of the
+// request updates it there, and it is written back once.  S^T k and S^T q: thread t takes column
+// t % V of the rows t / V + G j (G = threads / V row groups: 128 threads for a state of at most
+// 4096 floats, else 256); the groups' partial sums meet in shared memory.  Dynamic shared
+// memory: K V + 2 * 256 floats.
 __global__ void __launch_bounds__(kDecodeThreads) decode_generic_kernel(const DecodeArgs a) {
   extern __shared__ __align__(16) float dsm[];
   const int K = a.K, V = a.V;
   const int h = blockIdx.x % a.Hv;
   const int i = blockIdx.x / a.Hv;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, nt = blockDim.x;   // 256, or 128 for a small state
   const int s = resolve_slot(a, i);
   if (s < 0) {
     if (a.product) zero_output(a, i, h);
@@ -221,8 +222,8 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_generic_kernel(const De
   const int n4 = K * V / 4;
   float4* S4 = reinterpret_cast<float4*>(S);
   // the state streams into shared memory while the first token's q, k are read and normalised
-  for (int e = tid; e < n4; e += kDecodeThreads) cp_async16(S4 + e, reinterpret_cast<const float4*>(Sp) + e);
-  const int G = kDecodeThreads / V, c = tid % V, g = tid / V;
+  for (int e = tid; e < n4; e += nt) cp_async16(S4 + e, reinterpret_cast<const float4*>(Sp) + e);
+  const int G = nt / V, c = tid % V, g = tid / V;
   for (int t = 0; t < a.L; ++t) {
     const int it = i * a.L + t;
     __syncthreads();   // the previous token's sq / sk / su settled
@@ -237,7 +238,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_generic_kernel(const De
     if ((tid & 31) == 0) { part[0][tid >> 5] = s1; part[1][tid >> 5] = s2; part[2][tid >> 5] = s3; }
     __syncthreads();
     float nq = 0.f, nk = 0.f, dqk = 0.f;
-    for (int w = 0; w < kDecodeThreads / 32; ++w) { nq += part[0][w]; nk += part[1][w]; dqk += part[2][w]; }
+    for (int w = 0; w < nt / 32; ++w) { nq += part[0][w]; nk += part[1][w]; dqk += part[2][w]; }
     float rq = 1.f, rk = 1.f;
     if (a.use_qk_l2norm) { rq = 1.0f / sqrtf(nq + kL2Eps); rk = 1.0f / sqrtf(nk + kL2Eps); }
     if (tid < K) { sq[tid] = xq * rq; sk[tid] = xk * rk; }
@@ -278,7 +279,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_generic_kernel(const De
     }
     __syncthreads();
     float4* inter = a.intermediate ? reinterpret_cast<float4*>(a.intermediate + hv_off * (size_t)K * V) : nullptr;
-    for (int e = tid; e < n4; e += kDecodeThreads) {
+    for (int e = tid; e < n4; e += nt) {
       const int row = (4 * e) / V, c0 = 4 * e - row * V;
       const float kr = sk[row];
       float4 x = S4[e];
@@ -291,7 +292,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_generic_kernel(const De
     }
   }
   __syncthreads();
-  for (int e = tid; e < n4; e += kDecodeThreads) __stcs(reinterpret_cast<float4*>(Sp) + e, S4[e]);
+  for (int e = tid; e < n4; e += nt) __stcs(reinterpret_cast<float4*>(Sp) + e, S4[e]);
 }
 
 }  // namespace
@@ -314,7 +315,9 @@ cudaError_t launch_decode(const DecodeArgs& a) {
       if (err != cudaSuccess) return err;
       if (dev < 64) attr_set[dev].store(true, std::memory_order_relaxed);
     }
-    decode_generic_kernel<<<(unsigned)blocks, kDecodeThreads, smem, a.stream>>>(a);
+    // a small state (K V <= 4096 floats) takes 128 threads: twice the resident CTAs per SM
+    const int threads = a.K * a.V <= 4096 ? 128 : kDecodeThreads;
+    decode_generic_kernel<<<(unsigned)blocks, threads, smem, a.stream>>>(a);
   }
   return cudaGetLastError();
 }
