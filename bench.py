@@ -592,7 +592,7 @@ def main():
     d2h = o_host[0].numel() * o_host[0].element_size() + f_host[0].numel() * f_host[0].element_size()
     e2e_val = e2e_seq = link = dec_e2e = None
     if args.only is None:
-        e2e_steps = max(2, min(K, 20))   # long enough that the pipeline's fill and drain are a small share
+        e2e_steps = max(2, min(K, 50))   # the timed steps, as for the device timing: the pipeline's fill and drain a small share
         # one untimed step first: the caching allocator's first blocks of these sizes (GBs) are
         # device allocations, which would otherwise land in the first timed step
         g = {k: v.to(dev, non_blocking=True) for k, v in host.items()}
