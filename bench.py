@@ -639,6 +639,7 @@ def main():
         link = {"h2d_gbs": h2d / (h2d_ms / 1e3) / 1e9, "d2h_gbs": d2h / (d2h_ms / 1e3) / 1e9,
                 "h2d_ms": h2d_ms, "d2h_ms": d2h_ms, "call_ms": call_ms,
                 "h2d_ms_max": max(h2d_all), "d2h_ms_max": max(d2h_all), "call_ms_max": max(call_all),
+                "h2d_slowest_step": h2d_all.index(max(h2d_all)), "d2h_slowest_step": d2h_all.index(max(d2h_all)),
                 "how": "pinned host <-> device copies of one step, median (and slowest) over the "
                        "sequential end-to-end steps (CUDA events around the copies); call_ms: the "
                        "call between them. The host link and host memory are shared with other "
