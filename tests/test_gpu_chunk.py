@@ -95,7 +95,7 @@ def test_ragged_lengths(dtype, T):
     check(inp, "ragged %s T=%d" % (dtype, T))
 
 
-@pytest.mark.parametrize("KV", [(64, 64), (128, 64), (64, 128), (32, 32)])
+@pytest.mark.parametrize("KV", [(64, 64), (128, 64), (64, 128), (32, 32), (96, 96), (128, 32)])
 def test_other_head_dims(KV):
     K, V = KV
     for dtype in (torch.float32, torch.bfloat16):

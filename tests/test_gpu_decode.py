@@ -68,7 +68,7 @@ def test_decode_workload_full_size():
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("KV", [(128, 128), (64, 64), (64, 128), (32, 16)])
+@pytest.mark.parametrize("KV", [(128, 128), (64, 64), (64, 128), (32, 16), (96, 96), (128, 32)])
 def test_decode_shapes(dtype, KV):
     K, V = KV
     inp = synthetic.decode_inputs(n=37, Hqk=2, Hv=4, K=K, V=V, dtype=dtype, num_slots=50,
